@@ -1,0 +1,357 @@
+/*
+ * kda_oracle.c -- plain, slow, fp64 CPU oracle for Kimi Delta Attention (KDA).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product (the CUDA library and its
+ * Python binding) may include, link or call this file; only the tests, the
+ * smoke check and the benchmark's CPU-baseline leg use it.  It shares no code,
+ * header, table or helper with the CUDA path.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [blog]   "Kimi k3 技术报告详解（1）——架构再升华" (stevenstage.github.io/posts/blog7)
+ *            section "Kimi Delta Attention": the KDA recurrence
+ *                S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *                o_t = S_t^T q_t
+ *            section "Chunkwise parallel form": gamma^{i->j}, Gamma, W = M(Gamma*K),
+ *                U = M V, pseudo-values V~ = U - W S, A = Tril[(Q*Gamma)(K/Gamma)^T],
+ *                O = (Gamma*Q) S + A V~;  and the bounded gate
+ *                g = g_min * Sigmoid(e^{A_h} z),  alpha = exp(g).
+ *   [guide]  "A Look at Kimi K3: Three Core Innovations and Engineering Tuning Guide"
+ *            section 2.2: the same gate, and its torch pseudocode
+ *            g_min * sigmoid(exp(Ah) * z).
+ *
+ * Readings taken where the pages are silent (each is pinned by a test that does
+ * not call this file's chunked ordering):
+ *   - S is d_k x d_v (row = key channel), o_t = S_t^T q_t, no scale on q.
+ *   - M (never printed) = (I + StrictTril(Diag(beta)(Gamma*K)(K/Gamma)^T))^{-1} Diag(beta),
+ *     obtained by unrolling the recurrence inside one chunk.
+ *   - Tril in A is inclusive (o_r sees token r itself); the L above is strict.
+ *   - The chunk-to-chunk state update (not printed) is
+ *     S <- Diag(gamma^C) S + (K * gamma^C / Gamma)^T V~.
+ *   - A is per head, z is per key channel; chunks restart at every sequence
+ *     boundary and the last chunk of a sequence may be short.
+ *
+ * Layouts (all row-major, all double):
+ *   q, k, z : [T_total, H, dk]     v, o : [T_total, H, dv]     beta : [T_total, H]
+ *   A_log   : [H]                  S0, S_out : [N, H, dk, dv]
+ *   cu_seqlens : int64 [N + 1], cu[0] = 0, nondecreasing, cu[N] = T_total.
+ * Every (sequence, head) pair is independent; the work is spread over
+ * `nthreads` POSIX threads (<= 0 means 1).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ gate -- */
+
+/* Logistic function 1 / (1 + e^{-x}), written out. */
+static double logistic(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* [blog] "Chunkwise parallel form", bounded gate: g = g_min * Sigmoid(e^{A_h} z). */
+double kda_oracle_gate_value(double z, double A_log, double g_min)
+{
+    return g_min * logistic(exp(A_log) * z);
+}
+
+void kda_oracle_gate(const double *z, const double *A_log, double g_min, double *g,
+                     int64_t n_tokens, int H, int dk)
+{
+    for (int64_t t = 0; t < n_tokens; ++t)
+        for (int h = 0; h < H; ++h)
+            for (int c = 0; c < dk; ++c) {
+                int64_t idx = (t * H + h) * (int64_t)dk + c;
+                g[idx] = kda_oracle_gate_value(z[idx], A_log[h], g_min);
+            }
+}
+
+/* ------------------------------------------------------- shared job setup -- */
+
+typedef struct {
+    const double *q, *k, *v, *beta, *z, *A_log, *S0;
+    double *S_out, *o;
+    const int64_t *cu;
+    double g_min;
+    int N, H, dk, dv, C;
+    int mode; /* 0 = token recurrence, 1 = chunked form */
+    int64_t next_unit;
+    pthread_mutex_t lock;
+} job_t;
+
+/* --------------------------------------------------- recurrent ordering -- */
+
+/*
+ * [blog] "Kimi Delta Attention", KDA recurrence, one token at a time:
+ *   S' = Diag(alpha_t) S
+ *   S  = (I - beta k k^T) S' + beta k v^T  =  S' + k u^T  with  u = beta (v - S'^T k)
+ *   o  = S^T q
+ * S is dk x dv, row-major.  `work` holds dv doubles.
+ */
+static void recurrent_unit(const job_t *J, int n, int h, double *S, double *u, double *alpha)
+{
+    const int H = J->H, dk = J->dk, dv = J->dv;
+    if (J->S0)
+        memcpy(S, J->S0 + ((int64_t)n * H + h) * dk * dv, sizeof(double) * dk * dv);
+    else
+        memset(S, 0, sizeof(double) * dk * dv);
+
+    for (int64_t t = J->cu[n]; t < J->cu[n + 1]; ++t) {
+        const double *qt = J->q + (t * H + h) * dk;
+        const double *kt = J->k + (t * H + h) * dk;
+        const double *zt = J->z + (t * H + h) * dk;
+        const double *vt = J->v + (t * H + h) * dv;
+        const double bt = J->beta[t * H + h];
+        double *ot = J->o + (t * H + h) * dv;
+
+        for (int i = 0; i < dk; ++i)
+            alpha[i] = exp(kda_oracle_gate_value(zt[i], J->A_log[h], J->g_min));
+        /* S' = Diag(alpha) S */
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j)
+                S[i * dv + j] *= alpha[i];
+        /* u = beta (v - S'^T k) */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i)
+                acc += S[i * dv + j] * kt[i];
+            u[j] = bt * (vt[j] - acc);
+        }
+        /* S = S' + k u^T */
+        for (int i = 0; i < dk; ++i)
+            for (int j = 0; j < dv; ++j)
+                S[i * dv + j] += kt[i] * u[j];
+        /* o = S^T q */
+        for (int j = 0; j < dv; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < dk; ++i)
+                acc += S[i * dv + j] * qt[i];
+            ot[j] = acc;
+        }
+    }
+    if (J->S_out)
+        memcpy(J->S_out + ((int64_t)n * H + h) * dk * dv, S, sizeof(double) * dk * dv);
+}
+
+/* ----------------------------------------------------- chunked ordering -- */
+
+/*
+ * [blog] "Chunkwise parallel form", applied chunk by chunk (rows r = 0..L-1,
+ * L <= C), with the cumulative decay taken as exact fp64 products
+ *   Gam[r][c] = prod_{s<=r} alpha_s[c]                          (gamma^{1->r})
+ * and then
+ *   L[r][i]  = beta_r <Gam_r*k_r, k_i/Gam_i>   for i < r      (strict lower)
+ *   M        = (I + L)^{-1} Diag(beta)         by forward substitution
+ *   W        = M (Gam*K),  U = M V
+ *   Vt       = U - W S                                           (pseudo-values)
+ *   A[r][i]  = <Gam_r*q_r, k_i/Gam_i>          for i <= r      (inclusive)
+ *   O        = (Gam*Q) S + A Vt
+ *   S        <- Diag(Gam_last) S + (K * Gam_last / Gam)^T Vt
+ * No sub-tiling is needed here: with C <= 64 and g_min >= -6 the products stay
+ * inside the fp64 range (e^{+-384}).
+ */
+typedef struct {
+    double *Gam, *Kbar, *Khat, *Qbar, *Lm, *M, *W, *U, *Vt, *A, *Ktil, *S_new;
+} chunk_ws_t;
+
+static void chunked_unit(const job_t *J, int n, int h, double *S, const chunk_ws_t *w)
+{
+    const int H = J->H, dk = J->dk, dv = J->dv, C = J->C;
+    if (J->S0)
+        memcpy(S, J->S0 + ((int64_t)n * H + h) * dk * dv, sizeof(double) * dk * dv);
+    else
+        memset(S, 0, sizeof(double) * dk * dv);
+
+    for (int64_t t0 = J->cu[n]; t0 < J->cu[n + 1]; t0 += C) {
+        int64_t t1 = t0 + C;
+        if (t1 > J->cu[n + 1]) t1 = J->cu[n + 1];
+        const int L = (int)(t1 - t0);
+#define Q_(r, c) J->q[((t0 + (r)) * H + h) * dk + (c)]
+#define K_(r, c) J->k[((t0 + (r)) * H + h) * dk + (c)]
+#define Z_(r, c) J->z[((t0 + (r)) * H + h) * dk + (c)]
+#define V_(r, j) J->v[((t0 + (r)) * H + h) * dv + (j)]
+#define B_(r) J->beta[(t0 + (r)) * H + h]
+#define O_(r, j) J->o[((t0 + (r)) * H + h) * dv + (j)]
+
+        /* Gamma: cumulative product of alpha over the chunk, per key channel. */
+        for (int c = 0; c < dk; ++c) {
+            double run = 1.0;
+            for (int r = 0; r < L; ++r) {
+                run *= exp(kda_oracle_gate_value(Z_(r, c), J->A_log[h], J->g_min));
+                w->Gam[r * dk + c] = run;
+            }
+        }
+        for (int r = 0; r < L; ++r)
+            for (int c = 0; c < dk; ++c) {
+                const double G = w->Gam[r * dk + c];
+                w->Kbar[r * dk + c] = G * K_(r, c);
+                w->Khat[r * dk + c] = K_(r, c) / G;
+                w->Qbar[r * dk + c] = G * Q_(r, c);
+            }
+        /* L (strict) and A (inclusive) */
+        for (int r = 0; r < L; ++r)
+            for (int i = 0; i < L; ++i) {
+                double kk = 0.0, qk = 0.0;
+                for (int c = 0; c < dk; ++c) {
+                    kk += w->Kbar[r * dk + c] * w->Khat[i * dk + c];
+                    qk += w->Qbar[r * dk + c] * w->Khat[i * dk + c];
+                }
+                w->Lm[r * C + i] = (i < r) ? B_(r) * kk : 0.0;
+                w->A[r * C + i] = (i <= r) ? qk : 0.0;
+            }
+        /* (I + L) M = Diag(beta), row by row (forward substitution). */
+        for (int r = 0; r < L; ++r)
+            for (int i = 0; i < L; ++i) {
+                double acc = (i == r) ? B_(r) : 0.0;
+                for (int m = 0; m < r; ++m)
+                    acc -= w->Lm[r * C + m] * w->M[m * C + i];
+                w->M[r * C + i] = acc;
+            }
+        /* W = M (Gam*K), U = M V */
+        for (int r = 0; r < L; ++r) {
+            for (int c = 0; c < dk; ++c) {
+                double acc = 0.0;
+                for (int m = 0; m < L; ++m) acc += w->M[r * C + m] * w->Kbar[m * dk + c];
+                w->W[r * dk + c] = acc;
+            }
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int m = 0; m < L; ++m) acc += w->M[r * C + m] * V_(m, j);
+                w->U[r * dv + j] = acc;
+            }
+        }
+        /* Vt = U - W S */
+        for (int r = 0; r < L; ++r)
+            for (int j = 0; j < dv; ++j) {
+                double acc = 0.0;
+                for (int c = 0; c < dk; ++c) acc += w->W[r * dk + c] * S[c * dv + j];
+                w->Vt[r * dv + j] = w->U[r * dv + j] - acc;
+            }
+        /* O = (Gam*Q) S + A Vt */
+        for (int r = 0; r < L; ++r)
+            for (int j = 0; j < dv; ++j) {
+                double inter = 0.0, intra = 0.0;
+                for (int c = 0; c < dk; ++c) inter += w->Qbar[r * dk + c] * S[c * dv + j];
+                for (int i = 0; i <= r; ++i) intra += w->A[r * C + i] * w->Vt[i * dv + j];
+                O_(r, j) = inter + intra;
+            }
+        /* S <- Diag(Gam_last) S + (K * Gam_last / Gam)^T Vt */
+        for (int r = 0; r < L; ++r)
+            for (int c = 0; c < dk; ++c)
+                w->Ktil[r * dk + c] = K_(r, c) * (w->Gam[(L - 1) * dk + c] / w->Gam[r * dk + c]);
+        for (int c = 0; c < dk; ++c)
+            for (int j = 0; j < dv; ++j) {
+                double acc = w->Gam[(L - 1) * dk + c] * S[c * dv + j];
+                for (int r = 0; r < L; ++r) acc += w->Ktil[r * dk + c] * w->Vt[r * dv + j];
+                w->S_new[c * dv + j] = acc;
+            }
+        memcpy(S, w->S_new, sizeof(double) * dk * dv);
+#undef Q_
+#undef K_
+#undef Z_
+#undef V_
+#undef B_
+#undef O_
+    }
+    if (J->S_out)
+        memcpy(J->S_out + ((int64_t)n * H + h) * dk * dv, S, sizeof(double) * dk * dv);
+}
+
+/* ------------------------------------------------------------- threading -- */
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    const int dk = J->dk, dv = J->dv, C = J->C;
+    double *S = (double *)malloc(sizeof(double) * dk * dv);
+    double *u = (double *)malloc(sizeof(double) * (dv > dk ? dv : dk));
+    double *alpha = (double *)malloc(sizeof(double) * dk);
+    chunk_ws_t w;
+    memset(&w, 0, sizeof(w));
+    double *pool = NULL;
+    if (J->mode == 1) {
+        size_t need = (size_t)C * dk * 6 + (size_t)C * C * 3 + (size_t)C * dv * 2 + (size_t)dk * dv;
+        pool = (double *)calloc(need, sizeof(double));
+        double *p = pool;
+        w.Gam = p; p += (size_t)C * dk;
+        w.Kbar = p; p += (size_t)C * dk;
+        w.Khat = p; p += (size_t)C * dk;
+        w.Qbar = p; p += (size_t)C * dk;
+        w.W = p; p += (size_t)C * dk;
+        w.Ktil = p; p += (size_t)C * dk;
+        w.Lm = p; p += (size_t)C * C;
+        w.M = p; p += (size_t)C * C;
+        w.A = p; p += (size_t)C * C;
+        w.U = p; p += (size_t)C * dv;
+        w.Vt = p; p += (size_t)C * dv;
+        w.S_new = p;
+    }
+    for (;;) {
+        pthread_mutex_lock(&J->lock);
+        int64_t unit = J->next_unit++;
+        pthread_mutex_unlock(&J->lock);
+        if (unit >= (int64_t)J->N * J->H) break;
+        const int n = (int)(unit / J->H), h = (int)(unit % J->H);
+        if (J->mode == 0)
+            recurrent_unit(J, n, h, S, u, alpha);
+        else
+            chunked_unit(J, n, h, S, &w);
+    }
+    free(S);
+    free(u);
+    free(alpha);
+    free(pool);
+    return NULL;
+}
+
+static int run_job(job_t *J, int nthreads)
+{
+    if (J->N < 0 || J->H <= 0 || J->dk <= 0 || J->dv <= 0) return 1;
+    if (J->mode == 1 && J->C <= 0) return 1;
+    for (int n = 0; n < J->N; ++n)
+        if (J->cu[n + 1] < J->cu[n]) return 2;
+    if (J->cu[0] != 0) return 2;
+    if (nthreads < 1) nthreads = 1;
+    if ((int64_t)nthreads > (int64_t)J->N * J->H) nthreads = (int)((int64_t)J->N * J->H);
+    if (nthreads < 1) return 0;
+    J->next_unit = 0;
+    pthread_mutex_init(&J->lock, NULL);
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * nthreads);
+    for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, worker, J);
+    for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&J->lock);
+    return 0;
+}
+
+/*
+ * Token-by-token KDA over packed sequences.  Returns 0 on success, 1 on bad
+ * sizes, 2 on bad cu_seqlens.  S0 may be NULL (zero state); S_out may be NULL.
+ */
+int kda_oracle_recurrent(const double *q, const double *k, const double *v,
+                         const double *beta, const double *z, const double *A_log,
+                         double g_min, const double *S0, double *S_out,
+                         const int64_t *cu_seqlens, int N, int H, int dk, int dv,
+                         double *o, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.z = z; J.A_log = A_log; J.S0 = S0;
+    J.S_out = S_out; J.o = o; J.cu = cu_seqlens; J.g_min = g_min;
+    J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.C = 1; J.mode = 0;
+    return run_job(&J, nthreads);
+}
+
+/* Same result through the chunkwise-parallel form with chunk length C. */
+int kda_oracle_chunked(const double *q, const double *k, const double *v,
+                       const double *beta, const double *z, const double *A_log,
+                       double g_min, const double *S0, double *S_out,
+                       const int64_t *cu_seqlens, int N, int H, int dk, int dv,
+                       int C, double *o, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.beta = beta; J.z = z; J.A_log = A_log; J.S0 = S0;
+    J.S_out = S_out; J.o = o; J.cu = cu_seqlens; J.g_min = g_min;
+    J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.C = C; J.mode = 1;
+    return run_job(&J, nthreads);
+}
