@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one chunked forward over the long-context workload (B=1, T=65536, H=32,
+dk=dv=128, C=64, bf16 I/O, fp32 state, g_min=-5) with inputs resident in HBM.
+Prints ONE JSON line (rank 0): tokens/s over all ranks, TFLOP/s, the roofline of the
+dominant kernel, an end-to-end figure through the C ABI with host buffers, the decode
+step's GB/s, the clocks seen during the timed region and the CPU oracle baseline.
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (independent
+sequences, no data-path collective: weak scaling); timing is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle instead, on a bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "fwd_bf16_T65536_H32_d128"
+T, H, D, C = 65536, 32, 128, 64
+METRIC = ("KDA chunked-fwd tokens/s & TFLOP/s (T=64K,H=32,d=128) as % bf16 peak; "
+          "decode GB/s")
+# Algorithmic work per token-head at d=128, C=64 (bf16 I/O):
+BYTES_PER_TOKEN_HEAD = 4 * 2 * D + 2 + 2 * D        # q,k,v,z in; beta; o out = 1282 B
+STATE_BYTES = 4 * D * D                              # one fp32 state (S_out write)
+FLOP_CAUSAL = 6 * D * D + (C - 1) * D + 4 * (C + 1) * D + C * C // 3   # 141,013
+FLOP_DENSE = 6 * D * D + 2 * C * (3 * D + 2 * D) + C * C // 3           # 181,589
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "source": "fallback"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["source"] = "measured"
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, local_rank: int):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        self.gpu = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.REASONS, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- profiles --
+
+def traffic_from_profile(kernel_name: str, src_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_name)
+    if not d or d.get("source_sha1") != src_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def source_hash(*relpaths):
+    h = hashlib.sha1()
+    for r in relpaths:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ---------------------------------------------------------------- oracle --
+
+def oracle_sample(heads: int, tokens: int, nthreads: int, min_seconds: float = 0.0,
+                  max_repeats: int = 1):
+    """Time the fp64 oracle on `heads` heads x `tokens` tokens of the workload's inputs.
+
+    The same sample is repeated until `min_seconds` have passed (at most `max_repeats`
+    times).  Returns (seconds, repeats)."""
+    import numpy as np
+
+    import oracle
+    from serving_kda_chunkwise_gb300 import inputs
+    sp = inputs.workload_spec(WORKLOAD)
+    hs = list(range(heads))
+    t = {k: sp.tokens(k, 0, tokens, hs).astype(np.float64) for k in ("q", "k", "v", "beta", "z")}
+    A = sp.A_log[hs]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.recurrent(t["q"], t["k"], t["v"], t["beta"], t["z"], A, sp.g_min,
+                         nthreads=nthreads, want_state=False)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds or reps >= max_repeats:
+            break
+    return time.perf_counter() - t0, reps
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    nthreads = os.cpu_count() or 1
+    heads, tokens = 8, 16384
+    for _ in range(args.warmup):
+        oracle_sample(heads, tokens, nthreads)
+    secs = [oracle_sample(heads, tokens, nthreads)[0] for _ in range(args.steps)]
+    total = sum(secs)
+    # tokens/s of the full-width workload: token-heads processed / H / seconds
+    value = args.steps * heads * tokens / H / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, shapes of the workload)",
+            "config": {"workload": WORKLOAD, "T": T, "H": H, "d": D, "C": C, "g_min": -5.0},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads,
+                             "kind": "oracle",
+                             "sample": f"per step: {heads} of {H} heads x {tokens} tokens, "
+                                       f"fp64 token recurrence"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU --
+
+def run_ours(args, rank, world, local_rank, dist):
+    import numpy as np
+    import torch
+
+    from serving_kda_chunkwise_gb300 import inputs, kda
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    peaks = load_peaks()
+    sp = inputs.workload_spec(WORKLOAD, seed=1002 + 7919 * rank)
+    d = sp.to_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    S_out = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    o = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    ws_bytes = kda.workspace_size(T, 1, H, D, D, torch.bfloat16)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.fwd_chunked(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], sp.g_min,
+                        cu_seqlens=None, N=1, o=o, S_out=S_out, workspace=ws, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    kda.device_status(stream)
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    kda.device_status(stream)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    tok_s = world * T * args.steps / (ms / 1e3)
+    tflops_causal = world * T * H * FLOP_CAUSAL * args.steps / (ms / 1e3) / 1e12
+    tflops_dense = world * T * H * FLOP_DENSE * args.steps / (ms / 1e3) / 1e12
+
+    # dominant kernel: the whole forward is one kernel launch per step for now
+    bytes_per_launch = T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
+    kname = "fwd_generic_kernel"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic_from_profile(kname, source_hash(
+                    "serving_kda_chunkwise_gb300/csrc/fwd_generic.cu")),
+                "kernel": kname, "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": bytes_per_launch}
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    host = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "beta", "z")}
+    o_host = torch.empty((T, H, D), dtype=torch.bfloat16).pin_memory()
+    S_host = torch.empty((1, H, D, D), dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host.values())
+    d2h = o_host.numel() * 2 + S_host.numel() * 4
+    dd = {k: torch.empty_like(d[k]) for k in host}
+
+    def e2e_step():
+        for k2 in host:
+            dd[k2].copy_(host[k2], non_blocking=True)
+        kda.fwd_chunked(dd["q"], dd["k"], dd["v"], dd["beta"], dd["z"], d["A_log"], sp.g_min,
+                        cu_seqlens=None, N=1, o=o, S_out=S_out, workspace=ws, stream=stream)
+        o_host.copy_(o, non_blocking=True)
+        S_host.copy_(S_out, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = ev0.elapsed_time(ev1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    del dd, host
+
+    # decode step: 256 sequences x 32 heads, state updated in place
+    dec = None
+    if not args.no_decode:
+        dec = bench_decode(args, dev, stream, peaks)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        heads, tokens = 8, 32768
+        secs, reps = oracle_sample(heads, tokens, nthreads, min_seconds=10.0, max_repeats=12)
+        cpu = {"value": reps * heads * tokens / H / secs, "unit": "tokens/s", "cores": nthreads,
+               "kind": "oracle",
+               "sample": f"{heads} of {H} heads x {tokens} tokens of the workload, fp64 token "
+                         f"recurrence, repeated {reps}x ({secs:.1f} s)"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic (seeded, see serving_kda_chunkwise_gb300/inputs.py)",
+                "config": {"workload": WORKLOAD, "T": T, "H": H, "dk": D, "dv": D, "C": C,
+                           "g_min": sp.g_min, "io": "bf16", "state": "fp32",
+                           "l2": "inputs 2.69 GB per step > 129 MB L2; no flush needed",
+                           "parallelism": f"replicas x{world}"},
+                "tflops_causal": tflops_causal, "tflops_dense": tflops_dense,
+                "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
+                "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
+                "clocks": clk, "decode": dec, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+
+
+def bench_decode(args, dev, stream, peaks):
+    import torch
+
+    from serving_kda_chunkwise_gb300 import inputs, kda
+    w = inputs.DECODE_WORKLOAD
+    N, Hd, dk, dv = w["N"], w["H"], w["dk"], w["dv"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(w["seed"])
+    S = 0.02 * torch.randn((N, Hd, dk, dv), dtype=torch.float32, device=dev, generator=g)
+    A = torch.rand(Hd, device=dev, generator=g) * 2 - 1
+    ring = []
+    for _ in range(8):
+        x = inputs.decode_step_inputs(seed=w["seed"], step=len(ring), N=N, H=Hd, dk=dk, dv=dv)
+        ring.append({k: getattr(x, k).as_torch(dev) for k in ("q", "k", "v", "beta", "z")})
+    o = torch.empty((N, Hd, dv), dtype=torch.bfloat16, device=dev)
+
+    def step(i):
+        r = ring[i % len(ring)]
+        kda.decode_step(r["q"], r["k"], r["v"], r["beta"], r["z"], A, -5.0, S, o=o, stream=stream)
+
+    for i in range(5):
+        step(i)
+    torch.cuda.synchronize(dev)
+    n = args.decode_steps
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(n):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = ev0.elapsed_time(ev1) * 1e3 / n
+    per_head = 2 * 4 * dk * dv + 2 * (3 * dk + dv + 1) + 2 * dv
+    step_bytes = N * Hd * per_head
+    gbs = step_bytes / (us / 1e6) / 1e9
+    return {"us_per_step": us, "GB_per_step": step_bytes / 1e9, "GB_s": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"], "steps": n, "N": N, "H": Hd, "d": dk,
+            "kernel": "decode_kernel"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=200)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as td
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        td.init_process_group(backend=backend)
+        dist = td
+    try:
+        run_ours(args, rank, world, local_rank, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,134 @@
+/*
+ * kda.h -- C ABI of libkda.so: Kimi Delta Attention (KDA) on one GB300 (sm_103a).
+ *
+ * The operation (sources cited by page title and section):
+ *   [blog]  "Kimi k3 技术报告详解（1）——架构再升华" (stevenstage.github.io/posts/blog7)
+ *     section "Kimi Delta Attention" -- the KDA recurrence, per sequence and head:
+ *         S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *         o_t = S_t^T q_t                      (S is d_k x d_v, no scale on q)
+ *     section "Chunkwise parallel form" -- the same result computed chunk by chunk
+ *         (chunk length 64, 16-token sub-tiles) and the lower-bounded gate
+ *         g_t = g_min * Sigmoid(e^{A_h} z_t)  in (g_min, 0),   alpha_t = exp(g_t).
+ *   [guide] "A Look at Kimi K3: Three Core Innovations and Engineering Tuning Guide",
+ *     section 2.2 -- the same gate (per head A_h, per channel z), g_min in [-6, -3].
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     allocates no device memory; an entry point that needs scratch takes a
+ *     caller-provided workspace.  Every pointer must be 16-byte aligned.
+ *   - Layouts are contiguous row-major with the feature dimension innermost:
+ *         q, k, z : [T, H, dk]     v, o : [T, H, dv]     beta : [T, H]
+ *         A_log   : [H] fp32       state S : [N, H, dk, dv] fp32 (row = key channel)
+ *     where T is the number of tokens (packed over sequences).
+ *   - io_dt selects the element type of q, k, v, beta, z and o: KDA_F32 or KDA_BF16.
+ *     The recurrent state and all accumulation are fp32.
+ *   - dk, dv must be 64 or 128 (KDA_ERR_UNSUPPORTED otherwise); g_min must be < 0.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and the call
+ *     returns without synchronising.  Argument errors are detected on the host
+ *     before anything is enqueued and return KDA_ERR_INVALID_ARG / _UNSUPPORTED;
+ *     launch failures return KDA_ERR_CUDA.  Problems only visible on the device
+ *     (e.g. malformed cu_seqlens) set a device error word that kda_device_status()
+ *     reports.  kda_last_error() gives a readable message for the calling thread.
+ *   - Results are deterministic: the same inputs give bitwise identical outputs.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, g_min >= 0, ... */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. dk = 96)          */
+    KDA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed               */
+    KDA_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up                 */
+    KDA_ERR_DEVICE = 5        /* the device reported malformed input (cu_seqlens)   */
+} kda_status_t;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype_t;
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int kda_version(void);
+
+/* Static name of a status code. */
+const char *kda_status_string(kda_status_t status);
+
+/* Message describing the most recent failing call made by this thread ("" if none). */
+const char *kda_last_error(void);
+
+/*
+ * kda_gate -- the lower-bounded decay gate alone ([blog] "Chunkwise parallel form",
+ * [guide] 2.2):  g_out[t,h,c] = g_min * Sigmoid(exp(A_log[h]) * z[t,h,c]).
+ *   z      : [n_tokens, H, dk] of z_dt        A_log : [H] fp32
+ *   g_out  : [n_tokens, H, dk] fp32 (written)
+ * dk may be any positive multiple of 4 here.  n_tokens = 0 is a no-op.
+ */
+kda_status_t kda_gate(const void *z, kda_dtype_t z_dt, const float *A_log, float g_min,
+                      float *g_out, int64_t n_tokens, int H, int dk, kda_stream_t stream);
+
+/*
+ * Bytes of device workspace kda_fwd_chunked needs for this problem shape (0 when the
+ * selected kernels need none).  T_total is the packed token count, N the number of
+ * sequences.  Safe to call without a GPU.
+ */
+size_t kda_fwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv,
+                              kda_dtype_t io_dt);
+
+/*
+ * kda_fwd_chunked -- KDA forward over N packed sequences in the chunkwise-parallel form
+ * ([blog] "Chunkwise parallel form"; chunk length 64).
+ *   q, k, z     : [T_total, H, dk]   io_dt
+ *   v           : [T_total, H, dv]   io_dt
+ *   beta        : [T_total, H]       io_dt
+ *   A_log       : [H] fp32, g_min < 0
+ *   S0          : [N, H, dk, dv] fp32 initial state, or NULL for zeros
+ *   S_out       : [N, H, dk, dv] fp32 final state (written), or NULL; may alias S0
+ *   cu_seqlens  : device int32 [N + 1] token offsets (cu[0] = 0, nondecreasing,
+ *                 cu[N] = T_total), or NULL for N equal sequences of T_total / N tokens
+ *   o           : [T_total, H, dv] io_dt output (written)
+ *   workspace   : device scratch of at least kda_fwd_workspace_size(...) bytes
+ *                 (may be NULL when that size is 0); its contents are not preserved.
+ * A sequence may be empty; chunks never cross a sequence boundary.  With cu_seqlens
+ * malformed on the device the affected sequences are skipped and kda_device_status()
+ * returns KDA_ERR_DEVICE.
+ */
+kda_status_t kda_fwd_chunked(const void *q, const void *k, const void *v, const void *beta,
+                             const void *z, const float *A_log, float g_min, const float *S0,
+                             float *S_out, const int32_t *cu_seqlens, int N, int64_t T_total,
+                             int H, int dk, int dv, kda_dtype_t io_dt, void *o,
+                             void *workspace, size_t ws_bytes, kda_stream_t stream);
+
+/*
+ * kda_decode_step -- one token of the KDA recurrence ([blog] "Kimi Delta Attention")
+ * for N independent sequences, updating the state in place:
+ *   alpha = exp(g_min * Sigmoid(exp(A_log[h]) z));  S <- Diag(alpha) S;
+ *   u = beta (v - S^T k);  S <- S + k u^T;  o = S^T q.
+ *   q, k, z : [N, H, dk] io_dt    v : [N, H, dv] io_dt    beta : [N, H] io_dt
+ *   S       : [N, H, dk, dv] fp32, read and overwritten
+ *   o       : [N, H, dv] io_dt (written)
+ */
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const void *beta,
+                             const void *z, const float *A_log, float g_min, float *S, int N,
+                             int H, int dk, int dv, kda_dtype_t io_dt, void *o,
+                             kda_stream_t stream);
+
+/*
+ * Waits for `stream`, then reads and clears the device error word that kernels set
+ * when they meet malformed device-side input or give up a bounded wait.  Returns
+ * KDA_OK, KDA_ERR_DEVICE or KDA_ERR_TIMEOUT (or KDA_ERR_CUDA if the wait failed).
+ */
+kda_status_t kda_device_status(kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,224 @@
+// api.cu -- the C ABI of libkda.so (declared in include/kda.h): argument checks,
+// kernel selection and the device error word.  No entry point allocates device memory.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kda.h"
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace {
+
+__device__ unsigned g_device_error = 0u;
+
+thread_local std::string t_last_error;
+
+kda_status_t fail(kda_status_t s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kda_status_t fail(kda_status_t s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+kda_status_t cuda_fail(cudaError_t e, const char* where) {
+    return fail(KDA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define KDA_REQUIRE(cond, ...)                                   \
+    do {                                                         \
+        if (!(cond)) return fail(KDA_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+#define KDA_REQUIRE_PTR(p, name)                                                   \
+    do {                                                                           \
+        if ((p) == nullptr) return fail(KDA_ERR_INVALID_ARG, "%s is NULL", name);  \
+        if (!aligned16(p)) return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+#define KDA_OPTIONAL_PTR(p, name)                                                  \
+    do {                                                                           \
+        if ((p) != nullptr && !aligned16(p))                                       \
+            return fail(KDA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);   \
+    } while (0)
+
+// Device address of the error word on the current device (looked up once per device).
+unsigned* device_error_ptr() {
+    static std::mutex mu;
+    static unsigned* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned*>(p);
+    }
+    return cache[dev];
+}
+
+kda_status_t check_dims(int dk, int dv) {
+    if (dk <= 0 || dv <= 0) return fail(KDA_ERR_INVALID_ARG, "dk=%d dv=%d must be positive", dk, dv);
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128))
+        return fail(KDA_ERR_UNSUPPORTED, "dk=%d dv=%d: only 64 and 128 are supported", dk, dv);
+    return KDA_OK;
+}
+
+kda_status_t check_gmin(float g_min) {
+    if (!(g_min < 0.f) || !std::isfinite(g_min))
+        return fail(KDA_ERR_INVALID_ARG, "g_min=%g must be finite and negative", (double)g_min);
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 100; /* 0.1.0 */ }
+
+const char* kda_status_string(kda_status_t s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE";
+    }
+    return "KDA_ERR_UNKNOWN";
+}
+
+const char* kda_last_error(void) { return t_last_error.c_str(); }
+
+kda_status_t kda_gate(const void* z, kda_dtype_t z_dt, const float* A_log, float g_min,
+                      float* g_out, int64_t n_tokens, int H, int dk, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(z_dt == KDA_F32 || z_dt == KDA_BF16, "z_dt=%d is not a kda_dtype_t", (int)z_dt);
+    KDA_REQUIRE(n_tokens >= 0, "n_tokens=%lld must be >= 0", (long long)n_tokens);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    KDA_REQUIRE(dk > 0 && dk % 4 == 0, "dk=%d must be a positive multiple of 4", dk);
+    if (kda_status_t s = check_gmin(g_min)) return s;
+    if (n_tokens == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(z, "z");
+    KDA_REQUIRE_PTR(A_log, "A_log");
+    KDA_REQUIRE_PTR(g_out, "g_out");
+    cudaError_t e = kda::launch_gate(z, z_dt == KDA_BF16, A_log, g_min, g_out, n_tokens, H, dk,
+                                     reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_gate launch");
+    return KDA_OK;
+}
+
+size_t kda_fwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv, kda_dtype_t io_dt) {
+    (void)T_total; (void)N; (void)H; (void)dk; (void)dv; (void)io_dt;
+    return 0;
+}
+
+kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const void* beta,
+                             const void* z, const float* A_log, float g_min, const float* S0,
+                             float* S_out, const int32_t* cu_seqlens, int N, int64_t T_total,
+                             int H, int dk, int dv, kda_dtype_t io_dt, void* o, void* workspace,
+                             size_t ws_bytes, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
+    KDA_REQUIRE(N >= 0, "N=%d must be >= 0", N);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    KDA_REQUIRE(T_total >= 0, "T_total=%lld must be >= 0", (long long)T_total);
+    if (kda_status_t s = check_dims(dk, dv)) return s;
+    if (kda_status_t s = check_gmin(g_min)) return s;
+    if (cu_seqlens == nullptr) {
+        KDA_REQUIRE(N > 0 || T_total == 0, "N=0 requires T_total=0");
+        KDA_REQUIRE(N == 0 || T_total % N == 0,
+                    "without cu_seqlens T_total=%lld must be a multiple of N=%d",
+                    (long long)T_total, N);
+    }
+    KDA_REQUIRE((int64_t)N * H * 4 < (int64_t)1 << 31, "N*H=%lld is too large",
+                (long long)N * H);
+    if (N == 0) return KDA_OK;
+    if (T_total > 0) {
+        KDA_REQUIRE_PTR(q, "q");
+        KDA_REQUIRE_PTR(k, "k");
+        KDA_REQUIRE_PTR(v, "v");
+        KDA_REQUIRE_PTR(z, "z");
+        KDA_REQUIRE_PTR(o, "o");
+        KDA_REQUIRE(beta != nullptr, "beta is NULL");
+    }
+    KDA_REQUIRE_PTR(A_log, "A_log");
+    KDA_OPTIONAL_PTR(S0, "S0");
+    KDA_OPTIONAL_PTR(S_out, "S_out");
+    KDA_OPTIONAL_PTR(cu_seqlens, "cu_seqlens");
+    const size_t need = kda_fwd_workspace_size(T_total, N, H, dk, dv, io_dt);
+    if (need > 0) {
+        KDA_REQUIRE_PTR(workspace, "workspace");
+        KDA_REQUIRE(ws_bytes >= need, "workspace of %zu bytes is smaller than the %zu needed",
+                    ws_bytes, need);
+    }
+
+    kda::FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.z = z;
+    a.A_log = A_log; a.g_min = g_min; a.S0 = S0; a.S_out = S_out;
+    a.cu_seqlens = cu_seqlens; a.N = N; a.T_total = T_total; a.H = H; a.dk = dk; a.dv = dv;
+    a.io_bf16 = (io_dt == KDA_BF16); a.o = o; a.workspace = workspace; a.ws_bytes = ws_bytes;
+    a.dev_err = device_error_ptr();
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (a.dev_err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
+    cudaError_t e = kda::launch_fwd_generic(a);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_chunked launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* beta,
+                             const void* z, const float* A_log, float g_min, float* S, int N,
+                             int H, int dk, int dv, kda_dtype_t io_dt, void* o,
+                             kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
+    KDA_REQUIRE(N >= 0, "N=%d must be >= 0", N);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    if (kda_status_t s = check_dims(dk, dv)) return s;
+    if (kda_status_t s = check_gmin(g_min)) return s;
+    KDA_REQUIRE((int64_t)N * H < (int64_t)1 << 31, "N*H=%lld is too large", (long long)N * H);
+    if (N == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(q, "q");
+    KDA_REQUIRE_PTR(k, "k");
+    KDA_REQUIRE_PTR(v, "v");
+    KDA_REQUIRE_PTR(z, "z");
+    KDA_REQUIRE_PTR(o, "o");
+    KDA_REQUIRE_PTR(S, "S");
+    KDA_REQUIRE_PTR(A_log, "A_log");
+    KDA_REQUIRE(beta != nullptr, "beta is NULL");
+    cudaError_t e = kda::launch_decode(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv,
+                                       io_dt == KDA_BF16, o,
+                                       reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_decode_step launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_device_status(kda_stream_t stream) {
+    t_last_error.clear();
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_device_status wait");
+    unsigned word = 0u;
+    e = cudaMemcpyFromSymbol(&word, g_device_error, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_device_status read");
+    const unsigned zero = 0u;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_device_status clear");
+    if (word & kda::kDevErrTimeout)
+        return fail(KDA_ERR_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    if (word & kda::kDevErrBadSeqlens)
+        return fail(KDA_ERR_DEVICE, "malformed cu_seqlens met on the device (error word 0x%x)",
+                    word);
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,164 @@
+// decode.cu -- K4, one token of the KDA recurrence per sequence, state in place.
+//
+// "Kimi k3 技术报告详解（1）", section "Kimi Delta Attention":
+//   S_t = (I - beta k k^T) Diag(alpha) S_{t-1} + beta k v^T,   o_t = S_t^T q_t.
+// Rewritten for one pass over the state (S is d_k x d_v, row i = key channel):
+//   a_j = sum_i alpha_i k_i S_ij,   b_j = sum_i alpha_i q_i S_ij
+//   u_j = beta (v_j - a_j)                      (= beta (v - (Diag(alpha) S)^T k))
+//   S_ij <- alpha_i S_ij + k_i u_j             (= Diag(alpha) S + k u^T)
+//   o_j  = b_j + u_j (k . q)                    (= S_new^T q)
+// so each state element is read once and written once: the kernel is a pure HBM
+// stream of 2 * 4 * dk * dv bytes per (sequence, head).
+//
+// Layout: one CTA of 256 threads per (sequence, head).  A state row of dv fp32 is
+// covered by dv/4 lanes with one float4 each (a warp reads 512 contiguous bytes for
+// dv = 128); the dk rows are spread over the 8 warps, so every thread holds
+// dk*dv/1024 floats in registers between the read and the write.  All state loads are
+// issued before the gate is evaluated so their latency overlaps it.  Loads and stores
+// use the streaming cache hint: the state is touched once per step.
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+template <int DK, int DV, typename IO>
+__global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
+                                                     const IO* __restrict__ k,
+                                                     const IO* __restrict__ v,
+                                                     const IO* __restrict__ beta,
+                                                     const IO* __restrict__ z,
+                                                     const float* __restrict__ A_log, float g_min,
+                                                     float* __restrict__ S, int H,
+                                                     IO* __restrict__ o) {
+    constexpr int kWarps = 8;
+    constexpr int kLanesPerRow = DV / 4;
+    constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+    constexpr int kRowsPerPass = kRowsPerWarp * kWarps;
+    constexpr int kRowsPerThread = DK / kRowsPerPass;
+    static_assert(DK % kRowsPerPass == 0, "dk must be a multiple of the rows per pass");
+
+    __shared__ float s_alpha[DK], s_k[DK], s_q[DK], s_u[DV];
+    __shared__ float s_red[2][kWarps][DV];
+    __shared__ float s_kq;
+
+    const int nh = blockIdx.x;
+    const int h = nh % H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int col4 = lane % kLanesPerRow;
+    const int sub = lane / kLanesPerRow;
+    float* Sp = S + (size_t)nh * DK * DV;
+
+    float4 s[kRowsPerThread];
+#pragma unroll
+    for (int m = 0; m < kRowsPerThread; ++m) {
+        const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
+        s[m] = __ldcs(reinterpret_cast<const float4*>(Sp + (size_t)row * DV) + col4);
+    }
+
+    const float scale = expf(__ldg(A_log + h));
+    for (int c = tid; c < DK; c += blockDim.x) {
+        const size_t idx = (size_t)nh * DK + c;
+        s_alpha[c] = expf(gate_precise(to_f32(z[idx]), scale, g_min));
+        s_k[c] = to_f32(k[idx]);
+        s_q[c] = to_f32(q[idx]);
+    }
+    __syncthreads();
+
+    float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < kRowsPerThread; ++m) {
+        const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
+        const float ak = s_alpha[row] * s_k[row], aq = s_alpha[row] * s_q[row];
+        pa[0] = fmaf(ak, s[m].x, pa[0]); pa[1] = fmaf(ak, s[m].y, pa[1]);
+        pa[2] = fmaf(ak, s[m].z, pa[2]); pa[3] = fmaf(ak, s[m].w, pa[3]);
+        pb[0] = fmaf(aq, s[m].x, pb[0]); pb[1] = fmaf(aq, s[m].y, pb[1]);
+        pb[2] = fmaf(aq, s[m].z, pb[2]); pb[3] = fmaf(aq, s[m].w, pb[3]);
+    }
+#pragma unroll
+    for (int off = kLanesPerRow; off < 32; off <<= 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            pa[e] += __shfl_xor_sync(0xffffffffu, pa[e], off);
+            pb[e] += __shfl_xor_sync(0xffffffffu, pb[e], off);
+        }
+    if (sub == 0)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            s_red[0][warp][col4 * 4 + e] = pa[e];
+            s_red[1][warp][col4 * 4 + e] = pb[e];
+        }
+    if (warp == 0) {
+        float t = 0.f;
+        for (int c = lane; c < DK; c += 32) t = fmaf(s_k[c], s_q[c], t);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+        if (lane == 0) s_kq = t;
+    }
+    __syncthreads();
+
+    if (tid < DV) {
+        float a = 0.f, b = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            a += s_red[0][w][tid];
+            b += s_red[1][w][tid];
+        }
+        const float u = to_f32(beta[nh]) * (to_f32(v[(size_t)nh * DV + tid]) - a);
+        s_u[tid] = u;
+        o[(size_t)nh * DV + tid] = from_f32<IO>(fmaf(u, s_kq, b));
+    }
+    __syncthreads();
+
+    const float4 u4 = reinterpret_cast<const float4*>(s_u)[col4];
+#pragma unroll
+    for (int m = 0; m < kRowsPerThread; ++m) {
+        const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
+        const float al = s_alpha[row], kr = s_k[row];
+        float4 r;
+        r.x = fmaf(al, s[m].x, kr * u4.x);
+        r.y = fmaf(al, s[m].y, kr * u4.y);
+        r.z = fmaf(al, s[m].z, kr * u4.z);
+        r.w = fmaf(al, s[m].w, kr * u4.w);
+        __stcs(reinterpret_cast<float4*>(Sp + (size_t)row * DV) + col4, r);
+    }
+}
+
+template <int DK, int DV, typename IO>
+cudaError_t launch_t(const void* q, const void* k, const void* v, const void* beta, const void* z,
+                     const float* A_log, float g_min, float* S, int N, int H, void* o,
+                     cudaStream_t stream) {
+    const int grid = N * H;
+    decode_kernel<DK, DV, IO><<<grid, 256, 0, stream>>>(
+        static_cast<const IO*>(q), static_cast<const IO*>(k), static_cast<const IO*>(v),
+        static_cast<const IO*>(beta), static_cast<const IO*>(z), A_log, g_min, S, H,
+        static_cast<IO*>(o));
+    return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t dispatch_dims(const void* q, const void* k, const void* v, const void* beta,
+                          const void* z, const float* A_log, float g_min, float* S, int N, int H,
+                          int dk, int dv, void* o, cudaStream_t stream) {
+    if (dk == 128 && dv == 128)
+        return launch_t<128, 128, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+    if (dk == 128 && dv == 64)
+        return launch_t<128, 64, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+    if (dk == 64 && dv == 128)
+        return launch_t<64, 128, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+    return launch_t<64, 64, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* beta,
+                          const void* z, const float* A_log, float g_min, float* S, int N, int H,
+                          int dk, int dv, int io_bf16, void* o, cudaStream_t stream) {
+    if ((int64_t)N * H == 0) return cudaSuccess;
+    if (io_bf16)
+        return dispatch_dims<__nv_bfloat16>(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, o,
+                                            stream);
+    return dispatch_dims<float>(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, o, stream);
+}
+
+}  // namespace kda

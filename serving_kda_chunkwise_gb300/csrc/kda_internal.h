@@ -1,0 +1,41 @@
+// kda_internal.h -- host-side launchers shared between the C ABI (api.cu) and the
+// kernel translation units.  Not part of the public interface (that is include/kda.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+struct FwdArgs {
+    const void *q, *k, *v, *beta, *z;
+    const float* A_log;
+    float g_min;
+    const float* S0;
+    float* S_out;
+    const int32_t* cu_seqlens;
+    int N;
+    int64_t T_total;
+    int H, dk, dv;
+    int io_bf16;  // 1: bf16 I/O, 0: fp32 I/O
+    void* o;
+    void* workspace;
+    size_t ws_bytes;
+    unsigned* dev_err;
+    cudaStream_t stream;
+};
+
+// K1: elementwise gate.
+cudaError_t launch_gate(const void* z, int z_bf16, const float* A_log, float g_min, float* g_out,
+                        int64_t n_tokens, int H, int dk, cudaStream_t stream);
+
+// K4: one decode token per sequence, state updated in place.
+cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* beta,
+                          const void* z, const float* A_log, float g_min, float* S, int N, int H,
+                          int dk, int dv, int io_bf16, void* o, cudaStream_t stream);
+
+// Chunked forward on CUDA cores in fp32 (any dtype, dk/dv in {64,128}).
+cudaError_t launch_fwd_generic(const FwdArgs& a);
+
+}  // namespace kda

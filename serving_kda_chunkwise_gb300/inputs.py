@@ -2,21 +2,28 @@
 
 This module holds no arithmetic of the method itself (no gate, no decay, no
 recurrence): it only draws random tensors and rounds them to the storage dtype.
-Both the CUDA path and the CPU oracle read exactly the values it returns, so the
+Both the CUDA path and the CPU oracle read exactly the values it produces, so the
 oracle sees the bf16-rounded inputs widened to fp64.
 
-Recipe (per tensor, in this draw order, numpy PCG64 seeded with ``seed``):
-  lengths (varlen only) ~ U{lo..hi}          A_log ~ U(-1, 1) per head
-  q, k ~ N(0, 1), then L2-normalised over d_k for every (token, head)
-  v ~ N(0, 1)        beta = logistic(N(0, 1))        z ~ N(0, 1) per channel
-  S0 ~ N(0, 0.02^2) (when requested)
-then q, k, v, beta, z are rounded to the I/O dtype (bf16: round to nearest even).
+Recipe.  Every tensor is cut into blocks of ``BLOCK_TOKENS`` tokens (all heads); block
+b of tensor X is drawn from numpy PCG64 seeded with SeedSequence([seed, X's id, b]),
+so any block can be regenerated on its own, in any order and in parallel, with the
+same bits.  Per token and head:
+    q, k ~ N(0, 1), L2-normalised over d_k        v ~ N(0, 1)
+    beta = logistic(N(0, 1))                       z ~ N(0, 1) per channel
+and per problem:  A_log ~ U(-1, 1) per head,  S0 ~ N(0, 0.02^2),  varlen lengths
+~ U{lo..hi}.  q, k, v, beta, z are then rounded to the I/O dtype (bf16: nearest even).
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+import concurrent.futures as cf
+import os
+from dataclasses import dataclass
 
 import numpy as np
+
+BLOCK_TOKENS = 2048
+_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "z": 5, "A_log": 6, "S0": 7, "lengths": 8}
 
 # ----------------------------------------------------------------- rounding --
 
@@ -59,87 +66,182 @@ def store(x: np.ndarray, dtype: str) -> Stored:
     raise ValueError(dtype)
 
 
+def _round(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 values exactly representable in `dtype`."""
+    return bf16_bits_to_f32(f32_to_bf16_bits(x)) if dtype == "bf16" else x
+
+
 # ------------------------------------------------------------------- draws --
 
 
-def _normal(rng, shape):
-    return rng.standard_normal(size=shape, dtype=np.float32)
+def _gen(*key):
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(list(key))))
 
 
 def _unit_rows(x: np.ndarray) -> np.ndarray:
-    n = np.sqrt(np.sum(np.square(x, dtype=np.float64), axis=-1, keepdims=True))
-    return (x / np.maximum(n, 1e-30)).astype(np.float32)
+    n = np.sqrt(np.einsum("...i,...i->...", x, x, dtype=np.float32))[..., None]
+    return x / np.maximum(n, np.float32(1e-30))
 
 
 def _logistic(x: np.ndarray) -> np.ndarray:
-    return (1.0 / (1.0 + np.exp(-x.astype(np.float64)))).astype(np.float32)
+    return (1.0 / (1.0 + np.exp(-x))).astype(np.float32)
+
+
+def _draw(kind: str, rng, shape) -> np.ndarray:
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if kind in ("q", "k"):
+        return _unit_rows(x)
+    if kind == "beta":
+        return _logistic(x)
+    return x
+
+
+def _threads():
+    return max(1, min(32, os.cpu_count() or 1))
 
 
 @dataclass
-class ForwardInputs:
-    q: Stored
-    k: Stored
-    v: Stored
-    beta: Stored
-    z: Stored
-    A_log: np.ndarray                 # float32 [H]
-    S0: np.ndarray | None             # float32 [N, H, dk, dv] or None
-    cu_seqlens: np.ndarray            # int64 [N + 1]
-    g_min: float
+class ForwardSpec:
+    """Everything that defines one seeded forward problem (cheap; draws nothing big)."""
+    seed: int
+    H: int
+    dk: int
+    dv: int
     dtype: str
-    meta: dict = field(default_factory=dict)
+    cu_seqlens: np.ndarray      # int64 [N + 1]
+    A_log: np.ndarray           # float32 [H]
+    with_state: bool
+    g_min: float
 
     @property
     def T(self):
-        return self.q.values.shape[0]
-
-    @property
-    def H(self):
-        return self.q.values.shape[1]
-
-    @property
-    def dk(self):
-        return self.q.values.shape[2]
-
-    @property
-    def dv(self):
-        return self.v.values.shape[2]
+        return int(self.cu_seqlens[-1])
 
     @property
     def N(self):
         return self.cu_seqlens.shape[0] - 1
 
+    def width(self, kind):
+        return {"q": self.dk, "k": self.dk, "z": self.dk, "v": self.dv, "beta": None}[kind]
 
-def forward_inputs(*, seed: int, H: int, dk: int, dv: int, dtype: str,
-                   lengths=None, B: int = 1, T: int = 0, g_min: float = -5.0,
-                   with_state: bool = False, varlen_range=None) -> ForwardInputs:
-    """Draw one forward problem.
+    def block(self, kind: str, b: int) -> np.ndarray:
+        """Rounded float32 values of tensor `kind` for tokens [b*BT, min((b+1)*BT, T))."""
+        t0 = b * BLOCK_TOKENS
+        t1 = min(t0 + BLOCK_TOKENS, self.T)
+        w = self.width(kind)
+        shape = (t1 - t0, self.H) if w is None else (t1 - t0, self.H, w)
+        return _round(_draw(kind, _gen(self.seed, _IDS[kind], b), shape), self.dtype)
 
-    Either ``lengths`` (explicit per-sequence lengths), ``varlen_range=(count, lo, hi)``
-    (lengths drawn ~ U{lo..hi}) or ``B`` equal sequences of length ``T``.
-    """
-    rng = np.random.Generator(np.random.PCG64(seed))
+    def n_blocks(self):
+        return (self.T + BLOCK_TOKENS - 1) // BLOCK_TOKENS
+
+    def tokens(self, kind: str, t0: int, t1: int, heads=None) -> np.ndarray:
+        """Rounded float32 values for tokens [t0, t1), optionally a subset of heads."""
+        hs = None if heads is None else list(heads)
+
+        def piece(b):
+            blk = self.block(kind, b)
+            lo = max(t0 - b * BLOCK_TOKENS, 0)
+            hi = min(t1 - b * BLOCK_TOKENS, blk.shape[0])
+            blk = blk[lo:hi]
+            return blk if hs is None else np.ascontiguousarray(blk[:, hs])
+
+        blocks = range(t0 // BLOCK_TOKENS, (t1 + BLOCK_TOKENS - 1) // BLOCK_TOKENS)
+        with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+            parts = list(ex.map(piece, blocks))
+        if not parts:
+            w = self.width(kind)
+            nh = self.H if heads is None else len(list(heads))
+            return np.zeros((0, nh) if w is None else (0, nh, w), dtype=np.float32)
+        return np.concatenate(parts, axis=0)
+
+    def S0(self) -> np.ndarray | None:
+        if not self.with_state:
+            return None
+        rng = _gen(self.seed, _IDS["S0"])
+        return (np.float32(0.02) * rng.standard_normal((self.N, self.H, self.dk, self.dv),
+                                                       dtype=np.float32))
+
+    # ---- whole tensors -------------------------------------------------------
+
+    def host(self, kind: str) -> Stored:
+        """The whole tensor on the host (use for problems that fit comfortably in RAM)."""
+        return store(self.tokens(kind, 0, self.T), self.dtype)
+
+    def to_device(self, device="cuda"):
+        """All tensors on `device`, generated block by block in parallel host threads.
+
+        Returns a dict of torch tensors: q, k, v, beta, z (I/O dtype), A_log, S0 (fp32 or
+        None) and cu (int32 [N + 1]).
+        """
+        import torch
+        tdt = torch.bfloat16 if self.dtype == "bf16" else torch.float32
+        out = {}
+        for kind in ("q", "k", "v", "beta", "z"):
+            w = self.width(kind)
+            shape = (self.T, self.H) if w is None else (self.T, self.H, w)
+            out[kind] = torch.empty(shape, dtype=tdt, device=device)
+        jobs = [(kind, b) for kind in ("q", "k", "v", "beta", "z") for b in range(self.n_blocks())]
+
+        def make(job):
+            kind, b = job
+            x = self.block(kind, b)
+            if self.dtype == "bf16":
+                return job, torch.from_numpy(f32_to_bf16_bits(x).view(np.int16)).view(
+                    torch.bfloat16)
+            return job, torch.from_numpy(x)
+
+        with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+            for (kind, b), t in ex.map(make, jobs):
+                t0 = b * BLOCK_TOKENS
+                out[kind][t0:t0 + t.shape[0]].copy_(t)
+        out["A_log"] = torch.from_numpy(self.A_log).to(device)
+        S0 = self.S0()
+        out["S0"] = None if S0 is None else torch.from_numpy(S0).to(device)
+        out["cu"] = torch.from_numpy(self.cu_seqlens.astype(np.int32)).to(device)
+        return out
+
+
+def forward_spec(*, seed: int, H: int, dk: int, dv: int, dtype: str, lengths=None, B: int = 1,
+                 T: int = 0, g_min: float = -5.0, with_state: bool = False,
+                 varlen_range=None) -> ForwardSpec:
+    """Either explicit ``lengths``, ``varlen_range=(count, lo, hi)`` (lengths ~ U{lo..hi})
+    or ``B`` equal sequences of length ``T``."""
     if varlen_range is not None:
         count, lo, hi = varlen_range
-        lens = rng.integers(lo, hi + 1, size=count).astype(np.int64)
+        lens = _gen(seed, _IDS["lengths"]).integers(lo, hi + 1, size=count).astype(np.int64)
     elif lengths is not None:
         lens = np.asarray(lengths, dtype=np.int64)
     else:
         lens = np.full(B, T, dtype=np.int64)
     cu = np.zeros(lens.shape[0] + 1, dtype=np.int64)
     cu[1:] = np.cumsum(lens)
-    Tt = int(cu[-1])
-    N = lens.shape[0]
-    A_log = rng.uniform(-1.0, 1.0, size=H).astype(np.float32)
-    q = _unit_rows(_normal(rng, (Tt, H, dk)))
-    k = _unit_rows(_normal(rng, (Tt, H, dk)))
-    v = _normal(rng, (Tt, H, dv))
-    beta = _logistic(_normal(rng, (Tt, H)))
-    z = _normal(rng, (Tt, H, dk))
-    S0 = (0.02 * _normal(rng, (N, H, dk, dv))).astype(np.float32) if with_state else None
-    return ForwardInputs(store(q, dtype), store(k, dtype), store(v, dtype), store(beta, dtype),
-                         store(z, dtype), A_log, S0, cu, float(g_min), dtype,
-                         meta=dict(seed=seed))
+    A_log = _gen(seed, _IDS["A_log"]).uniform(-1.0, 1.0, size=H).astype(np.float32)
+    return ForwardSpec(seed, H, dk, dv, dtype, cu, A_log, with_state, float(g_min))
+
+
+@dataclass
+class ForwardInputs:
+    """A problem fully materialised on the host (small and medium sizes)."""
+    spec: ForwardSpec
+    q: Stored
+    k: Stored
+    v: Stored
+    beta: Stored
+    z: Stored
+    S0: np.ndarray | None
+
+    def __getattr__(self, name):
+        return getattr(self.spec, name)
+
+
+def forward_inputs(**kw) -> ForwardInputs:
+    sp = forward_spec(**kw)
+    return ForwardInputs(sp, sp.host("q"), sp.host("k"), sp.host("v"), sp.host("beta"),
+                         sp.host("z"), sp.S0())
+
+
+# ------------------------------------------------------------------ decode --
 
 
 @dataclass
@@ -153,28 +255,39 @@ class DecodeInputs:
 
 def decode_state(*, seed: int, N: int, H: int, dk: int, dv: int):
     """Initial decode state S ~ N(0, 0.02^2) [N,H,dk,dv] float32 and A_log ~ U(-1,1) [H]."""
-    rng = np.random.Generator(np.random.PCG64(seed))
-    A_log = rng.uniform(-1.0, 1.0, size=H).astype(np.float32)
-    S = (0.02 * _normal(rng, (N, H, dk, dv))).astype(np.float32)
+    A_log = _gen(seed, _IDS["A_log"]).uniform(-1.0, 1.0, size=H).astype(np.float32)
+    S = np.float32(0.02) * _gen(seed, _IDS["S0"]).standard_normal((N, H, dk, dv),
+                                                                   dtype=np.float32)
     return S, A_log
 
 
 def decode_step_inputs(*, seed: int, step: int, N: int, H: int, dk: int, dv: int,
                        dtype: str = "bf16") -> DecodeInputs:
     """Inputs for decode step ``step``: one new token for each of N sequences."""
-    rng = np.random.Generator(np.random.PCG64([seed, step]))
-    q = _unit_rows(_normal(rng, (N, H, dk)))
-    k = _unit_rows(_normal(rng, (N, H, dk)))
-    v = _normal(rng, (N, H, dv))
-    beta = _logistic(_normal(rng, (N, H)))
-    z = _normal(rng, (N, H, dk))
-    return DecodeInputs(store(q, dtype), store(k, dtype), store(v, dtype), store(beta, dtype),
-                        store(z, dtype))
+    out = {}
+    for kind in ("q", "k", "v", "beta", "z"):
+        w = {"q": dk, "k": dk, "z": dk, "v": dv, "beta": None}[kind]
+        shape = (N, H) if w is None else (N, H, w)
+        out[kind] = store(_draw(kind, _gen(seed, 100 + _IDS[kind], step), shape), dtype)
+    return DecodeInputs(**out)
+
+
+def decode_steps_iter(*, seed: int, steps: int, N: int, H: int, dk: int, dv: int,
+                      dtype: str = "bf16", lookahead: int = 32):
+    """Yield (step, DecodeInputs) in order, drawing upcoming steps in parallel threads."""
+    with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+        futs = {}
+        for step in range(steps):
+            for s in range(step, min(step + lookahead, steps)):
+                if s not in futs:
+                    futs[s] = ex.submit(decode_step_inputs, seed=seed, step=s, N=N, H=H, dk=dk,
+                                        dv=dv, dtype=dtype)
+            yield step, futs.pop(step).result()
 
 
 # ------------------------------------------------------ the named workloads --
 
-#: The five workloads, by what they are.  ``seed`` = 1000 + index.
+#: The forward workloads, by what they are.  ``seed`` = 1000 + index.
 WORKLOADS = {
     "fwd_f32_T256_H2_d64": dict(seed=1000, B=1, T=256, H=2, dk=64, dv=64, dtype="f32",
                                 with_state=False),
@@ -189,7 +302,14 @@ WORKLOADS = {
 #: g_min sweep for the long-context workload (same seed-1002 inputs for each value).
 LONG_GMIN_SWEEP = (-3.0, -5.0, -6.0)
 
+#: 256 sequences x 32 heads, one token per step for 1000 steps.
 DECODE_WORKLOAD = dict(seed=1004, N=256, H=32, dk=128, dv=128, steps=1000, dtype="bf16")
+
+
+def workload_spec(name: str, g_min: float = -5.0, **overrides) -> ForwardSpec:
+    kw = dict(WORKLOADS[name])
+    kw.update(overrides)
+    return forward_spec(g_min=g_min, **kw)
 
 
 def workload(name: str, g_min: float = -5.0, **overrides) -> ForwardInputs:

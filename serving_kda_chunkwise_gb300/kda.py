@@ -1,0 +1,181 @@
+"""Python binding of libkda.so: same entry-point names as include/kda.h.
+
+Argument marshalling only -- every step of the computation runs in the library's
+CUDA kernels.  Torch is used for device memory and streams.  Importing this module
+loads ``_build/libkda.so`` and raises if it is missing: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
+    KDA_ERR_DEVICE = range(6)
+KDA_F32, KDA_BF16 = 0, 1
+
+C_CHUNK = 64
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, func: str, msg: str):
+        self.status = status
+        super().__init__(f"{func}: {_lib.kda_status_string(status).decode()}: {msg}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libkda.so not found at {LIB_PATH}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                             ctypes.c_size_t)
+    lib.kda_version.restype = ctypes.c_int
+    lib.kda_version.argtypes = []
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_last_error.restype = ctypes.c_char_p
+    lib.kda_last_error.argtypes = []
+    lib.kda_gate.restype = ctypes.c_int
+    lib.kda_gate.argtypes = [vp, i32, vp, f32, vp, i64, i32, i32, vp]
+    lib.kda_fwd_workspace_size.restype = sz
+    lib.kda_fwd_workspace_size.argtypes = [i64, i32, i32, i32, i32, i32]
+    lib.kda_fwd_chunked.restype = ctypes.c_int
+    lib.kda_fwd_chunked.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, i32, i64, i32, i32,
+                                    i32, i32, vp, vp, sz, vp]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, i32, i32, i32, i32, i32, vp,
+                                    vp]
+    lib.kda_device_status.restype = ctypes.c_int
+    lib.kda_device_status.argtypes = [vp]
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes handle (for tests that call the C ABI directly)."""
+    return _lib
+
+
+def _check(status: int, func: str):
+    if status != KDA_OK:
+        raise KdaError(status, func, _lib.kda_last_error().decode())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported I/O dtype {t.dtype} (bf16 or fp32)")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def version() -> int:
+    return _lib.kda_version()
+
+
+def gate(z: torch.Tensor, A_log: torch.Tensor, g_min: float, g_out=None, stream=None):
+    """g = g_min * sigmoid(exp(A_log[h]) * z), z: [T, H, dk] -> fp32 [T, H, dk]."""
+    _need(z, "z")
+    _need(A_log, "A_log", torch.float32)
+    T, H, dk = z.shape
+    if g_out is None:
+        g_out = torch.empty((T, H, dk), dtype=torch.float32, device=z.device)
+    _need(g_out, "g_out", torch.float32)
+    _check(_lib.kda_gate(_ptr(z), _dt(z), _ptr(A_log), float(g_min), _ptr(g_out), T, H, dk,
+                         _stream(stream)), "kda_gate")
+    return g_out
+
+
+def workspace_size(T_total: int, N: int, H: int, dk: int, dv: int, io_dtype) -> int:
+    dt = KDA_BF16 if io_dtype == torch.bfloat16 else KDA_F32
+    return int(_lib.kda_fwd_workspace_size(int(T_total), int(N), int(H), int(dk), int(dv), dt))
+
+
+def fwd_chunked(q, k, v, beta, z, A_log, g_min: float, S0=None, cu_seqlens=None, N=None,
+                o=None, S_out=None, want_state: bool = True, workspace=None, stream=None):
+    """KDA forward over packed sequences (chunked form, C = 64).
+
+    q, k, z: [T, H, dk]; v: [T, H, dv]; beta: [T, H] (all one I/O dtype);
+    A_log: fp32 [H]; S0: fp32 [N, H, dk, dv] or None; cu_seqlens: int32 [N+1] on the
+    device, or None with N equal sequences (N defaults to 1).
+    Returns (o [T, H, dv], S_out [N, H, dk, dv] or None).
+    """
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (z, "z")):
+        _need(t, nm, q.dtype)
+    _need(A_log, "A_log", torch.float32)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.shape[0] - 1
+    elif N is None:
+        N = 1
+    if S0 is not None:
+        _need(S0, "S0", torch.float32)
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype)
+    if S_out is None and want_state:
+        S_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    if S_out is not None:
+        _need(S_out, "S_out", torch.float32)
+    need = workspace_size(T, N, H, dk, dv, q.dtype)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(_lib.kda_fwd_chunked(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z), _ptr(A_log),
+                                float(g_min), _ptr(S0), _ptr(S_out), _ptr(cu_seqlens), int(N),
+                                int(T), int(H), int(dk), int(dv), _dt(q), _ptr(o), _ptr(workspace),
+                                ws_bytes, _stream(stream)), "kda_fwd_chunked")
+    return o, S_out
+
+
+def decode_step(q, k, v, beta, z, A_log, g_min: float, S, o=None, stream=None):
+    """One decode token per sequence; S [N, H, dk, dv] fp32 is updated in place.
+
+    q, k, z: [N, H, dk]; v: [N, H, dv]; beta: [N, H].  Returns o [N, H, dv].
+    """
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (z, "z")):
+        _need(t, nm, q.dtype)
+    _need(A_log, "A_log", torch.float32)
+    _need(S, "S", torch.float32)
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype)
+    _check(_lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z), _ptr(A_log),
+                                float(g_min), _ptr(S), int(N), int(H), int(dk), int(dv), _dt(q),
+                                _ptr(o), _stream(stream)), "kda_decode_step")
+    return o
+
+
+def device_status(stream=None):
+    """Wait for the stream and raise if a kernel flagged malformed input or a timeout."""
+    _check(_lib.kda_device_status(_stream(stream)), "kda_device_status")

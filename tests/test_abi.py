@@ -1,0 +1,110 @@
+"""The C ABI without a GPU: libkda.so loads, exports every function include/kda.h declares,
+and rejects malformed arguments on the host before any CUDA work is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from serving_kda_chunkwise_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "kda_fwd_chunked" in names and "kda_decode_step" in names and "kda_gate" in names
+    for n in names:
+        assert hasattr(lib, n), f"libkda.so does not export {n}"
+
+
+def test_status_strings_and_version(lib):
+    lib.kda_status_string.restype = ctypes.c_char_p
+    assert lib.kda_status_string(0) == b"KDA_OK"
+    assert lib.kda_status_string(2) == b"KDA_ERR_UNSUPPORTED"
+    assert lib.kda_version() >= 100
+
+
+def _fwd(lib, **over):
+    vp = ctypes.c_void_p
+    aligned = vp(0x10000)
+    args = dict(q=aligned, k=aligned, v=aligned, beta=aligned, z=aligned, A_log=aligned,
+                g_min=ctypes.c_float(-5.0), S0=None, S_out=None, cu=None, N=1,
+                T=ctypes.c_int64(128), H=2, dk=128, dv=128, dt=1, o=aligned, ws=None,
+                ws_bytes=ctypes.c_size_t(0), stream=None)
+    args.update(over)
+    lib.kda_fwd_chunked.restype = ctypes.c_int
+    lib.kda_last_error.restype = ctypes.c_char_p
+    rc = lib.kda_fwd_chunked(args["q"], args["k"], args["v"], args["beta"], args["z"],
+                             args["A_log"], args["g_min"], args["S0"], args["S_out"], args["cu"],
+                             args["N"], args["T"], args["H"], args["dk"], args["dv"], args["dt"],
+                             args["o"], args["ws"], args["ws_bytes"], args["stream"])
+    return rc, lib.kda_last_error().decode()
+
+
+def test_fwd_argument_validation(lib):
+    vp = ctypes.c_void_p
+    cases = [
+        (dict(q=None), 1, "q is NULL"),
+        (dict(k=vp(0x10004)), 1, "16-byte"),
+        (dict(g_min=ctypes.c_float(0.0)), 1, "g_min"),
+        (dict(g_min=ctypes.c_float(float("nan"))), 1, "g_min"),
+        (dict(dk=96), 2, "only 64 and 128"),
+        (dict(dv=32), 2, "only 64 and 128"),
+        (dict(dk=0), 1, "positive"),
+        (dict(H=0), 1, "H=0"),
+        (dict(N=-1), 1, "N=-1"),
+        (dict(N=3), 1, "multiple of N"),
+        (dict(T=ctypes.c_int64(-1)), 1, "T_total"),
+        (dict(dt=7), 1, "kda_dtype_t"),
+        (dict(S0=vp(0x10008)), 1, "S0 is not 16-byte aligned"),
+    ]
+    for over, code, frag in cases:
+        rc, msg = _fwd(lib, **over)
+        assert rc == code, (over, rc, msg)
+        assert frag in msg, (over, msg)
+    # nothing to do is not an error and touches no device
+    rc, msg = _fwd(lib, N=0, T=ctypes.c_int64(0))
+    assert rc == 0, msg
+
+
+def test_decode_and_gate_validation(lib):
+    vp = ctypes.c_void_p
+    a = vp(0x10000)
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_last_error.restype = ctypes.c_char_p
+    rc = lib.kda_decode_step(a, a, a, a, a, a, ctypes.c_float(-5.0), None, 4, 2, 128, 128, 1, a,
+                             None)
+    assert rc == 1 and b"S is NULL" in lib.kda_last_error()
+    rc = lib.kda_decode_step(a, a, a, a, a, a, ctypes.c_float(1.0), a, 4, 2, 128, 128, 1, a, None)
+    assert rc == 1
+    rc = lib.kda_decode_step(a, a, a, a, a, a, ctypes.c_float(-5.0), a, 4, 2, 64, 96, 1, a, None)
+    assert rc == 2
+    lib.kda_gate.restype = ctypes.c_int
+    rc = lib.kda_gate(a, 1, a, ctypes.c_float(-5.0), a, ctypes.c_int64(10), 2, 6, None)
+    assert rc == 1 and b"multiple of 4" in lib.kda_last_error()
+    rc = lib.kda_gate(a, 1, a, ctypes.c_float(-5.0), None, ctypes.c_int64(10), 2, 8, None)
+    assert rc == 1 and b"g_out is NULL" in lib.kda_last_error()
+    rc = lib.kda_gate(None, 1, None, ctypes.c_float(-5.0), None, ctypes.c_int64(0), 2, 8, None)
+    assert rc == 0
+
+
+def test_workspace_size_needs_no_device(lib):
+    lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.kda_fwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    for dt in (0, 1):
+        n = lib.kda_fwd_workspace_size(65536, 1, 32, 128, 128, dt)
+        assert n >= 0

@@ -1,0 +1,35 @@
+"""Pins the reading of the bf16 tolerance ("2e-2 absolute after per-head normalisation").
+
+The exact result, rounded once to bf16, must pass any sensible reading of a bf16 output
+tolerance.  On the seeded B=2, T=4096, H=16, d=128 workload the outputs are heavy-tailed
+(max|o| / rms(o) ~ 20 per head), so the plain reading max|o_bf16 - o| / rms > 2e-2 for the
+exact answer itself; the reading used by the parity tests excludes the output format's
+own half-ulp and accepts the rounded exact answer with zero excess.
+"""
+import numpy as np
+
+import oracle
+from serving_kda_chunkwise_gb300 import inputs
+from kda_testutil import BF16_NORM_TOL, bf16_norm_err, plain_norm_err
+
+
+def test_bf16_rounding_of_exact_result():
+    inp = inputs.workload("fwd_bf16_B2_T4096_H16_d128")
+    o, _ = oracle.recurrent(inp.q.values, inp.k.values, inp.v.values, inp.beta.values,
+                            inp.z.values, inp.A_log, inp.g_min, S0=inp.S0,
+                            cu_seqlens=inp.cu_seqlens, want_state=False)
+    o_b = inputs.bf16_bits_to_f32(inputs.f32_to_bf16_bits(o.astype(np.float32))).astype(
+        np.float64)
+    plain = max(plain_norm_err(o_b[a:b, h], o[a:b, h])
+                for a, b in zip(inp.cu_seqlens[:-1], inp.cu_seqlens[1:]) for h in range(inp.H))
+    ours = max(bf16_norm_err(o_b[a:b, h], o[a:b, h])
+               for a, b in zip(inp.cu_seqlens[:-1], inp.cu_seqlens[1:]) for h in range(inp.H))
+    assert plain > BF16_NORM_TOL       # the plain reading rejects the exact answer
+    assert ours < 1e-6                 # ours accepts it (rounding is within half an ulp)
+    # and it still sees a real error: a 1% perturbation of the largest output fails
+    o_bad = o_b.copy()
+    a, b = inp.cu_seqlens[0], inp.cu_seqlens[1]
+    idx = np.unravel_index(np.argmax(np.abs(o[a:b, 0])), o[a:b, 0].shape)
+    o_bad[a + idx[0], 0, idx[1]] += 0.05 * np.sqrt(np.mean(o[a:b, 0] ** 2)) + 0.01 * abs(
+        o[a + idx[0], 0, idx[1]])
+    assert bf16_norm_err(o_bad[a:b, 0], o[a:b, 0]) > BF16_NORM_TOL
