@@ -118,9 +118,19 @@ kda_status_t kda_gate(const void* z, kda_dtype_t z_dt, const float* A_log, float
     return KDA_OK;
 }
 
+// Which forward kernels a problem takes: the tensor-core path for bf16 I/O with
+// dk = dv = 128, the fp32 CUDA-core path otherwise.  KDA_FWD_PATH=generic in the
+// environment forces the CUDA-core path (the tests use it to cross-check the two).
+static bool use_tc_path(int dk, int dv, kda_dtype_t io_dt) {
+    if (io_dt != KDA_BF16 || dk != 128 || dv != 128) return false;
+    const char* env = getenv("KDA_FWD_PATH");
+    return !(env && strcmp(env, "generic") == 0);
+}
+
 size_t kda_fwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv, kda_dtype_t io_dt) {
-    (void)T_total; (void)N; (void)H; (void)dk; (void)dv; (void)io_dt;
-    return 0;
+    if (T_total < 0 || N < 0 || H <= 0) return 0;
+    if (!use_tc_path(dk, dv, io_dt)) return 0;
+    return kda::fwd_tc_workspace_size(T_total, N, H);
 }
 
 kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const void* beta,
@@ -171,7 +181,8 @@ kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const 
     a.dev_err = device_error_ptr();
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     if (a.dev_err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
-    cudaError_t e = kda::launch_fwd_generic(a);
+    cudaError_t e =
+        use_tc_path(dk, dv, io_dt) ? kda::launch_fwd_tc(a) : kda::launch_fwd_generic(a);
     if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_chunked launch");
     return KDA_OK;
 }

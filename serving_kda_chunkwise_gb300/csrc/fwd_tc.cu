@@ -1,0 +1,790 @@
+// fwd_tc.cu -- chunked KDA forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA),
+// bf16 I/O, dk = dv = 128, chunk C = 64 with 16-token sub-tiles, fp32 state.
+//
+// Method ("Kimi k3 技术报告详解（1）——架构再升华", section "Chunkwise parallel form"):
+// per chunk, with G[r] = sum_{s<=r} g_s (per key channel) and gamma = e^G,
+//   L = StrictTril(Diag(beta)(Gamma*K)(K/Gamma)^T),  A = Tril((Gamma*Q)(K/Gamma)^T)
+//   M = (I + L)^{-1} Diag(beta),  W = M (Gamma*K),  U = M V                      (UT form)
+//   Vt = U - W S,  O = (Gamma*Q) S + A Vt,  S <- Diag(gamma^C) S + (K*gamma^C/Gamma)^T Vt
+// The last line (chunk-to-chunk update) is the recurrence unrolled over one chunk.
+//
+// Three launches on the caller's stream:
+//   plan_kernel   chunk offsets of every sequence (exclusive scan of ceil(len/64)).
+//   intra_kernel  every (chunk, head) in parallel (persistent, one CTA per SM, inputs by
+//                 TMA, next item prefetched): gate + in-chunk cumsum, the two sub-tiled
+//                 Gram matrices in ONE tcgen05 MMA, the UT solve on CUDA cores in fp32,
+//                 W and U by tcgen05; writes one "package" per (head, chunk) whose bytes
+//                 are the shared-memory image of the state kernel's MMA operands.
+//   state_kernel  one CTA per (sequence, head), serial over chunks: state S in fp32
+//                 registers, packages streamed in by bulk copies (double buffered),
+//                 X = S^T W^T, (Gamma Q S)^T, K~^T Vt and Vt A^T on tcgen05.
+//
+// Sub-tiling ("16-token tiles" of the same section; the bounded gate g > g_min is what
+// keeps these factors finite): the Gram entry for rows r >= i needs e^{G_r - G_i} per
+// channel.  With rho_s = G at the 8th row of sub-tile s (its middle), every row r of
+// sub-tile s uses ONE row factor e^{G_r - rho_s} (|exponent| <= 8|g_min| <= 48) and the
+// column operand for that sub-tile is k_i e^{rho_s - G_i}: for i in the same sub-tile the
+// exponent is again bounded by 48, for earlier i it is <= 0 (underflow there only drops
+// terms below e^{-39}).  So the column operand comes in four versions (sub-tile s uses
+// columns i < 16(s+1)); stacking them gives one B operand of 16+32+48+64 = 160 rows, and
+// stacking the q-side and (beta-scaled) k-side row operands gives A with M = 128: a single
+// M=128, N=160, K=128 MMA yields both Grams for every sub-tile pair.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "tc_util.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = 64;    // chunk length
+constexpr int kD = 128;   // head dim (dk = dv)
+constexpr int kThreads = 256;
+
+// ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
+constexpr uint32_t kPkgW = 0;        // W      [64 r][128 c] bf16, K-major sw128
+constexpr uint32_t kPkgQB = 16384;   // Gam*Q  [64 r][128 c] bf16, K-major sw128
+constexpr uint32_t kPkgKT = 32768;   // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
+constexpr uint32_t kPkgAQK = 49152;  // A      [64 r][64 i] bf16, K-major sw128
+constexpr uint32_t kPkgU = 57344;    // U      [64 r][128 j] bf16, plain row-major
+constexpr uint32_t kPkgG = 73728;    // gamma^C [128] fp32
+constexpr uint32_t kPkgBytes = 74240;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ================================================================= plan ====
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int N,
+                                                    int64_t T_total, int32_t* chunk_off,
+                                                    unsigned* err) {
+    __shared__ int32_t s_warp[32];
+    __shared__ int32_t s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) s_carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += blockDim.x) {
+        const int n = base + tid;
+        int32_t cnt = 0;
+        if (n < N) {
+            int64_t b, e;
+            seq_range(cu, n, N, T_total, err, b, e);
+            cnt = static_cast<int32_t>((e - b + kC - 1) / kC);
+        }
+        int32_t x = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_warp[w] = x;
+        __syncthreads();
+        if (w == 0) {
+            int32_t v = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int32_t y = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += y;
+            }
+            s_warp[lane] = v;
+        }
+        __syncthreads();
+        const int32_t incl = x + (w > 0 ? s_warp[w - 1] : 0);
+        if (n < N) chunk_off[n] = s_carry + incl - cnt;
+        __syncthreads();
+        if (tid == (int)blockDim.x - 1) s_carry += incl;
+        __syncthreads();
+    }
+    if (tid == 0) chunk_off[N] = s_carry;
+}
+
+// Sequence n holding global chunk `chunk` (largest n with chunk_off[n] <= chunk).
+__device__ __forceinline__ int find_seq(const int32_t* chunk_off, int N, int chunk) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(chunk_off + mid) <= chunk) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ================================================================ intra ====
+
+struct IntraParams {
+    CUtensorMap tq, tk, tv, tz;  // [T_total, H, 128] bf16, box 64 x 1 x 64, 128-byte swizzle
+    const __nv_bfloat16* beta;
+    const float* A_log;
+    const int32_t* cu;
+    const int32_t* chunk_off;
+    uint8_t* pkg;
+    unsigned* err;
+    int64_t T_total;
+    float g_min;
+    int N, H, maxchunks;
+};
+
+// shared-memory map of the intra kernel (offsets from a 1024-aligned base)
+constexpr uint32_t kInBuf = 65536;           // per input buffer: q, k, v, z (16 KB each)
+constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768, kOffZ = 49152;
+constexpr uint32_t kAStk = 2 * kInBuf;       // 131072: A stack [2 blk][128 rows][128 B]
+constexpr uint32_t kBStk = kAStk + 32768;    // 163840: B stack [2 blk][160 rows][128 B]
+constexpr uint32_t kBeta = kBStk + 40960;    // 204800: beta [64] fp32
+constexpr uint32_t kBars = kBeta + 256;      // mbarriers
+constexpr uint32_t kIntraSmem = kBars + 64 + 1024;  // + alignment slack
+// reuse after the Gram MMA: A stack -> A tile (8 KB) + M tile (8 KB); B stack -> L, T, Y fp32
+constexpr uint32_t kAqkTile = kAStk, kMTile = kAStk + 8192;
+constexpr int kLd = 65;                      // padded fp32 row stride of L and T
+constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4, kSY = kST + 64 * kLd * 4;
+static_assert(kSY + 3 * 256 * 4 <= kBStk + 40960, "solve scratch must fit the B stack");
+
+__device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
+
+__device__ __forceinline__ float bf16_at(const uint8_t* tile, uint32_t off) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + off));
+}
+__device__ __forceinline__ void put_bf16(uint8_t* tile, uint32_t off, float v) {
+    *reinterpret_cast<__nv_bfloat16*>(tile + off) = __float2bfloat16_rn(v);
+}
+
+struct ItemInfo {
+    int h, n, L;
+    int64_t t0;
+    size_t pkg;  // package index
+};
+
+__device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item) {
+    ItemInfo it;
+    const int chunk = item / p.H;
+    it.h = item - chunk * p.H;
+    it.n = find_seq(p.chunk_off, p.N, chunk);
+    int64_t b, e;
+    seq_range(p.cu, it.n, p.N, p.T_total, nullptr, b, e);
+    it.t0 = b + (int64_t)(chunk - __ldg(p.chunk_off + it.n)) * kC;
+    const int64_t rem = e - it.t0;
+    it.L = (int)(rem < kC ? rem : kC);
+    it.pkg = (size_t)it.h * p.maxchunks + chunk;
+    return it;
+}
+
+__device__ __forceinline__ void issue_inputs(const IntraParams& p, const ItemInfo& it,
+                                             uint8_t* buf, uint64_t* bar) {
+    mbar_expect_tx(bar, kInBuf);
+    const int t0 = (int)it.t0;
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb) {
+        tma_load_3d(buf + kOffQ + cb * 8192, &p.tq, cb * 64, it.h, t0, bar);
+        tma_load_3d(buf + kOffK + cb * 8192, &p.tk, cb * 64, it.h, t0, bar);
+        tma_load_3d(buf + kOffV + cb * 8192, &p.tv, cb * 64, it.h, t0, bar);
+        tma_load_3d(buf + kOffZ + cb * 8192, &p.tz, cb * 64, it.h, t0, bar);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(sm);
+    float* sBeta = reinterpret_cast<float*>(sm + kBeta);
+    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kBars);  // [2]
+    uint64_t* mma_bar = tma_bar + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 3);
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        mbar_init(&tma_bar[0], 1);
+        mbar_init(&tma_bar[1], 1);
+        mbar_init(mma_bar, 1);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_items = __ldg(p.chunk_off + p.N) * p.H;
+    uint32_t mma_phase = 0;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+
+    if (tid == 0 && (int)blockIdx.x < n_items)
+        issue_inputs(p, decode_item(p, blockIdx.x), sm, &tma_bar[0]);
+
+    int iter = 0;
+    int pending = ((int)blockIdx.x < n_items) ? 0 : -1;  // buffer with a load in flight (thread 0)
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
+        const int b = iter & 1;
+        uint8_t* buf = sm + b * kInBuf;
+        const ItemInfo it = decode_item(p, item);
+        if (tid == 0) {
+            bulk_wait_read0();  // previous item's package stores have read their smem
+            const int next = item + gridDim.x;
+            pending = -1;
+            if (next < n_items) {
+                fence_async_smem();
+                issue_inputs(p, decode_item(p, next), sm + (b ^ 1) * kInBuf, &tma_bar[b ^ 1]);
+                pending = b ^ 1;
+            }
+        }
+        if (tid < kC)
+            sBeta[tid] = (tid < it.L)
+                             ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h])
+                             : 0.f;
+        if (!mbar_wait(&tma_bar[b], (iter >> 1) & 1, p.err)) s_abort = 1;
+        __syncthreads();
+        if (s_abort) break;
+
+        uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
+
+        // ---- gate, in-chunk cumsum and every decay-scaled operand (one channel per thread)
+        if (tid < kD) {
+            const int c = tid;
+            const float scale = expf(__ldg(p.A_log + it.h));
+            float G[kC];
+            float acc = 0.f;
+#pragma unroll
+            for (int r = 0; r < kC; ++r) {
+                const float zz = bf16_at(buf + kOffZ, sw128_off(r, c, 64));
+                const float g = (r < it.L) ? p.g_min / (1.f + __expf(-scale * zz)) : 0.f;
+                acc += g;
+                G[r] = acc;
+            }
+            const float rho[4] = {G[7], G[23], G[39], G[55]};
+            const float Glast = G[kC - 1];
+            uint8_t* ast = sm + kAStk;
+            uint8_t* bst = sm + kBStk;
+#pragma unroll
+            for (int r = 0; r < kC; ++r) {
+                const int s = r >> 4;
+                const bool ok = r < it.L;
+                const uint32_t o64 = sw128_off(r, c, 64);
+                const float qv = ok ? bf16_at(buf + kOffQ, o64) : 0.f;
+                const float kv = ok ? bf16_at(buf + kOffK, o64) : 0.f;
+                const float e1 = __expf(G[r] - rho[s]);
+                put_bf16(ast, sw128_off(r, c, 128), qv * e1);
+                put_bf16(ast, sw128_off(64 + r, c, 128), sBeta[r] * kv * e1);
+#pragma unroll
+                for (int s2 = s; s2 < 4; ++s2)
+                    put_bf16(bst, sw128_off(kStkOff[s2] + r, c, 160), kv * __expf(rho[s2] - G[r]));
+                const float eg = __expf(G[r]);
+                put_bf16(buf + kOffZ, o64, kv * eg);                     // Gam*K for W = M(Gam*K)
+                put_bf16(pkg + kPkgQB, o64, qv * eg);                    // Gam*Q
+                put_bf16(pkg + kPkgKT, o64, kv * __expf(Glast - G[r]));  // K*gamma^C/Gam
+            }
+            reinterpret_cast<float*>(pkg + kPkgG)[c] = __expf(Glast);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- both Grams: D[128 x 160] = [Q'; beta K'] (128 x 128) * Bstack^T (128 x 160)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16(128, 160, false, false);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t a =
+                    sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + (ks & 3) * 32, 0, 1024);
+                const uint64_t bd =
+                    sdesc_sw128(sbase + kBStk + (ks >> 2) * 20480 + (ks & 3) * 32, 0, 1024);
+                mma_bf16(tmem, a, bd, idesc, ks > 0);
+            }
+            mma_commit(mma_bar);
+        }
+        if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
+        ++mma_phase;
+        tc_fence_after();
+
+        // ---- Gram epilogue: q-side rows -> A tile (bf16), k-side rows -> L (fp32)
+        if (warp < 4) {
+            const int m = tid;  // TMEM lane
+            const int side = m >> 6, r = m & 63, s = r >> 4;
+            float* sL = reinterpret_cast<float*>(sm + kSL);
+            uint8_t* aq = sm + kAqkTile;
+#pragma unroll
+            for (int g = 0; g < 10; ++g) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + 16 * g, v);
+                tmem_ld_wait();
+                const int sg = (g == 0) ? 0 : (g < 3) ? 1 : (g < 6) ? 2 : 3;
+                const int ib = 16 * g - kStkOff[sg];
+                if (sg == s) {
+                    if (side == 0) {
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            uint32_t pw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i0 = ib + 8 * hf + 2 * e;
+                                pw[e] = pack_bf16x2(i0 <= r ? v[8 * hf + 2 * e] : 0.f,
+                                                    i0 + 1 <= r ? v[8 * hf + 2 * e + 1] : 0.f);
+                            }
+                            *reinterpret_cast<uint4*>(aq + sw128_chunk(r, (ib >> 3) + hf)) =
+                                make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            sL[r * kLd + ib + e] = (ib + e < r) ? v[e] : 0.f;
+                    }
+                }
+            }
+            if (side == 0)  // columns past this sub-tile's version are zero
+                for (int ch = 2 * (s + 1); ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (s_abort) break;
+
+        // ---- T = (I + L)^{-1}: 16x16 diagonal blocks by forward substitution, then the
+        //      off-diagonal blocks by distance: T_ss' = -T_ss * sum_{t=s'}^{s-1} L_st T_ts'
+        {
+            const float* sL = reinterpret_cast<const float*>(sm + kSL);
+            float* sT = reinterpret_cast<float*>(sm + kST);
+            float* sY = reinterpret_cast<float*>(sm + kSY);
+            if (warp < 4 && lane < 16) {
+                const int s = warp, j = lane;
+                float t[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    float a = (rr == j) ? 1.f : 0.f;
+#pragma unroll
+                    for (int m = 0; m < rr; ++m)
+                        a = fmaf(-sL[(16 * s + rr) * kLd + 16 * s + m], t[m], a);
+                    t[rr] = a;
+                }
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) sT[(16 * s + rr) * kLd + 16 * s + j] = t[rr];
+            }
+            __syncthreads();
+            for (int d = 1; d < 4; ++d) {
+                const int nb = 4 - d;
+                for (int e = tid; e < nb * 256; e += kThreads) {
+                    const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + d;
+                    float y = 0.f;
+                    for (int t = sp; t < s; ++t)
+#pragma unroll
+                        for (int m = 0; m < 16; ++m)
+                            y = fmaf(sL[(16 * s + rr) * kLd + 16 * t + m],
+                                     sT[(16 * t + m) * kLd + 16 * sp + jj], y);
+                    sY[e] = y;
+                }
+                __syncthreads();
+                for (int e = tid; e < nb * 256; e += kThreads) {
+                    const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + d;
+                    float y = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; ++m)
+                        y = fmaf(sT[(16 * s + rr) * kLd + 16 * s + m], sY[(sp << 8) + m * 16 + jj],
+                                 y);
+                    sT[(16 * s + rr) * kLd + 16 * sp + jj] = -y;
+                }
+                __syncthreads();
+            }
+            // M = T Diag(beta) (lower triangle) as a bf16 K-major tile
+            {
+                const int r = tid >> 2, cq = tid & 3;
+                uint8_t* mt = sm + kMTile;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t pw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = 16 * cq + 8 * hf + 2 * e;
+                        const float m0 = (i0 <= r) ? sT[r * kLd + i0] * sBeta[i0] : 0.f;
+                        const float m1 =
+                            (i0 + 1 <= r) ? sT[r * kLd + i0 + 1] * sBeta[i0 + 1] : 0.f;
+                        pw[e] = pack_bf16x2(m0, m1);
+                    }
+                    *reinterpret_cast<uint4*>(mt + sw128_chunk(r, 2 * cq + hf)) =
+                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- W^T = (Gam K)^T M^T  and  U^T = V^T M^T  (M = 128 channels, N = 64 rows)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
+            const uint32_t ab = sbase + b * kInBuf;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bm = sdesc_sw128(sbase + kMTile + ks * 32, 0, 1024);
+                mma_bf16(tmem, sdesc_sw128(ab + kOffZ + ks * 2048, 8192, 1024), bm, idesc, ks > 0);
+                mma_bf16(tmem + 64, sdesc_sw128(ab + kOffV + ks * 2048, 8192, 1024), bm, idesc,
+                         ks > 0);
+            }
+            mma_commit(mma_bar);
+        }
+        if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
+        ++mma_phase;
+        tc_fence_after();
+        {
+            // warps 0-3: W (lane = channel c) into the q slot; warps 4-7: U (lane = j) into k slot
+            const int m = 32 * (warp & 3) + lane;
+            const uint32_t col0 = (warp < 4) ? 0 : 64;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + col0 + 16 * g, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = 16 * g + e;
+                    if (warp < 4)
+                        put_bf16(buf + kOffQ, sw128_off(r, m, 64), v[e]);
+                    else
+                        put_bf16(buf + kOffK, (uint32_t)(r * 256 + 2 * m), v[e]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (s_abort) break;
+        if (tid == 0) {
+            bulk_s2g(pkg + kPkgW, buf + kOffQ, 16384);
+            bulk_s2g(pkg + kPkgU, buf + kOffK, 16384);
+            bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 8192);
+            bulk_commit();
+        }
+    }
+    // teardown: stores complete, no load in flight, TMEM released
+    if (tid == 0) {
+        bulk_wait0();
+        if (s_abort && pending >= 0) mbar_wait(&tma_bar[pending], (iter >> 1) & 1, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ================================================================ state ====
+
+struct StateParams {
+    const uint8_t* pkg;
+    const int32_t* cu;
+    const int32_t* chunk_off;
+    const float* S0;
+    float* S_out;
+    __nv_bfloat16* o;
+    unsigned* err;
+    int64_t T_total;
+    int N, H, maxchunks;
+};
+
+constexpr uint32_t kStage = 74752;             // package stage stride (73 KB, 1024-aligned)
+constexpr uint32_t kSbf = 2 * kStage;          // S as bf16, A = S^T MN-major [2 blk][128 i][128 B]
+constexpr uint32_t kVt = kSbf + 32768;         // Vt^T K-major [128 j][64 r]
+constexpr uint32_t kSBars = kVt + 16384;
+constexpr uint32_t kStateSmem = kSBars + 64 + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(sm);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2]
+    uint64_t* mma1 = full + 2;
+    uint64_t* mma2 = full + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wg = tid >> 7;               // which half of the columns this thread owns
+    const int m = 32 * (warp & 3) + lane;  // TMEM lane = state row i / value column j
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const int nh = blockIdx.x, h = nh % p.H, n = nh / p.H;
+
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(mma1, 1);
+        mbar_init(mma2, 1);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int64_t t_begin, t_end;
+    seq_range(p.cu, n, p.N, p.T_total, nullptr, t_begin, t_end);
+    const int c0 = __ldg(p.chunk_off + n);
+    const int nch = __ldg(p.chunk_off + n + 1) - c0;
+    const uint8_t* pkg0 = p.pkg + ((size_t)h * p.maxchunks + c0) * kPkgBytes;
+
+    // S[i = m][64 wg + jj] in registers
+    float S[64];
+    const size_t sbase_g = ((size_t)nh * kD + m) * kD + 64 * wg;
+#pragma unroll
+    for (int jj = 0; jj < 64; jj += 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.S0) v = *reinterpret_cast<const float4*>(p.S0 + sbase_g + jj);
+        S[jj] = v.x; S[jj + 1] = v.y; S[jj + 2] = v.z; S[jj + 3] = v.w;
+    }
+    auto write_sbf = [&]() {
+        uint8_t* blk = sm + kSbf + wg * 16384;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            uint4 pk;
+            pk.x = pack_bf16x2(S[8 * ch], S[8 * ch + 1]);
+            pk.y = pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]);
+            pk.z = pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]);
+            pk.w = pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]);
+            *reinterpret_cast<uint4*>(blk + sw128_chunk(m, ch)) = pk;
+        }
+    };
+    write_sbf();
+    if (tid == 0 && nch > 0) {
+        mbar_expect_tx(&full[0], kPkgBytes);
+        bulk_g2s(sm, pkg0, kPkgBytes, &full[0]);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    int issued = (nch > 0) ? 1 : 0;  // packages requested so far (thread 0)
+    int t = 0;
+    for (; t < nch; ++t) {
+        const int st = t & 1;
+        const uint8_t* stage = sm + st * kStage;
+        const uint32_t sstage = sbase + st * kStage;
+        const int64_t t0 = t_begin + (int64_t)t * kC;
+        const int L = (int)((t_end - t0) < kC ? (t_end - t0) : kC);
+        if (tid == 0 && t + 1 < nch) {
+            fence_async_smem();
+            mbar_expect_tx(&full[st ^ 1], kPkgBytes);
+            bulk_g2s(sm + (st ^ 1) * kStage, pkg0 + (size_t)(t + 1) * kPkgBytes, kPkgBytes,
+                     &full[st ^ 1]);
+            issued = t + 2;
+        }
+        if (!mbar_wait(&full[st], (t >> 1) & 1, p.err)) s_abort = 1;
+
+        // X^T = S^T W^T (cols 0..63), (Gam Q S)^T = S^T (Gam Q)^T (cols 64..127)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
+                const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
+                mma_bf16(tmem, a, sdesc_sw128(sstage + kPkgW + kb, 0, 1024), idesc, ks > 0);
+            }
+            mma_commit(mma1);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
+                const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
+                mma_bf16(tmem + 64, a, sdesc_sw128(sstage + kPkgQB + kb, 0, 1024), idesc,
+                         ks > 0);
+            }
+        }
+        if (!mbar_wait(mma1, t & 1, p.err)) s_abort = 1;
+        tc_fence_after();
+
+        // Vt = U - X: thread owns value column j = m and rows r in [32 wg, 32 wg + 32)
+        {
+            const __nv_bfloat16* U = reinterpret_cast<const __nv_bfloat16*>(stage + kPkgU);
+#pragma unroll
+            for (int hx = 0; hx < 2; ++hx) {
+                float x[16];
+                tmem_ld16(tmem + lane_base + 32 * wg + 16 * hx, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t pw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int r = 32 * wg + 16 * hx + 8 * cc + 2 * e;
+                        const float u0 = __bfloat162float(U[r * kD + m]);
+                        const float u1 = __bfloat162float(U[(r + 1) * kD + m]);
+                        pw[e] = pack_bf16x2(u0 - x[8 * cc + 2 * e], u1 - x[8 * cc + 2 * e + 1]);
+                    }
+                    *reinterpret_cast<uint4*>(sm + kVt + sw128_chunk(m, 4 * wg + 2 * hx + cc)) =
+                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (s_abort) break;
+
+        // dS = K~^T Vt (cols 128..255);  O^T += Vt^T A^T (cols 64..127)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id2 = idesc_bf16(128, 128, true, false);
+            constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tmem + 128, sdesc_sw128(sstage + kPkgKT + ks * 2048, 8192, 1024),
+                         sdesc_sw128(sbase + kVt + ks * 32, 0, 1024), id2, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tmem + 64, sdesc_sw128(sbase + kVt + ks * 32, 0, 1024),
+                         sdesc_sw128(sstage + kPkgAQK + ks * 32, 0, 1024), id3, 1);
+            mma_commit(mma2);
+        }
+        if (!mbar_wait(mma2, t & 1, p.err)) s_abort = 1;
+        tc_fence_after();
+
+        // S <- gamma^C * S + dS ;  bf16 copy for the next chunk's MMAs
+        {
+            const float gam = reinterpret_cast<const float*>(stage + kPkgG)[m];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + 128 + 64 * wg + 16 * g, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gam, S[16 * g + e], v[e]);
+            }
+            write_sbf();
+        }
+        // output rows r in [32 wg, 32 wg + 32) of value column j = m
+        {
+            __nv_bfloat16* orow = p.o + ((size_t)t0 * p.H + h) * kD + m;
+#pragma unroll
+            for (int hx = 0; hx < 2; ++hx) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + 64 + 32 * wg + 16 * hx, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = 32 * wg + 16 * hx + e;
+                    if (r < L) orow[(size_t)r * p.H * kD] = __float2bfloat16_rn(v[e]);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (s_abort) break;
+    }
+    if (p.S_out && !s_abort) {
+#pragma unroll
+        for (int jj = 0; jj < 64; jj += 4)
+            *reinterpret_cast<float4*>(p.S_out + sbase_g + jj) =
+                make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
+    }
+    // on an abort, let a package copy still in flight land before leaving
+    if (tid == 0 && s_abort && issued > t + 1)
+        mbar_wait(&full[(t + 1) & 1], ((t + 1) >> 1) & 1, nullptr);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 256);
+    }
+}
+
+// ================================================================= host ====
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    const cuuint32_t box[3] = {64, 1, kC};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t fwd_tc_workspace_size(int64_t T_total, int N, int H) {
+    const int64_t maxchunks = T_total / kC + N;
+    return align_up((size_t)(N + 1) * sizeof(int32_t), 1024) +
+           (size_t)H * (size_t)maxchunks * kPkgBytes;
+}
+
+cudaError_t launch_fwd_tc(const FwdArgs& a) {
+    if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    int32_t* chunk_off = reinterpret_cast<int32_t*>(ws);
+    uint8_t* pkg = ws + align_up((size_t)(a.N + 1) * sizeof(int32_t), 1024);
+    const int maxchunks = (int)(a.T_total / kC + a.N);
+
+    plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, chunk_off, a.dev_err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    if (a.T_total > 0) {
+        IntraParams ip;
+        if (!make_map(&ip.tq, a.q, a.T_total, a.H) || !make_map(&ip.tk, a.k, a.T_total, a.H) ||
+            !make_map(&ip.tv, a.v, a.T_total, a.H) || !make_map(&ip.tz, a.z, a.T_total, a.H))
+            return cudaErrorInvalidValue;
+        ip.beta = static_cast<const __nv_bfloat16*>(a.beta);
+        ip.A_log = a.A_log;
+        ip.cu = a.cu_seqlens;
+        ip.chunk_off = chunk_off;
+        ip.pkg = pkg;
+        ip.err = a.dev_err;
+        ip.T_total = a.T_total;
+        ip.g_min = a.g_min;
+        ip.N = a.N;
+        ip.H = a.H;
+        ip.maxchunks = maxchunks;
+        e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kIntraSmem);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        intra_kernel<<<sms, kThreads, kIntraSmem, a.stream>>>(ip);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    StateParams sp;
+    sp.pkg = pkg;
+    sp.cu = a.cu_seqlens;
+    sp.chunk_off = chunk_off;
+    sp.S0 = a.S0;
+    sp.S_out = a.S_out;
+    sp.o = static_cast<__nv_bfloat16*>(a.o);
+    sp.err = a.dev_err;
+    sp.T_total = a.T_total;
+    sp.N = a.N;
+    sp.H = a.H;
+    sp.maxchunks = maxchunks;
+    e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStateSmem);
+    if (e != cudaSuccess) return e;
+    state_kernel<<<a.N * a.H, kThreads, kStateSmem, a.stream>>>(sp);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -38,4 +38,9 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const voi
 // Chunked forward on CUDA cores in fp32 (any dtype, dk/dv in {64,128}).
 cudaError_t launch_fwd_generic(const FwdArgs& a);
 
+// Chunked forward on tcgen05 tensor cores (bf16 I/O, dk = dv = 128); needs a workspace of
+// fwd_tc_workspace_size() bytes.
+size_t fwd_tc_workspace_size(int64_t T_total, int N, int H);
+cudaError_t launch_fwd_tc(const FwdArgs& a);
+
 }  // namespace kda

@@ -182,3 +182,20 @@ def test_fwd_bad_seqlens_reported(kda):
         kda.device_status()
     assert ei.value.status == kda.KDA_ERR_DEVICE
     kda.device_status()   # cleared
+
+
+def test_fwd_tensor_core_path_matches_cuda_core_path(kda, monkeypatch):
+    """The tcgen05 path (bf16, d=128) against the fp32 CUDA-core path on the same inputs."""
+    inp = inputs.forward_inputs(seed=81, lengths=[333, 64, 1, 190], H=3, dk=128, dv=128,
+                                dtype="bf16", with_state=True, g_min=-6.0)
+    o_tc, S_tc = gpu_forward(inp)
+    monkeypatch.setenv("KDA_FWD_PATH", "generic")
+    assert kda.workspace_size(inp.T, inp.N, inp.H, 128, 128, __import__("torch").bfloat16) == 0
+    o_cc, S_cc = gpu_forward(inp)
+    from kda_testutil import bf16_norm_err
+    for n in range(inp.N):
+        a, b = inp.cu_seqlens[n], inp.cu_seqlens[n + 1]
+        for h in range(inp.H):
+            assert bf16_norm_err(o_tc[a:b, h], o_cc[a:b, h].astype(np.float64)) < 2e-2
+            rms = np.sqrt(np.mean(S_cc[n, h] ** 2))
+            assert np.max(np.abs(S_tc[n, h] - S_cc[n, h])) / rms < 2e-2
