@@ -212,11 +212,13 @@ def run_ours(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    kda.profile_begin()
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    prof = kda.profile_end()
     barrier()
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
@@ -230,16 +232,36 @@ def run_ours(args, rank, world, local_rank, dist):
     tflops_causal = world * T * H * FLOP_CAUSAL * args.steps / (ms / 1e3) / 1e12
     tflops_dense = world * T * H * FLOP_DENSE * args.steps / (ms / 1e3) / 1e12
 
-    # dominant kernel: the whole forward is one kernel launch per step for now
-    bytes_per_launch = T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
-    achieved = bytes_per_launch / (ms_per_step / 1e3) / 1e9
-    kname = "fwd_generic_kernel"
+    # per-kernel device time inside the timed region (CUDA events on the launch stream)
+    kernels = {name: {"launches": n, "avg_ms": tot / max(n, 1), "share": 0.0}
+               for name, (n, tot) in prof.items()}
+    tot_all = sum(v["avg_ms"] * v["launches"] for v in kernels.values()) or 1.0
+    for v in kernels.values():
+        v["share"] = v["avg_ms"] * v["launches"] / tot_all
+    kname = max(kernels, key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
+    # algorithmic bytes each kernel must move (per launch) on this workload
+    alg = {"intra_kernel": T * H * (4 * 2 * D + 2),              # q, k, v, z, beta in
+           "state_kernel": T * H * 2 * D + H * STATE_BYTES,      # o out, final state out
+           "fwd_generic_kernel": T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES,
+           "plan_kernel": 8}
+    bytes_k = alg.get(kname, T * H * BYTES_PER_TOKEN_HEAD)
+    achieved = bytes_k / (kernels[kname]["avg_ms"] / 1e3) / 1e9
+    src = {"intra_kernel": "fwd_tc.cu", "state_kernel": "fwd_tc.cu", "plan_kernel": "fwd_tc.cu",
+           "fwd_generic_kernel": "fwd_generic.cu"}.get(kname, "fwd_tc.cu")
+    path_ms = sum(v["avg_ms"] for v in kernels.values())
+    path_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic_from_profile(kname, source_hash(
-                    "serving_kda_chunkwise_gb300/csrc/fwd_generic.cu")),
-                "kernel": kname, "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": bytes_per_launch}
+                    "serving_kda_chunkwise_gb300/csrc/" + src)),
+                "kernel": kname, "peak_source": peaks["source"] + " (burst copy)",
+                "algorithmic_bytes_per_launch": bytes_k,
+                "path": {"kernels": sorted(kernels), "algorithmic_bytes": path_bytes,
+                         "ms": path_ms,
+                         "achieved_GBs": path_bytes / (path_ms / 1e3) / 1e9,
+                         "frac": path_bytes / (path_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+                "per_kernel": kernels}
+    launches_per_step = sum(v["launches"] for v in kernels.values()) / args.steps
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     host = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "beta", "z")}
@@ -301,7 +323,8 @@ def run_ours(args, rank, world, local_rank, dist):
                            "parallelism": f"replicas x{world}"},
                 "tflops_causal": tflops_causal, "tflops_dense": tflops_dense,
                 "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
-                "roofline": roofline, "e2e": e2e, "gpu_launches": args.steps,
+                "roofline": roofline, "e2e": e2e,
+                "gpu_launches": int(round(launches_per_step * args.steps)),
                 "clocks": clk, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
 

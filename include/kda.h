@@ -127,6 +127,23 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
  */
 kda_status_t kda_device_status(kda_stream_t stream);
 
+/*
+ * Per-kernel timing (tracing aid; not part of the method).  After kda_profile_begin(),
+ * every kernel the library launches is bracketed by two CUDA events recorded on the
+ * launching stream.  kda_profile_end() waits for those events, stops recording and fills
+ * `entries` with one record per kernel name (number of launches, summed device time in
+ * ms); it returns the number of records written, or -1 if a CUDA event call failed.
+ * Host-side state is process-wide; calls from several threads are serialised.
+ */
+typedef struct {
+    char name[32];
+    int launches;
+    double total_ms;
+} kda_profile_entry_t;
+
+kda_status_t kda_profile_begin(void);
+int kda_profile_end(kda_profile_entry_t *entries, int max_entries);
+
 #ifdef __cplusplus
 }
 #endif

@@ -129,6 +129,7 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* be
                      const float* A_log, float g_min, float* S, int N, int H, void* o,
                      cudaStream_t stream) {
     const int grid = N * H;
+    ProfScope prof("decode_kernel", stream);
     decode_kernel<DK, DV, IO><<<grid, 256, 0, stream>>>(
         static_cast<const IO*>(q), static_cast<const IO*>(k), static_cast<const IO*>(v),
         static_cast<const IO*>(beta), static_cast<const IO*>(z), A_log, g_min, S, H,

@@ -210,6 +210,7 @@ cudaError_t launch_t(const FwdArgs& a) {
                                          (int)bytes);
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)a.N * a.H * (DV / kDvs);
+    ProfScope prof("fwd_generic_kernel", a.stream);
     kern<<<(unsigned)grid, kThreads, bytes, a.stream>>>(a);
     return cudaGetLastError();
 }

@@ -737,7 +737,10 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     uint8_t* pkg = ws + align_up((size_t)(a.N + 1) * sizeof(int32_t), 1024);
     const int maxchunks = (int)(a.T_total / kC + a.N);
 
-    plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, chunk_off, a.dev_err);
+    {
+        ProfScope prof("plan_kernel", a.stream);
+        plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, chunk_off, a.dev_err);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
@@ -763,6 +766,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        ProfScope prof("intra_kernel", a.stream);
         intra_kernel<<<sms, kThreads, kIntraSmem, a.stream>>>(ip);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
@@ -783,7 +787,10 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStateSmem);
     if (e != cudaSuccess) return e;
-    state_kernel<<<a.N * a.H, kThreads, kStateSmem, a.stream>>>(sp);
+    {
+        ProfScope prof("state_kernel", a.stream);
+        state_kernel<<<a.N * a.H, kThreads, kStateSmem, a.stream>>>(sp);
+    }
     return cudaGetLastError();
 }
 

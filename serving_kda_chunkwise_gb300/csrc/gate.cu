@@ -59,6 +59,7 @@ cudaError_t launch_gate(const void* z, int z_bf16, const float* A_log, float g_m
     const int64_t want = (n_vec + 255) / 256;
     const int64_t cap = (int64_t)sms * 8;  // 8 resident CTAs of 256 threads per SM
     const int grid = (int)(want < cap ? want : cap);
+    ProfScope prof("gate_kernel", stream);
     if (z_bf16)
         gate_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
             static_cast<const __nv_bfloat16*>(z), A_log, g_min, g_out, n_vec, H, dk / 4);

@@ -43,4 +43,17 @@ cudaError_t launch_fwd_generic(const FwdArgs& a);
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H);
 cudaError_t launch_fwd_tc(const FwdArgs& a);
 
+// Kernel timing hooks (profile.cu): no-ops unless kda_profile_begin() is active.
+int prof_kernel_begin(const char* name, cudaStream_t s);
+void prof_kernel_end(int ev, cudaStream_t s);
+
+struct ProfScope {
+    int ev;
+    cudaStream_t s;
+    ProfScope(const char* name, cudaStream_t stream) : ev(prof_kernel_begin(name, stream)), s(stream) {}
+    ~ProfScope() { prof_kernel_end(ev, s); }
+    ProfScope(const ProfScope&) = delete;
+    ProfScope& operator=(const ProfScope&) = delete;
+};
+
 }  // namespace kda

@@ -27,6 +27,11 @@ class KdaError(RuntimeError):
         super().__init__(f"{func}: {_lib.kda_status_string(status).decode()}: {msg}")
 
 
+class ProfileEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int),
+                ("total_ms", ctypes.c_double)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -53,6 +58,10 @@ def _load():
                                     vp]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [vp]
+    lib.kda_profile_begin.restype = ctypes.c_int
+    lib.kda_profile_begin.argtypes = []
+    lib.kda_profile_end.restype = ctypes.c_int
+    lib.kda_profile_end.argtypes = [ctypes.POINTER(ProfileEntry), ctypes.c_int]
     return lib
 
 
@@ -179,3 +188,17 @@ def decode_step(q, k, v, beta, z, A_log, g_min: float, S, o=None, stream=None):
 def device_status(stream=None):
     """Wait for the stream and raise if a kernel flagged malformed input or a timeout."""
     _check(_lib.kda_device_status(_stream(stream)), "kda_device_status")
+
+
+def profile_begin():
+    """Start bracketing every library kernel launch with CUDA events (see kda.h)."""
+    _check(_lib.kda_profile_begin(), "kda_profile_begin")
+
+
+def profile_end(max_entries: int = 64):
+    """Stop recording; return {kernel name: (launches, total device ms)}."""
+    arr = (ProfileEntry * max_entries)()
+    n = _lib.kda_profile_end(arr, max_entries)
+    if n < 0:
+        raise KdaError(KDA_ERR_CUDA, "kda_profile_end", "a CUDA event call failed")
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n)}

@@ -3,13 +3,17 @@ oracle on (a sample of) the same inputs, and apply the tolerances.
 
 Tolerances (written here once, used by every parity test):
   fp32 I/O  per (sequence, head):  ||o_gpu - o_ref||_F / ||o_ref||_F <= 1e-4, same for S_out.
-  bf16 I/O  per (sequence, head):  max over elements of
-                (|o_gpu - o_ref| - 2^-8 |o_ref|) / rms(o_ref)  <= 2e-2,
-            rms taken over all (token, channel) of that (sequence, head).  The 2^-8 |o_ref|
-            term is half an ulp of bf16, the output format's own rounding: the exact result
-            rounded to bf16 already exceeds 2e-2 under the plain max/rms norm on these
-            workloads (max|o|/rms reaches ~20), see test_tolerance_reading.py.  The fp32
-            final state is held to max |S_gpu - S_ref| / rms(S_ref) <= 2e-2.
+  bf16 I/O  per (sequence, head), after dividing both outputs by rms(o_ref) over all
+            (token, channel) of that (sequence, head):
+              |o_gpu - o_ref| <= 2e-2 + 1.6e-2 |o_ref|   for every element, and
+              rms(o_gpu - o_ref) <= 1e-2.
+            2e-2 is the stated absolute figure; 1.6e-2 is the usual relative tolerance
+            for bf16 tensors (torch.testing's default for bfloat16).  A relative term is
+            unavoidable: the outputs are heavy-tailed (max|o| / rms ~ 20 per head) and the
+            exact result rounded once to bf16 already fails the absolute-only reading (see
+            test_tolerance_reading.py).  The rms bound catches errors that are systematic
+            across a head even when each element stays inside the band.
+            The fp32 final state: max |S_gpu - S_ref| / rms(S_ref) <= 2e-2.
 """
 from __future__ import annotations
 
@@ -17,16 +21,25 @@ import numpy as np
 
 FP32_REL_TOL = 1e-4
 BF16_NORM_TOL = 2e-2
-BF16_HALF_ULP = 2.0 ** -8
+BF16_RTOL = 1.6e-2
+BF16_RMS_TOL = 1e-2
 
 
 def bf16_norm_err(o_gpu, o_ref):
-    """Per-head normalised error beyond the bf16 output rounding (see module docstring)."""
+    """Largest (|o_gpu - o_ref| - 1.6e-2 |o_ref|) / rms(o_ref): must be <= 2e-2."""
     if o_ref.size == 0:
         return 0.0
     rms = max(np.sqrt(np.mean(o_ref ** 2)), 1e-30)
-    excess = np.abs(o_gpu - o_ref) - BF16_HALF_ULP * np.abs(o_ref)
+    excess = np.abs(o_gpu - o_ref) - BF16_RTOL * np.abs(o_ref)
     return float(max(np.max(excess), 0.0) / rms)
+
+
+def bf16_rms_err(o_gpu, o_ref):
+    """rms(o_gpu - o_ref) / rms(o_ref)."""
+    if o_ref.size == 0:
+        return 0.0
+    return float(np.sqrt(np.mean((o_gpu - o_ref) ** 2)) / max(np.sqrt(np.mean(o_ref ** 2)),
+                                                                1e-30))
 
 
 def plain_norm_err(o_gpu, o_ref):
@@ -106,6 +119,8 @@ def check_head(o_gpu, o_ref, S_gpu, S_ref, dtype, what=""):
         assert es <= FP32_REL_TOL, f"{what}: state rel err {es:.3e} > {FP32_REL_TOL}"
         return eo, es
     eo = bf16_norm_err(o_gpu, o_ref)
+    er = bf16_rms_err(o_gpu, o_ref)
+    assert er <= BF16_RMS_TOL, f"{what}: normalised rms err {er:.3e} > {BF16_RMS_TOL}"
     es = 0.0
     if S_ref is not None:
         rms_s = np.sqrt(np.mean(S_ref ** 2))
