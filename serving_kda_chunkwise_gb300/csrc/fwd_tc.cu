@@ -48,11 +48,11 @@ constexpr int kD = 128;   // head dim (dk = dv)
 constexpr int kThreads = 256;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
-constexpr uint32_t kPkgW = 0;        // W      [64 r][128 c] bf16, K-major sw128
+constexpr uint32_t kPkgW = 0;        // W^T    [128 c][64 r] bf16 sw128: B = W^T MN-major
 constexpr uint32_t kPkgQB = 16384;   // Gam*Q  [64 r][128 c] bf16, K-major sw128
 constexpr uint32_t kPkgKT = 32768;   // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
 constexpr uint32_t kPkgAQK = 49152;  // A      [64 r][64 i] bf16, K-major sw128
-constexpr uint32_t kPkgU = 57344;    // U      [64 r][128 j] bf16, plain row-major
+constexpr uint32_t kPkgU = 57344;    // U^T    [128 j][64 r] bf16 sw128
 constexpr uint32_t kPkgG = 73728;    // gamma^C [128] fp32
 constexpr uint32_t kPkgBytes = 74240;
 
@@ -128,19 +128,31 @@ struct IntraParams {
     int N, H, maxchunks;
 };
 
-// shared-memory map of the intra kernel (offsets from a 1024-aligned base)
-constexpr uint32_t kInBuf = 65536;           // per input buffer: q, k, v, z (16 KB each)
-constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768, kOffZ = 49152;
-constexpr uint32_t kAStk = 2 * kInBuf;       // 131072: A stack [2 blk][128 rows][128 B]
-constexpr uint32_t kBStk = kAStk + 32768;    // 163840: B stack [2 blk][160 rows][128 B]
-constexpr uint32_t kBeta = kBStk + 40960;    // 204800: beta [64] fp32
-constexpr uint32_t kBars = kBeta + 256;      // mbarriers
+// Shared-memory map of the intra kernel (offsets from a 1024-aligned base).  The q, k, v
+// tiles are double buffered (next item prefetched by TMA); z has one buffer, refilled for
+// the next item as soon as the gate of the current one has been evaluated.
+constexpr uint32_t kInBuf = 49152;           // per input buffer: q, k, v (16 KB each)
+constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;
+constexpr uint32_t kAStk = 2 * kInBuf;       //  98304: A hi [2 blk][128 rows][128 B]
+constexpr uint32_t kALo = kAStk + 32768;     // 131072: q-side A lo [2 blk][64 rows][128 B]
+constexpr uint32_t kBStk = kALo + 16384;     // 147456: B hi [2 blk][160 rows][128 B]
+constexpr uint32_t kBLo = kBStk + 40960;     // 188416: diagonal-column lo [2 blk][64][128 B]
+constexpr uint32_t kZBuf = kBLo + 16384;     // 204800: z [2 blk][64 rows][128 B]
+constexpr uint32_t kXch = kZBuf + 16384;     // 221184: exchange (fp32): tot[128], rho[4][128],
+                                             //         E[4][128] = e^rho, F[4][128] = e^{Glast-rho}
+constexpr uint32_t kBeta = kXch + 13 * 512;  // 227840: beta [2][64] fp32
+constexpr uint32_t kBars = kBeta + 512;      // mbarriers
 constexpr uint32_t kIntraSmem = kBars + 64 + 1024;  // + alignment slack
-// reuse after the Gram MMA: A stack -> A tile (8 KB) + M tile (8 KB); B stack -> L, T, Y fp32
-constexpr uint32_t kAqkTile = kAStk, kMTile = kAStk + 8192;
+static_assert(kIntraSmem <= 232448, "intra kernel exceeds the shared-memory limit");
+// reuse after the Gram MMAs: A hi -> A tile (8 KB) + M tile (8 KB); A lo -> Gam*K (16 KB);
+// B hi -> L, T, Y (fp32).  After the W/U MMAs the q / k slots stage W^T and U^T.
+constexpr uint32_t kAqkTile = kAStk, kMTile = kAStk + 8192, kKbar = kALo;
 constexpr int kLd = 65;                      // padded fp32 row stride of L and T
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4, kSY = kST + 64 * kLd * 4;
 static_assert(kSY + 3 * 256 * 4 <= kBStk + 40960, "solve scratch must fit the B stack");
+// TMEM columns: main Gram accumulator [0, 160), q-side lo correction [256, 416);
+// later W^T [0, 64) and U^T [64, 128).
+constexpr uint32_t kTmemCols = 512, kTLo = 256;
 
 __device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
 
@@ -149,6 +161,13 @@ __device__ __forceinline__ float bf16_at(const uint8_t* tile, uint32_t off) {
 }
 __device__ __forceinline__ void put_bf16(uint8_t* tile, uint32_t off, float v) {
     *reinterpret_cast<__nv_bfloat16*>(tile + off) = __float2bfloat16_rn(v);
+}
+// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): twice bf16's significand.
+__device__ __forceinline__ void put_hilo(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off,
+                                         float v) {
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    *reinterpret_cast<__nv_bfloat16*>(hi_tile + off) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(lo_tile + off) = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
 struct ItemInfo {
@@ -171,8 +190,8 @@ __device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item) 
     return it;
 }
 
-__device__ __forceinline__ void issue_inputs(const IntraParams& p, const ItemInfo& it,
-                                             uint8_t* buf, uint64_t* bar) {
+__device__ __forceinline__ void issue_qkv(const IntraParams& p, const ItemInfo& it, uint8_t* buf,
+                                          uint64_t* bar) {
     mbar_expect_tx(bar, kInBuf);
     const int t0 = (int)it.t0;
 #pragma unroll
@@ -180,8 +199,21 @@ __device__ __forceinline__ void issue_inputs(const IntraParams& p, const ItemInf
         tma_load_3d(buf + kOffQ + cb * 8192, &p.tq, cb * 64, it.h, t0, bar);
         tma_load_3d(buf + kOffK + cb * 8192, &p.tk, cb * 64, it.h, t0, bar);
         tma_load_3d(buf + kOffV + cb * 8192, &p.tv, cb * 64, it.h, t0, bar);
-        tma_load_3d(buf + kOffZ + cb * 8192, &p.tz, cb * 64, it.h, t0, bar);
     }
+}
+
+__device__ __forceinline__ void issue_z(const IntraParams& p, const ItemInfo& it, uint8_t* zbuf,
+                                        uint64_t* bar) {
+    mbar_expect_tx(bar, 16384);
+#pragma unroll
+    for (int cb = 0; cb < 2; ++cb)
+        tma_load_3d(zbuf + cb * 8192, &p.tz, cb * 64, it.h, (int)it.t0, bar);
+}
+
+__device__ __forceinline__ void load_beta(const IntraParams& p, const ItemInfo& it, float* dst,
+                                          int tid) {
+    if (tid < kC)
+        dst[tid] = (tid < it.L) ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
@@ -189,21 +221,27 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    float* sBeta = reinterpret_cast<float*>(sm + kBeta);
-    uint64_t* tma_bar = reinterpret_cast<uint64_t*>(sm + kBars);  // [2]
-    uint64_t* mma_bar = tma_bar + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tma_bar + 3);
+    float* xtot = reinterpret_cast<float*>(sm + kXch);  // [128]
+    float* xrho = xtot + 128;                           // [4][128]
+    float* xE = xrho + 512;                             // [4][128]
+    float* xF = xE + 512;                               // [4][128]
+    uint64_t* qkv_bar = reinterpret_cast<uint64_t*>(sm + kBars);  // [2]
+    uint64_t* z_bar = qkv_bar + 2;
+    uint64_t* mma_bar = qkv_bar + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qkv_bar + 4);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = tid & 127, half = tid >> 7, r0 = 32 * half;  // operand pass: channel, rows
     if (tid == 0) {
-        mbar_init(&tma_bar[0], 1);
-        mbar_init(&tma_bar[1], 1);
+        mbar_init(&qkv_bar[0], 1);
+        mbar_init(&qkv_bar[1], 1);
+        mbar_init(z_bar, 1);
         mbar_init(mma_bar, 1);
         fence_mbar_init();
         s_abort = 0;
     }
-    if (warp == 0) tmem_alloc(tmem_slot, 256);
+    if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -212,87 +250,149 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     uint32_t mma_phase = 0;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
-    if (tid == 0 && (int)blockIdx.x < n_items)
-        issue_inputs(p, decode_item(p, blockIdx.x), sm, &tma_bar[0]);
+    // parity of the phase a load in flight will complete, or -1 (thread 0; for a clean abort)
+    int pend_q[2] = {-1, -1}, pend_z = -1;
+    if ((int)blockIdx.x < n_items) {
+        const ItemInfo first = decode_item(p, blockIdx.x);
+        if (tid == 0) {
+            issue_qkv(p, first, sm, &qkv_bar[0]);
+            issue_z(p, first, sm + kZBuf, z_bar);
+            pend_q[0] = 0;
+            pend_z = 0;
+        }
+        load_beta(p, first, reinterpret_cast<float*>(sm + kBeta), tid);
+    }
 
     int iter = 0;
-    int pending = ((int)blockIdx.x < n_items) ? 0 : -1;  // buffer with a load in flight (thread 0)
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
         const int b = iter & 1;
         uint8_t* buf = sm + b * kInBuf;
+        float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
         const ItemInfo it = decode_item(p, item);
+        const int next = item + gridDim.x;
+        const bool has_next = next < n_items;
+        ItemInfo nx;
+        if (has_next) nx = decode_item(p, next);
         if (tid == 0) {
             bulk_wait_read0();  // previous item's package stores have read their smem
-            const int next = item + gridDim.x;
-            pending = -1;
-            if (next < n_items) {
+            if (has_next) {
                 fence_async_smem();
-                issue_inputs(p, decode_item(p, next), sm + (b ^ 1) * kInBuf, &tma_bar[b ^ 1]);
-                pending = b ^ 1;
+                issue_qkv(p, nx, sm + (b ^ 1) * kInBuf, &qkv_bar[b ^ 1]);
+                pend_q[b ^ 1] = ((iter + 1) >> 1) & 1;
             }
         }
-        if (tid < kC)
-            sBeta[tid] = (tid < it.L)
-                             ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h])
-                             : 0.f;
-        if (!mbar_wait(&tma_bar[b], (iter >> 1) & 1, p.err)) s_abort = 1;
+        if (has_next) load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1), tid);
+        uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
+
+        // ---- gate and in-chunk cumsum: channel c, rows [r0, r0 + 32)
+        if (mbar_wait(z_bar, iter & 1, p.err)) {
+            if (tid == 0) pend_z = -1;
+        } else {
+            s_abort = 1;
+        }
+        float G[32];
+        {
+            const float scale = expf(__ldg(p.A_log + it.h));
+            float acc = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = r0 + rr;
+                const float zz = bf16_at(sm + kZBuf, sw128_off(r, c, 64));
+                acc += (r < it.L) ? p.g_min / (1.f + __expf(-scale * zz)) : 0.f;
+                G[rr] = acc;
+            }
+            if (half == 0) xtot[c] = acc;
+        }
+        __syncthreads();
+        if (half == 1) {
+            const float off = xtot[c];
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) G[rr] += off;
+        }
+        xrho[(2 * half) * 128 + c] = G[7];       // rho of sub-tile 2*half
+        xrho[(2 * half + 1) * 128 + c] = G[23];  // rho of sub-tile 2*half + 1
+        if (half == 1) xtot[c] = G[31];          // G of the chunk's last row
+        __syncthreads();
+        if (tid == 0 && has_next && pend_z < 0) {  // z is consumed: fetch the next item's
+            issue_z(p, nx, sm + kZBuf, z_bar);
+            pend_z = (iter + 1) & 1;
+        }
+        {
+            const float glast = xtot[c];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int s = 2 * half + q;
+                const float rho = xrho[s * 128 + c];
+                xE[s * 128 + c] = __expf(rho);
+                xF[s * 128 + c] = __expf(glast - rho);
+            }
+            if (half == 1) reinterpret_cast<float*>(pkg + kPkgG)[c] = __expf(glast);
+        }
+        if (mbar_wait(&qkv_bar[b], (iter >> 1) & 1, p.err)) {
+            if (tid == 0) pend_q[b] = -1;
+        } else {
+            s_abort = 1;
+        }
         __syncthreads();
         if (s_abort) break;
 
-        uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
-
-        // ---- gate, in-chunk cumsum and every decay-scaled operand (one channel per thread)
-        if (tid < kD) {
-            const int c = tid;
-            const float scale = expf(__ldg(p.A_log + it.h));
-            float G[kC];
-            float acc = 0.f;
+        // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
+        //      column operand of version s2 >= s is k_r e^{rho_s2 - G_r}.
 #pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                const float zz = bf16_at(buf + kOffZ, sw128_off(r, c, 64));
-                const float g = (r < it.L) ? p.g_min / (1.f + __expf(-scale * zz)) : 0.f;
-                acc += g;
-                G[r] = acc;
+        for (int rr = 0; rr < 32; ++rr) {
+            const int r = r0 + rr, s = r >> 4;
+            const bool ok = r < it.L;
+            const uint32_t o64 = sw128_off(r, c, 64);
+            const float qv = ok ? bf16_at(buf + kOffQ, o64) : 0.f;
+            const float kv = ok ? bf16_at(buf + kOffK, o64) : 0.f;
+            const float rho = xrho[s * 128 + c];
+            const float e1 = __expf(G[rr] - rho);
+            const float dc = __expf(rho - G[rr]);
+            put_hilo(sm + kAStk, sm + kALo, sw128_off(r, c, 128), qv * e1);
+            put_bf16(sm + kAStk, sw128_off(64 + r, c, 128), sBeta[r] * kv * e1);
+            {
+                const float v = kv * dc;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                *reinterpret_cast<__nv_bfloat16*>(sm + kBStk + sw128_off(kStkOff[s] + r, c, 160)) = hi;
+                *reinterpret_cast<__nv_bfloat16*>(sm + kBLo + o64) =
+                    __float2bfloat16_rn(v - __bfloat162float(hi));
             }
-            const float rho[4] = {G[7], G[23], G[39], G[55]};
-            const float Glast = G[kC - 1];
-            uint8_t* ast = sm + kAStk;
-            uint8_t* bst = sm + kBStk;
-#pragma unroll
-            for (int r = 0; r < kC; ++r) {
-                const int s = r >> 4;
-                const bool ok = r < it.L;
-                const uint32_t o64 = sw128_off(r, c, 64);
-                const float qv = ok ? bf16_at(buf + kOffQ, o64) : 0.f;
-                const float kv = ok ? bf16_at(buf + kOffK, o64) : 0.f;
-                const float e1 = __expf(G[r] - rho[s]);
-                put_bf16(ast, sw128_off(r, c, 128), qv * e1);
-                put_bf16(ast, sw128_off(64 + r, c, 128), sBeta[r] * kv * e1);
-#pragma unroll
-                for (int s2 = s; s2 < 4; ++s2)
-                    put_bf16(bst, sw128_off(kStkOff[s2] + r, c, 160), kv * __expf(rho[s2] - G[r]));
-                const float eg = __expf(G[r]);
-                put_bf16(buf + kOffZ, o64, kv * eg);                     // Gam*K for W = M(Gam*K)
-                put_bf16(pkg + kPkgQB, o64, qv * eg);                    // Gam*Q
-                put_bf16(pkg + kPkgKT, o64, kv * __expf(Glast - G[r]));  // K*gamma^C/Gam
-            }
-            reinterpret_cast<float*>(pkg + kPkgG)[c] = __expf(Glast);
+            for (int s2 = s + 1; s2 < 4; ++s2)
+                put_bf16(sm + kBStk, sw128_off(kStkOff[s2] + r, c, 160),
+                         kv * __expf(xrho[s2 * 128 + c] - G[rr]));
+            put_bf16(pkg + kPkgQB, o64, qv * e1 * xE[s * 128 + c]);  // Gam*Q
+            put_bf16(pkg + kPkgKT, o64, kv * dc * xF[s * 128 + c]);  // K*gamma^C/Gam
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
 
-        // ---- both Grams: D[128 x 160] = [Q'; beta K'] (128 x 128) * Bstack^T (128 x 160)
+        // ---- Grams: D = [Q'; beta K']_hi Bstack_hi^T (+ diagonal-column lo terms),
+        //      D_lo = Q'_lo Bstack_hi^T (its k-side lanes are unused)
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16(128, 160, false, false);
+            constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
+            constexpr uint32_t id16 = idesc_bf16(128, 16, false, false);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a =
-                    sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + (ks & 3) * 32, 0, 1024);
-                const uint64_t bd =
-                    sdesc_sw128(sbase + kBStk + (ks >> 2) * 20480 + (ks & 3) * 32, 0, 1024);
-                mma_bf16(tmem, a, bd, idesc, ks > 0);
+                const uint32_t kofs = (ks & 3) * 32;
+                const uint64_t ah = sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + kofs, 0, 1024);
+                const uint64_t bh = sdesc_sw128(sbase + kBStk + (ks >> 2) * 20480 + kofs, 0, 1024);
+                mma_bf16(tmem, ah, bh, id160, ks > 0);
+                const uint64_t al = sdesc_sw128(sbase + kALo + (ks >> 2) * 8192 + kofs, 0, 1024);
+                mma_bf16(tmem + kTLo, al, bh, id160, ks > 0);
+            }
+#pragma unroll
+            for (int sv = 0; sv < 4; ++sv) {
+                const uint32_t dcol = kStkOff[sv] + 16 * sv;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kofs = (ks & 3) * 32;
+                    const uint64_t ah = sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + kofs, 0, 1024);
+                    const uint64_t bl =
+                        sdesc_sw128(sbase + kBLo + sv * 2048 + (ks >> 2) * 8192 + kofs, 0, 1024);
+                    mma_bf16(tmem + dcol, ah, bl, id16, 1);
+                }
             }
             mma_commit(mma_bar);
         }
@@ -300,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         ++mma_phase;
         tc_fence_after();
 
-        // ---- Gram epilogue: q-side rows -> A tile (bf16), k-side rows -> L (fp32)
+        // ---- Gram epilogue (warps 0-3): q-side rows -> A tile (bf16), k-side rows -> L (fp32)
         if (warp < 4) {
             const int m = tid;  // TMEM lane
             const int side = m >> 6, r = m & 63, s = r >> 4;
@@ -308,8 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             uint8_t* aq = sm + kAqkTile;
 #pragma unroll
             for (int g = 0; g < 10; ++g) {
-                float v[16];
+                float v[16], vl[16];
                 tmem_ld16(tmem + lane_base + 16 * g, v);
+                tmem_ld16(tmem + lane_base + kTLo + 16 * g, vl);
                 tmem_ld_wait();
                 const int sg = (g == 0) ? 0 : (g < 3) ? 1 : (g < 6) ? 2 : 3;
                 const int ib = 16 * g - kStkOff[sg];
@@ -320,9 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                             uint32_t pw[4];
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const int i0 = ib + 8 * hf + 2 * e;
-                                pw[e] = pack_bf16x2(i0 <= r ? v[8 * hf + 2 * e] : 0.f,
-                                                    i0 + 1 <= r ? v[8 * hf + 2 * e + 1] : 0.f);
+                                const int j0 = 8 * hf + 2 * e, i0 = ib + j0;
+                                pw[e] = pack_bf16x2(i0 <= r ? v[j0] + vl[j0] : 0.f,
+                                                    i0 + 1 <= r ? v[j0 + 1] + vl[j0 + 1] : 0.f);
                             }
                             *reinterpret_cast<uint4*>(aq + sw128_chunk(r, (ib >> 3) + hf)) =
                                 make_uint4(pw[0], pw[1], pw[2], pw[3]);
@@ -337,6 +438,15 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             if (side == 0)  // columns past this sub-tile's version are zero
                 for (int ch = 2 * (s + 1); ch < 8; ++ch)
                     *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
+        }
+        // Gam*K for W = M (Gam*K), as A = (Gam K)^T MN-major, into the A-lo region
+#pragma unroll
+        for (int rr = 0; rr < 32; ++rr) {
+            const int r = r0 + rr, s = r >> 4;
+            const uint32_t o64 = sw128_off(r, c, 64);
+            const float kv = (r < it.L) ? bf16_at(buf + kOffK, o64) : 0.f;
+            put_bf16(sm + kKbar, o64,
+                     kv * __expf(G[rr] - xrho[s * 128 + c]) * xE[s * 128 + c]);
         }
         tc_fence_before();
         __syncthreads();
@@ -419,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t bm = sdesc_sw128(sbase + kMTile + ks * 32, 0, 1024);
-                mma_bf16(tmem, sdesc_sw128(ab + kOffZ + ks * 2048, 8192, 1024), bm, idesc, ks > 0);
+                mma_bf16(tmem, sdesc_sw128(sbase + kKbar + ks * 2048, 8192, 1024), bm, idesc, ks > 0);
                 mma_bf16(tmem + 64, sdesc_sw128(ab + kOffV + ks * 2048, 8192, 1024), bm, idesc,
                          ks > 0);
             }
@@ -429,21 +539,24 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         ++mma_phase;
         tc_fence_after();
         {
-            // warps 0-3: W (lane = channel c) into the q slot; warps 4-7: U (lane = j) into k slot
+            // warps 0-3: lane = channel c, row c of the W^T tile (q slot);
+            // warps 4-7: lane = value column j, row j of the U^T tile (k slot).
+            // Both tiles: [128 rows][64 r] bf16, 128-byte swizzle.
             const int m = 32 * (warp & 3) + lane;
             const uint32_t col0 = (warp < 4) ? 0 : 64;
+            uint8_t* dst = buf + ((warp < 4) ? kOffQ : kOffK);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float v[16];
                 tmem_ld16(tmem + lane_base + col0 + 16 * g, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r = 16 * g + e;
-                    if (warp < 4)
-                        put_bf16(buf + kOffQ, sw128_off(r, m, 64), v[e]);
-                    else
-                        put_bf16(buf + kOffK, (uint32_t)(r * 256 + 2 * m), v[e]);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint4 pk = make_uint4(pack_bf16x2(v[8 * hf], v[8 * hf + 1]),
+                                                pack_bf16x2(v[8 * hf + 2], v[8 * hf + 3]),
+                                                pack_bf16x2(v[8 * hf + 4], v[8 * hf + 5]),
+                                                pack_bf16x2(v[8 * hf + 6], v[8 * hf + 7]));
+                    *reinterpret_cast<uint4*>(dst + sw128_chunk(m, 2 * g + hf)) = pk;
                 }
             }
         }
@@ -461,13 +574,17 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     // teardown: stores complete, no load in flight, TMEM released
     if (tid == 0) {
         bulk_wait0();
-        if (s_abort && pending >= 0) mbar_wait(&tma_bar[pending], (iter >> 1) & 1, nullptr);
+        if (s_abort) {
+            for (int q = 0; q < 2; ++q)
+                if (pend_q[q] >= 0) mbar_wait(&qkv_bar[q], pend_q[q], nullptr);
+            if (pend_z >= 0) mbar_wait(z_bar, pend_z, nullptr);
+        }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -579,11 +696,12 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
+            constexpr uint32_t idesc_w = idesc_bf16(128, 64, true, true);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
-                const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
-                mma_bf16(tmem, a, sdesc_sw128(sstage + kPkgW + kb, 0, 1024), idesc, ks > 0);
+                mma_bf16(tmem, a, sdesc_sw128(sstage + kPkgW + ks * 2048, 8192, 1024), idesc_w,
+                         ks > 0);
             }
             mma_commit(mma1);
 #pragma unroll
@@ -599,7 +717,6 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
 
         // Vt = U - X: thread owns value column j = m and rows r in [32 wg, 32 wg + 32)
         {
-            const __nv_bfloat16* U = reinterpret_cast<const __nv_bfloat16*>(stage + kPkgU);
 #pragma unroll
             for (int hx = 0; hx < 2; ++hx) {
                 float x[16];
@@ -607,13 +724,15 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
                 tmem_ld_wait();
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
+                    const uint4 u4 = *reinterpret_cast<const uint4*>(
+                        stage + kPkgU + sw128_chunk(m, 4 * wg + 2 * hx + cc));
+                    const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
                     uint32_t pw[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int r = 32 * wg + 16 * hx + 8 * cc + 2 * e;
-                        const float u0 = __bfloat162float(U[r * kD + m]);
-                        const float u1 = __bfloat162float(U[(r + 1) * kD + m]);
-                        pw[e] = pack_bf16x2(u0 - x[8 * cc + 2 * e], u1 - x[8 * cc + 2 * e + 1]);
+                        const float2 u = __bfloat1622float2(
+                            *reinterpret_cast<const __nv_bfloat162*>(&uw[e]));
+                        pw[e] = pack_bf16x2(u.x - x[8 * cc + 2 * e], u.y - x[8 * cc + 2 * e + 1]);
                     }
                     *reinterpret_cast<uint4*>(sm + kVt + sw128_chunk(m, 4 * wg + 2 * hx + cc)) =
                         make_uint4(pw[0], pw[1], pw[2], pw[3]);
