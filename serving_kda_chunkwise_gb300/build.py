@@ -50,8 +50,8 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def _compile(src: str, verbose: bool, extra) -> str:
-    obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, verbose: bool, extra, out_dir: str) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-I", INCLUDE, "-I", CSRC, "-c", src,
                                                          "-o", obj]
     if verbose:
@@ -64,23 +64,30 @@ def _compile(src: str, verbose: bool, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libkda.so; return its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir=None) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libkda.so; return its path.
+
+    ``extra_flags`` (e.g. -DKDA_PHASE_TIMING) require ``out_dir``: such variant builds never
+    replace the library in _build/."""
+    if extra_flags and not out_dir:
+        raise ValueError("variant builds need their own out_dir")
+    out_dir = out_dir or OUT_DIR
+    lib_path = os.path.join(out_dir, "libkda.so")
     if not force and not extra_flags and up_to_date():
         return LIB_PATH
-    os.makedirs(OUT_DIR, exist_ok=True)
+    os.makedirs(out_dir, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose, extra_flags), srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose, extra_flags, out_dir), srcs))
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     if verbose:
         print(" ".join(cmd), flush=True)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link of libkda.so failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -58,6 +58,28 @@ constexpr uint32_t kPkgBytes = 74240;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Optional phase timers (debug builds with -DKDA_PHASE_TIMING only): thread 0 of CTA 0
+// accumulates clock64() deltas between marked points of each kernel's loop.
+#ifdef KDA_PHASE_TIMING
+__device__ unsigned long long g_phase[32];
+#define KDA_PHASE_INIT() long long kda_t_last = clock64()
+#define KDA_PHASE(i)                                                 \
+    do {                                                             \
+        if (blockIdx.x == 0 && threadIdx.x == 0) {                   \
+            const long long kda_t = clock64();                       \
+            g_phase[(i)] += (unsigned long long)(kda_t - kda_t_last); \
+            kda_t_last = kda_t;                                      \
+        }                                                            \
+    } while (0)
+#else
+#define KDA_PHASE_INIT() \
+    do {                 \
+    } while (0)
+#define KDA_PHASE(i) \
+    do {             \
+    } while (0)
+#endif
+
 // ================================================================= plan ====
 
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int N,
@@ -163,11 +185,12 @@ __device__ __forceinline__ void put_bf16(uint8_t* tile, uint32_t off, float v) {
     *reinterpret_cast<__nv_bfloat16*>(tile + off) = __float2bfloat16_rn(v);
 }
 // v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): twice bf16's significand.
-__device__ __forceinline__ void put_hilo(uint8_t* hi_tile, uint8_t* lo_tile, uint32_t off,
-                                         float v) {
+__device__ __forceinline__ void put_hilo(uint8_t* hi_tile, uint32_t hi_off, uint8_t* lo_tile,
+                                         uint32_t lo_off, float v) {
     const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    *reinterpret_cast<__nv_bfloat16*>(hi_tile + off) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(lo_tile + off) = __float2bfloat16_rn(v - __bfloat162float(hi));
+    *reinterpret_cast<__nv_bfloat16*>(hi_tile + hi_off) = hi;
+    *reinterpret_cast<__nv_bfloat16*>(lo_tile + lo_off) =
+        __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
 struct ItemInfo {
@@ -264,7 +287,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     }
 
     int iter = 0;
+    KDA_PHASE_INIT();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
+        KDA_PHASE(7);
         const int b = iter & 1;
         uint8_t* buf = sm + b * kInBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
@@ -290,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         } else {
             s_abort = 1;
         }
+        KDA_PHASE(0);
         float G[32];
         {
             const float scale = expf(__ldg(p.A_log + it.h));
@@ -334,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             s_abort = 1;
         }
         __syncthreads();
+        KDA_PHASE(1);
         if (s_abort) break;
 
         // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
@@ -348,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             const float rho = xrho[s * 128 + c];
             const float e1 = __expf(G[rr] - rho);
             const float dc = __expf(rho - G[rr]);
-            put_hilo(sm + kAStk, sm + kALo, sw128_off(r, c, 128), qv * e1);
+            put_hilo(sm + kAStk, sw128_off(r, c, 128), sm + kALo, o64, qv * e1);
             put_bf16(sm + kAStk, sw128_off(64 + r, c, 128), sBeta[r] * kv * e1);
             {
                 const float v = kv * dc;
@@ -366,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(2);
 
         // ---- Grams: D = [Q'; beta K']_hi Bstack_hi^T (+ diagonal-column lo terms),
         //      D_lo = Q'_lo Bstack_hi^T (its k-side lanes are unused)
@@ -399,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
+        KDA_PHASE(3);
 
         // ---- Gram epilogue (warps 0-3): q-side rows -> A tile (bf16), k-side rows -> L (fp32)
         if (warp < 4) {
@@ -450,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         }
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(4);
         if (s_abort) break;
 
         // ---- T = (I + L)^{-1}: 16x16 diagonal blocks by forward substitution, then the
@@ -520,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(5);
 
         // ---- W^T = (Gam K)^T M^T  and  U^T = V^T M^T  (M = 128 channels, N = 64 rows)
         if (tid == 0) {
@@ -563,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(6);
         if (s_abort) break;
         if (tid == 0) {
             bulk_s2g(pkg + kPkgW, buf + kOffQ, 16384);
@@ -677,6 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
 
     int issued = (nch > 0) ? 1 : 0;  // packages requested so far (thread 0)
     int t = 0;
+    KDA_PHASE_INIT();
     for (; t < nch; ++t) {
         const int st = t & 1;
         const uint8_t* stage = sm + st * kStage;
@@ -691,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
             issued = t + 2;
         }
         if (!mbar_wait(&full[st], (t >> 1) & 1, p.err)) s_abort = 1;
+        KDA_PHASE(16);
 
         // X^T = S^T W^T (cols 0..63), (Gam Q S)^T = S^T (Gam Q)^T (cols 64..127)
         if (tid == 0) {
@@ -714,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         }
         if (!mbar_wait(mma1, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
+        KDA_PHASE(17);
 
         // Vt = U - X: thread owns value column j = m and rows r in [32 wg, 32 wg + 32)
         {
@@ -742,6 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(18);
         if (s_abort) break;
 
         // dS = K~^T Vt (cols 128..255);  O^T += Vt^T A^T (cols 64..127)
@@ -761,6 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         }
         if (!mbar_wait(mma2, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
+        KDA_PHASE(19);
 
         // S <- gamma^C * S + dS ;  bf16 copy for the next chunk's MMAs
         {
@@ -793,6 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        KDA_PHASE(20);
         if (s_abort) break;
     }
     if (p.S_out && !s_abort) {
@@ -842,6 +880,15 @@ bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
 }
 
 }  // namespace
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
+    if (n > 32) n = 32;
+    if (cudaMemcpyFromSymbol(out, g_phase, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+    static const unsigned long long zeros[32] = {};
+    return cudaMemcpyToSymbol(g_phase, zeros, sizeof zeros) == cudaSuccess ? n : -1;
+}
+#endif
 
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H) {
     const int64_t maxchunks = T_total / kC + N;

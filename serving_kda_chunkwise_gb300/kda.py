@@ -12,7 +12,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+# KDA_LIBRARY may name another build of the same library (e.g. an instrumented one).
+LIB_PATH = os.environ.get("KDA_LIBRARY") or os.path.join(_HERE, "_build", "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
     KDA_ERR_DEVICE = range(6)
