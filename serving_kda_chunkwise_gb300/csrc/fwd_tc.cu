@@ -150,26 +150,28 @@ struct IntraParams {
     int N, H, maxchunks;
 };
 
-// Shared-memory map of the intra kernel (offsets from a 1024-aligned base).  The q, k, v
-// tiles are double buffered (next item prefetched by TMA); z has one buffer, refilled for
-// the next item as soon as the gate of the current one has been evaluated.
-constexpr uint32_t kInBuf = 49152;           // per input buffer: q, k, v (16 KB each)
-constexpr uint32_t kOffQ = 0, kOffK = 16384, kOffV = 32768;
-constexpr uint32_t kAStk = 2 * kInBuf;       //  98304: A hi [2 blk][128 rows][128 B]
-constexpr uint32_t kALo = kAStk + 32768;     // 131072: q-side A lo [2 blk][64 rows][128 B]
-constexpr uint32_t kBStk = kALo + 16384;     // 147456: B hi [2 blk][160 rows][128 B]
-constexpr uint32_t kBLo = kBStk + 40960;     // 188416: diagonal-column lo [2 blk][64][128 B]
-constexpr uint32_t kZBuf = kBLo + 16384;     // 204800: z [2 blk][64 rows][128 B]
-constexpr uint32_t kXch = kZBuf + 16384;     // 221184: exchange (fp32): tot[128], rho[4][128],
-                                             //         E[4][128] = e^rho, F[4][128] = e^{Glast-rho}
-constexpr uint32_t kBeta = kXch + 13 * 512;  // 227840: beta [2][64] fp32
-constexpr uint32_t kBars = kBeta + 512;      // mbarriers
+// Shared-memory map of the intra kernel (offsets from a 1024-aligned base).  q and k are
+// double buffered (the next item's are fetched by TMA once this item's operands are built);
+// v and z have one buffer each, refilled as soon as the current item has consumed them.
+constexpr uint32_t kQKBuf = 32768;            // per q/k buffer: q, k (16 KB each)
+constexpr uint32_t kOffQ = 0, kOffK = 16384;
+constexpr uint32_t kVBuf = 2 * kQKBuf;        //  65536: v   [2 blk][64 rows][128 B]
+constexpr uint32_t kZBuf = kVBuf + 16384;     //  81920: z
+constexpr uint32_t kKbar = kZBuf + 16384;     //  98304: Gam*K (A of W = M Gam K, MN-major);
+                                              //         earlier: cumsum block totals fp32[16][128]
+constexpr uint32_t kAStk = kKbar + 16384;     // 114688: A hi [2 blk][128 rows][128 B]
+constexpr uint32_t kALo = kAStk + 32768;      // 147456: q-side A lo [2 blk][64 rows][128 B]
+constexpr uint32_t kBStk = kALo + 16384;      // 163840: B hi [2 blk][160 rows][128 B]
+constexpr uint32_t kBLo = kBStk + 40960;      // 204800: diagonal-column lo [2 blk][64][128 B]
+constexpr uint32_t kXch = kBLo + 16384;       // 221184: rho fp32[4][128], glast fp32[128]
+constexpr uint32_t kBeta = kXch + 2560;       // 223744: beta [2][64] fp32
+constexpr uint32_t kBars = kBeta + 512;       // 224256: mbarriers
 constexpr uint32_t kIntraSmem = kBars + 64 + 1024;  // + alignment slack
 static_assert(kIntraSmem <= 232448, "intra kernel exceeds the shared-memory limit");
-// reuse after the Gram MMAs: A hi -> A tile (8 KB) + M tile (8 KB); A lo -> Gam*K (16 KB);
-// B hi -> L, T, Y (fp32).  After the W/U MMAs the q / k slots stage W^T and U^T.
-constexpr uint32_t kAqkTile = kAStk, kMTile = kAStk + 8192, kKbar = kALo;
-constexpr int kLd = 65;                      // padded fp32 row stride of L and T
+// reuse after the Gram MMAs: A hi -> A tile (8 KB) + M tile (8 KB); B hi -> L, T, Y (fp32).
+// After the W/U MMAs the q / k slots of the current buffer stage W^T and U^T.
+constexpr uint32_t kAqkTile = kAStk, kMTile = kAStk + 8192;
+constexpr int kLd = 65;                       // padded fp32 row stride of L and T
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4, kSY = kST + 64 * kLd * 4;
 static_assert(kSY + 3 * 256 * 4 <= kBStk + 40960, "solve scratch must fit the B stack");
 // TMEM columns: main Gram accumulator [0, 160), q-side lo correction [256, 416);
@@ -177,21 +179,6 @@ static_assert(kSY + 3 * 256 * 4 <= kBStk + 40960, "solve scratch must fit the B 
 constexpr uint32_t kTmemCols = 512, kTLo = 256;
 
 __device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
-
-__device__ __forceinline__ float bf16_at(const uint8_t* tile, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + off));
-}
-__device__ __forceinline__ void put_bf16(uint8_t* tile, uint32_t off, float v) {
-    *reinterpret_cast<__nv_bfloat16*>(tile + off) = __float2bfloat16_rn(v);
-}
-// v = hi + lo with hi = bf16(v) and lo = bf16(v - hi): twice bf16's significand.
-__device__ __forceinline__ void put_hilo(uint8_t* hi_tile, uint32_t hi_off, uint8_t* lo_tile,
-                                         uint32_t lo_off, float v) {
-    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-    *reinterpret_cast<__nv_bfloat16*>(hi_tile + hi_off) = hi;
-    *reinterpret_cast<__nv_bfloat16*>(lo_tile + lo_off) =
-        __float2bfloat16_rn(v - __bfloat162float(hi));
-}
 
 struct ItemInfo {
     int h, n, L;
@@ -213,24 +200,17 @@ __device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item) 
     return it;
 }
 
-__device__ __forceinline__ void issue_qkv(const IntraParams& p, const ItemInfo& it, uint8_t* buf,
-                                          uint64_t* bar) {
-    mbar_expect_tx(bar, kInBuf);
-    const int t0 = (int)it.t0;
+// TMA: [64 rows][128] bf16 tiles of one or two tensors for this item (two 64-column
+// blocks each), completing on `bar`.
+__device__ __forceinline__ void load_tiles(const CUtensorMap* m0, uint8_t* d0,
+                                           const CUtensorMap* m1, uint8_t* d1,
+                                           const ItemInfo& it, uint64_t* bar) {
+    mbar_expect_tx(bar, m1 ? 32768 : 16384);
 #pragma unroll
     for (int cb = 0; cb < 2; ++cb) {
-        tma_load_3d(buf + kOffQ + cb * 8192, &p.tq, cb * 64, it.h, t0, bar);
-        tma_load_3d(buf + kOffK + cb * 8192, &p.tk, cb * 64, it.h, t0, bar);
-        tma_load_3d(buf + kOffV + cb * 8192, &p.tv, cb * 64, it.h, t0, bar);
+        tma_load_3d(d0 + cb * 8192, m0, cb * 64, it.h, (int)it.t0, bar);
+        if (m1) tma_load_3d(d1 + cb * 8192, m1, cb * 64, it.h, (int)it.t0, bar);
     }
-}
-
-__device__ __forceinline__ void issue_z(const IntraParams& p, const ItemInfo& it, uint8_t* zbuf,
-                                        uint64_t* bar) {
-    mbar_expect_tx(bar, 16384);
-#pragma unroll
-    for (int cb = 0; cb < 2; ++cb)
-        tma_load_3d(zbuf + cb * 8192, &p.tz, cb * 64, it.h, (int)it.t0, bar);
 }
 
 __device__ __forceinline__ void load_beta(const IntraParams& p, const ItemInfo& it, float* dst,
@@ -239,26 +219,57 @@ __device__ __forceinline__ void load_beta(const IntraParams& p, const ItemInfo& 
         dst[tid] = (tid < it.L) ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
 }
 
+// 8 consecutive bf16 of a swizzled tile <-> fp32 registers
+__device__ __forceinline__ void ld8(const uint8_t* p, float (&v)[8]) {
+    const uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        v[2 * e] = f.x;
+        v[2 * e + 1] = f.y;
+    }
+}
+__device__ __forceinline__ uint4 pk8(const float (&v)[8]) {
+    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                      pack_bf16x2(v[6], v[7]));
+}
+// hi = bf16(v), lo = bf16(v - hi)
+__device__ __forceinline__ void pk8_hilo(const float (&v)[8], uint4& hi, uint4& lo) {
+    float h[8], l[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        h[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+        l[e] = v[e] - h[e];
+    }
+    hi = pk8(h);
+    lo = pk8(l);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    float* xtot = reinterpret_cast<float*>(sm + kXch);  // [128]
-    float* xrho = xtot + 128;                           // [4][128]
-    float* xE = xrho + 512;                             // [4][128]
-    float* xF = xE + 512;                               // [4][128]
-    uint64_t* qkv_bar = reinterpret_cast<uint64_t*>(sm + kBars);  // [2]
-    uint64_t* z_bar = qkv_bar + 2;
-    uint64_t* mma_bar = qkv_bar + 3;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qkv_bar + 4);
+    float* tot = reinterpret_cast<float*>(sm + kKbar);   // [16][128] cumsum block totals
+    float* xrho = reinterpret_cast<float*>(sm + kXch);   // [4][128]
+    float* xgl = xrho + 512;                             // [128]
+    uint64_t* qk_bar = reinterpret_cast<uint64_t*>(sm + kBars);  // [2]
+    uint64_t* v_bar = qk_bar + 2;
+    uint64_t* z_bar = qk_bar + 3;
+    uint64_t* mma_bar = qk_bar + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qk_bar + 5);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = tid & 127, half = tid >> 7, r0 = 32 * half;  // operand pass: channel, rows
+    // operand passes: 8 channels [8 cg, 8 cg + 8) of rows [4 rg, 4 rg + 4)
+    const int cg = tid & 15, rg = tid >> 4, sub = rg >> 2;
+    const uint32_t cofs = (cg >> 3) * 8192;  // 64-column block of the channel group
+    const int ch0 = 8 * cg;
     if (tid == 0) {
-        mbar_init(&qkv_bar[0], 1);
-        mbar_init(&qkv_bar[1], 1);
+        mbar_init(&qk_bar[0], 1);
+        mbar_init(&qk_bar[1], 1);
+        mbar_init(v_bar, 1);
         mbar_init(z_bar, 1);
         mbar_init(mma_bar, 1);
         fence_mbar_init();
@@ -274,16 +285,19 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
     // parity of the phase a load in flight will complete, or -1 (thread 0; for a clean abort)
-    int pend_q[2] = {-1, -1}, pend_z = -1;
+    int pend_q[2] = {-1, -1}, pend_v = -1, pend_z = -1;
+    ItemInfo nx;
     if ((int)blockIdx.x < n_items) {
-        const ItemInfo first = decode_item(p, blockIdx.x);
+        nx = decode_item(p, blockIdx.x);
         if (tid == 0) {
-            issue_qkv(p, first, sm, &qkv_bar[0]);
-            issue_z(p, first, sm + kZBuf, z_bar);
+            load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, nx, &qk_bar[0]);
+            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
+            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
             pend_q[0] = 0;
+            pend_v = 0;
             pend_z = 0;
         }
-        load_beta(p, first, reinterpret_cast<float*>(sm + kBeta), tid);
+        load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta), tid);
     }
 
     int iter = 0;
@@ -291,70 +305,73 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
         KDA_PHASE(7);
         const int b = iter & 1;
-        uint8_t* buf = sm + b * kInBuf;
+        uint8_t* qk = sm + b * kQKBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
-        const ItemInfo it = decode_item(p, item);
+        const ItemInfo it = nx;
         const int next = item + gridDim.x;
         const bool has_next = next < n_items;
-        ItemInfo nx;
-        if (has_next) nx = decode_item(p, next);
-        if (tid == 0) {
-            bulk_wait_read0();  // previous item's package stores have read their smem
-            if (has_next) {
-                fence_async_smem();
-                issue_qkv(p, nx, sm + (b ^ 1) * kInBuf, &qkv_bar[b ^ 1]);
-                pend_q[b ^ 1] = ((iter + 1) >> 1) & 1;
-            }
-        }
-        if (has_next) load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1), tid);
+        if (has_next) nx = decode_item(p, next);  // used only later: its latency overlaps
         uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
 
-        // ---- gate and in-chunk cumsum: channel c, rows [r0, r0 + 32)
+        // the previous item's package stores read the A stack and the other q/k buffer
+        if (tid == 0) bulk_wait_read0();
+
+        // ---- gate and in-chunk cumsum (two-level scan over 16 row groups of 4 rows)
         if (mbar_wait(z_bar, iter & 1, p.err)) {
             if (tid == 0) pend_z = -1;
         } else {
             s_abort = 1;
         }
         KDA_PHASE(0);
-        float G[32];
+        float G[4][8];
         {
             const float scale = expf(__ldg(p.A_log + it.h));
-            float acc = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = r0 + rr;
-                const float zz = bf16_at(sm + kZBuf, sw128_off(r, c, 64));
-                acc += (r < it.L) ? p.g_min / (1.f + __expf(-scale * zz)) : 0.f;
-                G[rr] = acc;
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * rg + i;
+                float zz[8];
+                ld8(sm + kZBuf + cofs + sw128_chunk(r, cg & 7), zz);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    acc[e] += (r < it.L) ? p.g_min / (1.f + __expf(-scale * zz[e])) : 0.f;
+                    G[i][e] = acc[e];
+                }
             }
-            if (half == 0) xtot[c] = acc;
-        }
-        __syncthreads();
-        if (half == 1) {
-            const float off = xtot[c];
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) G[rr] += off;
+            for (int e = 0; e < 8; ++e) tot[rg * 128 + ch0 + e] = acc[e];
         }
-        xrho[(2 * half) * 128 + c] = G[7];       // rho of sub-tile 2*half
-        xrho[(2 * half + 1) * 128 + c] = G[23];  // rho of sub-tile 2*half + 1
-        if (half == 1) xtot[c] = G[31];          // G of the chunk's last row
         __syncthreads();
-        if (tid == 0 && has_next && pend_z < 0) {  // z is consumed: fetch the next item's
-            issue_z(p, nx, sm + kZBuf, z_bar);
+        if (tid == 0 && has_next) {  // z is consumed: fetch the next item's
+            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
             pend_z = (iter + 1) & 1;
         }
-        {
-            const float glast = xtot[c];
+        if (has_next) load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1), tid);
+        if (tid < kD) {  // exclusive scan of the block totals, one channel per thread
+            float a = 0.f;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int s = 2 * half + q;
-                const float rho = xrho[s * 128 + c];
-                xE[s * 128 + c] = __expf(rho);
-                xF[s * 128 + c] = __expf(glast - rho);
+            for (int g = 0; g < 16; ++g) {
+                const float v = tot[g * 128 + tid];
+                tot[g * 128 + tid] = a;
+                a += v;
             }
-            if (half == 1) reinterpret_cast<float*>(pkg + kPkgG)[c] = __expf(glast);
+            xgl[tid] = a;  // G of the chunk's last row
         }
-        if (mbar_wait(&qkv_bar[b], (iter >> 1) & 1, p.err)) {
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float off = tot[rg * 128 + ch0 + e];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) G[i][e] += off;
+        }
+        if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
+        if (rg == 15)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = __expf(xgl[ch0 + e]);
+        if (mbar_wait(&qk_bar[b], (iter >> 1) & 1, p.err)) {
             if (tid == 0) pend_q[b] = -1;
         } else {
             s_abort = 1;
@@ -365,35 +382,75 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 
         // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
         //      column operand of version s2 >= s is k_r e^{rho_s2 - G_r}.
+        {
+            float rho[8], Es[8], Fs[8];
 #pragma unroll
-        for (int rr = 0; rr < 32; ++rr) {
-            const int r = r0 + rr, s = r >> 4;
-            const bool ok = r < it.L;
-            const uint32_t o64 = sw128_off(r, c, 64);
-            const float qv = ok ? bf16_at(buf + kOffQ, o64) : 0.f;
-            const float kv = ok ? bf16_at(buf + kOffK, o64) : 0.f;
-            const float rho = xrho[s * 128 + c];
-            const float e1 = __expf(G[rr] - rho);
-            const float dc = __expf(rho - G[rr]);
-            put_hilo(sm + kAStk, sw128_off(r, c, 128), sm + kALo, o64, qv * e1);
-            put_bf16(sm + kAStk, sw128_off(64 + r, c, 128), sBeta[r] * kv * e1);
-            {
-                const float v = kv * dc;
-                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-                *reinterpret_cast<__nv_bfloat16*>(sm + kBStk + sw128_off(kStkOff[s] + r, c, 160)) = hi;
-                *reinterpret_cast<__nv_bfloat16*>(sm + kBLo + o64) =
-                    __float2bfloat16_rn(v - __bfloat162float(hi));
+            for (int e = 0; e < 8; ++e) {
+                rho[e] = xrho[sub * 128 + ch0 + e];
+                Es[e] = __expf(rho[e]);                      // e^{rho_s}
+                Fs[e] = __expf(xgl[ch0 + e] - rho[e]);       // e^{G_last - rho_s}
             }
-            for (int s2 = s + 1; s2 < 4; ++s2)
-                put_bf16(sm + kBStk, sw128_off(kStkOff[s2] + r, c, 160),
-                         kv * __expf(xrho[s2 * 128 + c] - G[rr]));
-            put_bf16(pkg + kPkgQB, o64, qv * e1 * xE[s * 128 + c]);  // Gam*Q
-            put_bf16(pkg + kPkgKT, o64, kv * dc * xF[s * 128 + c]);  // K*gamma^C/Gam
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = 4 * rg + i;
+                const bool ok = r < it.L;
+                const uint32_t o64 = cofs + sw128_chunk(r, cg & 7);
+                const uint32_t o128 = (cg >> 3) * 16384 + sw128_chunk(r, cg & 7);
+                float qv[8], kv[8], e1[8], dc[8], t[8];
+                ld8(qk + kOffQ + o64, qv);
+                ld8(qk + kOffK + o64, kv);
+                const float br = sBeta[r];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (!ok) { qv[e] = 0.f; kv[e] = 0.f; }
+                    e1[e] = __expf(G[i][e] - rho[e]);
+                    dc[e] = __expf(rho[e] - G[i][e]);
+                }
+                uint4 hi, lo;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = qv[e] * e1[e];
+                pk8_hilo(t, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kAStk + o128) = hi;
+                *reinterpret_cast<uint4*>(sm + kALo + o64) = lo;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = br * kv[e] * e1[e];
+                *reinterpret_cast<uint4*>(sm + kAStk + o128 + 64 * 128) = pk8(t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e];
+                pk8_hilo(t, hi, lo);
+                *reinterpret_cast<uint4*>(
+                    sm + kBStk + (cg >> 3) * 20480 + sw128_chunk(kStkOff[sub] + r, cg & 7)) = hi;
+                *reinterpret_cast<uint4*>(sm + kBLo + o64) = lo;
+                for (int s2 = sub + 1; s2 < 4; ++s2) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        t[e] = kv[e] * __expf(xrho[s2 * 128 + ch0 + e] - G[i][e]);
+                    *reinterpret_cast<uint4*>(sm + kBStk + (cg >> 3) * 20480 +
+                                              sw128_chunk(kStkOff[s2] + r, cg & 7)) = pk8(t);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = qv[e] * e1[e] * Es[e];
+                *reinterpret_cast<uint4*>(pkg + kPkgQB + o64) = pk8(t);       // Gam*Q
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e] * Fs[e];
+                *reinterpret_cast<uint4*>(pkg + kPkgKT + o64) = pk8(t);       // K*gamma^C/Gam
+#pragma unroll
+                for (int e = 0; e < 8; ++e) t[e] = kv[e] * e1[e] * Es[e];
+                *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
+            }
         }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
         KDA_PHASE(2);
+        if (tid == 0) {
+            if (has_next) {
+                fence_async_smem();
+                load_tiles(&p.tq, sm + (b ^ 1) * kQKBuf + kOffQ, &p.tk,
+                           sm + (b ^ 1) * kQKBuf + kOffK, nx, &qk_bar[b ^ 1]);
+                pend_q[b ^ 1] = ((iter + 1) >> 1) & 1;
+            }
+        }
 
         // ---- Grams: D = [Q'; beta K']_hi Bstack_hi^T (+ diagonal-column lo terms),
         //      D_lo = Q'_lo Bstack_hi^T (its k-side lanes are unused)
@@ -468,15 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 for (int ch = 2 * (s + 1); ch < 8; ++ch)
                     *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
         }
-        // Gam*K for W = M (Gam*K), as A = (Gam K)^T MN-major, into the A-lo region
-#pragma unroll
-        for (int rr = 0; rr < 32; ++rr) {
-            const int r = r0 + rr, s = r >> 4;
-            const uint32_t o64 = sw128_off(r, c, 64);
-            const float kv = (r < it.L) ? bf16_at(buf + kOffK, o64) : 0.f;
-            put_bf16(sm + kKbar, o64,
-                     kv * __expf(G[rr] - xrho[s * 128 + c]) * xE[s * 128 + c]);
-        }
         tc_fence_before();
         __syncthreads();
         KDA_PHASE(4);
@@ -493,11 +541,16 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 float t[16];
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
-                    float a = (rr == j) ? 1.f : 0.f;
+                    float lrow[16];
 #pragma unroll
-                    for (int m = 0; m < rr; ++m)
-                        a = fmaf(-sL[(16 * s + rr) * kLd + 16 * s + m], t[m], a);
-                    t[rr] = a;
+                    for (int m = 0; m < rr; ++m) lrow[m] = sL[(16 * s + rr) * kLd + 16 * s + m];
+                    float a = (rr == j) ? 1.f : 0.f, a2 = 0.f;
+#pragma unroll
+                    for (int m = 0; m < rr; m += 2) {
+                        a = fmaf(-lrow[m], t[m], a);
+                        if (m + 1 < rr) a2 = fmaf(-lrow[m + 1], t[m + 1], a2);
+                    }
+                    t[rr] = a + a2;
                 }
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) sT[(16 * s + rr) * kLd + 16 * s + j] = t[rr];
@@ -507,23 +560,28 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 const int nb = 4 - d;
                 for (int e = tid; e < nb * 256; e += kThreads) {
                     const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + d;
-                    float y = 0.f;
+                    float y0 = 0.f, y1 = 0.f;
                     for (int t = sp; t < s; ++t)
 #pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            y = fmaf(sL[(16 * s + rr) * kLd + 16 * t + m],
-                                     sT[(16 * t + m) * kLd + 16 * sp + jj], y);
-                    sY[e] = y;
+                        for (int m = 0; m < 16; m += 2) {
+                            y0 = fmaf(sL[(16 * s + rr) * kLd + 16 * t + m],
+                                      sT[(16 * t + m) * kLd + 16 * sp + jj], y0);
+                            y1 = fmaf(sL[(16 * s + rr) * kLd + 16 * t + m + 1],
+                                      sT[(16 * t + m + 1) * kLd + 16 * sp + jj], y1);
+                        }
+                    sY[e] = y0 + y1;
                 }
                 __syncthreads();
                 for (int e = tid; e < nb * 256; e += kThreads) {
                     const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + d;
-                    float y = 0.f;
+                    float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-                    for (int m = 0; m < 16; ++m)
-                        y = fmaf(sT[(16 * s + rr) * kLd + 16 * s + m], sY[(sp << 8) + m * 16 + jj],
-                                 y);
-                    sT[(16 * s + rr) * kLd + 16 * sp + jj] = -y;
+                    for (int m = 0; m < 16; m += 2) {
+                        y0 = fmaf(sT[(16 * s + rr) * kLd + 16 * s + m], sY[(sp << 8) + m * 16 + jj], y0);
+                        y1 = fmaf(sT[(16 * s + rr) * kLd + 16 * s + m + 1],
+                                  sY[(sp << 8) + (m + 1) * 16 + jj], y1);
+                    }
+                    sT[(16 * s + rr) * kLd + 16 * sp + jj] = -(y0 + y1);
                 }
                 __syncthreads();
             }
@@ -553,15 +611,19 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         KDA_PHASE(5);
 
         // ---- W^T = (Gam K)^T M^T  and  U^T = V^T M^T  (M = 128 channels, N = 64 rows)
+        if (mbar_wait(v_bar, iter & 1, p.err)) {
+            if (tid == 0) pend_v = -1;
+        } else {
+            s_abort = 1;
+        }
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
-            const uint32_t ab = sbase + b * kInBuf;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t bm = sdesc_sw128(sbase + kMTile + ks * 32, 0, 1024);
                 mma_bf16(tmem, sdesc_sw128(sbase + kKbar + ks * 2048, 8192, 1024), bm, idesc, ks > 0);
-                mma_bf16(tmem + 64, sdesc_sw128(ab + kOffV + ks * 2048, 8192, 1024), bm, idesc,
+                mma_bf16(tmem + 64, sdesc_sw128(sbase + kVBuf + ks * 2048, 8192, 1024), bm, idesc,
                          ks > 0);
             }
             mma_commit(mma_bar);
@@ -569,13 +631,18 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
+        if (tid == 0 && has_next) {  // v is consumed: fetch the next item's
+            fence_async_smem();
+            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
+            pend_v = (iter + 1) & 1;
+        }
         {
             // warps 0-3: lane = channel c, row c of the W^T tile (q slot);
             // warps 4-7: lane = value column j, row j of the U^T tile (k slot).
             // Both tiles: [128 rows][64 r] bf16, 128-byte swizzle.
             const int m = 32 * (warp & 3) + lane;
             const uint32_t col0 = (warp < 4) ? 0 : 64;
-            uint8_t* dst = buf + ((warp < 4) ? kOffQ : kOffK);
+            uint8_t* dst = qk + ((warp < 4) ? kOffQ : kOffK);
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float v[16];
@@ -597,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         KDA_PHASE(6);
         if (s_abort) break;
         if (tid == 0) {
-            bulk_s2g(pkg + kPkgW, buf + kOffQ, 16384);
-            bulk_s2g(pkg + kPkgU, buf + kOffK, 16384);
+            bulk_s2g(pkg + kPkgW, qk + kOffQ, 16384);
+            bulk_s2g(pkg + kPkgU, qk + kOffK, 16384);
             bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 8192);
             bulk_commit();
         }
@@ -608,7 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         bulk_wait0();
         if (s_abort) {
             for (int q = 0; q < 2; ++q)
-                if (pend_q[q] >= 0) mbar_wait(&qkv_bar[q], pend_q[q], nullptr);
+                if (pend_q[q] >= 0) mbar_wait(&qk_bar[q], pend_q[q], nullptr);
+            if (pend_v >= 0) mbar_wait(v_bar, pend_v, nullptr);
             if (pend_z >= 0) mbar_wait(z_bar, pend_z, nullptr);
         }
     }

@@ -13,7 +13,8 @@ Tolerances (written here once, used by every parity test):
             exact result rounded once to bf16 already fails the absolute-only reading (see
             test_tolerance_reading.py).  The rms bound catches errors that are systematic
             across a head even when each element stays inside the band.
-            The fp32 final state: max |S_gpu - S_ref| / rms(S_ref) <= 2e-2.
+            The fp32 final state of a bf16 problem is held to the same two bounds
+            (normalised by rms(S_ref)).
 """
 from __future__ import annotations
 
@@ -123,8 +124,9 @@ def check_head(o_gpu, o_ref, S_gpu, S_ref, dtype, what=""):
     assert er <= BF16_RMS_TOL, f"{what}: normalised rms err {er:.3e} > {BF16_RMS_TOL}"
     es = 0.0
     if S_ref is not None:
-        rms_s = np.sqrt(np.mean(S_ref ** 2))
-        es = np.max(np.abs(S_gpu - S_ref)) / max(rms_s, 1e-30)
+        es = bf16_norm_err(np.asarray(S_gpu, np.float64), S_ref)
+        ers = bf16_rms_err(np.asarray(S_gpu, np.float64), S_ref)
+        assert ers <= BF16_RMS_TOL, f"{what}: normalised state rms err {ers:.3e}"
     assert eo <= BF16_NORM_TOL, f"{what}: normalised output err {eo:.3e} > {BF16_NORM_TOL}"
     assert es <= BF16_NORM_TOL, f"{what}: normalised state err {es:.3e} > {BF16_NORM_TOL}"
     return eo, es
