@@ -48,13 +48,21 @@ constexpr int kD = 128;   // head dim (dk = dv)
 constexpr int kThreads = 256;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
-constexpr uint32_t kPkgW = 0;        // W^T    [128 c][64 r] bf16 sw128: B = W^T MN-major
-constexpr uint32_t kPkgQB = 16384;   // Gam*Q  [64 r][128 c] bf16, K-major sw128
-constexpr uint32_t kPkgKT = 32768;   // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
-constexpr uint32_t kPkgAQK = 49152;  // A      [64 r][64 i] bf16, K-major sw128
-constexpr uint32_t kPkgU = 57344;    // U^T    [128 j][64 r] bf16 sw128
-constexpr uint32_t kPkgG = 73728;    // gamma^C [128] fp32
-constexpr uint32_t kPkgBytes = 74240;
+// part A (double buffered by the state kernel: needed at the start of a chunk)
+constexpr uint32_t kPkgW = 0;         // W^T    [128 c][64 r] bf16 sw128: B = W^T MN-major
+constexpr uint32_t kPkgQB = 16384;    // Gam*Q  [64 r][128 c] bf16, K-major sw128
+constexpr uint32_t kPkgPartA = 32768;
+// part B (single buffered: needed from the middle of a chunk on)
+constexpr uint32_t kPkgKT = 32768;    // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
+constexpr uint32_t kPkgAQK = 49152;   // A hi   [64 r][64 i] bf16, K-major sw128
+constexpr uint32_t kPkgAQKLo = 57344; // A lo   (A = hi + lo, bf16 each)
+constexpr uint32_t kPkgG = 65536;     // gamma^C [128] fp32
+constexpr uint32_t kPkgPartB = 66048 - 32768;
+// part C (single buffered)
+constexpr uint32_t kPkgU = 66048;     // U^T    [128 j][64 r] fp32, 16-byte chunk c of row j at
+                                      //        chunk position c ^ (j & 15)
+constexpr uint32_t kPkgUBytes = 32768;
+constexpr uint32_t kPkgBytes = kPkgU + kPkgUBytes;  // 98816
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -168,15 +176,17 @@ constexpr uint32_t kBeta = kXch + 2560;       // 223744: beta [2][64] fp32
 constexpr uint32_t kBars = kBeta + 512;       // 224256: mbarriers
 constexpr uint32_t kIntraSmem = kBars + 64 + 1024;  // + alignment slack
 static_assert(kIntraSmem <= 232448, "intra kernel exceeds the shared-memory limit");
-// reuse after the Gram MMAs: A hi -> A tile (8 KB) + M tile (8 KB); B hi -> L, T, Y (fp32).
+// reuse after the Gram MMAs: A hi -> A tile hi, lo (8 KB each) + M tile (8 KB);
+// B hi -> L, T, Y (fp32).
 // After the W/U MMAs the q / k slots of the current buffer stage W^T and U^T.
-constexpr uint32_t kAqkTile = kAStk, kMTile = kAStk + 8192;
+constexpr uint32_t kAqkTile = kAStk, kAqkLoTile = kAStk + 8192, kMTile = kAStk + 16384;
 constexpr int kLd = 65;                       // padded fp32 row stride of L and T
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4, kSY = kST + 64 * kLd * 4;
 static_assert(kSY + 3 * 256 * 4 <= kBStk + 40960, "solve scratch must fit the B stack");
-// TMEM columns: main Gram accumulator [0, 160), q-side lo correction [256, 416);
+// TMEM columns: main Gram accumulator [0, 160), diagonal-column lo correction [160, 224),
+// q-side lo correction [256, 416);
 // later W^T [0, 64) and U^T [64, 128).
-constexpr uint32_t kTmemCols = 512, kTLo = 256;
+constexpr uint32_t kTmemCols = 512, kTLo = 256, kTDiag = 160;
 
 __device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
 
@@ -246,6 +256,42 @@ __device__ __forceinline__ void pk8_hilo(const float (&v)[8], uint4& hi, uint4& 
     lo = pk8(l);
 }
 
+// Off-diagonal blocks at distance D of T = (I + L)^{-1} (16x16 blocks, fp32):
+//   Y_{s,s'} = sum_{t=s'}^{s-1} L_{s,t} T_{t,s'},   T_{s,s'} = -T_{s,s} Y_{s,s'},   s = s' + D.
+// Every thread computes whole dot products with its operands loaded ahead.
+template <int D>
+__device__ __forceinline__ void solve_round(const float* sL, float* sT, float* sY, int tid) {
+    constexpr int kNb = 4 - D;
+    for (int e = tid; e < kNb * 256; e += kThreads) {
+        const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + D;
+        float l[16 * D], t[16 * D];
+#pragma unroll
+        for (int m = 0; m < 16 * D; ++m) {
+            l[m] = sL[(16 * s + rr) * kLd + 16 * sp + m];
+            t[m] = sT[(16 * sp + m) * kLd + 16 * sp + jj];
+        }
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 16 * D; ++m) y[m & 3] = fmaf(l[m], t[m], y[m & 3]);
+        sY[e] = (y[0] + y[1]) + (y[2] + y[3]);
+    }
+    __syncthreads();
+    for (int e = tid; e < kNb * 256; e += kThreads) {
+        const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + D;
+        float l[16], y4[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            l[m] = sT[(16 * s + rr) * kLd + 16 * s + m];
+            y4[m] = sY[(sp << 8) + m * 16 + jj];
+        }
+        float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < 16; ++m) y[m & 3] = fmaf(l[m], y4[m], y[m & 3]);
+        sT[(16 * s + rr) * kLd + 16 * sp + jj] = -((y[0] + y[1]) + (y[2] + y[3]));
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -310,7 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         const ItemInfo it = nx;
         const int next = item + gridDim.x;
         const bool has_next = next < n_items;
-        if (has_next) nx = decode_item(p, next);  // used only later: its latency overlaps
+        float beta_next = 0.f;  // the next item's beta[tid]: loaded now, stored after the pass
+        if (has_next) {
+            nx = decode_item(p, next);  // used only later: its latency overlaps
+            if (tid < nx.L)
+                beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
+        }
         uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
 
         // the previous item's package stores read the A stack and the other q/k buffer
@@ -346,7 +397,6 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
             pend_z = (iter + 1) & 1;
         }
-        if (has_next) load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1), tid);
         if (tid < kD) {  // exclusive scan of the block totals, one channel per thread
             float a = 0.f;
 #pragma unroll
@@ -439,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
             }
         }
+        if (tid < kC) reinterpret_cast<float*>(sm + kBeta)[64 * (b ^ 1) + tid] = beta_next;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -457,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
-            constexpr uint32_t id16 = idesc_bf16(128, 16, false, false);
+            constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kofs = (ks & 3) * 32;
@@ -467,17 +518,13 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 const uint64_t al = sdesc_sw128(sbase + kALo + (ks >> 2) * 8192 + kofs, 0, 1024);
                 mma_bf16(tmem + kTLo, al, bh, id160, ks > 0);
             }
+            // diagonal-column lo parts of all four versions at once: D' = A_hi Blo^T
 #pragma unroll
-            for (int sv = 0; sv < 4; ++sv) {
-                const uint32_t dcol = kStkOff[sv] + 16 * sv;
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t kofs = (ks & 3) * 32;
-                    const uint64_t ah = sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + kofs, 0, 1024);
-                    const uint64_t bl =
-                        sdesc_sw128(sbase + kBLo + sv * 2048 + (ks >> 2) * 8192 + kofs, 0, 1024);
-                    mma_bf16(tmem + dcol, ah, bl, id16, 1);
-                }
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t kofs = (ks & 3) * 32;
+                const uint64_t ah = sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + kofs, 0, 1024);
+                const uint64_t bl = sdesc_sw128(sbase + kBLo + (ks >> 2) * 8192 + kofs, 0, 1024);
+                mma_bf16(tmem + kTDiag, ah, bl, id64, ks > 0);
             }
             mma_commit(mma_bar);
         }
@@ -494,25 +541,32 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             uint8_t* aq = sm + kAqkTile;
 #pragma unroll
             for (int g = 0; g < 10; ++g) {
-                float v[16], vl[16];
-                tmem_ld16(tmem + lane_base + 16 * g, v);
-                tmem_ld16(tmem + lane_base + kTLo + 16 * g, vl);
-                tmem_ld_wait();
+                float v[16], vl[16], vd[16];
                 const int sg = (g == 0) ? 0 : (g < 3) ? 1 : (g < 6) ? 2 : 3;
                 const int ib = 16 * g - kStkOff[sg];
+                const bool diag = (ib == 16 * sg);  // this group holds version sg's own sub-tile
+                tmem_ld16(tmem + lane_base + 16 * g, v);
+                tmem_ld16(tmem + lane_base + kTLo + 16 * g, vl);
+                if (diag) tmem_ld16(tmem + lane_base + kTDiag + 16 * sg, vd);
+                tmem_ld_wait();
+                if (diag)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] += vd[e];
                 if (sg == s) {
                     if (side == 0) {
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
-                            uint32_t pw[4];
+                            float a8[8];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int j0 = 8 * hf + 2 * e, i0 = ib + j0;
-                                pw[e] = pack_bf16x2(i0 <= r ? v[j0] + vl[j0] : 0.f,
-                                                    i0 + 1 <= r ? v[j0 + 1] + vl[j0 + 1] : 0.f);
+                            for (int e = 0; e < 8; ++e) {
+                                const int j0 = 8 * hf + e;
+                                a8[e] = (ib + j0 <= r) ? v[j0] + vl[j0] : 0.f;
                             }
-                            *reinterpret_cast<uint4*>(aq + sw128_chunk(r, (ib >> 3) + hf)) =
-                                make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                            uint4 hi, lo;
+                            pk8_hilo(a8, hi, lo);
+                            *reinterpret_cast<uint4*>(aq + sw128_chunk(r, (ib >> 3) + hf)) = hi;
+                            *reinterpret_cast<uint4*>(sm + kAqkLoTile +
+                                                      sw128_chunk(r, (ib >> 3) + hf)) = lo;
                         }
                     } else {
 #pragma unroll
@@ -522,8 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 }
             }
             if (side == 0)  // columns past this sub-tile's version are zero
-                for (int ch = 2 * (s + 1); ch < 8; ++ch)
+                for (int ch = 2 * (s + 1); ch < 8; ++ch) {
                     *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4*>(sm + kAqkLoTile + sw128_chunk(r, ch)) =
+                        make_uint4(0, 0, 0, 0);
+                }
         }
         tc_fence_before();
         __syncthreads();
@@ -556,35 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 for (int rr = 0; rr < 16; ++rr) sT[(16 * s + rr) * kLd + 16 * s + j] = t[rr];
             }
             __syncthreads();
-            for (int d = 1; d < 4; ++d) {
-                const int nb = 4 - d;
-                for (int e = tid; e < nb * 256; e += kThreads) {
-                    const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + d;
-                    float y0 = 0.f, y1 = 0.f;
-                    for (int t = sp; t < s; ++t)
-#pragma unroll
-                        for (int m = 0; m < 16; m += 2) {
-                            y0 = fmaf(sL[(16 * s + rr) * kLd + 16 * t + m],
-                                      sT[(16 * t + m) * kLd + 16 * sp + jj], y0);
-                            y1 = fmaf(sL[(16 * s + rr) * kLd + 16 * t + m + 1],
-                                      sT[(16 * t + m + 1) * kLd + 16 * sp + jj], y1);
-                        }
-                    sY[e] = y0 + y1;
-                }
-                __syncthreads();
-                for (int e = tid; e < nb * 256; e += kThreads) {
-                    const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + d;
-                    float y0 = 0.f, y1 = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 16; m += 2) {
-                        y0 = fmaf(sT[(16 * s + rr) * kLd + 16 * s + m], sY[(sp << 8) + m * 16 + jj], y0);
-                        y1 = fmaf(sT[(16 * s + rr) * kLd + 16 * s + m + 1],
-                                  sY[(sp << 8) + (m + 1) * 16 + jj], y1);
-                    }
-                    sT[(16 * s + rr) * kLd + 16 * sp + jj] = -(y0 + y1);
-                }
-                __syncthreads();
-            }
+            solve_round<1>(sL, sT, sY, tid);
+            solve_round<2>(sL, sT, sY, tid);
+            solve_round<3>(sL, sT, sY, tid);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile
             {
                 const int r = tid >> 2, cq = tid & 3;
@@ -637,24 +668,38 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             pend_v = (iter + 1) & 1;
         }
         {
-            // warps 0-3: lane = channel c, row c of the W^T tile (q slot);
-            // warps 4-7: lane = value column j, row j of the U^T tile (k slot).
-            // Both tiles: [128 rows][64 r] bf16, 128-byte swizzle.
+            // warps 0-3: lane = channel c -> row c of the W^T tile (bf16 [128][64], sw128,
+            //            staged in the q slot); warps 4-7: lane = value column j -> row j of
+            //            U^T, fp32, written straight into the package.
             const int m = 32 * (warp & 3) + lane;
-            const uint32_t col0 = (warp < 4) ? 0 : 64;
-            uint8_t* dst = qk + ((warp < 4) ? kOffQ : kOffK);
+            if (warp < 4) {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + col0 + 16 * g, v);
-                tmem_ld_wait();
+                for (int g = 0; g < 4; ++g) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const uint4 pk = make_uint4(pack_bf16x2(v[8 * hf], v[8 * hf + 1]),
-                                                pack_bf16x2(v[8 * hf + 2], v[8 * hf + 3]),
-                                                pack_bf16x2(v[8 * hf + 4], v[8 * hf + 5]),
-                                                pack_bf16x2(v[8 * hf + 6], v[8 * hf + 7]));
-                    *reinterpret_cast<uint4*>(dst + sw128_chunk(m, 2 * g + hf)) = pk;
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const uint4 pk = make_uint4(pack_bf16x2(v[8 * hf], v[8 * hf + 1]),
+                                                    pack_bf16x2(v[8 * hf + 2], v[8 * hf + 3]),
+                                                    pack_bf16x2(v[8 * hf + 4], v[8 * hf + 5]),
+                                                    pack_bf16x2(v[8 * hf + 6], v[8 * hf + 7]));
+                        *reinterpret_cast<uint4*>(qk + kOffQ + sw128_chunk(m, 2 * g + hf)) = pk;
+                    }
+                }
+            } else {
+                uint8_t* urow = pkg + kPkgU + m * 256;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float v[16];
+                    tmem_ld16(tmem + lane_base + 64 + 16 * g, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int cidx = 4 * g + q;  // 16-byte chunk: r in [4 cidx, 4 cidx + 4)
+                        *reinterpret_cast<float4*>(urow + ((cidx ^ (m & 15)) << 4)) =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    }
                 }
             }
         }
@@ -665,8 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if (s_abort) break;
         if (tid == 0) {
             bulk_s2g(pkg + kPkgW, qk + kOffQ, 16384);
-            bulk_s2g(pkg + kPkgU, qk + kOffK, 16384);
-            bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 8192);
+            bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 16384);  // A hi and lo
             bulk_commit();
         }
     }
@@ -702,21 +746,30 @@ struct StateParams {
     int N, H, maxchunks;
 };
 
-constexpr uint32_t kStage = 74752;             // package stage stride (73 KB, 1024-aligned)
-constexpr uint32_t kSbf = 2 * kStage;          // S as bf16, A = S^T MN-major [2 blk][128 i][128 B]
-constexpr uint32_t kVt = kSbf + 32768;         // Vt^T K-major [128 j][64 r]
-constexpr uint32_t kSBars = kVt + 16384;
+// shared-memory map of the state kernel (1024-aligned offsets)
+constexpr uint32_t kPA = 0;                    // package part A, two stages of 32 KB
+constexpr uint32_t kPB = 2 * kPkgPartA;        //  65536: package part B (one stage)
+constexpr uint32_t kUBuf = kPB + 33792;        //  99328: U^T fp32 [128 j][64 r] (one stage)
+constexpr uint32_t kSbf = kUBuf + kPkgUBytes;  // 132096: S bf16, A = S^T MN-major [2][128 i][128 B]
+constexpr uint32_t kVt = kSbf + 32768;         // 164864: Vt^T hi, K-major [128 j][64 r]
+constexpr uint32_t kVtLo = kVt + 16384;        // 181248: Vt^T lo
+constexpr uint32_t kOt = kVtLo + 16384;        // 197632: O [64 r][128 j] bf16 row-major (staging)
+constexpr uint32_t kSBars = kOt + 16384;       // 214016
 constexpr uint32_t kStateSmem = kSBars + 64 + 1024;
+static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limit");
+static_assert(kPkgPartB <= 33792, "package part B must fit its stage");
 
 __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2]
-    uint64_t* mma1 = full + 2;
-    uint64_t* mma2 = full + 3;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + 4);
+    uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2]
+    uint64_t* fullB = fullA + 2;
+    uint64_t* ubar = fullA + 3;
+    uint64_t* mma1 = fullA + 4;
+    uint64_t* mma2 = fullA + 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 6);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -726,8 +779,10 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
     const int nh = blockIdx.x, h = nh % p.H, n = nh / p.H;
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        mbar_init(&fullA[0], 1);
+        mbar_init(&fullA[1], 1);
+        mbar_init(fullB, 1);
+        mbar_init(ubar, 1);
         mbar_init(mma1, 1);
         mbar_init(mma2, 1);
         fence_mbar_init();
@@ -767,31 +822,43 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         }
     };
     write_sbf();
+    // parity of the phase an in-flight copy will complete, or -1 (thread 0; for a clean abort)
+    int pend_a[2] = {-1, -1}, pend_b = -1, pend_u = -1;
     if (tid == 0 && nch > 0) {
-        mbar_expect_tx(&full[0], kPkgBytes);
-        bulk_g2s(sm, pkg0, kPkgBytes, &full[0]);
+        mbar_expect_tx(&fullA[0], kPkgPartA);
+        bulk_g2s(sm + kPA, pkg0, kPkgPartA, &fullA[0]);
+        mbar_expect_tx(fullB, kPkgPartB);
+        bulk_g2s(sm + kPB, pkg0 + kPkgPartA, kPkgPartB, fullB);
+        mbar_expect_tx(ubar, kPkgUBytes);
+        bulk_g2s(sm + kUBuf, pkg0 + kPkgU, kPkgUBytes, ubar);
+        pend_a[0] = 0;
+        pend_b = 0;
+        pend_u = 0;
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
 
-    int issued = (nch > 0) ? 1 : 0;  // packages requested so far (thread 0)
     int t = 0;
     KDA_PHASE_INIT();
     for (; t < nch; ++t) {
         const int st = t & 1;
-        const uint8_t* stage = sm + st * kStage;
-        const uint32_t sstage = sbase + st * kStage;
+        const uint32_t sA = sbase + kPA + st * kPkgPartA;
+        const uint32_t sB = sbase + kPB - kPkgPartA;  // so that sB + kPkgKT etc. index part B
         const int64_t t0 = t_begin + (int64_t)t * kC;
         const int L = (int)((t_end - t0) < kC ? (t_end - t0) : kC);
+        const uint8_t* pkg_t = pkg0 + (size_t)t * kPkgBytes;
         if (tid == 0 && t + 1 < nch) {
             fence_async_smem();
-            mbar_expect_tx(&full[st ^ 1], kPkgBytes);
-            bulk_g2s(sm + (st ^ 1) * kStage, pkg0 + (size_t)(t + 1) * kPkgBytes, kPkgBytes,
-                     &full[st ^ 1]);
-            issued = t + 2;
+            mbar_expect_tx(&fullA[st ^ 1], kPkgPartA);
+            bulk_g2s(sm + kPA + (st ^ 1) * kPkgPartA, pkg_t + kPkgBytes, kPkgPartA, &fullA[st ^ 1]);
+            pend_a[st ^ 1] = ((t + 1) >> 1) & 1;
         }
-        if (!mbar_wait(&full[st], (t >> 1) & 1, p.err)) s_abort = 1;
+        if (mbar_wait(&fullA[st], (t >> 1) & 1, p.err)) {
+            if (tid == 0) pend_a[st] = -1;
+        } else {
+            s_abort = 1;
+        }
         KDA_PHASE(16);
 
         // X^T = S^T W^T (cols 0..63), (Gam Q S)^T = S^T (Gam Q)^T (cols 64..127)
@@ -802,43 +869,49 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
-                mma_bf16(tmem, a, sdesc_sw128(sstage + kPkgW + ks * 2048, 8192, 1024), idesc_w,
-                         ks > 0);
+                mma_bf16(tmem, a, sdesc_sw128(sA + kPkgW + ks * 2048, 8192, 1024), idesc_w, ks > 0);
             }
             mma_commit(mma1);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
                 const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
-                mma_bf16(tmem + 64, a, sdesc_sw128(sstage + kPkgQB + kb, 0, 1024), idesc,
-                         ks > 0);
+                mma_bf16(tmem + 64, a, sdesc_sw128(sA + kPkgQB + kb, 0, 1024), idesc, ks > 0);
             }
         }
+        bool ok = mbar_wait(ubar, t & 1, p.err);
+        ok = mbar_wait(fullB, t & 1, p.err) && ok;
+        if (tid == 0 && ok) pend_u = pend_b = -1;
+        if (!ok) s_abort = 1;
+        const float gam = reinterpret_cast<const float*>(sm + kPB + (kPkgG - kPkgPartA))[m];
         if (!mbar_wait(mma1, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
         KDA_PHASE(17);
 
-        // Vt = U - X: thread owns value column j = m and rows r in [32 wg, 32 wg + 32)
+        // Vt = U - X (hi and lo bf16 parts): thread owns value column j = m, rows r in
+        // [32 wg, 32 wg + 32)
         {
+            const uint8_t* urow = sm + kUBuf + m * 256;
 #pragma unroll
             for (int hx = 0; hx < 2; ++hx) {
                 float x[16];
                 tmem_ld16(tmem + lane_base + 32 * wg + 16 * hx, x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const uint4 u4 = *reinterpret_cast<const uint4*>(
-                        stage + kPkgU + sw128_chunk(m, 4 * wg + 2 * hx + cc));
-                    const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
-                    uint32_t pw[4];
+                for (int cc = 0; cc < 2; ++cc) {  // 8 rows: r0 = 32 wg + 16 hx + 8 cc
+                    const int c4 = 8 * wg + 4 * hx + 2 * cc;  // fp32 chunk index of r0
+                    const float4 ua = *reinterpret_cast<const float4*>(urow + ((c4 ^ (m & 15)) << 4));
+                    const float4 ub =
+                        *reinterpret_cast<const float4*>(urow + (((c4 + 1) ^ (m & 15)) << 4));
+                    const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+                    float d8[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 u = __bfloat1622float2(
-                            *reinterpret_cast<const __nv_bfloat162*>(&uw[e]));
-                        pw[e] = pack_bf16x2(u.x - x[8 * cc + 2 * e], u.y - x[8 * cc + 2 * e + 1]);
-                    }
-                    *reinterpret_cast<uint4*>(sm + kVt + sw128_chunk(m, 4 * wg + 2 * hx + cc)) =
-                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    for (int e = 0; e < 8; ++e) d8[e] = u[e] - x[8 * cc + e];
+                    uint4 hi, lo;
+                    pk8_hilo(d8, hi, lo);
+                    const uint32_t off = sw128_chunk(m, 4 * wg + 2 * hx + cc);
+                    *reinterpret_cast<uint4*>(sm + kVt + off) = hi;
+                    *reinterpret_cast<uint4*>(sm + kVtLo + off) = lo;
                 }
             }
         }
@@ -847,29 +920,46 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         __syncthreads();
         KDA_PHASE(18);
         if (s_abort) break;
+        if (tid == 0 && t + 1 < nch) {  // U of this chunk is consumed: fetch the next one
+            fence_async_smem();
+            mbar_expect_tx(ubar, kPkgUBytes);
+            bulk_g2s(sm + kUBuf, pkg_t + kPkgBytes + kPkgU, kPkgUBytes, ubar);
+            pend_u = (t + 1) & 1;
+        }
 
-        // dS = K~^T Vt (cols 128..255);  O^T += Vt^T A^T (cols 64..127)
+        // dS = K~^T Vt (cols 128..255);  O^T += Vt^T A^T with both in hi + lo (cols 64..127)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id2 = idesc_bf16(128, 128, true, false);
             constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + 128, sdesc_sw128(sstage + kPkgKT + ks * 2048, 8192, 1024),
+                mma_bf16(tmem + 128, sdesc_sw128(sB + kPkgKT + ks * 2048, 8192, 1024),
                          sdesc_sw128(sbase + kVt + ks * 32, 0, 1024), id2, ks > 0);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + 64, sdesc_sw128(sbase + kVt + ks * 32, 0, 1024),
-                         sdesc_sw128(sstage + kPkgAQK + ks * 32, 0, 1024), id3, 1);
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t vh = sdesc_sw128(sbase + kVt + ks * 32, 0, 1024);
+                const uint64_t vl = sdesc_sw128(sbase + kVtLo + ks * 32, 0, 1024);
+                const uint64_t ah = sdesc_sw128(sB + kPkgAQK + ks * 32, 0, 1024);
+                const uint64_t al = sdesc_sw128(sB + kPkgAQKLo + ks * 32, 0, 1024);
+                mma_bf16(tmem + 64, vh, ah, id3, 1);
+                mma_bf16(tmem + 64, vl, ah, id3, 1);
+                mma_bf16(tmem + 64, vh, al, id3, 1);
+            }
             mma_commit(mma2);
         }
         if (!mbar_wait(mma2, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
         KDA_PHASE(19);
+        if (tid == 0 && t + 1 < nch) {  // part B of this chunk is consumed
+            fence_async_smem();
+            mbar_expect_tx(fullB, kPkgPartB);
+            bulk_g2s(sm + kPB, pkg_t + kPkgBytes + kPkgPartA, kPkgPartB, fullB);
+            pend_b = (t + 1) & 1;
+        }
 
         // S <- gamma^C * S + dS ;  bf16 copy for the next chunk's MMAs
         {
-            const float gam = reinterpret_cast<const float*>(stage + kPkgG)[m];
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
                 float v[16];
@@ -880,19 +970,17 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
             }
             write_sbf();
         }
-        // output rows r in [32 wg, 32 wg + 32) of value column j = m
+        // output: O^T[j = m][r] for r in [32 wg, 32 wg + 32) -> O tile [r][j]
         {
-            __nv_bfloat16* orow = p.o + ((size_t)t0 * p.H + h) * kD + m;
+            __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(sm + kOt);
 #pragma unroll
             for (int hx = 0; hx < 2; ++hx) {
                 float v[16];
                 tmem_ld16(tmem + lane_base + 64 + 32 * wg + 16 * hx, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r = 32 * wg + 16 * hx + e;
-                    if (r < L) orow[(size_t)r * p.H * kD] = __float2bfloat16_rn(v[e]);
-                }
+                for (int e = 0; e < 16; ++e)
+                    ot[(32 * wg + 16 * hx + e) * kD + m] = __float2bfloat16_rn(v[e]);
             }
         }
         fence_async_smem();
@@ -900,6 +988,17 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         __syncthreads();
         KDA_PHASE(20);
         if (s_abort) break;
+        // the valid rows of the O tile -> o, 16 bytes per store
+        {
+            __nv_bfloat16* obase = p.o + ((size_t)t0 * p.H + h) * kD;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int u = tid + kThreads * k, r = u >> 4, cc = u & 15;
+                if (r < L)
+                    *reinterpret_cast<uint4*>(obase + (size_t)r * p.H * kD + 8 * cc) =
+                        *reinterpret_cast<const uint4*>(sm + kOt + r * 256 + 16 * cc);
+            }
+        }
     }
     if (p.S_out && !s_abort) {
 #pragma unroll
@@ -907,9 +1006,13 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
             *reinterpret_cast<float4*>(p.S_out + sbase_g + jj) =
                 make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
     }
-    // on an abort, let a package copy still in flight land before leaving
-    if (tid == 0 && s_abort && issued > t + 1)
-        mbar_wait(&full[(t + 1) & 1], ((t + 1) >> 1) & 1, nullptr);
+    // on an abort, let copies still in flight land before leaving
+    if (tid == 0 && s_abort) {
+        for (int q = 0; q < 2; ++q)
+            if (pend_a[q] >= 0) mbar_wait(&fullA[q], pend_a[q], nullptr);
+        if (pend_b >= 0) mbar_wait(fullB, pend_b, nullptr);
+        if (pend_u >= 0) mbar_wait(ubar, pend_u, nullptr);
+    }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
