@@ -70,14 +70,20 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // accumulates clock64() deltas between marked points of each kernel's loop.
 #ifdef KDA_PHASE_TIMING
 __device__ unsigned long long g_phase[32];
-#define KDA_PHASE_INIT() long long kda_t_last = clock64()
-#define KDA_PHASE(i)                                                 \
-    do {                                                             \
-        if (blockIdx.x == 0 && threadIdx.x == 0) {                   \
-            const long long kda_t = clock64();                       \
-            g_phase[(i)] += (unsigned long long)(kda_t - kda_t_last); \
-            kda_t_last = kda_t;                                      \
-        }                                                            \
+#define KDA_PHASE_INIT()              \
+    long long kda_t_last = clock64(); \
+    unsigned long long kda_acc[32] = {}
+#define KDA_PHASE(i)                                                \
+    do {                                                            \
+        const long long kda_t = clock64();                          \
+        kda_acc[(i)] += (unsigned long long)(kda_t - kda_t_last);   \
+        kda_t_last = kda_t;                                         \
+    } while (0)
+#define KDA_PHASE_FLUSH()                                                     \
+    do {                                                                      \
+        if (blockIdx.x == 0 && threadIdx.x == 0)                              \
+            for (int kda_i = 0; kda_i < 32; ++kda_i)                          \
+                if (kda_acc[kda_i]) atomicAdd(&g_phase[kda_i], kda_acc[kda_i]); \
     } while (0)
 #else
 #define KDA_PHASE_INIT() \
@@ -85,6 +91,9 @@ __device__ unsigned long long g_phase[32];
     } while (0)
 #define KDA_PHASE(i) \
     do {             \
+    } while (0)
+#define KDA_PHASE_FLUSH() \
+    do {                  \
     } while (0)
 #endif
 
@@ -356,12 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         const ItemInfo it = nx;
         const int next = item + gridDim.x;
         const bool has_next = next < n_items;
-        float beta_next = 0.f;  // the next item's beta[tid]: loaded now, stored after the pass
-        if (has_next) {
-            nx = decode_item(p, next);  // used only later: its latency overlaps
-            if (tid < nx.L)
-                beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
-        }
+        float beta_next = 0.f;  // the next item's beta[tid]: loaded mid-item, stored later
+        if (has_next) nx = decode_item(p, next);  // used only later: its latency overlaps
         uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
 
         // the previous item's package stores read the A stack and the other q/k buffer
@@ -397,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
             pend_z = (iter + 1) & 1;
         }
+        if (has_next && tid < nx.L)
+            beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
         if (tid < kD) {  // exclusive scan of the block totals, one channel per thread
             float a = 0.f;
 #pragma unroll
@@ -613,9 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 for (int rr = 0; rr < 16; ++rr) sT[(16 * s + rr) * kLd + 16 * s + j] = t[rr];
             }
             __syncthreads();
+            KDA_PHASE(8);
             solve_round<1>(sL, sT, sY, tid);
+            KDA_PHASE(9);
             solve_round<2>(sL, sT, sY, tid);
+            KDA_PHASE(10);
             solve_round<3>(sL, sT, sY, tid);
+            KDA_PHASE(11);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile
             {
                 const int r = tid >> 2, cq = tid & 3;
@@ -714,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             bulk_commit();
         }
     }
+    KDA_PHASE_FLUSH();
     // teardown: stores complete, no load in flight, TMEM released
     if (tid == 0) {
         bulk_wait0();
@@ -1000,6 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
             }
         }
     }
+    KDA_PHASE_FLUSH();
     if (p.S_out && !s_abort) {
 #pragma unroll
         for (int jj = 0; jj < 64; jj += 4)

@@ -5,7 +5,8 @@ import numpy as np
 import pytest
 
 from serving_kda_chunkwise_gb300 import inputs
-from kda_testutil import check_forward, gpu_forward, oracle_forward
+from kda_testutil import (BF16_NORM_TOL, BF16_RMS_TOL, bf16_norm_err, bf16_rms_err,
+                          check_forward, gpu_forward, oracle_forward)
 
 pytestmark = pytest.mark.gpu
 
@@ -89,10 +90,16 @@ def test_fwd_resume_equals_single_call(kda):
         o_chain = torch.empty_like(o_full)
         for idx, o in parts_o:
             o_chain[idx] = o
-        ref = o_full.float()
-        rms = ref.pow(2).mean().sqrt()
-        assert ((o_chain.float() - ref).abs().max() / rms).item() < 2e-2
-        assert ((S - S_full).abs().max() / S_full.pow(2).mean().sqrt()).item() < 2e-2
+        # chained vs single call differ only by rounding: same per-head rule as the parity tests
+        oc, of = o_chain.float().cpu().numpy(), o_full.float().cpu().numpy().astype(np.float64)
+        for n in range(2):
+            for h in range(4):
+                sl = slice(1000 * n, 1000 * (n + 1))
+                assert bf16_norm_err(oc[sl, h], of[sl, h]) <= BF16_NORM_TOL
+                assert bf16_rms_err(oc[sl, h], of[sl, h]) <= BF16_RMS_TOL
+                sc = S[n, h].cpu().numpy()
+                sf = S_full[n, h].cpu().numpy().astype(np.float64)
+                assert bf16_norm_err(sc, sf) <= BF16_NORM_TOL
 
 
 def test_fwd_state_aliasing_and_determinism(kda):
@@ -149,10 +156,13 @@ def test_fwd_decode_consistency(kda):
         outs.append(kda.decode_step(d["q"][t:t + 1], d["k"][t:t + 1], d["v"][t:t + 1],
                                     d["beta"][t:t + 1], d["z"][t:t + 1], d["A_log"], inp.g_min,
                                     S))
-    o_dec = torch.cat(outs).float()
-    rms = o_fwd.float().pow(2).mean().sqrt()
-    assert ((o_dec - o_fwd.float()).abs().max() / rms).item() < 2e-2
-    assert ((S - S_fwd).abs().max() / S_fwd.pow(2).mean().sqrt()).item() < 2e-2
+    o_dec = torch.cat(outs).float().cpu().numpy()
+    o_f = o_fwd.float().cpu().numpy().astype(np.float64)
+    for h in range(2):
+        assert bf16_norm_err(o_dec[:, h], o_f[:, h]) <= BF16_NORM_TOL
+        assert bf16_rms_err(o_dec[:, h], o_f[:, h]) <= BF16_RMS_TOL
+        assert bf16_norm_err(S[0, h].cpu().numpy(), S_fwd[0, h].cpu().numpy().astype(np.float64)) \
+            <= BF16_NORM_TOL
 
 
 def test_fwd_invariant_state_held(kda):
@@ -192,7 +202,6 @@ def test_fwd_tensor_core_path_matches_cuda_core_path(kda, monkeypatch):
     monkeypatch.setenv("KDA_FWD_PATH", "generic")
     assert kda.workspace_size(inp.T, inp.N, inp.H, 128, 128, __import__("torch").bfloat16) == 0
     o_cc, S_cc = gpu_forward(inp)
-    from kda_testutil import bf16_norm_err
     for n in range(inp.N):
         a, b = inp.cu_seqlens[n], inp.cu_seqlens[n + 1]
         for h in range(inp.H):
