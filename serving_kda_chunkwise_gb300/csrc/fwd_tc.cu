@@ -190,8 +190,11 @@ static_assert(kIntraSmem <= 232448, "intra kernel exceeds the shared-memory limi
 // After the W/U MMAs the q / k slots of the current buffer stage W^T and U^T.
 constexpr uint32_t kAqkTile = kAStk, kAqkLoTile = kAStk + 8192, kMTile = kAStk + 16384;
 constexpr int kLd = 65;                       // padded fp32 row stride of L and T
-constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4, kSY = kST + 64 * kLd * 4;
-static_assert(kSY + 3 * 256 * 4 <= kBStk + 40960, "solve scratch must fit the B stack");
+constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4;
+static_assert(kST + 64 * kLd * 4 <= kBStk + 40960, "L and T must fit the B stack");
+// the solve's per-warp scratch (4 warps x 3 tiles x 16 x 20 floats) reuses the A-lo region
+constexpr uint32_t kSolveScr = kALo;
+static_assert(4 * 3 * 16 * 20 * 4 <= 16384, "solve scratch must fit the A-lo region");
 // TMEM columns: main Gram accumulator [0, 160), diagonal-column lo correction [160, 224),
 // q-side lo correction [256, 416);
 // later W^T [0, 64) and U^T [64, 128).
@@ -265,40 +268,136 @@ __device__ __forceinline__ void pk8_hilo(const float (&v)[8], uint4& hi, uint4& 
     lo = pk8(l);
 }
 
-// Off-diagonal blocks at distance D of T = (I + L)^{-1} (16x16 blocks, fp32):
-//   Y_{s,s'} = sum_{t=s'}^{s-1} L_{s,t} T_{t,s'},   T_{s,s'} = -T_{s,s} Y_{s,s'},   s = s' + D.
-// Every thread computes whole dot products with its operands loaded ahead.
-template <int D>
-__device__ __forceinline__ void solve_round(const float* sL, float* sT, float* sY, int tid) {
-    constexpr int kNb = 4 - D;
-    for (int e = tid; e < kNb * 256; e += kThreads) {
-        const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + D;
-        float l[16 * D], t[16 * D];
+// ---- 16x16 fp32 tiles on the legacy warp-level tensor-core path (mma.sync, tf32 inputs,
+//      fp32 accumulation), used for the small triangular solve.  A tile is held by a warp
+//      as two m16n8 accumulators: element (row, col) of accumulator nn, slot q sits in lane
+//      4*(row % 8) + (col % 8) / 2 with row = g + 8*(q >> 1), col = 8*nn + 2*t + (q & 1).
+struct Tile16 {
+    float c[2][4];
+};
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ void tile_zero(Tile16& f) {
 #pragma unroll
-        for (int m = 0; m < 16 * D; ++m) {
-            l[m] = sL[(16 * s + rr) * kLd + 16 * sp + m];
-            t[m] = sT[(16 * sp + m) * kLd + 16 * sp + jj];
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f.c[nn][q] = 0.f;
+}
+
+// f = scale * X + diag * I
+__device__ __forceinline__ void tile_load(Tile16& f, const float* X, int ld, float scale,
+                                          float diag) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = g + 8 * (q >> 1), col = 8 * nn + 2 * t + (q & 1);
+            f.c[nn][q] = scale * X[row * ld + col] + (row == col ? diag : 0.f);
         }
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
+}
+
+// X = scale * f + diag * I
+__device__ __forceinline__ void tile_store(const Tile16& f, float* X, int ld, float scale,
+                                           float diag) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
 #pragma unroll
-        for (int m = 0; m < 16 * D; ++m) y[m & 3] = fmaf(l[m], t[m], y[m & 3]);
-        sY[e] = (y[0] + y[1]) + (y[2] + y[3]);
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = g + 8 * (q >> 1), col = 8 * nn + 2 * t + (q & 1);
+            X[row * ld + col] = scale * f.c[nn][q] + (row == col ? diag : 0.f);
+        }
+}
+
+// f += A B  (A, B: 16x16 fp32 tiles in shared memory, row-major with strides lda, ldb)
+__device__ __forceinline__ void tile_mma(Tile16& f, const float* A, int lda, const float* B,
+                                         int ldb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t a0 = to_tf32(A[g * lda + 8 * kk + t]);
+        const uint32_t a1 = to_tf32(A[(g + 8) * lda + 8 * kk + t]);
+        const uint32_t a2 = to_tf32(A[g * lda + 8 * kk + t + 4]);
+        const uint32_t a3 = to_tf32(A[(g + 8) * lda + 8 * kk + t + 4]);
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn) {
+            const uint32_t b0 = to_tf32(B[(8 * kk + t) * ldb + 8 * nn + g]);
+            const uint32_t b1 = to_tf32(B[(8 * kk + t + 4) * ldb + 8 * nn + g]);
+            asm volatile(
+                "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 "
+                "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                : "+f"(f.c[nn][0]), "+f"(f.c[nn][1]), "+f"(f.c[nn][2]), "+f"(f.c[nn][3])
+                : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        }
+    }
+}
+
+// T = (I + L)^{-1} for the 64x64 strictly lower L (16x16 blocks).  Warp w < 4 first inverts
+// diagonal block w as (I - N)(I + N^2)(I + N^4)(I + N^8), N = L_ww (N^16 = 0); then the
+// off-diagonal blocks follow by distance d: T_{s,s'} = -T_ss sum_{t=s'}^{s-1} L_st T_{t,s'}.
+// `scr` is per-warp scratch of 3 tiles of 16 x kScrLd floats.
+constexpr int kScrLd = 20;
+constexpr int kScrTile = 16 * kScrLd;
+
+__device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* scr_all,
+                                             int warp) {
+    float* scr = scr_all + warp * 3 * kScrTile;
+    float* sP = scr;                 // running product
+    float* sN = scr + kScrTile;      // N^(2^k)
+    float* sIN = scr + 2 * kScrTile; // I + N^(2^k)
+    if (warp < 4) {
+        const float* Lb = sL + (16 * warp) * kLd + 16 * warp;
+        Tile16 f, q;
+        tile_load(f, Lb, kLd, -1.f, 1.f);  // P = I - N
+        tile_store(f, sP, kScrLd, 1.f, 0.f);
+        tile_zero(q);
+        tile_mma(q, Lb, kLd, Lb, kLd);     // N^2
+        __syncwarp();
+        tile_store(q, sN, kScrLd, 1.f, 0.f);
+        tile_store(q, sIN, kScrLd, 1.f, 1.f);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {      // P <- P (I + N^2^k), N <- N^2 (k < 2)
+            tile_zero(f);
+            tile_mma(f, sP, kScrLd, sIN, kScrLd);
+            if (k < 2) {
+                tile_zero(q);
+                tile_mma(q, sN, kScrLd, sN, kScrLd);
+            }
+            __syncwarp();
+            if (k < 2) {
+                tile_store(f, sP, kScrLd, 1.f, 0.f);
+                tile_store(q, sN, kScrLd, 1.f, 0.f);
+                tile_store(q, sIN, kScrLd, 1.f, 1.f);
+            } else {
+                tile_store(f, sT + (16 * warp) * kLd + 16 * warp, kLd, 1.f, 0.f);
+            }
+            __syncwarp();
+        }
     }
     __syncthreads();
-    for (int e = tid; e < kNb * 256; e += kThreads) {
-        const int sp = e >> 8, rr = (e >> 4) & 15, jj = e & 15, s = sp + D;
-        float l[16], y4[16];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            l[m] = sT[(16 * s + rr) * kLd + 16 * s + m];
-            y4[m] = sY[(sp << 8) + m * 16 + jj];
+    for (int d = 1; d < 4; ++d) {
+        if (warp < 4 - d) {
+            const int sp = warp, s = warp + d;
+            Tile16 y, f;
+            tile_zero(y);
+            for (int t = sp; t < s; ++t)
+                tile_mma(y, sL + (16 * s) * kLd + 16 * t, kLd, sT + (16 * t) * kLd + 16 * sp, kLd);
+            tile_store(y, sP, kScrLd, 1.f, 0.f);
+            __syncwarp();
+            tile_zero(f);
+            tile_mma(f, sT + (16 * s) * kLd + 16 * s, kLd, sP, kScrLd);
+            tile_store(f, sT + (16 * s) * kLd + 16 * sp, kLd, -1.f, 0.f);
         }
-        float y[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int m = 0; m < 16; ++m) y[m & 3] = fmaf(l[m], y4[m], y[m & 3]);
-        sT[(16 * s + rr) * kLd + 16 * sp + jj] = -((y[0] + y[1]) + (y[2] + y[3]));
+        __syncthreads();
     }
-    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
@@ -341,9 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 
     // parity of the phase a load in flight will complete, or -1 (thread 0; for a clean abort)
     int pend_q[2] = {-1, -1}, pend_v = -1, pend_z = -1;
-    ItemInfo nx;
+    ItemInfo nx, nx2;  // the next two items of this CTA, decoded ahead of use
     if ((int)blockIdx.x < n_items) {
         nx = decode_item(p, blockIdx.x);
+        if ((int)(blockIdx.x + gridDim.x) < n_items) nx2 = decode_item(p, blockIdx.x + gridDim.x);
         if (tid == 0) {
             load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, nx, &qk_bar[0]);
             load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
@@ -366,7 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         const int next = item + gridDim.x;
         const bool has_next = next < n_items;
         float beta_next = 0.f;  // the next item's beta[tid]: loaded mid-item, stored later
-        if (has_next) nx = decode_item(p, next);  // used only later: its latency overlaps
+        nx = nx2;
+        if (next + (int)gridDim.x < n_items) nx2 = decode_item(p, next + gridDim.x);
         uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
 
         // the previous item's package stores read the A stack and the other q/k buffer
@@ -540,14 +641,19 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         tc_fence_after();
         KDA_PHASE(3);
 
-        // ---- Gram epilogue (warps 0-3): q-side rows -> A tile (bf16), k-side rows -> L (fp32)
-        if (warp < 4) {
-            const int m = tid;  // TMEM lane
+        // ---- Gram epilogue: q-side rows -> A tile (bf16 hi + lo), k-side rows -> L (fp32).
+        //      TMEM lane m = 32 (warp % 4) + lane; the groups of 16 columns a lane quadrant
+        //      needs are split between the two warpgroups.
+        {
+            const int quad = warp & 3, wg = warp >> 2;
+            const int m = 32 * quad + lane;
             const int side = m >> 6, r = m & 63, s = r >> 4;
             float* sL = reinterpret_cast<float*>(sm + kSL);
             uint8_t* aq = sm + kAqkTile;
-#pragma unroll
-            for (int g = 0; g < 10; ++g) {
+            // rows 0..31 of a side need groups 0..2 (versions 0, 1); rows 32..63 groups 3..9
+            const int g_lo = (quad & 1) ? (wg ? 7 : 3) : (wg ? 2 : 0);
+            const int g_hi = (quad & 1) ? (wg ? 10 : 7) : (wg ? 3 : 2);
+            for (int g = g_lo; g < g_hi; ++g) {
                 float v[16], vl[16], vd[16];
                 const int sg = (g == 0) ? 0 : (g < 3) ? 1 : (g < 6) ? 2 : 3;
                 const int ib = 16 * g - kStkOff[sg];
@@ -582,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                     }
                 }
             }
-            if (side == 0)  // columns past this sub-tile's version are zero
+            if (side == 0 && wg == 0)  // columns past this sub-tile's version are zero
                 for (int ch = 2 * (s + 1); ch < 8; ++ch) {
                     *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4*>(sm + kAqkLoTile + sw128_chunk(r, ch)) =
@@ -599,34 +705,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         {
             const float* sL = reinterpret_cast<const float*>(sm + kSL);
             float* sT = reinterpret_cast<float*>(sm + kST);
-            float* sY = reinterpret_cast<float*>(sm + kSY);
-            if (warp < 4 && lane < 16) {
-                const int s = warp, j = lane;
-                float t[16];
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float lrow[16];
-#pragma unroll
-                    for (int m = 0; m < rr; ++m) lrow[m] = sL[(16 * s + rr) * kLd + 16 * s + m];
-                    float a = (rr == j) ? 1.f : 0.f, a2 = 0.f;
-#pragma unroll
-                    for (int m = 0; m < rr; m += 2) {
-                        a = fmaf(-lrow[m], t[m], a);
-                        if (m + 1 < rr) a2 = fmaf(-lrow[m + 1], t[m + 1], a2);
-                    }
-                    t[rr] = a + a2;
-                }
-#pragma unroll
-                for (int rr = 0; rr < 16; ++rr) sT[(16 * s + rr) * kLd + 16 * s + j] = t[rr];
-            }
-            __syncthreads();
+            float* sScr = reinterpret_cast<float*>(sm + kSolveScr);
+            solve_tril64(sL, sT, sScr, warp);
             KDA_PHASE(8);
-            solve_round<1>(sL, sT, sY, tid);
-            KDA_PHASE(9);
-            solve_round<2>(sL, sT, sY, tid);
-            KDA_PHASE(10);
-            solve_round<3>(sL, sT, sY, tid);
-            KDA_PHASE(11);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile
             {
                 const int r = tid >> 2, cq = tid & 3;
@@ -781,7 +862,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
     uint64_t* ubar = fullA + 3;
     uint64_t* mma1 = fullA + 4;
     uint64_t* mma2 = fullA + 5;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 6);
+    uint64_t* mma3 = fullA + 6;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 7);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -797,6 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         mbar_init(ubar, 1);
         mbar_init(mma1, 1);
         mbar_init(mma2, 1);
+        mbar_init(mma3, 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -860,6 +943,8 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         const int64_t t0 = t_begin + (int64_t)t * kC;
         const int L = (int)((t_end - t0) < kC ? (t_end - t0) : kC);
         const uint8_t* pkg_t = pkg0 + (size_t)t * kPkgBytes;
+        if (tid == 0 && t + 2 < nch)  // warm L2 with the package after next
+            l2_prefetch(pkg_t + 2 * (size_t)kPkgBytes, kPkgBytes);
         if (tid == 0 && t + 1 < nch) {
             fence_async_smem();
             mbar_expect_tx(&fullA[st ^ 1], kPkgPartA);
@@ -948,6 +1033,7 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem + 128, sdesc_sw128(sB + kPkgKT + ks * 2048, 8192, 1024),
                          sdesc_sw128(sbase + kVt + ks * 32, 0, 1024), id2, ks > 0);
+            mma_commit(mma2);  // the state update waits only for this
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 const uint64_t vh = sdesc_sw128(sbase + kVt + ks * 32, 0, 1024);
@@ -958,17 +1044,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
                 mma_bf16(tmem + 64, vl, ah, id3, 1);
                 mma_bf16(tmem + 64, vh, al, id3, 1);
             }
-            mma_commit(mma2);
+            mma_commit(mma3);
         }
         if (!mbar_wait(mma2, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
         KDA_PHASE(19);
-        if (tid == 0 && t + 1 < nch) {  // part B of this chunk is consumed
-            fence_async_smem();
-            mbar_expect_tx(fullB, kPkgPartB);
-            bulk_g2s(sm + kPB, pkg_t + kPkgBytes + kPkgPartA, kPkgPartB, fullB);
-            pend_b = (t + 1) & 1;
-        }
 
         // S <- gamma^C * S + dS ;  bf16 copy for the next chunk's MMAs
         {
@@ -981,6 +1061,14 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
                 for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gam, S[16 * g + e], v[e]);
             }
             write_sbf();
+        }
+        if (!mbar_wait(mma3, t & 1, p.err)) s_abort = 1;
+        tc_fence_after();
+        if (tid == 0 && t + 1 < nch) {  // part B of this chunk is consumed
+            fence_async_smem();
+            mbar_expect_tx(fullB, kPkgPartB);
+            bulk_g2s(sm + kPB, pkg_t + kPkgBytes + kPkgPartA, kPkgPartB, fullB);
+            pend_b = (t + 1) & 1;
         }
         // output: O^T[j = m][r] for r in [32 wg, 32 wg + 32) -> O tile [r][j]
         {

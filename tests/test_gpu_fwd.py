@@ -206,5 +206,5 @@ def test_fwd_tensor_core_path_matches_cuda_core_path(kda, monkeypatch):
         a, b = inp.cu_seqlens[n], inp.cu_seqlens[n + 1]
         for h in range(inp.H):
             assert bf16_norm_err(o_tc[a:b, h], o_cc[a:b, h].astype(np.float64)) < 2e-2
-            rms = np.sqrt(np.mean(S_cc[n, h] ** 2))
-            assert np.max(np.abs(S_tc[n, h] - S_cc[n, h])) / rms < 2e-2
+            assert bf16_norm_err(S_tc[n, h], S_cc[n, h].astype(np.float64)) <= BF16_NORM_TOL
+            assert bf16_rms_err(S_tc[n, h], S_cc[n, h].astype(np.float64)) <= BF16_RMS_TOL
