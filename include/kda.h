@@ -128,6 +128,29 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
 kda_status_t kda_device_status(kda_stream_t stream);
 
 /*
+ * kda_fwd_chunked_noalloc -- the same forward as kda_fwd_chunked for callers that must not
+ * allocate device memory (a runtime that owns every byte of GPU memory, a plugin that may
+ * not call the CUDA allocator, code where an allocation would synchronise the device).  The
+ * pages have no counterpart: this is an interface convenience.
+ * Arguments are those of kda_fwd_chunked without the workspace.  Scratch comes from a 64 MiB
+ * buffer compiled into the library, which every GPU that loads the library holds until the
+ * process exits; problems whose kda_fwd_workspace_size() exceeds 64 MiB are rejected with
+ * KDA_ERR_INVALID_ARG (nothing is launched).  No call allocates memory.
+ *  - The first call on a device looks up the buffer's device address (cudaGetSymbolAddress);
+ *    make that first call before any stream capture.
+ *  - All calls share the one buffer, which keeps the last call's contents; nothing in it
+ *    has to start at zero (every byte a call reads it has first written).  Calls whose
+ *    execution overlaps on the GPU (other streams, other threads) race on the buffer:
+ *    serialise them.
+ */
+kda_status_t kda_fwd_chunked_noalloc(const void *q, const void *k, const void *v,
+                                     const void *beta, const void *z, const float *A_log,
+                                     float g_min, const float *S0, float *S_out,
+                                     const int32_t *cu_seqlens, int N, int64_t T_total, int H,
+                                     int dk, int dv, kda_dtype_t io_dt, void *o,
+                                     kda_stream_t stream);
+
+/*
  * Per-kernel timing (tracing aid; not part of the method).  After kda_profile_begin(),
  * every kernel the library launches is bracketed by two CUDA events recorded on the
  * launching stream.  kda_profile_end() waits for those events, stops recording and fills

@@ -82,6 +82,13 @@ kda_status_t check_gmin(float g_min) {
 
 }  // namespace
 
+namespace kda {
+kda_status_t set_last_error(kda_status_t s, const char* msg) {
+    t_last_error = msg;
+    return s;
+}
+}  // namespace kda
+
 extern "C" {
 
 int kda_version(void) { return 100; /* 0.1.0 */ }

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include "kda.h"
 #include <stddef.h>
 #include <stdint.h>
 
@@ -42,6 +44,9 @@ cudaError_t launch_fwd_generic(const FwdArgs& a);
 // fwd_tc_workspace_size() bytes.
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H);
 cudaError_t launch_fwd_tc(const FwdArgs& a);
+
+// Records `msg` as the calling thread's last error (see kda_last_error) and returns `s`.
+kda_status_t set_last_error(kda_status_t s, const char* msg);
 
 // Kernel timing hooks (profile.cu): no-ops unless kda_profile_begin() is active.
 int prof_kernel_begin(const char* name, cudaStream_t s);
