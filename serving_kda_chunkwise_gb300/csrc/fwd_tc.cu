@@ -48,17 +48,18 @@ constexpr int kD = 128;   // head dim (dk = dv)
 constexpr int kThreads = 256;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
-// part A (double buffered by the state kernel: needed at the start of a chunk)
+// part A (needed at the start of a chunk)
 constexpr uint32_t kPkgW = 0;         // W^T    [128 c][64 r] bf16 sw128: B = W^T MN-major
 constexpr uint32_t kPkgQB = 16384;    // Gam*Q  [64 r][128 c] bf16, K-major sw128
 constexpr uint32_t kPkgPartA = 32768;
-// part B (single buffered: needed from the middle of a chunk on)
+// part B (needed from the middle of a chunk on)
 constexpr uint32_t kPkgKT = 32768;    // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
 constexpr uint32_t kPkgAQK = 49152;   // A hi   [64 r][64 i] bf16, K-major sw128
 constexpr uint32_t kPkgAQKLo = 57344; // A lo   (A = hi + lo, bf16 each)
+constexpr uint32_t kPkgPartB = 32768;
 constexpr uint32_t kPkgG = 65536;     // gamma^C [128] fp32
-constexpr uint32_t kPkgPartB = 66048 - 32768;
-// part C (single buffered)
+constexpr uint32_t kPkgGBytes = 512;
+// part C
 constexpr uint32_t kPkgU = 66048;     // U^T    [128 j][64 r] fp32, 16-byte chunk c of row j at
                                       //        chunk position c ^ (j & 15)
 constexpr uint32_t kPkgUBytes = 32768;
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 ld8(sm + kZBuf + cofs + sw128_chunk(r, cg & 7), zz);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    acc[e] += (r < it.L) ? p.g_min / (1.f + __expf(-scale * zz[e])) : 0.f;
+                    acc[e] += (r < it.L) ? __fdividef(p.g_min, 1.f + __expf(-scale * zz[e])) : 0.f;
                     G[i][e] = acc[e];
                 }
             }
@@ -815,6 +816,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 if (pend_q[q] >= 0) mbar_wait(&qk_bar[q], pend_q[q], nullptr);
             if (pend_v >= 0) mbar_wait(v_bar, pend_v, nullptr);
             if (pend_z >= 0) mbar_wait(z_bar, pend_z, nullptr);
+            mma_commit(mma_bar);  // arrives once every MMA issued so far has completed
+            mbar_wait(mma_bar, mma_phase & 1, nullptr);
         }
     }
     tc_fence_before();
@@ -841,29 +844,41 @@ struct StateParams {
 
 // shared-memory map of the state kernel (1024-aligned offsets)
 constexpr uint32_t kPA = 0;                    // package part A, two stages of 32 KB
-constexpr uint32_t kPB = 2 * kPkgPartA;        //  65536: package part B (one stage)
-constexpr uint32_t kUBuf = kPB + 33792;        //  99328: U^T fp32 [128 j][64 r] (one stage)
-constexpr uint32_t kSbf = kUBuf + kPkgUBytes;  // 132096: S bf16, A = S^T MN-major [2][128 i][128 B]
-constexpr uint32_t kVt = kSbf + 32768;         // 164864: Vt^T hi, K-major [128 j][64 r]
-constexpr uint32_t kVtLo = kVt + 16384;        // 181248: Vt^T lo
-constexpr uint32_t kOt = kVtLo + 16384;        // 197632: O [64 r][128 j] bf16 row-major (staging)
-constexpr uint32_t kSBars = kOt + 16384;       // 214016
-constexpr uint32_t kStateSmem = kSBars + 64 + 1024;
+constexpr uint32_t kPB = 2 * kPkgPartA;        //  65536: package part B, two stages of 32 KB
+constexpr uint32_t kUBuf = kPB + 2 * kPkgPartB;// 131072: U^T fp32 [128 j][64 r] (one stage)
+constexpr uint32_t kSbf = kUBuf + kPkgUBytes;  // 163840: S bf16, A = S^T MN-major [2][128 i][128 B]
+constexpr uint32_t kVt = kSbf + 32768;         // 196608: Vt^T hi, K-major [128 j][64 r]
+constexpr uint32_t kVtLo = kVt + 16384;        // 212992: Vt^T lo
+constexpr uint32_t kGam = kVtLo + 16384;       // 229376: gamma^C, two stages of 512 B
+constexpr uint32_t kSBars = kGam + 1024;       // 230400
+constexpr uint32_t kStateSmem = kSBars + 128 + 1024;
 static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limit");
-static_assert(kPkgPartB <= 33792, "package part B must fit its stage");
+// TMEM columns: X^T [0, 64); dS [128, 256); output accumulator, two buffers [64, 128), [256, 320)
+constexpr uint32_t kStateTmemCols = 512;
 
+__device__ __forceinline__ uint32_t out_col(int t) { return (t & 1) ? 256u : 64u; }
+
+// One CTA per (sequence, head), 256 threads.  Per chunk t (package parts A, B double
+// buffered; U single buffered):
+//   [MMA1(t): X^T = S^T W^T and (Gam Q S)^T into out_col(t), issued at the end of t-1]
+//   E1(t):  Vt = U - X  (bf16 hi + lo)                      | waits mma1
+//   MMA2(t): dS = K~^T Vt        -> commit mma2
+//   MMA3(t): O^T += Vt^T A^T     -> commit mma3 (hi/lo products)
+//   E2(t):  S <- gamma S + dS, bf16 copy of S               | waits mma2
+//   MMA1(t+1) issued
+//   E3(t):  O(t) -> global                                  | waits mma3; overlaps MMA1(t+1)
 __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
     uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2]
-    uint64_t* fullB = fullA + 2;
-    uint64_t* ubar = fullA + 3;
-    uint64_t* mma1 = fullA + 4;
-    uint64_t* mma2 = fullA + 5;
-    uint64_t* mma3 = fullA + 6;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 7);
+    uint64_t* fullB = fullA + 2;                                  // [2] (part B + gamma)
+    uint64_t* ubar = fullA + 4;
+    uint64_t* mma1 = fullA + 5;
+    uint64_t* mma2 = fullA + 6;
+    uint64_t* mma3 = fullA + 7;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 8);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -873,17 +888,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
     const int nh = blockIdx.x, h = nh % p.H, n = nh / p.H;
 
     if (tid == 0) {
-        mbar_init(&fullA[0], 1);
-        mbar_init(&fullA[1], 1);
-        mbar_init(fullB, 1);
-        mbar_init(ubar, 1);
-        mbar_init(mma1, 1);
-        mbar_init(mma2, 1);
-        mbar_init(mma3, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(&fullA[i], 1);
         fence_mbar_init();
         s_abort = 0;
     }
-    if (warp == 0) tmem_alloc(tmem_slot, 256);
+    if (warp == 0) tmem_alloc(tmem_slot, kStateTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -916,77 +925,89 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
             *reinterpret_cast<uint4*>(blk + sw128_chunk(m, ch)) = pk;
         }
     };
-    write_sbf();
     // parity of the phase an in-flight copy will complete, or -1 (thread 0; for a clean abort)
-    int pend_a[2] = {-1, -1}, pend_b = -1, pend_u = -1;
-    if (tid == 0 && nch > 0) {
-        mbar_expect_tx(&fullA[0], kPkgPartA);
-        bulk_g2s(sm + kPA, pkg0, kPkgPartA, &fullA[0]);
-        mbar_expect_tx(fullB, kPkgPartB);
-        bulk_g2s(sm + kPB, pkg0 + kPkgPartA, kPkgPartB, fullB);
+    int pend_a[2] = {-1, -1}, pend_b[2] = {-1, -1}, pend_u = -1;
+    auto issue_ab = [&](int t) {  // parts A and B (+ gamma) of chunk t into stage t & 1
+        const uint8_t* src = pkg0 + (size_t)t * kPkgBytes;
+        const int st = t & 1;
+        fence_async_smem();
+        mbar_expect_tx(&fullA[st], kPkgPartA);
+        bulk_g2s(sm + kPA + st * kPkgPartA, src, kPkgPartA, &fullA[st]);
+        mbar_expect_tx(&fullB[st], kPkgPartB + kPkgGBytes);
+        bulk_g2s(sm + kPB + st * kPkgPartB, src + kPkgKT, kPkgPartB, &fullB[st]);
+        bulk_g2s(sm + kGam + st * 512, src + kPkgG, kPkgGBytes, &fullB[st]);
+        pend_a[st] = pend_b[st] = (t >> 1) & 1;
+    };
+    auto issue_u = [&](int t) {
+        fence_async_smem();
         mbar_expect_tx(ubar, kPkgUBytes);
-        bulk_g2s(sm + kUBuf, pkg0 + kPkgU, kPkgUBytes, ubar);
-        pend_a[0] = 0;
-        pend_b = 0;
-        pend_u = 0;
+        bulk_g2s(sm + kUBuf, pkg0 + (size_t)t * kPkgBytes + kPkgU, kPkgUBytes, ubar);
+        pend_u = t & 1;
+    };
+    int mma1_commits = 0;  // thread 0: commits issued on mma1 (to drain MMAs on an abort)
+    auto issue_mma1 = [&](int t) {  // X^T and (Gam Q S)^T of chunk t (thread 0)
+        tc_fence_after();
+        ++mma1_commits;
+        const uint32_t sA = sbase + kPA + (t & 1) * kPkgPartA;
+        constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
+        constexpr uint32_t idesc_w = idesc_bf16(128, 64, true, true);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
+            mma_bf16(tmem, a, sdesc_sw128(sA + kPkgW + ks * 2048, 8192, 1024), idesc_w, ks > 0);
+        }
+        mma_commit(mma1);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
+            const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
+            mma_bf16(tmem + out_col(t), a, sdesc_sw128(sA + kPkgQB + kb, 0, 1024), idesc, ks > 0);
+        }
+    };
+    auto wait_a = [&](int t) {
+        if (mbar_wait(&fullA[t & 1], (t >> 1) & 1, p.err)) {
+            if (tid == 0) pend_a[t & 1] = -1;
+        } else {
+            s_abort = 1;
+        }
+    };
+
+    write_sbf();
+    if (tid == 0 && nch > 0) {
+        issue_ab(0);
+        issue_u(0);
+        if (nch > 1) issue_ab(1);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (nch > 0) {
+        wait_a(0);
+        if (tid == 0) issue_mma1(0);
+    }
 
     int t = 0;
     KDA_PHASE_INIT();
     for (; t < nch; ++t) {
         const int st = t & 1;
-        const uint32_t sA = sbase + kPA + st * kPkgPartA;
-        const uint32_t sB = sbase + kPB - kPkgPartA;  // so that sB + kPkgKT etc. index part B
+        const uint32_t sB = sbase + kPB + st * kPkgPartB - kPkgKT;  // sB + kPkgKT = part B
         const int64_t t0 = t_begin + (int64_t)t * kC;
         const int L = (int)((t_end - t0) < kC ? (t_end - t0) : kC);
-        const uint8_t* pkg_t = pkg0 + (size_t)t * kPkgBytes;
         if (tid == 0 && t + 2 < nch)  // warm L2 with the package after next
-            l2_prefetch(pkg_t + 2 * (size_t)kPkgBytes, kPkgBytes);
-        if (tid == 0 && t + 1 < nch) {
-            fence_async_smem();
-            mbar_expect_tx(&fullA[st ^ 1], kPkgPartA);
-            bulk_g2s(sm + kPA + (st ^ 1) * kPkgPartA, pkg_t + kPkgBytes, kPkgPartA, &fullA[st ^ 1]);
-            pend_a[st ^ 1] = ((t + 1) >> 1) & 1;
-        }
-        if (mbar_wait(&fullA[st], (t >> 1) & 1, p.err)) {
-            if (tid == 0) pend_a[st] = -1;
-        } else {
-            s_abort = 1;
-        }
-        KDA_PHASE(16);
-
-        // X^T = S^T W^T (cols 0..63), (Gam Q S)^T = S^T (Gam Q)^T (cols 64..127)
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
-            constexpr uint32_t idesc_w = idesc_bf16(128, 64, true, true);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
-                mma_bf16(tmem, a, sdesc_sw128(sA + kPkgW + ks * 2048, 8192, 1024), idesc_w, ks > 0);
-            }
-            mma_commit(mma1);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
-                const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
-                mma_bf16(tmem + 64, a, sdesc_sw128(sA + kPkgQB + kb, 0, 1024), idesc, ks > 0);
-            }
-        }
+            l2_prefetch(pkg0 + (size_t)(t + 2) * kPkgBytes, kPkgBytes);
         bool ok = mbar_wait(ubar, t & 1, p.err);
-        ok = mbar_wait(fullB, t & 1, p.err) && ok;
-        if (tid == 0 && ok) pend_u = pend_b = -1;
+        ok = mbar_wait(&fullB[st], (t >> 1) & 1, p.err) && ok;
+        if (tid == 0 && ok) {
+            pend_u = -1;
+            pend_b[st] = -1;
+        }
         if (!ok) s_abort = 1;
-        const float gam = reinterpret_cast<const float*>(sm + kPB + (kPkgG - kPkgPartA))[m];
+        const float gam = reinterpret_cast<const float*>(sm + kGam + st * 512)[m];
         if (!mbar_wait(mma1, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
-        KDA_PHASE(17);
+        KDA_PHASE(16);
 
-        // Vt = U - X (hi and lo bf16 parts): thread owns value column j = m, rows r in
-        // [32 wg, 32 wg + 32)
+        // E1: Vt = U - X (hi and lo bf16 parts): value column j = m, rows [32 wg, 32 wg + 32)
         {
             const uint8_t* urow = sm + kUBuf + m * 256;
 #pragma unroll
@@ -1015,17 +1036,11 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        KDA_PHASE(18);
+        KDA_PHASE(17);
         if (s_abort) break;
-        if (tid == 0 && t + 1 < nch) {  // U of this chunk is consumed: fetch the next one
-            fence_async_smem();
-            mbar_expect_tx(ubar, kPkgUBytes);
-            bulk_g2s(sm + kUBuf, pkg_t + kPkgBytes + kPkgU, kPkgUBytes, ubar);
-            pend_u = (t + 1) & 1;
-        }
 
-        // dS = K~^T Vt (cols 128..255);  O^T += Vt^T A^T with both in hi + lo (cols 64..127)
         if (tid == 0) {
+            if (t + 1 < nch) issue_u(t + 1);  // U of this chunk is consumed
             tc_fence_after();
             constexpr uint32_t id2 = idesc_bf16(128, 128, true, false);
             constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
@@ -1040,85 +1055,83 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
                 const uint64_t vl = sdesc_sw128(sbase + kVtLo + ks * 32, 0, 1024);
                 const uint64_t ah = sdesc_sw128(sB + kPkgAQK + ks * 32, 0, 1024);
                 const uint64_t al = sdesc_sw128(sB + kPkgAQKLo + ks * 32, 0, 1024);
-                mma_bf16(tmem + 64, vh, ah, id3, 1);
-                mma_bf16(tmem + 64, vl, ah, id3, 1);
-                mma_bf16(tmem + 64, vh, al, id3, 1);
+                mma_bf16(tmem + out_col(t), vh, ah, id3, 1);
+                mma_bf16(tmem + out_col(t), vl, ah, id3, 1);
+                mma_bf16(tmem + out_col(t), vh, al, id3, 1);
             }
             mma_commit(mma3);
         }
         if (!mbar_wait(mma2, t & 1, p.err)) s_abort = 1;
         tc_fence_after();
-        KDA_PHASE(19);
+        KDA_PHASE(18);
 
-        // S <- gamma^C * S + dS ;  bf16 copy for the next chunk's MMAs
-        {
+        // E2: S <- gamma^C * S + dS ;  bf16 copy of S for the next chunk's MMAs
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + 128 + 64 * wg + 16 * g, v);
-                tmem_ld_wait();
+        for (int g = 0; g < 4; ++g) {
+            float v[16];
+            tmem_ld16(tmem + lane_base + 128 + 64 * wg + 16 * g, v);
+            tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gam, S[16 * g + e], v[e]);
-            }
-            write_sbf();
+            for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gam, S[16 * g + e], v[e]);
         }
-        if (!mbar_wait(mma3, t & 1, p.err)) s_abort = 1;
-        tc_fence_after();
-        if (tid == 0 && t + 1 < nch) {  // part B of this chunk is consumed
-            fence_async_smem();
-            mbar_expect_tx(fullB, kPkgPartB);
-            bulk_g2s(sm + kPB, pkg_t + kPkgBytes + kPkgPartA, kPkgPartB, fullB);
-            pend_b = (t + 1) & 1;
-        }
-        // output: O^T[j = m][r] for r in [32 wg, 32 wg + 32) -> O tile [r][j]
-        {
-            __nv_bfloat16* ot = reinterpret_cast<__nv_bfloat16*>(sm + kOt);
-#pragma unroll
-            for (int hx = 0; hx < 2; ++hx) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + 64 + 32 * wg + 16 * hx, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    ot[(32 * wg + 16 * hx + e) * kD + m] = __float2bfloat16_rn(v[e]);
-            }
-        }
+        write_sbf();
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
-        KDA_PHASE(20);
+        KDA_PHASE(19);
         if (s_abort) break;
-        // the valid rows of the O tile -> o, 16 bytes per store
-        {
-            __nv_bfloat16* obase = p.o + ((size_t)t0 * p.H + h) * kD;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int u = tid + kThreads * k, r = u >> 4, cc = u & 15;
-                if (r < L)
-                    *reinterpret_cast<uint4*>(obase + (size_t)r * p.H * kD + 8 * cc) =
-                        *reinterpret_cast<const uint4*>(sm + kOt + r * 256 + 16 * cc);
+        if (t + 1 < nch) {
+            wait_a(t + 1);
+            if (tid == 0) {
+                issue_mma1(t + 1);
+                // stage t & 1 of parts A and B is consumed once mma3(t) lands (below);
+                // chunk t + 2 goes there
             }
         }
+        // E3: O^T(t)[j = m][r], r in [32 wg, 32 wg + 32) -> o   (overlaps MMA1(t + 1))
+        if (!mbar_wait(mma3, t & 1, p.err)) s_abort = 1;
+        tc_fence_after();
+        if (tid == 0 && t + 2 < nch) issue_ab(t + 2);
+        {
+            __nv_bfloat16* orow = p.o + ((size_t)t0 * p.H + h) * kD + m;
+#pragma unroll
+            for (int hx = 0; hx < 2; ++hx) {
+                float v[16];
+                tmem_ld16(tmem + lane_base + out_col(t) + 32 * wg + 16 * hx, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int r = 32 * wg + 16 * hx + e;
+                    if (r < L) orow[(size_t)r * p.H * kD] = __float2bfloat16_rn(v[e]);
+                }
+            }
+        }
+        tc_fence_before();
+        KDA_PHASE(20);
     }
     KDA_PHASE_FLUSH();
+    __syncthreads();
     if (p.S_out && !s_abort) {
 #pragma unroll
         for (int jj = 0; jj < 64; jj += 4)
             *reinterpret_cast<float4*>(p.S_out + sbase_g + jj) =
                 make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
     }
-    // on an abort, let copies still in flight land before leaving
+    // on an abort, let copies and MMAs still in flight land before leaving
     if (tid == 0 && s_abort) {
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < 2; ++q) {
             if (pend_a[q] >= 0) mbar_wait(&fullA[q], pend_a[q], nullptr);
-        if (pend_b >= 0) mbar_wait(fullB, pend_b, nullptr);
+            if (pend_b[q] >= 0) mbar_wait(&fullB[q], pend_b[q], nullptr);
+        }
         if (pend_u >= 0) mbar_wait(ubar, pend_u, nullptr);
+        mma_commit(mma1);  // arrives once every MMA issued so far has completed
+        mbar_wait(mma1, mma1_commits & 1, nullptr);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 256);
+        tmem_dealloc(tmem, kStateTmemCols);
     }
 }
 
