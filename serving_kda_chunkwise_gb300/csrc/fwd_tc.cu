@@ -15,9 +15,10 @@
 //                 Gram matrices in ONE tcgen05 MMA, the UT solve on CUDA cores in fp32,
 //                 W and U by tcgen05; writes one "package" per (head, chunk) whose bytes
 //                 are the shared-memory image of the state kernel's MMA operands.
-//   state_kernel  one CTA per (sequence, head), serial over chunks: state S in fp32
-//                 registers, packages streamed in by bulk copies (double buffered),
-//                 X = S^T W^T, (Gamma Q S)^T, K~^T Vt and Vt A^T on tcgen05.
+//   state_kernel  two CTAs per (sequence, head), each owning 64 of the 128 value columns
+//                 (the columns of S evolve independently), serial over chunks: state S in
+//                 fp32 registers, packages streamed in by bulk copies (double buffered),
+//                 [W; Gamma Q] S, K~^T Vt and A Vt on tcgen05.
 //
 // Sub-tiling ("16-token tiles" of the same section; the bounded gate g > g_min is what
 // keeps these factors finite): the Gram entry for rows r >= i needs e^{G_r - G_i} per
@@ -48,9 +49,12 @@ constexpr int kD = 128;   // head dim (dk = dv)
 constexpr int kThreads = 256;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
-// part A (needed at the start of a chunk)
-constexpr uint32_t kPkgW = 0;         // W^T    [128 c][64 r] bf16 sw128: B = W^T MN-major
-constexpr uint32_t kPkgQB = 16384;    // Gam*Q  [64 r][128 c] bf16, K-major sw128
+// part A (needed at the start of a chunk): the row stack [W; Gam*Q] of the state kernel's
+// first MMA, K-major sw128, two 64-channel blocks of 16 KB, each W rows 0..63 then Gam*Q
+// rows 0..63 (128 B per row)
+constexpr uint32_t kPkgStk = 0;
+constexpr uint32_t kPkgStkBlk = 16384;
+constexpr uint32_t kPkgStkQ = 8192;   // Gam*Q rows within a block
 constexpr uint32_t kPkgPartA = 32768;
 // part B (needed from the middle of a chunk on)
 constexpr uint32_t kPkgKT = 32768;    // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
@@ -59,10 +63,11 @@ constexpr uint32_t kPkgAQKLo = 57344; // A lo   (A = hi + lo, bf16 each)
 constexpr uint32_t kPkgPartB = 32768;
 constexpr uint32_t kPkgG = 65536;     // gamma^C [128] fp32
 constexpr uint32_t kPkgGBytes = 512;
-// part C
-constexpr uint32_t kPkgU = 66048;     // U^T    [128 j][64 r] fp32, 16-byte chunk c of row j at
-                                      //        chunk position c ^ (j & 15)
-constexpr uint32_t kPkgUBytes = 32768;
+// part C: U = M V in fp32, two halves of 64 value columns, each [64 r][64 j] with the
+// 16-byte chunk c of row r at chunk position c ^ (r & 15)
+constexpr uint32_t kPkgU = 66048;
+constexpr uint32_t kPkgUHalf = 16384;
+constexpr uint32_t kPkgUBytes = 2 * kPkgUHalf;
 constexpr uint32_t kPkgBytes = kPkgU + kPkgUBytes;  // 98816
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -86,7 +91,17 @@ __device__ unsigned long long g_phase[32];
             for (int kda_i = 0; kda_i < 32; ++kda_i)                          \
                 if (kda_acc[kda_i]) atomicAdd(&g_phase[kda_i], kda_acc[kda_i]); \
     } while (0)
+// per-chunk event clocks of CTA 0 for chunks [100, 228), one slot per event
+__device__ long long g_trace[128][32];
+#define KDA_TRACE(t, slot)                                                  \
+    do {                                                                    \
+        if (blockIdx.x == 0 && (t) >= 100 && (t) < 228)                     \
+            g_trace[(t) - 100][(slot)] = clock64();                         \
+    } while (0)
 #else
+#define KDA_TRACE(t, slot) \
+    do {                   \
+    } while (0)
 #define KDA_PHASE_INIT() \
     do {                 \
     } while (0)
@@ -188,7 +203,7 @@ constexpr uint32_t kIntraSmem = kBars + 64 + 1024;  // + alignment slack
 static_assert(kIntraSmem <= 232448, "intra kernel exceeds the shared-memory limit");
 // reuse after the Gram MMAs: A hi -> A tile hi, lo (8 KB each) + M tile (8 KB);
 // B hi -> L, T, Y (fp32).
-// After the W/U MMAs the q / k slots of the current buffer stage W^T and U^T.
+// The M tile is stored twice (rows 0..63 and 64..127 of a 128-row operand).
 constexpr uint32_t kAqkTile = kAStk, kAqkLoTile = kAStk + 8192, kMTile = kAStk + 16384;
 constexpr int kLd = 65;                       // padded fp32 row stride of L and T
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4;
@@ -198,7 +213,7 @@ constexpr uint32_t kSolveScr = kALo;
 static_assert(4 * 3 * 16 * 20 * 4 <= 16384, "solve scratch must fit the A-lo region");
 // TMEM columns: main Gram accumulator [0, 160), diagonal-column lo correction [160, 224),
 // q-side lo correction [256, 416);
-// later W^T [0, 64) and U^T [64, 128).
+// later W [0, 128) and U [128, 256).
 constexpr uint32_t kTmemCols = 512, kTLo = 256, kTDiag = 160;
 
 __device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
@@ -257,16 +272,17 @@ __device__ __forceinline__ uint4 pk8(const float (&v)[8]) {
     return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
                       pack_bf16x2(v[6], v[7]));
 }
-// hi = bf16(v), lo = bf16(v - hi)
+// hi = bf16(v), lo = bf16(v - hi)  (the fp32 value of a packed bf16 is its bits shifted up)
 __device__ __forceinline__ void pk8_hilo(const float (&v)[8], uint4& hi, uint4& lo) {
-    float h[8], l[8];
+    uint32_t h[4], l[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        h[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
-        l[e] = v[e] - h[e];
+    for (int e = 0; e < 4; ++e) {
+        h[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
+        l[e] = pack_bf16x2(v[2 * e] - __uint_as_float(h[e] << 16),
+                           v[2 * e + 1] - __uint_as_float(h[e] & 0xffff0000u));
     }
-    hi = pk8(h);
-    lo = pk8(l);
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // ---- 16x16 fp32 tiles on the legacy warp-level tensor-core path (mma.sync, tf32 inputs,
@@ -471,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if (next + (int)gridDim.x < n_items) nx2 = decode_item(p, next + gridDim.x);
         uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
 
-        // the previous item's package stores read the A stack and the other q/k buffer
+        // the previous item's package store reads the A tiles
         if (tid == 0) bulk_wait_read0();
 
         // ---- gate and in-chunk cumsum (two-level scan over 16 row groups of 4 rows)
@@ -589,7 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) t[e] = qv[e] * e1[e] * Es[e];
-                *reinterpret_cast<uint4*>(pkg + kPkgQB + o64) = pk8(t);       // Gam*Q
+                *reinterpret_cast<uint4*>(pkg + kPkgStk + (cg >> 3) * kPkgStkBlk + kPkgStkQ +
+                                          sw128_chunk(r, cg & 7)) = pk8(t);     // Gam*Q
 #pragma unroll
                 for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e] * Fs[e];
                 *reinterpret_cast<uint4*>(pkg + kPkgKT + o64) = pk8(t);       // K*gamma^C/Gam
@@ -709,7 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             float* sScr = reinterpret_cast<float*>(sm + kSolveScr);
             solve_tril64(sL, sT, sScr, warp);
             KDA_PHASE(8);
-            // M = T Diag(beta) (lower triangle) as a bf16 K-major tile
+            // M = T Diag(beta) (lower triangle) as a bf16 K-major tile, written twice: the
+            // 128-row operand [M; M] of the W / U MMA
             {
                 const int r = tid >> 2, cq = tid & 3;
                 uint8_t* mt = sm + kMTile;
@@ -724,8 +742,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                             (i0 + 1 <= r) ? sT[r * kLd + i0 + 1] * sBeta[i0 + 1] : 0.f;
                         pw[e] = pack_bf16x2(m0, m1);
                     }
-                    *reinterpret_cast<uint4*>(mt + sw128_chunk(r, 2 * cq + hf)) =
-                        make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    const uint4 pk = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    *reinterpret_cast<uint4*>(mt + sw128_chunk(r, 2 * cq + hf)) = pk;
+                    *reinterpret_cast<uint4*>(mt + 8192 + sw128_chunk(r, 2 * cq + hf)) = pk;
                 }
             }
         }
@@ -734,7 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         __syncthreads();
         KDA_PHASE(5);
 
-        // ---- W^T = (Gam K)^T M^T  and  U^T = V^T M^T  (M = 128 channels, N = 64 rows)
+        // ---- W = M (Gam K) and U = M V: A = [M; M] (rows 64..127 repeat rows 0..63, so
+        //      every TMEM lane quadrant holds a copy of the 64 rows), N = 128 channels each
         if (mbar_wait(v_bar, iter & 1, p.err)) {
             if (tid == 0) pend_v = -1;
         } else {
@@ -742,13 +762,14 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         }
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
+            constexpr uint32_t idesc = idesc_bf16(128, 128, false, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t bm = sdesc_sw128(sbase + kMTile + ks * 32, 0, 1024);
-                mma_bf16(tmem, sdesc_sw128(sbase + kKbar + ks * 2048, 8192, 1024), bm, idesc, ks > 0);
-                mma_bf16(tmem + 64, sdesc_sw128(sbase + kVBuf + ks * 2048, 8192, 1024), bm, idesc,
+                const uint64_t am = sdesc_sw128(sbase + kMTile + ks * 32, 0, 1024);
+                mma_bf16(tmem, am, sdesc_sw128(sbase + kKbar + ks * 2048, 8192, 1024), idesc,
                          ks > 0);
+                mma_bf16(tmem + 128, am, sdesc_sw128(sbase + kVBuf + ks * 2048, 8192, 1024),
+                         idesc, ks > 0);
             }
             mma_commit(mma_bar);
         }
@@ -761,36 +782,36 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             pend_v = (iter + 1) & 1;
         }
         {
-            // warps 0-3: lane = channel c -> row c of the W^T tile (bf16 [128][64], sw128,
-            //            staged in the q slot); warps 4-7: lane = value column j -> row j of
-            //            U^T, fp32, written straight into the package.
-            const int m = 32 * (warp & 3) + lane;
-            if (warp < 4) {
+            // lane quadrants 0, 1: W rows (bf16) -> the package row stack; quadrants 2, 3:
+            // U rows (fp32) -> part C.  The warpgroup picks the 64-column half.
+            const int quad = warp & 3, wg = warp >> 2;
+            const int r = 32 * (quad & 1) + lane;
+            if (quad < 2) {
+                uint8_t* dst = pkg + kPkgStk + wg * kPkgStkBlk;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     float v[16];
-                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                    tmem_ld16(tmem + lane_base + 64 * wg + 16 * g, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
-                        const uint4 pk = make_uint4(pack_bf16x2(v[8 * hf], v[8 * hf + 1]),
-                                                    pack_bf16x2(v[8 * hf + 2], v[8 * hf + 3]),
-                                                    pack_bf16x2(v[8 * hf + 4], v[8 * hf + 5]),
-                                                    pack_bf16x2(v[8 * hf + 6], v[8 * hf + 7]));
-                        *reinterpret_cast<uint4*>(qk + kOffQ + sw128_chunk(m, 2 * g + hf)) = pk;
+                        float v8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v8[e] = v[8 * hf + e];
+                        *reinterpret_cast<uint4*>(dst + sw128_chunk(r, 2 * g + hf)) = pk8(v8);
                     }
                 }
             } else {
-                uint8_t* urow = pkg + kPkgU + m * 256;
+                uint8_t* urow = pkg + kPkgU + wg * kPkgUHalf + r * 256;
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
                     float v[16];
-                    tmem_ld16(tmem + lane_base + 64 + 16 * g, v);
+                    tmem_ld16(tmem + lane_base + 128 + 64 * wg + 16 * g, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int cidx = 4 * g + q;  // 16-byte chunk: r in [4 cidx, 4 cidx + 4)
-                        *reinterpret_cast<float4*>(urow + ((cidx ^ (m & 15)) << 4)) =
+                        const int cidx = 4 * g + q;  // 16-byte chunk: columns [4 cidx, 4 cidx + 4)
+                        *reinterpret_cast<float4*>(urow + ((cidx ^ (r & 15)) << 4)) =
                             make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                     }
                 }
@@ -802,7 +823,6 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         KDA_PHASE(6);
         if (s_abort) break;
         if (tid == 0) {
-            bulk_s2g(pkg + kPkgW, qk + kOffQ, 16384);
             bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 16384);  // A hi and lo
             bulk_commit();
         }
@@ -831,6 +851,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 // ================================================================ state ====
 
 struct StateParams {
+    CUtensorMap to;  // o as [T_total, H, 128] bf16, box 64 x 1 x 64, 128-byte swizzle
     const uint8_t* pkg;
     const int32_t* cu;
     const int32_t* chunk_off;
@@ -842,61 +863,107 @@ struct StateParams {
     int N, H, maxchunks;
 };
 
+// The value columns of S are independent (column j of S, X, Vt and O depends only on
+// column j of V and S0), so each (sequence, head) is served by kSplit CTAs of kJ columns.
+constexpr int kSplit = 2;
+constexpr int kJ = kD / kSplit;  // 64
+
 // shared-memory map of the state kernel (1024-aligned offsets)
-constexpr uint32_t kPA = 0;                    // package part A, two stages of 32 KB
-constexpr uint32_t kPB = 2 * kPkgPartA;        //  65536: package part B, two stages of 32 KB
-constexpr uint32_t kUBuf = kPB + 2 * kPkgPartB;// 131072: U^T fp32 [128 j][64 r] (one stage)
-constexpr uint32_t kSbf = kUBuf + kPkgUBytes;  // 163840: S bf16, A = S^T MN-major [2][128 i][128 B]
-constexpr uint32_t kVt = kSbf + 32768;         // 196608: Vt^T hi, K-major [128 j][64 r]
-constexpr uint32_t kVtLo = kVt + 16384;        // 212992: Vt^T lo
-constexpr uint32_t kGam = kVtLo + 16384;       // 229376: gamma^C, two stages of 512 B
-constexpr uint32_t kSBars = kGam + 1024;       // 230400
+constexpr uint32_t kPA = 0;                         // package part A, two stages of 32 KB
+constexpr uint32_t kPB = 2 * kPkgPartA;             //  65536: part B, two stages of 32 KB
+constexpr uint32_t kUS = kPB + 2 * kPkgPartB;       // 131072: U (own half), two stages of 16 KB
+constexpr uint32_t kVt = kUS + 2 * kPkgUHalf;       // 163840: Vt [64 r][64 j] bf16 MN-major,
+                                                    //         two stages of (hi 8 KB, lo 8 KB)
+constexpr uint32_t kSbf = kVt + 2 * 16384;          // 196608: S bf16 [128 i][64 j] MN-major
+constexpr uint32_t kGam = kSbf + 16384;             // 212992: gamma^C, two stages of 512 B
+constexpr uint32_t kOSt = kGam + 1024;              // 214016: O tile [64 r][64 j] bf16 sw128,
+                                                    //         the source of a TMA store
+constexpr uint32_t kSBars = kOSt + 8192;            // 222208
 constexpr uint32_t kStateSmem = kSBars + 128 + 1024;
 static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limit");
-// TMEM columns: X^T [0, 64); dS [128, 256); output accumulator, two buffers [64, 128), [256, 320)
-constexpr uint32_t kStateTmemCols = 512;
+// TMEM columns: D1 = [X; Gam Q S + A Vt] for chunk t in [64 (t & 1), 64 (t & 1) + 64);
+// dS = K~^T Vt in [128, 192)
+constexpr uint32_t kStateTmemCols = 256, kDS = 128;
 
-__device__ __forceinline__ uint32_t out_col(int t) { return (t & 1) ? 256u : 64u; }
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the OR of `pred` over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
 
-// One CTA per (sequence, head), 256 threads.  Per chunk t (package parts A, B double
-// buffered; U single buffered):
-//   [MMA1(t): X^T = S^T W^T and (Gam Q S)^T into out_col(t), issued at the end of t-1]
-//   E1(t):  Vt = U - X  (bf16 hi + lo)                      | waits mma1
-//   MMA2(t): dS = K~^T Vt        -> commit mma2
-//   MMA3(t): O^T += Vt^T A^T     -> commit mma3 (hi/lo products)
-//   E2(t):  S <- gamma S + dS, bf16 copy of S               | waits mma2
-//   MMA1(t+1) issued
-//   E3(t):  O(t) -> global                                  | waits mma3; overlaps MMA1(t+1)
-__global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p) {
+// 8 epilogue warps, two idle warps, an MMA warp and a copy warp: warp w runs on SM
+// sub-partition w % 4, and the X warps (sub-partitions 0, 1) must not share theirs with
+// the threads that issue MMAs and copies.
+constexpr int kStateThreads = 384;
+constexpr int kMmaT = 320;   // the MMA thread: lane 0 of warp 10
+constexpr int kCopyT = 352;  // the copy thread: lane 0 of warp 11
+
+// One CTA per (sequence, head, column half).  TMEM lanes 0..63 of D1 hold the rows of
+// X = W S, lanes 64..127 the rows of O; a warp reaches only the lane quadrant (warp % 4),
+// so warps 0, 1, 4, 5 ("X warps") form Vt, warps 2, 3, 6, 7 ("O warps") write O and all
+// eight epilogue warps update S (one state row i per lane, 32 columns per warpgroup).
+// One thread issues every MMA, another every bulk copy; the warps meet only on mbarriers
+// (no CTA-wide barrier inside the chunk loop), so nothing waits on MMA or copy issue.
+// Per chunk t:
+//   MMA1(t)  D1 = [W; Gam Q] S                                  | waits s_ready(t - 1)
+//   E1(t)    X warps: Vt = U - X -> bf16 hi + lo     | waits mma1 | -> vt_ready
+//   MMA2(t)  dS = K~^T Vt -> mma2, then the first half of MMA3(t): O rows += A Vt (hi/lo
+//            products), overlapping E2(t)
+//   E2(t)    epilogue warps: S <- gamma^C S + dS, bf16 copy of S  | waits mma2 | -> s_ready
+//   MMA1(t + 1) -> mma1, then the second half of MMA3(t) -> mma3, overlapping E1(t + 1)
+//   E3(t)    O warps: O(t) -> global, overlapping E1(t + 1)       | waits mma3
+// MMA3 uses a 128-row A operand whose first 64 rows are whatever precedes the A tile in
+// shared memory: they only add into the X lanes of D1, which are consumed by then.
+// Every barrier that a thread may fall behind on is per stage, so a parity never aliases.
+__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_constant__ StateParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
     uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2]
     uint64_t* fullB = fullA + 2;                                  // [2] (part B + gamma)
-    uint64_t* ubar = fullA + 4;
-    uint64_t* mma1 = fullA + 5;
-    uint64_t* mma2 = fullA + 6;
-    uint64_t* mma3 = fullA + 7;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 8);
+    uint64_t* ubar = fullA + 4;                                   // [2]
+    uint64_t* mma3 = fullA + 6;                                   // [2]
+    uint64_t* vt_ready = fullA + 8;                               // [2], 128 arrivals
+    uint64_t* mma1 = fullA + 10;
+    uint64_t* mma2 = fullA + 11;
+    uint64_t* s_ready = fullA + 12;                               // 256 arrivals
+    uint64_t* drain = fullA + 13;  // used once, to let MMAs in flight land on an abort
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 14);
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wg = tid >> 7;               // which half of the columns this thread owns
-    const int m = 32 * (warp & 3) + lane;  // TMEM lane = state row i / value column j
-    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const int nh = blockIdx.x, h = nh % p.H, n = nh / p.H;
+    const int quad = warp & 3, wg = (warp >> 2) & 1;
+    const int row = 32 * quad + lane;  // TMEM lane: state row i; X row (< 64) / O row - 64
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
+    const bool epi = warp < 8;
+    const bool xwarp = epi && quad < 2;
+    const bool owarp = epi && quad >= 2;
+    const int half = blockIdx.x % kSplit;
+    const int nh = blockIdx.x / kSplit, h = nh % p.H, n = nh / p.H;
+    const int jc = kJ * half + 32 * wg;  // first value column of this (epilogue) thread
+    volatile int* abort = &s_abort;
 
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(&fullA[i], 1);
+        for (int i = 0; i < 14; ++i) mbar_init(&fullA[i], 1);
+        mbar_init(&vt_ready[0], 128);
+        mbar_init(&vt_ready[1], 128);
+        mbar_init(s_ready, 256);
         fence_mbar_init();
         s_abort = 0;
     }
     if (warp == 0) tmem_alloc(tmem_slot, kStateTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     int64_t t_begin, t_end;
     seq_range(p.cu, n, p.N, p.T_total, nullptr, t_begin, t_end);
@@ -904,228 +971,307 @@ __global__ void __launch_bounds__(kThreads, 1) state_kernel(const StateParams p)
     const int nch = __ldg(p.chunk_off + n + 1) - c0;
     const uint8_t* pkg0 = p.pkg + ((size_t)h * p.maxchunks + c0) * kPkgBytes;
 
-    // S[i = m][64 wg + jj] in registers
-    float S[64];
-    const size_t sbase_g = ((size_t)nh * kD + m) * kD + 64 * wg;
+    // S[i = row][jc + jj], jj < 32, in registers of the epilogue warps
+    float S[32];
+    const size_t sofs = ((size_t)nh * kD + row) * kD + jc;
 #pragma unroll
-    for (int jj = 0; jj < 64; jj += 4) {
+    for (int jj = 0; jj < 32; jj += 4) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.S0) v = *reinterpret_cast<const float4*>(p.S0 + sbase_g + jj);
+        if (p.S0 && epi) v = *reinterpret_cast<const float4*>(p.S0 + sofs + jj);
         S[jj] = v.x; S[jj + 1] = v.y; S[jj + 2] = v.z; S[jj + 3] = v.w;
     }
     auto write_sbf = [&]() {
-        uint8_t* blk = sm + kSbf + wg * 16384;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            uint4 pk;
-            pk.x = pack_bf16x2(S[8 * ch], S[8 * ch + 1]);
-            pk.y = pack_bf16x2(S[8 * ch + 2], S[8 * ch + 3]);
-            pk.z = pack_bf16x2(S[8 * ch + 4], S[8 * ch + 5]);
-            pk.w = pack_bf16x2(S[8 * ch + 6], S[8 * ch + 7]);
-            *reinterpret_cast<uint4*>(blk + sw128_chunk(m, ch)) = pk;
-        }
-    };
-    // parity of the phase an in-flight copy will complete, or -1 (thread 0; for a clean abort)
-    int pend_a[2] = {-1, -1}, pend_b[2] = {-1, -1}, pend_u = -1;
-    auto issue_ab = [&](int t) {  // parts A and B (+ gamma) of chunk t into stage t & 1
-        const uint8_t* src = pkg0 + (size_t)t * kPkgBytes;
-        const int st = t & 1;
-        fence_async_smem();
-        mbar_expect_tx(&fullA[st], kPkgPartA);
-        bulk_g2s(sm + kPA + st * kPkgPartA, src, kPkgPartA, &fullA[st]);
-        mbar_expect_tx(&fullB[st], kPkgPartB + kPkgGBytes);
-        bulk_g2s(sm + kPB + st * kPkgPartB, src + kPkgKT, kPkgPartB, &fullB[st]);
-        bulk_g2s(sm + kGam + st * 512, src + kPkgG, kPkgGBytes, &fullB[st]);
-        pend_a[st] = pend_b[st] = (t >> 1) & 1;
-    };
-    auto issue_u = [&](int t) {
-        fence_async_smem();
-        mbar_expect_tx(ubar, kPkgUBytes);
-        bulk_g2s(sm + kUBuf, pkg0 + (size_t)t * kPkgBytes + kPkgU, kPkgUBytes, ubar);
-        pend_u = t & 1;
-    };
-    int mma1_commits = 0;  // thread 0: commits issued on mma1 (to drain MMAs on an abort)
-    auto issue_mma1 = [&](int t) {  // X^T and (Gam Q S)^T of chunk t (thread 0)
-        tc_fence_after();
-        ++mma1_commits;
-        const uint32_t sA = sbase + kPA + (t & 1) * kPkgPartA;
-        constexpr uint32_t idesc = idesc_bf16(128, 64, true, false);
-        constexpr uint32_t idesc_w = idesc_bf16(128, 64, true, true);
+        for (int cc = 0; cc < 4; ++cc) {
+            float v8[8];
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
-            mma_bf16(tmem, a, sdesc_sw128(sA + kPkgW + ks * 2048, 8192, 1024), idesc_w, ks > 0);
-        }
-        mma_commit(mma1);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint64_t a = sdesc_sw128(sbase + kSbf + ks * 2048, 16384, 1024);
-            const uint32_t kb = (ks >> 2) * 8192 + (ks & 3) * 32;
-            mma_bf16(tmem + out_col(t), a, sdesc_sw128(sA + kPkgQB + kb, 0, 1024), idesc, ks > 0);
+            for (int e = 0; e < 8; ++e) v8[e] = S[8 * cc + e];
+            *reinterpret_cast<uint4*>(sm + kSbf + sw128_chunk(row, 4 * wg + cc)) = pk8(v8);
         }
     };
-    auto wait_a = [&](int t) {
-        if (mbar_wait(&fullA[t & 1], (t >> 1) & 1, p.err)) {
-            if (tid == 0) pend_a[t & 1] = -1;
-        } else {
-            s_abort = 1;
-        }
-    };
-
-    write_sbf();
-    if (tid == 0 && nch > 0) {
-        issue_ab(0);
-        issue_u(0);
-        if (nch > 1) issue_ab(1);
-    }
+    if (epi) write_sbf();
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (nch > 0) {
-        wait_a(0);
-        if (tid == 0) issue_mma1(0);
-    }
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
 
-    int t = 0;
-    KDA_PHASE_INIT();
-    for (; t < nch; ++t) {
-        const int st = t & 1;
-        const uint32_t sB = sbase + kPB + st * kPkgPartB - kPkgKT;  // sB + kPkgKT = part B
-        const int64_t t0 = t_begin + (int64_t)t * kC;
-        const int L = (int)((t_end - t0) < kC ? (t_end - t0) : kC);
-        if (tid == 0 && t + 2 < nch)  // warm L2 with the package after next
-            l2_prefetch(pkg0 + (size_t)(t + 2) * kPkgBytes, kPkgBytes);
-        bool ok = mbar_wait(ubar, t & 1, p.err);
-        ok = mbar_wait(&fullB[st], (t >> 1) & 1, p.err) && ok;
-        if (tid == 0 && ok) {
-            pend_u = -1;
-            pend_b[st] = -1;
-        }
-        if (!ok) s_abort = 1;
-        const float gam = reinterpret_cast<const float*>(sm + kGam + st * 512)[m];
-        if (!mbar_wait(mma1, t & 1, p.err)) s_abort = 1;
-        tc_fence_after();
-        KDA_PHASE(16);
-
-        // E1: Vt = U - X (hi and lo bf16 parts): value column j = m, rows [32 wg, 32 wg + 32)
-        {
-            const uint8_t* urow = sm + kUBuf + m * 256;
+    if (tid == kMmaT && nch > 0) {
+        // ------------------------------------------------------------ MMA thread
+        auto issue_mma1 = [&](int t) {  // D1(t) = [W; Gam Q] S
+            const uint32_t sA = sbase + kPA + (t & 1) * kPkgPartA;
+            constexpr uint32_t id = idesc_bf16(128, kJ, false, true);
 #pragma unroll
-            for (int hx = 0; hx < 2; ++hx) {
-                float x[16];
-                tmem_ld16(tmem + lane_base + 32 * wg + 16 * hx, x);
-                tmem_ld_wait();
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {  // 8 rows: r0 = 32 wg + 16 hx + 8 cc
-                    const int c4 = 8 * wg + 4 * hx + 2 * cc;  // fp32 chunk index of r0
-                    const float4 ua = *reinterpret_cast<const float4*>(urow + ((c4 ^ (m & 15)) << 4));
-                    const float4 ub =
-                        *reinterpret_cast<const float4*>(urow + (((c4 + 1) ^ (m & 15)) << 4));
-                    const float u[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
-                    float d8[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) d8[e] = u[e] - x[8 * cc + e];
-                    uint4 hi, lo;
-                    pk8_hilo(d8, hi, lo);
-                    const uint32_t off = sw128_chunk(m, 4 * wg + 2 * hx + cc);
-                    *reinterpret_cast<uint4*>(sm + kVt + off) = hi;
-                    *reinterpret_cast<uint4*>(sm + kVtLo + off) = lo;
-                }
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint64_t a =
+                    sdesc_sw128(sA + (ks >> 2) * kPkgStkBlk + (ks & 3) * 32, 0, 1024);
+                const uint64_t b = sdesc_sw128(sbase + kSbf + ks * 2048, 0, 1024);
+                mma_bf16(tmem + 64u * (t & 1), a, b, id, ks > 0);
             }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        KDA_PHASE(17);
-        if (s_abort) break;
-
-        if (tid == 0) {
-            if (t + 1 < nch) issue_u(t + 1);  // U of this chunk is consumed
+            mma_commit(mma1);
+        };
+        // MMA3(t), K steps [ks0, ks0 + 2): A_hi Vt_hi + A_hi Vt_lo + A_lo Vt_hi into the O
+        // rows.  The 128-row A operand is [rows before the tile; A]: A hi is preceded by K~
+        // block 1, A lo by A hi.
+        auto issue_mma3 = [&](int t, int ks0) {
+            const uint32_t sB = sbase + kPB + (t & 1) * kPkgPartB;
+            const uint32_t sVt = sbase + kVt + (t & 1) * 16384;
+            const uint32_t sAh = sB + (kPkgAQK - kPkgKT) - 8192;
+            const uint32_t sAl = sB + (kPkgAQKLo - kPkgKT) - 8192;
+            constexpr uint32_t id3 = idesc_bf16(128, kJ, false, true);
+            const uint32_t d = tmem + 64u * (t & 1);
+#pragma unroll
+            for (int ks = ks0; ks < ks0 + 2; ++ks) {
+                const uint64_t ah = sdesc_sw128(sAh + ks * 32, 0, 1024);
+                const uint64_t al = sdesc_sw128(sAl + ks * 32, 0, 1024);
+                const uint64_t vh = sdesc_sw128(sVt + ks * 2048, 0, 1024);
+                const uint64_t vl = sdesc_sw128(sVt + 8192 + ks * 2048, 0, 1024);
+                mma_bf16(d, ah, vh, id3, 1);
+                mma_bf16(d, ah, vl, id3, 1);
+                mma_bf16(d, al, vh, id3, 1);
+            }
+        };
+        int t = 0;
+        for (; t < nch; ++t) {
+            const int st = t & 1;
+            const uint32_t ph = (t >> 1) & 1;
+            if (t > 0 && !mbar_wait_ab(s_ready, (t - 1) & 1, p.err, abort)) break;
+            KDA_TRACE(t, 10);
             tc_fence_after();
-            constexpr uint32_t id2 = idesc_bf16(128, 128, true, false);
-            constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
+            if (!mbar_wait_ab(&fullA[st], ph, p.err, abort)) break;
+            KDA_TRACE(t, 11);
+            issue_mma1(t);
+            KDA_TRACE(t, 12);
+            if (t > 0) {
+                issue_mma3(t - 1, 2);
+                mma_commit(&mma3[(t - 1) & 1]);
+            }
+            KDA_TRACE(t, 13);
+            if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
+            KDA_TRACE(t, 14);
+            tc_fence_after();
+            if (!mbar_wait_ab(&fullB[st], ph, p.err, abort)) break;
+            KDA_TRACE(t, 15);
+            const uint32_t sB = sbase + kPB + st * kPkgPartB;
+            const uint32_t sVt = sbase + kVt + st * 16384;
+            constexpr uint32_t id2 = idesc_bf16(128, kJ, true, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + 128, sdesc_sw128(sB + kPkgKT + ks * 2048, 8192, 1024),
-                         sdesc_sw128(sbase + kVt + ks * 32, 0, 1024), id2, ks > 0);
-            mma_commit(mma2);  // the state update waits only for this
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t vh = sdesc_sw128(sbase + kVt + ks * 32, 0, 1024);
-                const uint64_t vl = sdesc_sw128(sbase + kVtLo + ks * 32, 0, 1024);
-                const uint64_t ah = sdesc_sw128(sB + kPkgAQK + ks * 32, 0, 1024);
-                const uint64_t al = sdesc_sw128(sB + kPkgAQKLo + ks * 32, 0, 1024);
-                mma_bf16(tmem + out_col(t), vh, ah, id3, 1);
-                mma_bf16(tmem + out_col(t), vl, ah, id3, 1);
-                mma_bf16(tmem + out_col(t), vh, al, id3, 1);
-            }
-            mma_commit(mma3);
+                mma_bf16(tmem + kDS, sdesc_sw128(sB + ks * 2048, 8192, 1024),
+                         sdesc_sw128(sVt + ks * 2048, 0, 1024), id2, ks > 0);
+            mma_commit(mma2);
+            KDA_TRACE(t, 16);
+            issue_mma3(t, 0);
+            KDA_TRACE(t, 17);
         }
-        if (!mbar_wait(mma2, t & 1, p.err)) s_abort = 1;
-        tc_fence_after();
-        KDA_PHASE(18);
+        if (t == nch) {
+            issue_mma3(nch - 1, 2);
+            mma_commit(&mma3[(nch - 1) & 1]);
+        }
+    }
 
-        // E2: S <- gamma^C * S + dS ;  bf16 copy of S for the next chunk's MMAs
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            float v[16];
-            tmem_ld16(tmem + lane_base + 128 + 64 * wg + 16 * g, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) S[16 * g + e] = fmaf(gam, S[16 * g + e], v[e]);
+    // the last chunk whose copy was issued into each stage (copy thread), for a drain
+    int lastA[2] = {-1, -1}, lastB[2] = {-1, -1}, lastU[2] = {-1, -1};
+    if (tid == kCopyT && nch > 0) {
+        // ----------------------------------------------------------- copy thread
+        auto issue_a = [&](int t) {
+            const int st = t & 1;
+            mbar_expect_tx(&fullA[st], kPkgPartA);
+            bulk_g2s(sm + kPA + st * kPkgPartA, pkg0 + (size_t)t * kPkgBytes, kPkgPartA,
+                     &fullA[st]);
+            lastA[st] = t;
+        };
+        auto issue_b = [&](int t) {
+            const int st = t & 1;
+            const uint8_t* src = pkg0 + (size_t)t * kPkgBytes;
+            mbar_expect_tx(&fullB[st], kPkgPartB + kPkgGBytes);
+            bulk_g2s(sm + kPB + st * kPkgPartB, src + kPkgKT, kPkgPartB, &fullB[st]);
+            bulk_g2s(sm + kGam + st * 512, src + kPkgG, kPkgGBytes, &fullB[st]);
+            lastB[st] = t;
+        };
+        auto issue_u = [&](int t) {
+            const int st = t & 1;
+            mbar_expect_tx(&ubar[st], kPkgUHalf);
+            bulk_g2s(sm + kUS + st * kPkgUHalf,
+                     pkg0 + (size_t)t * kPkgBytes + kPkgU + half * kPkgUHalf, kPkgUHalf,
+                     &ubar[st]);
+            lastU[st] = t;
+        };
+        for (int t = 0; t < 2 && t < nch; ++t) {
+            issue_a(t);
+            issue_u(t);
+            issue_b(t);
         }
-        write_sbf();
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        KDA_PHASE(19);
-        if (s_abort) break;
-        if (t + 1 < nch) {
-            wait_a(t + 1);
-            if (tid == 0) {
-                issue_mma1(t + 1);
-                // stage t & 1 of parts A and B is consumed once mma3(t) lands (below);
-                // chunk t + 2 goes there
+        for (int t = 0; t + 2 < nch; ++t) {
+            const int st = t & 1;
+            const uint32_t ph = (t >> 1) & 1;
+            if (t + 3 < nch) l2_prefetch(pkg0 + (size_t)(t + 3) * kPkgBytes, kPkgBytes);
+            // E1(t) has read stage st of U, and MMA1(t) (which E1 waited for) of part A
+            if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
+            KDA_TRACE(t, 18);
+            issue_u(t + 2);
+            issue_a(t + 2);
+            KDA_TRACE(t, 19);
+            // MMA2(t) and MMA3(t) have read stage st of part B; E2(t) has read gamma
+            if (!mbar_wait_ab(&mma3[st], ph, p.err, abort)) break;
+            KDA_TRACE(t, 20);
+            issue_b(t + 2);
+            KDA_TRACE(t, 21);
+        }
+    }
+
+    if (epi) {
+        // ------------------------------------------------------- epilogue warps
+        KDA_PHASE_INIT();
+        for (int t = 0; t < nch; ++t) {
+            const int st = t & 1;
+            const uint32_t ph = (t >> 1) & 1;
+            const uint32_t d1 = 64u * st;
+            const int64_t t0 = t_begin + (int64_t)t * kC;
+            if (xwarp) {
+                if (!mbar_wait_ab(mma1, t & 1, p.err, abort)) break;
+                if (tid == 0) KDA_TRACE(t, 0);
+                KDA_PHASE(21);
+                if (!mbar_wait_ab(&ubar[st], ph, p.err, abort)) break;
+                tc_fence_after();
+                if (tid == 0) KDA_TRACE(t, 1);
+                KDA_PHASE(16);
+                // E1: Vt = U - X for row r = row, columns [32 wg, 32 wg + 32) of this half
+                const uint8_t* urow = sm + kUS + st * kPkgUHalf + row * 256;
+                uint8_t* vt = sm + kVt + st * 16384;
+                float xx[2][16];
+                tmem_ld16(tmem + lane_base + d1 + 32 * wg, xx[0]);
+                tmem_ld16(tmem + lane_base + d1 + 32 * wg + 16, xx[1]);
+                tmem_ld_wait();
+                if (tid == 0) KDA_TRACE(t, 2);
+#pragma unroll
+                for (int hx = 0; hx < 2; ++hx) {
+                    const float* x = xx[hx];
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        const int c4 = 8 * wg + 4 * hx + 2 * cc;  // fp32 chunk of the 8 columns
+                        const float4 ua =
+                            *reinterpret_cast<const float4*>(urow + ((c4 ^ (row & 15)) << 4));
+                        const float4 ub = *reinterpret_cast<const float4*>(
+                            urow + (((c4 + 1) ^ (row & 15)) << 4));
+                        const float d8[8] = {ua.x - x[8 * cc], ua.y - x[8 * cc + 1],
+                                             ua.z - x[8 * cc + 2], ua.w - x[8 * cc + 3],
+                                             ub.x - x[8 * cc + 4], ub.y - x[8 * cc + 5],
+                                             ub.z - x[8 * cc + 6], ub.w - x[8 * cc + 7]};
+                        uint4 hi, lo;
+                        pk8_hilo(d8, hi, lo);
+                        const uint32_t off = sw128_chunk(row, 4 * wg + 2 * hx + cc);
+                        *reinterpret_cast<uint4*>(vt + off) = hi;
+                        *reinterpret_cast<uint4*>(vt + 8192 + off) = lo;
+                    }
+                    if (tid == 0 && hx == 0) KDA_TRACE(t, 22);
+                }
+                if (tid == 0) KDA_TRACE(t, 23);
+                fence_async_smem();
+                if (tid == 0) KDA_TRACE(t, 24);
+                tc_fence_before();
+                mbar_arrive(&vt_ready[st]);
+                if (tid == 0) KDA_TRACE(t, 3);
+                KDA_PHASE(17);
             }
-        }
-        // E3: O^T(t)[j = m][r], r in [32 wg, 32 wg + 32) -> o   (overlaps MMA1(t + 1))
-        if (!mbar_wait(mma3, t & 1, p.err)) s_abort = 1;
-        tc_fence_after();
-        if (tid == 0 && t + 2 < nch) issue_ab(t + 2);
-        {
-            __nv_bfloat16* orow = p.o + ((size_t)t0 * p.H + h) * kD + m;
-#pragma unroll
-            for (int hx = 0; hx < 2; ++hx) {
-                float v[16];
-                tmem_ld16(tmem + lane_base + out_col(t) + 32 * wg + 16 * hx, v);
+            // The O warps meet on a named barrier below, so they leave the loop only together
+            // (by a vote at its end); the X warps leave at the first wait that fails.
+            bool ok = mbar_wait_ab(mma2, t & 1, p.err, abort) &&
+                      mbar_wait_ab(&fullB[st], ph, p.err, abort);  // gamma^C of this chunk
+            if (xwarp && !ok) break;
+            tc_fence_after();
+            if (tid == 0) KDA_TRACE(t, 4);
+            if (tid == 64) KDA_TRACE(t, 6);
+            KDA_PHASE(18);
+            // E2: S <- gamma^C * S + dS ;  bf16 copy of S for the next chunk's MMA1
+            {
+                const float gam = reinterpret_cast<const float*>(sm + kGam + st * 512)[row];
+                float v[2][16];
+                tmem_ld16(tmem + lane_base + kDS + 32 * wg, v[0]);
+                tmem_ld16(tmem + lane_base + kDS + 32 * wg + 16, v[1]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int r = 32 * wg + 16 * hx + e;
-                    if (r < L) orow[(size_t)r * p.H * kD] = __float2bfloat16_rn(v[e]);
-                }
-            }
-        }
-        tc_fence_before();
-        KDA_PHASE(20);
-    }
-    KDA_PHASE_FLUSH();
-    __syncthreads();
-    if (p.S_out && !s_abort) {
+                for (int hx = 0; hx < 2; ++hx)
 #pragma unroll
-        for (int jj = 0; jj < 64; jj += 4)
-            *reinterpret_cast<float4*>(p.S_out + sbase_g + jj) =
+                    for (int e = 0; e < 16; ++e) S[16 * hx + e] = fmaf(gam, S[16 * hx + e], v[hx][e]);
+                write_sbf();
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(s_ready);
+            if (tid == 0) KDA_TRACE(t, 5);
+            if (tid == 64) KDA_TRACE(t, 7);
+            KDA_PHASE(19);
+            if (owarp) {
+                // E3: O rows r = row - 64, columns [jc, jc + 32) -> o
+                ok = ok && mbar_wait_ab(&mma3[st], ph, p.err, abort);
+                tc_fence_after();
+                if (tid == 64) KDA_TRACE(t, 8);
+                const int r = row - 64;
+                float v[2][16];
+                tmem_ld16(tmem + lane_base + d1 + 32 * wg, v[0]);
+                tmem_ld16(tmem + lane_base + d1 + 32 * wg + 16, v[1]);
+                tmem_ld_wait();
+                if (t0 + kC <= t_end) {
+                    // full chunk: stage the 64 x 64 tile, one TMA store writes it
+                    if (tid == 64) bulk_wait_read0();  // the previous store has read the tile
+                    named_bar_sync(2, 128);
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        float a8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) a8[e] = v[q8 >> 1][8 * (q8 & 1) + e];
+                        *reinterpret_cast<uint4*>(sm + kOSt + sw128_chunk(r, 4 * wg + q8)) =
+                            pk8(a8);
+                    }
+                    fence_async_smem();
+                    if (named_bar_or(2, 128, !ok)) break;
+                    if (tid == 64) {
+                        tma_store_3d(&p.to, sm + kOSt, kJ * half, h, (int)t0);
+                        bulk_commit();
+                    }
+                } else {
+                    if (named_bar_or(2, 128, !ok)) break;
+                    // ragged last chunk of a sequence: rows past its end belong to the next
+                    if (t0 + r < t_end) {
+                        __nv_bfloat16* orow = p.o + ((size_t)(t0 + r) * p.H + h) * kD + jc;
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            float a8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) a8[e] = v[q8 >> 1][8 * (q8 & 1) + e];
+                            *reinterpret_cast<uint4*>(orow + 8 * q8) = pk8(a8);
+                        }
+                    }
+                }
+                tc_fence_before();
+                if (tid == 64) KDA_TRACE(t, 9);
+            }
+            KDA_PHASE(20);
+        }
+        KDA_PHASE_FLUSH();
+    }
+
+    if (tid == 64) bulk_wait0();  // the output tile stores are complete
+    __syncthreads();
+    const bool aborted = s_abort != 0;
+    if (p.S_out && !aborted && epi) {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 4)
+            *reinterpret_cast<float4*>(p.S_out + sofs + jj) =
                 make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
     }
     // on an abort, let copies and MMAs still in flight land before leaving
-    if (tid == 0 && s_abort) {
+    if (aborted && tid == kCopyT) {
         for (int q = 0; q < 2; ++q) {
-            if (pend_a[q] >= 0) mbar_wait(&fullA[q], pend_a[q], nullptr);
-            if (pend_b[q] >= 0) mbar_wait(&fullB[q], pend_b[q], nullptr);
+            if (lastA[q] >= 0) mbar_wait(&fullA[q], (lastA[q] >> 1) & 1, nullptr);
+            if (lastB[q] >= 0) mbar_wait(&fullB[q], (lastB[q] >> 1) & 1, nullptr);
+            if (lastU[q] >= 0) mbar_wait(&ubar[q], (lastU[q] >> 1) & 1, nullptr);
         }
-        if (pend_u >= 0) mbar_wait(ubar, pend_u, nullptr);
-        mma_commit(mma1);  // arrives once every MMA issued so far has completed
-        mbar_wait(mma1, mma1_commits & 1, nullptr);
+    }
+    if (aborted && tid == kMmaT) {
+        mma_commit(drain);  // arrives once every MMA issued so far has completed
+        mbar_wait(drain, 0, nullptr);
     }
     tc_fence_before();
     __syncthreads();
@@ -1167,6 +1313,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
 }  // namespace
 
 #ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_trace(long long* out, int n) {
+    if (n > 128 * 32) n = 128 * 32;
+    return cudaMemcpyFromSymbol(out, g_trace, n * sizeof(long long)) == cudaSuccess ? n : -1;
+}
 extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
     if (n > 32) n = 32;
     if (cudaMemcpyFromSymbol(out, g_phase, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
@@ -1224,6 +1374,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     }
 
     StateParams sp;
+    if (a.T_total > 0 && !make_map(&sp.to, a.o, a.T_total, a.H)) return cudaErrorInvalidValue;
     sp.pkg = pkg;
     sp.cu = a.cu_seqlens;
     sp.chunk_off = chunk_off;
@@ -1240,7 +1391,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     if (e != cudaSuccess) return e;
     {
         ProfScope prof("state_kernel", a.stream);
-        state_kernel<<<a.N * a.H, kThreads, kStateSmem, a.stream>>>(sp);
+        state_kernel<<<a.N * a.H * kSplit, kStateThreads, kStateSmem, a.stream>>>(sp);
     }
     return cudaGetLastError();
 }

@@ -78,6 +78,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
     return true;
 }
 
+// As mbar_wait, but also gives up (returning false) once *abort is set by another thread;
+// a wait that runs out sets *abort itself.
+__device__ __forceinline__ bool mbar_wait_ab(uint64_t* bar, uint32_t parity, unsigned* err,
+                                             volatile int* abort) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait(addr, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(addr, parity)) {
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            if (err) atomicOr(err, kDevErrTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// Plain arrive (release at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // --------------------------------------------------------------- TMA / bulk --
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,
@@ -86,6 +109,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// TMA store of a tile from shared memory (this thread's bulk group).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
+                                             int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
         : "memory");
 }
 
