@@ -121,6 +121,25 @@ def source_hash(*relpaths):
     return h.hexdigest()
 
 
+# ----------------------------------------------------------- multi-rank --
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); identity when there is
+    no process group.  The reduction runs on `device` for NCCL, on the host for gloo."""
+    if dist is None:
+        return value
+    import torch
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return world * units_per_rank_step * steps / (ms / 1e3)
+
+
 # ---------------------------------------------------------------- oracle --
 
 def oracle_sample(heads: int, tokens: int, nthreads: int, min_seconds: float = 0.0,
@@ -184,7 +203,9 @@ def run_ours(args, rank, world, local_rank, dist):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
-    sp = inputs.workload_spec(WORKLOAD, seed=1002 + 7919 * rank)
+    kw = {"H": args.heads} if args.heads else {}
+    sp = inputs.workload_spec(WORKLOAD, seed=1002 + 7919 * rank, **kw)
+    H = sp.H
     d = sp.to_device(dev)
     stream = torch.cuda.current_stream(dev)
     S_out = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
@@ -223,12 +244,9 @@ def run_ours(args, rank, world, local_rank, dist):
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     kda.device_status(stream)
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     ms_per_step = ms / args.steps
-    tok_s = world * T * args.steps / (ms / 1e3)
+    tok_s = job_rate(world, T, args.steps, ms)
     tflops_causal = world * T * H * FLOP_CAUSAL * args.steps / (ms / 1e3) / 1e12
     tflops_dense = world * T * H * FLOP_DENSE * args.steps / (ms / 1e3) / 1e12
 
@@ -288,12 +306,8 @@ def run_ours(args, rank, world, local_rank, dist):
         e2e_step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = ev0.elapsed_time(ev1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * T * e2e_steps / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+    e2e = {"value": job_rate(world, T, e2e_steps, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
     del dd, host
 
@@ -366,7 +380,9 @@ def bench_decode(args, dev, stream, peaks):
     gbs = step_bytes / (us / 1e6) / 1e9
     return {"us_per_step": us, "GB_per_step": step_bytes / 1e9, "GB_s": gbs,
             "frac_hbm": gbs / peaks["hbm_gbs"], "steps": n, "N": N, "H": Hd, "d": dk,
-            "kernel": "decode_kernel"}
+            "kernel": "decode_kernel",
+            "traffic": traffic_from_profile(
+                "decode_kernel", source_hash("serving_kda_chunkwise_gb300/csrc/decode.cu"))}
 
 
 def main():
@@ -378,6 +394,9 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=0,
+                    help="run the forward workload with this many heads instead of 32 (a "
+                         "smaller case for profiler captures; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
