@@ -98,7 +98,17 @@ __device__ long long g_trace[128][32];
         if (blockIdx.x == 0 && (t) >= 100 && (t) < 228)                     \
             g_trace[(t) - 100][(slot)] = clock64();                         \
     } while (0)
+// per-warp event clocks of intra CTA 0, items [10, 26) of its sequence
+__device__ long long g_itrace[16][16][8];
+#define KDA_ITRACE(it, slot)                                                          \
+    do {                                                                              \
+        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (it) >= 10 && (it) < 26)    \
+            g_itrace[(it) - 10][threadIdx.x >> 5][(slot)] = clock64();               \
+    } while (0)
 #else
+#define KDA_ITRACE(it, slot) \
+    do {                     \
+    } while (0)
 #define KDA_TRACE(t, slot) \
     do {                   \
     } while (0)
@@ -115,9 +125,22 @@ __device__ long long g_trace[128][32];
 
 // ================================================================= plan ====
 
+// Sequence n holding global chunk `chunk` (largest n with chunk_off[n] <= chunk).
+__device__ __forceinline__ int find_seq(const int32_t* chunk_off, int N, int chunk) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (chunk_off[mid] <= chunk) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Chunk offsets of every sequence (exclusive scan of ceil(len / 64)), then one table entry
+// per global chunk: {t0 low, t0 high, sequence, rows}, so that a consumer decodes a chunk
+// with one 16-byte load.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int N,
                                                     int64_t T_total, int32_t* chunk_off,
-                                                    unsigned* err) {
+                                                    int4* chunk_tab, unsigned* err) {
     __shared__ int32_t s_warp[32];
     __shared__ int32_t s_carry;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -156,16 +179,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         __syncthreads();
     }
     if (tid == 0) chunk_off[N] = s_carry;
-}
-
-// Sequence n holding global chunk `chunk` (largest n with chunk_off[n] <= chunk).
-__device__ __forceinline__ int find_seq(const int32_t* chunk_off, int N, int chunk) {
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(chunk_off + mid) <= chunk) lo = mid; else hi = mid - 1;
+    __syncthreads();
+    const int total = s_carry;
+    for (int c = tid; c < total; c += blockDim.x) {
+        const int n = find_seq(chunk_off, N, c);
+        int64_t b, e;
+        seq_range(cu, n, N, T_total, nullptr, b, e);
+        const int64_t t0 = b + (int64_t)(c - chunk_off[n]) * kC;
+        const int64_t rem = e - t0;
+        chunk_tab[c] = make_int4(static_cast<int>(t0 & 0xffffffff), static_cast<int>(t0 >> 32), n,
+                                 static_cast<int>(rem < kC ? rem : kC));
     }
-    return lo;
 }
 
 // ================================================================ intra ====
@@ -176,6 +200,7 @@ struct IntraParams {
     const float* A_log;
     const int32_t* cu;
     const int32_t* chunk_off;
+    const int4* chunk_tab;
     uint8_t* pkg;
     unsigned* err;
     int64_t T_total;
@@ -191,7 +216,7 @@ constexpr uint32_t kOffQ = 0, kOffK = 16384;
 constexpr uint32_t kVBuf = 2 * kQKBuf;        //  65536: v   [2 blk][64 rows][128 B]
 constexpr uint32_t kZBuf = kVBuf + 16384;     //  81920: z
 constexpr uint32_t kKbar = kZBuf + 16384;     //  98304: Gam*K (A of W = M Gam K, MN-major);
-                                              //         earlier: cumsum block totals fp32[16][128]
+                                              //         earlier: per-warp cumsum totals fp32[8][128]
 constexpr uint32_t kAStk = kKbar + 16384;     // 114688: A hi [2 blk][128 rows][128 B]
 constexpr uint32_t kALo = kAStk + 32768;      // 147456: q-side A lo [2 blk][64 rows][128 B]
 constexpr uint32_t kBStk = kALo + 16384;      // 163840: B hi [2 blk][160 rows][128 B]
@@ -224,16 +249,17 @@ struct ItemInfo {
     size_t pkg;  // package index
 };
 
-__device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item) {
+// Item = chunk * H + head.  The table entry is fetched ahead and decoded when needed.
+__device__ __forceinline__ int4 fetch_item(const IntraParams& p, int item) {
+    return __ldg(p.chunk_tab + item / p.H);
+}
+__device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item, int4 e) {
     ItemInfo it;
     const int chunk = item / p.H;
     it.h = item - chunk * p.H;
-    it.n = find_seq(p.chunk_off, p.N, chunk);
-    int64_t b, e;
-    seq_range(p.cu, it.n, p.N, p.T_total, nullptr, b, e);
-    it.t0 = b + (int64_t)(chunk - __ldg(p.chunk_off + it.n)) * kC;
-    const int64_t rem = e - it.t0;
-    it.L = (int)(rem < kC ? rem : kC);
+    it.n = e.z;
+    it.t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
+    it.L = e.w;
     it.pkg = (size_t)it.h * p.maxchunks + chunk;
     return it;
 }
@@ -422,9 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    float* tot = reinterpret_cast<float*>(sm + kKbar);   // [16][128] cumsum block totals
+    float* tot = reinterpret_cast<float*>(sm + kKbar);   // [8 warps][128] cumsum totals
     float* xrho = reinterpret_cast<float*>(sm + kXch);   // [4][128]
-    float* xgl = xrho + 512;                             // [128]
     uint64_t* qk_bar = reinterpret_cast<uint64_t*>(sm + kBars);  // [2]
     uint64_t* v_bar = qk_bar + 2;
     uint64_t* z_bar = qk_bar + 3;
@@ -457,10 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 
     // parity of the phase a load in flight will complete, or -1 (thread 0; for a clean abort)
     int pend_q[2] = {-1, -1}, pend_v = -1, pend_z = -1;
-    ItemInfo nx, nx2;  // the next two items of this CTA, decoded ahead of use
+    ItemInfo nx;        // the next item of this CTA
+    int4 raw1, raw2;    // table entries of the two items after it, fetched ahead of use
     if ((int)blockIdx.x < n_items) {
-        nx = decode_item(p, blockIdx.x);
-        if ((int)(blockIdx.x + gridDim.x) < n_items) nx2 = decode_item(p, blockIdx.x + gridDim.x);
+        nx = decode_item(p, blockIdx.x, fetch_item(p, blockIdx.x));
+        if ((int)(blockIdx.x + gridDim.x) < n_items) raw1 = fetch_item(p, blockIdx.x + gridDim.x);
+        if ((int)(blockIdx.x + 2 * gridDim.x) < n_items)
+            raw2 = fetch_item(p, blockIdx.x + 2 * gridDim.x);
         if (tid == 0) {
             load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, nx, &qk_bar[0]);
             load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
@@ -471,99 +499,145 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         }
         load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta), tid);
     }
+    // A_log of the next item's head, fetched one item ahead
+    float alog_nx = ((int)blockIdx.x < n_items) ? __ldg(p.A_log + nx.h) : 0.f;
 
     int iter = 0;
     KDA_PHASE_INIT();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
         KDA_PHASE(7);
+        KDA_ITRACE(iter, 0);
         const int b = iter & 1;
         uint8_t* qk = sm + b * kQKBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
         const ItemInfo it = nx;
+        const float alog = alog_nx;
         const int next = item + gridDim.x;
         const bool has_next = next < n_items;
         float beta_next = 0.f;  // the next item's beta[tid]: loaded mid-item, stored later
-        nx = nx2;
-        if (next + (int)gridDim.x < n_items) nx2 = decode_item(p, next + gridDim.x);
+        if (has_next) {
+            nx = decode_item(p, next, raw1);
+            alog_nx = __ldg(p.A_log + nx.h);
+        }
+        raw1 = raw2;
+        if (next + 2 * (int)gridDim.x < n_items) raw2 = fetch_item(p, next + 2 * gridDim.x);
         uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
 
-        // the previous item's package store reads the A tiles
-        if (tid == 0) bulk_wait_read0();
-
-        // ---- gate and in-chunk cumsum (two-level scan over 16 row groups of 4 rows)
+        // ---- gate and in-chunk cumsum
         if (mbar_wait(z_bar, iter & 1, p.err)) {
             if (tid == 0) pend_z = -1;
         } else {
             s_abort = 1;
         }
         KDA_PHASE(0);
-        float G[4][8];
+        KDA_ITRACE(iter, 1);
+        // G[i][e]: cumulative gate of row 4 rg + i, channel ch0 + e; gl: G of the last row.
+        // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
+        // the 8 warps' totals (shared memory).
+        float G[4][8], gl[8], pre[8];
         {
-            const float scale = expf(__ldg(p.A_log + it.h));
+            const float scale = expf(alog);
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = 4 * rg + i;
+                const bool live = r < it.L;
                 float zz[8];
                 ld8(sm + kZBuf + cofs + sw128_chunk(r, cg & 7), zz);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    acc[e] += (r < it.L) ? __fdividef(p.g_min, 1.f + __expf(-scale * zz[e])) : 0.f;
+                    // evaluated for every row and masked after (a conditional evaluation
+                    // serialises the special-function work)
+                    const float g = __fdividef(p.g_min, 1.f + __expf(-scale * zz[e]));
+                    acc[e] += live ? g : 0.f;
                     G[i][e] = acc[e];
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) tot[rg * 128 + ch0 + e] = acc[e];
+            for (int e = 0; e < 8; ++e) {
+                const float lo = __shfl_up_sync(0xffffffffu, acc[e], 16);  // row group 2 warp
+                pre[e] = (lane >= 16) ? lo : 0.f;
+            }
+            if (lane >= 16)  // this warp's total over its 8 rows
+#pragma unroll
+                for (int e = 0; e < 8; ++e) tot[warp * 128 + ch0 + e] = acc[e] + pre[e];
         }
+        KDA_ITRACE(iter, 2);
         __syncthreads();
+        KDA_ITRACE(iter, 3);
+        KDA_PHASE(9);
         if (tid == 0 && has_next) {  // z is consumed: fetch the next item's
             load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
             pend_z = (iter + 1) & 1;
         }
         if (has_next && tid < nx.L)
             beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
-        if (tid < kD) {  // exclusive scan of the block totals, one channel per thread
-            float a = 0.f;
+        {
+            float4 ta[8], tb[8];  // all loads first, then branch-free sums
 #pragma unroll
-            for (int g = 0; g < 16; ++g) {
-                const float v = tot[g * 128 + tid];
-                tot[g * 128 + tid] = a;
-                a += v;
+            for (int w2 = 0; w2 < 8; ++w2) {
+                ta[w2] = *reinterpret_cast<const float4*>(tot + w2 * 128 + ch0);
+                tb[w2] = *reinterpret_cast<const float4*>(tot + w2 * 128 + ch0 + 4);
             }
-            xgl[tid] = a;  // G of the chunk's last row
-        }
-        __syncthreads();
+            float all[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float off = tot[rg * 128 + ch0 + e];
+            for (int w2 = 0; w2 < 8; ++w2) {
+                const float t8[8] = {ta[w2].x, ta[w2].y, ta[w2].z, ta[w2].w,
+                                     tb[w2].x, tb[w2].y, tb[w2].z, tb[w2].w};
+                const bool before = w2 < warp;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) G[i][e] += off;
+                for (int e = 0; e < 8; ++e) {
+                    all[e] += t8[e];
+                    pre[e] += before ? t8[e] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                gl[e] = all[e];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) G[i][e] += pre[e];
+            }
         }
+        KDA_PHASE(10);
+        KDA_ITRACE(iter, 4);
         if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
 #pragma unroll
             for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
         if (rg == 15)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = __expf(xgl[ch0 + e]);
+            for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = __expf(gl[e]);
         if (mbar_wait(&qk_bar[b], (iter >> 1) & 1, p.err)) {
             if (tid == 0) pend_q[b] = -1;
         } else {
             s_abort = 1;
         }
+        // the previous item's package stores read the A tiles, the B-stack region and
+        // the other q/k buffer: all are rewritten from here on
+        if (tid == 0) bulk_wait_read0();
+        KDA_ITRACE(iter, 5);
         __syncthreads();
+        KDA_ITRACE(iter, 6);
         KDA_PHASE(1);
         if (s_abort) break;
 
         // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
         //      column operand of version s2 >= s is k_r e^{rho_s2 - G_r}.
         {
-            float rho[8], Es[8], Fs[8];
+            // Ev[v][e] = e^{rho_{s2} - rho_s} for the later sub-tiles s2 = sub + 1 + v (<= 1;
+            // may underflow to 0, which drops Gram terms below e^-13 of their neighbours):
+            // the column operand of version s2 is then k e^{rho_s - G} Ev.
+            float rho[8], Es[8], Fs[8], Ev[3][8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 rho[e] = xrho[sub * 128 + ch0 + e];
                 Es[e] = __expf(rho[e]);                      // e^{rho_s}
-                Fs[e] = __expf(xgl[ch0 + e] - rho[e]);       // e^{G_last - rho_s}
+                Fs[e] = __expf(gl[e] - rho[e]);              // e^{G_last - rho_s}
+            }
+#pragma unroll
+            for (int v = 0; v < 3; ++v) {
+                const int s2 = min(sub + 1 + v, 3);  // entries past sub-tile 3 are unused
+#pragma unroll
+                for (int e = 0; e < 8; ++e) Ev[v][e] = __expf(xrho[s2 * 128 + ch0 + e] - rho[e]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -596,12 +670,15 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 *reinterpret_cast<uint4*>(
                     sm + kBStk + (cg >> 3) * 20480 + sw128_chunk(kStkOff[sub] + r, cg & 7)) = hi;
                 *reinterpret_cast<uint4*>(sm + kBLo + o64) = lo;
-                for (int s2 = sub + 1; s2 < 4; ++s2) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        t[e] = kv[e] * __expf(xrho[s2 * 128 + ch0 + e] - G[i][e]);
-                    *reinterpret_cast<uint4*>(sm + kBStk + (cg >> 3) * 20480 +
-                                              sw128_chunk(kStkOff[s2] + r, cg & 7)) = pk8(t);
+                for (int v = 0; v < 3; ++v) {
+                    const int s2 = sub + 1 + v;
+                    if (s2 < 4) {  // uniform within a warp
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e] * Ev[v][e];
+                        *reinterpret_cast<uint4*>(sm + kBStk + (cg >> 3) * 20480 +
+                                                  sw128_chunk(kStkOff[s2] + r, cg & 7)) = pk8(t);
+                    }
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) t[e] = qv[e] * e1[e] * Es[e];
@@ -616,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             }
         }
         if (tid < kC) reinterpret_cast<float*>(sm + kBeta)[64 * (b ^ 1) + tid] = beta_next;
+        KDA_ITRACE(iter, 7);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -782,39 +860,39 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             pend_v = (iter + 1) & 1;
         }
         {
-            // lane quadrants 0, 1: W rows (bf16) -> the package row stack; quadrants 2, 3:
-            // U rows (fp32) -> part C.  The warpgroup picks the 64-column half.
+            // lane quadrants 0, 1: W rows (bf16), quadrants 2, 3: U rows (fp32); the
+            // warpgroup picks the 64-column half.  Both are staged in shared memory in
+            // their package layout (W in this item's q slot, U in the B-stack region) and
+            // leave by bulk copies.
             const int quad = warp & 3, wg = warp >> 2;
             const int r = 32 * (quad & 1) + lane;
-            if (quad < 2) {
-                uint8_t* dst = pkg + kPkgStk + wg * kPkgStkBlk;
+            float v[4][16];
+            const uint32_t col = (quad < 2 ? 0u : 128u) + 64 * wg;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float v[16];
-                    tmem_ld16(tmem + lane_base + 64 * wg + 16 * g, v);
-                    tmem_ld_wait();
+            for (int g = 0; g < 4; ++g) tmem_ld16(tmem + lane_base + col + 16 * g, v[g]);
+            tmem_ld_wait();
+            if (quad < 2) {
+                uint8_t* dst = qk + kOffQ + wg * 8192;
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         float v8[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v8[e] = v[8 * hf + e];
+                        for (int e = 0; e < 8; ++e) v8[e] = v[g][8 * hf + e];
                         *reinterpret_cast<uint4*>(dst + sw128_chunk(r, 2 * g + hf)) = pk8(v8);
                     }
-                }
             } else {
-                uint8_t* urow = pkg + kPkgU + wg * kPkgUHalf + r * 256;
+                uint8_t* urow = sm + kBStk + wg * kPkgUHalf + r * 256;
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    float v[16];
-                    tmem_ld16(tmem + lane_base + 128 + 64 * wg + 16 * g, v);
-                    tmem_ld_wait();
+                for (int g = 0; g < 4; ++g)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int cidx = 4 * g + q;  // 16-byte chunk: columns [4 cidx, 4 cidx + 4)
                         *reinterpret_cast<float4*>(urow + ((cidx ^ (r & 15)) << 4)) =
-                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            make_float4(v[g][4 * q], v[g][4 * q + 1], v[g][4 * q + 2],
+                                        v[g][4 * q + 3]);
                     }
-                }
             }
         }
         fence_async_smem();
@@ -823,7 +901,10 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         KDA_PHASE(6);
         if (s_abort) break;
         if (tid == 0) {
-            bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 16384);  // A hi and lo
+            bulk_s2g(pkg + kPkgStk, qk + kOffQ, 8192);                     // W, channels 0..63
+            bulk_s2g(pkg + kPkgStk + kPkgStkBlk, qk + kOffQ + 8192, 8192);  // W, channels 64..127
+            bulk_s2g(pkg + kPkgU, sm + kBStk, kPkgUBytes);                  // U
+            bulk_s2g(pkg + kPkgAQK, sm + kAqkTile, 16384);                  // A hi and lo
             bulk_commit();
         }
     }
@@ -1313,6 +1394,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
 }  // namespace
 
 #ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_itrace(long long* out, int n) {
+    if (n > 16 * 16 * 8) n = 16 * 16 * 8;
+    return cudaMemcpyFromSymbol(out, g_itrace, n * sizeof(long long)) == cudaSuccess ? n : -1;
+}
 extern "C" int kda_debug_trace(long long* out, int n) {
     if (n > 128 * 32) n = 128 * 32;
     return cudaMemcpyFromSymbol(out, g_trace, n * sizeof(long long)) == cudaSuccess ? n : -1;
@@ -1325,22 +1410,27 @@ extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
 }
 #endif
 
+// workspace: chunk offsets [N + 1], the chunk table [maxchunks], then the packages
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H) {
     const int64_t maxchunks = T_total / kC + N;
     return align_up((size_t)(N + 1) * sizeof(int32_t), 1024) +
+           align_up((size_t)maxchunks * sizeof(int4), 1024) +
            (size_t)H * (size_t)maxchunks * kPkgBytes;
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-    int32_t* chunk_off = reinterpret_cast<int32_t*>(ws);
-    uint8_t* pkg = ws + align_up((size_t)(a.N + 1) * sizeof(int32_t), 1024);
     const int maxchunks = (int)(a.T_total / kC + a.N);
+    int32_t* chunk_off = reinterpret_cast<int32_t*>(ws);
+    int4* chunk_tab = reinterpret_cast<int4*>(ws + align_up((size_t)(a.N + 1) * sizeof(int32_t), 1024));
+    uint8_t* pkg = reinterpret_cast<uint8_t*>(chunk_tab) +
+                   align_up((size_t)maxchunks * sizeof(int4), 1024);
 
     {
         ProfScope prof("plan_kernel", a.stream);
-        plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, chunk_off, a.dev_err);
+        plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, chunk_off, chunk_tab,
+                                              a.dev_err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1354,6 +1444,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         ip.A_log = a.A_log;
         ip.cu = a.cu_seqlens;
         ip.chunk_off = chunk_off;
+        ip.chunk_tab = chunk_tab;
         ip.pkg = pkg;
         ip.err = a.dev_err;
         ip.T_total = a.T_total;
