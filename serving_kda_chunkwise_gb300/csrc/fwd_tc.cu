@@ -230,7 +230,8 @@ static_assert(kIntraSmem <= 232448, "intra kernel exceeds the shared-memory limi
 // B hi -> L, T, Y (fp32).
 // The M tile is stored twice (rows 0..63 and 64..127 of a 128-row operand).
 constexpr uint32_t kAqkTile = kAStk, kAqkLoTile = kAStk + 8192, kMTile = kAStk + 16384;
-constexpr int kLd = 65;                       // padded fp32 row stride of L and T
+constexpr int kLd = 68;                       // padded fp32 row stride of L and T (fewer
+                                              // bank conflicts in the 16x16 tile fragments)
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4;
 static_assert(kST + 64 * kLd * 4 <= kBStk + 40960, "L and T must fit the B stack");
 // the solve's per-warp scratch (4 warps x 3 tiles x 16 x 20 floats) reuses the A-lo region
@@ -281,6 +282,13 @@ __device__ __forceinline__ void load_beta(const IntraParams& p, const ItemInfo& 
                                           int tid) {
     if (tid < kC)
         dst[tid] = (tid < it.L) ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
+}
+
+// 2^x (the hardware approximation; results below 2^-126 flush to zero)
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // 8 consecutive bf16 of a swizzled tile <-> fp32 registers
@@ -534,9 +542,14 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         // G[i][e]: cumulative gate of row 4 rg + i, channel ch0 + e; gl: G of the last row.
         // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
         // the 8 warps' totals (shared memory).
+        // Cumulative gate in log2 units (G2 = G log2 e, so every decay factor is one ex2).
+        // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
+        // the 8 warps' totals (one thread per channel).
         float G[4][8], gl[8], pre[8];
+        float* xtot = xrho + 512;  // [128]: G2 of the chunk's last row
         {
-            const float scale = expf(alog);
+            const float scale2 = expf(alog) * 1.4426950408889634f;  // e^{A_log} log2 e
+            const float gmin2 = p.g_min * 1.4426950408889634f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -548,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 for (int e = 0; e < 8; ++e) {
                     // evaluated for every row and masked after (a conditional evaluation
                     // serialises the special-function work)
-                    const float g = __fdividef(p.g_min, 1.f + __expf(-scale * zz[e]));
+                    const float g = __fdividef(gmin2, 1.f + ex2f(-scale2 * zz[e]));
                     acc[e] += live ? g : 0.f;
                     G[i][e] = acc[e];
                 }
@@ -558,9 +571,11 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 const float lo = __shfl_up_sync(0xffffffffu, acc[e], 16);  // row group 2 warp
                 pre[e] = (lane >= 16) ? lo : 0.f;
             }
-            if (lane >= 16)  // this warp's total over its 8 rows
-#pragma unroll
-                for (int e = 0; e < 8; ++e) tot[warp * 128 + ch0 + e] = acc[e] + pre[e];
+            if (lane >= 16) {  // this warp's total over its 8 rows
+                float4* tw = reinterpret_cast<float4*>(tot + warp * 128 + ch0);
+                tw[0] = make_float4(acc[0] + pre[0], acc[1] + pre[1], acc[2] + pre[2], acc[3] + pre[3]);
+                tw[1] = make_float4(acc[4] + pre[4], acc[5] + pre[5], acc[6] + pre[6], acc[7] + pre[7]);
+            }
         }
         KDA_ITRACE(iter, 2);
         __syncthreads();
@@ -572,28 +587,30 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         }
         if (has_next && tid < nx.L)
             beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
+        if (tid < kD) {  // exclusive scan over the warps, in place, one channel per thread
+            float v[8];
+#pragma unroll
+            for (int w2 = 0; w2 < 8; ++w2) v[w2] = tot[w2 * 128 + tid];
+            float a = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < 8; ++w2) {
+                tot[w2 * 128 + tid] = a;
+                a += v[w2];
+            }
+            xtot[tid] = a;
+        }
+        __syncthreads();
         {
-            float4 ta[8], tb[8];  // all loads first, then branch-free sums
-#pragma unroll
-            for (int w2 = 0; w2 < 8; ++w2) {
-                ta[w2] = *reinterpret_cast<const float4*>(tot + w2 * 128 + ch0);
-                tb[w2] = *reinterpret_cast<const float4*>(tot + w2 * 128 + ch0 + 4);
-            }
-            float all[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w2 = 0; w2 < 8; ++w2) {
-                const float t8[8] = {ta[w2].x, ta[w2].y, ta[w2].z, ta[w2].w,
-                                     tb[w2].x, tb[w2].y, tb[w2].z, tb[w2].w};
-                const bool before = w2 < warp;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    all[e] += t8[e];
-                    pre[e] += before ? t8[e] : 0.f;
-                }
-            }
+            const float4 pa = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0);
+            const float4 pb = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0 + 4);
+            const float4 ga = *reinterpret_cast<const float4*>(xtot + ch0);
+            const float4 gb = *reinterpret_cast<const float4*>(xtot + ch0 + 4);
+            const float p8[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+            const float g8[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                gl[e] = all[e];
+                gl[e] = g8[e];
+                pre[e] += p8[e];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) G[i][e] += pre[e];
             }
@@ -605,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
         if (rg == 15)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = __expf(gl[e]);
+            for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = ex2f(gl[e]);
         if (mbar_wait(&qk_bar[b], (iter >> 1) & 1, p.err)) {
             if (tid == 0) pend_q[b] = -1;
         } else {
@@ -629,15 +646,15 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             float rho[8], Es[8], Fs[8], Ev[3][8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                rho[e] = xrho[sub * 128 + ch0 + e];
-                Es[e] = __expf(rho[e]);                      // e^{rho_s}
-                Fs[e] = __expf(gl[e] - rho[e]);              // e^{G_last - rho_s}
+                rho[e] = xrho[sub * 128 + ch0 + e];          // (log2 units, as G)
+                Es[e] = ex2f(rho[e]);                        // e^{rho_s}
+                Fs[e] = ex2f(gl[e] - rho[e]);                // e^{G_last - rho_s}
             }
 #pragma unroll
             for (int v = 0; v < 3; ++v) {
                 const int s2 = min(sub + 1 + v, 3);  // entries past sub-tile 3 are unused
 #pragma unroll
-                for (int e = 0; e < 8; ++e) Ev[v][e] = __expf(xrho[s2 * 128 + ch0 + e] - rho[e]);
+                for (int e = 0; e < 8; ++e) Ev[v][e] = ex2f(xrho[s2 * 128 + ch0 + e] - rho[e]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -652,8 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     if (!ok) { qv[e] = 0.f; kv[e] = 0.f; }
-                    e1[e] = __expf(G[i][e] - rho[e]);
-                    dc[e] = __expf(rho[e] - G[i][e]);
+                    e1[e] = ex2f(G[i][e] - rho[e]);
+                    dc[e] = ex2f(rho[e] - G[i][e]);
                 }
                 uint4 hi, lo;
 #pragma unroll
