@@ -397,11 +397,12 @@ constexpr int kScrLd = 20;
 constexpr int kScrTile = 16 * kScrLd;
 
 __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* scr_all,
-                                             int warp) {
+                                             int warp, int iter_for_trace) {
     float* scr = scr_all + warp * 3 * kScrTile;
     float* sP = scr;                 // running product
     float* sN = scr + kScrTile;      // N^(2^k)
     float* sIN = scr + 2 * kScrTile; // I + N^(2^k)
+    KDA_ITRACE(iter_for_trace, 0);
     if (warp < 4) {
         const float* Lb = sL + (16 * warp) * kLd + 16 * warp;
         Tile16 f, q;
@@ -432,7 +433,9 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
             __syncwarp();
         }
     }
+    KDA_ITRACE(iter_for_trace, 1);
     __syncthreads();
+    KDA_ITRACE(iter_for_trace, 2);
 #pragma unroll
     for (int d = 1; d < 4; ++d) {
         if (warp < 4 - d) {
@@ -447,6 +450,7 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
             tile_mma(f, sT + (16 * s) * kLd + 16 * s, kLd, sP, kScrLd);
             tile_store(f, sT + (16 * s) * kLd + 16 * sp, kLd, -1.f, 0.f);
         }
+        KDA_ITRACE(iter_for_trace, 2 + d);
         __syncthreads();
     }
 }
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     KDA_PHASE_INIT();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
         KDA_PHASE(7);
-        KDA_ITRACE(iter, 0);
+        (void)0;
         const int b = iter & 1;
         uint8_t* qk = sm + b * kQKBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
@@ -538,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             s_abort = 1;
         }
         KDA_PHASE(0);
-        KDA_ITRACE(iter, 1);
+        (void)0;
         // G[i][e]: cumulative gate of row 4 rg + i, channel ch0 + e; gl: G of the last row.
         // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
         // the 8 warps' totals (shared memory).
@@ -577,9 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                 tw[1] = make_float4(acc[4] + pre[4], acc[5] + pre[5], acc[6] + pre[6], acc[7] + pre[7]);
             }
         }
-        KDA_ITRACE(iter, 2);
         __syncthreads();
-        KDA_ITRACE(iter, 3);
         KDA_PHASE(9);
         if (tid == 0 && has_next) {  // z is consumed: fetch the next item's
             load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
@@ -616,7 +618,6 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             }
         }
         KDA_PHASE(10);
-        KDA_ITRACE(iter, 4);
         if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
 #pragma unroll
             for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
@@ -631,9 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         // the previous item's package stores read the A tiles, the B-stack region and
         // the other q/k buffer: all are rewritten from here on
         if (tid == 0) bulk_wait_read0();
-        KDA_ITRACE(iter, 5);
         __syncthreads();
-        KDA_ITRACE(iter, 6);
         KDA_PHASE(1);
         if (s_abort) break;
 
@@ -643,13 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             // Ev[v][e] = e^{rho_{s2} - rho_s} for the later sub-tiles s2 = sub + 1 + v (<= 1;
             // may underflow to 0, which drops Gram terms below e^-13 of their neighbours):
             // the column operand of version s2 is then k e^{rho_s - G} Ev.
-            float rho[8], Es[8], Fs[8], Ev[3][8];
+            float rho[8], Ev[3][8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                rho[e] = xrho[sub * 128 + ch0 + e];          // (log2 units, as G)
-                Es[e] = ex2f(rho[e]);                        // e^{rho_s}
-                Fs[e] = ex2f(gl[e] - rho[e]);                // e^{G_last - rho_s}
-            }
+            for (int e = 0; e < 8; ++e) rho[e] = xrho[sub * 128 + ch0 + e];  // (log2 units, as G)
 #pragma unroll
             for (int v = 0; v < 3; ++v) {
                 const int s2 = min(sub + 1 + v, 3);  // entries past sub-tile 3 are unused
@@ -697,20 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
                                                   sw128_chunk(kStkOff[s2] + r, cg & 7)) = pk8(t);
                     }
                 }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t[e] = qv[e] * e1[e] * Es[e];
-                *reinterpret_cast<uint4*>(pkg + kPkgStk + (cg >> 3) * kPkgStkBlk + kPkgStkQ +
-                                          sw128_chunk(r, cg & 7)) = pk8(t);     // Gam*Q
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e] * Fs[e];
-                *reinterpret_cast<uint4*>(pkg + kPkgKT + o64) = pk8(t);       // K*gamma^C/Gam
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t[e] = kv[e] * e1[e] * Es[e];
-                *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
             }
         }
         if (tid < kC) reinterpret_cast<float*>(sm + kBeta)[64 * (b ^ 1) + tid] = beta_next;
-        KDA_ITRACE(iter, 7);
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -749,6 +733,35 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             }
             mma_commit(mma_bar);
         }
+
+        // ---- while the Gram MMAs run: the globally scaled operands of the later products,
+        //      Gam*Q and K*gamma^C/Gam (package, for the state kernel) and Gam*K (W = M Gam K)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * rg + i;
+            const bool ok = r < it.L;
+            const uint32_t o64 = cofs + sw128_chunk(r, cg & 7);
+            float qv[8], kv[8], eg[8], ek[8], t[8];
+            ld8(qk + kOffQ + o64, qv);
+            ld8(qk + kOffK + o64, kv);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (!ok) { qv[e] = 0.f; kv[e] = 0.f; }
+                eg[e] = ex2f(G[i][e]);           // e^{G_r}
+                ek[e] = ex2f(gl[e] - G[i][e]);   // e^{G_last - G_r}
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = qv[e] * eg[e];
+            *reinterpret_cast<uint4*>(pkg + kPkgStk + (cg >> 3) * kPkgStkBlk + kPkgStkQ +
+                                      sw128_chunk(r, cg & 7)) = pk8(t);     // Gam*Q
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = kv[e] * ek[e];
+            *reinterpret_cast<uint4*>(pkg + kPkgKT + o64) = pk8(t);       // K*gamma^C/Gam
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t[e] = kv[e] * eg[e];
+            *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
+        }
+
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
@@ -819,7 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             const float* sL = reinterpret_cast<const float*>(sm + kSL);
             float* sT = reinterpret_cast<float*>(sm + kST);
             float* sScr = reinterpret_cast<float*>(sm + kSolveScr);
-            solve_tril64(sL, sT, sScr, warp);
+            solve_tril64(sL, sT, sScr, warp, iter);
+            KDA_ITRACE(iter, 6);
             KDA_PHASE(8);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile, written twice: the
             // 128-row operand [M; M] of the W / U MMA
