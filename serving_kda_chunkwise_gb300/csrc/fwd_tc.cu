@@ -234,9 +234,9 @@ constexpr int kLd = 68;                       // padded fp32 row stride of L and
                                               // bank conflicts in the 16x16 tile fragments)
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4;
 static_assert(kST + 64 * kLd * 4 <= kBStk + 40960, "L and T must fit the B stack");
-// the solve's per-warp scratch (4 warps x 3 tiles x 16 x 20 floats) reuses the A-lo region
+// the solve's per-warp scratch (4 warps x 16 x 20 floats) reuses the A-lo region
 constexpr uint32_t kSolveScr = kALo;
-static_assert(4 * 3 * 16 * 20 * 4 <= 16384, "solve scratch must fit the A-lo region");
+static_assert(4 * 16 * 20 * 4 <= 16384, "solve scratch must fit the A-lo region");
 // TMEM columns: main Gram accumulator [0, 160), diagonal-column lo correction [160, 224),
 // q-side lo correction [256, 416);
 // later W [0, 128) and U [128, 256).
@@ -340,19 +340,6 @@ __device__ __forceinline__ void tile_zero(Tile16& f) {
         for (int q = 0; q < 4; ++q) f.c[nn][q] = 0.f;
 }
 
-// f = scale * X + diag * I
-__device__ __forceinline__ void tile_load(Tile16& f, const float* X, int ld, float scale,
-                                          float diag) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nn = 0; nn < 2; ++nn)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int row = g + 8 * (q >> 1), col = 8 * nn + 2 * t + (q & 1);
-            f.c[nn][q] = scale * X[row * ld + col] + (row == col ? diag : 0.f);
-        }
-}
-
 // X = scale * f + diag * I
 __device__ __forceinline__ void tile_store(const Tile16& f, float* X, int ld, float scale,
                                            float diag) {
@@ -390,48 +377,41 @@ __device__ __forceinline__ void tile_mma(Tile16& f, const float* A, int lda, con
 }
 
 // T = (I + L)^{-1} for the 64x64 strictly lower L (16x16 blocks).  Warp w < 4 first inverts
-// diagonal block w as (I - N)(I + N^2)(I + N^4)(I + N^8), N = L_ww (N^16 = 0); then the
-// off-diagonal blocks follow by distance d: T_{s,s'} = -T_ss sum_{t=s'}^{s-1} L_st T_{t,s'}.
-// `scr` is per-warp scratch of 3 tiles of 16 x kScrLd floats.
+// diagonal block w by forward substitution in fp32 (lane j holds column j:
+// T_ij = delta_ij - sum_{k<i} L_ik T_kj); then the off-diagonal blocks follow by distance d:
+// T_{s,s'} = -T_ss sum_{t=s'}^{s-1} L_st T_{t,s'}.  `scr` is per-warp scratch of 16 x kScrLd
+// floats.
 constexpr int kScrLd = 20;
 constexpr int kScrTile = 16 * kScrLd;
 
+__device__ __forceinline__ int lane16() { return threadIdx.x & 15; }
+
 __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* scr_all,
                                              int warp, int iter_for_trace) {
-    float* scr = scr_all + warp * 3 * kScrTile;
-    float* sP = scr;                 // running product
-    float* sN = scr + kScrTile;      // N^(2^k)
-    float* sIN = scr + 2 * kScrTile; // I + N^(2^k)
+    float* sP = scr_all + warp * kScrTile;  // per-warp scratch tile
     KDA_ITRACE(iter_for_trace, 0);
     if (warp < 4) {
         const float* Lb = sL + (16 * warp) * kLd + 16 * warp;
-        Tile16 f, q;
-        tile_load(f, Lb, kLd, -1.f, 1.f);  // P = I - N
-        tile_store(f, sP, kScrLd, 1.f, 0.f);
-        tile_zero(q);
-        tile_mma(q, Lb, kLd, Lb, kLd);     // N^2
-        __syncwarp();
-        tile_store(q, sN, kScrLd, 1.f, 0.f);
-        tile_store(q, sIN, kScrLd, 1.f, 1.f);
-        __syncwarp();
+        const int j = lane16();
+        float tc[16];
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {      // P <- P (I + N^2^k), N <- N^2 (k < 2)
-            tile_zero(f);
-            tile_mma(f, sP, kScrLd, sIN, kScrLd);
-            if (k < 2) {
-                tile_zero(q);
-                tile_mma(q, sN, kScrLd, sN, kScrLd);
+        for (int i = 0; i < 16; ++i) {
+            float Lr[16];  // row i of the block (only k < i is used)
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4) {
+                if (4 * k4 < i) {
+                    const float4 v = *reinterpret_cast<const float4*>(Lb + i * kLd + 4 * k4);
+                    Lr[4 * k4] = v.x; Lr[4 * k4 + 1] = v.y; Lr[4 * k4 + 2] = v.z; Lr[4 * k4 + 3] = v.w;
+                }
             }
-            __syncwarp();
-            if (k < 2) {
-                tile_store(f, sP, kScrLd, 1.f, 0.f);
-                tile_store(q, sN, kScrLd, 1.f, 0.f);
-                tile_store(q, sIN, kScrLd, 1.f, 1.f);
-            } else {
-                tile_store(f, sT + (16 * warp) * kLd + 16 * warp, kLd, 1.f, 0.f);
-            }
-            __syncwarp();
+            float acc = (i == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int k = 0; k < i; ++k) acc = fmaf(-Lr[k], tc[k], acc);
+            tc[i] = acc;
         }
+        if ((threadIdx.x & 31) < 16)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sT[(16 * warp + i) * kLd + 16 * warp + j] = tc[i];
     }
     KDA_ITRACE(iter_for_trace, 1);
     __syncthreads();
@@ -1047,10 +1027,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     uint64_t* fullB = fullA + 2;                                  // [2] (part B + gamma)
     uint64_t* ubar = fullA + 4;                                   // [2]
     uint64_t* mma3 = fullA + 6;                                   // [2]
-    uint64_t* vt_ready = fullA + 8;                               // [2], 128 arrivals
+    uint64_t* vt_ready = fullA + 8;                               // [2], 4 arrivals
     uint64_t* mma1 = fullA + 10;
     uint64_t* mma2 = fullA + 11;
-    uint64_t* s_ready = fullA + 12;                               // 256 arrivals
+    uint64_t* s_ready = fullA + 12;                               // 8 arrivals
     uint64_t* drain = fullA + 13;  // used once, to let MMAs in flight land on an abort
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 14);
     __shared__ int s_abort;
@@ -1069,9 +1049,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
 
     if (tid == 0) {
         for (int i = 0; i < 14; ++i) mbar_init(&fullA[i], 1);
-        mbar_init(&vt_ready[0], 128);
-        mbar_init(&vt_ready[1], 128);
-        mbar_init(s_ready, 256);
+        mbar_init(&vt_ready[0], 4);  // one arrival per X warp
+        mbar_init(&vt_ready[1], 4);
+        mbar_init(s_ready, 8);       // one arrival per epilogue warp
         fence_mbar_init();
         s_abort = 0;
     }
@@ -1147,10 +1127,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         for (; t < nch; ++t) {
             const int st = t & 1;
             const uint32_t ph = (t >> 1) & 1;
+            // copies complete long before the handoffs: their waits go first, off the chain
+            if (!mbar_wait_ab(&fullA[st], ph, p.err, abort)) break;
             if (t > 0 && !mbar_wait_ab(s_ready, (t - 1) & 1, p.err, abort)) break;
             KDA_TRACE(t, 10);
             tc_fence_after();
-            if (!mbar_wait_ab(&fullA[st], ph, p.err, abort)) break;
             KDA_TRACE(t, 11);
             issue_mma1(t);
             KDA_TRACE(t, 12);
@@ -1159,10 +1140,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                 mma_commit(&mma3[(t - 1) & 1]);
             }
             KDA_TRACE(t, 13);
+            if (!mbar_wait_ab(&fullB[st], ph, p.err, abort)) break;
             if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
             KDA_TRACE(t, 14);
             tc_fence_after();
-            if (!mbar_wait_ab(&fullB[st], ph, p.err, abort)) break;
             KDA_TRACE(t, 15);
             const uint32_t sB = sbase + kPB + st * kPkgPartB;
             const uint32_t sVt = sbase + kVt + st * 16384;
@@ -1241,10 +1222,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             const uint32_t d1 = 64u * st;
             const int64_t t0 = t_begin + (int64_t)t * kC;
             if (xwarp) {
+                if (!mbar_wait_ab(&ubar[st], ph, p.err, abort)) break;
                 if (!mbar_wait_ab(mma1, t & 1, p.err, abort)) break;
                 if (tid == 0) KDA_TRACE(t, 0);
                 KDA_PHASE(21);
-                if (!mbar_wait_ab(&ubar[st], ph, p.err, abort)) break;
                 tc_fence_after();
                 if (tid == 0) KDA_TRACE(t, 1);
                 KDA_PHASE(16);
@@ -1282,14 +1263,15 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                 fence_async_smem();
                 if (tid == 0) KDA_TRACE(t, 24);
                 tc_fence_before();
-                mbar_arrive(&vt_ready[st]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&vt_ready[st]);
                 if (tid == 0) KDA_TRACE(t, 3);
                 KDA_PHASE(17);
             }
             // The O warps meet on a named barrier below, so they leave the loop only together
             // (by a vote at its end); the X warps leave at the first wait that fails.
-            bool ok = mbar_wait_ab(mma2, t & 1, p.err, abort) &&
-                      mbar_wait_ab(&fullB[st], ph, p.err, abort);  // gamma^C of this chunk
+            bool ok = mbar_wait_ab(&fullB[st], ph, p.err, abort) &&  // gamma^C of this chunk
+                      mbar_wait_ab(mma2, t & 1, p.err, abort);
             if (xwarp && !ok) break;
             tc_fence_after();
             if (tid == 0) KDA_TRACE(t, 4);
@@ -1310,7 +1292,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             }
             fence_async_smem();
             tc_fence_before();
-            mbar_arrive(s_ready);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_ready);
             if (tid == 0) KDA_TRACE(t, 5);
             if (tid == 64) KDA_TRACE(t, 7);
             KDA_PHASE(19);
