@@ -46,7 +46,9 @@ using namespace tc;
 
 constexpr int kC = 64;    // chunk length
 constexpr int kD = 128;   // head dim (dk = dv)
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;       // row-work threads of the intra kernel (8 warps)
+constexpr int kIntraThreads = 288;  // + one warp whose lane 0 issues copies and MMAs
+constexpr int kIss = 256;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
 // part A (needed at the start of a chunk): the row stack [W; Gam*Q] of the state kernel's
@@ -435,7 +437,7 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
+__global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -450,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool rows = warp < 8;  // warps 0..7 do the row work; lane 0 of warp 8 issues copies and MMAs
     // operand passes: 8 channels [8 cg, 8 cg + 8) of rows [4 rg, 4 rg + 4)
     const int cg = tid & 15, rg = tid >> 4, sub = rg >> 2;
     const uint32_t cofs = (cg >> 3) * 8192;  // 64-column block of the channel group
@@ -472,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     uint32_t mma_phase = 0;
     const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
-    // parity of the phase a load in flight will complete, or -1 (thread 0; for a clean abort)
+    // parity of the phase a load in flight will complete, or -1 (issuing thread; for a clean
+    // abort)
     int pend_q[2] = {-1, -1}, pend_v = -1, pend_z = -1;
     ItemInfo nx;        // the next item of this CTA
     int4 raw1, raw2;    // table entries of the two items after it, fetched ahead of use
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if ((int)(blockIdx.x + gridDim.x) < n_items) raw1 = fetch_item(p, blockIdx.x + gridDim.x);
         if ((int)(blockIdx.x + 2 * gridDim.x) < n_items)
             raw2 = fetch_item(p, blockIdx.x + 2 * gridDim.x);
-        if (tid == 0) {
+        if (tid == kIss) {
             load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, nx, &qk_bar[0]);
             load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
             load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 
         // ---- gate and in-chunk cumsum
         if (mbar_wait(z_bar, iter & 1, p.err)) {
-            if (tid == 0) pend_z = -1;
+            if (tid == kIss) pend_z = -1;
         } else {
             s_abort = 1;
         }
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         // the 8 warps' totals (one thread per channel).
         float G[4][8], gl[8], pre[8];
         float* xtot = xrho + 512;  // [128]: G2 of the chunk's last row
-        {
+        if (rows) {
             const float scale2 = expf(alog) * 1.4426950408889634f;  // e^{A_log} log2 e
             const float gmin2 = p.g_min * 1.4426950408889634f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -563,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         }
         __syncthreads();
         KDA_PHASE(9);
-        if (tid == 0 && has_next) {  // z is consumed: fetch the next item's
+        if (tid == kIss && has_next) {  // z is consumed: fetch the next item's
             load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
             pend_z = (iter + 1) & 1;
         }
@@ -582,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             xtot[tid] = a;
         }
         __syncthreads();
-        {
+        if (rows) {
             const float4 pa = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0);
             const float4 pb = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0 + 4);
             const float4 ga = *reinterpret_cast<const float4*>(xtot + ch0);
@@ -598,27 +602,27 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             }
         }
         KDA_PHASE(10);
-        if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
+        if (rows && (rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
 #pragma unroll
             for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
-        if (rg == 15)
+        if (rows && rg == 15)
 #pragma unroll
             for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = ex2f(gl[e]);
         if (mbar_wait(&qk_bar[b], (iter >> 1) & 1, p.err)) {
-            if (tid == 0) pend_q[b] = -1;
+            if (tid == kIss) pend_q[b] = -1;
         } else {
             s_abort = 1;
         }
         // the previous item's package stores read the A tiles, the B-stack region and
         // the other q/k buffer: all are rewritten from here on
-        if (tid == 0) bulk_wait_read0();
+        if (tid == kIss) bulk_wait_read0();
         __syncthreads();
         KDA_PHASE(1);
         if (s_abort) break;
 
         // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
         //      column operand of version s2 >= s is k_r e^{rho_s2 - G_r}.
-        {
+        if (rows) {
             // Ev[v][e] = e^{rho_{s2} - rho_s} for the later sub-tiles s2 = sub + 1 + v (<= 1;
             // may underflow to 0, which drops Gram terms below e^-13 of their neighbours):
             // the column operand of version s2 is then k e^{rho_s - G} Ev.
@@ -679,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         tc_fence_before();
         __syncthreads();
         KDA_PHASE(2);
-        if (tid == 0) {
+        if (tid == kIss) {
             if (has_next) {
                 fence_async_smem();
                 load_tiles(&p.tq, sm + (b ^ 1) * kQKBuf + kOffQ, &p.tk,
@@ -690,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 
         // ---- Grams: D = [Q'; beta K']_hi Bstack_hi^T (+ diagonal-column lo terms),
         //      D_lo = Q'_lo Bstack_hi^T (its k-side lanes are unused)
-        if (tid == 0) {
+        if (tid == kIss) {
             tc_fence_after();
             constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
             constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
@@ -716,6 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
 
         // ---- while the Gram MMAs run: the globally scaled operands of the later products,
         //      Gam*Q and K*gamma^C/Gam (package, for the state kernel) and Gam*K (W = M Gam K)
+        if (rows) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = 4 * rg + i;
@@ -741,6 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             for (int e = 0; e < 8; ++e) t[e] = kv[e] * eg[e];
             *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
         }
+        }
 
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
@@ -750,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         // ---- Gram epilogue: q-side rows -> A tile (bf16 hi + lo), k-side rows -> L (fp32).
         //      TMEM lane m = 32 (warp % 4) + lane; the groups of 16 columns a lane quadrant
         //      needs are split between the two warpgroups.
-        {
+        if (rows) {
             const int quad = warp & 3, wg = warp >> 2;
             const int m = 32 * quad + lane;
             const int side = m >> 6, r = m & 63, s = r >> 4;
@@ -817,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
             KDA_PHASE(8);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile, written twice: the
             // 128-row operand [M; M] of the W / U MMA
-            {
+            if (rows) {
                 const int r = tid >> 2, cq = tid & 3;
                 uint8_t* mt = sm + kMTile;
 #pragma unroll
@@ -845,11 +851,11 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         // ---- W = M (Gam K) and U = M V: A = [M; M] (rows 64..127 repeat rows 0..63, so
         //      every TMEM lane quadrant holds a copy of the 64 rows), N = 128 channels each
         if (mbar_wait(v_bar, iter & 1, p.err)) {
-            if (tid == 0) pend_v = -1;
+            if (tid == kIss) pend_v = -1;
         } else {
             s_abort = 1;
         }
-        if (tid == 0) {
+        if (tid == kIss) {
             tc_fence_after();
             constexpr uint32_t idesc = idesc_bf16(128, 128, false, true);
 #pragma unroll
@@ -865,12 +871,12 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
-        if (tid == 0 && has_next) {  // v is consumed: fetch the next item's
+        if (tid == kIss && has_next) {  // v is consumed: fetch the next item's
             fence_async_smem();
             load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
             pend_v = (iter + 1) & 1;
         }
-        {
+        if (rows) {
             // lane quadrants 0, 1: W rows (bf16), quadrants 2, 3: U rows (fp32); the
             // warpgroup picks the 64-column half.  Both are staged in shared memory in
             // their package layout (W in this item's q slot, U in the B-stack region) and
@@ -911,7 +917,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
         __syncthreads();
         KDA_PHASE(6);
         if (s_abort) break;
-        if (tid == 0) {
+        if (tid == kIss) {
             bulk_s2g(pkg + kPkgStk, qk + kOffQ, 8192);                     // W, channels 0..63
             bulk_s2g(pkg + kPkgStk + kPkgStkBlk, qk + kOffQ + 8192, 8192);  // W, channels 64..127
             bulk_s2g(pkg + kPkgU, sm + kBStk, kPkgUBytes);                  // U
@@ -921,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 1) intra_kernel(const __grid_constan
     }
     KDA_PHASE_FLUSH();
     // teardown: stores complete, no load in flight, TMEM released
-    if (tid == 0) {
+    if (tid == kIss) {
         bulk_wait0();
         if (s_abort) {
             for (int q = 0; q < 2; ++q)
@@ -1473,7 +1479,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         ProfScope prof("intra_kernel", a.stream);
-        intra_kernel<<<sms, kThreads, kIntraSmem, a.stream>>>(ip);
+        intra_kernel<<<sms, kIntraThreads, kIntraSmem, a.stream>>>(ip);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
