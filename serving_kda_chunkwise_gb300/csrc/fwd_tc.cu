@@ -15,7 +15,7 @@
 //                 Gram matrices in ONE tcgen05 MMA, the UT solve on CUDA cores in fp32,
 //                 W and U by tcgen05; writes one "package" per (head, chunk) whose bytes
 //                 are the shared-memory image of the state kernel's MMA operands.
-//   state_kernel  two CTAs per (sequence, head), each owning 64 of the 128 value columns
+//   state_kernel  four CTAs per (sequence, head), each owning 32 of the 128 value columns
 //                 (the columns of S evolve independently), serial over chunks: state S in
 //                 fp32 registers, packages streamed in by bulk copies (double buffered),
 //                 [W; Gamma Q] S, K~^T Vt and A Vt on tcgen05.
@@ -65,11 +65,11 @@ constexpr uint32_t kPkgAQKLo = 57344; // A lo   (A = hi + lo, bf16 each)
 constexpr uint32_t kPkgPartB = 32768;
 constexpr uint32_t kPkgG = 65536;     // gamma^C [128] fp32
 constexpr uint32_t kPkgGBytes = 512;
-// part C: U = M V in fp32, two halves of 64 value columns, each [64 r][64 j] with the
-// 16-byte chunk c of row r at chunk position c ^ (r & 15)
+// part C: U = M V in fp32, four quarters of 32 value columns, each [64 r][32 j] with the
+// 16-byte chunk c of row r at chunk position c ^ (r & 7)
 constexpr uint32_t kPkgU = 66048;
-constexpr uint32_t kPkgUHalf = 16384;
-constexpr uint32_t kPkgUBytes = 2 * kPkgUHalf;
+constexpr uint32_t kPkgUQ = 8192;
+constexpr uint32_t kPkgUBytes = 4 * kPkgUQ;
 constexpr uint32_t kPkgBytes = kPkgU + kPkgUBytes;  // 98816
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -567,10 +567,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         }
         __syncthreads();
         KDA_PHASE(9);
-        if (tid == kIss && has_next) {  // z is consumed: fetch the next item's
-            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
-            pend_z = (iter + 1) & 1;
-        }
         if (has_next && tid < nx.L)
             beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
         if (tid < kD) {  // exclusive scan over the warps, in place, one channel per thread
@@ -586,6 +582,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             xtot[tid] = a;
         }
         __syncthreads();
+        // z is consumed: fetch the next item's (issued here, where a long phase follows,
+        // so that a slow issue never holds up a barrier)
+        if (tid == kIss && has_next) {
+            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
+            pend_z = (iter + 1) & 1;
+        }
         if (rows) {
             const float4 pa = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0);
             const float4 pb = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0 + 4);
@@ -871,11 +873,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
-        if (tid == kIss && has_next) {  // v is consumed: fetch the next item's
-            fence_async_smem();
-            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
-            pend_v = (iter + 1) & 1;
-        }
         if (rows) {
             // lane quadrants 0, 1: W rows (bf16), quadrants 2, 3: U rows (fp32); the
             // warpgroup picks the 64-column half.  Both are staged in shared memory in
@@ -900,13 +897,15 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
                         *reinterpret_cast<uint4*>(dst + sw128_chunk(r, 2 * g + hf)) = pk8(v8);
                     }
             } else {
-                uint8_t* urow = sm + kBStk + wg * kPkgUHalf + r * 256;
+                // columns [64 wg + 4 cidx, +4): quarter 2 wg + (cidx >> 3), chunk cidx & 7
+                uint8_t* urow = sm + kBStk + 2 * wg * kPkgUQ + r * 128;
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int cidx = 4 * g + q;  // 16-byte chunk: columns [4 cidx, 4 cidx + 4)
-                        *reinterpret_cast<float4*>(urow + ((cidx ^ (r & 15)) << 4)) =
+                        const int cidx = 4 * g + q;
+                        *reinterpret_cast<float4*>(urow + (cidx >> 3) * kPkgUQ +
+                                                   (((cidx & 7) ^ (r & 7)) << 4)) =
                             make_float4(v[g][4 * q], v[g][4 * q + 1], v[g][4 * q + 2],
                                         v[g][4 * q + 3]);
                     }
@@ -917,6 +916,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         __syncthreads();
         KDA_PHASE(6);
         if (s_abort) break;
+        if (tid == kIss && has_next) {  // v is consumed: fetch the next item's
+            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
+            pend_v = (iter + 1) & 1;
+        }
         if (tid == kIss) {
             bulk_s2g(pkg + kPkgStk, qk + kOffQ, 8192);                     // W, channels 0..63
             bulk_s2g(pkg + kPkgStk + kPkgStkBlk, qk + kOffQ + 8192, 8192);  // W, channels 64..127
@@ -963,25 +966,26 @@ struct StateParams {
 
 // The value columns of S are independent (column j of S, X, Vt and O depends only on
 // column j of V and S0), so each (sequence, head) is served by kSplit CTAs of kJ columns.
-constexpr int kSplit = 2;
-constexpr int kJ = kD / kSplit;  // 64
+constexpr int kSplit = 4;
+constexpr int kJ = kD / kSplit;  // 32: the 32-wide bf16 tiles use the 64-byte swizzle
 
 // shared-memory map of the state kernel (1024-aligned offsets)
 constexpr uint32_t kPA = 0;                         // package part A, two stages of 32 KB
 constexpr uint32_t kPB = 2 * kPkgPartA;             //  65536: part B, two stages of 32 KB
-constexpr uint32_t kUS = kPB + 2 * kPkgPartB;       // 131072: U (own half), two stages of 16 KB
-constexpr uint32_t kVt = kUS + 2 * kPkgUHalf;       // 163840: Vt [64 r][64 j] bf16 MN-major,
-                                                    //         two stages of (hi 8 KB, lo 8 KB)
-constexpr uint32_t kSbf = kVt + 2 * 16384;          // 196608: S bf16 [128 i][64 j] MN-major
-constexpr uint32_t kGam = kSbf + 16384;             // 212992: gamma^C, two stages of 512 B
-constexpr uint32_t kOSt = kGam + 1024;              // 214016: O tile [64 r][64 j] bf16 sw128,
+constexpr uint32_t kUS = kPB + 2 * kPkgPartB;       // 131072: U (own quarter), two stages of 8 KB
+constexpr uint32_t kVt = kUS + 2 * kPkgUQ;          // 147456: Vt [64 r][32 j] bf16 MN-major sw64,
+                                                    //         two stages of (hi 4 KB, lo 4 KB)
+constexpr uint32_t kVtStage = 8192, kVtLo = 4096;
+constexpr uint32_t kSbf = kVt + 2 * kVtStage;       // 163840: S bf16 [128 i][32 j] MN-major sw64
+constexpr uint32_t kGam = kSbf + 8192;              // 172032: gamma^C, two stages of 512 B
+constexpr uint32_t kOSt = kGam + 1024;              // 173056: O tile [64 r][32 j] bf16 sw64,
                                                     //         the source of a TMA store
-constexpr uint32_t kSBars = kOSt + 8192;            // 222208
-constexpr uint32_t kStateSmem = kSBars + 128 + 1024;
+constexpr uint32_t kSBars = kOSt + 4096;            // 177152
+constexpr uint32_t kStateSmem = kSBars + 256 + 1024;
 static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limit");
-// TMEM columns: D1 = [X; Gam Q S + A Vt] for chunk t in [64 (t & 1), 64 (t & 1) + 64);
-// dS = K~^T Vt in [128, 192)
-constexpr uint32_t kStateTmemCols = 256, kDS = 128;
+// TMEM columns: D1 = [X; Gam Q S + A Vt] for chunk t in [32 (t & 1), 32 (t & 1) + 32);
+// dS = K~^T Vt in [64, 96)
+constexpr uint32_t kStateTmemCols = 128, kDS = 64;
 
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -1007,10 +1011,11 @@ constexpr int kStateThreads = 384;
 constexpr int kMmaT = 320;   // the MMA thread: lane 0 of warp 10
 constexpr int kCopyT = 352;  // the copy thread: lane 0 of warp 11
 
-// One CTA per (sequence, head, column half).  TMEM lanes 0..63 of D1 hold the rows of
-// X = W S, lanes 64..127 the rows of O; a warp reaches only the lane quadrant (warp % 4),
-// so warps 0, 1, 4, 5 ("X warps") form Vt, warps 2, 3, 6, 7 ("O warps") write O and all
-// eight epilogue warps update S (one state row i per lane, 32 columns per warpgroup).
+// One CTA per (sequence, head, quarter of the value columns).  TMEM lanes 0..63 of D1 hold
+// the rows of X = W S, lanes 64..127 the rows of O; a warp reaches only the lane quadrant
+// (warp % 4), so warps 0, 1, 4, 5 ("X warps") form Vt, warps 2, 3, 6, 7 ("O warps") write O
+// and all eight epilogue warps update S (one state row i per lane, 16 columns per
+// warpgroup).
 // One thread issues every MMA, another every bulk copy; the warps meet only on mbarriers
 // (no CTA-wide barrier inside the chunk loop), so nothing waits on MMA or copy issue.
 // Per chunk t:
@@ -1048,9 +1053,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const bool epi = warp < 8;
     const bool xwarp = epi && quad < 2;
     const bool owarp = epi && quad >= 2;
-    const int half = blockIdx.x % kSplit;
+    const int part = blockIdx.x % kSplit;  // which 32 value columns
     const int nh = blockIdx.x / kSplit, h = nh % p.H, n = nh / p.H;
-    const int jc = kJ * half + 32 * wg;  // first value column of this (epilogue) thread
+    const int jc = kJ * part + 16 * wg;    // first of the 16 value columns of this epilogue thread
     volatile int* abort = &s_abort;
 
     if (tid == 0) {
@@ -1069,22 +1074,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const int nch = __ldg(p.chunk_off + n + 1) - c0;
     const uint8_t* pkg0 = p.pkg + ((size_t)h * p.maxchunks + c0) * kPkgBytes;
 
-    // S[i = row][jc + jj], jj < 32, in registers of the epilogue warps
-    float S[32];
+    // S[i = row][jc + jj], jj < 16, in registers of the epilogue warps
+    float S[16];
     const size_t sofs = ((size_t)nh * kD + row) * kD + jc;
 #pragma unroll
-    for (int jj = 0; jj < 32; jj += 4) {
+    for (int jj = 0; jj < 16; jj += 4) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (p.S0 && epi) v = *reinterpret_cast<const float4*>(p.S0 + sofs + jj);
         S[jj] = v.x; S[jj + 1] = v.y; S[jj + 2] = v.z; S[jj + 3] = v.w;
     }
     auto write_sbf = [&]() {
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
             float v8[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) v8[e] = S[8 * cc + e];
-            *reinterpret_cast<uint4*>(sm + kSbf + sw128_chunk(row, 4 * wg + cc)) = pk8(v8);
+            *reinterpret_cast<uint4*>(sm + kSbf + sw64_chunk(row, 2 * wg + cc)) = pk8(v8);
         }
     };
     if (epi) write_sbf();
@@ -1103,8 +1108,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             for (int ks = 0; ks < 8; ++ks) {
                 const uint64_t a =
                     sdesc_sw128(sA + (ks >> 2) * kPkgStkBlk + (ks & 3) * 32, 0, 1024);
-                const uint64_t b = sdesc_sw128(sbase + kSbf + ks * 2048, 0, 1024);
-                mma_bf16(tmem + 64u * (t & 1), a, b, id, ks > 0);
+                const uint64_t b = sdesc_sw64(sbase + kSbf + ks * 1024, 0, 512);
+                mma_bf16(tmem + uint32_t(kJ) * (t & 1), a, b, id, ks > 0);
             }
             mma_commit(mma1);
         };
@@ -1113,17 +1118,17 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         // block 1, A lo by A hi.
         auto issue_mma3 = [&](int t, int ks0) {
             const uint32_t sB = sbase + kPB + (t & 1) * kPkgPartB;
-            const uint32_t sVt = sbase + kVt + (t & 1) * 16384;
+            const uint32_t sVt = sbase + kVt + (t & 1) * kVtStage;
             const uint32_t sAh = sB + (kPkgAQK - kPkgKT) - 8192;
             const uint32_t sAl = sB + (kPkgAQKLo - kPkgKT) - 8192;
             constexpr uint32_t id3 = idesc_bf16(128, kJ, false, true);
-            const uint32_t d = tmem + 64u * (t & 1);
+            const uint32_t d = tmem + uint32_t(kJ) * (t & 1);
 #pragma unroll
             for (int ks = ks0; ks < ks0 + 2; ++ks) {
                 const uint64_t ah = sdesc_sw128(sAh + ks * 32, 0, 1024);
                 const uint64_t al = sdesc_sw128(sAl + ks * 32, 0, 1024);
-                const uint64_t vh = sdesc_sw128(sVt + ks * 2048, 0, 1024);
-                const uint64_t vl = sdesc_sw128(sVt + 8192 + ks * 2048, 0, 1024);
+                const uint64_t vh = sdesc_sw64(sVt + ks * 1024, 0, 512);
+                const uint64_t vl = sdesc_sw64(sVt + kVtLo + ks * 1024, 0, 512);
                 mma_bf16(d, ah, vh, id3, 1);
                 mma_bf16(d, ah, vl, id3, 1);
                 mma_bf16(d, al, vh, id3, 1);
@@ -1152,12 +1157,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             tc_fence_after();
             KDA_TRACE(t, 15);
             const uint32_t sB = sbase + kPB + st * kPkgPartB;
-            const uint32_t sVt = sbase + kVt + st * 16384;
+            const uint32_t sVt = sbase + kVt + st * kVtStage;
             constexpr uint32_t id2 = idesc_bf16(128, kJ, true, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem + kDS, sdesc_sw128(sB + ks * 2048, 8192, 1024),
-                         sdesc_sw128(sVt + ks * 2048, 0, 1024), id2, ks > 0);
+                         sdesc_sw64(sVt + ks * 1024, 0, 512), id2, ks > 0);
             mma_commit(mma2);
             KDA_TRACE(t, 16);
             issue_mma3(t, 0);
@@ -1190,10 +1195,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         };
         auto issue_u = [&](int t) {
             const int st = t & 1;
-            mbar_expect_tx(&ubar[st], kPkgUHalf);
-            bulk_g2s(sm + kUS + st * kPkgUHalf,
-                     pkg0 + (size_t)t * kPkgBytes + kPkgU + half * kPkgUHalf, kPkgUHalf,
-                     &ubar[st]);
+            mbar_expect_tx(&ubar[st], kPkgUQ);
+            bulk_g2s(sm + kUS + st * kPkgUQ, pkg0 + (size_t)t * kPkgBytes + kPkgU + part * kPkgUQ,
+                     kPkgUQ, &ubar[st]);
             lastU[st] = t;
         };
         for (int t = 0; t < 2 && t < nch; ++t) {
@@ -1225,7 +1229,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
         for (int t = 0; t < nch; ++t) {
             const int st = t & 1;
             const uint32_t ph = (t >> 1) & 1;
-            const uint32_t d1 = 64u * st;
+            const uint32_t d1 = uint32_t(kJ) * st;
             const int64_t t0 = t_begin + (int64_t)t * kC;
             if (xwarp) {
                 if (!mbar_wait_ab(&ubar[st], ph, p.err, abort)) break;
@@ -1235,35 +1239,28 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                 tc_fence_after();
                 if (tid == 0) KDA_TRACE(t, 1);
                 KDA_PHASE(16);
-                // E1: Vt = U - X for row r = row, columns [32 wg, 32 wg + 32) of this half
-                const uint8_t* urow = sm + kUS + st * kPkgUHalf + row * 256;
-                uint8_t* vt = sm + kVt + st * 16384;
-                float xx[2][16];
-                tmem_ld16(tmem + lane_base + d1 + 32 * wg, xx[0]);
-                tmem_ld16(tmem + lane_base + d1 + 32 * wg + 16, xx[1]);
+                // E1: Vt = U - X for row r = row, columns [16 wg, 16 wg + 16) of this quarter
+                const uint8_t* urow = sm + kUS + st * kPkgUQ + row * 128;
+                uint8_t* vt = sm + kVt + st * kVtStage;
+                float x[16];
+                tmem_ld16(tmem + lane_base + d1 + 16 * wg, x);
                 tmem_ld_wait();
                 if (tid == 0) KDA_TRACE(t, 2);
 #pragma unroll
-                for (int hx = 0; hx < 2; ++hx) {
-                    const float* x = xx[hx];
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c4 = 8 * wg + 4 * hx + 2 * cc;  // fp32 chunk of the 8 columns
-                        const float4 ua =
-                            *reinterpret_cast<const float4*>(urow + ((c4 ^ (row & 15)) << 4));
-                        const float4 ub = *reinterpret_cast<const float4*>(
-                            urow + (((c4 + 1) ^ (row & 15)) << 4));
-                        const float d8[8] = {ua.x - x[8 * cc], ua.y - x[8 * cc + 1],
-                                             ua.z - x[8 * cc + 2], ua.w - x[8 * cc + 3],
-                                             ub.x - x[8 * cc + 4], ub.y - x[8 * cc + 5],
-                                             ub.z - x[8 * cc + 6], ub.w - x[8 * cc + 7]};
-                        uint4 hi, lo;
-                        pk8_hilo(d8, hi, lo);
-                        const uint32_t off = sw128_chunk(row, 4 * wg + 2 * hx + cc);
-                        *reinterpret_cast<uint4*>(vt + off) = hi;
-                        *reinterpret_cast<uint4*>(vt + 8192 + off) = lo;
-                    }
-                    if (tid == 0 && hx == 0) KDA_TRACE(t, 22);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c4 = 4 * wg + 2 * cc;  // fp32 chunk of the 8 columns
+                    const float4 ua = *reinterpret_cast<const float4*>(urow + ((c4 ^ (row & 7)) << 4));
+                    const float4 ub =
+                        *reinterpret_cast<const float4*>(urow + (((c4 + 1) ^ (row & 7)) << 4));
+                    const float d8[8] = {ua.x - x[8 * cc], ua.y - x[8 * cc + 1],
+                                         ua.z - x[8 * cc + 2], ua.w - x[8 * cc + 3],
+                                         ub.x - x[8 * cc + 4], ub.y - x[8 * cc + 5],
+                                         ub.z - x[8 * cc + 6], ub.w - x[8 * cc + 7]};
+                    uint4 hi, lo;
+                    pk8_hilo(d8, hi, lo);
+                    const uint32_t off = sw64_chunk(row, 2 * wg + cc);
+                    *reinterpret_cast<uint4*>(vt + off) = hi;
+                    *reinterpret_cast<uint4*>(vt + kVtLo + off) = lo;
                 }
                 if (tid == 0) KDA_TRACE(t, 23);
                 fence_async_smem();
@@ -1286,14 +1283,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             // E2: S <- gamma^C * S + dS ;  bf16 copy of S for the next chunk's MMA1
             {
                 const float gam = reinterpret_cast<const float*>(sm + kGam + st * 512)[row];
-                float v[2][16];
-                tmem_ld16(tmem + lane_base + kDS + 32 * wg, v[0]);
-                tmem_ld16(tmem + lane_base + kDS + 32 * wg + 16, v[1]);
+                float v[16];
+                tmem_ld16(tmem + lane_base + kDS + 16 * wg, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int hx = 0; hx < 2; ++hx)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) S[16 * hx + e] = fmaf(gam, S[16 * hx + e], v[hx][e]);
+                for (int e = 0; e < 16; ++e) S[e] = fmaf(gam, S[e], v[e]);
                 write_sbf();
             }
             fence_async_smem();
@@ -1309,26 +1303,24 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                 tc_fence_after();
                 if (tid == 64) KDA_TRACE(t, 8);
                 const int r = row - 64;
-                float v[2][16];
-                tmem_ld16(tmem + lane_base + d1 + 32 * wg, v[0]);
-                tmem_ld16(tmem + lane_base + d1 + 32 * wg + 16, v[1]);
+                float v[16];
+                tmem_ld16(tmem + lane_base + d1 + 16 * wg, v);
                 tmem_ld_wait();
                 if (t0 + kC <= t_end) {
-                    // full chunk: stage the 64 x 64 tile, one TMA store writes it
+                    // full chunk: stage the 64 x 32 tile, one TMA store writes it
                     if (tid == 64) bulk_wait_read0();  // the previous store has read the tile
                     named_bar_sync(2, 128);
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
+                    for (int q8 = 0; q8 < 2; ++q8) {
                         float a8[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) a8[e] = v[q8 >> 1][8 * (q8 & 1) + e];
-                        *reinterpret_cast<uint4*>(sm + kOSt + sw128_chunk(r, 4 * wg + q8)) =
-                            pk8(a8);
+                        for (int e = 0; e < 8; ++e) a8[e] = v[8 * q8 + e];
+                        *reinterpret_cast<uint4*>(sm + kOSt + sw64_chunk(r, 2 * wg + q8)) = pk8(a8);
                     }
                     fence_async_smem();
                     if (named_bar_or(2, 128, !ok)) break;
                     if (tid == 64) {
-                        tma_store_3d(&p.to, sm + kOSt, kJ * half, h, (int)t0);
+                        tma_store_3d(&p.to, sm + kOSt, kJ * part, h, (int)t0);
                         bulk_commit();
                     }
                 } else {
@@ -1337,10 +1329,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                     if (t0 + r < t_end) {
                         __nv_bfloat16* orow = p.o + ((size_t)(t0 + r) * p.H + h) * kD + jc;
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
+                        for (int q8 = 0; q8 < 2; ++q8) {
                             float a8[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) a8[e] = v[q8 >> 1][8 * (q8 & 1) + e];
+                            for (int e = 0; e < 8; ++e) a8[e] = v[8 * q8 + e];
                             *reinterpret_cast<uint4*>(orow + 8 * q8) = pk8(a8);
                         }
                     }
@@ -1358,7 +1350,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
     const bool aborted = s_abort != 0;
     if (p.S_out && !aborted && epi) {
 #pragma unroll
-        for (int jj = 0; jj < 32; jj += 4)
+        for (int jj = 0; jj < 16; jj += 4)
             *reinterpret_cast<float4*>(p.S_out + sofs + jj) =
                 make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
     }
@@ -1398,15 +1390,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H) {
+// [T_total, H, 128] bf16 tensor, boxes of `box_cols` columns x 1 head x 64 rows; 64-column
+// boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int box_cols = 64) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
     const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-    const cuuint32_t box[3] = {64, 1, kC};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, kC};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1485,7 +1480,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     }
 
     StateParams sp;
-    if (a.T_total > 0 && !make_map(&sp.to, a.o, a.T_total, a.H)) return cudaErrorInvalidValue;
+    if (a.T_total > 0 && !make_map(&sp.to, a.o, a.T_total, a.H, kJ)) return cudaErrorInvalidValue;
     sp.pkg = pkg;
     sp.cu = a.cu_seqlens;
     sp.chunk_off = chunk_off;

@@ -1,8 +1,8 @@
 // tc_util.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, TMA / bulk copies,
 // tcgen05 (TMEM allocation, MMA, loads) and the shared-memory operand descriptors.
 //
-// Operand tiles used with these helpers are bf16 in the 128-byte-swizzled canonical
-// layout: the tile is stored as [block][row][128 B], where a "row" holds 64 consecutive
+// Operand tiles used with these helpers are mostly bf16 in the 128-byte-swizzled canonical
+// layout (a 64-byte-swizzled variant serves 32-element-wide tiles): the tile is stored as [block][row][128 B], where a "row" holds 64 consecutive
 // elements of the contiguous dimension, 8 rows form a 1024-byte swizzle atom and the
 // 16-byte chunk j of row r sits at chunk position (j ^ (r % 8)).  Every tile starts on
 // a 1024-byte boundary.  Such a tile serves two ways:
@@ -233,6 +233,17 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle (8-row x 64-byte atoms of 512 bytes).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(4) << 61;  // 64-byte swizzle
+    return d;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
                                                   bool b_mn_major) {
@@ -254,6 +265,12 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col, int rows) {
 // one 64-column block.
 __device__ __forceinline__ uint32_t sw128_chunk(int row, int j) {
     return static_cast<uint32_t>(row * 128 + ((j ^ (row & 7)) << 4));
+}
+
+// Byte offset of the 16-byte chunk j (0..3) of `row` in a 64-byte-swizzled tile of 64-byte
+// rows (the chunk index is XORed with bits 1..2 of the row).
+__device__ __forceinline__ uint32_t sw64_chunk(int row, int j) {
+    return static_cast<uint32_t>(row * 64 + ((j ^ ((row >> 1) & 3)) << 4));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
