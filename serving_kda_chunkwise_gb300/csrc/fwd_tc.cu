@@ -46,8 +46,7 @@ using namespace tc;
 
 constexpr int kC = 64;    // chunk length
 constexpr int kD = 128;   // head dim (dk = dv)
-constexpr int kThreads = 256;       // row-work threads of the intra kernel (8 warps)
-constexpr int kIntraThreads = 288;  // + one warp whose lane 0 issues copies and MMAs
+constexpr int kIntraThreads = 288;  // 8 row-work warps + one warp whose lane 0 issues copies and MMAs
 constexpr int kIss = 256;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
@@ -236,9 +235,9 @@ constexpr int kLd = 68;                       // padded fp32 row stride of L and
                                               // bank conflicts in the 16x16 tile fragments)
 constexpr uint32_t kSL = kBStk, kST = kBStk + 64 * kLd * 4;
 static_assert(kST + 64 * kLd * 4 <= kBStk + 40960, "L and T must fit the B stack");
-// the solve's per-warp scratch (4 warps x 16 x 20 floats) reuses the A-lo region
+// the solve's scratch (9 tiles of 16 x 20 floats) reuses the A-lo region
 constexpr uint32_t kSolveScr = kALo;
-static_assert(4 * 16 * 20 * 4 <= 16384, "solve scratch must fit the A-lo region");
+static_assert(9 * 16 * 20 * 4 <= 16384, "solve scratch must fit the A-lo region");
 // TMEM columns: main Gram accumulator [0, 160), diagonal-column lo correction [160, 224),
 // q-side lo correction [256, 416);
 // later W [0, 128) and U [128, 256).
@@ -342,6 +341,18 @@ __device__ __forceinline__ void tile_zero(Tile16& f) {
         for (int q = 0; q < 4; ++q) f.c[nn][q] = 0.f;
 }
 
+// f = scale * X
+__device__ __forceinline__ void tile_load(Tile16& f, const float* X, int ld, float scale) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int row = g + 8 * (q >> 1), col = 8 * nn + 2 * t + (q & 1);
+            f.c[nn][q] = scale * X[row * ld + col];
+        }
+}
+
 // X = scale * f + diag * I
 __device__ __forceinline__ void tile_store(const Tile16& f, float* X, int ld, float scale,
                                            float diag) {
@@ -380,9 +391,8 @@ __device__ __forceinline__ void tile_mma(Tile16& f, const float* A, int lda, con
 
 // T = (I + L)^{-1} for the 64x64 strictly lower L (16x16 blocks).  Warp w < 4 first inverts
 // diagonal block w by forward substitution in fp32 (lane j holds column j:
-// T_ij = delta_ij - sum_{k<i} L_ik T_kj); then the off-diagonal blocks follow by distance d:
-// T_{s,s'} = -T_ss sum_{t=s'}^{s-1} L_st T_{t,s'}.  `scr` is per-warp scratch of 16 x kScrLd
-// floats.
+// T_ij = delta_ij - sum_{k<i} L_ik T_kj); the off-diagonal blocks follow from the expansion
+// below.  `scr_all` holds 9 scratch tiles of 16 x kScrLd floats.
 constexpr int kScrLd = 20;
 constexpr int kScrTile = 16 * kScrLd;
 
@@ -390,7 +400,6 @@ __device__ __forceinline__ int lane16() { return threadIdx.x & 15; }
 
 __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* scr_all,
                                              int warp, int iter_for_trace) {
-    float* sP = scr_all + warp * kScrTile;  // per-warp scratch tile
     KDA_ITRACE(iter_for_trace, 0);
     if (warp < 4) {
         const float* Lb = sL + (16 * warp) * kLd + 16 * warp;
@@ -418,23 +427,65 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
     KDA_ITRACE(iter_for_trace, 1);
     __syncthreads();
     KDA_ITRACE(iter_for_trace, 2);
-#pragma unroll
-    for (int d = 1; d < 4; ++d) {
-        if (warp < 4 - d) {
-            const int sp = warp, s = warp + d;
-            Tile16 y, f;
-            tile_zero(y);
-            for (int t = sp; t < s; ++t)
-                tile_mma(y, sL + (16 * s) * kLd + 16 * t, kLd, sT + (16 * t) * kLd + 16 * sp, kLd);
-            tile_store(y, sP, kScrLd, 1.f, 0.f);
-            __syncwarp();
-            tile_zero(f);
-            tile_mma(f, sT + (16 * s) * kLd + 16 * s, kLd, sP, kScrLd);
-            tile_store(f, sT + (16 * s) * kLd + 16 * sp, kLd, -1.f, 0.f);
-        }
-        KDA_ITRACE(iter_for_trace, 2 + d);
-        __syncthreads();
+    // Off-diagonal blocks: with Delta the inverted diagonal blocks and F_ij = Delta_i L_ij
+    // (i > j, nilpotent), T = (I + F)^{-1} Delta = (I - F + F^2 - F^3) Delta, so
+    //   T_{i+1,i} = -F_{i+1,i} Delta_i,
+    //   T_20 = G20 Delta_0, G20 = -F20 + F21 F10;   T_31 = G31 Delta_1, G31 = -F31 + F32 F21;
+    //   T_30 = G30 Delta_0, G30 = -F30 + F31 F10 - F32 G20:
+    // four levels of independent 16x16 products instead of a chain by distance.
+    auto Lb = [&](int i, int j) { return sL + (16 * i) * kLd + 16 * j; };
+    auto Tb = [&](int i, int j) { return sT + (16 * i) * kLd + 16 * j; };
+    auto Sc = [&](int k) { return scr_all + k * kScrTile; };  // F10 F21 F32 F20 F31 F30 G20 G31 H30
+    // level 1: F_ij = Delta_i L_ij for the six off-diagonal blocks
+    if (warp < 6) {
+        // (i, j) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0), packed in nibbles
+        const int i = (0x332321 >> (4 * warp)) & 15, j = (0x010210 >> (4 * warp)) & 15;
+        Tile16 f;
+        tile_zero(f);
+        tile_mma(f, Tb(i, i), kLd, Lb(i, j), kLd);
+        tile_store(f, Sc(warp), kScrLd, 1.f, 0.f);
     }
+    __syncthreads();
+    // level 2: G20, G31, H30 = -F30 + F31 F10; T10, T21, T32
+    if (warp < 3) {
+        // G20 = -F20 + F21 F10, G31 = -F31 + F32 F21, H30 = -F30 + F31 F10
+        const int fa = (0x421 >> (4 * warp)) & 15, fb = (0x010 >> (4 * warp)) & 15;
+        Tile16 f;
+        tile_load(f, Sc(3 + warp), kScrLd, -1.f);
+        tile_mma(f, Sc(fa), kScrLd, Sc(fb), kScrLd);
+        tile_store(f, Sc(6 + warp), kScrLd, 1.f, 0.f);
+    } else if (warp < 6) {
+        const int k = warp - 3;  // T_{k+1,k} = -F_{k+1,k} Delta_k
+        Tile16 f;
+        tile_zero(f);
+        tile_mma(f, Sc(k), kScrLd, Tb(k, k), kLd);
+        tile_store(f, Tb(k + 1, k), kLd, -1.f, 0.f);
+    }
+    __syncthreads();
+    // levels 3 and 4: G30 then T30 (warp 0); T20, T31 (warps 1, 2)
+    if (warp == 0) {
+        Tile16 f, q;
+        tile_load(f, Sc(8), kScrLd, 1.f);  // H30
+        tile_zero(q);
+        tile_mma(q, Sc(2), kScrLd, Sc(6), kScrLd);  // F32 G20
+#pragma unroll
+        for (int nn = 0; nn < 2; ++nn)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) f.c[nn][e] -= q.c[nn][e];
+        tile_store(f, Sc(8), kScrLd, 1.f, 0.f);  // G30
+        __syncwarp();
+        tile_zero(q);
+        tile_mma(q, Sc(8), kScrLd, Tb(0, 0), kLd);
+        tile_store(q, Tb(3, 0), kLd, 1.f, 0.f);
+    } else if (warp < 3) {
+        const int k = warp - 1;  // T_{k+2,k} = G_{k+2,k} Delta_k
+        Tile16 f;
+        tile_zero(f);
+        tile_mma(f, Sc(6 + k), kScrLd, Tb(k, k), kLd);
+        tile_store(f, Tb(k + 2, k), kLd, 1.f, 0.f);
+    }
+    KDA_ITRACE(iter_for_trace, 3);
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
