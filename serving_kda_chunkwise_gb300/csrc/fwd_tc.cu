@@ -251,9 +251,29 @@ struct ItemInfo {
     size_t pkg;  // package index
 };
 
+// Loads that are issued well ahead of their use.  The asm keeps each load where it is
+// written: a plain load may be sunk to its first use, which would expose its latency there.
+__device__ __forceinline__ int4 ld_ahead(const int4* q) {
+    int4 r;
+    asm volatile("ld.global.nc.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(q));
+    return r;
+}
+__device__ __forceinline__ float ld_ahead(const float* q) {
+    float r;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(q));
+    return r;
+}
+__device__ __forceinline__ unsigned short ld_ahead(const __nv_bfloat16* q) {
+    unsigned short r;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(r) : "l"(q));
+    return r;
+}
+
 // Item = chunk * H + head.  The table entry is fetched ahead and decoded when needed.
 __device__ __forceinline__ int4 fetch_item(const IntraParams& p, int item) {
-    return __ldg(p.chunk_tab + item / p.H);
+    return ld_ahead(p.chunk_tab + item / p.H);
 }
 __device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item, int4 e) {
     ItemInfo it;
@@ -400,7 +420,6 @@ __device__ __forceinline__ int lane16() { return threadIdx.x & 15; }
 
 __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* scr_all,
                                              int warp, int iter_for_trace) {
-    KDA_ITRACE(iter_for_trace, 0);
     if (warp < 4) {
         const float* Lb = sL + (16 * warp) * kLd + 16 * warp;
         const int j = lane16();
@@ -424,9 +443,7 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
 #pragma unroll
             for (int i = 0; i < 16; ++i) sT[(16 * warp + i) * kLd + 16 * warp + j] = tc[i];
     }
-    KDA_ITRACE(iter_for_trace, 1);
     __syncthreads();
-    KDA_ITRACE(iter_for_trace, 2);
     // Off-diagonal blocks: with Delta the inverted diagonal blocks and F_ij = Delta_i L_ij
     // (i > j, nilpotent), T = (I + F)^{-1} Delta = (I - F + F^2 - F^3) Delta, so
     //   T_{i+1,i} = -F_{i+1,i} Delta_i,
@@ -484,7 +501,6 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
         tile_mma(f, Sc(6 + k), kScrLd, Tb(k, k), kLd);
         tile_store(f, Tb(k + 2, k), kLd, 1.f, 0.f);
     }
-    KDA_ITRACE(iter_for_trace, 3);
     __syncthreads();
 }
 
@@ -553,7 +569,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
     KDA_PHASE_INIT();
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
         KDA_PHASE(7);
-        (void)0;
         const int b = iter & 1;
         uint8_t* qk = sm + b * kQKBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
@@ -564,7 +579,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         float beta_next = 0.f;  // the next item's beta[tid]: loaded mid-item, stored later
         if (has_next) {
             nx = decode_item(p, next, raw1);
-            alog_nx = __ldg(p.A_log + nx.h);
+            alog_nx = ld_ahead(p.A_log + nx.h);
         }
         raw1 = raw2;
         if (next + 2 * (int)gridDim.x < n_items) raw2 = fetch_item(p, next + 2 * gridDim.x);
@@ -577,7 +592,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             s_abort = 1;
         }
         KDA_PHASE(0);
-        (void)0;
         // G[i][e]: cumulative gate of row 4 rg + i, channel ch0 + e; gl: G of the last row.
         // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
         // the 8 warps' totals (shared memory).
@@ -619,7 +633,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         __syncthreads();
         KDA_PHASE(9);
         if (has_next && tid < nx.L)
-            beta_next = __bfloat162float(p.beta[(size_t)(nx.t0 + tid) * p.H + nx.h]);
+            beta_next = __bfloat162float(__ushort_as_bfloat16(
+                ld_ahead(p.beta + (size_t)(nx.t0 + tid) * p.H + nx.h)));
         if (tid < kD) {  // exclusive scan over the warps, in place, one channel per thread
             float v[8];
 #pragma unroll
@@ -872,7 +887,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             float* sT = reinterpret_cast<float*>(sm + kST);
             float* sScr = reinterpret_cast<float*>(sm + kSolveScr);
             solve_tril64(sL, sT, sScr, warp, iter);
-            KDA_ITRACE(iter, 6);
             KDA_PHASE(8);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile, written twice: the
             // 128-row operand [M; M] of the W / U MMA

@@ -166,6 +166,98 @@ def fwd_chunked(q, k, v, beta, z, A_log, g_min: float, S0=None, cu_seqlens=None,
     return o, S_out
 
 
+_copy_streams = {}
+
+
+def _streams(device):
+    key = torch.device(device).index or 0
+    if key not in _copy_streams:
+        _copy_streams[key] = tuple(torch.cuda.Stream(device=device) for _ in range(3))
+    return _copy_streams[key]
+
+
+def fwd_chunked_host(q, k, v, beta, z, A_log, g_min: float, S0=None, cu_seqlens=None, N=None,
+                     o=None, S_out=None, segments: int = 8, device="cuda"):
+    """kda_fwd_chunked from (pinned) host tensors to (pinned) host outputs.
+
+    Same arguments as fwd_chunked, all on the host (cu_seqlens an int32 host tensor or None).
+    The work is cut into `segments` pieces and pipelined on three streams: the host-to-device
+    copy of piece s + 1, the forward of piece s and the device-to-host copy of piece s - 1
+    overlap.  One sequence is cut at multiples of 64 tokens, its fp32 state carried on the
+    device from piece to piece (the result equals one call over the whole sequence); several
+    sequences are grouped whole.  Returns (o, S_out) on the host.
+    """
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    dev = torch.device(device)
+    if cu_seqlens is None:
+        N = 1 if N is None else int(N)
+        cu = [T * n // N for n in range(N + 1)]
+    else:
+        cu = [int(x) for x in cu_seqlens.tolist()]
+        N = len(cu) - 1
+    # pieces: (first token, end token, first sequence, end sequence)
+    if N == 1:
+        step = -(-max(T, 1) // max(segments, 1))
+        step = -(-step // C_CHUNK) * C_CHUNK
+        pieces = [(a, min(a + step, T), 0, 1) for a in range(0, T, step)] or [(0, 0, 0, 1)]
+    else:
+        pieces, first, target = [], 0, max(T // max(segments, 1), 1)
+        for n in range(1, N + 1):
+            if cu[n] - cu[first] >= target or n == N:
+                pieces.append((cu[first], cu[n], first, n))
+                first = n
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype).pin_memory()
+    if S_out is None:
+        S_out = torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory()
+    s_in, s_comp, s_out = _streams(dev)
+    cur = torch.cuda.current_stream(dev)
+    for s in (s_in, s_comp, s_out):
+        s.wait_stream(cur)
+    with torch.cuda.stream(s_in):
+        dq, dk_, dv_, db, dz = (torch.empty_like(t, device=dev) for t in (q, k, v, beta, z))
+        dA = A_log.to(dev, non_blocking=True)
+        S = (torch.zeros((N, H, dk, dv), dtype=torch.float32, device=dev) if S0 is None
+             else S0.to(dev, non_blocking=True))
+        do = torch.empty((T, H, dv), dtype=q.dtype, device=dev)
+        longest = max(b - a for a, b, _, _ in pieces)
+        most = max(n1 - n0 for _, _, n0, n1 in pieces)
+        need = workspace_size(longest, most, H, dk, dv, q.dtype)
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    done_in = []
+    for a, b, n0, n1 in pieces:
+        with torch.cuda.stream(s_in):
+            for dst, src in ((dq, q), (dk_, k), (dv_, v), (db, beta), (dz, z)):
+                dst[a:b].copy_(src[a:b], non_blocking=True)
+            cu_d = None
+            if N > 1:
+                cu_d = torch.tensor([c - cu[n0] for c in cu[n0:n1 + 1]], dtype=torch.int32).to(
+                    dev, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_in)
+            done_in.append((ev, cu_d))
+    for (a, b, n0, n1), (ev, cu_d) in zip(pieces, done_in):
+        s_comp.wait_event(ev)
+        Sp = S[n0:n1]
+        if b > a or N > 1:
+            fwd_chunked(dq[a:b], dk_[a:b], dv_[a:b], db[a:b], dz[a:b], dA, g_min, S0=Sp,
+                        cu_seqlens=cu_d, N=n1 - n0, o=do[a:b], S_out=Sp, workspace=ws,
+                        stream=s_comp)
+        ev2 = torch.cuda.Event()
+        ev2.record(s_comp)
+        s_out.wait_event(ev2)
+        with torch.cuda.stream(s_out):
+            o[a:b].copy_(do[a:b], non_blocking=True)
+    with torch.cuda.stream(s_out):
+        S_out.copy_(S, non_blocking=True)
+    for t in (dq, dk_, dv_, db, dz, dA, S, do, ws):
+        t.record_stream(s_out)
+    cur.wait_stream(s_out)
+    s_out.synchronize()
+    return o, S_out
+
+
 def decode_step(q, k, v, beta, z, A_log, g_min: float, S, o=None, stream=None):
     """One decode token per sequence; S [N, H, dk, dv] fp32 is updated in place.
 
