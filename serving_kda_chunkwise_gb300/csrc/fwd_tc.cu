@@ -766,22 +766,25 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             tc_fence_after();
             constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
             constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
+            // descriptors differ only in the start-address field (address / 16)
+            const uint64_t dA = sdesc_sw128(sbase + kAStk, 0, 1024);
+            const uint64_t dB = sdesc_sw128(sbase + kBStk, 0, 1024);
+            const uint64_t dAl = sdesc_sw128(sbase + kALo, 0, 1024);
+            const uint64_t dBl = sdesc_sw128(sbase + kBLo, 0, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kofs = (ks & 3) * 32;
-                const uint64_t ah = sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + kofs, 0, 1024);
-                const uint64_t bh = sdesc_sw128(sbase + kBStk + (ks >> 2) * 20480 + kofs, 0, 1024);
+                const uint64_t ah = dA + (((ks >> 2) * 16384 + kofs) >> 4);
+                const uint64_t bh = dB + (((ks >> 2) * 20480 + kofs) >> 4);
                 mma_bf16(tmem, ah, bh, id160, ks > 0);
-                const uint64_t al = sdesc_sw128(sbase + kALo + (ks >> 2) * 8192 + kofs, 0, 1024);
-                mma_bf16(tmem + kTLo, al, bh, id160, ks > 0);
+                mma_bf16(tmem + kTLo, dAl + (((ks >> 2) * 8192 + kofs) >> 4), bh, id160, ks > 0);
             }
             // diagonal-column lo parts of all four versions at once: D' = A_hi Blo^T
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kofs = (ks & 3) * 32;
-                const uint64_t ah = sdesc_sw128(sbase + kAStk + (ks >> 2) * 16384 + kofs, 0, 1024);
-                const uint64_t bl = sdesc_sw128(sbase + kBLo + (ks >> 2) * 8192 + kofs, 0, 1024);
-                mma_bf16(tmem + kTDiag, ah, bl, id64, ks > 0);
+                mma_bf16(tmem + kTDiag, dA + (((ks >> 2) * 16384 + kofs) >> 4),
+                         dBl + (((ks >> 2) * 8192 + kofs) >> 4), id64, ks > 0);
             }
             mma_commit(mma_bar);
         }
@@ -925,13 +928,14 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         if (tid == kIss) {
             tc_fence_after();
             constexpr uint32_t idesc = idesc_bf16(128, 128, false, true);
+            const uint64_t dM = sdesc_sw128(sbase + kMTile, 0, 1024);
+            const uint64_t dK = sdesc_sw128(sbase + kKbar, 8192, 1024);
+            const uint64_t dV = sdesc_sw128(sbase + kVBuf, 8192, 1024);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t am = sdesc_sw128(sbase + kMTile + ks * 32, 0, 1024);
-                mma_bf16(tmem, am, sdesc_sw128(sbase + kKbar + ks * 2048, 8192, 1024), idesc,
-                         ks > 0);
-                mma_bf16(tmem + 128, am, sdesc_sw128(sbase + kVBuf + ks * 2048, 8192, 1024),
-                         idesc, ks > 0);
+                const uint64_t am = dM + ((ks * 32) >> 4);
+                mma_bf16(tmem, am, dK + ((ks * 2048) >> 4), idesc, ks > 0);
+                mma_bf16(tmem + 128, am, dV + ((ks * 2048) >> 4), idesc, ks > 0);
             }
             mma_commit(mma_bar);
         }
@@ -1166,16 +1170,19 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
 
     if (tid == kMmaT && nch > 0) {
         // ------------------------------------------------------------ MMA thread
+        // Descriptors differ only in the start-address field (address / 16, low 14 bits,
+        // which never carries for shared-memory offsets): base values are built once and
+        // offsets added.
+        const uint64_t dA1 = sdesc_sw128(sbase + kPA, 0, 1024);
+        const uint64_t dS1 = sdesc_sw64(sbase + kSbf, 0, 512);
         auto issue_mma1 = [&](int t) {  // D1(t) = [W; Gam Q] S
-            const uint32_t sA = sbase + kPA + (t & 1) * kPkgPartA;
+            const uint64_t a0 = dA1 + ((t & 1) * kPkgPartA >> 4);
             constexpr uint32_t id = idesc_bf16(128, kJ, false, true);
+            const uint32_t d = tmem + uint32_t(kJ) * (t & 1);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint64_t a =
-                    sdesc_sw128(sA + (ks >> 2) * kPkgStkBlk + (ks & 3) * 32, 0, 1024);
-                const uint64_t b = sdesc_sw64(sbase + kSbf + ks * 1024, 0, 512);
-                mma_bf16(tmem + uint32_t(kJ) * (t & 1), a, b, id, ks > 0);
-            }
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16(d, a0 + (((ks >> 2) * kPkgStkBlk + (ks & 3) * 32) >> 4),
+                         dS1 + ((ks * 1024) >> 4), id, ks > 0);
             mma_commit(mma1);
         };
         // MMA3(t), K steps [ks0, ks0 + 2): A_hi Vt_hi + A_hi Vt_lo + A_lo Vt_hi into the O
