@@ -1206,6 +1206,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                 mma_bf16(d, al, vh, id3, 1);
             }
         };
+        const uint64_t dKt = sdesc_sw128(sbase + kPB, 8192, 1024);
+        const uint64_t dVt2 = sdesc_sw64(sbase + kVt, 0, 512);
         int t = 0;
         for (; t < nch; ++t) {
             const int st = t & 1;
@@ -1228,13 +1230,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             KDA_TRACE(t, 14);
             tc_fence_after();
             KDA_TRACE(t, 15);
-            const uint32_t sB = sbase + kPB + st * kPkgPartB;
-            const uint32_t sVt = sbase + kVt + st * kVtStage;
             constexpr uint32_t id2 = idesc_bf16(128, kJ, true, true);
+            const uint64_t k0 = dKt + (st * kPkgPartB >> 4), v0 = dVt2 + (st * kVtStage >> 4);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kDS, sdesc_sw128(sB + ks * 2048, 8192, 1024),
-                         sdesc_sw64(sVt + ks * 1024, 0, 512), id2, ks > 0);
+                mma_bf16(tmem + kDS, k0 + ((ks * 2048) >> 4), v0 + ((ks * 1024) >> 4), id2, ks > 0);
             mma_commit(mma2);
             KDA_TRACE(t, 16);
             issue_mma3(t, 0);
