@@ -13,9 +13,11 @@
 // Layout: one CTA of 256 threads per (sequence, head).  A state row of dv fp32 is
 // covered by dv/4 lanes with one float4 each (a warp reads 512 contiguous bytes for
 // dv = 128); the dk rows are spread over the 8 warps, so every thread holds
-// dk*dv/1024 floats in registers between the read and the write.  All state loads are
-// issued before the gate is evaluated so their latency overlaps it.  Loads and stores
-// use the streaming cache hint: the state is touched once per step.
+// dk*dv/1024 floats per pass.  The state is read twice: once for the two reductions (all
+// loads issued before the gate is evaluated, so their latency overlaps it) and again, from
+// L2, for the update, so that no thread holds the state in registers across the
+// reductions and more CTAs fit on an SM.  HBM sees one read and one write; the second
+// read and the write carry the streaming hint.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -49,11 +51,13 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
     const int sub = lane / kLanesPerRow;
     float* Sp = S + (size_t)nh * DK * DV;
 
-    float4 s[kRowsPerThread];
+    // first half of this thread's rows in flight while the gate is evaluated
+    constexpr int kHalf = (kRowsPerThread + 1) / 2;
+    float4 s[kHalf];
 #pragma unroll
-    for (int m = 0; m < kRowsPerThread; ++m) {
+    for (int m = 0; m < kHalf; ++m) {
         const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
-        s[m] = __ldcs(reinterpret_cast<const float4*>(Sp + (size_t)row * DV) + col4);
+        s[m] = __ldcg(reinterpret_cast<const float4*>(Sp + (size_t)row * DV) + col4);
     }
 
     const float scale = expf(__ldg(A_log + h));
@@ -66,14 +70,25 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
     __syncthreads();
 
     float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int m = 0; m < kRowsPerThread; ++m) {
+    auto accumulate = [&](int m, const float4& sv) {
         const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
         const float ak = s_alpha[row] * s_k[row], aq = s_alpha[row] * s_q[row];
-        pa[0] = fmaf(ak, s[m].x, pa[0]); pa[1] = fmaf(ak, s[m].y, pa[1]);
-        pa[2] = fmaf(ak, s[m].z, pa[2]); pa[3] = fmaf(ak, s[m].w, pa[3]);
-        pb[0] = fmaf(aq, s[m].x, pb[0]); pb[1] = fmaf(aq, s[m].y, pb[1]);
-        pb[2] = fmaf(aq, s[m].z, pb[2]); pb[3] = fmaf(aq, s[m].w, pb[3]);
+        pa[0] = fmaf(ak, sv.x, pa[0]); pa[1] = fmaf(ak, sv.y, pa[1]);
+        pa[2] = fmaf(ak, sv.z, pa[2]); pa[3] = fmaf(ak, sv.w, pa[3]);
+        pb[0] = fmaf(aq, sv.x, pb[0]); pb[1] = fmaf(aq, sv.y, pb[1]);
+        pb[2] = fmaf(aq, sv.z, pb[2]); pb[3] = fmaf(aq, sv.w, pb[3]);
+    };
+    {
+        float4 s2[kRowsPerThread - kHalf];  // second half, issued before the first is used
+#pragma unroll
+        for (int m = kHalf; m < kRowsPerThread; ++m) {
+            const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
+            s2[m - kHalf] = __ldcg(reinterpret_cast<const float4*>(Sp + (size_t)row * DV) + col4);
+        }
+#pragma unroll
+        for (int m = 0; m < kHalf; ++m) accumulate(m, s[m]);
+#pragma unroll
+        for (int m = kHalf; m < kRowsPerThread; ++m) accumulate(m, s2[m - kHalf]);
     }
 #pragma unroll
     for (int off = kLanesPerRow; off < 32; off <<= 1)
@@ -114,13 +129,15 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
 #pragma unroll
     for (int m = 0; m < kRowsPerThread; ++m) {
         const int row = m * kRowsPerPass + warp * kRowsPerWarp + sub;
+        float4* sp = reinterpret_cast<float4*>(Sp + (size_t)row * DV) + col4;
+        const float4 sv = __ldcs(sp);  // second read, from L2
         const float al = s_alpha[row], kr = s_k[row];
         float4 r;
-        r.x = fmaf(al, s[m].x, kr * u4.x);
-        r.y = fmaf(al, s[m].y, kr * u4.y);
-        r.z = fmaf(al, s[m].z, kr * u4.z);
-        r.w = fmaf(al, s[m].w, kr * u4.w);
-        __stcs(reinterpret_cast<float4*>(Sp + (size_t)row * DV) + col4, r);
+        r.x = fmaf(al, sv.x, kr * u4.x);
+        r.y = fmaf(al, sv.y, kr * u4.y);
+        r.z = fmaf(al, sv.z, kr * u4.z);
+        r.w = fmaf(al, sv.w, kr * u4.w);
+        __stcs(sp, r);
     }
 }
 
