@@ -13,11 +13,11 @@
 // Layout: one CTA of 256 threads per (sequence, head).  A state row of dv fp32 is
 // covered by dv/4 lanes with one float4 each (a warp reads 512 contiguous bytes for
 // dv = 128); the dk rows are spread over the 8 warps, so every thread holds
-// dk*dv/1024 floats per pass.  The state is read twice: once for the two reductions (all
-// loads issued before the gate is evaluated, so their latency overlaps it) and again, from
-// L2, for the update, so that no thread holds the state in registers across the
-// reductions and more CTAs fit on an SM.  HBM sees one read and one write; the second
-// read and the write carry the streaming hint.
+// dk*dv/1024 floats.  The state is read twice: once for the two reductions (half of a
+// thread's rows in flight while the gate is evaluated, the other half issued before the
+// first is used) and again, from L2, for the update, so that no thread holds the whole
+// state in registers and four CTAs fit on an SM.  HBM sees one read and one write; the
+// second read and the write carry the streaming hint.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
