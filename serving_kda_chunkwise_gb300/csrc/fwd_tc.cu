@@ -9,12 +9,15 @@
 // The last line (chunk-to-chunk update) is the recurrence unrolled over one chunk.
 //
 // Three launches on the caller's stream:
-//   plan_kernel   chunk offsets of every sequence (exclusive scan of ceil(len/64)).
-//   intra_kernel  every (chunk, head) in parallel (persistent, one CTA per SM, inputs by
-//                 TMA, next item prefetched): gate + in-chunk cumsum, the two sub-tiled
-//                 Gram matrices in ONE tcgen05 MMA, the UT solve on CUDA cores in fp32,
-//                 W and U by tcgen05; writes one "package" per (head, chunk) whose bytes
-//                 are the shared-memory image of the state kernel's MMA operands.
+//   plan_kernel   chunk offsets of every sequence (exclusive scan of ceil(len/64)) and a
+//                 table entry per chunk (first row, sequence, rows).
+//   intra_kernel  every (chunk, head) in parallel (persistent, one CTA per SM: 8 row-work
+//                 warps and one issuing warp; inputs by TMA, next item prefetched): gate +
+//                 in-chunk cumsum, the two sub-tiled Gram matrices in ONE tcgen05 MMA, the
+//                 UT solve (fp32 forward substitution on the diagonal blocks, tf32
+//                 mma.sync for the rest), W and U by tcgen05; writes one "package" per
+//                 (head, chunk) whose bytes are the shared-memory image of the state
+//                 kernel's MMA operands.
 //   state_kernel  four CTAs per (sequence, head), each owning 32 of the 128 value columns
 //                 (the columns of S evolve independently), serial over chunks: state S in
 //                 fp32 registers, packages streamed in by bulk copies (double buffered),
