@@ -293,7 +293,7 @@ def run_ours(args, rank, world, local_rank, dist):
         # the repo's host-buffer entry point: pinned host inputs in, pinned host outputs back,
         # host<->device copies of one piece overlapping the compute of its neighbours
         kda.fwd_chunked_host(host["q"], host["k"], host["v"], host["beta"], host["z"], A_host,
-                             sp.g_min, o=o_host, S_out=S_host, segments=8, device=dev)
+                             sp.g_min, o=o_host, S_out=S_host, segments=16, device=dev)
 
     e2e_steps = max(1, min(args.steps, 5))
     e2e_step()
