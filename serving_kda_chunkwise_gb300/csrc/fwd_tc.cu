@@ -11,8 +11,8 @@
 // Three launches on the caller's stream:
 //   plan_kernel   chunk offsets of every sequence (exclusive scan of ceil(len/64)) and a
 //                 table entry per chunk (first row, sequence, rows).
-//   intra_kernel  every (chunk, head) in parallel (persistent, one CTA per SM: 8 row-work
-//                 warps and one issuing warp; inputs by TMA, next item prefetched): gate +
+//   intra_kernel  every (chunk, head) in parallel (persistent, one CTA per SM: 8 warps, one
+//                 thread of which also issues; inputs by TMA, next item prefetched): gate +
 //                 in-chunk cumsum, the two sub-tiled Gram matrices in ONE tcgen05 MMA, the
 //                 UT solve (fp32 forward substitution on the diagonal blocks, tf32
 //                 mma.sync for the rest), W and U by tcgen05; writes one "package" per
@@ -49,8 +49,10 @@ using namespace tc;
 
 constexpr int kC = 64;    // chunk length
 constexpr int kD = 128;   // head dim (dk = dv)
-constexpr int kIntraThreads = 288;  // 8 row-work warps + one warp whose lane 0 issues copies and MMAs
-constexpr int kIss = 256;
+// 8 warps (two per SM sub-partition, so up to 255 registers a thread); lane 0 of warp 6,
+// whose row work is among the lightest, also issues every copy and MMA
+constexpr int kIntraThreads = 256;
+constexpr int kIss = 192;
 
 // ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
 // part A (needed at the start of a chunk): the row stack [W; Gam*Q] of the state kernel's
@@ -522,7 +524,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
     __shared__ int s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool rows = warp < 8;  // warps 0..7 do the row work; lane 0 of warp 8 issues copies and MMAs
     // operand passes: 8 channels [8 cg, 8 cg + 8) of rows [4 rg, 4 rg + 4)
     const int cg = tid & 15, rg = tid >> 4, sub = rg >> 2;
     const uint32_t cofs = (cg >> 3) * 8192;  // 64-column block of the channel group
@@ -548,25 +549,24 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
     // parity of the phase a load in flight will complete, or -1 (issuing thread; for a clean
     // abort)
     int pend_q[2] = {-1, -1}, pend_v = -1, pend_z = -1;
-    ItemInfo nx;        // the next item of this CTA
-    int4 raw1, raw2;    // table entries of the two items after it, fetched ahead of use
-    if ((int)blockIdx.x < n_items) {
-        nx = decode_item(p, blockIdx.x, fetch_item(p, blockIdx.x));
-        if ((int)(blockIdx.x + gridDim.x) < n_items) raw1 = fetch_item(p, blockIdx.x + gridDim.x);
-        if ((int)(blockIdx.x + 2 * gridDim.x) < n_items)
-            raw2 = fetch_item(p, blockIdx.x + 2 * gridDim.x);
-        if (tid == kIss) {
-            load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, nx, &qk_bar[0]);
-            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
-            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
-            pend_q[0] = 0;
-            pend_v = 0;
-            pend_z = 0;
-        }
-        load_beta(p, nx, reinterpret_cast<float*>(sm + kBeta), tid);
+    // The issuing thread walks the item table and publishes each item's description and
+    // A_log in s_item / s_alog (two slots by item parity) one item before its use, so the
+    // row warps start an item without global loads.
+    __shared__ ItemInfo s_item[2];
+    __shared__ float s_alog[2];
+    if ((int)blockIdx.x < n_items && tid == kIss) {
+        const ItemInfo first = decode_item(p, blockIdx.x, fetch_item(p, blockIdx.x));
+        load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, first, &qk_bar[0]);
+        load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, first, v_bar);
+        load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, first, z_bar);
+        pend_q[0] = 0;
+        pend_v = 0;
+        pend_z = 0;
+        s_item[0] = first;
+        s_alog[0] = __ldg(p.A_log + first.h);
     }
-    // A_log of the next item's head, fetched one item ahead
-    float alog_nx = ((int)blockIdx.x < n_items) ? __ldg(p.A_log + nx.h) : 0.f;
+    __syncthreads();
+    if ((int)blockIdx.x < n_items) load_beta(p, s_item[0], reinterpret_cast<float*>(sm + kBeta), tid);
 
     int iter = 0;
     KDA_PHASE_INIT();
@@ -575,18 +575,17 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         const int b = iter & 1;
         uint8_t* qk = sm + b * kQKBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
-        const ItemInfo it = nx;
-        const float alog = alog_nx;
+        const int itL = s_item[b].L;  // rows of this item (< 64 for a sequence's last chunk)
+        const float alog = s_alog[b];
         const int next = item + gridDim.x;
         const bool has_next = next < n_items;
-        float beta_next = 0.f;  // the next item's beta[tid]: loaded mid-item, stored later
-        if (has_next) {
-            nx = decode_item(p, next, raw1);
-            alog_nx = ld_ahead(p.A_log + nx.h);
-        }
-        raw1 = raw2;
-        if (next + 2 * (int)gridDim.x < n_items) raw2 = fetch_item(p, next + 2 * gridDim.x);
-        uint8_t* pkg = p.pkg + it.pkg * kPkgBytes;
+        unsigned short beta_nx[2] = {0, 0};  // issuing thread's warp: the next item's beta (bf16)
+        float alog_nx = 0.f;                 // issuing thread: the next item's A_log
+        // issuing thread: the next item's table entry, decoded once the scan is done
+        int4 raw_next;
+        if (tid == kIss && has_next) raw_next = fetch_item(p, next);
+        // this item's package (re-read where used: nothing held in registers across phases)
+        auto item_pkg = [&]() { return p.pkg + s_item[b].pkg * kPkgBytes; };
 
         // ---- gate and in-chunk cumsum
         if (mbar_wait(z_bar, iter & 1, p.err)) {
@@ -596,21 +595,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         }
         KDA_PHASE(0);
         // G[i][e]: cumulative gate of row 4 rg + i, channel ch0 + e; gl: G of the last row.
-        // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
-        // the 8 warps' totals (shared memory).
         // Cumulative gate in log2 units (G2 = G log2 e, so every decay factor is one ex2).
         // Scan: in-thread over 4 rows, in-warp over its two row groups (shuffle), then over
         // the 8 warps' totals (one thread per channel).
         float G[4][8], gl[8], pre[8];
         float* xtot = xrho + 512;  // [128]: G2 of the chunk's last row
-        if (rows) {
+        {
             const float scale2 = expf(alog) * 1.4426950408889634f;  // e^{A_log} log2 e
             const float gmin2 = p.g_min * 1.4426950408889634f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = 4 * rg + i;
-                const bool live = r < it.L;
+                const bool live = r < itL;
                 float zz[8];
                 ld8(sm + kZBuf + cofs + sw128_chunk(r, cg & 7), zz);
 #pragma unroll
@@ -635,9 +632,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         }
         __syncthreads();
         KDA_PHASE(9);
-        if (has_next && tid < nx.L)
-            beta_next = __bfloat162float(__ushort_as_bfloat16(
-                ld_ahead(p.beta + (size_t)(nx.t0 + tid) * p.H + nx.h)));
         if (tid < kD) {  // exclusive scan over the warps, in place, one channel per thread
             float v[8];
 #pragma unroll
@@ -651,13 +645,29 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             xtot[tid] = a;
         }
         __syncthreads();
-        // z is consumed: fetch the next item's (issued here, where a long phase follows,
-        // so that a slow issue never holds up a barrier)
-        if (tid == kIss && has_next) {
-            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
-            pend_z = (iter + 1) & 1;
+        // z is consumed: the issuing thread publishes the next item and fetches its z
+        // (issued here, where a long phase follows, so that a slow issue never holds up a
+        // barrier)
+        if (warp == (kIss >> 5) && has_next) {
+            if (tid == kIss) {
+                const ItemInfo nx = decode_item(p, next, raw_next);
+                s_item[b ^ 1] = nx;  // read after the next CTA barrier
+                alog_nx = ld_ahead(p.A_log + nx.h);
+                load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
+                pend_z = (iter + 1) & 1;
+            }
+            __syncwarp();
+            // the next item's beta (rows lane, lane + 32), stored into its slot during the
+            // operand pass, where this warp has no other work
+            const ItemInfo& nxs = s_item[b ^ 1];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int r = lane + 32 * h2;
+                if (r < nxs.L)
+                    beta_nx[h2] = ld_ahead(p.beta + (size_t)(nxs.t0 + r) * p.H + nxs.h);
+            }
         }
-        if (rows) {
+        {
             const float4 pa = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0);
             const float4 pb = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0 + 4);
             const float4 ga = *reinterpret_cast<const float4*>(xtot + ch0);
@@ -673,12 +683,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             }
         }
         KDA_PHASE(10);
-        if (rows && (rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
+        if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
 #pragma unroll
             for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
-        if (rows && rg == 15)
+        if (rg == 15)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(pkg + kPkgG)[ch0 + e] = ex2f(gl[e]);
+            for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(item_pkg() + kPkgG)[ch0 + e] = ex2f(gl[e]);
         if (mbar_wait(&qk_bar[b], (iter >> 1) & 1, p.err)) {
             if (tid == kIss) pend_q[b] = -1;
         } else {
@@ -691,9 +701,16 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         KDA_PHASE(1);
         if (s_abort) break;
 
+        if (warp == (kIss >> 5)) {
+            float* dst = reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1);
+            dst[lane] = __bfloat162float(__ushort_as_bfloat16(beta_nx[0]));
+            dst[lane + 32] = __bfloat162float(__ushort_as_bfloat16(beta_nx[1]));
+            if (lane == 0) s_alog[b ^ 1] = alog_nx;
+        }
+
         // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
         //      column operand of version s2 >= s is k_r e^{rho_s2 - G_r}.
-        if (rows) {
+        {
             // Ev[v][e] = e^{rho_{s2} - rho_s} for the later sub-tiles s2 = sub + 1 + v (<= 1;
             // may underflow to 0, which drops Gram terms below e^-13 of their neighbours):
             // the column operand of version s2 is then k e^{rho_s - G} Ev.
@@ -709,7 +726,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = 4 * rg + i;
-                const bool ok = r < it.L;
+                const bool ok = r < itL;
                 const uint32_t o64 = cofs + sw128_chunk(r, cg & 7);
                 const uint32_t o128 = (cg >> 3) * 16384 + sw128_chunk(r, cg & 7);
                 float qv[8], kv[8], e1[8], dc[8], t[8];
@@ -749,7 +766,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
                 }
             }
         }
-        if (tid < kC) reinterpret_cast<float*>(sm + kBeta)[64 * (b ^ 1) + tid] = beta_next;
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -758,7 +774,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             if (has_next) {
                 fence_async_smem();
                 load_tiles(&p.tq, sm + (b ^ 1) * kQKBuf + kOffQ, &p.tk,
-                           sm + (b ^ 1) * kQKBuf + kOffK, nx, &qk_bar[b ^ 1]);
+                           sm + (b ^ 1) * kQKBuf + kOffK, s_item[b ^ 1], &qk_bar[b ^ 1]);
                 pend_q[b ^ 1] = ((iter + 1) >> 1) & 1;
             }
         }
@@ -794,11 +810,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
 
         // ---- while the Gram MMAs run: the globally scaled operands of the later products,
         //      Gam*Q and K*gamma^C/Gam (package, for the state kernel) and Gam*K (W = M Gam K)
-        if (rows) {
+        {
+        uint8_t* pkg = item_pkg();
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int r = 4 * rg + i;
-            const bool ok = r < it.L;
+            const bool ok = r < itL;
             const uint32_t o64 = cofs + sw128_chunk(r, cg & 7);
             float qv[8], kv[8], eg[8], ek[8], t[8];
             ld8(qk + kOffQ + o64, qv);
@@ -830,7 +847,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         // ---- Gram epilogue: q-side rows -> A tile (bf16 hi + lo), k-side rows -> L (fp32).
         //      TMEM lane m = 32 (warp % 4) + lane; the groups of 16 columns a lane quadrant
         //      needs are split between the two warpgroups.
-        if (rows) {
+        {
             const int quad = warp & 3, wg = warp >> 2;
             const int m = 32 * quad + lane;
             const int side = m >> 6, r = m & 63, s = r >> 4;
@@ -896,7 +913,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
             KDA_PHASE(8);
             // M = T Diag(beta) (lower triangle) as a bf16 K-major tile, written twice: the
             // 128-row operand [M; M] of the W / U MMA
-            if (rows) {
+            {
                 const int r = tid >> 2, cq = tid & 3;
                 uint8_t* mt = sm + kMTile;
 #pragma unroll
@@ -945,7 +962,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
-        if (rows) {
+        {
             // lane quadrants 0, 1: W rows (bf16), quadrants 2, 3: U rows (fp32); the
             // warpgroup picks the 64-column half.  Both are staged in shared memory in
             // their package layout (W in this item's q slot, U in the B-stack region) and
@@ -989,10 +1006,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
         KDA_PHASE(6);
         if (s_abort) break;
         if (tid == kIss && has_next) {  // v is consumed: fetch the next item's
-            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, nx, v_bar);
+            load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, s_item[b ^ 1], v_bar);
             pend_v = (iter + 1) & 1;
         }
         if (tid == kIss) {
+            uint8_t* pkg = item_pkg();
             bulk_s2g(pkg + kPkgStk, qk + kOffQ, 8192);                     // W, channels 0..63
             bulk_s2g(pkg + kPkgStk + kPkgStkBlk, qk + kOffQ + 8192, 8192);  // W, channels 64..127
             bulk_s2g(pkg + kPkgU, sm + kBStk, kPkgUBytes);                  // U
