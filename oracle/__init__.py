@@ -9,7 +9,7 @@ only compiles it with gcc and marshals numpy arrays into it.
 What it computes, and the page each step follows, is written at the top of
 ``kda_oracle.c``:  the token-by-token KDA recurrence and, independently, the
 chunkwise-parallel form with an explicit forward-substitution inverse, plus the
-lower-bounded sigmoid gate.
+lower-bounded sigmoid gate and the gated, RMS-normalised output step.
 """
 from __future__ import annotations
 
@@ -61,6 +61,9 @@ def _load():
             lib.kda_oracle_recurrent.argtypes = common + [_dp, ctypes.c_int]
             lib.kda_oracle_chunked.restype = ctypes.c_int
             lib.kda_oracle_chunked.argtypes = common + [ctypes.c_int, _dp, ctypes.c_int]
+            lib.kda_oracle_output_norm_gate.restype = None
+            lib.kda_oracle_output_norm_gate.argtypes = [_dp, _dp, _dp, ctypes.c_double, _dp,
+                                                        ctypes.c_int64, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -89,6 +92,26 @@ def gate(z, A_log, g_min: float) -> np.ndarray:
 
 def gate_value(z: float, A_log: float, g_min: float) -> float:
     return float(_load().kda_oracle_gate_value(float(z), float(A_log), float(g_min)))
+
+
+def output_norm_gate(o, gate, w=None, eps: float = 1e-6) -> np.ndarray:
+    """sigmoid(gate) * w * o / sqrt(mean(o^2) + eps), the mean over the last axis (dv).
+
+    o, gate: [..., dv] (one row per (token, head)); w: [dv] or None (ones).
+    """
+    o = _f64(o)
+    gate = _f64(gate)
+    assert gate.shape == o.shape
+    dv = o.shape[-1]
+    n_rows = o.size // dv if dv else 0
+    wc = None if w is None else _f64(w)
+    if wc is not None:
+        assert wc.shape == (dv,)
+    y = np.empty_like(o)
+    if n_rows:
+        _load().kda_oracle_output_norm_gate(_ptr(o), _ptr(gate), _ptr(wc), float(eps), _ptr(y),
+                                            n_rows, dv)
+    return y
 
 
 def _run(mode, q, k, v, beta, z, A_log, g_min, S0=None, cu_seqlens=None, C=64,

@@ -36,6 +36,13 @@
  *   cu_seqlens : int64 [N + 1], cu[0] = 0, nondecreasing, cu[N] = T_total.
  * Every (sequence, head) pair is independent; the work is spread over
  * `nthreads` POSIX threads (<= 0 means 1).
+ *
+ * Gated output step ([blog] section "Gated MLA": y_t = W_o [Sigmoid(W_g x_t) (.)
+ * RMSNorm(o~_t)]) without the two projections, which need trained weights:
+ *     y[t,h,j] = Sigmoid(gate[t,h,j]) * w[j] * o[t,h,j] / sqrt(mean_j' o[t,h,j']^2 + eps)
+ * Readings: the norm is per head over its d_v channels; gate is W_g x_t given as an input;
+ * w is the norm's per-channel weight (all ones when absent); eps >= 0 is added to the mean
+ * square.
  */
 #include <math.h>
 #include <pthread.h>
@@ -63,6 +70,26 @@ void kda_oracle_gate(const double *z, const double *A_log, double g_min, double 
                 int64_t idx = (t * H + h) * (int64_t)dk + c;
                 g[idx] = kda_oracle_gate_value(z[idx], A_log[h], g_min);
             }
+}
+
+/* ------------------------------------------------------- gated output -- */
+
+/* [blog] "Gated MLA": Sigmoid(gate) times the RMS-normalised head output, per row of dv
+ * channels (a row is one (token, head)).  w may be NULL (unit weights). */
+void kda_oracle_output_norm_gate(const double *o, const double *gate, const double *w,
+                                 double eps, double *y, int64_t n_rows, int dv)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        const double *orow = o + r * dv, *grow = gate + r * dv;
+        double ms = 0.0;
+        for (int j = 0; j < dv; ++j) ms += orow[j] * orow[j];
+        ms /= dv;
+        const double inv_rms = 1.0 / sqrt(ms + eps);
+        for (int j = 0; j < dv; ++j) {
+            const double wj = w ? w[j] : 1.0;
+            y[r * dv + j] = logistic(grow[j]) * wj * orow[j] * inv_rms;
+        }
+    }
 }
 
 /* ------------------------------------------------------- shared job setup -- */
