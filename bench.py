@@ -309,6 +309,10 @@ def run_ours(args, rank, world, local_rank, dist):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
     del host
 
+    # the gated output step after the forward ("Gated MLA"), on the forward's output, with the
+    # workload's z standing in for the gate logits (same shape, N(0, 1))
+    og = bench_output_gate(dev, stream, peaks, o, d["z"])
+
     # decode step: 256 sequences x 32 heads, state updated in place
     dec = None
     if not args.no_decode:
@@ -337,8 +341,38 @@ def run_ours(args, rank, world, local_rank, dist):
                 "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
                 "roofline": roofline, "e2e": e2e,
                 "gpu_launches": int(round(launches_per_step * args.steps)),
-                "clocks": clk, "decode": dec, "cpu_baseline": cpu}
+                "clocks": clk, "output_gate": og, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
+
+
+def bench_output_gate(dev, stream, peaks, o, gate, reps=20):
+    """y = sigmoid(gate) * w * o / rms(o) per (token, head) on the forward's output shape:
+    one read of o and gate, one write of y (HBM-bound)."""
+    import torch
+
+    from serving_kda_chunkwise_gb300 import kda
+    T_, H_, dv = o.shape
+    w = torch.ones(dv, dtype=torch.float32, device=dev)
+    y = torch.empty_like(o)
+    for _ in range(3):
+        kda.output_norm_gate(o, gate, w, 1e-6, y=y, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(reps):
+        kda.output_norm_gate(o, gate, w, 1e-6, y=y, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = ev0.elapsed_time(ev1) * 1e3 / reps
+    nbytes = 3 * o.numel() * o.element_size() + dv * 4
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"us_per_call": us, "GB_per_call": nbytes / 1e9, "GB_s": gbs,
+            "frac_hbm": gbs / peaks["hbm_gbs"], "shape": [T_, H_, dv], "dtype": "bf16",
+            "kernel": "output_gate_kernel",
+            "traffic": traffic_from_profile(
+                "output_gate_kernel",
+                source_hash("serving_kda_chunkwise_gb300/csrc/output_gate.cu"))}
 
 
 def bench_decode(args, dev, stream, peaks):
@@ -376,11 +410,34 @@ def bench_decode(args, dev, stream, peaks):
     per_head = 2 * 4 * dk * dv + 2 * (3 * dk + dv + 1) + 2 * dv
     step_bytes = N * Hd * per_head
     gbs = step_bytes / (us / 1e6) / 1e9
+
+    # the same step with the gated output step fused (a ring entry's v stands in for the gate
+    # logits): y replaces o, plus one read of the gate
+    wv = torch.ones(dv, dtype=torch.float32, device=dev)
+
+    def gated(i):
+        r = ring[i % len(ring)]
+        kda.decode_step_gated(r["q"], r["k"], r["v"], r["beta"], r["z"], A, -5.0, S,
+                              ring[(i + 1) % len(ring)]["v"], wv, 1e-6, y=o, stream=stream)
+
+    for i in range(5):
+        gated(i)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for i in range(n):
+        gated(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_g = ev0.elapsed_time(ev1) * 1e3 / n
+    gated_bytes = step_bytes + N * Hd * 2 * dv
     return {"us_per_step": us, "GB_per_step": step_bytes / 1e9, "GB_s": gbs,
             "frac_hbm": gbs / peaks["hbm_gbs"], "steps": n, "N": N, "H": Hd, "d": dk,
             "kernel": "decode_kernel",
             "traffic": traffic_from_profile(
-                "decode_kernel", source_hash("serving_kda_chunkwise_gb300/csrc/decode.cu"))}
+                "decode_kernel", source_hash("serving_kda_chunkwise_gb300/csrc/decode.cu")),
+            "gated": {"us_per_step": us_g,
+                      "frac_hbm": gated_bytes / (us_g / 1e6) / 1e9 / peaks["hbm_gbs"],
+                      "kernel": "decode_gated_kernel"}}
 
 
 def main():

@@ -121,6 +121,36 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
                              kda_stream_t stream);
 
 /*
+ * kda_output_norm_gate -- the gated output step of [blog] section "Gated MLA", whose layer
+ * output is y_t = W_o [Sigmoid(W_g x_t) (.) RMSNorm(o~_t)]: the part between the two
+ * projections (which need trained weights), per (token, head) row of dv channels:
+ *     y[t,h,j] = Sigmoid(gate[t,h,j]) * norm_w[j] * o[t,h,j] / sqrt(mean_j o[t,h,j]^2 + eps)
+ *   o, gate : [n_tokens, H, dv] io_dt; gate is W_g x_t, computed by the caller
+ *   norm_w  : [dv] fp32 weight of the norm, or NULL for ones
+ *   eps     : finite and >= 0, added to the mean square
+ *   y       : [n_tokens, H, dv] io_dt (written); may be the same buffer as o
+ * dv must be 64 or 128.  n_tokens = 0 is a no-op.
+ */
+kda_status_t kda_output_norm_gate(const void *o, const void *gate, const float *norm_w,
+                                  float eps, void *y, int64_t n_tokens, int H, int dv,
+                                  kda_dtype_t io_dt, kda_stream_t stream);
+
+/*
+ * kda_decode_step_gated -- kda_decode_step with the gated output step fused into it: the
+ * state update is the same, and in place of o the call writes, per (sequence, head),
+ *     y = Sigmoid(gate) * norm_w * o / sqrt(mean(o^2) + eps)        (as kda_output_norm_gate)
+ * so o never reaches memory.
+ *   gate   : [N, H, dv] io_dt        norm_w : [dv] fp32 or NULL        eps : finite, >= 0
+ *   y      : [N, H, dv] io_dt (written)
+ * Other arguments and rules as kda_decode_step.
+ */
+kda_status_t kda_decode_step_gated(const void *q, const void *k, const void *v,
+                                   const void *beta, const void *z, const float *A_log,
+                                   float g_min, float *S, const void *gate, const float *norm_w,
+                                   float eps, int N, int H, int dk, int dv, kda_dtype_t io_dt,
+                                   void *y, kda_stream_t stream);
+
+/*
  * Waits for `stream`, then reads and clears the device error word that kernels set
  * when they meet malformed device-side input or give up a bounded wait.  Returns
  * KDA_OK, KDA_ERR_DEVICE or KDA_ERR_TIMEOUT (or KDA_ERR_CUDA if the wait failed).

@@ -221,6 +221,59 @@ kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const 
     return KDA_OK;
 }
 
+kda_status_t kda_output_norm_gate(const void* o, const void* gate, const float* norm_w,
+                                  float eps, void* y, int64_t n_tokens, int H, int dv,
+                                  kda_dtype_t io_dt, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
+    KDA_REQUIRE(n_tokens >= 0, "n_tokens=%lld must be >= 0", (long long)n_tokens);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    KDA_REQUIRE(dv > 0, "dv=%d must be positive", dv);
+    if (dv != 64 && dv != 128) return fail(KDA_ERR_UNSUPPORTED, "dv=%d: only 64 and 128 are supported", dv);
+    KDA_REQUIRE(eps >= 0.f && std::isfinite(eps), "eps=%g must be finite and >= 0", (double)eps);
+    if (n_tokens == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(o, "o");
+    KDA_REQUIRE_PTR(gate, "gate");
+    KDA_REQUIRE_PTR(y, "y");
+    KDA_OPTIONAL_PTR(norm_w, "norm_w");
+    cudaError_t e = kda::launch_output_gate(o, gate, norm_w, eps, y, n_tokens * H, dv,
+                                            io_dt == KDA_BF16,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_output_norm_gate launch");
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_step_gated(const void* q, const void* k, const void* v,
+                                   const void* beta, const void* z, const float* A_log,
+                                   float g_min, float* S, const void* gate, const float* norm_w,
+                                   float eps, int N, int H, int dk, int dv, kda_dtype_t io_dt,
+                                   void* y, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
+    KDA_REQUIRE(N >= 0, "N=%d must be >= 0", N);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    if (kda_status_t s = check_dims(dk, dv)) return s;
+    if (kda_status_t s = check_gmin(g_min)) return s;
+    KDA_REQUIRE(eps >= 0.f && std::isfinite(eps), "eps=%g must be finite and >= 0", (double)eps);
+    KDA_REQUIRE((int64_t)N * H < (int64_t)1 << 31, "N*H=%lld is too large", (long long)N * H);
+    if (N == 0) return KDA_OK;
+    KDA_REQUIRE_PTR(q, "q");
+    KDA_REQUIRE_PTR(k, "k");
+    KDA_REQUIRE_PTR(v, "v");
+    KDA_REQUIRE_PTR(z, "z");
+    KDA_REQUIRE_PTR(gate, "gate");
+    KDA_REQUIRE_PTR(y, "y");
+    KDA_REQUIRE_PTR(S, "S");
+    KDA_REQUIRE_PTR(A_log, "A_log");
+    KDA_OPTIONAL_PTR(norm_w, "norm_w");
+    KDA_REQUIRE(beta != nullptr, "beta is NULL");
+    cudaError_t e = kda::launch_decode_gated(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv,
+                                             io_dt == KDA_BF16, gate, norm_w, eps, y,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_decode_step_gated launch");
+    return KDA_OK;
+}
+
 kda_status_t kda_device_status(kda_stream_t stream) {
     t_last_error.clear();
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -18,13 +18,19 @@
 // first is used) and again, from L2, for the update, so that no thread holds the whole
 // state in registers and four CTAs fit on an SM.  HBM sees one read and one write; the
 // second read and the write carry the streaming hint.
+//
+// The gated variant fuses the output step of section "Gated MLA" of the same page (between
+// its two projections): instead of o it writes
+//   y_j = Sigmoid(gate_j) * w_j * o_j / sqrt(mean_j o_j^2 + eps),
+// the mean over the dv outputs of the (sequence, head), which one CTA holds, so o never
+// reaches memory.
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
 namespace kda {
 namespace {
 
-template <int DK, int DV, typename IO>
+template <int DK, int DV, typename IO, bool kGated>
 __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
                                                      const IO* __restrict__ k,
                                                      const IO* __restrict__ v,
@@ -32,6 +38,8 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
                                                      const IO* __restrict__ z,
                                                      const float* __restrict__ A_log, float g_min,
                                                      float* __restrict__ S, int H,
+                                                     const IO* __restrict__ gate,
+                                                     const float* __restrict__ norm_w, float eps,
                                                      IO* __restrict__ o) {
     constexpr int kWarps = 8;
     constexpr int kLanesPerRow = DV / 4;
@@ -43,6 +51,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
     __shared__ float s_alpha[DK], s_k[DK], s_q[DK], s_u[DV];
     __shared__ float s_red[2][kWarps][DV];
     __shared__ float s_kq;
+    __shared__ float s_ss[DV / 32];  // gated variant: partial sums of o^2
 
     const int nh = blockIdx.x;
     const int h = nh % H;
@@ -112,6 +121,7 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
     }
     __syncthreads();
 
+    float o_j = 0.f;  // output channel tid (tid < DV)
     if (tid < DV) {
         float a = 0.f, b = 0.f;
 #pragma unroll
@@ -121,9 +131,25 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
         }
         const float u = to_f32(beta[nh]) * (to_f32(v[(size_t)nh * DV + tid]) - a);
         s_u[tid] = u;
-        o[(size_t)nh * DV + tid] = from_f32<IO>(fmaf(u, s_kq, b));
+        o_j = fmaf(u, s_kq, b);
+        if (!kGated) o[(size_t)nh * DV + tid] = from_f32<IO>(o_j);
+    }
+    if (kGated && warp < DV / 32) {  // the DV outputs are warps 0 .. DV/32 - 1
+        float sq = o_j * o_j;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        if (lane == 0) s_ss[warp] = sq;
     }
     __syncthreads();
+    if (kGated && tid < DV) {
+        float ms = 0.f;
+#pragma unroll
+        for (int w = 0; w < DV / 32; ++w) ms += s_ss[w];
+        const float inv_rms = rsqrtf(ms * (1.f / DV) + eps);
+        const float wj = norm_w ? __ldg(norm_w + tid) : 1.f;
+        const float gj = to_f32(gate[(size_t)nh * DV + tid]);
+        o[(size_t)nh * DV + tid] = from_f32<IO>(o_j * inv_rms * wj / (1.f + __expf(-gj)));
+    }
 
     const float4 u4 = reinterpret_cast<const float4*>(s_u)[col4];
 #pragma unroll
@@ -141,30 +167,56 @@ __global__ void __launch_bounds__(256) decode_kernel(const IO* __restrict__ q,
     }
 }
 
+struct DecodeOut {
+    const void* gate;     // gated variant: [N, H, dv] io_dt, or nullptr for plain o
+    const float* norm_w;  // [dv] or nullptr (ones)
+    float eps;
+    void* out;            // o, or y for the gated variant
+};
+
 template <int DK, int DV, typename IO>
 cudaError_t launch_t(const void* q, const void* k, const void* v, const void* beta, const void* z,
-                     const float* A_log, float g_min, float* S, int N, int H, void* o,
+                     const float* A_log, float g_min, float* S, int N, int H, const DecodeOut& d,
                      cudaStream_t stream) {
     const int grid = N * H;
-    ProfScope prof("decode_kernel", stream);
-    decode_kernel<DK, DV, IO><<<grid, 256, 0, stream>>>(
-        static_cast<const IO*>(q), static_cast<const IO*>(k), static_cast<const IO*>(v),
-        static_cast<const IO*>(beta), static_cast<const IO*>(z), A_log, g_min, S, H,
-        static_cast<IO*>(o));
+    const IO* gate = static_cast<const IO*>(d.gate);
+    if (gate) {
+        ProfScope prof("decode_gated_kernel", stream);
+        decode_kernel<DK, DV, IO, true><<<grid, 256, 0, stream>>>(
+            static_cast<const IO*>(q), static_cast<const IO*>(k), static_cast<const IO*>(v),
+            static_cast<const IO*>(beta), static_cast<const IO*>(z), A_log, g_min, S, H, gate,
+            d.norm_w, d.eps, static_cast<IO*>(d.out));
+    } else {
+        ProfScope prof("decode_kernel", stream);
+        decode_kernel<DK, DV, IO, false><<<grid, 256, 0, stream>>>(
+            static_cast<const IO*>(q), static_cast<const IO*>(k), static_cast<const IO*>(v),
+            static_cast<const IO*>(beta), static_cast<const IO*>(z), A_log, g_min, S, H, nullptr,
+            nullptr, 0.f, static_cast<IO*>(d.out));
+    }
     return cudaGetLastError();
 }
 
 template <typename IO>
 cudaError_t dispatch_dims(const void* q, const void* k, const void* v, const void* beta,
                           const void* z, const float* A_log, float g_min, float* S, int N, int H,
-                          int dk, int dv, void* o, cudaStream_t stream) {
+                          int dk, int dv, const DecodeOut& d, cudaStream_t stream) {
     if (dk == 128 && dv == 128)
-        return launch_t<128, 128, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+        return launch_t<128, 128, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, d, stream);
     if (dk == 128 && dv == 64)
-        return launch_t<128, 64, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+        return launch_t<128, 64, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, d, stream);
     if (dk == 64 && dv == 128)
-        return launch_t<64, 128, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
-    return launch_t<64, 64, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, o, stream);
+        return launch_t<64, 128, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, d, stream);
+    return launch_t<64, 64, IO>(q, k, v, beta, z, A_log, g_min, S, N, H, d, stream);
+}
+
+cudaError_t decode_any(const void* q, const void* k, const void* v, const void* beta,
+                       const void* z, const float* A_log, float g_min, float* S, int N, int H,
+                       int dk, int dv, int io_bf16, const DecodeOut& d, cudaStream_t stream) {
+    if ((int64_t)N * H == 0) return cudaSuccess;
+    if (io_bf16)
+        return dispatch_dims<__nv_bfloat16>(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, d,
+                                            stream);
+    return dispatch_dims<float>(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, d, stream);
 }
 
 }  // namespace
@@ -172,11 +224,16 @@ cudaError_t dispatch_dims(const void* q, const void* k, const void* v, const voi
 cudaError_t launch_decode(const void* q, const void* k, const void* v, const void* beta,
                           const void* z, const float* A_log, float g_min, float* S, int N, int H,
                           int dk, int dv, int io_bf16, void* o, cudaStream_t stream) {
-    if ((int64_t)N * H == 0) return cudaSuccess;
-    if (io_bf16)
-        return dispatch_dims<__nv_bfloat16>(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, o,
-                                            stream);
-    return dispatch_dims<float>(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, o, stream);
+    return decode_any(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, io_bf16,
+                      DecodeOut{nullptr, nullptr, 0.f, o}, stream);
+}
+
+cudaError_t launch_decode_gated(const void* q, const void* k, const void* v, const void* beta,
+                                const void* z, const float* A_log, float g_min, float* S, int N,
+                                int H, int dk, int dv, int io_bf16, const void* gate,
+                                const float* norm_w, float eps, void* y, cudaStream_t stream) {
+    return decode_any(q, k, v, beta, z, A_log, g_min, S, N, H, dk, dv, io_bf16,
+                      DecodeOut{gate, norm_w, eps, y}, stream);
 }
 
 }  // namespace kda

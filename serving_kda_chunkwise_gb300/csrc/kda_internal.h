@@ -37,6 +37,17 @@ cudaError_t launch_decode(const void* q, const void* k, const void* v, const voi
                           const void* z, const float* A_log, float g_min, float* S, int N, int H,
                           int dk, int dv, int io_bf16, void* o, cudaStream_t stream);
 
+// K4 with the gated output step of "Gated MLA" fused: writes y instead of o.
+cudaError_t launch_decode_gated(const void* q, const void* k, const void* v, const void* beta,
+                                const void* z, const float* A_log, float g_min, float* S, int N,
+                                int H, int dk, int dv, int io_bf16, const void* gate,
+                                const float* norm_w, float eps, void* y, cudaStream_t stream);
+
+// The gated output step alone: rows of dv channels (one per token and head).
+cudaError_t launch_output_gate(const void* o, const void* gate, const float* norm_w, float eps,
+                               void* y, int64_t n_rows, int dv, int io_bf16,
+                               cudaStream_t stream);
+
 // Chunked forward on CUDA cores in fp32 (any dtype, dk/dv in {64,128}).
 cudaError_t launch_fwd_generic(const FwdArgs& a);
 

@@ -13,6 +13,8 @@ same bits.  Per token and head:
     beta = logistic(N(0, 1))                       z ~ N(0, 1) per channel
 and per problem:  A_log ~ U(-1, 1) per head,  S0 ~ N(0, 0.02^2),  varlen lengths
 ~ U{lo..hi}.  q, k, v, beta, z are then rounded to the I/O dtype (bf16: nearest even).
+For the gated output step: head outputs o ~ N(0, 1) times a per-(token, head) scale
+~ U(0.1, 10) (which the norm removes), gate logits ~ N(0, 1), norm weight ~ U(0.5, 1.5).
 """
 from __future__ import annotations
 
@@ -23,7 +25,8 @@ from dataclasses import dataclass
 import numpy as np
 
 BLOCK_TOKENS = 2048
-_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "z": 5, "A_log": 6, "S0": 7, "lengths": 8}
+_IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "z": 5, "A_log": 6, "S0": 7, "lengths": 8,
+        "o_head": 9, "gate": 10, "norm_w": 11}
 
 # ----------------------------------------------------------------- rounding --
 
@@ -285,6 +288,39 @@ def decode_steps_iter(*, seed: int, steps: int, N: int, H: int, dk: int, dv: int
             yield step, futs.pop(step).result()
 
 
+@dataclass
+class OutputGateInputs:
+    o: Stored                   # [T, H, dv] head outputs
+    gate: Stored                # [T, H, dv] gate logits (W_g x, given)
+    norm_w: np.ndarray | None   # float32 [dv], or None for unit weights
+
+
+def output_gate_inputs(*, seed: int, T: int, H: int, dv: int, dtype: str,
+                       with_weight: bool = True) -> OutputGateInputs:
+    nb = -(-T // BLOCK_TOKENS)
+
+    def block(kind, b):
+        t0 = b * BLOCK_TOKENS
+        n = min(BLOCK_TOKENS, T - t0)
+        rng = _gen(seed, _IDS[kind], b)
+        x = rng.standard_normal(size=(n, H, dv), dtype=np.float32)
+        if kind == "o_head":
+            x *= rng.uniform(0.1, 10.0, size=(n, H, 1)).astype(np.float32)
+        return x
+
+    out = {}
+    for kind in ("o_head", "gate"):
+        if T == 0:
+            out[kind] = np.zeros((0, H, dv), dtype=np.float32)
+            continue
+        with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+            parts = list(ex.map(lambda b: block(kind, b), range(nb)))
+        out[kind] = np.concatenate(parts, axis=0)
+    w = (_gen(seed, _IDS["norm_w"]).uniform(0.5, 1.5, size=dv).astype(np.float32)
+         if with_weight else None)
+    return OutputGateInputs(store(out["o_head"], dtype), store(out["gate"], dtype), w)
+
+
 # ------------------------------------------------------ the named workloads --
 
 #: The forward workloads, by what they are.  ``seed`` = 1000 + index.
@@ -301,6 +337,9 @@ WORKLOADS = {
 
 #: g_min sweep for the long-context workload (same seed-1002 inputs for each value).
 LONG_GMIN_SWEEP = (-3.0, -5.0, -6.0)
+
+#: The gated output step at the long-context forward's output shape.
+OUTPUT_GATE_WORKLOAD = dict(seed=1005, T=65536, H=32, dv=128, dtype="bf16")
 
 #: 256 sequences x 32 heads, one token per step for 1000 steps.
 DECODE_WORKLOAD = dict(seed=1004, N=256, H=32, dk=128, dv=128, steps=1000, dtype="bf16")

@@ -57,6 +57,11 @@ def _load():
     lib.kda_decode_step.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, i32, i32, i32, i32, i32, vp,
                                     vp]
+    lib.kda_output_norm_gate.restype = ctypes.c_int
+    lib.kda_output_norm_gate.argtypes = [vp, vp, vp, f32, vp, i64, i32, i32, i32, vp]
+    lib.kda_decode_step_gated.restype = ctypes.c_int
+    lib.kda_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, f32, i32, i32,
+                                          i32, i32, i32, vp, vp]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [vp]
     lib.kda_profile_begin.restype = ctypes.c_int
@@ -276,6 +281,46 @@ def decode_step(q, k, v, beta, z, A_log, g_min: float, S, o=None, stream=None):
                                 float(g_min), _ptr(S), int(N), int(H), int(dk), int(dv), _dt(q),
                                 _ptr(o), _stream(stream)), "kda_decode_step")
     return o
+
+
+def output_norm_gate(o, gate, norm_w=None, eps: float = 1e-6, y=None, stream=None):
+    """y = sigmoid(gate) * norm_w * o / sqrt(mean(o^2) + eps) per (token, head) row.
+
+    o, gate: [T, H, dv] (bf16 or fp32); norm_w: [dv] fp32 or None; y may be o (in place).
+    """
+    _need(o, "o")
+    _need(gate, "gate", o.dtype)
+    if norm_w is not None:
+        _need(norm_w, "norm_w", torch.float32)
+    T, H, dv = o.shape
+    if y is None:
+        y = torch.empty_like(o)
+    _need(y, "y", o.dtype)
+    _check(_lib.kda_output_norm_gate(_ptr(o), _ptr(gate), _ptr(norm_w), float(eps), _ptr(y),
+                                     int(T), int(H), int(dv), _dt(o), _stream(stream)),
+           "kda_output_norm_gate")
+    return y
+
+
+def decode_step_gated(q, k, v, beta, z, A_log, g_min: float, S, gate, norm_w=None,
+                      eps: float = 1e-6, y=None, stream=None):
+    """decode_step with the gated output step fused: returns y [N, H, dv] in place of o."""
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (z, "z"), (gate, "gate")):
+        _need(t, nm, q.dtype)
+    _need(A_log, "A_log", torch.float32)
+    _need(S, "S", torch.float32)
+    if norm_w is not None:
+        _need(norm_w, "norm_w", torch.float32)
+    N, H, dk = q.shape
+    dv = v.shape[2]
+    if y is None:
+        y = torch.empty((N, H, dv), dtype=q.dtype, device=q.device)
+    _need(y, "y", q.dtype)
+    _check(_lib.kda_decode_step_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z),
+                                      _ptr(A_log), float(g_min), _ptr(S), _ptr(gate),
+                                      _ptr(norm_w), float(eps), int(N), int(H), int(dk), int(dv),
+                                      _dt(q), _ptr(y), _stream(stream)), "kda_decode_step_gated")
+    return y
 
 
 def device_status(stream=None):

@@ -108,3 +108,31 @@ def test_workspace_size_needs_no_device(lib):
     for dt in (0, 1):
         n = lib.kda_fwd_workspace_size(65536, 1, 32, 128, 128, dt)
         assert n >= 0
+
+
+def test_output_gate_validation(lib):
+    vp, f = ctypes.c_void_p, ctypes.c_float
+    a = vp(0x10000)
+    lib.kda_output_norm_gate.restype = ctypes.c_int
+    lib.kda_decode_step_gated.restype = ctypes.c_int
+    lib.kda_last_error.restype = ctypes.c_char_p
+    i64 = ctypes.c_int64
+    # o, gate, norm_w, eps, y, n_tokens, H, dv, io_dt, stream
+    assert lib.kda_output_norm_gate(a, a, None, f(1e-6), a, i64(4), 2, 96, 1, None) == 2
+    assert lib.kda_output_norm_gate(a, a, None, f(-1.0), a, i64(4), 2, 128, 1, None) == 1
+    assert b"eps" in lib.kda_last_error()
+    assert lib.kda_output_norm_gate(a, None, None, f(1e-6), a, i64(4), 2, 128, 1, None) == 1
+    assert b"gate is NULL" in lib.kda_last_error()
+    assert lib.kda_output_norm_gate(a, a, vp(0x10004), f(1e-6), a, i64(4), 2, 128, 1, None) == 1
+    assert b"norm_w is not 16-byte aligned" in lib.kda_last_error()
+    assert lib.kda_output_norm_gate(None, None, None, f(0.0), None, i64(0), 2, 64, 0, None) == 0
+    # q, k, v, beta, z, A_log, g_min, S, gate, norm_w, eps, N, H, dk, dv, io_dt, y, stream
+    rc = lib.kda_decode_step_gated(a, a, a, a, a, a, f(-5.0), a, None, None, f(1e-6), 4, 2, 128,
+                                   128, 1, a, None)
+    assert rc == 1 and b"gate is NULL" in lib.kda_last_error()
+    rc = lib.kda_decode_step_gated(a, a, a, a, a, a, f(-5.0), a, a, None, f(float("nan")), 4, 2,
+                                   128, 128, 1, a, None)
+    assert rc == 1 and b"eps" in lib.kda_last_error()
+    rc = lib.kda_decode_step_gated(a, a, a, a, a, a, f(-5.0), a, a, None, f(1e-6), 4, 2, 128, 96,
+                                   1, a, None)
+    assert rc == 2
