@@ -9,7 +9,9 @@ only compiles it with gcc and marshals numpy arrays into it.
 What it computes, and the page each step follows, is written at the top of
 ``kda_oracle.c``:  the token-by-token KDA recurrence and, independently, the
 chunkwise-parallel form with an explicit forward-substitution inverse, plus the
-lower-bounded sigmoid gate and the gated, RMS-normalised output step.
+lower-bounded sigmoid gate and the gated, RMS-normalised output step.  The
+quantile-balancing bias update of the mixture-of-experts router is plain numpy, in
+``oracle/quantile_balance.py``.
 """
 from __future__ import annotations
 
