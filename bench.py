@@ -313,6 +313,9 @@ def run_ours(args, rank, world, local_rank, dist):
     # workload's z standing in for the gate logits (same shape, N(0, 1))
     og = bench_output_gate(dev, stream, peaks, o, d["z"])
 
+    # quantile balancing of a routing batch (65536 tokens x 256 experts, k = 8)
+    qbm = bench_quantile_balance(dev, stream, peaks)
+
     # decode step: 256 sequences x 32 heads, state updated in place
     dec = None
     if not args.no_decode:
@@ -341,7 +344,7 @@ def run_ours(args, rank, world, local_rank, dist):
                 "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
                 "roofline": roofline, "e2e": e2e,
                 "gpu_launches": int(round(launches_per_step * args.steps)),
-                "clocks": clk, "output_gate": og, "decode": dec, "cpu_baseline": cpu}
+                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
 
 
@@ -373,6 +376,41 @@ def bench_output_gate(dev, stream, peaks, o, gate, reps=20):
             "traffic": traffic_from_profile(
                 "output_gate_kernel",
                 source_hash("serving_kda_chunkwise_gb300/csrc/output_gate.cu"))}
+
+
+def bench_quantile_balance(dev, stream, peaks, reps=20):
+    """The quantile-balancing bias update on one routing batch.  The scores (64 MB) fit in
+    L2, so L2 is flushed (a 256 MB write, outside the timed region) before every call."""
+    import torch
+
+    from serving_kda_chunkwise_gb300 import inputs, kda
+    w = inputs.QB_WORKLOAD
+    s_np, b_np = inputs.qb_inputs(seed=w["seed"], m=w["m"], n=w["n"])
+    sc = torch.from_numpy(s_np).to(dev)
+    bias = torch.from_numpy(b_np).to(dev)
+    ws = torch.empty(kda.library().kda_quantile_balance_workspace_size(w["m"], w["n"]),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        kda.quantile_balance(sc, bias, w["k"], workspace=ws, stream=stream)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        kda.quantile_balance(sc, bias, w["k"], workspace=ws, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(ev0.elapsed_time(ev1))
+    times.sort()
+    us = times[len(times) // 2] * 1e3
+    nbytes = sc.numel() * 4  # one read of the scores: the algorithmic minimum
+    gbs = nbytes / (us / 1e6) / 1e9
+    return {"us_per_call": us, "m": w["m"], "n": w["n"], "k": w["k"],
+            "scores_GB": nbytes / 1e9, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+            "l2": "flushed before every call", "kernels": ["qb_alpha_kernel", "qb_hist_kernel",
+                                                          "qb_select_kernel", "qb_mean_kernel"]}
 
 
 def bench_decode(args, dev, stream, peaks):

@@ -10,7 +10,8 @@
  *         (chunk length 64, 16-token sub-tiles) and the lower-bounded gate
  *         g_t = g_min * Sigmoid(e^{A_h} z_t)  in (g_min, 0),   alpha_t = exp(g_t).
  *   [guide] "A Look at Kimi K3: Three Core Innovations and Engineering Tuning Guide",
- *     section 2.2 -- the same gate (per head A_h, per channel z), g_min in [-6, -3].
+ *     section 2.2 -- the same gate (per head A_h, per channel z), g_min in [-6, -3];
+ *     section 4.2 -- quantile-based expert thresholds.
  *
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
@@ -149,6 +150,28 @@ kda_status_t kda_decode_step_gated(const void *q, const void *k, const void *v,
                                    float g_min, float *S, const void *gate, const float *norm_w,
                                    float eps, int N, int H, int dk, int dv, kda_dtype_t io_dt,
                                    void *y, kda_stream_t stream);
+
+/*
+ * kda_quantile_balance -- quantile-balancing update of a mixture-of-experts router's expert
+ * biases ([blog] section "Quantile Balancing (QB)"; [guide] section 4.2):
+ *     alpha_i   = the (k+1)-th largest of scores[i,:] + bias          (token threshold)
+ *     margin_ij = scores[i,j] - alpha_i
+ *     bhat_j    = -(the (q+1)-th largest of margin[:,j]),  q = floor(m k / n)
+ *                 (expert j would then receive exactly q tokens)
+ *     bias_new  = bhat - mean(bhat)
+ * s + bias and the margins are formed in fp32 and the selections are exact, so alpha and
+ * bhat are bitwise reproducible; equal values count separately ("(q+1)-th largest" of the
+ * sorted list).
+ *   scores    : [m, n] fp32 device, row-major (token-major)       bias : [n] fp32
+ *   k         : experts per token, 0 <= k < n;   1 <= n <= 1024;   1 <= m < 2^31
+ *   bias_new  : [n] fp32 (written)
+ *   bhat, alpha : [n] and [m] fp32 outputs, or NULL when not wanted
+ *   workspace : device scratch of kda_quantile_balance_workspace_size(m, n) bytes
+ */
+size_t kda_quantile_balance_workspace_size(int64_t m, int n);
+kda_status_t kda_quantile_balance(const float *scores, const float *bias, int64_t m, int n,
+                                  int k, float *bias_new, float *bhat, float *alpha,
+                                  void *workspace, size_t ws_bytes, kda_stream_t stream);
 
 /*
  * Waits for `stream`, then reads and clears the device error word that kernels set

@@ -274,6 +274,34 @@ kda_status_t kda_decode_step_gated(const void* q, const void* k, const void* v,
     return KDA_OK;
 }
 
+size_t kda_quantile_balance_workspace_size(int64_t m, int n) {
+    if (m <= 0 || n <= 0) return 0;
+    return kda::qb_workspace_size(m, n);
+}
+
+kda_status_t kda_quantile_balance(const float* scores, const float* bias, int64_t m, int n,
+                                  int k, float* bias_new, float* bhat, float* alpha,
+                                  void* workspace, size_t ws_bytes, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(m >= 1 && m < ((int64_t)1 << 31), "m=%lld must be in [1, 2^31)", (long long)m);
+    KDA_REQUIRE(n >= 1 && n <= 1024, "n=%d must be in [1, 1024]", n);
+    KDA_REQUIRE(k >= 0 && k < n, "k=%d must satisfy 0 <= k < n=%d", k, n);
+    KDA_REQUIRE_PTR(scores, "scores");
+    KDA_REQUIRE_PTR(bias, "bias");
+    KDA_REQUIRE_PTR(bias_new, "bias_new");
+    KDA_OPTIONAL_PTR(bhat, "bhat");
+    KDA_OPTIONAL_PTR(alpha, "alpha");
+    const size_t need = kda::qb_workspace_size(m, n);
+    KDA_REQUIRE_PTR(workspace, "workspace");
+    KDA_REQUIRE(ws_bytes >= need, "workspace of %zu bytes is smaller than the %zu needed",
+                ws_bytes, need);
+    cudaError_t e = kda::launch_quantile_balance(scores, bias, m, n, k, bias_new, bhat, alpha,
+                                                 workspace,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_quantile_balance launch");
+    return KDA_OK;
+}
+
 kda_status_t kda_device_status(kda_stream_t stream) {
     t_last_error.clear();
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -48,6 +48,12 @@ cudaError_t launch_output_gate(const void* o, const void* gate, const float* nor
                                void* y, int64_t n_rows, int dv, int io_bf16,
                                cudaStream_t stream);
 
+// Quantile-balancing bias update of the expert router (qb.cu).
+size_t qb_workspace_size(int64_t m, int n);
+cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, int n, int k,
+                                    float* b_new, float* bhat, float* alpha, void* workspace,
+                                    cudaStream_t stream);
+
 // Chunked forward on CUDA cores in fp32 (any dtype, dk/dv in {64,128}).
 cudaError_t launch_fwd_generic(const FwdArgs& a);
 

@@ -15,6 +15,9 @@ and per problem:  A_log ~ U(-1, 1) per head,  S0 ~ N(0, 0.02^2),  varlen lengths
 ~ U{lo..hi}.  q, k, v, beta, z are then rounded to the I/O dtype (bf16: nearest even).
 For the gated output step: head outputs o ~ N(0, 1) times a per-(token, head) scale
 ~ U(0.1, 10) (which the norm removes), gate logits ~ N(0, 1), norm weight ~ U(0.5, 1.5).
+For quantile balancing: router scores s_ij ~ N(0, 1) + mu_j with a per-expert popularity
+mu_j ~ N(0, 0.5^2) (so that some experts are over-chosen), current biases ~ N(0, 0.1^2);
+optionally rounded to a grid of 1/4 to force ties.
 """
 from __future__ import annotations
 
@@ -26,7 +29,8 @@ import numpy as np
 
 BLOCK_TOKENS = 2048
 _IDS = {"q": 1, "k": 2, "v": 3, "beta": 4, "z": 5, "A_log": 6, "S0": 7, "lengths": 8,
-        "o_head": 9, "gate": 10, "norm_w": 11}
+        "o_head": 9, "gate": 10, "norm_w": 11, "router": 12, "popularity": 13,
+        "expert_bias": 14}
 
 # ----------------------------------------------------------------- rounding --
 
@@ -321,6 +325,25 @@ def output_gate_inputs(*, seed: int, T: int, H: int, dv: int, dtype: str,
     return OutputGateInputs(store(out["o_head"], dtype), store(out["gate"], dtype), w)
 
 
+def qb_inputs(*, seed: int, m: int, n: int, grid: float = 0.0):
+    """(scores [m, n] float32, bias [n] float32) for the quantile-balancing update."""
+    mu = _gen(seed, _IDS["popularity"]).normal(0.0, 0.5, size=n).astype(np.float32)
+    nb = -(-m // BLOCK_TOKENS)
+
+    def block(b):
+        t0 = b * BLOCK_TOKENS
+        rows = min(BLOCK_TOKENS, m - t0)
+        return _gen(seed, _IDS["router"], b).standard_normal(size=(rows, n), dtype=np.float32)
+
+    with cf.ThreadPoolExecutor(max_workers=_threads()) as ex:
+        s = np.concatenate(list(ex.map(block, range(nb))), axis=0) + mu[None, :]
+    bias = _gen(seed, _IDS["expert_bias"]).normal(0.0, 0.1, size=n).astype(np.float32)
+    if grid:
+        s = np.round(s / grid) * grid
+        bias = np.round(bias / grid) * grid
+    return np.ascontiguousarray(s, dtype=np.float32), bias.astype(np.float32)
+
+
 # ------------------------------------------------------ the named workloads --
 
 #: The forward workloads, by what they are.  ``seed`` = 1000 + index.
@@ -340,6 +363,9 @@ LONG_GMIN_SWEEP = (-3.0, -5.0, -6.0)
 
 #: The gated output step at the long-context forward's output shape.
 OUTPUT_GATE_WORKLOAD = dict(seed=1005, T=65536, H=32, dv=128, dtype="bf16")
+
+#: Quantile balancing: one routing batch of 65536 tokens over 256 experts, 8 per token.
+QB_WORKLOAD = dict(seed=1006, m=65536, n=256, k=8)
 
 #: 256 sequences x 32 heads, one token per step for 1000 steps.
 DECODE_WORKLOAD = dict(seed=1004, N=256, H=32, dk=128, dv=128, steps=1000, dtype="bf16")

@@ -62,6 +62,10 @@ def _load():
     lib.kda_decode_step_gated.restype = ctypes.c_int
     lib.kda_decode_step_gated.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, vp, f32, i32, i32,
                                           i32, i32, i32, vp, vp]
+    lib.kda_quantile_balance_workspace_size.restype = sz
+    lib.kda_quantile_balance_workspace_size.argtypes = [i64, i32]
+    lib.kda_quantile_balance.restype = ctypes.c_int
+    lib.kda_quantile_balance.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [vp]
     lib.kda_profile_begin.restype = ctypes.c_int
@@ -321,6 +325,31 @@ def decode_step_gated(q, k, v, beta, z, A_log, g_min: float, S, gate, norm_w=Non
                                       _ptr(norm_w), float(eps), int(N), int(H), int(dk), int(dv),
                                       _dt(q), _ptr(y), _stream(stream)), "kda_decode_step_gated")
     return y
+
+
+def quantile_balance(scores, bias, k: int, want_bhat=False, want_alpha=False, workspace=None,
+                     stream=None):
+    """Quantile-balancing bias update: returns bias_new [n] (and bhat [n], alpha [m] when
+    asked).  scores: [m, n] fp32 (token-major), bias: [n] fp32."""
+    _need(scores, "scores", torch.float32)
+    _need(bias, "bias", torch.float32)
+    m, n = scores.shape
+    dev = scores.device
+    b_new = torch.empty(n, dtype=torch.float32, device=dev)
+    bhat = torch.empty(n, dtype=torch.float32, device=dev) if want_bhat else None
+    alpha = torch.empty(m, dtype=torch.float32, device=dev) if want_alpha else None
+    need = int(_lib.kda_quantile_balance_workspace_size(int(m), int(n)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(_lib.kda_quantile_balance(_ptr(scores), _ptr(bias), int(m), int(n), int(k),
+                                     _ptr(b_new), _ptr(bhat), _ptr(alpha), _ptr(workspace),
+                                     workspace.numel(), _stream(stream)), "kda_quantile_balance")
+    out = [b_new]
+    if want_bhat:
+        out.append(bhat)
+    if want_alpha:
+        out.append(alpha)
+    return out[0] if len(out) == 1 else tuple(out)
 
 
 def device_status(stream=None):

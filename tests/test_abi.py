@@ -136,3 +136,27 @@ def test_output_gate_validation(lib):
     rc = lib.kda_decode_step_gated(a, a, a, a, a, a, f(-5.0), a, a, None, f(1e-6), 4, 2, 128, 96,
                                    1, a, None)
     assert rc == 2
+
+
+def test_quantile_balance_validation(lib):
+    vp = ctypes.c_void_p
+    a = vp(0x10000)
+    i64 = ctypes.c_int64
+    lib.kda_quantile_balance.restype = ctypes.c_int
+    lib.kda_quantile_balance_workspace_size.restype = ctypes.c_size_t
+    lib.kda_last_error.restype = ctypes.c_char_p
+    need = lib.kda_quantile_balance_workspace_size(i64(1000), 64)
+    assert need >= 1000 * 4 + 64 * 256 * 4
+    # scores, bias, m, n, k, bias_new, bhat, alpha, workspace, ws_bytes, stream
+    rc = lib.kda_quantile_balance(a, a, i64(1000), 2000, 8, a, None, None, a,
+                                  ctypes.c_size_t(need), None)
+    assert rc == 1 and b"n=2000" in lib.kda_last_error()
+    rc = lib.kda_quantile_balance(a, a, i64(1000), 64, 64, a, None, None, a,
+                                  ctypes.c_size_t(need), None)
+    assert rc == 1 and b"k=64" in lib.kda_last_error()
+    rc = lib.kda_quantile_balance(a, a, i64(1000), 64, 8, a, None, None, a,
+                                  ctypes.c_size_t(need - 1), None)
+    assert rc == 1 and b"workspace" in lib.kda_last_error()
+    rc = lib.kda_quantile_balance(a, a, i64(0), 64, 8, a, None, None, a,
+                                  ctypes.c_size_t(need), None)
+    assert rc == 1
