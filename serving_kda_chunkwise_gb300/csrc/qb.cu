@@ -11,9 +11,10 @@
 // s + b and the margins are formed in fp32; the selections are exact (no arithmetic).
 //
 // Kernels, all on the caller's stream:
-//   qb_alpha_kernel   one warp per token: the row's n values in registers (n <= 1024), the
-//                     (k+1)-th largest by k+1 rounds of warp maximum and removal of one
-//                     occurrence.
+//   qb_alpha_kernel   one warp per token: the row's n values in registers (n <= 1024,
+//                     ceil(n/32) per lane), the (k+1)-th largest by k+1 rounds of warp
+//                     maximum and removal of one occurrence (or the (n-k)-th smallest, by
+//                     rounds of minimum, when that takes fewer rounds).
 //   qb_hist_kernel    radix select over the margins of every expert at once, 8 bits per pass
 //                     (4 passes, most significant digit first) on an order-preserving
 //                     uint32 key, inverted so that ascending keys are descending margins:
@@ -33,9 +34,6 @@
 namespace kda {
 namespace {
 
-constexpr int kMaxExperts = 1024;
-constexpr int kPerLane = kMaxExperts / 32;
-
 // order-preserving map of fp32 to uint32 (ascending floats -> ascending keys), inverted so
 // that ascending keys are descending floats
 __device__ __forceinline__ uint32_t desc_key(float x) {
@@ -49,42 +47,58 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float(u);
 }
 
+// kP values per lane (n <= 32 kP).  The (k+1)-th largest is found by k+1 rounds of "take the
+// warp maximum, remove one occurrence", or, when that is shorter, as the (n-k)-th smallest by
+// rounds of minimum.
+template <int kP>
 __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__ s,
                                                        const float* __restrict__ b, int64_t m,
                                                        int n, int k, float* __restrict__ alpha) {
     const int lane = threadIdx.x & 31;
+    const bool from_top = k + 1 <= n - k;
+    const int rounds = from_top ? k + 1 : n - k;
+    const float pad = from_top ? -INFINITY : INFINITY;  // never selected
+    float bj[kP];
+#pragma unroll
+    for (int e = 0; e < kP; ++e) {
+        const int j = lane + 32 * e;
+        bj[e] = (j < n) ? __ldg(b + j) : 0.f;
+    }
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t i = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); i < m;
          i += warps) {
-        float v[kPerLane];
+        float v[kP];
 #pragma unroll
-        for (int e = 0; e < kPerLane; ++e) {
+        for (int e = 0; e < kP; ++e) {
             const int j = lane + 32 * e;
-            v[e] = (j < n) ? s[i * n + j] + __ldg(b + j) : -INFINITY;
+            // s + b in fp32; the top-down search works on -v, so both are "largest first"
+            const float x = (j < n) ? s[i * n + j] + bj[e] : pad;
+            v[e] = from_top ? x : -x;
         }
-        float a = -INFINITY;
-        for (int r = 0; r <= k; ++r) {
+        float a = 0.f;
+        for (int r = 0; r < rounds; ++r) {
             float mx = v[0];
 #pragma unroll
-            for (int e = 1; e < kPerLane; ++e) mx = fmaxf(mx, v[e]);
+            for (int e = 1; e < kP; ++e) mx = fmaxf(mx, v[e]);
             float wm = mx;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+            for (int off = 16; off > 0; off >>= 1)
+                wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
             a = wm;
-            if (r == k) break;
+            if (r + 1 == rounds) break;
             // remove one occurrence of the maximum: in the lowest lane holding it, its first
             const unsigned holders = __ballot_sync(0xffffffffu, mx == wm);
             if (lane == __ffs(holders) - 1) {
                 bool done = false;
 #pragma unroll
-                for (int e = 0; e < kPerLane; ++e)
+                for (int e = 0; e < kP; ++e)
                     if (!done && v[e] == wm) {
                         v[e] = -INFINITY;
                         done = true;
                     }
             }
         }
-        if (lane == 0) alpha[i] = a;
+        if (lane == 0) alpha[i] = from_top ? a : -a;
     }
 }
 
@@ -109,11 +123,23 @@ __global__ void __launch_bounds__(256) qb_hist_kernel(const float* __restrict__ 
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = min(m, r0 + rows_per_cta);
     if (live) {
-        for (int64_t i = r0 + warp; i < r1; i += 8) {
-            const uint32_t key = desc_key(s[i * n + col] - __ldg(alpha + i));
+        auto count = [&](float x, float al) {
+            const uint32_t key = desc_key(x - al);
             if (shift == 24 || (key >> (shift + 8)) == prefix)
                 atomicAdd(&sh[lane][(key >> shift) & 255u], 1u);
+        };
+        int64_t i = r0 + warp;
+        for (; i + 24 < r1; i += 32) {  // four rows per step, loads first
+            float x[4], al[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                x[u] = s[(i + 8 * u) * n + col];
+                al[u] = __ldg(alpha + i + 8 * u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) count(x[u], al[u]);
         }
+        for (; i < r1; i += 8) count(s[i * n + col], __ldg(alpha + i));
     }
     __syncthreads();
     for (int idx = threadIdx.x; idx < 32 * 256; idx += blockDim.x) {
@@ -218,7 +244,19 @@ cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, i
         const int64_t want = (m + 7) / 8;
         const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
         ProfScope prof("qb_alpha_kernel", stream);
-        qb_alpha_kernel<<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+        const int per_lane = (n + 31) / 32;
+        if (per_lane <= 1)
+            qb_alpha_kernel<1><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+        else if (per_lane <= 2)
+            qb_alpha_kernel<2><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+        else if (per_lane <= 4)
+            qb_alpha_kernel<4><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+        else if (per_lane <= 8)
+            qb_alpha_kernel<8><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+        else if (per_lane <= 16)
+            qb_alpha_kernel<16><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+        else
+            qb_alpha_kernel<32><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
     }
     const uint32_t q = (uint32_t)((m * k) / n);
     const int col_blocks = (n + 31) / 32;
