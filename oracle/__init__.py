@@ -57,8 +57,10 @@ def _load():
             lib.kda_oracle_gate.restype = None
             lib.kda_oracle_gate.argtypes = [_dp, _dp, ctypes.c_double, _dp,
                                             ctypes.c_int64, ctypes.c_int, ctypes.c_int]
-            common = [_dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_double, _dp, _dp, _i64p,
-                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+            lib.kda_oracle_gate_softplus_value.restype = ctypes.c_double
+            lib.kda_oracle_gate_softplus_value.argtypes = [ctypes.c_double] * 2
+            common = [_dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_double, ctypes.c_int, _dp, _dp,
+                      _i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_recurrent.restype = ctypes.c_int
             lib.kda_oracle_recurrent.argtypes = common + [_dp, ctypes.c_int]
             lib.kda_oracle_chunked.restype = ctypes.c_int
@@ -116,8 +118,16 @@ def output_norm_gate(o, gate, w=None, eps: float = 1e-6) -> np.ndarray:
     return y
 
 
+GATES = {"sigmoid": 0, "softplus": 1}
+
+
+def gate_softplus_value(z: float, A_log: float) -> float:
+    """g = -e^{A_log} softplus(z): the gate the lower bound replaces."""
+    return float(_load().kda_oracle_gate_softplus_value(float(z), float(A_log)))
+
+
 def _run(mode, q, k, v, beta, z, A_log, g_min, S0=None, cu_seqlens=None, C=64,
-         nthreads=None, want_state=True):
+         nthreads=None, want_state=True, gate="sigmoid"):
     q, k, v, beta, z, A_log = (_f64(x) for x in (q, k, v, beta, z, A_log))
     T, H, dk = q.shape
     dv = v.shape[2]
@@ -137,7 +147,7 @@ def _run(mode, q, k, v, beta, z, A_log, g_min, S0=None, cu_seqlens=None, C=64,
     nt = default_threads() if nthreads is None else int(nthreads)
     lib = _load()
     args = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z), _ptr(A_log), float(g_min),
-            _ptr(S0c), _ptr(S_out), cu.ctypes.data_as(_i64p), N, H, dk, dv]
+            GATES[gate], _ptr(S0c), _ptr(S_out), cu.ctypes.data_as(_i64p), N, H, dk, dv]
     if mode == "recurrent":
         rc = lib.kda_oracle_recurrent(*args, _ptr(o), nt)
     else:
@@ -148,17 +158,20 @@ def _run(mode, q, k, v, beta, z, A_log, g_min, S0=None, cu_seqlens=None, C=64,
 
 
 def recurrent(q, k, v, beta, z, A_log, g_min, S0=None, cu_seqlens=None, nthreads=None,
-              want_state=True):
-    """Token-by-token KDA.  Returns (o [T,H,dv], S_out [N,H,dk,dv]) in float64."""
+              want_state=True, gate="sigmoid"):
+    """Token-by-token KDA.  Returns (o [T,H,dv], S_out [N,H,dk,dv]) in float64.
+
+    gate: "sigmoid" (g_min * sigmoid(e^A z)) or "softplus" (-e^A softplus(z); g_min unused).
+    """
     return _run("recurrent", q, k, v, beta, z, A_log, g_min, S0, cu_seqlens,
-                nthreads=nthreads, want_state=want_state)
+                nthreads=nthreads, want_state=want_state, gate=gate)
 
 
 def chunked(q, k, v, beta, z, A_log, g_min, S0=None, cu_seqlens=None, C=64, nthreads=None,
-            want_state=True):
+            want_state=True, gate="sigmoid"):
     """The same result through the chunkwise-parallel form (chunk length C)."""
     return _run("chunked", q, k, v, beta, z, A_log, g_min, S0, cu_seqlens, C=C,
-                nthreads=nthreads, want_state=want_state)
+                nthreads=nthreads, want_state=want_state, gate=gate)
 
 
 def decode_steps(S, q, k, v, beta, z, A_log, g_min, nthreads=None):

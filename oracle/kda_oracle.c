@@ -14,7 +14,8 @@
  *            section "Chunkwise parallel form": gamma^{i->j}, Gamma, W = M(Gamma*K),
  *                U = M V, pseudo-values V~ = U - W S, A = Tril[(Q*Gamma)(K/Gamma)^T],
  *                O = (Gamma*Q) S + A V~;  and the bounded gate
- *                g = g_min * Sigmoid(e^{A_h} z),  alpha = exp(g).
+ *                g = g_min * Sigmoid(e^{A_h} z),  alpha = exp(g);  and the gate it
+ *                replaces, g = -e^{A_h} Softplus(z) (a comparison variant).
  *   [guide]  "A Look at Kimi K3: Three Core Innovations and Engineering Tuning Guide"
  *            section 2.2: the same gate, and its torch pseudocode
  *            g_min * sigmoid(exp(Ah) * z).
@@ -61,6 +62,23 @@ double kda_oracle_gate_value(double z, double A_log, double g_min)
     return g_min * logistic(exp(A_log) * z);
 }
 
+/* Softplus(x) = ln(1 + e^x), written so that e^x never overflows. */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
+
+/* [blog] "Chunkwise parallel form", the gate the bound replaces:
+ * g = -e^{A_h} Softplus(z), in (-inf, 0). */
+double kda_oracle_gate_softplus_value(double z, double A_log)
+{
+    return -exp(A_log) * softplus(z);
+}
+
+/* The gate of a job: kind 0 = bounded sigmoid gate, 1 = negative softplus (g_min unused). */
+static double gate_of(int kind, double z, double A_log, double g_min)
+{
+    return kind == 1 ? kda_oracle_gate_softplus_value(z, A_log)
+                     : kda_oracle_gate_value(z, A_log, g_min);
+}
+
 void kda_oracle_gate(const double *z, const double *A_log, double g_min, double *g,
                      int64_t n_tokens, int H, int dk)
 {
@@ -99,6 +117,7 @@ typedef struct {
     double *S_out, *o;
     const int64_t *cu;
     double g_min;
+    int gate_kind; /* 0 = bounded sigmoid gate, 1 = negative softplus */
     int N, H, dk, dv, C;
     int mode; /* 0 = token recurrence, 1 = chunked form */
     int64_t next_unit;
@@ -131,7 +150,7 @@ static void recurrent_unit(const job_t *J, int n, int h, double *S, double *u, d
         double *ot = J->o + (t * H + h) * dv;
 
         for (int i = 0; i < dk; ++i)
-            alpha[i] = exp(kda_oracle_gate_value(zt[i], J->A_log[h], J->g_min));
+            alpha[i] = exp(gate_of(J->gate_kind, zt[i], J->A_log[h], J->g_min));
         /* S' = Diag(alpha) S */
         for (int i = 0; i < dk; ++i)
             for (int j = 0; j < dv; ++j)
@@ -203,7 +222,7 @@ static void chunked_unit(const job_t *J, int n, int h, double *S, const chunk_ws
         for (int c = 0; c < dk; ++c) {
             double run = 1.0;
             for (int r = 0; r < L; ++r) {
-                run *= exp(kda_oracle_gate_value(Z_(r, c), J->A_log[h], J->g_min));
+                run *= exp(gate_of(J->gate_kind, Z_(r, c), J->A_log[h], J->g_min));
                 w->Gam[r * dk + c] = run;
             }
         }
@@ -353,17 +372,21 @@ static int run_job(job_t *J, int nthreads)
 /*
  * Token-by-token KDA over packed sequences.  Returns 0 on success, 1 on bad
  * sizes, 2 on bad cu_seqlens.  S0 may be NULL (zero state); S_out may be NULL.
+ * gate_kind 0: the bounded gate g_min Sigmoid(e^{A_h} z); 1: -e^{A_h} Softplus(z), the
+ * gate the bound replaces (g_min unused).  The chunked form below multiplies decays
+ * into exact fp64 products, which underflow when a chunk's total decay passes e^-745:
+ * fine for the bounded gate, not for every softplus input.
  */
 int kda_oracle_recurrent(const double *q, const double *k, const double *v,
                          const double *beta, const double *z, const double *A_log,
-                         double g_min, const double *S0, double *S_out,
+                         double g_min, int gate_kind, const double *S0, double *S_out,
                          const int64_t *cu_seqlens, int N, int H, int dk, int dv,
                          double *o, int nthreads)
 {
     job_t J;
     memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.beta = beta; J.z = z; J.A_log = A_log; J.S0 = S0;
-    J.S_out = S_out; J.o = o; J.cu = cu_seqlens; J.g_min = g_min;
+    J.S_out = S_out; J.o = o; J.cu = cu_seqlens; J.g_min = g_min; J.gate_kind = gate_kind;
     J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.C = 1; J.mode = 0;
     return run_job(&J, nthreads);
 }
@@ -371,14 +394,14 @@ int kda_oracle_recurrent(const double *q, const double *k, const double *v,
 /* Same result through the chunkwise-parallel form with chunk length C. */
 int kda_oracle_chunked(const double *q, const double *k, const double *v,
                        const double *beta, const double *z, const double *A_log,
-                       double g_min, const double *S0, double *S_out,
+                       double g_min, int gate_kind, const double *S0, double *S_out,
                        const int64_t *cu_seqlens, int N, int H, int dk, int dv,
                        int C, double *o, int nthreads)
 {
     job_t J;
     memset(&J, 0, sizeof(J));
     J.q = q; J.k = k; J.v = v; J.beta = beta; J.z = z; J.A_log = A_log; J.S0 = S0;
-    J.S_out = S_out; J.o = o; J.cu = cu_seqlens; J.g_min = g_min;
+    J.S_out = S_out; J.o = o; J.cu = cu_seqlens; J.g_min = g_min; J.gate_kind = gate_kind;
     J.N = N; J.H = H; J.dk = dk; J.dv = dv; J.C = C; J.mode = 1;
     return run_job(&J, nthreads);
 }
