@@ -313,6 +313,10 @@ def run_ours(args, rank, world, local_rank, dist):
     # workload's z standing in for the gate logits (same shape, N(0, 1))
     og = bench_output_gate(dev, stream, peaks, o, d["z"])
 
+    # what the bound buys: the same forward on the explicit per-pair path, with the bounded
+    # gate and with the unbounded gate it replaces
+    gcmp = bench_gate_comparison(dev, stream, d, sp, o, S_out, ms_per_step)
+
     # quantile balancing of a routing batch (65536 tokens x 256 experts, k = 8)
     qbm = bench_quantile_balance(dev, stream, peaks)
 
@@ -344,7 +348,7 @@ def run_ours(args, rank, world, local_rank, dist):
                 "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
                 "roofline": roofline, "e2e": e2e,
                 "gpu_launches": int(round(launches_per_step * args.steps)),
-                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "decode": dec, "cpu_baseline": cpu}
+                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "gate_comparison": gcmp, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
 
 
@@ -376,6 +380,46 @@ def bench_output_gate(dev, stream, peaks, o, gate, reps=20):
             "traffic": traffic_from_profile(
                 "output_gate_kernel",
                 source_hash("serving_kda_chunkwise_gb300/csrc/output_gate.cu"))}
+
+
+def bench_gate_comparison(dev, stream, d, sp, o, S_out, bounded_ms, reps=2):
+    """The forward on the explicit path (every pair's decay formed on CUDA cores), with the
+    bounded sigmoid gate and with the negative-softplus gate it replaces, against the
+    tensor-core path that the bound makes possible (bounded_ms, timed above)."""
+    import torch
+
+    from serving_kda_chunkwise_gb300 import kda
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(dev)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(reps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return ev0.elapsed_time(ev1) / reps
+
+    def explicit_sigmoid():
+        os.environ["KDA_FWD_PATH"] = "generic"
+        try:
+            kda.fwd_chunked(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], sp.g_min,
+                            cu_seqlens=None, N=1, o=o, S_out=S_out, stream=stream)
+        finally:
+            del os.environ["KDA_FWD_PATH"]
+
+    def explicit_softplus():
+        kda.fwd_chunked_softplus(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"],
+                                 cu_seqlens=None, N=1, o=o, S_out=S_out, stream=stream)
+
+    ms_sig = timed(explicit_sigmoid)
+    ms_sp = timed(explicit_softplus)
+    return {"bounded_gate_tensor_core_ms": bounded_ms, "bounded_gate_explicit_ms": ms_sig,
+            "softplus_gate_explicit_ms": ms_sp,
+            "speedup_of_bound": ms_sp / bounded_ms, "steps": reps,
+            "kernel": "fwd_generic_kernel"}
 
 
 def bench_quantile_balance(dev, stream, peaks, reps=20):

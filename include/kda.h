@@ -108,6 +108,21 @@ kda_status_t kda_fwd_chunked(const void *q, const void *k, const void *v, const 
                              void *workspace, size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * kda_fwd_chunked_softplus -- the same chunked forward with the gate the bound replaces
+ * ([blog] "Chunkwise parallel form"): g = -e^{A_log[h]} Softplus(z), unbounded below, so
+ * no decay factor can be split into a bounded row factor and column factor.  This runs the
+ * explicit path (every pair's decay e^{G_r - G_i}, exponent <= 0, formed on CUDA cores in
+ * fp32), a comparison variant: it measures what the bound buys.  Arguments as
+ * kda_fwd_chunked without g_min and without a workspace (none is needed).  z must be finite
+ * or -inf.
+ */
+kda_status_t kda_fwd_chunked_softplus(const void *q, const void *k, const void *v,
+                                      const void *beta, const void *z, const float *A_log,
+                                      const float *S0, float *S_out, const int32_t *cu_seqlens,
+                                      int N, int64_t T_total, int H, int dk, int dv,
+                                      kda_dtype_t io_dt, void *o, kda_stream_t stream);
+
+/*
  * kda_decode_step -- one token of the KDA recurrence ([blog] "Kimi Delta Attention")
  * for N independent sequences, updating the state in place:
  *   alpha = exp(g_min * Sigmoid(exp(A_log[h]) z));  S <- Diag(alpha) S;

@@ -194,6 +194,51 @@ kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const 
     return KDA_OK;
 }
 
+kda_status_t kda_fwd_chunked_softplus(const void* q, const void* k, const void* v,
+                                      const void* beta, const void* z, const float* A_log,
+                                      const float* S0, float* S_out, const int32_t* cu_seqlens,
+                                      int N, int64_t T_total, int H, int dk, int dv,
+                                      kda_dtype_t io_dt, void* o, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
+    KDA_REQUIRE(N >= 0, "N=%d must be >= 0", N);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    KDA_REQUIRE(T_total >= 0, "T_total=%lld must be >= 0", (long long)T_total);
+    if (kda_status_t s = check_dims(dk, dv)) return s;
+    if (cu_seqlens == nullptr) {
+        KDA_REQUIRE(N > 0 || T_total == 0, "N=0 requires T_total=0");
+        KDA_REQUIRE(N == 0 || T_total % N == 0,
+                    "without cu_seqlens T_total=%lld must be a multiple of N=%d",
+                    (long long)T_total, N);
+    }
+    KDA_REQUIRE((int64_t)N * H * 4 < (int64_t)1 << 31, "N*H=%lld is too large",
+                (long long)N * H);
+    if (N == 0) return KDA_OK;
+    if (T_total > 0) {
+        KDA_REQUIRE_PTR(q, "q");
+        KDA_REQUIRE_PTR(k, "k");
+        KDA_REQUIRE_PTR(v, "v");
+        KDA_REQUIRE_PTR(z, "z");
+        KDA_REQUIRE_PTR(o, "o");
+        KDA_REQUIRE(beta != nullptr, "beta is NULL");
+    }
+    KDA_REQUIRE_PTR(A_log, "A_log");
+    KDA_OPTIONAL_PTR(S0, "S0");
+    KDA_OPTIONAL_PTR(S_out, "S_out");
+    KDA_OPTIONAL_PTR(cu_seqlens, "cu_seqlens");
+    kda::FwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.z = z;
+    a.A_log = A_log; a.g_min = -1.f; a.S0 = S0; a.S_out = S_out;
+    a.cu_seqlens = cu_seqlens; a.N = N; a.T_total = T_total; a.H = H; a.dk = dk; a.dv = dv;
+    a.io_bf16 = (io_dt == KDA_BF16); a.gate_kind = 1; a.o = o;
+    a.dev_err = device_error_ptr();
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (a.dev_err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
+    cudaError_t e = kda::launch_fwd_generic(a);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_chunked_softplus launch");
+    return KDA_OK;
+}
+
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* beta,
                              const void* z, const float* A_log, float g_min, float* S, int N,
                              int H, int dk, int dv, kda_dtype_t io_dt, void* o,

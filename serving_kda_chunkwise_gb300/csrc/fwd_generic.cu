@@ -13,7 +13,9 @@
 //   O  = (Gamma*Q) S + A Vt
 //   S <- Diag(gamma^C) S + (K * gamma^C / Gamma)^T Vt
 // Every decay factor is formed as e^{(difference of log-decays)} with a non-positive
-// exponent, so nothing can overflow for any g_min.
+// exponent, so nothing can overflow for any g_min -- nor for the unbounded gate the bound
+// replaces, g = -e^{A_h} Softplus(z), which this kernel also takes (gate_kind = 1): it is the
+// explicit per-pair path that such a gate needs.
 //
 // Parallelism: one CTA per (sequence, head, 32-column slice of d_v).  The columns of S
 // evolve independently (each column obeys the recurrence with its own v_j), so the
@@ -92,7 +94,8 @@ __global__ void __launch_bounds__(kThreads) fwd_generic_kernel(FwdArgs a) {
                 const size_t off = ((size_t)(t0 + r) * H + h) * DK + c;
                 qq = to_f32(q[off]);
                 kk = to_f32(k[off]);
-                gg = gate_precise(to_f32(z[off]), scale, a.g_min);
+                gg = a.gate_kind ? gate_softplus(to_f32(z[off]), scale)
+                                 : gate_precise(to_f32(z[off]), scale, a.g_min);
             }
             sQ[r * PK + c] = qq;
             sK[r * PK + c] = kk;

@@ -27,6 +27,14 @@ __device__ __forceinline__ float gate_precise(float z, float scale, float g_min)
     return g_min / (1.0f + expf(-scale * z));
 }
 
+// The gate the bound replaces (same page and section): g = -e^{A_h} Softplus(z), in
+// (-inf, 0), Softplus(z) = ln(1 + e^z) written so that e^z never overflows.  z = -inf gives
+// -0 (alpha = 1); z must be finite otherwise (z = +inf would give g = -inf).
+__device__ __forceinline__ float gate_softplus(float z, float scale) {
+    const float sp = z > 0.f ? z + log1pf(expf(-z)) : log1pf(expf(z));
+    return -scale * sp;
+}
+
 // Token range [begin, end) of sequence n.  cu == nullptr means N equal sequences of
 // T_total / N tokens.  A malformed range raises kDevErrBadSeqlens and reads as empty.
 __device__ __forceinline__ void seq_range(const int32_t* cu, int n, int N, int64_t T_total,

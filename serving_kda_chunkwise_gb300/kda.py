@@ -66,6 +66,9 @@ def _load():
     lib.kda_quantile_balance_workspace_size.argtypes = [i64, i32]
     lib.kda_quantile_balance.restype = ctypes.c_int
     lib.kda_quantile_balance.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.kda_fwd_chunked_softplus.restype = ctypes.c_int
+    lib.kda_fwd_chunked_softplus.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32,
+                                             i32, i32, i32, vp, vp]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [vp]
     lib.kda_profile_begin.restype = ctypes.c_int
@@ -264,6 +267,35 @@ def fwd_chunked_host(q, k, v, beta, z, A_log, g_min: float, S0=None, cu_seqlens=
         t.record_stream(s_out)
     cur.wait_stream(s_out)
     s_out.synchronize()
+    return o, S_out
+
+
+def fwd_chunked_softplus(q, k, v, beta, z, A_log, S0=None, cu_seqlens=None, N=None, o=None,
+                         S_out=None, want_state=True, stream=None):
+    """The chunked forward with the unbounded gate -e^A softplus(z) (explicit path).
+
+    Same arguments as fwd_chunked without g_min and workspace.  Returns (o, S_out).
+    """
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (z, "z")):
+        _need(t, nm, q.dtype)
+    _need(A_log, "A_log", torch.float32)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    elif N is None:
+        N = 1
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=q.dtype, device=q.device)
+    if S_out is None and want_state:
+        S_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
+    if S0 is not None:
+        _need(S0, "S0", torch.float32)
+    _check(_lib.kda_fwd_chunked_softplus(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z),
+                                         _ptr(A_log), _ptr(S0), _ptr(S_out), _ptr(cu_seqlens),
+                                         int(N), int(T), int(H), int(dk), int(dv), _dt(q),
+                                         _ptr(o), _stream(stream)), "kda_fwd_chunked_softplus")
     return o, S_out
 
 

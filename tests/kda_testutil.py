@@ -80,7 +80,7 @@ def gpu_forward(inp, use_cu=True, want_state=True, **kw):
     return o, S
 
 
-def oracle_forward(inp, seqs=None, heads=None, nthreads=None):
+def oracle_forward(inp, seqs=None, heads=None, nthreads=None, gate="sigmoid"):
     """Oracle on the exact stored inputs, optionally restricted to some sequences/heads.
 
     Returns dict {(n, h): (o [len, dv], S [dk, dv])} in float64.
@@ -101,7 +101,7 @@ def oracle_forward(inp, seqs=None, heads=None, nthreads=None):
             t = {kind: sp.tokens(kind, a, b, hs) for kind in ("q", "k", "v", "beta", "z")}
         S0 = None if S0_all is None else S0_all[n:n + 1][:, hs]
         o, S = oracle.recurrent(t["q"], t["k"], t["v"], t["beta"], t["z"], sp.A_log[hs], sp.g_min,
-                                S0=S0, nthreads=nthreads)
+                                S0=S0, nthreads=nthreads, gate=gate)
         for ii, h in enumerate(hs):
             out[(n, h)] = (o[:, ii], S[0, ii])
     return out

@@ -160,3 +160,21 @@ def test_quantile_balance_validation(lib):
     rc = lib.kda_quantile_balance(a, a, i64(0), 64, 8, a, None, None, a,
                                   ctypes.c_size_t(need), None)
     assert rc == 1
+
+
+def test_softplus_forward_validation(lib):
+    vp = ctypes.c_void_p
+    a = vp(0x10000)
+    i64 = ctypes.c_int64
+    lib.kda_fwd_chunked_softplus.restype = ctypes.c_int
+    lib.kda_last_error.restype = ctypes.c_char_p
+    # q, k, v, beta, z, A_log, S0, S_out, cu, N, T, H, dk, dv, io_dt, o, stream
+    rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 1, i64(64), 2, 96,
+                                      128, 1, a, None)
+    assert rc == 2
+    rc = lib.kda_fwd_chunked_softplus(a, a, a, a, None, a, None, None, None, 1, i64(64), 2, 128,
+                                      128, 1, a, None)
+    assert rc == 1 and b"z is NULL" in lib.kda_last_error()
+    rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 3, i64(64), 2, 128,
+                                      128, 1, a, None)
+    assert rc == 1 and b"multiple of N" in lib.kda_last_error()
