@@ -11,7 +11,8 @@ What it computes, and the page each step follows, is written at the top of
 chunkwise-parallel form with an explicit forward-substitution inverse, plus the
 lower-bounded sigmoid gate and the gated, RMS-normalised output step.  The
 quantile-balancing bias update of the mixture-of-experts router is plain numpy, in
-``oracle/quantile_balance.py``.
+``oracle/quantile_balance.py``; the gradients of the forward are fp64 torch reverse-mode
+differentiation of the token recurrence, in ``oracle/kda_backward.py``.
 """
 from __future__ import annotations
 
