@@ -123,6 +123,28 @@ kda_status_t kda_fwd_chunked_softplus(const void *q, const void *k, const void *
                                       kda_dtype_t io_dt, void *o, kda_stream_t stream);
 
 /*
+ * kda_bwd -- gradients of kda_fwd_chunked's outputs ([blog] "Kimi Delta Attention": the
+ * derivatives of the recurrence the page defines; the pages print no backward).  For a loss
+ * with gradient dout [T_total, H, dv] io_dt on o and dS_out [N, H, dk, dv] fp32 (or NULL) on
+ * S_out, writes
+ *   dq, dk, dz : [T_total, H, dk] io_dt     dv : [T_total, H, dv] io_dt
+ *   dbeta      : [T_total, H] io_dt         dA_log : [H] fp32 (summed over sequences)
+ *   dS0        : [N, H, dk, dv] fp32, or NULL when not wanted
+ * Other arguments as kda_fwd_chunked (same inputs, S0 may be NULL).  The workspace
+ * (kda_bwd_workspace_size bytes) holds the state at every chunk start and per-CTA scratch.
+ * This is the token-level reverse recurrence on CUDA cores in fp32: correct for every
+ * shape kda_fwd_chunked takes, serial over the tokens of a sequence (not the chunked
+ * tensor-core backward).  Deterministic.
+ */
+size_t kda_bwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv);
+kda_status_t kda_bwd(const void *q, const void *k, const void *v, const void *beta,
+                     const void *z, const float *A_log, float g_min, const float *S0,
+                     const int32_t *cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
+                     kda_dtype_t io_dt, const void *dout, const float *dS_out, void *dq,
+                     void *dk_out, void *dv_out, void *dbeta, void *dz, float *dA_log,
+                     float *dS0, void *workspace, size_t ws_bytes, kda_stream_t stream);
+
+/*
  * kda_decode_step -- one token of the KDA recurrence ([blog] "Kimi Delta Attention")
  * for N independent sequences, updating the state in place:
  *   alpha = exp(g_min * Sigmoid(exp(A_log[h]) z));  S <- Diag(alpha) S;

@@ -239,6 +239,64 @@ kda_status_t kda_fwd_chunked_softplus(const void* q, const void* k, const void* 
     return KDA_OK;
 }
 
+size_t kda_bwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv) {
+    if (T_total < 0 || N <= 0 || H <= 0 || check_dims(dk, dv) != KDA_OK) return 0;
+    return kda::bwd_workspace_size_public(T_total, N, H, dk, dv);
+}
+
+kda_status_t kda_bwd(const void* q, const void* k, const void* v, const void* beta,
+                     const void* z, const float* A_log, float g_min, const float* S0,
+                     const int32_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
+                     kda_dtype_t io_dt, const void* dout, const float* dS_out, void* dq,
+                     void* dk_out, void* dv_out, void* dbeta, void* dz, float* dA_log,
+                     float* dS0, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
+    KDA_REQUIRE(N > 0, "N=%d must be positive", N);
+    KDA_REQUIRE(H > 0, "H=%d must be positive", H);
+    KDA_REQUIRE(T_total >= 0, "T_total=%lld must be >= 0", (long long)T_total);
+    if (kda_status_t s = check_dims(dk, dv)) return s;
+    if (kda_status_t s = check_gmin(g_min)) return s;
+    if (cu_seqlens == nullptr)
+        KDA_REQUIRE(T_total % N == 0, "without cu_seqlens T_total=%lld must be a multiple of N=%d",
+                    (long long)T_total, N);
+    KDA_REQUIRE((int64_t)N * H < (int64_t)1 << 31, "N*H=%lld is too large", (long long)N * H);
+    if (T_total > 0) {
+        KDA_REQUIRE_PTR(q, "q");
+        KDA_REQUIRE_PTR(k, "k");
+        KDA_REQUIRE_PTR(v, "v");
+        KDA_REQUIRE_PTR(z, "z");
+        KDA_REQUIRE_PTR(dout, "dout");
+        KDA_REQUIRE_PTR(dq, "dq");
+        KDA_REQUIRE_PTR(dk_out, "dk");
+        KDA_REQUIRE_PTR(dv_out, "dv");
+        KDA_REQUIRE_PTR(dz, "dz");
+        KDA_REQUIRE(beta != nullptr, "beta is NULL");
+        KDA_REQUIRE(dbeta != nullptr, "dbeta is NULL");
+    }
+    KDA_REQUIRE_PTR(A_log, "A_log");
+    KDA_REQUIRE_PTR(dA_log, "dA_log");
+    KDA_OPTIONAL_PTR(S0, "S0");
+    KDA_OPTIONAL_PTR(dS_out, "dS_out");
+    KDA_OPTIONAL_PTR(dS0, "dS0");
+    KDA_OPTIONAL_PTR(cu_seqlens, "cu_seqlens");
+    const size_t need = kda::bwd_workspace_size_public(T_total, N, H, dk, dv);
+    KDA_REQUIRE_PTR(workspace, "workspace");
+    KDA_REQUIRE(ws_bytes >= need, "workspace of %zu bytes is smaller than the %zu needed",
+                ws_bytes, need);
+    kda::BwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.beta = beta; a.z = z; a.dout = dout;
+    a.A_log = A_log; a.g_min = g_min; a.S0 = S0; a.dS_out = dS_out; a.cu_seqlens = cu_seqlens;
+    a.N = N; a.T_total = T_total; a.H = H; a.dk = dk; a.dv = dv; a.io_bf16 = io_dt == KDA_BF16;
+    a.dq = dq; a.dk_ = dk_out; a.dv_ = dv_out; a.dbeta = dbeta; a.dz = dz; a.dA_log = dA_log;
+    a.dS0 = dS0; a.workspace = workspace; a.dev_err = device_error_ptr();
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    if (a.dev_err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
+    cudaError_t e = kda::launch_bwd(a);
+    if (e != cudaSuccess) return cuda_fail(e, "kda_bwd launch");
+    return KDA_OK;
+}
+
 kda_status_t kda_decode_step(const void* q, const void* k, const void* v, const void* beta,
                              const void* z, const float* A_log, float g_min, float* S, int N,
                              int H, int dk, int dv, kda_dtype_t io_dt, void* o,

@@ -29,6 +29,29 @@ struct FwdArgs {
     cudaStream_t stream;
 };
 
+struct BwdArgs {
+    const void *q, *k, *v, *beta, *z, *dout;
+    const float* A_log;
+    float g_min;
+    const float* S0;
+    const float* dS_out;
+    const int32_t* cu_seqlens;
+    int N;
+    int64_t T_total;
+    int H, dk, dv;
+    int io_bf16;
+    void *dq, *dk_, *dv_, *dbeta, *dz;
+    float* dA_log;
+    float* dS0;
+    void* workspace;
+    unsigned* dev_err;
+    cudaStream_t stream;
+};
+
+// Gradients of the forward (bwd.cu): token-level reverse mode on CUDA cores.
+size_t bwd_workspace_size_public(int64_t T_total, int N, int H, int dk, int dv);
+cudaError_t launch_bwd(const BwdArgs& a);
+
 // K1: elementwise gate.
 cudaError_t launch_gate(const void* z, int z_bf16, const float* A_log, float g_min, float* g_out,
                         int64_t n_tokens, int H, int dk, cudaStream_t stream);

@@ -69,6 +69,11 @@ def _load():
     lib.kda_fwd_chunked_softplus.restype = ctypes.c_int
     lib.kda_fwd_chunked_softplus.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32,
                                              i32, i32, i32, vp, vp]
+    lib.kda_bwd_workspace_size.restype = sz
+    lib.kda_bwd_workspace_size.argtypes = [i64, i32, i32, i32, i32]
+    lib.kda_bwd.restype = ctypes.c_int
+    lib.kda_bwd.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, i32, i64, i32, i32, i32, i32,
+                            vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [vp]
     lib.kda_profile_begin.restype = ctypes.c_int
@@ -297,6 +302,43 @@ def fwd_chunked_softplus(q, k, v, beta, z, A_log, S0=None, cu_seqlens=None, N=No
                                          int(N), int(T), int(H), int(dk), int(dv), _dt(q),
                                          _ptr(o), _stream(stream)), "kda_fwd_chunked_softplus")
     return o, S_out
+
+
+def bwd(q, k, v, beta, z, A_log, g_min: float, dout, S0=None, dS_out=None, cu_seqlens=None,
+        N=None, want_dS0=True, workspace=None, stream=None):
+    """Gradients of fwd_chunked's (o, S_out) for upstream gradients dout (and dS_out).
+
+    Returns a dict: dq, dk, dv, dbeta, dz (io dtype), dA_log [H] fp32, dS0 [N,H,dk,dv] fp32.
+    """
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (z, "z"), (dout, "dout")):
+        _need(t, nm, q.dtype)
+    _need(A_log, "A_log", torch.float32)
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if cu_seqlens is not None:
+        _need(cu_seqlens, "cu_seqlens", torch.int32)
+        N = cu_seqlens.numel() - 1
+    elif N is None:
+        N = 1
+    for t, nm in ((S0, "S0"), (dS_out, "dS_out")):
+        if t is not None:
+            _need(t, nm, torch.float32)
+    dev = q.device
+    out = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+           "dbeta": torch.empty_like(beta), "dz": torch.empty_like(z),
+           "dA_log": torch.empty(H, dtype=torch.float32, device=dev),
+           "dS0": (torch.empty((N, H, dk, dv), dtype=torch.float32, device=dev)
+                   if want_dS0 else None)}
+    need = int(_lib.kda_bwd_workspace_size(int(T), int(N), int(H), int(dk), int(dv)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _check(_lib.kda_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z), _ptr(A_log),
+                        float(g_min), _ptr(S0), _ptr(cu_seqlens), int(N), int(T), int(H),
+                        int(dk), int(dv), _dt(q), _ptr(dout), _ptr(dS_out), _ptr(out["dq"]),
+                        _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dbeta"]), _ptr(out["dz"]),
+                        _ptr(out["dA_log"]), _ptr(out["dS0"]), _ptr(workspace),
+                        workspace.numel(), _stream(stream)), "kda_bwd")
+    return out
 
 
 def decode_step(q, k, v, beta, z, A_log, g_min: float, S, o=None, stream=None):

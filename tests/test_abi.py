@@ -178,3 +178,28 @@ def test_softplus_forward_validation(lib):
     rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 3, i64(64), 2, 128,
                                       128, 1, a, None)
     assert rc == 1 and b"multiple of N" in lib.kda_last_error()
+
+
+def test_bwd_validation(lib):
+    vp = ctypes.c_void_p
+    a = vp(0x10000)
+    i64, f = ctypes.c_int64, ctypes.c_float
+    lib.kda_bwd.restype = ctypes.c_int
+    lib.kda_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.kda_last_error.restype = ctypes.c_char_p
+    need = lib.kda_bwd_workspace_size(i64(640), 2, 4, 128, 128)
+    assert need >= (640 // 64 + 3) * 4 * 128 * 128 * 4
+    assert lib.kda_bwd_workspace_size(i64(640), 2, 4, 96, 128) == 0
+
+    def call(**kw):
+        args = dict(q=a, k=a, v=a, beta=a, z=a, A=a, gmin=f(-5.0), S0=None, cu=None, N=2,
+                    T=i64(640), H=4, dk=128, dv=128, dt=1, do=a, dS=None, dq=a, dkk=a, dvv=a,
+                    db=a, dz=a, dA=a, dS0=None, ws=a, wsb=ctypes.c_size_t(need))
+        args.update(kw)
+        return lib.kda_bwd(*args.values(), None)
+
+    assert call(dk=96) == 2
+    assert call(gmin=f(0.5)) == 1
+    assert call(do=None) == 1 and b"dout is NULL" in lib.kda_last_error()
+    assert call(wsb=ctypes.c_size_t(need - 1)) == 1 and b"workspace" in lib.kda_last_error()
+    assert call(T=i64(641)) == 1 and b"multiple of N" in lib.kda_last_error()

@@ -1,0 +1,89 @@
+"""GPU parity of the backward (kda_bwd) against the fp64 reverse-mode oracle
+(oracle/kda_backward.py), on the same stored inputs and upstream gradients.
+
+Tolerance, per (sequence, head) and gradient tensor: fp32 I/O ||d - d_ref||_F / ||d_ref||_F
+<= 1e-4; bf16 I/O the forward's rule (after dividing by rms(d_ref): |d - d_ref| <= 2e-2 +
+1.6e-2 |d_ref| and rms(d - d_ref) <= 1e-2).  dA_log (summed over sequences) and dS0 are fp32
+outputs: relative 1e-4 for fp32 problems, 1e-2 for bf16 problems.
+"""
+import numpy as np
+import pytest
+
+from oracle import kda_backward as kb
+from serving_kda_chunkwise_gb300 import inputs
+from kda_testutil import BF16_NORM_TOL, BF16_RMS_TOL, bf16_norm_err, bf16_rms_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import torch  # noqa: F401
+    from serving_kda_chunkwise_gb300 import kda as _k
+    return _k
+
+
+def _close(d, ref, dtype, what):
+    d = np.asarray(d, dtype=np.float64)
+    assert np.all(np.isfinite(d)), what
+    if dtype == "f32":
+        rel = np.linalg.norm(d - ref) / max(np.linalg.norm(ref), 1e-30)
+        assert rel <= 1e-4, f"{what}: {rel:.3e}"
+    else:
+        assert bf16_norm_err(d, ref) <= BF16_NORM_TOL, what
+        assert bf16_rms_err(d, ref) <= BF16_RMS_TOL, what
+
+
+def _run(kda, lengths, H, d, dtype, seed, with_dS=True):
+    import torch
+    inp = inputs.forward_inputs(seed=seed, lengths=lengths, H=H, dk=d, dv=d, dtype=dtype,
+                                with_state=True)
+    rng = np.random.default_rng(seed + 1)
+    T, N = int(inp.cu_seqlens[-1]), len(lengths)
+    do = inputs.store(rng.standard_normal((T, H, d)).astype(np.float32), dtype)
+    dS = rng.standard_normal((N, H, d, d)).astype(np.float32) if with_dS else None
+    dev = {nm: getattr(inp, nm).as_torch("cuda") for nm in ("q", "k", "v", "beta", "z")}
+    g = kda.bwd(dev["q"], dev["k"], dev["v"], dev["beta"], dev["z"],
+                torch.from_numpy(inp.A_log).cuda(), inp.g_min, do.as_torch("cuda"),
+                S0=torch.from_numpy(inp.S0).cuda(),
+                dS_out=None if dS is None else torch.from_numpy(dS).cuda(),
+                cu_seqlens=torch.from_numpy(inp.cu_seqlens.astype(np.int32)).cuda())
+    kda.device_status()
+    ref = kb.backward(inp.q.values, inp.k.values, inp.v.values, inp.beta.values, inp.z.values,
+                      inp.A_log, inp.g_min, do.values, S0=inp.S0, dS_out=dS,
+                      cu_seqlens=inp.cu_seqlens)
+    cu = inp.cu_seqlens
+    for nm in ("dq", "dk", "dv", "dbeta", "dz"):
+        got = g[nm].float().cpu().numpy()
+        for n in range(N):
+            a, b = int(cu[n]), int(cu[n + 1])
+            if b == a:
+                continue
+            for h in range(H):
+                _close(got[a:b, h], ref[nm][a:b, h], dtype, f"{nm} seq {n} head {h}")
+    tol = 1e-4 if dtype == "f32" else 1e-2
+    dA, dS0 = g["dA_log"].cpu().numpy(), g["dS0"].cpu().numpy()
+    np.testing.assert_allclose(dA, ref["dA_log"], rtol=tol,
+                               atol=tol * np.max(np.abs(ref["dA_log"])))
+    for n in range(N):
+        for h in range(H):
+            rel = np.linalg.norm(dS0[n, h] - ref["dS0"][n, h]) / np.linalg.norm(ref["dS0"][n, h])
+            assert rel <= tol, f"dS0 seq {n} head {h}: {rel:.3e}"
+    return g
+
+
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("f32", 128), ("bf16", 128)])
+def test_matches_oracle(kda, dtype, d):
+    _run(kda, [70, 0, 129, 1], H=2, d=d, dtype=dtype, seed=71)
+
+
+def test_without_final_state_gradient(kda):
+    _run(kda, [200], H=3, d=64, dtype="f32", seed=72, with_dS=False)
+
+
+def test_deterministic(kda):
+    import torch
+    g1 = _run(kda, [150, 33], H=2, d=128, dtype="bf16", seed=73)
+    g2 = _run(kda, [150, 33], H=2, d=128, dtype="bf16", seed=73)
+    for nm in g1:
+        assert torch.equal(g1[nm], g2[nm]), nm
