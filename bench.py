@@ -317,6 +317,10 @@ def run_ours(args, rank, world, local_rank, dist):
     # gate and with the unbounded gate it replaces
     gcmp = bench_gate_comparison(dev, stream, d, sp, o, S_out, ms_per_step)
 
+    # gradients of the same forward (token-level backward), the workload's v standing in for
+    # the upstream gradient of o
+    bw = bench_backward(dev, stream, d, sp, peaks) if not args.no_backward else None
+
     # quantile balancing of a routing batch (65536 tokens x 256 experts, k = 8)
     qbm = bench_quantile_balance(dev, stream, peaks)
 
@@ -348,7 +352,7 @@ def run_ours(args, rank, world, local_rank, dist):
                 "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
                 "roofline": roofline, "e2e": e2e,
                 "gpu_launches": int(round(launches_per_step * args.steps)),
-                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "gate_comparison": gcmp, "decode": dec, "cpu_baseline": cpu}
+                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "gate_comparison": gcmp, "backward": bw, "decode": dec, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
 
 
@@ -380,6 +384,35 @@ def bench_output_gate(dev, stream, peaks, o, gate, reps=20):
             "traffic": traffic_from_profile(
                 "output_gate_kernel",
                 source_hash("serving_kda_chunkwise_gb300/csrc/output_gate.cu"))}
+
+
+def bench_backward(dev, stream, d, sp, peaks, reps=1):
+    """kda_bwd on the forward workload (one sequence of 65536 tokens, 32 heads)."""
+    import torch
+
+    from serving_kda_chunkwise_gb300 import kda
+    T_, H_, dk = d["q"].shape
+    dS = torch.zeros((1, H_, dk, dk), dtype=torch.float32, device=dev)
+    ws = torch.empty(kda.library().kda_bwd_workspace_size(T_, 1, H_, dk, dk), dtype=torch.uint8,
+                     device=dev)
+
+    def run():
+        return kda.bwd(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], sp.g_min, d["v"],
+                       dS_out=dS, N=1, workspace=ws, stream=stream)
+
+    run()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(reps):
+        run()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1) / reps
+    return {"ms_per_call": ms, "tokens_per_s": T_ / (ms / 1e3), "T": T_, "H": H_, "d": dk,
+            "form": "token-level reverse recurrence on CUDA cores (serial over tokens)",
+            "kernels": ["bwd_ckpt_kernel", "bwd_kernel", "bwd_dA_kernel"]}
 
 
 def bench_gate_comparison(dev, stream, d, sp, o, S_out, bounded_ms, reps=2):
@@ -531,6 +564,7 @@ def main():
     ap.add_argument("--decode-steps", type=int, default=200)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="run the forward workload with this many heads instead of 32 (a "
                          "smaller case for profiler captures; not a bench line)")
