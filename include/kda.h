@@ -211,6 +211,16 @@ kda_status_t kda_quantile_balance(const float *scores, const float *bias, int64_
                                   void *workspace, size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * kda_selftest_timeout -- the failure path of the bounded device waits, without a fault:
+ * enqueues a kernel that waits on an mbarrier nothing ever arrives on, gives up after
+ * limit_us microseconds (1 .. 2e6), sets the timeout bit of the device error word and
+ * returns, exactly as the library's kernels do when a wait runs out.  The next
+ * kda_device_status() on the stream then returns KDA_ERR_TIMEOUT (and clears the word).
+ * Not part of the method; a diagnostic of the error reporting.
+ */
+kda_status_t kda_selftest_timeout(unsigned limit_us, kda_stream_t stream);
+
+/*
  * Waits for `stream`, then reads and clears the device error word that kernels set
  * when they meet malformed device-side input or give up a bounded wait.  Returns
  * KDA_OK, KDA_ERR_DEVICE or KDA_ERR_TIMEOUT (or KDA_ERR_CUDA if the wait failed).

@@ -405,6 +405,18 @@ kda_status_t kda_quantile_balance(const float* scores, const float* bias, int64_
     return KDA_OK;
 }
 
+kda_status_t kda_selftest_timeout(unsigned limit_us, kda_stream_t stream) {
+    t_last_error.clear();
+    KDA_REQUIRE(limit_us >= 1 && limit_us <= 2000000u, "limit_us=%u must be in [1, 2e6]",
+                limit_us);
+    unsigned* err = device_error_ptr();
+    if (err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
+    cudaError_t e = kda::launch_selftest_timeout((uint64_t)limit_us * 1000u, err,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kda_selftest_timeout launch");
+    return KDA_OK;
+}
+
 kda_status_t kda_device_status(kda_stream_t stream) {
     t_last_error.clear();
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -52,6 +52,9 @@ struct BwdArgs {
 size_t bwd_workspace_size_public(int64_t T_total, int N, int H, int dk, int dv);
 cudaError_t launch_bwd(const BwdArgs& a);
 
+// A bounded wait that runs out (selftest.cu): sets the timeout bit of the error word.
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, unsigned* err, cudaStream_t stream);
+
 // K1: elementwise gate.
 cudaError_t launch_gate(const void* z, int z_bf16, const float* A_log, float g_min, float* g_out,
                         int64_t n_tokens, int H, int dk, cudaStream_t stream);

@@ -74,6 +74,8 @@ def _load():
     lib.kda_bwd.restype = ctypes.c_int
     lib.kda_bwd.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, vp, i32, i64, i32, i32, i32, i32,
                             vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.kda_selftest_timeout.restype = ctypes.c_int
+    lib.kda_selftest_timeout.argtypes = [ctypes.c_uint, vp]
     lib.kda_device_status.restype = ctypes.c_int
     lib.kda_device_status.argtypes = [vp]
     lib.kda_profile_begin.restype = ctypes.c_int
@@ -424,6 +426,11 @@ def quantile_balance(scores, bias, k: int, want_bhat=False, want_alpha=False, wo
     if want_alpha:
         out.append(alpha)
     return out[0] if len(out) == 1 else tuple(out)
+
+
+def selftest_timeout(limit_us: int = 50000, stream=None):
+    """Enqueue a bounded wait that runs out (see kda_selftest_timeout in kda.h)."""
+    _check(_lib.kda_selftest_timeout(int(limit_us), _stream(stream)), "kda_selftest_timeout")
 
 
 def device_status(stream=None):
