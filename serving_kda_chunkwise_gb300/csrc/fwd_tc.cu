@@ -97,27 +97,7 @@ __device__ unsigned long long g_phase[32];
             for (int kda_i = 0; kda_i < 32; ++kda_i)                          \
                 if (kda_acc[kda_i]) atomicAdd(&g_phase[kda_i], kda_acc[kda_i]); \
     } while (0)
-// per-chunk event clocks of CTA 0 for chunks [100, 228), one slot per event
-__device__ long long g_trace[128][32];
-#define KDA_TRACE(t, slot)                                                  \
-    do {                                                                    \
-        if (blockIdx.x == 0 && (t) >= 100 && (t) < 228)                     \
-            g_trace[(t) - 100][(slot)] = clock64();                         \
-    } while (0)
-// per-warp event clocks of intra CTA 0, items [10, 26) of its sequence
-__device__ long long g_itrace[16][16][8];
-#define KDA_ITRACE(it, slot)                                                          \
-    do {                                                                              \
-        if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (it) >= 10 && (it) < 26)    \
-            g_itrace[(it) - 10][threadIdx.x >> 5][(slot)] = clock64();               \
-    } while (0)
 #else
-#define KDA_ITRACE(it, slot) \
-    do {                     \
-    } while (0)
-#define KDA_TRACE(t, slot) \
-    do {                   \
-    } while (0)
 #define KDA_PHASE_INIT() \
     do {                 \
     } while (0)
@@ -1236,30 +1216,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             // copies complete long before the handoffs: their waits go first, off the chain
             if (!mbar_wait_ab(&fullA[st], ph, p.err, abort)) break;
             if (t > 0 && !mbar_wait_ab(s_ready, (t - 1) & 1, p.err, abort)) break;
-            KDA_TRACE(t, 10);
             tc_fence_after();
-            KDA_TRACE(t, 11);
             issue_mma1(t);
-            KDA_TRACE(t, 12);
             if (t > 0) {
                 issue_mma3(t - 1, 2);
                 mma_commit(&mma3[(t - 1) & 1]);
             }
-            KDA_TRACE(t, 13);
             if (!mbar_wait_ab(&fullB[st], ph, p.err, abort)) break;
             if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
-            KDA_TRACE(t, 14);
             tc_fence_after();
-            KDA_TRACE(t, 15);
             constexpr uint32_t id2 = idesc_bf16(128, kJ, true, true);
             const uint64_t k0 = dKt + (st * kPkgPartB >> 4), v0 = dVt2 + (st * kVtStage >> 4);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tmem + kDS, k0 + ((ks * 2048) >> 4), v0 + ((ks * 1024) >> 4), id2, ks > 0);
             mma_commit(mma2);
-            KDA_TRACE(t, 16);
             issue_mma3(t, 0);
-            KDA_TRACE(t, 17);
         }
         if (t == nch) {
             issue_mma3(nch - 1, 2);
@@ -1304,15 +1276,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             if (t + 3 < nch) l2_prefetch(pkg0 + (size_t)(t + 3) * kPkgBytes, kPkgBytes);
             // E1(t) has read stage st of U, and MMA1(t) (which E1 waited for) of part A
             if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
-            KDA_TRACE(t, 18);
             issue_u(t + 2);
             issue_a(t + 2);
-            KDA_TRACE(t, 19);
             // MMA2(t) and MMA3(t) have read stage st of part B; E2(t) has read gamma
             if (!mbar_wait_ab(&mma3[st], ph, p.err, abort)) break;
-            KDA_TRACE(t, 20);
             issue_b(t + 2);
-            KDA_TRACE(t, 21);
         }
     }
 
@@ -1327,10 +1295,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             if (xwarp) {
                 if (!mbar_wait_ab(&ubar[st], ph, p.err, abort)) break;
                 if (!mbar_wait_ab(mma1, t & 1, p.err, abort)) break;
-                if (tid == 0) KDA_TRACE(t, 0);
                 KDA_PHASE(21);
                 tc_fence_after();
-                if (tid == 0) KDA_TRACE(t, 1);
                 KDA_PHASE(16);
                 // E1: Vt = U - X for row r = row, columns [16 wg, 16 wg + 16) of this quarter
                 const uint8_t* urow = sm + kUS + st * kPkgUQ + row * 128;
@@ -1338,7 +1304,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                 float x[16];
                 tmem_ld16(tmem + lane_base + d1 + 16 * wg, x);
                 tmem_ld_wait();
-                if (tid == 0) KDA_TRACE(t, 2);
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c4 = 4 * wg + 2 * cc;  // fp32 chunk of the 8 columns
@@ -1355,13 +1320,10 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                     *reinterpret_cast<uint4*>(vt + off) = hi;
                     *reinterpret_cast<uint4*>(vt + kVtLo + off) = lo;
                 }
-                if (tid == 0) KDA_TRACE(t, 23);
                 fence_async_smem();
-                if (tid == 0) KDA_TRACE(t, 24);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&vt_ready[st]);
-                if (tid == 0) KDA_TRACE(t, 3);
                 KDA_PHASE(17);
             }
             // The O warps meet on a named barrier below, so they leave the loop only together
@@ -1370,8 +1332,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                       mbar_wait_ab(mma2, t & 1, p.err, abort);
             if (xwarp && !ok) break;
             tc_fence_after();
-            if (tid == 0) KDA_TRACE(t, 4);
-            if (tid == 64) KDA_TRACE(t, 6);
             KDA_PHASE(18);
             // E2: S <- gamma^C * S + dS ;  bf16 copy of S for the next chunk's MMA1
             {
@@ -1387,14 +1347,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(s_ready);
-            if (tid == 0) KDA_TRACE(t, 5);
-            if (tid == 64) KDA_TRACE(t, 7);
             KDA_PHASE(19);
             if (owarp) {
                 // E3: O rows r = row - 64, columns [jc, jc + 32) -> o
                 ok = ok && mbar_wait_ab(&mma3[st], ph, p.err, abort);
                 tc_fence_after();
-                if (tid == 64) KDA_TRACE(t, 8);
                 const int r = row - 64;
                 float v[16];
                 tmem_ld16(tmem + lane_base + d1 + 16 * wg, v);
@@ -1431,7 +1388,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_co
                     }
                 }
                 tc_fence_before();
-                if (tid == 64) KDA_TRACE(t, 9);
             }
             KDA_PHASE(20);
         }
@@ -1502,14 +1458,6 @@ bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int box_
 }  // namespace
 
 #ifdef KDA_PHASE_TIMING
-extern "C" int kda_debug_itrace(long long* out, int n) {
-    if (n > 16 * 16 * 8) n = 16 * 16 * 8;
-    return cudaMemcpyFromSymbol(out, g_itrace, n * sizeof(long long)) == cudaSuccess ? n : -1;
-}
-extern "C" int kda_debug_trace(long long* out, int n) {
-    if (n > 128 * 32) n = 128 * 32;
-    return cudaMemcpyFromSymbol(out, g_trace, n * sizeof(long long)) == cudaSuccess ? n : -1;
-}
 extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
     if (n > 32) n = 32;
     if (cudaMemcpyFromSymbol(out, g_phase, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
