@@ -8,7 +8,12 @@
  *         o_t = S_t^T q_t                      (S is d_k x d_v, no scale on q)
  *     section "Chunkwise parallel form" -- the same result computed chunk by chunk
  *         (chunk length 64, 16-token sub-tiles) and the lower-bounded gate
- *         g_t = g_min * Sigmoid(e^{A_h} z_t)  in (g_min, 0),   alpha_t = exp(g_t).
+ *         g_t = g_min * Sigmoid(e^{A_h} z_t)  in (g_min, 0),   alpha_t = exp(g_t),
+ *         which replaces g_t = -e^{A_h} Softplus(z_t)  (kda_fwd_chunked_softplus);
+ *     section "Gated MLA" -- the layer output W_o [Sigmoid(W_g x_t) (.) RMSNorm(o~_t)]
+ *         (kda_output_norm_gate, kda_decode_step_gated: the part between W_g and W_o);
+ *     load-balancing section "Quantile Balancing (QB)" -- the expert-bias update
+ *         (kda_quantile_balance).
  *   [guide] "A Look at Kimi K3: Three Core Innovations and Engineering Tuning Guide",
  *     section 2.2 -- the same gate (per head A_h, per channel z), g_min in [-6, -3];
  *     section 4.2 -- quantile-based expert thresholds.

@@ -91,7 +91,7 @@ kda_status_t set_last_error(kda_status_t s, const char* msg) {
 
 extern "C" {
 
-int kda_version(void) { return 100; /* 0.1.0 */ }
+int kda_version(void) { return 200; /* 0.2.0: backward, softplus variant, output step, quantile balancing */ }
 
 const char* kda_status_string(kda_status_t s) {
     switch (s) {
