@@ -87,3 +87,9 @@ def test_deterministic(kda):
     g2 = _run(kda, [150, 33], H=2, d=128, dtype="bf16", seed=73)
     for nm in g1:
         assert torch.equal(g1[nm], g2[nm]), nm
+
+
+def test_long_sequences(kda):
+    """Sequences of 2100 and 1000 tokens (33 and 16 chunks, ragged tails): the checkpoints and
+    the per-chunk recompute over many chunks."""
+    _run(kda, [2100, 1000], H=2, d=128, dtype="bf16", seed=74)

@@ -62,3 +62,16 @@ def test_no_decay_and_no_writes_holds_state(kda):
     assert np.array_equal(S, inp.S0)
     ref = np.einsum("thc,hcj->thj", inp.q.values.astype(np.float64), inp.S0[0].astype(np.float64))
     np.testing.assert_allclose(o, ref, rtol=1e-5, atol=1e-7)
+
+
+def test_full_size_sampled(kda):
+    """The benchmark's comparison shape (T = 65536, H = 32, d = 128, bf16): heads 0 and 17
+    against the token recurrence."""
+    sp = inputs.workload_spec("fwd_bf16_T65536_H32_d128")
+    d = sp.to_device("cuda")
+    o, S = kda.fwd_chunked_softplus(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], N=1)
+    kda.device_status()
+    o = o.float().cpu().numpy()
+    S = S.cpu().numpy()
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    check_forward(sp, o, S, oracle_forward(sp, heads=[0, 17], gate="softplus"))
