@@ -11,16 +11,26 @@
 //   dz = dx e^{A_h};   dA_h += sum dx x.
 // The pages print no backward; these are the derivatives of the forward they define.
 //
-// This is the token-level form on CUDA cores in fp32 (a first backward: serial over tokens,
-// latency-bound; the chunked tensor-core backward is not built).  One CTA of 512 threads per
-// (sequence, head): warp w owns rows [w dk/16, (w+1) dk/16) of the d_k x d_v state and lane
-// l owns columns l, l + 32, ..; S and dS live in registers.
-//   bwd_ckpt_kernel   the forward, storing S at the start of every 64-token chunk
-//   bwd_kernel        per chunk, last to first: re-run the chunk's forward from its checkpoint
-//                     storing the state before every token (scratch), then step back through
-//                     the tokens with the rules above
-//   bwd_dA_kernel     dA_log[h] = the per-(sequence, head) partial sums, added in sequence
-//                     order (deterministic)
+// On CUDA cores in fp32, parallel over chunks.  The gradient of the state is the only serial
+// quantity, and over one 64-token chunk it is affine: going back through token t maps
+// dS_t to B_t (dS_t + q_t do_t^T) with B_t = Diag(alpha_t) (I - beta_t k_t k_t^T), so
+//   dS_(chunk start) = Phi dS_(chunk end) + Psi,  Phi = B_t0 .. B_t1-1,
+//   Psi = sum_t B_t0 .. B_t (q_t do_t^T).
+// Kernels (512 threads; warp w owns rows [w dk/16, (w+1) dk/16) of a state-shaped matrix and
+// lane l its columns l, l + 32, ..; matrices live in registers):
+//   bwd_plan_kernel   chunk offsets of every sequence and a table entry per chunk
+//   bwd_fwdtrans_kernel  per (chunk, head), all in parallel: the chunk's forward map on the
+//                     state, S_end = A S_start + B
+//   bwd_chain_kernel<fwd>  per (sequence, head): S at every chunk start (S <- A S + B, first
+//                     chunk first), the checkpoints
+//   bwd_phi_kernel    per (chunk, head), all in parallel: Phi and Psi of the chunk
+//   bwd_chain_kernel  per (sequence, head): dS at every chunk end, last chunk first
+//                     (dS <- Phi dS + Psi, a 128 x 128 x 128 product per chunk), and dS0
+//   bwd_item_kernel   per (chunk, head), all in parallel: the chunk's forward from its
+//                     checkpoint (the state before every token kept in per-CTA scratch), then
+//                     the reverse rules above token by token from the chunk's dS
+//   bwd_dA_kernel     dA_log[h] = the per-(chunk, head) partial sums in chunk order
+//                     (deterministic)
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -31,9 +41,6 @@ constexpr int kBwdThreads = 512;
 constexpr int kBwdWarps = kBwdThreads / 32;
 constexpr int kBwdC = 64;
 
-// checkpoint slot of the chunk that starts at token t0 of sequence n (injective: see the
-// workspace description in bwd_workspace_size)
-__device__ __forceinline__ int64_t ckpt_slot(int64_t t0, int n) { return t0 / kBwdC + n; }
 
 template <int DK, int DV>
 struct BwdLayout {
@@ -120,53 +127,310 @@ struct BwdParams {
     int64_t T_total;
     void *dq, *dk, *dv, *dbeta, *dz;
     float* dS0;
-    float* ckpt;       // [slots][H][DK][DV]
-    float* snap;       // [grid][64][DK][DV]
-    float* dA_part;    // [N][H]
+    int32_t* chunk_off;  // [N + 1]: first global chunk of each sequence, then the total
+    int4* chunk_tab;     // [chunks]: {first token (low, high), sequence, rows}
+    float* ckpt;         // [chunks][H][DK][DV]: the state at each chunk start
+    float* phi;          // [chunks][H][DK][DK]
+    float* psi;          // [chunks][H][DK][DV]
+    float* dsend;        // [chunks][H][DK][DV]: the state's gradient at each chunk end
+    float* snap;         // [grid][64][DK][DV]: per-CTA scratch
+    float* dA_item;      // [chunks][H]
     unsigned* err;
 };
 
-template <typename IO, int DK, int DV>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_ckpt_kernel(const BwdParams p) {
-    using L = BwdLayout<DK, DV>;
-    __shared__ TokVec<DK, DV> tv;
-    __shared__ float part[kBwdWarps][DV];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int nh = blockIdx.x; nh < p.N * p.H; nh += gridDim.x) {
-        const int h = nh % p.H, n = nh / p.H;
-        int64_t tb, te;
-        seq_range(p.cu, n, p.N, p.T_total, p.err, tb, te);
-        const float scale = expf(p.A_log[h]);
-        float S[L::RPW][L::CPL];
-#pragma unroll
-        for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-            for (int c = 0; c < L::CPL; ++c)
-                S[r][c] = p.S0 ? p.S0[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c]
-                               : 0.f;
-        for (int64_t t = tb; t < te; ++t) {
-            if ((t - tb) % kBwdC == 0) {  // the state before this chunk
-                float* dst = p.ckpt + ((size_t)ckpt_slot(t, n) * p.H + h) * DK * DV;
-#pragma unroll
-                for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-                    for (int c = 0; c < L::CPL; ++c)
-                        dst[(warp * L::RPW + r) * DV + lane + 32 * c] = S[r][c];
-            }
-            __syncthreads();  // the previous token's vectors are no longer read
-            load_token<IO, DK, DV>(tv, static_cast<const IO*>(p.q), static_cast<const IO*>(p.k),
-                                   static_cast<const IO*>(p.v), static_cast<const IO*>(p.beta),
-                                   static_cast<const IO*>(p.z), nullptr, t, p.H, h, scale,
-                                   p.g_min, tid);
-            __syncthreads();
-            fwd_token<DK, DV>(S, tv, part, warp, lane, tid);
+// chunk offsets (serial scan by one thread: N is small next to the work) and the chunk table
+__global__ void __launch_bounds__(1024) bwd_plan_kernel(const int32_t* __restrict__ cu, int N,
+                                                        int64_t T_total, int32_t* chunk_off,
+                                                        int4* chunk_tab, unsigned* err) {
+    if (threadIdx.x == 0) {
+        int32_t acc = 0;
+        for (int n = 0; n < N; ++n) {
+            int64_t b, e;
+            seq_range(cu, n, N, T_total, err, b, e);
+            chunk_off[n] = acc;
+            acc += (int32_t)((e - b + kBwdC - 1) / kBwdC);
         }
-        __syncthreads();
+        chunk_off[N] = acc;
+    }
+    __syncthreads();
+    const int32_t total = chunk_off[N];
+    for (int32_t c = threadIdx.x; c < total; c += blockDim.x) {
+        int lo = 0, hi = N - 1;  // the last sequence whose first chunk is <= c
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (chunk_off[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        int64_t b, e;
+        seq_range(cu, lo, N, T_total, nullptr, b, e);
+        const int64_t t0 = b + (int64_t)(c - chunk_off[lo]) * kBwdC;
+        const int64_t rows = e - t0 < kBwdC ? e - t0 : kBwdC;
+        chunk_tab[c] = make_int4((int)(t0 & 0xffffffff), (int)(t0 >> 32), lo, (int)rows);
     }
 }
 
 template <typename IO, int DK, int DV>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams p) {
+    using L = BwdLayout<DK, DV>;
+    constexpr int CK = DK / 32;  // Phi columns per lane
+    __shared__ TokVec<DK, DV> tv;
+    __shared__ float partA[kBwdWarps][DK];
+    __shared__ float partB[kBwdWarps][DV];
+    __shared__ float duA[DK];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const IO* q = static_cast<const IO*>(p.q);
+    const IO* k = static_cast<const IO*>(p.k);
+    const IO* v = static_cast<const IO*>(p.v);
+    const IO* beta = static_cast<const IO*>(p.beta);
+    const IO* z = static_cast<const IO*>(p.z);
+    const IO* dout = static_cast<const IO*>(p.dout);
+    const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int h = (int)(it % p.H);
+        const int4 e = p.chunk_tab[it / p.H];
+        const int64_t t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
+        const int64_t t1 = t0 + e.w;
+        const float scale = expf(p.A_log[h]);
+        float Phi[L::RPW][CK], Psi[L::RPW][L::CPL];
+#pragma unroll
+        for (int r = 0; r < L::RPW; ++r) {
+#pragma unroll
+            for (int c = 0; c < CK; ++c) Phi[r][c] = (warp * L::RPW + r == lane + 32 * c) ? 1.f : 0.f;
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) Psi[r][c] = 0.f;
+        }
+        for (int64_t t = t1 - 1; t >= t0; --t) {
+            __syncthreads();  // the previous token's vectors and sums are consumed
+            load_token<IO, DK, DV>(tv, q, k, v, beta, z, dout, t, p.H, h, scale, p.g_min, tid);
+            __syncthreads();
+            // Psi += q do^T; column sums of Phi^T k and Psi^T k
+            float pa[CK], pb[L::CPL];
+#pragma unroll
+            for (int c = 0; c < CK; ++c) pa[c] = 0.f;
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) pb[c] = 0.f;
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const int i = warp * L::RPW + r;
+                const float kk = tv.k[i], qq = tv.q[i];
+#pragma unroll
+                for (int c = 0; c < CK; ++c) pa[c] = fmaf(Phi[r][c], kk, pa[c]);
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    Psi[r][c] = fmaf(qq, tv.dout[lane + 32 * c], Psi[r][c]);
+                    pb[c] = fmaf(Psi[r][c], kk, pb[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < CK; ++c) partA[warp][lane + 32 * c] = pa[c];
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) partB[warp][lane + 32 * c] = pb[c];
+            __syncthreads();
+            if (tid < DK) {
+                float sa = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sa += partA[w2][tid];
+                duA[tid] = sa;
+            } else if (tid >= 256 && tid < 256 + DV) {
+                float sb = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sb += partB[w2][tid - 256];
+                tv.du[tid - 256] = sb;
+            }
+            __syncthreads();
+            // X <- Diag(alpha) (X - beta k du^T) for X = Phi and Psi
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const int i = warp * L::RPW + r;
+                const float a = tv.alpha[i], bk = tv.beta * tv.k[i];
+#pragma unroll
+                for (int c = 0; c < CK; ++c) Phi[r][c] = a * fmaf(-bk, duA[lane + 32 * c], Phi[r][c]);
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c)
+                    Psi[r][c] = a * fmaf(-bk, tv.du[lane + 32 * c], Psi[r][c]);
+            }
+        }
+        float* ph = p.phi + (size_t)it * DK * DK;
+        float* ps = p.psi + (size_t)it * DK * DV;
+#pragma unroll
+        for (int r = 0; r < L::RPW; ++r) {
+            const int i = warp * L::RPW + r;
+#pragma unroll
+            for (int c = 0; c < CK; ++c) ph[i * DK + lane + 32 * c] = Phi[r][c];
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) ps[i * DV + lane + 32 * c] = Psi[r][c];
+        }
+    }
+}
+
+// The forward map of one chunk on the state, S_end = A S_start + B, for every (chunk, head) in
+// parallel: A and B follow the token recurrence from A = I, B = 0 (per token X <- Diag(alpha)X,
+// then X <- X - beta k (k^T X)^T, and for B also + beta k v^T).  Stored in the Phi / Psi
+// buffers, which the backward stages reuse afterwards.
+template <typename IO, int DK, int DV>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdParams p) {
+    using L = BwdLayout<DK, DV>;
+    constexpr int CK = DK / 32;
+    __shared__ TokVec<DK, DV> tv;
+    __shared__ float partA[kBwdWarps][DK];
+    __shared__ float partB[kBwdWarps][DV];
+    __shared__ float wA[DK];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const IO* q = static_cast<const IO*>(p.q);
+    const IO* k = static_cast<const IO*>(p.k);
+    const IO* v = static_cast<const IO*>(p.v);
+    const IO* beta = static_cast<const IO*>(p.beta);
+    const IO* z = static_cast<const IO*>(p.z);
+    const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int h = (int)(it % p.H);
+        const int4 e = p.chunk_tab[it / p.H];
+        const int64_t t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
+        const int64_t t1 = t0 + e.w;
+        const float scale = expf(p.A_log[h]);
+        float A[L::RPW][CK], B[L::RPW][L::CPL];
+#pragma unroll
+        for (int r = 0; r < L::RPW; ++r) {
+#pragma unroll
+            for (int c = 0; c < CK; ++c) A[r][c] = (warp * L::RPW + r == lane + 32 * c) ? 1.f : 0.f;
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) B[r][c] = 0.f;
+        }
+        for (int64_t t = t0; t < t1; ++t) {
+            __syncthreads();
+            load_token<IO, DK, DV>(tv, q, k, v, beta, z, nullptr, t, p.H, h, scale, p.g_min, tid);
+            __syncthreads();
+            float pa[CK], pb[L::CPL];
+#pragma unroll
+            for (int c = 0; c < CK; ++c) pa[c] = 0.f;
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) pb[c] = 0.f;
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const int i = warp * L::RPW + r;
+                const float a = tv.alpha[i], kk = tv.k[i];
+#pragma unroll
+                for (int c = 0; c < CK; ++c) {
+                    A[r][c] *= a;
+                    pa[c] = fmaf(A[r][c], kk, pa[c]);
+                }
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    B[r][c] *= a;
+                    pb[c] = fmaf(B[r][c], kk, pb[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < CK; ++c) partA[warp][lane + 32 * c] = pa[c];
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) partB[warp][lane + 32 * c] = pb[c];
+            __syncthreads();
+            if (tid < DK) {
+                float sa = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sa += partA[w2][tid];
+                wA[tid] = sa;
+            } else if (tid >= 256 && tid < 256 + DV) {
+                float sb = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sb += partB[w2][tid - 256];
+                tv.w[tid - 256] = sb - tv.v[tid - 256];  // (k^T B') - v
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const float bk = tv.beta * tv.k[warp * L::RPW + r];
+#pragma unroll
+                for (int c = 0; c < CK; ++c) A[r][c] = fmaf(-bk, wA[lane + 32 * c], A[r][c]);
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) B[r][c] = fmaf(-bk, tv.w[lane + 32 * c], B[r][c]);
+            }
+        }
+        float* pa_out = p.phi + (size_t)it * DK * DK;
+        float* pb_out = p.psi + (size_t)it * DK * DV;
+#pragma unroll
+        for (int r = 0; r < L::RPW; ++r) {
+            const int i = warp * L::RPW + r;
+#pragma unroll
+            for (int c = 0; c < CK; ++c) pa_out[i * DK + lane + 32 * c] = A[r][c];
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) pb_out[i * DV + lane + 32 * c] = B[r][c];
+        }
+    }
+}
+
+// Dynamic shared memory of the chain kernel: dS (the right operand of Phi dS) and Phi, the
+// latter loaded by the whole CTA in one coalesced pass per chunk.
+// kFwd: the states at the chunk starts (S <- A S + B, first chunk first, each start stored
+// in the checkpoints); otherwise the state's gradient at the chunk ends (dS <- Phi dS + Psi,
+// last chunk first, each end stored) and finally dS0.
+template <int DK, int DV, bool kFwd>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const BwdParams p) {
+    using L = BwdLayout<DK, DV>;
+    extern __shared__ __align__(16) float chain_smem[];
+    float* dss = chain_smem;            // [DK][DV]
+    float* phs = chain_smem + DK * DV;  // [DK][DK]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int nh = blockIdx.x; nh < p.N * p.H; nh += gridDim.x) {
+        const int h = nh % p.H, n = nh / p.H;
+        const float* init = kFwd ? p.S0 : p.dS_out;
+        float dS[L::RPW][L::CPL];  // the carried matrix (S forward, dS backward)
+#pragma unroll
+        for (int r = 0; r < L::RPW; ++r)
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c)
+                dS[r][c] = init ? init[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c]
+                                : 0.f;
+        const int32_t g0 = p.chunk_off[n], g1 = p.chunk_off[n + 1];
+        for (int32_t step = 0; step < g1 - g0; ++step) {
+            const int32_t g = kFwd ? g0 + step : g1 - 1 - step;
+            const size_t it = (size_t)g * p.H + h;
+            float* de = (kFwd ? p.ckpt : p.dsend) + it * DK * DV;
+            const float4* ph4 = reinterpret_cast<const float4*>(p.phi + it * DK * DK);
+            const float* ps = p.psi + it * DK * DV;
+            for (int i4 = tid; i4 < DK * DK / 4; i4 += kBwdThreads)
+                reinterpret_cast<float4*>(phs)[i4] = __ldg(ph4 + i4);
+            float acc[L::RPW][L::CPL];
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r)
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    const int i = warp * L::RPW + r, j = lane + 32 * c;
+                    de[i * DV + j] = dS[r][c];
+                    dss[i * DV + j] = dS[r][c];
+                    acc[r][c] = ps[i * DV + j];
+                }
+            __syncthreads();
+            // dS <- Phi dS + Psi
+            for (int l = 0; l < DK; ++l) {
+                float dl[L::CPL];
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) dl[c] = dss[l * DV + lane + 32 * c];
+#pragma unroll
+                for (int r = 0; r < L::RPW; ++r) {
+                    const float f = phs[(warp * L::RPW + r) * DK + l];
+#pragma unroll
+                    for (int c = 0; c < L::CPL; ++c) acc[r][c] = fmaf(f, dl[c], acc[r][c]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r)
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) dS[r][c] = acc[r][c];
+            __syncthreads();  // dss and phs are rewritten for the next chunk
+        }
+        if (!kFwd && p.dS0) {
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r)
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c)
+                    p.dS0[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c] = dS[r][c];
+        }
+    }
+}
+
+template <typename IO, int DK, int DV>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
     __shared__ TokVec<DK, DV> tv;
     __shared__ float part[kBwdWarps][DV];
@@ -181,253 +445,292 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const BwdParams p) 
     const IO* beta = static_cast<const IO*>(p.beta);
     const IO* z = static_cast<const IO*>(p.z);
     const IO* dout = static_cast<const IO*>(p.dout);
-    for (int nh = blockIdx.x; nh < p.N * p.H; nh += gridDim.x) {
-        const int h = nh % p.H, n = nh / p.H;
-        int64_t tb, te;
-        seq_range(p.cu, n, p.N, p.T_total, p.err, tb, te);
+    const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int h = (int)(it % p.H);
+        const int4 e = p.chunk_tab[it / p.H];
+        const int64_t t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
+        const int64_t t1 = t0 + e.w;
         const float scale = expf(p.A_log[h]);
         float dA_acc = 0.f;
-        float dS[L::RPW][L::CPL];
+        float dS[L::RPW][L::CPL];  // the state's gradient at the chunk end
+        const float* de = p.dsend + (size_t)it * DK * DV;
 #pragma unroll
         for (int r = 0; r < L::RPW; ++r)
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c)
-                dS[r][c] = p.dS_out
-                               ? p.dS_out[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c]
-                               : 0.f;
-        const int64_t nchunks = (te - tb + kBwdC - 1) / kBwdC;
-        for (int64_t ci = nchunks - 1; ci >= 0; --ci) {
-            const int64_t t0 = tb + ci * kBwdC;
-            const int64_t t1 = (t0 + kBwdC < te) ? t0 + kBwdC : te;
-            // ---- the chunk's forward from its checkpoint, keeping the state before each token
-            float S[L::RPW][L::CPL];
-            const float* src = p.ckpt + ((size_t)ckpt_slot(t0, n) * p.H + h) * DK * DV;
+                dS[r][c] = de[(warp * L::RPW + r) * DV + lane + 32 * c];
+        // ---- the chunk's forward from its checkpoint, keeping the state before each token
+        float S[L::RPW][L::CPL];
+        const float* src = p.ckpt + (size_t)it * DK * DV;
+#pragma unroll
+        for (int r = 0; r < L::RPW; ++r)
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c)
+                S[r][c] = src[(warp * L::RPW + r) * DV + lane + 32 * c];
+        for (int64_t t = t0; t < t1; ++t) {
+            float* dst = snap + (size_t)(t - t0) * DK * DV;
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r)
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c)
-                    S[r][c] = src[(warp * L::RPW + r) * DV + lane + 32 * c];
-            for (int64_t t = t0; t < t1; ++t) {
-                float* dst = snap + (size_t)(t - t0) * DK * DV;
+                    dst[(warp * L::RPW + r) * DV + lane + 32 * c] = S[r][c];
+            __syncthreads();
+            load_token<IO, DK, DV>(tv, q, k, v, beta, z, nullptr, t, p.H, h, scale, p.g_min,
+                                   tid);
+            __syncthreads();
+            if (t + 1 < t1) fwd_token<DK, DV>(S, tv, part, warp, lane, tid);
+        }
+        // ---- back through the chunk's tokens
+        for (int64_t t = t1 - 1; t >= t0; --t) {
+            __syncthreads();  // previous token's vectors and partial sums are consumed
+            load_token<IO, DK, DV>(tv, q, k, v, beta, z, dout, t, p.H, h, scale, p.g_min,
+                                   tid);
+            float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
+            const float* ps = snap + (size_t)(t - t0) * DK * DV;
 #pragma unroll
-                for (int r = 0; r < L::RPW; ++r)
+            for (int r = 0; r < L::RPW; ++r)
 #pragma unroll
-                    for (int c = 0; c < L::CPL; ++c)
-                        dst[(warp * L::RPW + r) * DV + lane + 32 * c] = S[r][c];
-                __syncthreads();
-                load_token<IO, DK, DV>(tv, q, k, v, beta, z, nullptr, t, p.H, h, scale, p.g_min,
-                                       tid);
-                __syncthreads();
-                if (t + 1 < t1) fwd_token<DK, DV>(S, tv, part, warp, lane, tid);
-            }
-            // ---- back through the chunk's tokens
-            for (int64_t t = t1 - 1; t >= t0; --t) {
-                __syncthreads();  // previous token's vectors and partial sums are consumed
-                load_token<IO, DK, DV>(tv, q, k, v, beta, z, dout, t, p.H, h, scale, p.g_min,
-                                       tid);
-                float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
-                const float* ps = snap + (size_t)(t - t0) * DK * DV;
+                for (int c = 0; c < L::CPL; ++c)
+                    P[r][c] = ps[(warp * L::RPW + r) * DV + lane + 32 * c];
+            __syncthreads();
+            // B1: S' = alpha P; column sums of S' k (for w) and of (dS + q do^T) k (for du)
+            float pw[L::CPL], pdu[L::CPL];
 #pragma unroll
-                for (int r = 0; r < L::RPW; ++r)
+            for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
 #pragma unroll
-                    for (int c = 0; c < L::CPL; ++c)
-                        P[r][c] = ps[(warp * L::RPW + r) * DV + lane + 32 * c];
-                __syncthreads();
-                // B1: S' = alpha P; column sums of S' k (for w) and of (dS + q do^T) k (for du)
-                float pw[L::CPL], pdu[L::CPL];
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
-#pragma unroll
-                for (int r = 0; r < L::RPW; ++r) {
-                    const int i = warp * L::RPW + r;
-                    const float a = tv.alpha[i], kk = tv.k[i], qq = tv.q[i];
-#pragma unroll
-                    for (int c = 0; c < L::CPL; ++c) {
-                        const int j = lane + 32 * c;
-                        dS[r][c] = fmaf(qq, tv.dout[j], dS[r][c]);
-                        pw[c] = fmaf(a * P[r][c], kk, pw[c]);
-                        pdu[c] = fmaf(dS[r][c], kk, pdu[c]);
-                    }
-                }
+            for (int r = 0; r < L::RPW; ++r) {
+                const int i = warp * L::RPW + r;
+                const float a = tv.alpha[i], kk = tv.k[i], qq = tv.q[i];
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
-                    part[warp][lane + 32 * c] = pw[c];
-                    part2[warp][lane + 32 * c] = pdu[c];
-                }
-                __syncthreads();
-                // B2: w, u, du per column; dv and the dbeta partial
-                float wdu = 0.f;
-                if (tid < DV) {
-                    float s = 0.f, d = 0.f;
-#pragma unroll
-                    for (int w2 = 0; w2 < kBwdWarps; ++w2) {
-                        s += part[w2][tid];
-                        d += part2[w2][tid];
-                    }
-                    const float wj = tv.v[tid] - s;
-                    tv.w[tid] = wj;
-                    tv.u[tid] = tv.beta * wj;
-                    tv.du[tid] = d;
-                    wdu = d * wj;
-                    const size_t vo = ((size_t)t * p.H + h) * DV + tid;
-                    static_cast<IO*>(p.dv)[vo] = from_f32<IO>(tv.beta * d);
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
-                if (lane == 0) red[warp] = wdu;
-                __syncthreads();
-                if (tid == 0) {
-                    float b = 0.f;
-#pragma unroll
-                    for (int w2 = 0; w2 < DV / 32; ++w2) b += red[w2];
-                    static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(b);
-                }
-                // B3: per element; row sums of S_t do (dq), dS u - S' beta du (dk), dS' P (dalpha)
-#pragma unroll
-                for (int r = 0; r < L::RPW; ++r) {
-                    const int i = warp * L::RPW + r;
-                    const float a = tv.alpha[i], kk = tv.k[i];
-                    float sq = 0.f, sk = 0.f, sa = 0.f;
-#pragma unroll
-                    for (int c = 0; c < L::CPL; ++c) {
-                        const int j = lane + 32 * c;
-                        const float sp = a * P[r][c];
-                        const float bdu = tv.beta * tv.du[j];
-                        sq = fmaf(sp + kk * tv.u[j], tv.dout[j], sq);
-                        sk = fmaf(dS[r][c], tv.u[j], sk);
-                        sk = fmaf(-sp, bdu, sk);
-                        const float dsp = fmaf(-kk, bdu, dS[r][c]);
-                        sa = fmaf(dsp, P[r][c], sa);
-                        dS[r][c] = a * dsp;
-                    }
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                        sk += __shfl_xor_sync(0xffffffffu, sk, off);
-                        sa += __shfl_xor_sync(0xffffffffu, sa, off);
-                    }
-                    if (lane == 0) {
-                        rowv[0][i] = sq;
-                        rowv[1][i] = sk;
-                        rowv[2][i] = sa;
-                    }
-                }
-                __syncthreads();
-                // B4: per key channel: dq, dk, dz and the dA_log partial
-                if (tid < DK) {
-                    const size_t ko = ((size_t)t * p.H + h) * DK + tid;
-                    const float x = tv.x[tid];
-                    const float s = 1.0f / (1.0f + expf(-x));
-                    const float dx = rowv[2][tid] * tv.alpha[tid] * p.g_min * s * (1.0f - s);
-                    static_cast<IO*>(p.dq)[ko] = from_f32<IO>(rowv[0][tid]);
-                    static_cast<IO*>(p.dk)[ko] = from_f32<IO>(rowv[1][tid]);
-                    static_cast<IO*>(p.dz)[ko] = from_f32<IO>(dx * scale);
-                    dA_acc = fmaf(dx, x, dA_acc);
+                    const int j = lane + 32 * c;
+                    dS[r][c] = fmaf(qq, tv.dout[j], dS[r][c]);
+                    pw[c] = fmaf(a * P[r][c], kk, pw[c]);
+                    pdu[c] = fmaf(dS[r][c], kk, pdu[c]);
                 }
             }
-        }
-        // dS0 and this (sequence, head)'s dA_log partial
-        if (p.dS0) {
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r)
+            for (int c = 0; c < L::CPL; ++c) {
+                part[warp][lane + 32 * c] = pw[c];
+                part2[warp][lane + 32 * c] = pdu[c];
+            }
+            __syncthreads();
+            // B2: w, u, du per column; dv and the dbeta partial
+            float wdu = 0.f;
+            if (tid < DV) {
+                float s = 0.f, d = 0.f;
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c)
-                    p.dS0[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c] = dS[r][c];
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) {
+                    s += part[w2][tid];
+                    d += part2[w2][tid];
+                }
+                const float wj = tv.v[tid] - s;
+                tv.w[tid] = wj;
+                tv.u[tid] = tv.beta * wj;
+                tv.du[tid] = d;
+                wdu = d * wj;
+                const size_t vo = ((size_t)t * p.H + h) * DV + tid;
+                static_cast<IO*>(p.dv)[vo] = from_f32<IO>(tv.beta * d);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
+            if (lane == 0) red[warp] = wdu;
+            __syncthreads();
+            if (tid == 0) {
+                float b = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < DV / 32; ++w2) b += red[w2];
+                static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(b);
+            }
+            // B3: per element; row sums of S_t do (dq), dS u - S' beta du (dk), dS' P (dalpha)
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const int i = warp * L::RPW + r;
+                const float a = tv.alpha[i], kk = tv.k[i];
+                float sq = 0.f, sk = 0.f, sa = 0.f;
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    const int j = lane + 32 * c;
+                    const float sp = a * P[r][c];
+                    const float bdu = tv.beta * tv.du[j];
+                    sq = fmaf(sp + kk * tv.u[j], tv.dout[j], sq);
+                    sk = fmaf(dS[r][c], tv.u[j], sk);
+                    sk = fmaf(-sp, bdu, sk);
+                    const float dsp = fmaf(-kk, bdu, dS[r][c]);
+                    sa = fmaf(dsp, P[r][c], sa);
+                    dS[r][c] = a * dsp;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
+                    sa += __shfl_xor_sync(0xffffffffu, sa, off);
+                }
+                if (lane == 0) {
+                    rowv[0][i] = sq;
+                    rowv[1][i] = sk;
+                    rowv[2][i] = sa;
+                }
+            }
+            __syncthreads();
+            // B4: per key channel: dq, dk, dz and the dA_log partial
+            if (tid < DK) {
+                const size_t ko = ((size_t)t * p.H + h) * DK + tid;
+                const float x = tv.x[tid];
+                const float s = 1.0f / (1.0f + expf(-x));
+                const float dx = rowv[2][tid] * tv.alpha[tid] * p.g_min * s * (1.0f - s);
+                static_cast<IO*>(p.dq)[ko] = from_f32<IO>(rowv[0][tid]);
+                static_cast<IO*>(p.dk)[ko] = from_f32<IO>(rowv[1][tid]);
+                static_cast<IO*>(p.dz)[ko] = from_f32<IO>(dx * scale);
+                dA_acc = fmaf(dx, x, dA_acc);
+            }
         }
+        // this (chunk, head)'s dA_log partial
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, off);
         __syncthreads();
         if (lane == 0) red[warp] = dA_acc;
         __syncthreads();
         if (tid == 0) {
-            float s = 0.f;
+            float s2 = 0.f;
 #pragma unroll
-            for (int w2 = 0; w2 < DK / 32; ++w2) s += red[w2];
-            p.dA_part[nh] = s;
+            for (int w2 = 0; w2 < DK / 32; ++w2) s2 += red[w2];
+            p.dA_item[it] = s2;
         }
         __syncthreads();
     }
 }
 
-__global__ void bwd_dA_kernel(const float* __restrict__ part, int N, int H,
-                              float* __restrict__ dA_log) {
+__global__ void bwd_dA_kernel(const float* __restrict__ part, const int32_t* __restrict__ chunk_off,
+                              int N, int H, float* __restrict__ dA_log) {
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H) return;
+    const int32_t nc = chunk_off[N];
     float s = 0.f;
-    for (int n = 0; n < N; ++n) s += part[(size_t)n * H + h];
+    for (int32_t g = 0; g < nc; ++g) s += part[(size_t)g * H + h];
     dA_log[h] = s;
 }
 
 template <typename IO, int DK, int DV>
-cudaError_t launch_t(const BwdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream_t stream) {
+    constexpr int chain_smem = (DK * DV + DK * DK) * 4;
+    cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    if (e != cudaSuccess) return e;
     {
-        ProfScope prof("bwd_ckpt_kernel", stream);
-        bwd_ckpt_kernel<IO, DK, DV><<<grid, kBwdThreads, 0, stream>>>(p);
+        ProfScope prof("bwd_fwdtrans_kernel", stream);
+        bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, 0, stream>>>(p);
     }
     {
-        ProfScope prof("bwd_kernel", stream);
-        bwd_kernel<IO, DK, DV><<<grid, kBwdThreads, 0, stream>>>(p);
+        ProfScope prof("bwd_fchain_kernel", stream);
+        bwd_chain_kernel<DK, DV, true><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
+    }
+    {
+        ProfScope prof("bwd_phi_kernel", stream);
+        bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, 0, stream>>>(p);
+    }
+    {
+        ProfScope prof("bwd_chain_kernel", stream);
+        bwd_chain_kernel<DK, DV, false><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
+    }
+    {
+        ProfScope prof("bwd_item_kernel", stream);
+        bwd_item_kernel<IO, DK, DV><<<grid_items, kBwdThreads, 0, stream>>>(p);
     }
     return cudaGetLastError();
 }
 
-int bwd_grid(int N, int H) {
+int sm_count() {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t units = (int64_t)N * H;
-    const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 2;
-    return (int)(units < cap ? units : cap);
+    return sms > 0 ? sms : 1;
 }
 
 }  // namespace
 
-// Workspace: checkpoint slots floor(t0 / 64) + n over every chunk start t0 of sequence n --
-// distinct for distinct chunks (a sequence's chunks advance the first term by one each, and
-// the next sequence starts at least one slot further on), fewer than T/64 + N + 1 -- each
-// d_k x d_v fp32 per head; 64 states of scratch per CTA; N x H dA_log partials.
-size_t bwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv, int grid) {
+// Workspace, for at most C = T/64 + N chunks: chunk offsets [N + 1] and table [C]; the state
+// at each chunk start, Psi and the state's gradient at each chunk end [C][H][dk][dv] fp32;
+// Phi [C][H][dk][dk] fp32; 64 states of scratch per CTA of the per-chunk kernel; [C][H]
+// dA_log partials.
+struct BwdLayoutWs {
+    size_t off, tab, ckpt, phi, psi, dsend, snap, dA, total;
+};
+
+BwdLayoutWs bwd_ws_layout(int64_t T_total, int N, int H, int dk, int dv, int grid_items) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t slots = (size_t)(T_total / kBwdC + N + 1);
-    return al(slots * H * dk * dv * 4) + al((size_t)grid * kBwdC * dk * dv * 4) +
-           al((size_t)N * H * 4);
+    const size_t C = (size_t)(T_total / kBwdC + N);
+    BwdLayoutWs w{};
+    size_t o = 0;
+    w.off = o;   o += al((size_t)(N + 1) * 4);
+    w.tab = o;   o += al(C * 16);
+    w.ckpt = o;  o += al(C * H * dk * dv * 4);
+    w.phi = o;   o += al(C * H * dk * dk * 4);
+    w.psi = o;   o += al(C * H * dk * dv * 4);
+    w.dsend = o; o += al(C * H * dk * dv * 4);
+    w.snap = o;  o += al((size_t)grid_items * kBwdC * dk * dv * 4);
+    w.dA = o;    o += al(C * H * 4);
+    w.total = o;
+    return w;
+}
+
+int bwd_grid_items(int64_t T_total, int N, int H) {
+    const int64_t items = (T_total / kBwdC + N) * (int64_t)H;
+    const int64_t cap = (int64_t)sm_count() * 2;
+    return (int)(items < cap ? (items > 0 ? items : 1) : cap);
 }
 
 size_t bwd_workspace_size_public(int64_t T_total, int N, int H, int dk, int dv) {
-    return bwd_workspace_size(T_total, N, H, dk, dv, bwd_grid(N, H));
+    return bwd_ws_layout(T_total, N, H, dk, dv, bwd_grid_items(T_total, N, H)).total;
 }
 
 cudaError_t launch_bwd(const BwdArgs& a) {
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
-    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const int grid = bwd_grid(a.N, a.H);
-    const size_t slots = (size_t)(a.T_total / kBwdC + a.N + 1);
-    uint8_t* w = static_cast<uint8_t*>(a.workspace);
+    const int grid_items = bwd_grid_items(a.T_total, a.N, a.H);
+    const int64_t nh = (int64_t)a.N * a.H;
+    const int cap_nh = sm_count() * 2;
+    const int grid_nh = (int)(nh < cap_nh ? nh : cap_nh);
+    const BwdLayoutWs w = bwd_ws_layout(a.T_total, a.N, a.H, a.dk, a.dv, grid_items);
+    uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     BwdParams p{};
     p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.z = a.z; p.dout = a.dout;
     p.A_log = a.A_log; p.g_min = a.g_min; p.S0 = a.S0; p.dS_out = a.dS_out; p.cu = a.cu_seqlens;
     p.N = a.N; p.H = a.H; p.T_total = a.T_total;
     p.dq = a.dq; p.dk = a.dk_; p.dv = a.dv_; p.dbeta = a.dbeta; p.dz = a.dz; p.dS0 = a.dS0;
-    p.ckpt = reinterpret_cast<float*>(w);
-    p.snap = reinterpret_cast<float*>(w + al(slots * a.H * a.dk * a.dv * 4));
-    p.dA_part = reinterpret_cast<float*>(w + al(slots * a.H * a.dk * a.dv * 4) +
-                                         al((size_t)grid * kBwdC * a.dk * a.dv * 4));
+    p.chunk_off = reinterpret_cast<int32_t*>(ws + w.off);
+    p.chunk_tab = reinterpret_cast<int4*>(ws + w.tab);
+    p.ckpt = reinterpret_cast<float*>(ws + w.ckpt);
+    p.phi = reinterpret_cast<float*>(ws + w.phi);
+    p.psi = reinterpret_cast<float*>(ws + w.psi);
+    p.dsend = reinterpret_cast<float*>(ws + w.dsend);
+    p.snap = reinterpret_cast<float*>(ws + w.snap);
+    p.dA_item = reinterpret_cast<float*>(ws + w.dA);
     p.err = a.dev_err;
+    {
+        ProfScope prof("bwd_plan_kernel", a.stream);
+        bwd_plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, p.chunk_off,
+                                                  p.chunk_tab, a.dev_err);
+    }
     cudaError_t e;
     if (a.io_bf16) {
-        if (a.dk == 128 && a.dv == 128) e = launch_t<__nv_bfloat16, 128, 128>(p, grid, a.stream);
-        else if (a.dk == 128 && a.dv == 64) e = launch_t<__nv_bfloat16, 128, 64>(p, grid, a.stream);
-        else if (a.dk == 64 && a.dv == 128) e = launch_t<__nv_bfloat16, 64, 128>(p, grid, a.stream);
-        else e = launch_t<__nv_bfloat16, 64, 64>(p, grid, a.stream);
+        if (a.dk == 128 && a.dv == 128) e = launch_t<__nv_bfloat16, 128, 128>(p, grid_nh, grid_items, a.stream);
+        else if (a.dk == 128 && a.dv == 64) e = launch_t<__nv_bfloat16, 128, 64>(p, grid_nh, grid_items, a.stream);
+        else if (a.dk == 64 && a.dv == 128) e = launch_t<__nv_bfloat16, 64, 128>(p, grid_nh, grid_items, a.stream);
+        else e = launch_t<__nv_bfloat16, 64, 64>(p, grid_nh, grid_items, a.stream);
     } else {
-        if (a.dk == 128 && a.dv == 128) e = launch_t<float, 128, 128>(p, grid, a.stream);
-        else if (a.dk == 128 && a.dv == 64) e = launch_t<float, 128, 64>(p, grid, a.stream);
-        else if (a.dk == 64 && a.dv == 128) e = launch_t<float, 64, 128>(p, grid, a.stream);
-        else e = launch_t<float, 64, 64>(p, grid, a.stream);
+        if (a.dk == 128 && a.dv == 128) e = launch_t<float, 128, 128>(p, grid_nh, grid_items, a.stream);
+        else if (a.dk == 128 && a.dv == 64) e = launch_t<float, 128, 64>(p, grid_nh, grid_items, a.stream);
+        else if (a.dk == 64 && a.dv == 128) e = launch_t<float, 64, 128>(p, grid_nh, grid_items, a.stream);
+        else e = launch_t<float, 64, 64>(p, grid_nh, grid_items, a.stream);
     }
     if (e != cudaSuccess) return e;
     ProfScope prof("bwd_dA_kernel", a.stream);
-    bwd_dA_kernel<<<(a.H + 127) / 128, 128, 0, a.stream>>>(p.dA_part, a.N, a.H, a.dA_log);
+    bwd_dA_kernel<<<(a.H + 127) / 128, 128, 0, a.stream>>>(p.dA_item, p.chunk_off, a.N, a.H,
+                                                           a.dA_log);
     return cudaGetLastError();
 }
 
