@@ -494,19 +494,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 for (int c = 0; c < L::CPL; ++c)
                     P[r][c] = ps[(warp * L::RPW + r) * DV + lane + 32 * c];
             __syncthreads();
-            // B1: S' = alpha P; column sums of S' k (for w) and of (dS + q do^T) k (for du)
+            // B1: dS += q do^T; column sums of S' k = P (alpha k) (for w) and of dS k (for du)
+            float doj[L::CPL];
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) doj[c] = tv.dout[lane + 32 * c];
             float pw[L::CPL], pdu[L::CPL];
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
-                const float a = tv.alpha[i], kk = tv.k[i], qq = tv.q[i];
+                const float kk = tv.k[i], qq = tv.q[i], ak = tv.alpha[i] * kk;
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
-                    const int j = lane + 32 * c;
-                    dS[r][c] = fmaf(qq, tv.dout[j], dS[r][c]);
-                    pw[c] = fmaf(a * P[r][c], kk, pw[c]);
+                    dS[r][c] = fmaf(qq, doj[c], dS[r][c]);
+                    pw[c] = fmaf(P[r][c], ak, pw[c]);
                     pdu[c] = fmaf(dS[r][c], kk, pdu[c]);
                 }
             }
@@ -516,62 +518,85 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 part2[warp][lane + 32 * c] = pdu[c];
             }
             __syncthreads();
-            // B2: w, u, du per column; dv and the dbeta partial
-            float wdu = 0.f;
+            // B2: w, u per column (first warps), du and dv per column (middle warps)
             if (tid < DV) {
-                float s = 0.f, d = 0.f;
+                float s = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) {
-                    s += part[w2][tid];
-                    d += part2[w2][tid];
-                }
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) s += part[w2][tid];
                 const float wj = tv.v[tid] - s;
                 tv.w[tid] = wj;
                 tv.u[tid] = tv.beta * wj;
-                tv.du[tid] = d;
-                wdu = d * wj;
-                const size_t vo = ((size_t)t * p.H + h) * DV + tid;
+            } else if (tid >= 256 && tid < 256 + DV) {
+                const int j = tid - 256;
+                float d = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) d += part2[w2][j];
+                tv.du[j] = d;
+                const size_t vo = ((size_t)t * p.H + h) * DV + j;
                 static_cast<IO*>(p.dv)[vo] = from_f32<IO>(tv.beta * d);
             }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
-            if (lane == 0) red[warp] = wdu;
             __syncthreads();
-            if (tid == 0) {
-                float b = 0.f;
+            // B3: per element.  With S' = Diag(alpha) P and S_t = S' + k u^T the row sums are
+            //   dq_i     = alpha_i sum_j P_ij do_j + k_i (u . do)
+            //   dk_i     = sum_j dS_ij u_j - alpha_i sum_j P_ij beta du_j
+            //   dalpha_i = sum_j (dS_ij - k_i beta du_j) P_ij
+            // the per-row factors are applied to each lane's partial before the lanes are summed.
+            float uj[L::CPL], bduj[L::CPL];
+            float ud = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < DV / 32; ++w2) b += red[w2];
-                static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(b);
+            for (int c = 0; c < L::CPL; ++c) {
+                uj[c] = tv.u[lane + 32 * c];
+                bduj[c] = tv.beta * tv.du[lane + 32 * c];
+                ud = fmaf(uj[c], doj[c], ud);
             }
-            // B3: per element; row sums of S_t do (dq), dS u - S' beta du (dk), dS' P (dalpha)
+            float vals[32];  // [quantity][row]: 3 x RPW used, the rest zero
+#pragma unroll
+            for (int x = 0; x < 32; ++x) vals[x] = 0.f;
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
                 const float a = tv.alpha[i], kk = tv.k[i];
-                float sq = 0.f, sk = 0.f, sa = 0.f;
+                float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
-                    const int j = lane + 32 * c;
-                    const float sp = a * P[r][c];
-                    const float bdu = tv.beta * tv.du[j];
-                    sq = fmaf(sp + kk * tv.u[j], tv.dout[j], sq);
-                    sk = fmaf(dS[r][c], tv.u[j], sk);
-                    sk = fmaf(-sp, bdu, sk);
-                    const float dsp = fmaf(-kk, bdu, dS[r][c]);
-                    sa = fmaf(dsp, P[r][c], sa);
+                    s1 = fmaf(P[r][c], doj[c], s1);
+                    s2 = fmaf(dS[r][c], uj[c], s2);
+                    s3 = fmaf(P[r][c], bduj[c], s3);
+                    const float dsp = fmaf(-kk, bduj[c], dS[r][c]);
+                    s4 = fmaf(dsp, P[r][c], s4);
                     dS[r][c] = a * dsp;
                 }
+                vals[r] = a * s1;
+                vals[8 + r] = fmaf(-a, s3, s2);
+                vals[16 + r] = s4;
+            }
+            // sum over the 32 lanes, halving the values each step: lane l ends with value l
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    sq += __shfl_xor_sync(0xffffffffu, sq, off);
-                    sk += __shfl_xor_sync(0xffffffffu, sk, off);
-                    sa += __shfl_xor_sync(0xffffffffu, sa, off);
+            for (int m = 16; m >= 1; m >>= 1) {
+                const bool up = (lane & m) != 0;
+#pragma unroll
+                for (int x = 0; x < m; ++x) {
+                    const float send = up ? vals[x] : vals[x + m];
+                    const float keep = up ? vals[x + m] : vals[x];
+                    vals[x] = keep + __shfl_xor_sync(0xffffffffu, send, m);
                 }
-                if (lane == 0) {
-                    rowv[0][i] = sq;
-                    rowv[1][i] = sk;
-                    rowv[2][i] = sa;
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) ud += __shfl_xor_sync(0xffffffffu, ud, off);
+            {
+                const int qn = lane >> 3, r = lane & 7;
+                if (qn < 3 && r < L::RPW) {
+                    const int i = warp * L::RPW + r;
+                    rowv[qn][i] = qn == 0 ? fmaf(tv.k[i], ud, vals[0]) : vals[0];
                 }
+            }
+            if (warp == kBwdWarps - 1) {  // dbeta = du . w
+                float wdu = 0.f;
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) wdu = fmaf(tv.du[lane + 32 * c], tv.w[lane + 32 * c], wdu);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
+                if (lane == 0) static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(wdu);
             }
             __syncthreads();
             // B4: per key channel: dq, dk, dz and the dA_log partial
