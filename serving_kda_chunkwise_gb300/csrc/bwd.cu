@@ -21,11 +21,11 @@
 //   bwd_plan_kernel   chunk offsets of every sequence and a table entry per chunk
 //   bwd_fwdtrans_kernel  per (chunk, head), all in parallel: the chunk's forward map on the
 //                     state, S_end = A S_start + B
-//   bwd_chain_kernel<fwd>  per (sequence, head): S at every chunk start (S <- A S + B, first
-//                     chunk first), the checkpoints
+//   bwd_chain_kernel<fwd>  per (sequence, head, 32-column slice): S at every chunk start
+//                     (S <- A S + B, first chunk first), the checkpoints
 //   bwd_phi_kernel    per (chunk, head), all in parallel: Phi and Psi of the chunk
-//   bwd_chain_kernel  per (sequence, head): dS at every chunk end, last chunk first
-//                     (dS <- Phi dS + Psi, a 128 x 128 x 128 product per chunk), and dS0
+//   bwd_chain_kernel  per (sequence, head, 32-column slice): dS at every chunk end, last
+//                     chunk first (dS <- Phi dS + Psi), and dS0
 //   bwd_item_kernel   per (chunk, head), all in parallel: the chunk's forward from its
 //                     checkpoint (the state before every token kept in per-CTA scratch), then
 //                     the reverse rules above token by token from the chunk's dS
@@ -359,28 +359,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
     }
 }
 
-// Dynamic shared memory of the chain kernel: dS (the right operand of Phi dS) and Phi, the
-// latter loaded by the whole CTA in one coalesced pass per chunk.
-// kFwd: the states at the chunk starts (S <- A S + B, first chunk first, each start stored
-// in the checkpoints); otherwise the state's gradient at the chunk ends (dS <- Phi dS + Psi,
-// last chunk first, each end stored) and finally dS0.
+// The chain over a sequence's chunks, column slice by column slice (X <- Phi X + Psi acts on
+// each column of X alone): CTA (nh, slice) carries columns [32 slice, 32 slice + 32) of X.
+// kFwd: the states at the chunk starts (X = S, Phi/Psi holding the chunk's forward map A/B,
+// first chunk first, each start stored in the checkpoints); otherwise the state's gradient
+// at the chunk ends (X = dS, last chunk first, each end stored) and finally dS0.
+// Warp w owns rows [RPW w, RPW (w + 1)), lane l column 32 slice + l.  Dynamic shared memory:
+// the slice of X [DK][32] and the chunk's Phi [DK][DK], loaded by the whole CTA in one
+// coalesced pass per chunk.
+constexpr int kChainCols = 32;
+
 template <int DK, int DV, bool kFwd>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const BwdParams p) {
-    using L = BwdLayout<DK, DV>;
+    constexpr int RPW = DK / kBwdWarps;
+    constexpr int NS = DV / kChainCols;
     extern __shared__ __align__(16) float chain_smem[];
-    float* dss = chain_smem;            // [DK][DV]
-    float* phs = chain_smem + DK * DV;  // [DK][DK]
+    float* xs = chain_smem;                  // [DK][32]
+    float* phs = chain_smem + DK * kChainCols;  // [DK][DK]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int nh = blockIdx.x; nh < p.N * p.H; nh += gridDim.x) {
+    for (int blk = blockIdx.x; blk < p.N * p.H * NS; blk += gridDim.x) {
+        const int nh = blk / NS, col = (blk % NS) * kChainCols + lane;
         const int h = nh % p.H, n = nh / p.H;
         const float* init = kFwd ? p.S0 : p.dS_out;
-        float dS[L::RPW][L::CPL];  // the carried matrix (S forward, dS backward)
+        float X[RPW];
 #pragma unroll
-        for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-            for (int c = 0; c < L::CPL; ++c)
-                dS[r][c] = init ? init[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c]
-                                : 0.f;
+        for (int r = 0; r < RPW; ++r)
+            X[r] = init ? init[((size_t)nh * DK + warp * RPW + r) * DV + col] : 0.f;
         const int32_t g0 = p.chunk_off[n], g1 = p.chunk_off[n + 1];
         for (int32_t step = 0; step < g1 - g0; ++step) {
             const int32_t g = kFwd ? g0 + step : g1 - 1 - step;
@@ -390,41 +394,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const BwdPara
             const float* ps = p.psi + it * DK * DV;
             for (int i4 = tid; i4 < DK * DK / 4; i4 += kBwdThreads)
                 reinterpret_cast<float4*>(phs)[i4] = __ldg(ph4 + i4);
-            float acc[L::RPW][L::CPL];
+            float acc[RPW];
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c) {
-                    const int i = warp * L::RPW + r, j = lane + 32 * c;
-                    de[i * DV + j] = dS[r][c];
-                    dss[i * DV + j] = dS[r][c];
-                    acc[r][c] = ps[i * DV + j];
-                }
+            for (int r = 0; r < RPW; ++r) {
+                const int i = warp * RPW + r;
+                de[i * DV + col] = X[r];
+                xs[i * kChainCols + lane] = X[r];
+                acc[r] = ps[i * DV + col];
+            }
             __syncthreads();
-            // dS <- Phi dS + Psi
-            for (int l = 0; l < DK; ++l) {
-                float dl[L::CPL];
+            // X <- Phi X + Psi, four Phi columns per shared-memory load
+            for (int l = 0; l < DK; l += 4) {
+                const float x0 = xs[(l + 0) * kChainCols + lane];
+                const float x1 = xs[(l + 1) * kChainCols + lane];
+                const float x2 = xs[(l + 2) * kChainCols + lane];
+                const float x3 = xs[(l + 3) * kChainCols + lane];
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c) dl[c] = dss[l * DV + lane + 32 * c];
-#pragma unroll
-                for (int r = 0; r < L::RPW; ++r) {
-                    const float f = phs[(warp * L::RPW + r) * DK + l];
-#pragma unroll
-                    for (int c = 0; c < L::CPL; ++c) acc[r][c] = fmaf(f, dl[c], acc[r][c]);
+                for (int r = 0; r < RPW; ++r) {
+                    const float4 f = *reinterpret_cast<const float4*>(phs + (warp * RPW + r) * DK + l);
+                    acc[r] = fmaf(f.x, x0, acc[r]);
+                    acc[r] = fmaf(f.y, x1, acc[r]);
+                    acc[r] = fmaf(f.z, x2, acc[r]);
+                    acc[r] = fmaf(f.w, x3, acc[r]);
                 }
             }
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c) dS[r][c] = acc[r][c];
-            __syncthreads();  // dss and phs are rewritten for the next chunk
+            for (int r = 0; r < RPW; ++r) X[r] = acc[r];
+            __syncthreads();  // xs and phs are rewritten for the next chunk
         }
         if (!kFwd && p.dS0) {
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c)
-                    p.dS0[((size_t)nh * DK + warp * L::RPW + r) * DV + lane + 32 * c] = dS[r][c];
+            for (int r = 0; r < RPW; ++r)
+                p.dS0[((size_t)nh * DK + warp * RPW + r) * DV + col] = X[r];
         }
     }
 }
@@ -639,7 +640,7 @@ __global__ void bwd_dA_kernel(const float* __restrict__ part, const int32_t* __r
 
 template <typename IO, int DK, int DV>
 cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream_t stream) {
-    constexpr int chain_smem = (DK * DV + DK * DK) * 4;
+    constexpr int chain_smem = (DK * kChainCols + DK * DK) * 4;
     cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
     if (e == cudaSuccess)
@@ -716,7 +717,7 @@ size_t bwd_workspace_size_public(int64_t T_total, int N, int H, int dk, int dv) 
 cudaError_t launch_bwd(const BwdArgs& a) {
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
     const int grid_items = bwd_grid_items(a.T_total, a.N, a.H);
-    const int64_t nh = (int64_t)a.N * a.H;
+    const int64_t nh = (int64_t)a.N * a.H * (a.dv / kChainCols);  // chain CTAs: column slices
     const int cap_nh = sm_count() * 2;
     const int grid_nh = (int)(nh < cap_nh ? nh : cap_nh);
     const BwdLayoutWs w = bwd_ws_layout(a.T_total, a.N, a.H, a.dk, a.dv, grid_items);
