@@ -48,74 +48,6 @@ struct BwdLayout {
     static constexpr int CPL = DV / 32;         // columns per lane
 };
 
-// the per-token vectors in shared memory
-template <int DK, int DV>
-struct TokVec {
-    float k[DK], q[DK], alpha[DK], x[DK];
-    float v[DV], dout[DV], w[DV], u[DV], du[DV];
-    float beta;
-};
-
-template <typename IO, int DK, int DV>
-__device__ __forceinline__ void load_token(TokVec<DK, DV>& tv, const IO* q, const IO* k,
-                                           const IO* v, const IO* beta, const IO* z,
-                                           const IO* dout, int64_t t, int H, int h, float scale,
-                                           float g_min, int tid) {
-    const size_t kofs = ((size_t)t * H + h) * DK, vofs = ((size_t)t * H + h) * DV;
-    if (tid < DK) {
-        tv.k[tid] = to_f32(k[kofs + tid]);
-        tv.q[tid] = to_f32(q[kofs + tid]);
-        const float x = scale * to_f32(z[kofs + tid]);
-        tv.x[tid] = x;
-        tv.alpha[tid] = expf(g_min / (1.0f + expf(-x)));
-    } else if (tid >= 256 && tid < 256 + DV) {
-        const int j = tid - 256;
-        tv.v[j] = to_f32(v[vofs + j]);
-        if (dout) tv.dout[j] = to_f32(dout[vofs + j]);
-    }
-    if (tid == 511) tv.beta = to_f32(beta[(size_t)t * H + h]);
-}
-
-// one forward token on the register-resident state (S <- S' + k u^T); uses tv.w, tv.u and
-// `part` ([warps][DV]) as scratch; two barriers
-template <int DK, int DV>
-__device__ __forceinline__ void fwd_token(float (&S)[BwdLayout<DK, DV>::RPW][BwdLayout<DK, DV>::CPL],
-                                          TokVec<DK, DV>& tv, float (*part)[DV], int warp,
-                                          int lane, int tid) {
-    using L = BwdLayout<DK, DV>;
-    float pc[L::CPL];
-#pragma unroll
-    for (int c = 0; c < L::CPL; ++c) pc[c] = 0.f;
-#pragma unroll
-    for (int r = 0; r < L::RPW; ++r) {
-        const int i = warp * L::RPW + r;
-        const float a = tv.alpha[i], kk = tv.k[i];
-#pragma unroll
-        for (int c = 0; c < L::CPL; ++c) {
-            S[r][c] *= a;
-            pc[c] = fmaf(S[r][c], kk, pc[c]);
-        }
-    }
-#pragma unroll
-    for (int c = 0; c < L::CPL; ++c) part[warp][lane + 32 * c] = pc[c];
-    __syncthreads();
-    if (tid < DV) {
-        float s = 0.f;
-#pragma unroll
-        for (int w2 = 0; w2 < kBwdWarps; ++w2) s += part[w2][tid];
-        const float wj = tv.v[tid] - s;
-        tv.w[tid] = wj;
-        tv.u[tid] = tv.beta * wj;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < L::RPW; ++r) {
-        const float kk = tv.k[warp * L::RPW + r];
-#pragma unroll
-        for (int c = 0; c < L::CPL; ++c) S[r][c] = fmaf(kk, tv.u[lane + 32 * c], S[r][c]);
-    }
-}
-
 struct BwdParams {
     const void *q, *k, *v, *beta, *z, *dout;
     const float* A_log;
@@ -169,28 +101,94 @@ __global__ void __launch_bounds__(1024) bwd_plan_kernel(const int32_t* __restric
     }
 }
 
+// One chunk's token inputs, staged in (dynamic) shared memory as fp32 by the whole CTA at the
+// start of an item, so that the per-token steps read no global memory: k, q [64][DK], the
+// gate's x = e^{A_h} z and alpha = exp(g) [64][DK], v, do [64][DV], beta [64].  Arrays a
+// kernel does not use are given no space (nullptr).
+template <int DK, int DV>
+struct Stage {
+    float *k, *q, *x, *a, *v, *dout, *beta;
+};
+
+// carve the arrays out of `base` in a fixed order; returns the floats used
+template <int DK, int DV>
+__host__ __device__ constexpr int stage_floats(bool q, bool x, bool v, bool dout) {
+    return kBwdC * DK * (2 + (q ? 1 : 0) + (x ? 1 : 0)) + kBwdC * DV * ((v ? 1 : 0) + (dout ? 1 : 0)) +
+           kBwdC;
+}
+
+template <int DK, int DV>
+__device__ __forceinline__ Stage<DK, DV> stage_carve(float* base, bool q, bool x, bool v,
+                                                     bool dout) {
+    Stage<DK, DV> st{};
+    st.k = base;            base += kBwdC * DK;
+    st.a = base;            base += kBwdC * DK;
+    if (q) { st.q = base;   base += kBwdC * DK; }
+    if (x) { st.x = base;   base += kBwdC * DK; }
+    if (v) { st.v = base;   base += kBwdC * DV; }
+    if (dout) { st.dout = base; base += kBwdC * DV; }
+    st.beta = base;
+    return st;
+}
+
+template <typename IO, int DK, int DV>
+__device__ __forceinline__ void stage_chunk(const Stage<DK, DV>& st, const BwdParams& p,
+                                            int64_t t0, int rows, int h, float scale) {
+    const IO* k = static_cast<const IO*>(p.k);
+    const IO* q = static_cast<const IO*>(p.q);
+    const IO* z = static_cast<const IO*>(p.z);
+    const IO* v = static_cast<const IO*>(p.v);
+    const IO* dout = static_cast<const IO*>(p.dout);
+    const IO* beta = static_cast<const IO*>(p.beta);
+    const size_t kb = ((size_t)t0 * p.H + h) * DK, vb = ((size_t)t0 * p.H + h) * DV;
+    for (int idx = threadIdx.x; idx < rows * DK; idx += kBwdThreads) {
+        const int tt = idx / DK, i = idx % DK;
+        const size_t o = kb + (size_t)tt * p.H * DK + i;
+        st.k[idx] = to_f32(k[o]);
+        if (st.q) st.q[idx] = to_f32(q[o]);
+        const float xv = scale * to_f32(z[o]);
+        if (st.x) st.x[idx] = xv;
+        st.a[idx] = expf(p.g_min / (1.0f + expf(-xv)));
+    }
+    if (st.v || st.dout) {
+        for (int idx = threadIdx.x; idx < rows * DV; idx += kBwdThreads) {
+            const int tt = idx / DV, j = idx % DV;
+            const size_t o = vb + (size_t)tt * p.H * DV + j;
+            if (st.v) st.v[idx] = to_f32(v[o]);
+            if (st.dout) st.dout[idx] = to_f32(dout[o]);
+        }
+    }
+    for (int tt = threadIdx.x; tt < rows; tt += kBwdThreads)
+        st.beta[tt] = to_f32(beta[(size_t)(t0 + tt) * p.H + h]);
+}
+
+// the item (chunk, head) `it`: head, first token, rows
+__device__ __forceinline__ void item_of(const BwdParams& p, int64_t it, int& h, int64_t& t0,
+                                        int& rows) {
+    h = (int)(it % p.H);
+    const int4 e = p.chunk_tab[it / p.H];
+    t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
+    rows = e.w;
+}
+
 template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
     constexpr int CK = DK / 32;  // Phi columns per lane
-    __shared__ TokVec<DK, DV> tv;
-    __shared__ float partA[kBwdWarps][DK];
-    __shared__ float partB[kBwdWarps][DV];
-    __shared__ float duA[DK];
+    extern __shared__ __align__(16) float stage_smem[];
+    const Stage<DK, DV> st = stage_carve<DK, DV>(stage_smem, true, false, false, true);
+    // column sums, double-buffered so that two barriers per token suffice
+    __shared__ float partA[2][kBwdWarps][DK];
+    __shared__ float partB[2][kBwdWarps][DV];
+    __shared__ float duA[2][DK], duB[2][DV];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const IO* q = static_cast<const IO*>(p.q);
-    const IO* k = static_cast<const IO*>(p.k);
-    const IO* v = static_cast<const IO*>(p.v);
-    const IO* beta = static_cast<const IO*>(p.beta);
-    const IO* z = static_cast<const IO*>(p.z);
-    const IO* dout = static_cast<const IO*>(p.dout);
     const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int h = (int)(it % p.H);
-        const int4 e = p.chunk_tab[it / p.H];
-        const int64_t t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
-        const int64_t t1 = t0 + e.w;
-        const float scale = expf(p.A_log[h]);
+        int h, rows;
+        int64_t t0;
+        item_of(p, it, h, t0, rows);
+        __syncthreads();  // the previous item's staged inputs are consumed
+        stage_chunk<IO, DK, DV>(st, p, t0, rows, h, expf(p.A_log[h]));
         float Phi[L::RPW][CK], Psi[L::RPW][L::CPL];
 #pragma unroll
         for (int r = 0; r < L::RPW; ++r) {
@@ -199,55 +197,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) Psi[r][c] = 0.f;
         }
-        for (int64_t t = t1 - 1; t >= t0; --t) {
-            __syncthreads();  // the previous token's vectors and sums are consumed
-            load_token<IO, DK, DV>(tv, q, k, v, beta, z, dout, t, p.H, h, scale, p.g_min, tid);
-            __syncthreads();
+        __syncthreads();
+        for (int tt = rows - 1; tt >= 0; --tt) {
+            const int b = tt & 1;
+            const float* kt = st.k + tt * DK;
+            const float* qt = st.q + tt * DK;
+            const float* at = st.a + tt * DK;
+            const float* dot = st.dout + tt * DV;
             // Psi += q do^T; column sums of Phi^T k and Psi^T k
-            float pa[CK], pb[L::CPL];
+            float pa[CK], pb[L::CPL], doj[L::CPL];
 #pragma unroll
             for (int c = 0; c < CK; ++c) pa[c] = 0.f;
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) pb[c] = 0.f;
+            for (int c = 0; c < L::CPL; ++c) {
+                pb[c] = 0.f;
+                doj[c] = dot[lane + 32 * c];
+            }
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
-                const float kk = tv.k[i], qq = tv.q[i];
+                const float kk = kt[i], qq = qt[i];
 #pragma unroll
                 for (int c = 0; c < CK; ++c) pa[c] = fmaf(Phi[r][c], kk, pa[c]);
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
-                    Psi[r][c] = fmaf(qq, tv.dout[lane + 32 * c], Psi[r][c]);
+                    Psi[r][c] = fmaf(qq, doj[c], Psi[r][c]);
                     pb[c] = fmaf(Psi[r][c], kk, pb[c]);
                 }
             }
 #pragma unroll
-            for (int c = 0; c < CK; ++c) partA[warp][lane + 32 * c] = pa[c];
+            for (int c = 0; c < CK; ++c) partA[b][warp][lane + 32 * c] = pa[c];
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) partB[warp][lane + 32 * c] = pb[c];
+            for (int c = 0; c < L::CPL; ++c) partB[b][warp][lane + 32 * c] = pb[c];
             __syncthreads();
             if (tid < DK) {
                 float sa = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) sa += partA[w2][tid];
-                duA[tid] = sa;
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sa += partA[b][w2][tid];
+                duA[b][tid] = sa;
             } else if (tid >= 256 && tid < 256 + DV) {
                 float sb = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) sb += partB[w2][tid - 256];
-                tv.du[tid - 256] = sb;
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sb += partB[b][w2][tid - 256];
+                duB[b][tid - 256] = sb;
             }
             __syncthreads();
             // X <- Diag(alpha) (X - beta k du^T) for X = Phi and Psi
+            const float bt = st.beta[tt];
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
-                const float a = tv.alpha[i], bk = tv.beta * tv.k[i];
+                const float a = at[i], bk = bt * kt[i];
 #pragma unroll
-                for (int c = 0; c < CK; ++c) Phi[r][c] = a * fmaf(-bk, duA[lane + 32 * c], Phi[r][c]);
+                for (int c = 0; c < CK; ++c) Phi[r][c] = a * fmaf(-bk, duA[b][lane + 32 * c], Phi[r][c]);
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c)
-                    Psi[r][c] = a * fmaf(-bk, tv.du[lane + 32 * c], Psi[r][c]);
+                    Psi[r][c] = a * fmaf(-bk, duB[b][lane + 32 * c], Psi[r][c]);
             }
         }
         float* ph = p.phi + (size_t)it * DK * DK;
@@ -271,23 +276,19 @@ template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
     constexpr int CK = DK / 32;
-    __shared__ TokVec<DK, DV> tv;
-    __shared__ float partA[kBwdWarps][DK];
-    __shared__ float partB[kBwdWarps][DV];
-    __shared__ float wA[DK];
+    extern __shared__ __align__(16) float stage_smem[];
+    const Stage<DK, DV> st = stage_carve<DK, DV>(stage_smem, false, false, true, false);
+    __shared__ float partA[2][kBwdWarps][DK];
+    __shared__ float partB[2][kBwdWarps][DV];
+    __shared__ float wA[2][DK], wB[2][DV];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const IO* q = static_cast<const IO*>(p.q);
-    const IO* k = static_cast<const IO*>(p.k);
-    const IO* v = static_cast<const IO*>(p.v);
-    const IO* beta = static_cast<const IO*>(p.beta);
-    const IO* z = static_cast<const IO*>(p.z);
     const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int h = (int)(it % p.H);
-        const int4 e = p.chunk_tab[it / p.H];
-        const int64_t t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
-        const int64_t t1 = t0 + e.w;
-        const float scale = expf(p.A_log[h]);
+        int h, rows;
+        int64_t t0;
+        item_of(p, it, h, t0, rows);
+        __syncthreads();  // the previous item's staged inputs are consumed
+        stage_chunk<IO, DK, DV>(st, p, t0, rows, h, expf(p.A_log[h]));
         float A[L::RPW][CK], B[L::RPW][L::CPL];
 #pragma unroll
         for (int r = 0; r < L::RPW; ++r) {
@@ -296,10 +297,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) B[r][c] = 0.f;
         }
-        for (int64_t t = t0; t < t1; ++t) {
-            __syncthreads();
-            load_token<IO, DK, DV>(tv, q, k, v, beta, z, nullptr, t, p.H, h, scale, p.g_min, tid);
-            __syncthreads();
+        __syncthreads();
+        for (int tt = 0; tt < rows; ++tt) {
+            const int b = tt & 1;
+            const float* kt = st.k + tt * DK;
+            const float* at = st.a + tt * DK;
             float pa[CK], pb[L::CPL];
 #pragma unroll
             for (int c = 0; c < CK; ++c) pa[c] = 0.f;
@@ -308,7 +310,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
-                const float a = tv.alpha[i], kk = tv.k[i];
+                const float a = at[i], kk = kt[i];
 #pragma unroll
                 for (int c = 0; c < CK; ++c) {
                     A[r][c] *= a;
@@ -321,29 +323,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
                 }
             }
 #pragma unroll
-            for (int c = 0; c < CK; ++c) partA[warp][lane + 32 * c] = pa[c];
+            for (int c = 0; c < CK; ++c) partA[b][warp][lane + 32 * c] = pa[c];
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) partB[warp][lane + 32 * c] = pb[c];
+            for (int c = 0; c < L::CPL; ++c) partB[b][warp][lane + 32 * c] = pb[c];
             __syncthreads();
             if (tid < DK) {
                 float sa = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) sa += partA[w2][tid];
-                wA[tid] = sa;
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sa += partA[b][w2][tid];
+                wA[b][tid] = sa;
             } else if (tid >= 256 && tid < 256 + DV) {
                 float sb = 0.f;
 #pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) sb += partB[w2][tid - 256];
-                tv.w[tid - 256] = sb - tv.v[tid - 256];  // (k^T B') - v
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) sb += partB[b][w2][tid - 256];
+                wB[b][tid - 256] = sb - st.v[tt * DV + tid - 256];  // (k^T B') - v
             }
             __syncthreads();
+            const float bt = st.beta[tt];
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const float bk = tv.beta * tv.k[warp * L::RPW + r];
+                const float bk = bt * kt[warp * L::RPW + r];
 #pragma unroll
-                for (int c = 0; c < CK; ++c) A[r][c] = fmaf(-bk, wA[lane + 32 * c], A[r][c]);
+                for (int c = 0; c < CK; ++c) A[r][c] = fmaf(-bk, wA[b][lane + 32 * c], A[r][c]);
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c) B[r][c] = fmaf(-bk, tv.w[lane + 32 * c], B[r][c]);
+                for (int c = 0; c < L::CPL; ++c) B[r][c] = fmaf(-bk, wB[b][lane + 32 * c], B[r][c]);
             }
         }
         float* pa_out = p.phi + (size_t)it * DK * DK;
@@ -365,8 +368,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
 // first chunk first, each start stored in the checkpoints); otherwise the state's gradient
 // at the chunk ends (X = dS, last chunk first, each end stored) and finally dS0.
 // Warp w owns rows [RPW w, RPW (w + 1)), lane l column 32 slice + l.  Dynamic shared memory:
-// the slice of X [DK][32] and the chunk's Phi [DK][DK], loaded by the whole CTA in one
-// coalesced pass per chunk.
+// the slice of X [DK][32] and the chunk's Phi [DK][DK], fetched by the whole CTA into
+// registers one chunk ahead (coalesced float4s) and stored to shared memory per chunk.
 constexpr int kChainCols = 32;
 
 template <int DK, int DV, bool kFwd>
@@ -386,22 +389,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const BwdPara
         for (int r = 0; r < RPW; ++r)
             X[r] = init ? init[((size_t)nh * DK + warp * RPW + r) * DV + col] : 0.f;
         const int32_t g0 = p.chunk_off[n], g1 = p.chunk_off[n + 1];
+        // the next chunk's Phi (this thread's float4s of it) and Psi column, fetched one chunk
+        // ahead so that the loads overlap the product
+        constexpr int kPf = DK * DK / 4 / kBwdThreads;
+        float4 pf[kPf];
+        float psv[RPW];
+        auto fetch = [&](int32_t step) {
+            const int32_t g = kFwd ? g0 + step : g1 - 1 - step;
+            const size_t it = (size_t)g * p.H + h;
+            const float4* ph4 = reinterpret_cast<const float4*>(p.phi + it * DK * DK);
+#pragma unroll
+            for (int x = 0; x < kPf; ++x) pf[x] = __ldg(ph4 + tid + x * kBwdThreads);
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) psv[r] = p.psi[it * DK * DV + (warp * RPW + r) * DV + col];
+        };
+        if (g1 > g0) fetch(0);
         for (int32_t step = 0; step < g1 - g0; ++step) {
             const int32_t g = kFwd ? g0 + step : g1 - 1 - step;
             const size_t it = (size_t)g * p.H + h;
             float* de = (kFwd ? p.ckpt : p.dsend) + it * DK * DV;
-            const float4* ph4 = reinterpret_cast<const float4*>(p.phi + it * DK * DK);
-            const float* ps = p.psi + it * DK * DV;
-            for (int i4 = tid; i4 < DK * DK / 4; i4 += kBwdThreads)
-                reinterpret_cast<float4*>(phs)[i4] = __ldg(ph4 + i4);
+#pragma unroll
+            for (int x = 0; x < kPf; ++x) reinterpret_cast<float4*>(phs)[tid + x * kBwdThreads] = pf[x];
             float acc[RPW];
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
                 const int i = warp * RPW + r;
                 de[i * DV + col] = X[r];
                 xs[i * kChainCols + lane] = X[r];
-                acc[r] = ps[i * DV + col];
+                acc[r] = psv[r];
             }
+            if (step + 1 < g1 - g0) fetch(step + 1);
             __syncthreads();
             // X <- Phi X + Psi, four Phi columns per shared-memory load
             for (int l = 0; l < DK; l += 4) {
@@ -430,82 +447,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const BwdPara
     }
 }
 
+// Per (chunk, head): the chunk's forward from its checkpoint, keeping the state before each
+// token in per-CTA scratch (thread-private float4s, laid out [token][float4][thread] so that
+// every store and load is coalesced), then the reverse rules token by token from the chunk's
+// dS.  Two barriers per forward token and three per reverse token, double-buffered where a
+// shared vector is rewritten before every reader has passed the next barrier.
 template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
-    __shared__ TokVec<DK, DV> tv;
+    constexpr int NE = L::RPW * L::CPL;  // state elements per thread
+    constexpr int NV4 = NE / 4;
+    static_assert(NE % 4 == 0, "state elements per thread");
+    extern __shared__ __align__(16) float stage_smem[];
+    const Stage<DK, DV> st = stage_carve<DK, DV>(stage_smem, true, true, true, true);
     __shared__ float part[kBwdWarps][DV];
     __shared__ float part2[kBwdWarps][DV];
+    __shared__ float w_s[DV], u_s[DV], du_s[DV];
     __shared__ float rowv[3][DK];  // dq, dk, dalpha
     __shared__ float red[kBwdWarps];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float* snap = p.snap + (size_t)blockIdx.x * kBwdC * DK * DV;
-    const IO* q = static_cast<const IO*>(p.q);
-    const IO* k = static_cast<const IO*>(p.k);
-    const IO* v = static_cast<const IO*>(p.v);
-    const IO* beta = static_cast<const IO*>(p.beta);
-    const IO* z = static_cast<const IO*>(p.z);
-    const IO* dout = static_cast<const IO*>(p.dout);
+    float4* snap = reinterpret_cast<float4*>(p.snap) + (size_t)blockIdx.x * kBwdC * NV4 * kBwdThreads;
     const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int h = (int)(it % p.H);
-        const int4 e = p.chunk_tab[it / p.H];
-        const int64_t t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
-        const int64_t t1 = t0 + e.w;
+        int h, rows;
+        int64_t t0;
+        item_of(p, it, h, t0, rows);
         const float scale = expf(p.A_log[h]);
+        __syncthreads();  // the previous item's staged inputs and sums are consumed
+        stage_chunk<IO, DK, DV>(st, p, t0, rows, h, scale);
         float dA_acc = 0.f;
         float dS[L::RPW][L::CPL];  // the state's gradient at the chunk end
+        float S[L::RPW][L::CPL];   // the state at the chunk start
         const float* de = p.dsend + (size_t)it * DK * DV;
-#pragma unroll
-        for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-            for (int c = 0; c < L::CPL; ++c)
-                dS[r][c] = de[(warp * L::RPW + r) * DV + lane + 32 * c];
-        // ---- the chunk's forward from its checkpoint, keeping the state before each token
-        float S[L::RPW][L::CPL];
         const float* src = p.ckpt + (size_t)it * DK * DV;
 #pragma unroll
         for (int r = 0; r < L::RPW; ++r)
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c)
-                S[r][c] = src[(warp * L::RPW + r) * DV + lane + 32 * c];
-        for (int64_t t = t0; t < t1; ++t) {
-            float* dst = snap + (size_t)(t - t0) * DK * DV;
+            for (int c = 0; c < L::CPL; ++c) {
+                const int o = (warp * L::RPW + r) * DV + lane + 32 * c;
+                dS[r][c] = de[o];
+                S[r][c] = src[o];
+            }
+        __syncthreads();
+        // ---- the chunk's forward from its checkpoint, keeping the state before each token
+        for (int tt = 0; tt < rows; ++tt) {
+            float4* dst = snap + (size_t)tt * NV4 * kBwdThreads + tid;
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r)
+            for (int x = 0; x < NV4; ++x) {
+                const int e = 4 * x;
+                dst[x * kBwdThreads] =
+                    make_float4(S[e / L::CPL][e % L::CPL], S[(e + 1) / L::CPL][(e + 1) % L::CPL],
+                                S[(e + 2) / L::CPL][(e + 2) % L::CPL],
+                                S[(e + 3) / L::CPL][(e + 3) % L::CPL]);
+            }
+            if (tt + 1 == rows) break;  // the last token's state is not needed
+            const float* kt = st.k + tt * DK;
+            const float* at = st.a + tt * DK;
+            float pc[L::CPL];
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c)
-                    dst[(warp * L::RPW + r) * DV + lane + 32 * c] = S[r][c];
+            for (int c = 0; c < L::CPL; ++c) pc[c] = 0.f;
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const int i = warp * L::RPW + r;
+                const float a = at[i], kk = kt[i];
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    S[r][c] *= a;
+                    pc[c] = fmaf(S[r][c], kk, pc[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < L::CPL; ++c) part[warp][lane + 32 * c] = pc[c];
             __syncthreads();
-            load_token<IO, DK, DV>(tv, q, k, v, beta, z, nullptr, t, p.H, h, scale, p.g_min,
-                                   tid);
+            if (tid < DV) {
+                float s = 0.f;
+#pragma unroll
+                for (int w2 = 0; w2 < kBwdWarps; ++w2) s += part[w2][tid];
+                u_s[tid] = st.beta[tt] * (st.v[tt * DV + tid] - s);
+            }
             __syncthreads();
-            if (t + 1 < t1) fwd_token<DK, DV>(S, tv, part, warp, lane, tid);
+#pragma unroll
+            for (int r = 0; r < L::RPW; ++r) {
+                const float kk = kt[warp * L::RPW + r];
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) S[r][c] = fmaf(kk, u_s[lane + 32 * c], S[r][c]);
+            }
         }
         // ---- back through the chunk's tokens
-        for (int64_t t = t1 - 1; t >= t0; --t) {
-            __syncthreads();  // previous token's vectors and partial sums are consumed
-            load_token<IO, DK, DV>(tv, q, k, v, beta, z, dout, t, p.H, h, scale, p.g_min,
-                                   tid);
-            float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
-            const float* ps = snap + (size_t)(t - t0) * DK * DV;
+        float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
+        auto load_snap = [&](int tt) {
+            const float4* ps = snap + (size_t)tt * NV4 * kBwdThreads + tid;
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r)
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c)
-                    P[r][c] = ps[(warp * L::RPW + r) * DV + lane + 32 * c];
-            __syncthreads();
+            for (int x = 0; x < NV4; ++x) {
+                const float4 f = ps[x * kBwdThreads];
+                const int e = 4 * x;
+                P[e / L::CPL][e % L::CPL] = f.x;
+                P[(e + 1) / L::CPL][(e + 1) % L::CPL] = f.y;
+                P[(e + 2) / L::CPL][(e + 2) % L::CPL] = f.z;
+                P[(e + 3) / L::CPL][(e + 3) % L::CPL] = f.w;
+            }
+        };
+        if (rows > 0) load_snap(rows - 1);
+        for (int tt = rows - 1; tt >= 0; --tt) {
+            const int64_t t = t0 + tt;
+            const float* kt = st.k + tt * DK;
+            const float* qt = st.q + tt * DK;
+            const float* at = st.a + tt * DK;
+            const float bt = st.beta[tt];
             // B1: dS += q do^T; column sums of S' k = P (alpha k) (for w) and of dS k (for du)
             float doj[L::CPL];
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) doj[c] = tv.dout[lane + 32 * c];
+            for (int c = 0; c < L::CPL; ++c) doj[c] = st.dout[tt * DV + lane + 32 * c];
             float pw[L::CPL], pdu[L::CPL];
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
-                const float kk = tv.k[i], qq = tv.q[i], ak = tv.alpha[i] * kk;
+                const float kk = kt[i], qq = qt[i], ak = at[i] * kk;
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
                     dS[r][c] = fmaf(qq, doj[c], dS[r][c]);
@@ -524,17 +583,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 float s = 0.f;
 #pragma unroll
                 for (int w2 = 0; w2 < kBwdWarps; ++w2) s += part[w2][tid];
-                const float wj = tv.v[tid] - s;
-                tv.w[tid] = wj;
-                tv.u[tid] = tv.beta * wj;
+                const float wj = st.v[tt * DV + tid] - s;
+                w_s[tid] = wj;
+                u_s[tid] = bt * wj;
             } else if (tid >= 256 && tid < 256 + DV) {
                 const int j = tid - 256;
                 float d = 0.f;
 #pragma unroll
                 for (int w2 = 0; w2 < kBwdWarps; ++w2) d += part2[w2][j];
-                tv.du[j] = d;
+                du_s[j] = d;
                 const size_t vo = ((size_t)t * p.H + h) * DV + j;
-                static_cast<IO*>(p.dv)[vo] = from_f32<IO>(tv.beta * d);
+                static_cast<IO*>(p.dv)[vo] = from_f32<IO>(bt * d);
             }
             __syncthreads();
             // B3: per element.  With S' = Diag(alpha) P and S_t = S' + k u^T the row sums are
@@ -546,8 +605,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
             float ud = 0.f;
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) {
-                uj[c] = tv.u[lane + 32 * c];
-                bduj[c] = tv.beta * tv.du[lane + 32 * c];
+                uj[c] = u_s[lane + 32 * c];
+                bduj[c] = bt * du_s[lane + 32 * c];
                 ud = fmaf(uj[c], doj[c], ud);
             }
             float vals[32];  // [quantity][row]: 3 x RPW used, the rest zero
@@ -556,7 +615,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
                 const int i = warp * L::RPW + r;
-                const float a = tv.alpha[i], kk = tv.k[i];
+                const float a = at[i], kk = kt[i];
                 float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
@@ -571,6 +630,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 vals[8 + r] = fmaf(-a, s3, s2);
                 vals[16 + r] = s4;
             }
+            if (tt > 0) load_snap(tt - 1);  // P is dead from here on: fetch the next one
             // sum over the 32 lanes, halving the values each step: lane l ends with value l
 #pragma unroll
             for (int m = 16; m >= 1; m >>= 1) {
@@ -588,13 +648,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 const int qn = lane >> 3, r = lane & 7;
                 if (qn < 3 && r < L::RPW) {
                     const int i = warp * L::RPW + r;
-                    rowv[qn][i] = qn == 0 ? fmaf(tv.k[i], ud, vals[0]) : vals[0];
+                    rowv[qn][i] = qn == 0 ? fmaf(kt[i], ud, vals[0]) : vals[0];
                 }
             }
             if (warp == kBwdWarps - 1) {  // dbeta = du . w
                 float wdu = 0.f;
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c) wdu = fmaf(tv.du[lane + 32 * c], tv.w[lane + 32 * c], wdu);
+                for (int c = 0; c < L::CPL; ++c) wdu = fmaf(du_s[lane + 32 * c], w_s[lane + 32 * c], wdu);
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
                 if (lane == 0) static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(wdu);
@@ -603,9 +663,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
             // B4: per key channel: dq, dk, dz and the dA_log partial
             if (tid < DK) {
                 const size_t ko = ((size_t)t * p.H + h) * DK + tid;
-                const float x = tv.x[tid];
+                const float x = st.x[tt * DK + tid];
                 const float s = 1.0f / (1.0f + expf(-x));
-                const float dx = rowv[2][tid] * tv.alpha[tid] * p.g_min * s * (1.0f - s);
+                const float dx = rowv[2][tid] * at[tid] * p.g_min * s * (1.0f - s);
                 static_cast<IO*>(p.dq)[ko] = from_f32<IO>(rowv[0][tid]);
                 static_cast<IO*>(p.dk)[ko] = from_f32<IO>(rowv[1][tid]);
                 static_cast<IO*>(p.dz)[ko] = from_f32<IO>(dx * scale);
@@ -624,7 +684,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
             for (int w2 = 0; w2 < DK / 32; ++w2) s2 += red[w2];
             p.dA_item[it] = s2;
         }
-        __syncthreads();
     }
 }
 
@@ -646,10 +705,22 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, false>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
+    constexpr int smem_fwdtrans = stage_floats<DK, DV>(false, false, true, false) * 4;
+    constexpr int smem_phi = stage_floats<DK, DV>(true, false, false, true) * 4;
+    constexpr int smem_item = stage_floats<DK, DV>(true, true, true, true) * 4;
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_fwdtrans_kernel<IO, DK, DV>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_fwdtrans);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_phi_kernel<IO, DK, DV>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_phi);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bwd_item_kernel<IO, DK, DV>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_item);
     if (e != cudaSuccess) return e;
     {
         ProfScope prof("bwd_fwdtrans_kernel", stream);
-        bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, 0, stream>>>(p);
+        bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_fwdtrans, stream>>>(p);
     }
     {
         ProfScope prof("bwd_fchain_kernel", stream);
@@ -657,7 +728,7 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream
     }
     {
         ProfScope prof("bwd_phi_kernel", stream);
-        bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, 0, stream>>>(p);
+        bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_phi, stream>>>(p);
     }
     {
         ProfScope prof("bwd_chain_kernel", stream);
@@ -665,7 +736,7 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream
     }
     {
         ProfScope prof("bwd_item_kernel", stream);
-        bwd_item_kernel<IO, DK, DV><<<grid_items, kBwdThreads, 0, stream>>>(p);
+        bwd_item_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_item, stream>>>(p);
     }
     return cudaGetLastError();
 }
