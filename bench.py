@@ -410,9 +410,14 @@ def bench_backward(dev, stream, d, sp, peaks, reps=1):
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     ms = ev0.elapsed_time(ev1) / reps
+    kda.profile_begin()
+    run()
+    torch.cuda.synchronize(dev)
+    split = {k: round(v[1], 3) for k, v in kda.profile_end().items()}
     return {"ms_per_call": ms, "tokens_per_s": T_ / (ms / 1e3), "T": T_, "H": H_, "d": dk,
-            "form": "token-level reverse recurrence on CUDA cores (serial over tokens)",
-            "kernels": ["bwd_ckpt_kernel", "bwd_kernel", "bwd_dA_kernel"]}
+            "form": "parallel over 64-token chunks on CUDA cores: per-chunk forward maps and "
+                    "gradient transfer matrices, two short chains over chunks, per-chunk reverse",
+            "kernel_ms": split}
 
 
 def bench_gate_comparison(dev, stream, d, sp, o, S_out, bounded_ms, reps=2):

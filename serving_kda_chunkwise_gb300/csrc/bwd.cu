@@ -171,6 +171,21 @@ __device__ __forceinline__ void item_of(const BwdParams& p, int64_t it, int& h, 
     rows = e.w;
 }
 
+// a warp's RPW consecutive rows of a staged [DK] vector, as 16-byte shared-memory loads
+template <int RPW>
+__device__ __forceinline__ void load_rows(const float* v, int warp, float (&out)[RPW]) {
+    static_assert(RPW % 4 == 0, "rows per warp");
+    const float4* v4 = reinterpret_cast<const float4*>(v + warp * RPW);
+#pragma unroll
+    for (int x = 0; x < RPW / 4; ++x) {
+        const float4 f = v4[x];
+        out[4 * x] = f.x;
+        out[4 * x + 1] = f.y;
+        out[4 * x + 2] = f.z;
+        out[4 * x + 3] = f.w;
+    }
+}
+
 template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
@@ -213,10 +228,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams
                 pb[c] = 0.f;
                 doj[c] = dot[lane + 32 * c];
             }
+            float kr[L::RPW], qr[L::RPW];
+            load_rows<L::RPW>(kt, warp, kr);
+            load_rows<L::RPW>(qt, warp, qr);
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const int i = warp * L::RPW + r;
-                const float kk = kt[i], qq = qt[i];
+                const float kk = kr[r], qq = qr[r];
 #pragma unroll
                 for (int c = 0; c < CK; ++c) pa[c] = fmaf(Phi[r][c], kk, pa[c]);
 #pragma unroll
@@ -244,10 +261,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams
             __syncthreads();
             // X <- Diag(alpha) (X - beta k du^T) for X = Phi and Psi
             const float bt = st.beta[tt];
+            float ar[L::RPW];
+            load_rows<L::RPW>(at, warp, ar);
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const int i = warp * L::RPW + r;
-                const float a = at[i], bk = bt * kt[i];
+                const float a = ar[r], bk = bt * kr[r];
 #pragma unroll
                 for (int c = 0; c < CK; ++c) Phi[r][c] = a * fmaf(-bk, duA[b][lane + 32 * c], Phi[r][c]);
 #pragma unroll
@@ -307,10 +325,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
             for (int c = 0; c < CK; ++c) pa[c] = 0.f;
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) pb[c] = 0.f;
+            float kr[L::RPW], ar[L::RPW];
+            load_rows<L::RPW>(kt, warp, kr);
+            load_rows<L::RPW>(at, warp, ar);
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const int i = warp * L::RPW + r;
-                const float a = at[i], kk = kt[i];
+                const float a = ar[r], kk = kr[r];
 #pragma unroll
                 for (int c = 0; c < CK; ++c) {
                     A[r][c] *= a;
@@ -342,7 +362,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fwdtrans_kernel(const BwdP
             const float bt = st.beta[tt];
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const float bk = bt * kt[warp * L::RPW + r];
+                const float bk = bt * kr[r];
 #pragma unroll
                 for (int c = 0; c < CK; ++c) A[r][c] = fmaf(-bk, wA[b][lane + 32 * c], A[r][c]);
 #pragma unroll
@@ -501,19 +521,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                                 S[(e + 3) / L::CPL][(e + 3) % L::CPL]);
             }
             if (tt + 1 == rows) break;  // the last token's state is not needed
-            const float* kt = st.k + tt * DK;
-            const float* at = st.a + tt * DK;
+            float kr[L::RPW], ar[L::RPW];
+            load_rows<L::RPW>(st.k + tt * DK, warp, kr);
+            load_rows<L::RPW>(st.a + tt * DK, warp, ar);
             float pc[L::CPL];
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) pc[c] = 0.f;
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const int i = warp * L::RPW + r;
-                const float a = at[i], kk = kt[i];
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
-                    S[r][c] *= a;
-                    pc[c] = fmaf(S[r][c], kk, pc[c]);
+                    S[r][c] *= ar[r];
+                    pc[c] = fmaf(S[r][c], kr[r], pc[c]);
                 }
             }
 #pragma unroll
@@ -526,12 +545,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 u_s[tid] = st.beta[tt] * (st.v[tt * DV + tid] - s);
             }
             __syncthreads();
+            float uc[L::CPL];
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r) {
-                const float kk = kt[warp * L::RPW + r];
+            for (int c = 0; c < L::CPL; ++c) uc[c] = u_s[lane + 32 * c];
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c) S[r][c] = fmaf(kk, u_s[lane + 32 * c], S[r][c]);
-            }
+            for (int r = 0; r < L::RPW; ++r)
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) S[r][c] = fmaf(kr[r], uc[c], S[r][c]);
         }
         // ---- back through the chunk's tokens
         float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
@@ -561,15 +581,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
             float pw[L::CPL], pdu[L::CPL];
 #pragma unroll
             for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
+            {
+                float kr[L::RPW], qr[L::RPW], ar[L::RPW];
+                load_rows<L::RPW>(kt, warp, kr);
+                load_rows<L::RPW>(qt, warp, qr);
+                load_rows<L::RPW>(at, warp, ar);
 #pragma unroll
-            for (int r = 0; r < L::RPW; ++r) {
-                const int i = warp * L::RPW + r;
-                const float kk = kt[i], qq = qt[i], ak = at[i] * kk;
+                for (int r = 0; r < L::RPW; ++r) {
+                    const float ak = ar[r] * kr[r];
 #pragma unroll
-                for (int c = 0; c < L::CPL; ++c) {
-                    dS[r][c] = fmaf(qq, doj[c], dS[r][c]);
-                    pw[c] = fmaf(P[r][c], ak, pw[c]);
-                    pdu[c] = fmaf(dS[r][c], kk, pdu[c]);
+                    for (int c = 0; c < L::CPL; ++c) {
+                        dS[r][c] = fmaf(qr[r], doj[c], dS[r][c]);
+                        pw[c] = fmaf(P[r][c], ak, pw[c]);
+                        pdu[c] = fmaf(dS[r][c], kr[r], pdu[c]);
+                    }
                 }
             }
 #pragma unroll
@@ -612,10 +637,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
             float vals[32];  // [quantity][row]: 3 x RPW used, the rest zero
 #pragma unroll
             for (int x = 0; x < 32; ++x) vals[x] = 0.f;
+            float kr[L::RPW], ar[L::RPW];
+            load_rows<L::RPW>(kt, warp, kr);
+            load_rows<L::RPW>(at, warp, ar);
 #pragma unroll
             for (int r = 0; r < L::RPW; ++r) {
-                const int i = warp * L::RPW + r;
-                const float a = at[i], kk = kt[i];
+                const float a = ar[r], kk = kr[r];
                 float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) {
