@@ -65,7 +65,7 @@ struct BwdParams {
     float* phi;          // [chunks][H][DK][DK]
     float* psi;          // [chunks][H][DK][DV]
     float* dsend;        // [chunks][H][DK][DV]: the state's gradient at each chunk end
-    float* snap;         // [grid][64][DK][DV]: per-CTA scratch
+    float* snap;         // [grid][16][DK][DV]: per-CTA scratch (sub-block starts, token states)
     float* dA_item;      // [chunks][H]
     unsigned* err;
 };
@@ -467,11 +467,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_chain_kernel(const BwdPara
     }
 }
 
-// Per (chunk, head): the chunk's forward from its checkpoint, keeping the state before each
-// token in per-CTA scratch (thread-private float4s, laid out [token][float4][thread] so that
-// every store and load is coalesced), then the reverse rules token by token from the chunk's
-// dS.  Two barriers per forward token and three per reverse token, double-buffered where a
-// shared vector is rewritten before every reader has passed the next barrier.
+// Per (chunk, head): the reverse rules token by token from the chunk's dS, with the state
+// before each token recomputed from the chunk's checkpoint by sub-blocks of kSB tokens: one
+// forward pass keeps the state at every sub-block start (and the states of the last
+// sub-block); each earlier sub-block is re-run from its start just before it is reversed.
+// Per-CTA scratch: kNB sub-block starts and kSB token states, thread-private float4s laid out
+// [slot][float4][thread] so that every store and load is coalesced; the kSB states that are
+// written and read back within a sub-block stay in L2.  Two barriers per forward token and
+// three per reverse token.
+constexpr int kSB = 8;
+constexpr int kNB = kBwdC / kSB;
+
 template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
@@ -486,7 +492,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
     __shared__ float rowv[3][DK];  // dq, dk, dalpha
     __shared__ float red[kBwdWarps];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float4* snap = reinterpret_cast<float4*>(p.snap) + (size_t)blockIdx.x * kBwdC * NV4 * kBwdThreads;
+    float4* bnd = reinterpret_cast<float4*>(p.snap) +
+                  (size_t)blockIdx.x * (kNB + kSB) * NV4 * kBwdThreads + tid;
+    float4* snp = bnd + (size_t)kNB * NV4 * kBwdThreads;
+    auto put = [&](float4* base, int slot, const float (&X)[L::RPW][L::CPL]) {
+#pragma unroll
+        for (int x = 0; x < NV4; ++x) {
+            const int e = 4 * x;
+            base[((size_t)slot * NV4 + x) * kBwdThreads] =
+                make_float4(X[e / L::CPL][e % L::CPL], X[(e + 1) / L::CPL][(e + 1) % L::CPL],
+                            X[(e + 2) / L::CPL][(e + 2) % L::CPL],
+                            X[(e + 3) / L::CPL][(e + 3) % L::CPL]);
+        }
+    };
+    auto get = [&](const float4* base, int slot, float (&X)[L::RPW][L::CPL]) {
+#pragma unroll
+        for (int x = 0; x < NV4; ++x) {
+            const float4 f = base[((size_t)slot * NV4 + x) * kBwdThreads];
+            const int e = 4 * x;
+            X[e / L::CPL][e % L::CPL] = f.x;
+            X[(e + 1) / L::CPL][(e + 1) % L::CPL] = f.y;
+            X[(e + 2) / L::CPL][(e + 2) % L::CPL] = f.z;
+            X[(e + 3) / L::CPL][(e + 3) % L::CPL] = f.w;
+        }
+    };
     const int64_t items = (int64_t)p.chunk_off[p.N] * p.H;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
         int h, rows;
@@ -509,18 +538,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
                 S[r][c] = src[o];
             }
         __syncthreads();
-        // ---- the chunk's forward from its checkpoint, keeping the state before each token
-        for (int tt = 0; tt < rows; ++tt) {
-            float4* dst = snap + (size_t)tt * NV4 * kBwdThreads + tid;
-#pragma unroll
-            for (int x = 0; x < NV4; ++x) {
-                const int e = 4 * x;
-                dst[x * kBwdThreads] =
-                    make_float4(S[e / L::CPL][e % L::CPL], S[(e + 1) / L::CPL][(e + 1) % L::CPL],
-                                S[(e + 2) / L::CPL][(e + 2) % L::CPL],
-                                S[(e + 3) / L::CPL][(e + 3) % L::CPL]);
-            }
-            if (tt + 1 == rows) break;  // the last token's state is not needed
+        // one forward token on S (S <- Diag(alpha) S + k u^T, u = beta (v - S'^T k))
+        auto fwd_step = [&](int tt) {
             float kr[L::RPW], ar[L::RPW];
             load_rows<L::RPW>(st.k + tt * DK, warp, kr);
             load_rows<L::RPW>(st.a + tt * DK, warp, ar);
@@ -552,151 +571,158 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_item_kernel(const BwdParam
             for (int r = 0; r < L::RPW; ++r)
 #pragma unroll
                 for (int c = 0; c < L::CPL; ++c) S[r][c] = fmaf(kr[r], uc[c], S[r][c]);
-        }
-        // ---- back through the chunk's tokens
-        float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
-        auto load_snap = [&](int tt) {
-            const float4* ps = snap + (size_t)tt * NV4 * kBwdThreads + tid;
-#pragma unroll
-            for (int x = 0; x < NV4; ++x) {
-                const float4 f = ps[x * kBwdThreads];
-                const int e = 4 * x;
-                P[e / L::CPL][e % L::CPL] = f.x;
-                P[(e + 1) / L::CPL][(e + 1) % L::CPL] = f.y;
-                P[(e + 2) / L::CPL][(e + 2) % L::CPL] = f.z;
-                P[(e + 3) / L::CPL][(e + 3) % L::CPL] = f.w;
-            }
         };
-        if (rows > 0) load_snap(rows - 1);
-        for (int tt = rows - 1; tt >= 0; --tt) {
-            const int64_t t = t0 + tt;
-            const float* kt = st.k + tt * DK;
-            const float* qt = st.q + tt * DK;
-            const float* at = st.a + tt * DK;
-            const float bt = st.beta[tt];
-            // B1: dS += q do^T; column sums of S' k = P (alpha k) (for w) and of dS k (for du)
-            float doj[L::CPL];
+        // ---- first forward pass: the sub-block starts, and the last sub-block's states
+        const int nb = (rows + kSB - 1) / kSB;
+        for (int tt = 0; tt < rows; ++tt) {
+            if (tt % kSB == 0 && tt / kSB < nb - 1) put(bnd, tt / kSB, S);
+            if (tt >= (nb - 1) * kSB) put(snp, tt % kSB, S);
+            if (tt + 1 == rows) break;  // the last token's state is not needed
+            fwd_step(tt);
+        }
+        // ---- back through the chunk's tokens, sub-block by sub-block from the last
+        float P[L::RPW][L::CPL];  // S_{t-1}, this thread's part
+        for (int b = nb - 1; b >= 0; --b) {
+            const int lo = b * kSB, hi = min(lo + kSB, rows);
+            if (b < nb - 1) {  // re-run the sub-block from its start, keeping its states
+                get(bnd, b, S);
+                for (int tt = lo; tt < hi; ++tt) {
+                    put(snp, tt - lo, S);
+                    if (tt + 1 == hi) break;
+                    fwd_step(tt);
+                }
+            }
+            get(snp, hi - 1 - lo, P);
+            for (int tt = hi - 1; tt >= lo; --tt) {
+                const int64_t t = t0 + tt;
+                const float* kt = st.k + tt * DK;
+                const float* qt = st.q + tt * DK;
+                const float* at = st.a + tt * DK;
+                const float bt = st.beta[tt];
+                // B1: dS += q do^T; column sums of S' k = P (alpha k) (for w) and of dS k (for du)
+                float doj[L::CPL];
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) doj[c] = st.dout[tt * DV + lane + 32 * c];
-            float pw[L::CPL], pdu[L::CPL];
+                for (int c = 0; c < L::CPL; ++c) doj[c] = st.dout[tt * DV + lane + 32 * c];
+                float pw[L::CPL], pdu[L::CPL];
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
-            {
-                float kr[L::RPW], qr[L::RPW], ar[L::RPW];
+                for (int c = 0; c < L::CPL; ++c) pw[c] = pdu[c] = 0.f;
+                {
+                    float kr[L::RPW], qr[L::RPW], ar[L::RPW];
+                    load_rows<L::RPW>(kt, warp, kr);
+                    load_rows<L::RPW>(qt, warp, qr);
+                    load_rows<L::RPW>(at, warp, ar);
+#pragma unroll
+                    for (int r = 0; r < L::RPW; ++r) {
+                        const float ak = ar[r] * kr[r];
+#pragma unroll
+                        for (int c = 0; c < L::CPL; ++c) {
+                            dS[r][c] = fmaf(qr[r], doj[c], dS[r][c]);
+                            pw[c] = fmaf(P[r][c], ak, pw[c]);
+                            pdu[c] = fmaf(dS[r][c], kr[r], pdu[c]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    part[warp][lane + 32 * c] = pw[c];
+                    part2[warp][lane + 32 * c] = pdu[c];
+                }
+                __syncthreads();
+                // B2: w, u per column (first warps), du and dv per column (middle warps)
+                if (tid < DV) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < kBwdWarps; ++w2) s += part[w2][tid];
+                    const float wj = st.v[tt * DV + tid] - s;
+                    w_s[tid] = wj;
+                    u_s[tid] = bt * wj;
+                } else if (tid >= 256 && tid < 256 + DV) {
+                    const int j = tid - 256;
+                    float d = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < kBwdWarps; ++w2) d += part2[w2][j];
+                    du_s[j] = d;
+                    const size_t vo = ((size_t)t * p.H + h) * DV + j;
+                    static_cast<IO*>(p.dv)[vo] = from_f32<IO>(bt * d);
+                }
+                __syncthreads();
+                // B3: per element.  With S' = Diag(alpha) P and S_t = S' + k u^T the row sums are
+                //   dq_i     = alpha_i sum_j P_ij do_j + k_i (u . do)
+                //   dk_i     = sum_j dS_ij u_j - alpha_i sum_j P_ij beta du_j
+                //   dalpha_i = sum_j (dS_ij - k_i beta du_j) P_ij
+                // the per-row factors are applied to each lane's partial before the lanes are summed.
+                float uj[L::CPL], bduj[L::CPL];
+                float ud = 0.f;
+#pragma unroll
+                for (int c = 0; c < L::CPL; ++c) {
+                    uj[c] = u_s[lane + 32 * c];
+                    bduj[c] = bt * du_s[lane + 32 * c];
+                    ud = fmaf(uj[c], doj[c], ud);
+                }
+                float vals[32];  // [quantity][row]: 3 x RPW used, the rest zero
+#pragma unroll
+                for (int x = 0; x < 32; ++x) vals[x] = 0.f;
+                float kr[L::RPW], ar[L::RPW];
                 load_rows<L::RPW>(kt, warp, kr);
-                load_rows<L::RPW>(qt, warp, qr);
                 load_rows<L::RPW>(at, warp, ar);
 #pragma unroll
                 for (int r = 0; r < L::RPW; ++r) {
-                    const float ak = ar[r] * kr[r];
+                    const float a = ar[r], kk = kr[r];
+                    float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
 #pragma unroll
                     for (int c = 0; c < L::CPL; ++c) {
-                        dS[r][c] = fmaf(qr[r], doj[c], dS[r][c]);
-                        pw[c] = fmaf(P[r][c], ak, pw[c]);
-                        pdu[c] = fmaf(dS[r][c], kr[r], pdu[c]);
+                        s1 = fmaf(P[r][c], doj[c], s1);
+                        s2 = fmaf(dS[r][c], uj[c], s2);
+                        s3 = fmaf(P[r][c], bduj[c], s3);
+                        const float dsp = fmaf(-kk, bduj[c], dS[r][c]);
+                        s4 = fmaf(dsp, P[r][c], s4);
+                        dS[r][c] = a * dsp;
+                    }
+                    vals[r] = a * s1;
+                    vals[8 + r] = fmaf(-a, s3, s2);
+                    vals[16 + r] = s4;
+                }
+                if (tt > lo) get(snp, tt - 1 - lo, P);  // P is dead from here on: fetch the next one
+                // sum over the 32 lanes, halving the values each step: lane l ends with value l
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) {
+                    const bool up = (lane & m) != 0;
+#pragma unroll
+                    for (int x = 0; x < m; ++x) {
+                        const float send = up ? vals[x] : vals[x + m];
+                        const float keep = up ? vals[x + m] : vals[x];
+                        vals[x] = keep + __shfl_xor_sync(0xffffffffu, send, m);
                     }
                 }
-            }
 #pragma unroll
-            for (int c = 0; c < L::CPL; ++c) {
-                part[warp][lane + 32 * c] = pw[c];
-                part2[warp][lane + 32 * c] = pdu[c];
-            }
-            __syncthreads();
-            // B2: w, u per column (first warps), du and dv per column (middle warps)
-            if (tid < DV) {
-                float s = 0.f;
-#pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) s += part[w2][tid];
-                const float wj = st.v[tt * DV + tid] - s;
-                w_s[tid] = wj;
-                u_s[tid] = bt * wj;
-            } else if (tid >= 256 && tid < 256 + DV) {
-                const int j = tid - 256;
-                float d = 0.f;
-#pragma unroll
-                for (int w2 = 0; w2 < kBwdWarps; ++w2) d += part2[w2][j];
-                du_s[j] = d;
-                const size_t vo = ((size_t)t * p.H + h) * DV + j;
-                static_cast<IO*>(p.dv)[vo] = from_f32<IO>(bt * d);
-            }
-            __syncthreads();
-            // B3: per element.  With S' = Diag(alpha) P and S_t = S' + k u^T the row sums are
-            //   dq_i     = alpha_i sum_j P_ij do_j + k_i (u . do)
-            //   dk_i     = sum_j dS_ij u_j - alpha_i sum_j P_ij beta du_j
-            //   dalpha_i = sum_j (dS_ij - k_i beta du_j) P_ij
-            // the per-row factors are applied to each lane's partial before the lanes are summed.
-            float uj[L::CPL], bduj[L::CPL];
-            float ud = 0.f;
-#pragma unroll
-            for (int c = 0; c < L::CPL; ++c) {
-                uj[c] = u_s[lane + 32 * c];
-                bduj[c] = bt * du_s[lane + 32 * c];
-                ud = fmaf(uj[c], doj[c], ud);
-            }
-            float vals[32];  // [quantity][row]: 3 x RPW used, the rest zero
-#pragma unroll
-            for (int x = 0; x < 32; ++x) vals[x] = 0.f;
-            float kr[L::RPW], ar[L::RPW];
-            load_rows<L::RPW>(kt, warp, kr);
-            load_rows<L::RPW>(at, warp, ar);
-#pragma unroll
-            for (int r = 0; r < L::RPW; ++r) {
-                const float a = ar[r], kk = kr[r];
-                float s1 = 0.f, s2 = 0.f, s3 = 0.f, s4 = 0.f;
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c) {
-                    s1 = fmaf(P[r][c], doj[c], s1);
-                    s2 = fmaf(dS[r][c], uj[c], s2);
-                    s3 = fmaf(P[r][c], bduj[c], s3);
-                    const float dsp = fmaf(-kk, bduj[c], dS[r][c]);
-                    s4 = fmaf(dsp, P[r][c], s4);
-                    dS[r][c] = a * dsp;
+                for (int off = 16; off > 0; off >>= 1) ud += __shfl_xor_sync(0xffffffffu, ud, off);
+                {
+                    const int qn = lane >> 3, r = lane & 7;
+                    if (qn < 3 && r < L::RPW) {
+                        const int i = warp * L::RPW + r;
+                        rowv[qn][i] = qn == 0 ? fmaf(kt[i], ud, vals[0]) : vals[0];
+                    }
                 }
-                vals[r] = a * s1;
-                vals[8 + r] = fmaf(-a, s3, s2);
-                vals[16 + r] = s4;
-            }
-            if (tt > 0) load_snap(tt - 1);  // P is dead from here on: fetch the next one
-            // sum over the 32 lanes, halving the values each step: lane l ends with value l
+                if (warp == kBwdWarps - 1) {  // dbeta = du . w
+                    float wdu = 0.f;
 #pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) {
-                const bool up = (lane & m) != 0;
+                    for (int c = 0; c < L::CPL; ++c) wdu = fmaf(du_s[lane + 32 * c], w_s[lane + 32 * c], wdu);
 #pragma unroll
-                for (int x = 0; x < m; ++x) {
-                    const float send = up ? vals[x] : vals[x + m];
-                    const float keep = up ? vals[x + m] : vals[x];
-                    vals[x] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+                    for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
+                    if (lane == 0) static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(wdu);
                 }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ud += __shfl_xor_sync(0xffffffffu, ud, off);
-            {
-                const int qn = lane >> 3, r = lane & 7;
-                if (qn < 3 && r < L::RPW) {
-                    const int i = warp * L::RPW + r;
-                    rowv[qn][i] = qn == 0 ? fmaf(kt[i], ud, vals[0]) : vals[0];
+                __syncthreads();
+                // B4: per key channel: dq, dk, dz and the dA_log partial
+                if (tid < DK) {
+                    const size_t ko = ((size_t)t * p.H + h) * DK + tid;
+                    const float x = st.x[tt * DK + tid];
+                    const float s = 1.0f / (1.0f + expf(-x));
+                    const float dx = rowv[2][tid] * at[tid] * p.g_min * s * (1.0f - s);
+                    static_cast<IO*>(p.dq)[ko] = from_f32<IO>(rowv[0][tid]);
+                    static_cast<IO*>(p.dk)[ko] = from_f32<IO>(rowv[1][tid]);
+                    static_cast<IO*>(p.dz)[ko] = from_f32<IO>(dx * scale);
+                    dA_acc = fmaf(dx, x, dA_acc);
                 }
-            }
-            if (warp == kBwdWarps - 1) {  // dbeta = du . w
-                float wdu = 0.f;
-#pragma unroll
-                for (int c = 0; c < L::CPL; ++c) wdu = fmaf(du_s[lane + 32 * c], w_s[lane + 32 * c], wdu);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) wdu += __shfl_xor_sync(0xffffffffu, wdu, off);
-                if (lane == 0) static_cast<IO*>(p.dbeta)[(size_t)t * p.H + h] = from_f32<IO>(wdu);
-            }
-            __syncthreads();
-            // B4: per key channel: dq, dk, dz and the dA_log partial
-            if (tid < DK) {
-                const size_t ko = ((size_t)t * p.H + h) * DK + tid;
-                const float x = st.x[tt * DK + tid];
-                const float s = 1.0f / (1.0f + expf(-x));
-                const float dx = rowv[2][tid] * at[tid] * p.g_min * s * (1.0f - s);
-                static_cast<IO*>(p.dq)[ko] = from_f32<IO>(rowv[0][tid]);
-                static_cast<IO*>(p.dk)[ko] = from_f32<IO>(rowv[1][tid]);
-                static_cast<IO*>(p.dz)[ko] = from_f32<IO>(dx * scale);
-                dA_acc = fmaf(dx, x, dA_acc);
             }
         }
         // this (chunk, head)'s dA_log partial
@@ -779,8 +805,8 @@ int sm_count() {
 
 // Workspace, for at most C = T/64 + N chunks: chunk offsets [N + 1] and table [C]; the state
 // at each chunk start, Psi and the state's gradient at each chunk end [C][H][dk][dv] fp32;
-// Phi [C][H][dk][dk] fp32; 64 states of scratch per CTA of the per-chunk kernel; [C][H]
-// dA_log partials.
+// Phi [C][H][dk][dk] fp32; kNB + kSB = 16 states of scratch per CTA of the per-chunk kernel;
+// [C][H] dA_log partials.
 struct BwdLayoutWs {
     size_t off, tab, ckpt, phi, psi, dsend, snap, dA, total;
 };
@@ -796,7 +822,7 @@ BwdLayoutWs bwd_ws_layout(int64_t T_total, int N, int H, int dk, int dv, int gri
     w.phi = o;   o += al(C * H * dk * dk * 4);
     w.psi = o;   o += al(C * H * dk * dv * 4);
     w.dsend = o; o += al(C * H * dk * dv * 4);
-    w.snap = o;  o += al((size_t)grid_items * kBwdC * dk * dv * 4);
+    w.snap = o;  o += al((size_t)grid_items * (kNB + kSB) * dk * dv * 4);
     w.dA = o;    o += al(C * H * 4);
     w.total = o;
     return w;
