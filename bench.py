@@ -317,7 +317,7 @@ def run_ours(args, rank, world, local_rank, dist):
     # gate and with the unbounded gate it replaces
     gcmp = bench_gate_comparison(dev, stream, d, sp, o, S_out, ms_per_step)
 
-    # gradients of the same forward (token-level backward), the workload's v standing in for
+    # gradients of the same forward (backward parallel over chunks), the workload's v standing in for
     # the upstream gradient of o
     bw = bench_backward(dev, stream, d, sp, peaks) if not args.no_backward else None
 
