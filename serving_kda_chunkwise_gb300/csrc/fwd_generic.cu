@@ -27,7 +27,7 @@ namespace kda {
 namespace {
 
 constexpr int kC = 64;      // chunk length
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kDvs = 32;    // d_v columns per CTA
 
 template <int DK>
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kThreads) fwd_generic_kernel(FwdArgs a) {
     }
 
     const int j = tid % kDvs;     // column owned in the state phases
-    const int rg = tid / kDvs;    // row group (0..7)
+    const int rg = tid / kDvs;    // row group (0 .. kThreads / 32 - 1)
 
     for (int64_t t0 = t_begin; t0 < t_end; t0 += kC) {
         const int L = (int)((t_end - t0) < kC ? (t_end - t0) : kC);
