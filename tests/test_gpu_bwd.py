@@ -34,14 +34,15 @@ def _close(d, ref, dtype, what):
         assert bf16_rms_err(d, ref) <= BF16_RMS_TOL, what
 
 
-def _run(kda, lengths, H, d, dtype, seed, with_dS=True):
+def _run(kda, lengths, H, d, dtype, seed, with_dS=True, dv=None):
     import torch
-    inp = inputs.forward_inputs(seed=seed, lengths=lengths, H=H, dk=d, dv=d, dtype=dtype,
+    dv = d if dv is None else dv
+    inp = inputs.forward_inputs(seed=seed, lengths=lengths, H=H, dk=d, dv=dv, dtype=dtype,
                                 with_state=True)
     rng = np.random.default_rng(seed + 1)
     T, N = int(inp.cu_seqlens[-1]), len(lengths)
-    do = inputs.store(rng.standard_normal((T, H, d)).astype(np.float32), dtype)
-    dS = rng.standard_normal((N, H, d, d)).astype(np.float32) if with_dS else None
+    do = inputs.store(rng.standard_normal((T, H, dv)).astype(np.float32), dtype)
+    dS = rng.standard_normal((N, H, d, dv)).astype(np.float32) if with_dS else None
     dev = {nm: getattr(inp, nm).as_torch("cuda") for nm in ("q", "k", "v", "beta", "z")}
     g = kda.bwd(dev["q"], dev["k"], dev["v"], dev["beta"], dev["z"],
                 torch.from_numpy(inp.A_log).cuda(), inp.g_min, do.as_torch("cuda"),
@@ -75,6 +76,13 @@ def _run(kda, lengths, H, d, dtype, seed, with_dS=True):
 @pytest.mark.parametrize("dtype,d", [("f32", 64), ("f32", 128), ("bf16", 128)])
 def test_matches_oracle(kda, dtype, d):
     _run(kda, [70, 0, 129, 1], H=2, d=d, dtype=dtype, seed=71)
+
+
+@pytest.mark.parametrize("dtype,dk,dv", [("f32", 64, 128), ("f32", 128, 64), ("bf16", 64, 64)])
+def test_other_head_sizes(kda, dtype, dk, dv):
+    """d_k != d_v (the state's rows and columns split differently over the threads) and bf16
+    at d = 64."""
+    _run(kda, [90, 17], H=2, d=dk, dv=dv, dtype=dtype, seed=75)
 
 
 def test_without_final_state_gradient(kda):
