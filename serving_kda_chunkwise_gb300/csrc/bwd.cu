@@ -11,13 +11,16 @@
 //   dz = dx e^{A_h};   dA_h += sum dx x.
 // The pages print no backward; these are the derivatives of the forward they define.
 //
-// On CUDA cores in fp32, parallel over chunks.  The gradient of the state is the only serial
-// quantity, and over one 64-token chunk it is affine: going back through token t maps
-// dS_t to B_t (dS_t + q_t do_t^T) with B_t = Diag(alpha_t) (I - beta_t k_t k_t^T), so
+// On CUDA cores in fp32, parallel over chunks.  The state and its gradient are the only
+// serial quantities, and over one 64-token chunk both are affine.  Forward, S_t =
+// (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T, so S_(chunk end) =
+// A S_(chunk start) + B.  Backward, going back through token t maps dS_t to
+// B_t (dS_t + q_t do_t^T) with B_t = Diag(alpha_t) (I - beta_t k_t k_t^T), so
 //   dS_(chunk start) = Phi dS_(chunk end) + Psi,  Phi = B_t0 .. B_t1-1,
 //   Psi = sum_t B_t0 .. B_t (q_t do_t^T).
-// Kernels (512 threads; warp w owns rows [w dk/16, (w+1) dk/16) of a state-shaped matrix and
-// lane l its columns l, l + 32, ..; matrices live in registers):
+// Kernels (512 threads; in the per-chunk kernels warp w owns rows [w dk/16, (w+1) dk/16) of a
+// state-shaped matrix and lane l its columns l, l + 32, ..; matrices live in registers, and
+// each chunk's token inputs are staged in shared memory once):
 //   bwd_plan_kernel   chunk offsets of every sequence and a table entry per chunk
 //   bwd_fwdtrans_kernel  per (chunk, head), all in parallel: the chunk's forward map on the
 //                     state, S_end = A S_start + B
@@ -26,9 +29,9 @@
 //   bwd_phi_kernel    per (chunk, head), all in parallel: Phi and Psi of the chunk
 //   bwd_chain_kernel  per (sequence, head, 32-column slice): dS at every chunk end, last
 //                     chunk first (dS <- Phi dS + Psi), and dS0
-//   bwd_item_kernel   per (chunk, head), all in parallel: the chunk's forward from its
-//                     checkpoint (the state before every token kept in per-CTA scratch), then
-//                     the reverse rules above token by token from the chunk's dS
+//   bwd_item_kernel   per (chunk, head), all in parallel: the reverse rules above token by
+//                     token from the chunk's dS, the state before each token recomputed from
+//                     the chunk's checkpoint by 8-token sub-blocks (per-CTA scratch)
 //   bwd_dA_kernel     dA_log[h] = the per-(chunk, head) partial sums in chunk order
 //                     (deterministic)
 #include "kda_common.cuh"
