@@ -101,3 +101,45 @@ def test_long_sequences(kda):
     """Sequences of 2100 and 1000 tokens (33 and 16 chunks, ragged tails): the checkpoints and
     the per-chunk recompute over many chunks."""
     _run(kda, [2100, 1000], H=2, d=128, dtype="bf16", seed=74)
+
+
+def test_full_size_window(kda):
+    """The benchmark's backward shape and launch configuration (one sequence of T = 65536
+    tokens, H = 32, d = 128, bf16, dS_out = 0), with the upstream gradient do nonzero only on
+    tokens [t_a, t_b).  The state's gradient is then exactly zero from t_b on, so every
+    gradient of a token at or after t_b is exactly zero; and the gradients of the tokens in
+    [w0, t_b) are those of the window alone started from the state at w0, which the oracle
+    gives exactly: the C token recurrence over [0, w0), then the reverse-mode oracle over
+    [w0, t_b).  This crosses the two chains over all 1024 chunks (the state at every chunk
+    start, the gradient at every chunk end).  Sampled heads 3 and 29; the window starts and
+    ends inside chunks."""
+    import torch
+    import oracle
+    sp = inputs.workload_spec("fwd_bf16_T65536_H32_d128")
+    d = sp.to_device("cuda")
+    T, H, dk, dv = sp.T, sp.H, sp.dk, sp.dv
+    t_a, t_b = 40013, 40163
+    w0 = t_a - 100
+    rng = np.random.default_rng(76)
+    do_win = inputs.store(rng.standard_normal((t_b - t_a, H, dv)).astype(np.float32), "bf16")
+    do = torch.zeros((T, H, dv), dtype=torch.bfloat16, device="cuda")
+    do[t_a:t_b] = do_win.as_torch("cuda")
+    g = kda.bwd(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], sp.g_min, do,
+                dS_out=torch.zeros((1, H, dk, dv), dtype=torch.float32, device="cuda"), N=1)
+    kda.device_status()
+    for nm in ("dq", "dk", "dv", "dbeta", "dz"):
+        assert torch.count_nonzero(g[nm][t_b:]).item() == 0, f"{nm} after the window"
+    heads = [3, 29]
+    kinds = ("q", "k", "v", "beta", "z")
+    pre = {kind: sp.tokens(kind, 0, w0, heads) for kind in kinds}
+    _, S_w0 = oracle.recurrent(pre["q"], pre["k"], pre["v"], pre["beta"], pre["z"],
+                               sp.A_log[heads], sp.g_min)
+    win = {kind: sp.tokens(kind, w0, t_b, heads) for kind in kinds}
+    do_ref = np.zeros((t_b - w0, len(heads), dv))
+    do_ref[t_a - w0:] = do_win.values[:, heads]
+    ref = kb.backward(win["q"], win["k"], win["v"], win["beta"], win["z"], sp.A_log[heads],
+                      sp.g_min, do_ref, S0=S_w0)
+    for nm in ("dq", "dk", "dv", "dbeta", "dz"):
+        got = g[nm][w0:t_b].float().cpu().numpy()
+        for ii, h in enumerate(heads):
+            _close(got[:, h], ref[nm][:, ii], "bf16", f"{nm} head {h}")
