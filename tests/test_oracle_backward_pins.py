@@ -7,6 +7,8 @@ What pins what:
   finite diffs     central differences of the loss in every input (q, k, v, beta, z, A_log,
                    S0) agree with the returned gradients on tiny problems (a dropped term or
                    a transposed operand in the forward changes one of them)
+  two orderings    the hand-derived reverse of the chunk form (backward_chunked), chunk by
+                   chunk, agrees with the reverse mode through the token recurrence
   closed forms     with beta = 0 and alpha = 1 (z = -inf) the state is S0 throughout, so
                    dq_t = S0 do_t, dS0 = sum_t q_t do_t^T + dS_out, and dv = dk = 0
 """
@@ -80,3 +82,19 @@ def test_closed_form_without_decay_or_writes():
     np.testing.assert_allclose(g["dS0"][0], np.einsum("thi,thj->hij", q, do) + dS[0],
                                rtol=1e-13)
     assert np.all(g["dv"] == 0.0) and np.all(g["dk"] == 0.0)
+
+
+@pytest.mark.parametrize("C", [1, 4, 16, 64])
+def test_chunked_ordering_matches_reverse_mode(C):
+    """Two independent orderings of the same gradients: torch's reverse mode through the
+    token recurrence, and the hand-derived reverse of the chunk form, chunk by chunk.  C = 1
+    reduces the chunk form to the token step; ragged last chunks, an empty sequence and
+    d_k != d_v included."""
+    lengths = [70, 0, 37, 5]
+    q, k, v, beta, z, A, S0, do, dS, cu = _prob(4, sum(lengths), 2, 6, 3, lengths=lengths)
+    ref = kb.backward(q, k, v, beta, z, A, -5.0, do, S0=S0, dS_out=dS, cu_seqlens=cu)
+    got = kb.backward_chunked(q, k, v, beta, z, A, -5.0, do, S0=S0, dS_out=dS, cu_seqlens=cu,
+                              C=C)
+    for nm in ("dq", "dk", "dv", "dbeta", "dz", "dA_log", "dS0"):
+        scale = np.max(np.abs(ref[nm])) if ref[nm].size else 1.0
+        assert np.max(np.abs(got[nm] - ref[nm])) <= 1e-10 * max(scale, 1e-30), nm
