@@ -113,13 +113,14 @@ struct Stage {
     float *k, *q, *x, *a, *v, *dout, *beta;
 };
 
-// carve the arrays out of `base` in a fixed order; returns the floats used
+// the floats a Stage with these arrays occupies (k and alpha always, beta always)
 template <int DK, int DV>
 __host__ __device__ constexpr int stage_floats(bool q, bool x, bool v, bool dout) {
-    return kBwdC * DK * (2 + (q ? 1 : 0) + (x ? 1 : 0)) + kBwdC * DV * ((v ? 1 : 0) + (dout ? 1 : 0)) +
-           kBwdC;
+    return kBwdC * DK * (2 + (q ? 1 : 0) + (x ? 1 : 0)) +
+           kBwdC * DV * ((v ? 1 : 0) + (dout ? 1 : 0)) + kBwdC;
 }
 
+// carve the arrays out of `base` in a fixed order (the layout stage_floats counts)
 template <int DK, int DV>
 __device__ __forceinline__ Stage<DK, DV> stage_carve(float* base, bool q, bool x, bool v,
                                                      bool dout) {
@@ -189,13 +190,15 @@ __device__ __forceinline__ void load_rows(const float* v, int warp, float (&out)
     }
 }
 
+// Phi and Psi of every (chunk, head) in parallel, tokens in reverse from Phi = I, Psi = 0:
+// X <- Diag(alpha) (I - beta k k^T) X per token, and Psi += q do^T before its step.
 template <typename IO, int DK, int DV>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_phi_kernel(const BwdParams p) {
     using L = BwdLayout<DK, DV>;
     constexpr int CK = DK / 32;  // Phi columns per lane
     extern __shared__ __align__(16) float stage_smem[];
     const Stage<DK, DV> st = stage_carve<DK, DV>(stage_smem, true, false, false, true);
-    // column sums, double-buffered so that two barriers per token suffice
+    // per-warp column sums and their totals, in buffers alternating with the token's parity
     __shared__ float partA[2][kBwdWarps][DK];
     __shared__ float partB[2][kBwdWarps][DV];
     __shared__ float duA[2][DK], duB[2][DV];
