@@ -188,7 +188,11 @@ def test_bwd_validation(lib):
     lib.kda_bwd_workspace_size.restype = ctypes.c_size_t
     lib.kda_last_error.restype = ctypes.c_char_p
     need = lib.kda_bwd_workspace_size(i64(640), 2, 4, 128, 128)
-    assert need >= (640 // 64 + 3) * 4 * 128 * 128 * 4
+    # per (chunk, head): the checkpoint, Psi and the end gradient [dk][dv] and Phi [dk][dk],
+    # fp32, for the T/64 + N chunks the layout provisions
+    assert need >= (640 // 64 + 2) * 4 * (3 * 128 * 128 + 128 * 128) * 4
+    assert (lib.kda_bwd_workspace_size(i64(640), 2, 4, 64, 128)
+            >= (640 // 64 + 2) * 4 * (3 * 64 * 128 + 64 * 64) * 4)
     assert lib.kda_bwd_workspace_size(i64(640), 2, 4, 96, 128) == 0
 
     def call(**kw):
