@@ -414,7 +414,15 @@ def bench_backward(dev, stream, d, sp, peaks, reps=1):
     run()
     torch.cuda.synchronize(dev)
     split = {k: round(v[1], 3) for k, v in kda.profile_end().items()}
+    # algorithmic bytes: per token and head, q, k, z, v, beta and do read and dq, dk, dz, dv,
+    # dbeta written (io dtype); per head, dS_out read and dS0 written (fp32)
+    dv = d["v"].shape[2]
+    e = d["q"].element_size()
+    nbytes = (T_ * H_ * ((3 * dk + 2 * dv + 1) * e + (3 * dk + dv + 1) * e)
+              + 2 * H_ * dk * dv * 4)
+    gbs = nbytes / (ms / 1e3) / 1e9
     return {"ms_per_call": ms, "tokens_per_s": T_ / (ms / 1e3), "T": T_, "H": H_, "d": dk,
+            "algorithmic_GB": nbytes / 1e9, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
             "form": "parallel over 64-token chunks on CUDA cores: per-chunk forward maps and "
                     "gradient transfer matrices, two short chains over chunks, per-chunk reverse",
             "kernel_ms": split}
