@@ -19,9 +19,16 @@
  *     section 4.2 -- quantile-based expert thresholds.
  *
  * Conventions shared by every entry point
- *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *     allocates no device memory; an entry point that needs scratch takes a
- *     caller-provided workspace.  Every pointer must be 16-byte aligned.
+ *   - All tensor pointers are DEVICE pointers owned by the caller; every pointer must be
+ *     16-byte aligned.  No entry point allocates device memory.  Every entry point that
+ *     needs scratch takes a caller-provided workspace, except kda_fwd_chunked_noalloc,
+ *     whose scratch is a 64 MiB static device buffer inside the library: it occupies
+ *     memory on every GPU the library's module is loaded on, from that moment until the
+ *     process exits.
+ *   - The first call on a device looks up and caches, for that device ordinal, the device
+ *     addresses of the library's static device variables (the error word below and the
+ *     no-alloc scratch).  Do not reset a device (cudaDeviceReset) after calling into the
+ *     library on it: the cached addresses would then be stale.
  *   - Layouts are contiguous row-major with the feature dimension innermost:
  *         q, k, z : [T, H, dk]     v, o : [T, H, dv]     beta : [T, H]
  *         A_log   : [H] fp32       state S : [N, H, dk, dv] fp32 (row = key channel)

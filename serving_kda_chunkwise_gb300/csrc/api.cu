@@ -140,12 +140,15 @@ size_t kda_fwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv, kda
     return kda::fwd_tc_workspace_size(T_total, N, H);
 }
 
-kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const void* beta,
-                             const void* z, const float* A_log, float g_min, const float* S0,
-                             float* S_out, const int32_t* cu_seqlens, int N, int64_t T_total,
-                             int H, int dk, int dv, kda_dtype_t io_dt, void* o, void* workspace,
-                             size_t ws_bytes, kda_stream_t stream) {
-    t_last_error.clear();
+}  // extern "C"
+
+namespace kda {
+// The argument checks of kda_fwd_chunked other than the workspace ones (shared with
+// kda_fwd_chunked_noalloc, which must report a malformed call before anything else).
+kda_status_t check_fwd_args(const void* q, const void* k, const void* v, const void* beta,
+                            const void* z, const float* A_log, float g_min, const float* S0,
+                            float* S_out, const int32_t* cu_seqlens, int N, int64_t T_total,
+                            int H, int dk, int dv, kda_dtype_t io_dt, void* o) {
     KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
     KDA_REQUIRE(N >= 0, "N=%d must be >= 0", N);
     KDA_REQUIRE(H > 0, "H=%d must be positive", H);
@@ -173,6 +176,22 @@ kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const 
     KDA_OPTIONAL_PTR(S0, "S0");
     KDA_OPTIONAL_PTR(S_out, "S_out");
     KDA_OPTIONAL_PTR(cu_seqlens, "cu_seqlens");
+    return KDA_OK;
+}
+}  // namespace kda
+
+extern "C" {
+
+kda_status_t kda_fwd_chunked(const void* q, const void* k, const void* v, const void* beta,
+                             const void* z, const float* A_log, float g_min, const float* S0,
+                             float* S_out, const int32_t* cu_seqlens, int N, int64_t T_total,
+                             int H, int dk, int dv, kda_dtype_t io_dt, void* o, void* workspace,
+                             size_t ws_bytes, kda_stream_t stream) {
+    t_last_error.clear();
+    if (kda_status_t s = kda::check_fwd_args(q, k, v, beta, z, A_log, g_min, S0, S_out,
+                                             cu_seqlens, N, T_total, H, dk, dv, io_dt, o))
+        return s;
+    if (N == 0) return KDA_OK;
     const size_t need = kda_fwd_workspace_size(T_total, N, H, dk, dv, io_dt);
     if (need > 0) {
         KDA_REQUIRE_PTR(workspace, "workspace");

@@ -1,0 +1,485 @@
+// fwd_chain.cu -- the serial stage of the tensor-core chunked forward: for every (sequence,
+// head), chunk after chunk, the pseudo-values, the output and the state update
+// ("Kimi k3 技术报告详解（1）——架构再升华", section "Chunkwise parallel form"):
+//   Vt = U - W S,   O = (Gamma*Q) S + A Vt,   S <- Diag(gamma^C) S + K~^T Vt.
+//
+// One CTA per (sequence, head) at a time, all 128 value columns, with the state kept
+// transposed in tensor memory: lane j of TMEM holds column j of S (row j of S^T).  Then
+// every product of the chain has S^T or Vt^T as its A operand, read straight from TMEM,
+// and the package tiles (bf16, in shared memory) as B operands:
+//   MMA1  D1  = S^T [W; Gamma*Q]^T        (M = 128 value columns, N = 128, K = 128 keys)
+//             -> lanes j, columns r < 64: X^T = (W S)^T;  columns 64 + r: ((Gamma*Q) S)^T
+//   E1    Vt^T = U^T - X^T, rounded to bf16 hi + lo and stored back into TMEM
+//   MMA2  dS^T = [Vt_hi | Vt_lo | Vt_hi]^T [K~_hi; K~_hi; K~_lo]   (K = 3 x 64 tokens)
+//   E2    S^T <- S^T Diag(gamma^C) + dS^T in fp32 registers; bf16 copy of S^T into TMEM
+//   MMA3  O^T += [Vt_hi | Vt_lo | Vt_hi]^T [A_hi; A_hi; A_lo]^T  (into D1's columns 64..127)
+//   E3    O^T -> bf16 -> shared-memory tile [64 r][128 j] -> one TMA store
+// The state update takes three bf16 products (hi x hi, lo x hi, hi x lo) so that the fp32
+// state is not limited by bf16 rounding of K~ or Vt; the output takes the same three.
+// No intermediate of the chain goes through shared memory, so a chain step is
+// MMA1 -> E1 -> MMA2 -> E2 with one TMEM round trip per epilogue.
+//
+// Threads: 8 epilogue warps (warp w reaches TMEM lanes 32 (w % 4) .. + 31, i.e. value columns
+// j; warps w and w + 4 split the other index), one thread issuing every MMA, one issuing
+// every bulk copy.  They meet only on mbarriers.  Each CTA walks a fixed list of (sequence,
+// head) chains: sequences sorted longest first, dealt to the CTAs in a snake order.
+#include <cuda.h>
+
+#include "fwd_tc_layout.cuh"
+#include "kda_common.cuh"
+#include "tc_util.cuh"
+
+namespace kda {
+namespace fwdtc {
+namespace {
+
+using namespace tc;
+
+// Optional per-phase cycle counters (debug builds with -DKDA_PHASE_TIMING only): the MMA
+// thread and lane 0 of epilogue warp 0 of CTA 0 accumulate clock64() deltas.
+#ifdef KDA_PHASE_TIMING
+__device__ unsigned long long g_chain_phase[16];
+#define CH_T0() long long ch_t = clock64()
+#define CH_MARK(i)                                                       \
+    do {                                                                 \
+        const long long ch_n = clock64();                                \
+        if (blockIdx.x == 0) atomicAdd(&g_chain_phase[(i)], (unsigned long long)(ch_n - ch_t)); \
+        ch_t = ch_n;                                                     \
+    } while (0)
+#else
+#define CH_T0() \
+    do {        \
+    } while (0)
+#define CH_MARK(i) \
+    do {           \
+    } while (0)
+#endif
+
+constexpr int kChainThreads = 320;
+constexpr int kMmaT = 256;   // lane 0 of warp 8
+constexpr int kCopyT = 288;  // lane 0 of warp 9
+
+// shared memory (1024-aligned offsets)
+constexpr uint32_t kSPA = 0;          // part A, two stages of 32 KB
+constexpr uint32_t kSKC = 65536;      // K~ hi + lo (32 KB)
+constexpr uint32_t kSAT = 98304;      // A hi + lo (16 KB)
+constexpr uint32_t kSU = 114688;      // U, two stages of 32 KB
+constexpr uint32_t kSG = 180224;      // gamma^C, four stages of 512 B
+constexpr uint32_t kSO = 182272;      // output tile [64 r][128 j] bf16 (256-byte rows)
+constexpr uint32_t kSBars = 198656;
+constexpr uint32_t kChainSmem = kSBars + 256 + 1024;
+static_assert(kChainSmem <= 232448, "chain kernel exceeds the shared-memory limit");
+
+// TMEM columns: S^T bf16 [0, 64); Vt^T bf16 hi [64, 96), lo [96, 128); D1 for chunk g in
+// [128 + 128 (g & 1), +128); dS^T [384, 512)
+constexpr uint32_t kTS = 0, kTV = 64, kTVlo = 96, kTD1 = 128, kTDS = 384, kTCols = 512;
+
+struct ChainParams {
+    CUtensorMap to;  // o: [T_total, H, 128] bf16, box 128 x 1 x 64, no swizzle
+    const uint8_t* pkg;
+    const int32_t* cu;
+    const int32_t* chunk_off;
+    const int32_t* order;
+    const float* S0;
+    float* S_out;
+    __nv_bfloat16* o;
+    unsigned* err;
+    int64_t T_total;
+    int N, H, maxchunks;
+};
+
+// The k-th chain of CTA b out of G: snake order over the longest-first list.
+__device__ __forceinline__ int chain_of(int k, int b, int G) {
+    return k * G + ((k & 1) ? (G - 1 - b) : b);
+}
+
+struct Chain {
+    int n, h, nch;
+    int64_t t_begin, t_end;
+    const uint8_t* pkg0;
+};
+
+__device__ __forceinline__ Chain decode_chain(const ChainParams& p, int ci) {
+    Chain c;
+    c.n = __ldg(p.order + ci / p.H);
+    c.h = ci % p.H;
+    seq_range(p.cu, c.n, p.N, p.T_total, nullptr, c.t_begin, c.t_end);
+    const int c0 = __ldg(p.chunk_off + c.n);
+    c.nch = __ldg(p.chunk_off + c.n + 1) - c0;
+    c.pkg0 = p.pkg + ((size_t)c.h * p.maxchunks + c0) * kPkgBytes;
+    return c;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the OR of `pred` over the participating threads.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+__global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(sm);
+    uint64_t* fullPA = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2] part A
+    uint64_t* fullU = fullPA + 2;                                  // [2] U + gamma^C
+    uint64_t* fullKC = fullPA + 4;
+    uint64_t* fullAT = fullPA + 5;
+    uint64_t* mma1 = fullPA + 6;                                   // [2]
+    uint64_t* mma2 = fullPA + 8;
+    uint64_t* mma3 = fullPA + 9;
+    uint64_t* vt_ready = fullPA + 10;                              // [2], 8 arrivals
+    uint64_t* s_ready = fullPA + 12;                               // 8 arrivals
+    uint64_t* drain = fullPA + 13;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullPA + 14);
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int* abort = &s_abort;
+    if (tid == 0) {
+        for (int i = 0; i < 14; ++i) mbar_init(&fullPA[i], 1);
+        mbar_init(&vt_ready[0], 8);
+        mbar_init(&vt_ready[1], 8);
+        mbar_init(s_ready, 8);
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kTCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_chains = p.N * p.H;
+    const int G = gridDim.x;
+
+    if (tid == kMmaT) {
+        // ------------------------------------------------------------ MMA thread
+        constexpr uint32_t id1 = idesc_bf16(128, 128, false, false);
+        constexpr uint32_t id2 = idesc_bf16(128, 128, false, true);
+        constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
+        const uint64_t dPA = sdesc_sw128(sbase + kSPA, 0, 1024);
+        const uint64_t dKC = sdesc_sw128(sbase + kSKC, 8192, 1024);
+        const uint64_t dAT = sdesc_sw128(sbase + kSAT, 0, 1024);
+        uint32_t g = 0;
+        bool ok = true;
+        CH_T0();
+        for (int k = 0; ok; ++k) {
+            const int ci = chain_of(k, blockIdx.x, G);
+            if (ci >= n_chains) break;
+            const Chain c = decode_chain(p, ci);
+            for (int t = 0; t < c.nch; ++t, ++g) {
+                const uint32_t st = g & 1, ph = (g >> 1) & 1;
+                if (!mbar_wait_ab(&fullPA[st], ph, p.err, abort)) { ok = false; break; }
+                CH_MARK(0);
+                if (!mbar_wait_ab(s_ready, g & 1, p.err, abort)) { ok = false; break; }
+                CH_MARK(1);
+                tc_fence_after();
+                const uint32_t d1 = tmem + kTD1 + 128 * st;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ts(d1, tmem + kTS + 8 * ks,
+                                dPA + ((st * kPkgPartA + (ks >> 2) * kPkgStkBlk + (ks & 3) * 32) >> 4),
+                                id1, ks > 0);
+                mma_commit(&mma1[st]);
+                CH_MARK(2);
+                if (!mbar_wait_ab(fullKC, g & 1, p.err, abort)) { ok = false; break; }
+                CH_MARK(3);
+                if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) { ok = false; break; }
+                CH_MARK(4);
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 12; ++ks) {
+                    const int seg = ks >> 2, kk = ks & 3;
+                    mma_bf16_ts(tmem + kTDS, tmem + (seg == 1 ? kTVlo : kTV) + 8 * kk,
+                                dKC + (((seg == 2 ? 16384u : 0u) + kk * 2048) >> 4), id2, ks > 0);
+                }
+                mma_commit(mma2);
+                CH_MARK(5);
+                if (!mbar_wait_ab(fullAT, g & 1, p.err, abort)) { ok = false; break; }
+                CH_MARK(6);
+#pragma unroll
+                for (int ks = 0; ks < 12; ++ks) {
+                    const int seg = ks >> 2, kk = ks & 3;
+                    mma_bf16_ts(d1 + 64, tmem + (seg == 1 ? kTVlo : kTV) + 8 * kk,
+                                dAT + (((seg == 2 ? 8192u : 0u) + kk * 32) >> 4), id3, 1);
+                }
+                mma_commit(mma3);
+                CH_MARK(7);
+            }
+        }
+    }
+
+    // the barrier phases a drain must let land (copy thread)
+    int lastPA[2] = {-1, -1}, lastU[2] = {-1, -1}, lastKC = -1, lastAT = -1;
+    if (tid == kCopyT) {
+        // ----------------------------------------------------------- copy thread
+        uint32_t g = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int ci = chain_of(k, blockIdx.x, G);
+            if (ci >= n_chains) break;
+            const Chain c = decode_chain(p, ci);
+            for (int t = 0; t < c.nch; ++t, ++g) {
+                const uint32_t st = g & 1;
+                const uint8_t* src = c.pkg0 + (size_t)t * kPkgBytes;
+                if (t + 3 < c.nch) l2_prefetch(src + 3 * (size_t)kPkgBytes, kPkgBytes);
+                // part A and gamma^C: stage st is free once MMA1 of chunk g - 2 has completed
+                if (g >= 2 && !mbar_wait_ab(&mma1[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
+                mbar_expect_tx(&fullPA[st], kPkgPartA);
+                bulk_g2s(sm + kSPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
+                lastPA[st] = (int)((g >> 1) & 1);
+                // U and gamma^C (which E1 waits for and E2 reads): U stage st is free once E1 of
+                // chunk g - 2 is done; gamma stage g & 3 once E2 of chunk g - 4 is (E2(g - 4)
+                // precedes E1(g - 2) on the same warps)
+                if (g >= 2 && !mbar_wait_ab(&vt_ready[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
+                mbar_expect_tx(&fullU[st], kPkgUBytes + kPkgGBytes);
+                bulk_g2s(sm + kSU + st * kPkgUBytes, src + kPkgU, kPkgUBytes, &fullU[st]);
+                bulk_g2s(sm + kSG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
+                lastU[st] = (int)((g >> 1) & 1);
+                // K~: free once MMA2 of chunk g - 1 has completed
+                if (g >= 1 && !mbar_wait_ab(mma2, (g - 1) & 1, p.err, abort)) { ok = false; break; }
+                mbar_expect_tx(fullKC, kPkgKTBytes);
+                bulk_g2s(sm + kSKC, src + kPkgKT, kPkgKTBytes, fullKC);
+                lastKC = (int)(g & 1);
+                // A: free once MMA3 of chunk g - 1 has completed
+                if (g >= 1 && !mbar_wait_ab(mma3, (g - 1) & 1, p.err, abort)) { ok = false; break; }
+                mbar_expect_tx(fullAT, kPkgAQKBytes);
+                bulk_g2s(sm + kSAT, src + kPkgAQK, kPkgAQKBytes, fullAT);
+                lastAT = (int)(g & 1);
+            }
+        }
+    }
+
+    if (warp < 8) {
+        // ------------------------------------------------------- epilogue warps
+        const int q = warp & 3, wg = warp >> 2;
+        const int j = 32 * q + lane;  // value column = TMEM lane
+        const uint32_t lb = static_cast<uint32_t>(32 * q) << 16;
+        uint32_t g = 0;
+        bool ok = true;
+        CH_T0();
+        const bool rec = (tid == 0);
+        for (int k = 0; ok; ++k) {
+            const int ci = chain_of(k, blockIdx.x, G);
+            if (ci >= n_chains) break;
+            const Chain c = decode_chain(p, ci);
+            // S[e] = S[i = 64 wg + e][j] (fp32, registers)
+            float S[64];
+            const size_t sbase_el = ((size_t)(c.n * p.H + c.h) * kD + 64 * wg) * kD + j;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) S[e] = p.S0 ? p.S0[sbase_el + (size_t)e * kD] : 0.f;
+            if (c.nch > 0) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pk[e] = pack2(S[2 * e], S[2 * e + 1]);
+                tmem_st32(tmem + lb + kTS + 32 * wg, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_ready);
+            }
+            for (int t = 0; t < c.nch; ++t, ++g) {
+                const uint32_t st = g & 1, ph = (g >> 1) & 1;
+                const int64_t t0 = c.t_begin + (int64_t)t * kC;
+                // ---- E1: Vt^T = U^T - X^T for tokens r = 32 wg + e
+                bool okc = mbar_wait_ab(&fullU[st], ph, p.err, abort);
+                if (rec) CH_MARK(8);
+                okc = okc && mbar_wait_ab(&mma1[st], ph, p.err, abort);
+                if (rec) CH_MARK(9);
+                if (okc) {
+                    tc_fence_after();
+                    const uint8_t* ub = sm + kSU + st * kPkgUBytes + q * kPkgUQ + (lane & 3) * 4;
+                    const uint32_t cpos = lane >> 2;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {  // 16 tokens at a time
+                        float x[16];
+                        tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg + 16 * hf, x);
+                        tmem_ld_wait();
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int e2 = 0; e2 < 8; ++e2) {
+                            float v2[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int r = 32 * wg + 16 * hf + 2 * e2 + u;
+                                const float uu = *reinterpret_cast<const float*>(
+                                    ub + r * 128 + ((cpos ^ (uint32_t)(r & 7)) << 4));
+                                v2[u] = uu - x[2 * e2 + u];
+                            }
+                            hi[e2] = pack2(v2[0], v2[1]);
+                            lo[e2] = pack2(v2[0] - __uint_as_float(hi[e2] << 16),
+                                           v2[1] - __uint_as_float(hi[e2] & 0xffff0000u));
+                        }
+                        tmem_st8(tmem + lb + kTV + 16 * wg + 8 * hf, hi);
+                        tmem_st8(tmem + lb + kTVlo + 16 * wg + 8 * hf, lo);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&vt_ready[st]);
+                if (rec) CH_MARK(10);
+                // ---- E2: S^T <- S^T Diag(gamma^C) + dS^T; bf16 copy for the next MMA1
+                okc = okc && mbar_wait_ab(mma2, g & 1, p.err, abort);
+                if (rec) CH_MARK(11);
+                if (okc) {
+                    tc_fence_after();
+                    const float* gam = reinterpret_cast<const float*>(sm + kSG + (g & 3) * kPkgGBytes) + 64 * wg;
+#pragma unroll
+                    for (int qt = 0; qt < 4; ++qt) {  // 16 key channels at a time
+                        float d[16];
+                        tmem_ld16(tmem + lb + kTDS + 64 * wg + 16 * qt, d);
+                        tmem_ld_wait();
+                        uint32_t pk[8];
+#pragma unroll
+                        for (int e4 = 0; e4 < 4; ++e4) {
+                            const float4 gv = *reinterpret_cast<const float4*>(gam + 16 * qt + 4 * e4);
+                            const int e = 16 * qt + 4 * e4;
+                            S[e] = fmaf(gv.x, S[e], d[4 * e4]);
+                            S[e + 1] = fmaf(gv.y, S[e + 1], d[4 * e4 + 1]);
+                            S[e + 2] = fmaf(gv.z, S[e + 2], d[4 * e4 + 2]);
+                            S[e + 3] = fmaf(gv.w, S[e + 3], d[4 * e4 + 3]);
+                            pk[2 * e4] = pack2(S[e], S[e + 1]);
+                            pk[2 * e4 + 1] = pack2(S[e + 2], S[e + 3]);
+                        }
+                        tmem_st8(tmem + lb + kTS + 32 * wg + 8 * qt, pk);
+                    }
+                    tmem_st_wait();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && t + 1 < c.nch) mbar_arrive(s_ready);
+                if (rec) CH_MARK(12);
+                // ---- E3: O^T -> bf16 -> o
+                okc = okc && mbar_wait_ab(mma3, g & 1, p.err, abort);
+                if (rec) CH_MARK(13);
+                if (okc) tc_fence_after();
+                if (t0 + kC <= c.t_end) {
+                    // full chunk: stage the 64 x 128 tile, one TMA store writes it
+                    if (tid == 0) bulk_wait_read0();  // the previous store has read the tile
+                    named_bar_sync(1, 256);
+                    if (okc) {
+                        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kSO);
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            float ov[16];
+                            tmem_ld16(tmem + lb + kTD1 + 128 * st + 64 + 32 * wg + 16 * hf, ov);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                so[(32 * wg + 16 * hf + e) * kD + j] = __float2bfloat16_rn(ov[e]);
+                        }
+                    }
+                    fence_async_smem();
+                    if (named_bar_or(1, 256, !okc)) { ok = false; break; }
+                    if (tid == 0) {
+                        tma_store_3d(&p.to, sm + kSO, 0, c.h, (int)t0);
+                        bulk_commit();
+                    }
+                } else {
+                    if (named_bar_or(1, 256, !okc)) { ok = false; break; }
+                    // ragged last chunk of a sequence: rows past its end belong to the next
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float ov[16];
+                        tmem_ld16(tmem + lb + kTD1 + 128 * st + 64 + 32 * wg + 16 * hf, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int64_t row = t0 + 32 * wg + 16 * hf + e;
+                            if (row < c.t_end)
+                                p.o[((size_t)row * p.H + c.h) * kD + j] = __float2bfloat16_rn(ov[e]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                if (rec) CH_MARK(14);
+            }
+            if (!ok) break;
+            if (p.S_out) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e) p.S_out[sbase_el + (size_t)e * kD] = S[e];
+            }
+        }
+    }
+
+    if (tid == 0) bulk_wait0();  // the output tile stores are complete
+    __syncthreads();
+    const bool aborted = s_abort != 0;
+    // on an abort, let copies and MMAs still in flight land before leaving
+    if (aborted && tid == kCopyT) {
+        for (int s2 = 0; s2 < 2; ++s2) {
+            if (lastPA[s2] >= 0) mbar_wait(&fullPA[s2], lastPA[s2], nullptr);
+            if (lastU[s2] >= 0) mbar_wait(&fullU[s2], lastU[s2], nullptr);
+        }
+        if (lastKC >= 0) mbar_wait(fullKC, lastKC, nullptr);
+        if (lastAT >= 0) mbar_wait(fullAT, lastAT, nullptr);
+    }
+    if (aborted && tid == kMmaT) {
+        mma_commit(drain);  // arrives once every MMA issued so far has completed
+        mbar_wait(drain, 0, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTCols);
+    }
+}
+
+}  // namespace
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_chain_cycles(unsigned long long* out, int n) {
+    if (n > 16) n = 16;
+    if (cudaMemcpyFromSymbol(out, g_chain_phase, n * sizeof(unsigned long long)) != cudaSuccess)
+        return -1;
+    static const unsigned long long zeros[16] = {};
+    return cudaMemcpyToSymbol(g_chain_phase, zeros, sizeof zeros) == cudaSuccess ? n : -1;
+}
+#endif
+
+cudaError_t launch_chain(const ChainArgs& a) {
+    ChainParams p;
+    if (a.T_total > 0 && !make_map(&p.to, a.o, a.T_total, a.H, 128)) return cudaErrorInvalidValue;
+    p.pkg = a.pkg;
+    p.cu = a.cu;
+    p.chunk_off = a.chunk_off;
+    p.order = a.order;
+    p.S0 = a.S0;
+    p.S_out = a.S_out;
+    p.o = static_cast<__nv_bfloat16*>(a.o);
+    p.err = a.err;
+    p.T_total = a.T_total;
+    p.N = a.N;
+    p.H = a.H;
+    p.maxchunks = a.maxchunks;
+    cudaError_t e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kChainSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t chains = (int64_t)a.N * a.H;
+    const int grid = (int)(chains < sms ? chains : sms);
+    if (grid == 0) return cudaSuccess;
+    ProfScope prof("chain_kernel", a.stream);
+    chain_kernel<<<grid, kChainThreads, kChainSmem, a.stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace fwdtc
+}  // namespace kda

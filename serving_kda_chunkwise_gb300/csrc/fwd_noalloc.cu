@@ -44,6 +44,10 @@ extern "C" kda_status_t kda_fwd_chunked_noalloc(
     const float* A_log, float g_min, const float* S0, float* S_out, const int32_t* cu_seqlens,
     int N, int64_t T_total, int H, int dk, int dv, kda_dtype_t io_dt, void* o,
     kda_stream_t stream) {
+    // a malformed call is reported as such before the scratch size is looked at
+    if (kda_status_t s = kda::check_fwd_args(q, k, v, beta, z, A_log, g_min, S0, S_out,
+                                             cu_seqlens, N, T_total, H, dk, dv, io_dt, o))
+        return s;
     const size_t need = kda_fwd_workspace_size(T_total, N, H, dk, dv, io_dt);
     if (need == 0)  // the selected kernels need no scratch
         return kda_fwd_chunked(q, k, v, beta, z, A_log, g_min, S0, S_out, cu_seqlens, N, T_total,

@@ -38,45 +38,21 @@
 
 #include <mutex>
 
+#include "fwd_tc_layout.cuh"
 #include "kda_common.cuh"
 #include "kda_internal.h"
 #include "tc_util.cuh"
 
 namespace kda {
+namespace fwdtc {
 namespace {
 
 using namespace tc;
 
-constexpr int kC = 64;    // chunk length
-constexpr int kD = 128;   // head dim (dk = dv)
 // 8 warps (two per SM sub-partition, so up to 255 registers a thread); lane 0 of warp 6,
 // whose row work is among the lightest, also issues every copy and MMA
 constexpr int kIntraThreads = 256;
 constexpr int kIss = 192;
-
-// ---- package: per (head, chunk), the bytes the state kernel copies to shared memory ----
-// part A (needed at the start of a chunk): the row stack [W; Gam*Q] of the state kernel's
-// first MMA, K-major sw128, two 64-channel blocks of 16 KB, each W rows 0..63 then Gam*Q
-// rows 0..63 (128 B per row)
-constexpr uint32_t kPkgStk = 0;
-constexpr uint32_t kPkgStkBlk = 16384;
-constexpr uint32_t kPkgStkQ = 8192;   // Gam*Q rows within a block
-constexpr uint32_t kPkgPartA = 32768;
-// part B (needed from the middle of a chunk on)
-constexpr uint32_t kPkgKT = 32768;    // K~ = K*gamma^C/Gam, [c blk][64 r][128 B]: A = K~^T MN-major
-constexpr uint32_t kPkgAQK = 49152;   // A hi   [64 r][64 i] bf16, K-major sw128
-constexpr uint32_t kPkgAQKLo = 57344; // A lo   (A = hi + lo, bf16 each)
-constexpr uint32_t kPkgPartB = 32768;
-constexpr uint32_t kPkgG = 65536;     // gamma^C [128] fp32
-constexpr uint32_t kPkgGBytes = 512;
-// part C: U = M V in fp32, four quarters of 32 value columns, each [64 r][32 j] with the
-// 16-byte chunk c of row r at chunk position c ^ (r & 7)
-constexpr uint32_t kPkgU = 66048;
-constexpr uint32_t kPkgUQ = 8192;
-constexpr uint32_t kPkgUBytes = 4 * kPkgUQ;
-constexpr uint32_t kPkgBytes = kPkgU + kPkgUBytes;  // 98816
-
-size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Optional phase timers (debug builds with -DKDA_PHASE_TIMING only): thread 0 of CTA 0
 // accumulates clock64() deltas between marked points of each kernel's loop.
@@ -126,7 +102,8 @@ __device__ __forceinline__ int find_seq(const int32_t* chunk_off, int N, int chu
 // with one 16-byte load.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cu, int N,
                                                     int64_t T_total, int32_t* chunk_off,
-                                                    int4* chunk_tab, unsigned* err) {
+                                                    int4* chunk_tab, int32_t* order,
+                                                    unsigned* err) {
     __shared__ int32_t s_warp[32];
     __shared__ int32_t s_carry;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -175,6 +152,23 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         const int64_t rem = e - t0;
         chunk_tab[c] = make_int4(static_cast<int>(t0 & 0xffffffff), static_cast<int>(t0 >> 32), n,
                                  static_cast<int>(rem < kC ? rem : kC));
+    }
+    // Sequences by decreasing chunk count (ties by index) for the chain stage, whose work
+    // per sequence is serial: the longest chains start first.  Beyond kOrderMax sequences
+    // the O(N^2) ranking is skipped and the index order kept.
+    constexpr int kOrderMax = 4096;
+    for (int n = tid; n < N; n += blockDim.x) {
+        if (N > kOrderMax) {
+            order[n] = n;
+            continue;
+        }
+        const int32_t cn = chunk_off[n + 1] - chunk_off[n];
+        int rank = 0;
+        for (int m = 0; m < N; ++m) {
+            const int32_t cm = chunk_off[m + 1] - chunk_off[m];
+            rank += (cm > cn) || (cm == cn && m < n);
+        }
+        order[rank] = n;
     }
 }
 
@@ -812,7 +806,12 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
                                       sw128_chunk(r, cg & 7)) = pk8(t);     // Gam*Q
 #pragma unroll
             for (int e = 0; e < 8; ++e) t[e] = kv[e] * ek[e];
-            *reinterpret_cast<uint4*>(pkg + kPkgKT + o64) = pk8(t);       // K*gamma^C/Gam
+            {
+                uint4 hi, lo;
+                pk8_hilo(t, hi, lo);
+                *reinterpret_cast<uint4*>(pkg + kPkgKT + o64) = hi;        // K*gamma^C/Gam
+                *reinterpret_cast<uint4*>(pkg + kPkgKTLo + o64) = lo;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) t[e] = kv[e] * eg[e];
             *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
@@ -1019,410 +1018,6 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
     }
 }
 
-// ================================================================ state ====
-
-struct StateParams {
-    CUtensorMap to;  // o as [T_total, H, 128] bf16, box 64 x 1 x 64, 128-byte swizzle
-    const uint8_t* pkg;
-    const int32_t* cu;
-    const int32_t* chunk_off;
-    const float* S0;
-    float* S_out;
-    __nv_bfloat16* o;
-    unsigned* err;
-    int64_t T_total;
-    int N, H, maxchunks;
-};
-
-// The value columns of S are independent (column j of S, X, Vt and O depends only on
-// column j of V and S0), so each (sequence, head) is served by kSplit CTAs of kJ columns.
-constexpr int kSplit = 4;
-constexpr int kJ = kD / kSplit;  // 32: the 32-wide bf16 tiles use the 64-byte swizzle
-
-// shared-memory map of the state kernel (1024-aligned offsets)
-constexpr uint32_t kPA = 0;                         // package part A, two stages of 32 KB
-constexpr uint32_t kPB = 2 * kPkgPartA;             //  65536: part B, two stages of 32 KB
-constexpr uint32_t kUS = kPB + 2 * kPkgPartB;       // 131072: U (own quarter), two stages of 8 KB
-constexpr uint32_t kVt = kUS + 2 * kPkgUQ;          // 147456: Vt [64 r][32 j] bf16 MN-major sw64,
-                                                    //         two stages of (hi 4 KB, lo 4 KB)
-constexpr uint32_t kVtStage = 8192, kVtLo = 4096;
-constexpr uint32_t kSbf = kVt + 2 * kVtStage;       // 163840: S bf16 [128 i][32 j] MN-major sw64
-constexpr uint32_t kGam = kSbf + 8192;              // 172032: gamma^C, two stages of 512 B
-constexpr uint32_t kOSt = kGam + 1024;              // 173056: O tile [64 r][32 j] bf16 sw64,
-                                                    //         the source of a TMA store
-constexpr uint32_t kSBars = kOSt + 4096;            // 177152
-constexpr uint32_t kStateSmem = kSBars + 256 + 1024;
-static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limit");
-// TMEM columns: D1 = [X; Gam Q S + A Vt] for chunk t in [32 (t & 1), 32 (t & 1) + 32);
-// dS = K~^T Vt in [64, 96)
-constexpr uint32_t kStateTmemCols = 128, kDS = 64;
-
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Named barrier that also returns the OR of `pred` over the participating threads.
-__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-// 8 epilogue warps, two idle warps, an MMA warp and a copy warp: warp w runs on SM
-// sub-partition w % 4, and the X warps (sub-partitions 0, 1) must not share theirs with
-// the threads that issue MMAs and copies.
-constexpr int kStateThreads = 384;
-constexpr int kMmaT = 320;   // the MMA thread: lane 0 of warp 10
-constexpr int kCopyT = 352;  // the copy thread: lane 0 of warp 11
-
-// One CTA per (sequence, head, quarter of the value columns).  TMEM lanes 0..63 of D1 hold
-// the rows of X = W S, lanes 64..127 the rows of O; a warp reaches only the lane quadrant
-// (warp % 4), so warps 0, 1, 4, 5 ("X warps") form Vt, warps 2, 3, 6, 7 ("O warps") write O
-// and all eight epilogue warps update S (one state row i per lane, 16 columns per
-// warpgroup).
-// One thread issues every MMA, another every bulk copy; the warps meet only on mbarriers
-// (no CTA-wide barrier inside the chunk loop), so nothing waits on MMA or copy issue.
-// Per chunk t:
-//   MMA1(t)  D1 = [W; Gam Q] S                                  | waits s_ready(t - 1)
-//   E1(t)    X warps: Vt = U - X -> bf16 hi + lo     | waits mma1 | -> vt_ready
-//   MMA2(t)  dS = K~^T Vt -> mma2, then the first half of MMA3(t): O rows += A Vt (hi/lo
-//            products), overlapping E2(t)
-//   E2(t)    epilogue warps: S <- gamma^C S + dS, bf16 copy of S  | waits mma2 | -> s_ready
-//   MMA1(t + 1) -> mma1, then the second half of MMA3(t) -> mma3, overlapping E1(t + 1)
-//   E3(t)    O warps: O(t) -> global, overlapping E1(t + 1)       | waits mma3
-// MMA3 uses a 128-row A operand whose first 64 rows are whatever precedes the A tile in
-// shared memory: they only add into the X lanes of D1, which are consumed by then.
-// Every barrier that a thread may fall behind on is per stage, so a parity never aliases.
-__global__ void __launch_bounds__(kStateThreads, 1) state_kernel(const __grid_constant__ StateParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t sbase = smem_u32(sm);
-    uint64_t* fullA = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2]
-    uint64_t* fullB = fullA + 2;                                  // [2] (part B + gamma)
-    uint64_t* ubar = fullA + 4;                                   // [2]
-    uint64_t* mma3 = fullA + 6;                                   // [2]
-    uint64_t* vt_ready = fullA + 8;                               // [2], 4 arrivals
-    uint64_t* mma1 = fullA + 10;
-    uint64_t* mma2 = fullA + 11;
-    uint64_t* s_ready = fullA + 12;                               // 8 arrivals
-    uint64_t* drain = fullA + 13;  // used once, to let MMAs in flight land on an abort
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullA + 14);
-    __shared__ int s_abort;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, wg = (warp >> 2) & 1;
-    const int row = 32 * quad + lane;  // TMEM lane: state row i; X row (< 64) / O row - 64
-    const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
-    const bool epi = warp < 8;
-    const bool xwarp = epi && quad < 2;
-    const bool owarp = epi && quad >= 2;
-    const int part = blockIdx.x % kSplit;  // which 32 value columns
-    const int nh = blockIdx.x / kSplit, h = nh % p.H, n = nh / p.H;
-    const int jc = kJ * part + 16 * wg;    // first of the 16 value columns of this epilogue thread
-    volatile int* abort = &s_abort;
-
-    if (tid == 0) {
-        for (int i = 0; i < 14; ++i) mbar_init(&fullA[i], 1);
-        mbar_init(&vt_ready[0], 4);  // one arrival per X warp
-        mbar_init(&vt_ready[1], 4);
-        mbar_init(s_ready, 8);       // one arrival per epilogue warp
-        fence_mbar_init();
-        s_abort = 0;
-    }
-    if (warp == 0) tmem_alloc(tmem_slot, kStateTmemCols);
-
-    int64_t t_begin, t_end;
-    seq_range(p.cu, n, p.N, p.T_total, nullptr, t_begin, t_end);
-    const int c0 = __ldg(p.chunk_off + n);
-    const int nch = __ldg(p.chunk_off + n + 1) - c0;
-    const uint8_t* pkg0 = p.pkg + ((size_t)h * p.maxchunks + c0) * kPkgBytes;
-
-    // S[i = row][jc + jj], jj < 16, in registers of the epilogue warps
-    float S[16];
-    const size_t sofs = ((size_t)nh * kD + row) * kD + jc;
-#pragma unroll
-    for (int jj = 0; jj < 16; jj += 4) {
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (p.S0 && epi) v = *reinterpret_cast<const float4*>(p.S0 + sofs + jj);
-        S[jj] = v.x; S[jj + 1] = v.y; S[jj + 2] = v.z; S[jj + 3] = v.w;
-    }
-    auto write_sbf = [&]() {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            float v8[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v8[e] = S[8 * cc + e];
-            *reinterpret_cast<uint4*>(sm + kSbf + sw64_chunk(row, 2 * wg + cc)) = pk8(v8);
-        }
-    };
-    if (epi) write_sbf();
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (tid == kMmaT && nch > 0) {
-        // ------------------------------------------------------------ MMA thread
-        // Descriptors differ only in the start-address field (address / 16, low 14 bits,
-        // which never carries for shared-memory offsets): base values are built once and
-        // offsets added.
-        const uint64_t dA1 = sdesc_sw128(sbase + kPA, 0, 1024);
-        const uint64_t dS1 = sdesc_sw64(sbase + kSbf, 0, 512);
-        auto issue_mma1 = [&](int t) {  // D1(t) = [W; Gam Q] S
-            const uint64_t a0 = dA1 + ((t & 1) * kPkgPartA >> 4);
-            constexpr uint32_t id = idesc_bf16(128, kJ, false, true);
-            const uint32_t d = tmem + uint32_t(kJ) * (t & 1);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16(d, a0 + (((ks >> 2) * kPkgStkBlk + (ks & 3) * 32) >> 4),
-                         dS1 + ((ks * 1024) >> 4), id, ks > 0);
-            mma_commit(mma1);
-        };
-        // MMA3(t), K steps [ks0, ks0 + 2): A_hi Vt_hi + A_hi Vt_lo + A_lo Vt_hi into the O
-        // rows.  The 128-row A operand is [rows before the tile; A]: A hi is preceded by K~
-        // block 1, A lo by A hi.
-        auto issue_mma3 = [&](int t, int ks0) {
-            const uint32_t sB = sbase + kPB + (t & 1) * kPkgPartB;
-            const uint32_t sVt = sbase + kVt + (t & 1) * kVtStage;
-            const uint32_t sAh = sB + (kPkgAQK - kPkgKT) - 8192;
-            const uint32_t sAl = sB + (kPkgAQKLo - kPkgKT) - 8192;
-            constexpr uint32_t id3 = idesc_bf16(128, kJ, false, true);
-            const uint32_t d = tmem + uint32_t(kJ) * (t & 1);
-#pragma unroll
-            for (int ks = ks0; ks < ks0 + 2; ++ks) {
-                const uint64_t ah = sdesc_sw128(sAh + ks * 32, 0, 1024);
-                const uint64_t al = sdesc_sw128(sAl + ks * 32, 0, 1024);
-                const uint64_t vh = sdesc_sw64(sVt + ks * 1024, 0, 512);
-                const uint64_t vl = sdesc_sw64(sVt + kVtLo + ks * 1024, 0, 512);
-                mma_bf16(d, ah, vh, id3, 1);
-                mma_bf16(d, ah, vl, id3, 1);
-                mma_bf16(d, al, vh, id3, 1);
-            }
-        };
-        const uint64_t dKt = sdesc_sw128(sbase + kPB, 8192, 1024);
-        const uint64_t dVt2 = sdesc_sw64(sbase + kVt, 0, 512);
-        int t = 0;
-        for (; t < nch; ++t) {
-            const int st = t & 1;
-            const uint32_t ph = (t >> 1) & 1;
-            // copies complete long before the handoffs: their waits go first, off the chain
-            if (!mbar_wait_ab(&fullA[st], ph, p.err, abort)) break;
-            if (t > 0 && !mbar_wait_ab(s_ready, (t - 1) & 1, p.err, abort)) break;
-            tc_fence_after();
-            issue_mma1(t);
-            if (t > 0) {
-                issue_mma3(t - 1, 2);
-                mma_commit(&mma3[(t - 1) & 1]);
-            }
-            if (!mbar_wait_ab(&fullB[st], ph, p.err, abort)) break;
-            if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
-            tc_fence_after();
-            constexpr uint32_t id2 = idesc_bf16(128, kJ, true, true);
-            const uint64_t k0 = dKt + (st * kPkgPartB >> 4), v0 = dVt2 + (st * kVtStage >> 4);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tmem + kDS, k0 + ((ks * 2048) >> 4), v0 + ((ks * 1024) >> 4), id2, ks > 0);
-            mma_commit(mma2);
-            issue_mma3(t, 0);
-        }
-        if (t == nch) {
-            issue_mma3(nch - 1, 2);
-            mma_commit(&mma3[(nch - 1) & 1]);
-        }
-    }
-
-    // the last chunk whose copy was issued into each stage (copy thread), for a drain
-    int lastA[2] = {-1, -1}, lastB[2] = {-1, -1}, lastU[2] = {-1, -1};
-    if (tid == kCopyT && nch > 0) {
-        // ----------------------------------------------------------- copy thread
-        auto issue_a = [&](int t) {
-            const int st = t & 1;
-            mbar_expect_tx(&fullA[st], kPkgPartA);
-            bulk_g2s(sm + kPA + st * kPkgPartA, pkg0 + (size_t)t * kPkgBytes, kPkgPartA,
-                     &fullA[st]);
-            lastA[st] = t;
-        };
-        auto issue_b = [&](int t) {
-            const int st = t & 1;
-            const uint8_t* src = pkg0 + (size_t)t * kPkgBytes;
-            mbar_expect_tx(&fullB[st], kPkgPartB + kPkgGBytes);
-            bulk_g2s(sm + kPB + st * kPkgPartB, src + kPkgKT, kPkgPartB, &fullB[st]);
-            bulk_g2s(sm + kGam + st * 512, src + kPkgG, kPkgGBytes, &fullB[st]);
-            lastB[st] = t;
-        };
-        auto issue_u = [&](int t) {
-            const int st = t & 1;
-            mbar_expect_tx(&ubar[st], kPkgUQ);
-            bulk_g2s(sm + kUS + st * kPkgUQ, pkg0 + (size_t)t * kPkgBytes + kPkgU + part * kPkgUQ,
-                     kPkgUQ, &ubar[st]);
-            lastU[st] = t;
-        };
-        for (int t = 0; t < 2 && t < nch; ++t) {
-            issue_a(t);
-            issue_u(t);
-            issue_b(t);
-        }
-        for (int t = 0; t + 2 < nch; ++t) {
-            const int st = t & 1;
-            const uint32_t ph = (t >> 1) & 1;
-            if (t + 3 < nch) l2_prefetch(pkg0 + (size_t)(t + 3) * kPkgBytes, kPkgBytes);
-            // E1(t) has read stage st of U, and MMA1(t) (which E1 waited for) of part A
-            if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) break;
-            issue_u(t + 2);
-            issue_a(t + 2);
-            // MMA2(t) and MMA3(t) have read stage st of part B; E2(t) has read gamma
-            if (!mbar_wait_ab(&mma3[st], ph, p.err, abort)) break;
-            issue_b(t + 2);
-        }
-    }
-
-    if (epi) {
-        // ------------------------------------------------------- epilogue warps
-        KDA_PHASE_INIT();
-        for (int t = 0; t < nch; ++t) {
-            const int st = t & 1;
-            const uint32_t ph = (t >> 1) & 1;
-            const uint32_t d1 = uint32_t(kJ) * st;
-            const int64_t t0 = t_begin + (int64_t)t * kC;
-            if (xwarp) {
-                if (!mbar_wait_ab(&ubar[st], ph, p.err, abort)) break;
-                if (!mbar_wait_ab(mma1, t & 1, p.err, abort)) break;
-                KDA_PHASE(21);
-                tc_fence_after();
-                KDA_PHASE(16);
-                // E1: Vt = U - X for row r = row, columns [16 wg, 16 wg + 16) of this quarter
-                const uint8_t* urow = sm + kUS + st * kPkgUQ + row * 128;
-                uint8_t* vt = sm + kVt + st * kVtStage;
-                float x[16];
-                tmem_ld16(tmem + lane_base + d1 + 16 * wg, x);
-                tmem_ld_wait();
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c4 = 4 * wg + 2 * cc;  // fp32 chunk of the 8 columns
-                    const float4 ua = *reinterpret_cast<const float4*>(urow + ((c4 ^ (row & 7)) << 4));
-                    const float4 ub =
-                        *reinterpret_cast<const float4*>(urow + (((c4 + 1) ^ (row & 7)) << 4));
-                    const float d8[8] = {ua.x - x[8 * cc], ua.y - x[8 * cc + 1],
-                                         ua.z - x[8 * cc + 2], ua.w - x[8 * cc + 3],
-                                         ub.x - x[8 * cc + 4], ub.y - x[8 * cc + 5],
-                                         ub.z - x[8 * cc + 6], ub.w - x[8 * cc + 7]};
-                    uint4 hi, lo;
-                    pk8_hilo(d8, hi, lo);
-                    const uint32_t off = sw64_chunk(row, 2 * wg + cc);
-                    *reinterpret_cast<uint4*>(vt + off) = hi;
-                    *reinterpret_cast<uint4*>(vt + kVtLo + off) = lo;
-                }
-                fence_async_smem();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&vt_ready[st]);
-                KDA_PHASE(17);
-            }
-            // The O warps meet on a named barrier below, so they leave the loop only together
-            // (by a vote at its end); the X warps leave at the first wait that fails.
-            bool ok = mbar_wait_ab(&fullB[st], ph, p.err, abort) &&  // gamma^C of this chunk
-                      mbar_wait_ab(mma2, t & 1, p.err, abort);
-            if (xwarp && !ok) break;
-            tc_fence_after();
-            KDA_PHASE(18);
-            // E2: S <- gamma^C * S + dS ;  bf16 copy of S for the next chunk's MMA1
-            {
-                const float gam = reinterpret_cast<const float*>(sm + kGam + st * 512)[row];
-                float v[16];
-                tmem_ld16(tmem + lane_base + kDS + 16 * wg, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) S[e] = fmaf(gam, S[e], v[e]);
-                write_sbf();
-            }
-            fence_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_ready);
-            KDA_PHASE(19);
-            if (owarp) {
-                // E3: O rows r = row - 64, columns [jc, jc + 32) -> o
-                ok = ok && mbar_wait_ab(&mma3[st], ph, p.err, abort);
-                tc_fence_after();
-                const int r = row - 64;
-                float v[16];
-                tmem_ld16(tmem + lane_base + d1 + 16 * wg, v);
-                tmem_ld_wait();
-                if (t0 + kC <= t_end) {
-                    // full chunk: stage the 64 x 32 tile, one TMA store writes it
-                    if (tid == 64) bulk_wait_read0();  // the previous store has read the tile
-                    named_bar_sync(2, 128);
-#pragma unroll
-                    for (int q8 = 0; q8 < 2; ++q8) {
-                        float a8[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) a8[e] = v[8 * q8 + e];
-                        *reinterpret_cast<uint4*>(sm + kOSt + sw64_chunk(r, 2 * wg + q8)) = pk8(a8);
-                    }
-                    fence_async_smem();
-                    if (named_bar_or(2, 128, !ok)) break;
-                    if (tid == 64) {
-                        tma_store_3d(&p.to, sm + kOSt, kJ * part, h, (int)t0);
-                        bulk_commit();
-                    }
-                } else {
-                    if (named_bar_or(2, 128, !ok)) break;
-                    // ragged last chunk of a sequence: rows past its end belong to the next
-                    if (t0 + r < t_end) {
-                        __nv_bfloat16* orow = p.o + ((size_t)(t0 + r) * p.H + h) * kD + jc;
-#pragma unroll
-                        for (int q8 = 0; q8 < 2; ++q8) {
-                            float a8[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) a8[e] = v[8 * q8 + e];
-                            *reinterpret_cast<uint4*>(orow + 8 * q8) = pk8(a8);
-                        }
-                    }
-                }
-                tc_fence_before();
-            }
-            KDA_PHASE(20);
-        }
-        KDA_PHASE_FLUSH();
-    }
-
-    if (tid == 64) bulk_wait0();  // the output tile stores are complete
-    __syncthreads();
-    const bool aborted = s_abort != 0;
-    if (p.S_out && !aborted && epi) {
-#pragma unroll
-        for (int jj = 0; jj < 16; jj += 4)
-            *reinterpret_cast<float4*>(p.S_out + sofs + jj) =
-                make_float4(S[jj], S[jj + 1], S[jj + 2], S[jj + 3]);
-    }
-    // on an abort, let copies and MMAs still in flight land before leaving
-    if (aborted && tid == kCopyT) {
-        for (int q = 0; q < 2; ++q) {
-            if (lastA[q] >= 0) mbar_wait(&fullA[q], (lastA[q] >> 1) & 1, nullptr);
-            if (lastB[q] >= 0) mbar_wait(&fullB[q], (lastB[q] >> 1) & 1, nullptr);
-            if (lastU[q] >= 0) mbar_wait(&ubar[q], (lastU[q] >> 1) & 1, nullptr);
-        }
-    }
-    if (aborted && tid == kMmaT) {
-        mma_commit(drain);  // arrives once every MMA issued so far has completed
-        mbar_wait(drain, 0, nullptr);
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kStateTmemCols);
-    }
-}
-
 // ================================================================= host ====
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1439,26 +1034,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// [T_total, H, 128] bf16 tensor, boxes of `box_cols` columns x 1 head x 64 rows; 64-column
-// boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int box_cols = 64) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
-    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, kC};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 #ifdef KDA_PHASE_TIMING
-extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
+int debug_phase_cycles(unsigned long long* out, int n) {
     if (n > 32) n = 32;
     if (cudaMemcpyFromSymbol(out, g_phase, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
     static const unsigned long long zeros[32] = {};
@@ -1466,35 +1045,58 @@ extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
 }
 #endif
 
-// workspace: chunk offsets [N + 1], the chunk table [maxchunks], then the packages
+// [T_total, H, 128] bf16 tensor, boxes of `box_cols` columns x 1 head x 64 rows; 64-column
+// boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle, 128-column boxes none.
+bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int box_cols) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, kC};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle sw = box_cols == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                   : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fwdtc
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_phase_cycles(unsigned long long* out, int n) {
+    return fwdtc::debug_phase_cycles(out, n);
+}
+#endif
+
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H) {
-    const int64_t maxchunks = T_total / kC + N;
-    return align_up((size_t)(N + 1) * sizeof(int32_t), 1024) +
-           align_up((size_t)maxchunks * sizeof(int4), 1024) +
-           (size_t)H * (size_t)maxchunks * kPkgBytes;
+    return fwdtc::ws_layout(T_total, N, H).total;
 }
 
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
+    using namespace fwdtc;
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+    const WsLayout L = ws_layout(a.T_total, a.N, a.H);
     const int maxchunks = (int)(a.T_total / kC + a.N);
-    int32_t* chunk_off = reinterpret_cast<int32_t*>(ws);
-    int4* chunk_tab = reinterpret_cast<int4*>(ws + align_up((size_t)(a.N + 1) * sizeof(int32_t), 1024));
-    uint8_t* pkg = reinterpret_cast<uint8_t*>(chunk_tab) +
-                   align_up((size_t)maxchunks * sizeof(int4), 1024);
+    int32_t* chunk_off = reinterpret_cast<int32_t*>(ws + L.off_chunk_off);
+    int4* chunk_tab = reinterpret_cast<int4*>(ws + L.off_tab);
+    int32_t* order = reinterpret_cast<int32_t*>(ws + L.off_order);
+    uint8_t* pkg = ws + L.off_pkg;
 
     {
         ProfScope prof("plan_kernel", a.stream);
         plan_kernel<<<1, 1024, 0, a.stream>>>(a.cu_seqlens, a.N, a.T_total, chunk_off, chunk_tab,
-                                              a.dev_err);
+                                              order, a.dev_err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
     if (a.T_total > 0) {
         IntraParams ip;
-        if (!make_map(&ip.tq, a.q, a.T_total, a.H) || !make_map(&ip.tk, a.k, a.T_total, a.H) ||
-            !make_map(&ip.tv, a.v, a.T_total, a.H) || !make_map(&ip.tz, a.z, a.T_total, a.H))
+        if (!make_map(&ip.tq, a.q, a.T_total, a.H, 64) || !make_map(&ip.tk, a.k, a.T_total, a.H, 64) ||
+            !make_map(&ip.tv, a.v, a.T_total, a.H, 64) || !make_map(&ip.tz, a.z, a.T_total, a.H, 64))
             return cudaErrorInvalidValue;
         ip.beta = static_cast<const __nv_bfloat16*>(a.beta);
         ip.A_log = a.A_log;
@@ -1520,27 +1122,21 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         if (e != cudaSuccess) return e;
     }
 
-    StateParams sp;
-    if (a.T_total > 0 && !make_map(&sp.to, a.o, a.T_total, a.H, kJ)) return cudaErrorInvalidValue;
-    sp.pkg = pkg;
-    sp.cu = a.cu_seqlens;
-    sp.chunk_off = chunk_off;
-    sp.S0 = a.S0;
-    sp.S_out = a.S_out;
-    sp.o = static_cast<__nv_bfloat16*>(a.o);
-    sp.err = a.dev_err;
-    sp.T_total = a.T_total;
-    sp.N = a.N;
-    sp.H = a.H;
-    sp.maxchunks = maxchunks;
-    e = cudaFuncSetAttribute(state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStateSmem);
-    if (e != cudaSuccess) return e;
-    {
-        ProfScope prof("state_kernel", a.stream);
-        state_kernel<<<a.N * a.H * kSplit, kStateThreads, kStateSmem, a.stream>>>(sp);
-    }
-    return cudaGetLastError();
+    ChainArgs ca;
+    ca.pkg = pkg;
+    ca.cu = a.cu_seqlens;
+    ca.chunk_off = chunk_off;
+    ca.order = order;
+    ca.S0 = a.S0;
+    ca.S_out = a.S_out;
+    ca.o = a.o;
+    ca.err = a.dev_err;
+    ca.T_total = a.T_total;
+    ca.N = a.N;
+    ca.H = a.H;
+    ca.maxchunks = maxchunks;
+    ca.stream = a.stream;
+    return launch_chain(ca);
 }
 
 }  // namespace kda

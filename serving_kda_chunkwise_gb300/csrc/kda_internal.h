@@ -89,6 +89,13 @@ cudaError_t launch_fwd_generic(const FwdArgs& a);
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H);
 cudaError_t launch_fwd_tc(const FwdArgs& a);
 
+// The argument checks of kda_fwd_chunked except those of the workspace (api.cu): KDA_OK, or
+// the failing status with the calling thread's last error set.
+kda_status_t check_fwd_args(const void* q, const void* k, const void* v, const void* beta,
+                            const void* z, const float* A_log, float g_min, const float* S0,
+                            float* S_out, const int32_t* cu_seqlens, int N, int64_t T_total,
+                            int H, int dk, int dv, kda_dtype_t io_dt, void* o);
+
 // Records `msg` as the calling thread's last error (see kda_last_error) and returns `s`.
 kda_status_t set_last_error(kda_status_t s, const char* msg);
 

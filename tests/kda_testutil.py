@@ -5,16 +5,18 @@ Tolerances (written here once, used by every parity test):
   fp32 I/O  per (sequence, head):  ||o_gpu - o_ref||_F / ||o_ref||_F <= 1e-4, same for S_out.
   bf16 I/O  per (sequence, head), after dividing both outputs by rms(o_ref) over all
             (token, channel) of that (sequence, head):
-              |o_gpu - o_ref| <= 2e-2 + 1.6e-2 |o_ref|   for every element, and
+              |o_gpu - o_ref| <= 2e-2 + 2^-8 |o_ref|   for every element, and
               rms(o_gpu - o_ref) <= 1e-2.
-            2e-2 is the stated absolute figure; 1.6e-2 is the usual relative tolerance
-            for bf16 tensors (torch.testing's default for bfloat16).  A relative term is
-            unavoidable: the outputs are heavy-tailed (max|o| / rms ~ 20 per head) and the
-            exact result rounded once to bf16 already fails the absolute-only reading (see
-            test_tolerance_reading.py).  The rms bound catches errors that are systematic
-            across a head even when each element stays inside the band.
-            The fp32 final state of a bf16 problem is held to the same two bounds
-            (normalised by rms(S_ref)).
+            2e-2 is the stated absolute figure.  2^-8 |o_ref| bounds half a bf16 ulp of the
+            reference value: the output is stored in bf16, and one correct rounding of the
+            exact result moves it by up to that much (the outputs are heavy-tailed,
+            max|o| / rms ~ 20 per head, so the rounded exact answer alone can exceed 2e-2
+            of rms; see test_tolerance_reading.py).  Nothing else is allowed beyond 2e-2.
+            The rms bound catches errors that are systematic across a head even when each
+            element stays inside the band.
+            The fp32 final state of a bf16 problem is not rounded on output, so it gets no
+            relative term: max|S_gpu - S_ref| <= 2e-2 rms(S_ref) and
+            rms(S_gpu - S_ref) <= 1e-2 rms(S_ref).
 """
 from __future__ import annotations
 
@@ -22,12 +24,12 @@ import numpy as np
 
 FP32_REL_TOL = 1e-4
 BF16_NORM_TOL = 2e-2
-BF16_RTOL = 1.6e-2
+BF16_RTOL = 2.0 ** -8
 BF16_RMS_TOL = 1e-2
 
 
 def bf16_norm_err(o_gpu, o_ref):
-    """Largest (|o_gpu - o_ref| - 1.6e-2 |o_ref|) / rms(o_ref): must be <= 2e-2."""
+    """Largest (|o_gpu - o_ref| - 2^-8 |o_ref|) / rms(o_ref): must be <= 2e-2."""
     if o_ref.size == 0:
         return 0.0
     rms = max(np.sqrt(np.mean(o_ref ** 2)), 1e-30)
@@ -48,6 +50,11 @@ def plain_norm_err(o_gpu, o_ref):
     if o_ref.size == 0:
         return 0.0
     return float(np.max(np.abs(o_gpu - o_ref)) / max(np.sqrt(np.mean(o_ref ** 2)), 1e-30))
+
+
+def state_err(S_gpu, S_ref):
+    """max |S_gpu - S_ref| / rms(S_ref) for the fp32 final state: must be <= 2e-2."""
+    return plain_norm_err(np.asarray(S_gpu, np.float64), np.asarray(S_ref, np.float64))
 
 
 def _spec(x):
@@ -124,7 +131,7 @@ def check_head(o_gpu, o_ref, S_gpu, S_ref, dtype, what=""):
     assert er <= BF16_RMS_TOL, f"{what}: normalised rms err {er:.3e} > {BF16_RMS_TOL}"
     es = 0.0
     if S_ref is not None:
-        es = bf16_norm_err(np.asarray(S_gpu, np.float64), S_ref)
+        es = state_err(S_gpu, S_ref)
         ers = bf16_rms_err(np.asarray(S_gpu, np.float64), S_ref)
         assert ers <= BF16_RMS_TOL, f"{what}: normalised state rms err {ers:.3e}"
     assert eo <= BF16_NORM_TOL, f"{what}: normalised output err {eo:.3e} > {BF16_NORM_TOL}"

@@ -207,3 +207,37 @@ def test_bwd_validation(lib):
     assert call(do=None) == 1 and b"dout is NULL" in lib.kda_last_error()
     assert call(wsb=ctypes.c_size_t(need - 1)) == 1 and b"workspace" in lib.kda_last_error()
     assert call(T=i64(641)) == 1 and b"multiple of N" in lib.kda_last_error()
+
+
+def _noalloc(lib, **over):
+    vp = ctypes.c_void_p
+    a = vp(0x10000)
+    args = dict(q=a, k=a, v=a, beta=a, z=a, A_log=a, g_min=ctypes.c_float(-5.0), S0=None,
+                S_out=None, cu=None, N=1, T=ctypes.c_int64(128), H=2, dk=128, dv=128, dt=1, o=a)
+    args.update(over)
+    f = lib.kda_fwd_chunked_noalloc
+    f.restype = ctypes.c_int
+    lib.kda_last_error.restype = ctypes.c_char_p
+    rc = f(args["q"], args["k"], args["v"], args["beta"], args["z"], args["A_log"], args["g_min"],
+           args["S0"], args["S_out"], args["cu"], args["N"], args["T"], args["H"], args["dk"],
+           args["dv"], args["dt"], args["o"], None)
+    return rc, lib.kda_last_error().decode()
+
+
+def test_noalloc_rejects_problems_beyond_its_buffer(lib):
+    """A problem whose scratch exceeds the built-in 64 MiB is refused before any launch."""
+    lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
+    lib.kda_fwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    T = 65536
+    assert lib.kda_fwd_workspace_size(T, 1, 32, 128, 128, 1) > (64 << 20)
+    rc, msg = _noalloc(lib, T=ctypes.c_int64(T), H=32)
+    assert rc == 1 and "built into the library" in msg
+
+
+def test_noalloc_reports_malformed_arguments_first(lib):
+    """A malformed call names the bad argument, even when the problem is also too large."""
+    rc, msg = _noalloc(lib, q=None, T=ctypes.c_int64(65536), H=32)
+    assert rc == 1 and "q is NULL" in msg
+    rc, msg = _noalloc(lib, N=3, T=ctypes.c_int64(65536 + 1), H=32)
+    assert rc == 1 and "multiple of N" in msg

@@ -3,7 +3,7 @@
 
 Tolerance, per (sequence, head) and gradient tensor: fp32 I/O ||d - d_ref||_F / ||d_ref||_F
 <= 1e-4; bf16 I/O the forward's rule (after dividing by rms(d_ref): |d - d_ref| <= 2e-2 +
-1.6e-2 |d_ref| and rms(d - d_ref) <= 1e-2).  dA_log (summed over sequences) and dS0 are fp32
+2^-8 |d_ref|, the last term half a bf16 ulp of the stored gradient, and rms(d - d_ref) <= 1e-2).  dA_log (summed over sequences) and dS0 are fp32
 outputs: relative 1e-4 for fp32 problems, 1e-2 for bf16 problems.
 """
 import numpy as np
