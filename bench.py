@@ -260,11 +260,13 @@ def run_ours(args, rank, world, local_rank, dist):
     # algorithmic bytes each kernel must move (per launch) on this workload
     alg = {"intra_kernel": T * H * (4 * 2 * D + 2),              # q, k, v, z, beta in
            "chain_kernel": T * H * 2 * D + H * STATE_BYTES,      # o out, final state out
+           "fwd_fused_kernel": T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES,  # whole path
            "fwd_generic_kernel": T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES,
            "plan_kernel": 8}
     bytes_k = alg.get(kname, T * H * BYTES_PER_TOKEN_HEAD)
     achieved = bytes_k / (kernels[kname]["avg_ms"] / 1e3) / 1e9
-    src = {"intra_kernel": "fwd_tc.cu", "chain_kernel": "fwd_chain.cu", "plan_kernel": "fwd_tc.cu",
+    src = {"intra_kernel": "fwd_tc.cu", "chain_kernel": "fwd_tc.cu", "plan_kernel": "fwd_tc.cu",
+           "fwd_fused_kernel": "fwd_tc.cu",
            "fwd_generic_kernel": "fwd_generic.cu"}.get(kname, "fwd_tc.cu")
     path_ms = sum(v["avg_ms"] for v in kernels.values())
     path_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES

@@ -1,4 +1,4 @@
-// fwd_chain.cu -- the serial stage of the tensor-core chunked forward: for every (sequence,
+// fwd_chain.cuh -- the serial stage of the tensor-core chunked forward: for every (sequence,
 // head), chunk after chunk, the pseudo-values, the output and the state update
 // ("Kimi k3 技术报告详解（1）——架构再升华", section "Chunkwise parallel form"):
 //   Vt = U - W S,   O = (Gamma*Q) S + A Vt,   S <- Diag(gamma^C) S + K~^T Vt.
@@ -13,7 +13,7 @@
 //   MMA2  dS^T = [Vt_hi | Vt_lo | Vt_hi]^T [K~_hi; K~_hi; K~_lo]   (K = 3 x 64 tokens)
 //   E2    S^T <- S^T Diag(gamma^C) + dS^T in fp32 registers; bf16 copy of S^T into TMEM
 //   MMA3  O^T += [Vt_hi | Vt_lo | Vt_hi]^T [A_hi; A_hi; A_lo]^T  (into D1's columns 64..127)
-//   E3    O^T -> bf16 -> shared-memory tile [64 r][128 j] -> one TMA store
+//   E3    O^T -> bf16 -> o (for each token, the 32 lanes of a warp store 64 contiguous bytes)
 // The state update takes three bf16 products (hi x hi, lo x hi, hi x lo) so that the fp32
 // state is not limited by bf16 rounding of K~ or Vt; the output takes the same three.
 // No intermediate of the chain goes through shared memory, so a chain step is
@@ -23,6 +23,8 @@
 // j; warps w and w + 4 split the other index), one thread issuing every MMA, one issuing
 // every bulk copy.  They meet only on mbarriers.  Each CTA walks a fixed list of (sequence,
 // head) chains: sequences sorted longest first, dealt to the CTAs in a snake order.
+#pragma once
+
 #include <cuda.h>
 
 #include "fwd_tc_layout.cuh"
@@ -43,7 +45,7 @@ __device__ unsigned long long g_chain_phase[16];
 #define CH_MARK(i)                                                       \
     do {                                                                 \
         const long long ch_n = clock64();                                \
-        if (blockIdx.x == 0) atomicAdd(&g_chain_phase[(i)], (unsigned long long)(ch_n - ch_t)); \
+        if (cta == 0) atomicAdd(&g_chain_phase[(i)], (unsigned long long)(ch_n - ch_t)); \
         ch_t = ch_n;                                                     \
     } while (0)
 #else
@@ -56,6 +58,9 @@ __device__ unsigned long long g_chain_phase[16];
 #endif
 
 constexpr int kChainThreads = 320;
+// Barrier over the chain stage's 320 threads (the fused kernel's CTAs have more threads; the
+// rest leave at once).
+__device__ __forceinline__ void chain_sync() { asm volatile("bar.sync 1, 320;" ::: "memory"); }
 constexpr int kMmaT = 256;   // lane 0 of warp 8
 constexpr int kCopyT = 288;  // lane 0 of warp 9
 
@@ -65,8 +70,7 @@ constexpr uint32_t kSKC = 65536;      // K~ hi + lo (32 KB)
 constexpr uint32_t kSAT = 98304;      // A hi + lo (16 KB)
 constexpr uint32_t kSU = 114688;      // U, two stages of 32 KB
 constexpr uint32_t kSG = 180224;      // gamma^C, four stages of 512 B
-constexpr uint32_t kSO = 182272;      // output tile [64 r][128 j] bf16 (256-byte rows)
-constexpr uint32_t kSBars = 198656;
+constexpr uint32_t kSBars = 182272;
 constexpr uint32_t kChainSmem = kSBars + 256 + 1024;
 static_assert(kChainSmem <= 232448, "chain kernel exceeds the shared-memory limit");
 
@@ -75,7 +79,6 @@ static_assert(kChainSmem <= 232448, "chain kernel exceeds the shared-memory limi
 constexpr uint32_t kTS = 0, kTV = 64, kTVlo = 96, kTD1 = 128, kTDS = 384, kTCols = 512;
 
 struct ChainParams {
-    CUtensorMap to;  // o: [T_total, H, 128] bf16, box 128 x 1 x 64, no swizzle
     const uint8_t* pkg;
     const int32_t* cu;
     const int32_t* chunk_off;
@@ -86,6 +89,13 @@ struct ChainParams {
     unsigned* err;
     int64_t T_total;
     int N, H, maxchunks;
+    // fused kernel only (fused = 0 otherwise): CTA c serves chain c and reads chunk t from
+    // ring slot c * ring_slots + t % ring_slots once ready[slot] >= t + 1; it raises
+    // consumed[c] to t + 1 once every part of chunk t is in shared memory
+    int fused, ring_slots;
+    const uint8_t* ring;
+    const uint32_t* ready;
+    uint32_t* consumed;
 };
 
 // The k-th chain of CTA b out of G: snake order over the longest-first list.
@@ -94,13 +104,14 @@ __device__ __forceinline__ int chain_of(int k, int b, int G) {
 }
 
 struct Chain {
-    int n, h, nch;
+    int ci, n, h, nch;
     int64_t t_begin, t_end;
     const uint8_t* pkg0;
 };
 
 __device__ __forceinline__ Chain decode_chain(const ChainParams& p, int ci) {
     Chain c;
+    c.ci = ci;
     c.n = __ldg(p.order + ci / p.H);
     c.h = ci % p.H;
     seq_range(p.cu, c.n, p.N, p.T_total, nullptr, c.t_begin, c.t_end);
@@ -110,27 +121,9 @@ __device__ __forceinline__ Chain decode_chain(const ChainParams& p, int ci) {
     return c;
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Named barrier that also returns the OR of `pred` over the participating threads.
-__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, %2, %3, q;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
-__global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainParams p) {
-    extern __shared__ uint8_t smem_raw[];
+__device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_raw, int cta, int ncta) {
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -140,30 +133,33 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
     uint64_t* fullAT = fullPA + 5;
     uint64_t* mma1 = fullPA + 6;                                   // [2]
     uint64_t* mma2 = fullPA + 8;
-    uint64_t* mma3 = fullPA + 9;
-    uint64_t* vt_ready = fullPA + 10;                              // [2], 8 arrivals
-    uint64_t* s_ready = fullPA + 12;                               // 8 arrivals
-    uint64_t* drain = fullPA + 13;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullPA + 14);
+    uint64_t* mma3 = fullPA + 9;                                   // [2]
+    uint64_t* vt_ready = fullPA + 11;                              // [2], 8 arrivals
+    uint64_t* s_ready = fullPA + 13;                               // 8 arrivals
+    uint64_t* drain = fullPA + 14;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullPA + 15);
     __shared__ int s_abort;
+    __shared__ uint32_t s_landed_v;  // fused: chunks (counted over the CTA's chains) in smem
+    volatile uint32_t* s_landed = &s_landed_v;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &s_abort;
     if (tid == 0) {
-        for (int i = 0; i < 14; ++i) mbar_init(&fullPA[i], 1);
+        for (int i = 0; i < 15; ++i) mbar_init(&fullPA[i], 1);
         mbar_init(&vt_ready[0], 8);
         mbar_init(&vt_ready[1], 8);
         mbar_init(s_ready, 8);
         fence_mbar_init();
         s_abort = 0;
+        s_landed_v = 0;
     }
     if (warp == 0) tmem_alloc(tmem_slot, kTCols);
     tc_fence_before();
-    __syncthreads();
+    chain_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int n_chains = p.N * p.H;
-    const int G = gridDim.x;
+    const int G = ncta;
 
     if (tid == kMmaT) {
         // ------------------------------------------------------------ MMA thread
@@ -177,7 +173,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         bool ok = true;
         CH_T0();
         for (int k = 0; ok; ++k) {
-            const int ci = chain_of(k, blockIdx.x, G);
+            const int ci = chain_of(k, cta, G);
             if (ci >= n_chains) break;
             const Chain c = decode_chain(p, ci);
             for (int t = 0; t < c.nch; ++t, ++g) {
@@ -210,55 +206,100 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
                 CH_MARK(5);
                 if (!mbar_wait_ab(fullAT, g & 1, p.err, abort)) { ok = false; break; }
                 CH_MARK(6);
+                if (p.fused) *s_landed = g + 1;  // every part of chunk g is in shared memory
 #pragma unroll
                 for (int ks = 0; ks < 12; ++ks) {
                     const int seg = ks >> 2, kk = ks & 3;
                     mma_bf16_ts(d1 + 64, tmem + (seg == 1 ? kTVlo : kTV) + 8 * kk,
                                 dAT + (((seg == 2 ? 8192u : 0u) + kk * 32) >> 4), id3, 1);
                 }
-                mma_commit(mma3);
+                mma_commit(&mma3[st]);
                 CH_MARK(7);
             }
         }
     }
 
-    // the barrier phases a drain must let land (copy thread)
-    int lastPA[2] = {-1, -1}, lastU[2] = {-1, -1}, lastKC = -1, lastAT = -1;
-    if (tid == kCopyT) {
-        // ----------------------------------------------------------- copy thread
+    // Copy lanes: lanes 0..3 of warp 9 each stream one part of the packages, so that a part
+    // is fetched as soon as its buffer is free, independently of the others.
+    //   lane 0: part A ([W; Gamma*Q]), two stages, free once MMA1 of chunk g - 2 completed;
+    //   lane 1: U and gamma^C, two stages of U (free once E1 of chunk g - 2 is done) and four
+    //           of gamma (E2 of chunk g - 4 precedes E1 of chunk g - 2 on the same warps);
+    //   lane 2: K~ hi + lo, one stage, free once MMA2 of chunk g - 1 completed;
+    //   lane 3: A hi + lo, one stage, free once MMA3 of chunk g - 1 completed.
+    int last_ph[2] = {-1, -1};  // the phase parity a drain must let land, per stage
+    const int cpart = (warp == kCopyT / 32 && lane < 4) ? lane : -1;
+    if (cpart >= 0) {
         uint32_t g = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            const int ci = chain_of(k, blockIdx.x, G);
+            const int ci = chain_of(k, cta, G);
             if (ci >= n_chains) break;
             const Chain c = decode_chain(p, ci);
             for (int t = 0; t < c.nch; ++t, ++g) {
                 const uint32_t st = g & 1;
-                const uint8_t* src = c.pkg0 + (size_t)t * kPkgBytes;
-                if (t + 3 < c.nch) l2_prefetch(src + 3 * (size_t)kPkgBytes, kPkgBytes);
-                // part A and gamma^C: stage st is free once MMA1 of chunk g - 2 has completed
-                if (g >= 2 && !mbar_wait_ab(&mma1[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
-                mbar_expect_tx(&fullPA[st], kPkgPartA);
-                bulk_g2s(sm + kSPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
-                lastPA[st] = (int)((g >> 1) & 1);
-                // U and gamma^C (which E1 waits for and E2 reads): U stage st is free once E1 of
-                // chunk g - 2 is done; gamma stage g & 3 once E2 of chunk g - 4 is (E2(g - 4)
-                // precedes E1(g - 2) on the same warps)
-                if (g >= 2 && !mbar_wait_ab(&vt_ready[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
-                mbar_expect_tx(&fullU[st], kPkgUBytes + kPkgGBytes);
-                bulk_g2s(sm + kSU + st * kPkgUBytes, src + kPkgU, kPkgUBytes, &fullU[st]);
-                bulk_g2s(sm + kSG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
-                lastU[st] = (int)((g >> 1) & 1);
-                // K~: free once MMA2 of chunk g - 1 has completed
-                if (g >= 1 && !mbar_wait_ab(mma2, (g - 1) & 1, p.err, abort)) { ok = false; break; }
-                mbar_expect_tx(fullKC, kPkgKTBytes);
-                bulk_g2s(sm + kSKC, src + kPkgKT, kPkgKTBytes, fullKC);
-                lastKC = (int)(g & 1);
-                // A: free once MMA3 of chunk g - 1 has completed
-                if (g >= 1 && !mbar_wait_ab(mma3, (g - 1) & 1, p.err, abort)) { ok = false; break; }
-                mbar_expect_tx(fullAT, kPkgAQKBytes);
-                bulk_g2s(sm + kSAT, src + kPkgAQK, kPkgAQKBytes, fullAT);
-                lastAT = (int)(g & 1);
+                const uint8_t* src;
+                if (p.fused) {
+                    const size_t slot = (size_t)c.ci * p.ring_slots + t % p.ring_slots;
+                    src = p.ring + slot * kPkgBytes;
+                    if (!wait_flag_ge(p.ready + slot, (uint32_t)t + 1, p.err, abort)) { ok = false; break; }
+                    fence_proxy_async_global();
+                } else {
+                    src = c.pkg0 + (size_t)t * kPkgBytes;
+                }
+                if (cpart == 0) {
+                    if (!p.fused && t + 3 < c.nch) l2_prefetch(src + 3 * (size_t)kPkgBytes, kPkgBytes);
+                    if (g >= 2 && !mbar_wait_ab(&mma1[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
+                    mbar_expect_tx(&fullPA[st], kPkgPartA);
+                    bulk_g2s(sm + kSPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
+                    last_ph[st] = (int)((g >> 1) & 1);
+                } else if (cpart == 1) {
+                    if (g >= 2 && !mbar_wait_ab(&vt_ready[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
+                    mbar_expect_tx(&fullU[st], kPkgUBytes + kPkgGBytes);
+                    bulk_g2s(sm + kSU + st * kPkgUBytes, src + kPkgU, kPkgUBytes, &fullU[st]);
+                    bulk_g2s(sm + kSG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
+                    last_ph[st] = (int)((g >> 1) & 1);
+                } else if (cpart == 2) {
+                    if (g >= 1 && !mbar_wait_ab(mma2, (g - 1) & 1, p.err, abort)) { ok = false; break; }
+                    mbar_expect_tx(fullKC, kPkgKTBytes);
+                    bulk_g2s(sm + kSKC, src + kPkgKT, kPkgKTBytes, fullKC);
+                    last_ph[0] = (int)(g & 1);
+                } else {
+                    if (g >= 1 && !mbar_wait_ab(&mma3[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err, abort)) { ok = false; break; }
+                    mbar_expect_tx(fullAT, kPkgAQKBytes);
+                    bulk_g2s(sm + kSAT, src + kPkgAQK, kPkgAQKBytes, fullAT);
+                    last_ph[0] = (int)(g & 1);
+                }
+            }
+        }
+    }
+
+    if (p.fused && warp == kCopyT / 32 && lane == 4) {
+        // ------------------------------------------------ ring-slot releaser (fused)
+        // Once the MMA thread has seen every part of chunk g land in shared memory, hand
+        // the chunk's ring slot back to the intra stage (a gpu-scope release, kept off the
+        // MMA thread).
+        uint32_t g = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int ci = chain_of(k, cta, G);
+            if (ci >= n_chains) break;
+            const Chain c = decode_chain(p, ci);
+            for (int t = 0; t < c.nch; ++t, ++g) {
+                if (*s_landed < g + 1) {
+                    const uint64_t t0 = globaltimer();
+                    while (*s_landed < g + 1) {
+                        if (*abort) { ok = false; break; }
+                        if (globaltimer() - t0 > kWaitLimitNs) {
+                            atomicOr(p.err, kDevErrTimeout);
+                            *abort = 1;
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!ok) break;
+                }
+                st_release_gpu(p.consumed + c.ci, (uint32_t)t + 1);
             }
         }
     }
@@ -272,8 +313,38 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         bool ok = true;
         CH_T0();
         const bool rec = (tid == 0);
+        // E3 of chunk gg (first token t0): O^T -> bf16 -> o, straight from the lanes (for each
+        // token the 32 lanes of a warp write 64 contiguous bytes); rows past the sequence end
+        // belong to the next sequence and are skipped
+        auto store_out = [&](uint32_t gg, int64_t t0, const Chain& c) -> bool {
+            if (!mbar_wait_ab(&mma3[gg & 1], (gg >> 1) & 1, p.err, abort)) return false;
+            tc_fence_after();
+            float o0[16], o1[16];
+            const uint32_t col = tmem + lb + kTD1 + 128 * (gg & 1) + 64 + 32 * wg;
+            tmem_ld16(col, o0);
+            tmem_ld16(col + 16, o1);
+            tmem_ld_wait();
+            const int64_t r0 = t0 + 32 * wg;
+            __nv_bfloat16* orow = p.o + ((size_t)r0 * p.H + c.h) * kD + j;
+            const size_t rstride = (size_t)p.H * kD;
+            if (r0 + 32 <= c.t_end) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) orow[e * rstride] = __float2bfloat16_rn(o0[e]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) orow[(16 + e) * rstride] = __float2bfloat16_rn(o1[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (r0 + e < c.t_end) orow[e * rstride] = __float2bfloat16_rn(o0[e]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (r0 + 16 + e < c.t_end) orow[(16 + e) * rstride] = __float2bfloat16_rn(o1[e]);
+            }
+            tc_fence_before();
+            return true;
+        };
         for (int k = 0; ok; ++k) {
-            const int ci = chain_of(k, blockIdx.x, G);
+            const int ci = chain_of(k, cta, G);
             if (ci >= n_chains) break;
             const Chain c = decode_chain(p, ci);
             // S[e] = S[i = 64 wg + e][j] (fp32, registers)
@@ -294,34 +365,38 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
             for (int t = 0; t < c.nch; ++t, ++g) {
                 const uint32_t st = g & 1, ph = (g >> 1) & 1;
                 const int64_t t0 = c.t_begin + (int64_t)t * kC;
-                // ---- E1: Vt^T = U^T - X^T for tokens r = 32 wg + e
+                // ---- E1: Vt^T = U^T - X^T for tokens r = 32 wg + e.  U is read from shared
+                //      memory while MMA1 runs.
                 bool okc = mbar_wait_ab(&fullU[st], ph, p.err, abort);
                 if (rec) CH_MARK(8);
+                float uu[32];
+                if (okc) {
+                    const uint8_t* ub = sm + kSU + st * kPkgUBytes + q * kPkgUQ + (lane & 3) * 4;
+                    const uint32_t cpos = lane >> 2;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int r = 32 * wg + e;
+                        uu[e] = *reinterpret_cast<const float*>(ub + r * 128 + ((cpos ^ (uint32_t)(r & 7)) << 4));
+                    }
+                }
                 okc = okc && mbar_wait_ab(&mma1[st], ph, p.err, abort);
                 if (rec) CH_MARK(9);
                 if (okc) {
                     tc_fence_after();
-                    const uint8_t* ub = sm + kSU + st * kPkgUBytes + q * kPkgUQ + (lane & 3) * 4;
-                    const uint32_t cpos = lane >> 2;
+                    float x0[16], x1[16];
+                    tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg, x0);
+                    tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg + 16, x1);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {  // 16 tokens at a time
-                        float x[16];
-                        tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg + 16 * hf, x);
-                        tmem_ld_wait();
+                    for (int hf = 0; hf < 2; ++hf) {
                         uint32_t hi[8], lo[8];
 #pragma unroll
                         for (int e2 = 0; e2 < 8; ++e2) {
-                            float v2[2];
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int r = 32 * wg + 16 * hf + 2 * e2 + u;
-                                const float uu = *reinterpret_cast<const float*>(
-                                    ub + r * 128 + ((cpos ^ (uint32_t)(r & 7)) << 4));
-                                v2[u] = uu - x[2 * e2 + u];
-                            }
-                            hi[e2] = pack2(v2[0], v2[1]);
-                            lo[e2] = pack2(v2[0] - __uint_as_float(hi[e2] << 16),
-                                           v2[1] - __uint_as_float(hi[e2] & 0xffff0000u));
+                            const float a0 = uu[16 * hf + 2 * e2] - (hf ? x1[2 * e2] : x0[2 * e2]);
+                            const float a1 = uu[16 * hf + 2 * e2 + 1] - (hf ? x1[2 * e2 + 1] : x0[2 * e2 + 1]);
+                            hi[e2] = pack2(a0, a1);
+                            lo[e2] = pack2(a0 - __uint_as_float(hi[e2] << 16),
+                                           a1 - __uint_as_float(hi[e2] & 0xffff0000u));
                         }
                         tmem_st8(tmem + lb + kTV + 16 * wg + 8 * hf, hi);
                         tmem_st8(tmem + lb + kTVlo + 16 * wg + 8 * hf, lo);
@@ -332,6 +407,9 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&vt_ready[st]);
                 if (rec) CH_MARK(10);
+                // ---- E3 of the previous chunk, while MMA2 of this one runs
+                if (t > 0 && !store_out(g - 1, t0 - kC, c)) { ok = false; break; }
+                if (rec) CH_MARK(13);
                 // ---- E2: S^T <- S^T Diag(gamma^C) + dS^T; bf16 copy for the next MMA1
                 okc = okc && mbar_wait_ab(mma2, g & 1, p.err, abort);
                 if (rec) CH_MARK(11);
@@ -339,23 +417,32 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
                     tc_fence_after();
                     const float* gam = reinterpret_cast<const float*>(sm + kSG + (g & 3) * kPkgGBytes) + 64 * wg;
 #pragma unroll
-                    for (int qt = 0; qt < 4; ++qt) {  // 16 key channels at a time
-                        float d[16];
-                        tmem_ld16(tmem + lb + kTDS + 64 * wg + 16 * qt, d);
-                        tmem_ld_wait();
-                        uint32_t pk[8];
+                    for (int hf = 0; hf < 2; ++hf) {  // 32 key channels at a time
+                        float d0[16], d1v[16];
+                        tmem_ld16(tmem + lb + kTDS + 64 * wg + 32 * hf, d0);
+                        tmem_ld16(tmem + lb + kTDS + 64 * wg + 32 * hf + 16, d1v);
+                        float4 gv[8];
 #pragma unroll
-                        for (int e4 = 0; e4 < 4; ++e4) {
-                            const float4 gv = *reinterpret_cast<const float4*>(gam + 16 * qt + 4 * e4);
-                            const int e = 16 * qt + 4 * e4;
-                            S[e] = fmaf(gv.x, S[e], d[4 * e4]);
-                            S[e + 1] = fmaf(gv.y, S[e + 1], d[4 * e4 + 1]);
-                            S[e + 2] = fmaf(gv.z, S[e + 2], d[4 * e4 + 2]);
-                            S[e + 3] = fmaf(gv.w, S[e + 3], d[4 * e4 + 3]);
-                            pk[2 * e4] = pack2(S[e], S[e + 1]);
-                            pk[2 * e4 + 1] = pack2(S[e + 2], S[e + 3]);
+                        for (int e4 = 0; e4 < 8; ++e4)
+                            gv[e4] = *reinterpret_cast<const float4*>(gam + 32 * hf + 4 * e4);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int qt = 0; qt < 2; ++qt) {
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int e4 = 0; e4 < 4; ++e4) {
+                                const float4 g4 = gv[4 * qt + e4];
+                                const int e = 32 * hf + 16 * qt + 4 * e4;
+                                const float* dd = qt ? d1v : d0;
+                                S[e] = fmaf(g4.x, S[e], dd[4 * e4]);
+                                S[e + 1] = fmaf(g4.y, S[e + 1], dd[4 * e4 + 1]);
+                                S[e + 2] = fmaf(g4.z, S[e + 2], dd[4 * e4 + 2]);
+                                S[e + 3] = fmaf(g4.w, S[e + 3], dd[4 * e4 + 3]);
+                                pk[2 * e4] = pack2(S[e], S[e + 1]);
+                                pk[2 * e4 + 1] = pack2(S[e + 2], S[e + 3]);
+                            }
+                            tmem_st8(tmem + lb + kTS + 32 * wg + 16 * hf + 8 * qt, pk);
                         }
-                        tmem_st8(tmem + lb + kTS + 32 * wg + 8 * qt, pk);
                     }
                     tmem_st_wait();
                 }
@@ -363,48 +450,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0 && t + 1 < c.nch) mbar_arrive(s_ready);
                 if (rec) CH_MARK(12);
-                // ---- E3: O^T -> bf16 -> o
-                okc = okc && mbar_wait_ab(mma3, g & 1, p.err, abort);
-                if (rec) CH_MARK(13);
-                if (okc) tc_fence_after();
-                if (t0 + kC <= c.t_end) {
-                    // full chunk: stage the 64 x 128 tile, one TMA store writes it
-                    if (tid == 0) bulk_wait_read0();  // the previous store has read the tile
-                    named_bar_sync(1, 256);
-                    if (okc) {
-                        __nv_bfloat16* so = reinterpret_cast<__nv_bfloat16*>(sm + kSO);
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            float ov[16];
-                            tmem_ld16(tmem + lb + kTD1 + 128 * st + 64 + 32 * wg + 16 * hf, ov);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                so[(32 * wg + 16 * hf + e) * kD + j] = __float2bfloat16_rn(ov[e]);
-                        }
-                    }
-                    fence_async_smem();
-                    if (named_bar_or(1, 256, !okc)) { ok = false; break; }
-                    if (tid == 0) {
-                        tma_store_3d(&p.to, sm + kSO, 0, c.h, (int)t0);
-                        bulk_commit();
-                    }
-                } else {
-                    if (named_bar_or(1, 256, !okc)) { ok = false; break; }
-                    // ragged last chunk of a sequence: rows past its end belong to the next
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        float ov[16];
-                        tmem_ld16(tmem + lb + kTD1 + 128 * st + 64 + 32 * wg + 16 * hf, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int64_t row = t0 + 32 * wg + 16 * hf + e;
-                            if (row < c.t_end)
-                                p.o[((size_t)row * p.H + c.h) * kD + j] = __float2bfloat16_rn(ov[e]);
-                        }
-                    }
-                }
+                if (t + 1 == c.nch && !store_out(g, t0, c)) { ok = false; break; }
                 tc_fence_before();
                 if (rec) CH_MARK(14);
             }
@@ -416,24 +462,20 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         }
     }
 
-    if (tid == 0) bulk_wait0();  // the output tile stores are complete
-    __syncthreads();
+    chain_sync();
     const bool aborted = s_abort != 0;
     // on an abort, let copies and MMAs still in flight land before leaving
-    if (aborted && tid == kCopyT) {
-        for (int s2 = 0; s2 < 2; ++s2) {
-            if (lastPA[s2] >= 0) mbar_wait(&fullPA[s2], lastPA[s2], nullptr);
-            if (lastU[s2] >= 0) mbar_wait(&fullU[s2], lastU[s2], nullptr);
-        }
-        if (lastKC >= 0) mbar_wait(fullKC, lastKC, nullptr);
-        if (lastAT >= 0) mbar_wait(fullAT, lastAT, nullptr);
+    if (aborted && cpart >= 0) {
+        uint64_t* bar = cpart == 0 ? fullPA : cpart == 1 ? fullU : cpart == 2 ? fullKC : fullAT;
+        for (int s2 = 0; s2 < 2; ++s2)
+            if (last_ph[s2] >= 0) mbar_wait(&bar[s2], last_ph[s2], nullptr);
     }
     if (aborted && tid == kMmaT) {
         mma_commit(drain);  // arrives once every MMA issued so far has completed
         mbar_wait(drain, 0, nullptr);
     }
     tc_fence_before();
-    __syncthreads();
+    chain_sync();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, kTCols);
@@ -441,45 +483,5 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
 }
 
 }  // namespace
-
-#ifdef KDA_PHASE_TIMING
-extern "C" int kda_debug_chain_cycles(unsigned long long* out, int n) {
-    if (n > 16) n = 16;
-    if (cudaMemcpyFromSymbol(out, g_chain_phase, n * sizeof(unsigned long long)) != cudaSuccess)
-        return -1;
-    static const unsigned long long zeros[16] = {};
-    return cudaMemcpyToSymbol(g_chain_phase, zeros, sizeof zeros) == cudaSuccess ? n : -1;
-}
-#endif
-
-cudaError_t launch_chain(const ChainArgs& a) {
-    ChainParams p;
-    if (a.T_total > 0 && !make_map(&p.to, a.o, a.T_total, a.H, 128)) return cudaErrorInvalidValue;
-    p.pkg = a.pkg;
-    p.cu = a.cu;
-    p.chunk_off = a.chunk_off;
-    p.order = a.order;
-    p.S0 = a.S0;
-    p.S_out = a.S_out;
-    p.o = static_cast<__nv_bfloat16*>(a.o);
-    p.err = a.err;
-    p.T_total = a.T_total;
-    p.N = a.N;
-    p.H = a.H;
-    p.maxchunks = a.maxchunks;
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kChainSmem);
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t chains = (int64_t)a.N * a.H;
-    const int grid = (int)(chains < sms ? chains : sms);
-    if (grid == 0) return cudaSuccess;
-    ProfScope prof("chain_kernel", a.stream);
-    chain_kernel<<<grid, kChainThreads, kChainSmem, a.stream>>>(p);
-    return cudaGetLastError();
-}
-
 }  // namespace fwdtc
 }  // namespace kda

@@ -71,23 +71,6 @@ inline WsLayout ws_layout(int64_t T_total, int N, int H) {
     return l;
 }
 
-// Chain stage (fwd_chain.cu): for every (sequence, head), serial over its chunks, reads
-// the packages and writes o and the final state.
-struct ChainArgs {
-    const uint8_t* pkg;
-    const int32_t* cu;
-    const int32_t* chunk_off;
-    const int32_t* order;
-    const float* S0;
-    float* S_out;
-    void* o;
-    unsigned* err;
-    int64_t T_total;
-    int N, H, maxchunks;
-    cudaStream_t stream;
-};
-cudaError_t launch_chain(const ChainArgs& a);
-
 // [T_total, H, 128] bf16 tensor map with boxes of `box_cols` columns x 1 head x 64 rows:
 // 64-column boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle, 128-column
 // boxes none (fwd_tc.cu).

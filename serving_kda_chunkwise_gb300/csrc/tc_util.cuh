@@ -101,6 +101,39 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// ------------------------------------------------- flags in global memory --
+// Producer/consumer handoffs between CTAs of one launch (all CTAs co-resident).
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy and async-proxy (bulk copy) accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Wait until *p >= target; false (and the timeout bit set, *abort raised) when the bound
+// runs out, or false at once when *abort is already set.
+__device__ __forceinline__ bool wait_flag_ge(const uint32_t* p, uint32_t target, unsigned* err,
+                                             volatile int* abort) {
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    while (ld_acquire_gpu(p) < target) {
+        if (*abort) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            if (err) atomicOr(err, kDevErrTimeout);
+            *abort = 1;
+            return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
+}
+
 // --------------------------------------------------------------- TMA / bulk --
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1,

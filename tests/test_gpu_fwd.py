@@ -208,3 +208,23 @@ def test_fwd_tensor_core_path_matches_cuda_core_path(kda, monkeypatch):
             assert bf16_norm_err(o_tc[a:b, h], o_cc[a:b, h].astype(np.float64)) < 2e-2
             assert state_err(S_tc[n, h], S_cc[n, h].astype(np.float64)) <= BF16_NORM_TOL
             assert bf16_rms_err(S_tc[n, h], S_cc[n, h].astype(np.float64)) <= BF16_RMS_TOL
+
+
+def test_fwd_fused_matches_two_launch(kda, monkeypatch):
+    """Equal-length sequences without cu_seqlens take the fused form (one cooperative launch,
+    packages handed from the intra stage to the chain stage through a ring in L2).  It runs
+    the same arithmetic as the two-launch form, so the results are bitwise equal, and both
+    meet the parity rule against the oracle."""
+    inp = inputs.forward_inputs(seed=91, B=3, T=1000, H=5, dk=128, dv=128, dtype="bf16",
+                                with_state=True, g_min=-6.0)
+    kda.profile_begin()
+    o_f, S_f = gpu_forward(inp, use_cu=False)
+    names = kda.profile_end()
+    assert "fwd_fused_kernel" in names and "chain_kernel" not in names
+    monkeypatch.setenv("KDA_FWD_FUSED", "0")
+    kda.profile_begin()
+    o_2, S_2 = gpu_forward(inp, use_cu=False)
+    names = kda.profile_end()
+    assert "chain_kernel" in names and "fwd_fused_kernel" not in names
+    assert np.array_equal(o_f, o_2) and np.array_equal(S_f, S_2)
+    check_forward(inp, o_f, S_f, oracle_forward(inp))
