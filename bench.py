@@ -204,8 +204,10 @@ def run_ours(args, rank, world, local_rank, dist):
     dev = torch.device("cuda", local_rank)
     peaks = load_peaks()
     kw = {"H": args.heads} if args.heads else {}
+    if args.tokens:
+        kw["T"] = args.tokens
     sp = inputs.workload_spec(WORKLOAD, seed=1002 + 7919 * rank, **kw)
-    H = sp.H
+    H, T = sp.H, sp.T
     d = sp.to_device(dev)
     stream = torch.cuda.current_stream(dev)
     S_out = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
@@ -583,6 +585,9 @@ def main():
     ap.add_argument("--heads", type=int, default=0,
                     help="run the forward workload with this many heads instead of 32 (a "
                          "smaller case for profiler captures; not a bench line)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="run the forward workload with this many tokens instead of 65536 "
+                         "(a smaller case for profiler captures; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -65,13 +65,13 @@ constexpr int kMmaT = 256;   // lane 0 of warp 8
 constexpr int kCopyT = 288;  // lane 0 of warp 9
 
 // shared memory (1024-aligned offsets)
-constexpr uint32_t kSPA = 0;          // part A, two stages of 32 KB
-constexpr uint32_t kSKC = 65536;      // K~ hi + lo (32 KB)
-constexpr uint32_t kSAT = 98304;      // A hi + lo (16 KB)
-constexpr uint32_t kSU = 114688;      // U, two stages of 32 KB
-constexpr uint32_t kSG = 180224;      // gamma^C, four stages of 512 B
-constexpr uint32_t kSBars = 182272;
-constexpr uint32_t kChainSmem = kSBars + 256 + 1024;
+constexpr uint32_t kChPA = 0;          // part A, two stages of 32 KB
+constexpr uint32_t kChKC = 65536;      // K~ hi + lo (32 KB)
+constexpr uint32_t kChAT = 98304;      // A hi + lo (16 KB)
+constexpr uint32_t kChU = 114688;      // U, two stages of 32 KB
+constexpr uint32_t kChG = 180224;      // gamma^C, four stages of 512 B
+constexpr uint32_t kChBars = 182272;
+constexpr uint32_t kChainSmem = kChBars + 256 + 1024;
 static_assert(kChainSmem <= 232448, "chain kernel exceeds the shared-memory limit");
 
 // TMEM columns: S^T bf16 [0, 64); Vt^T bf16 hi [64, 96), lo [96, 128); D1 for chunk g in
@@ -127,7 +127,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
-    uint64_t* fullPA = reinterpret_cast<uint64_t*>(sm + kSBars);  // [2] part A
+    uint64_t* fullPA = reinterpret_cast<uint64_t*>(sm + kChBars);  // [2] part A
     uint64_t* fullU = fullPA + 2;                                  // [2] U + gamma^C
     uint64_t* fullKC = fullPA + 4;
     uint64_t* fullAT = fullPA + 5;
@@ -166,9 +166,9 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
         constexpr uint32_t id1 = idesc_bf16(128, 128, false, false);
         constexpr uint32_t id2 = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
-        const uint64_t dPA = sdesc_sw128(sbase + kSPA, 0, 1024);
-        const uint64_t dKC = sdesc_sw128(sbase + kSKC, 8192, 1024);
-        const uint64_t dAT = sdesc_sw128(sbase + kSAT, 0, 1024);
+        const uint64_t dPA = sdesc_sw128(sbase + kChPA, 0, 1024);
+        const uint64_t dKC = sdesc_sw128(sbase + kChKC, 8192, 1024);
+        const uint64_t dAT = sdesc_sw128(sbase + kChAT, 0, 1024);
         uint32_t g = 0;
         bool ok = true;
         CH_T0();
@@ -250,23 +250,23 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                     if (!p.fused && t + 3 < c.nch) l2_prefetch(src + 3 * (size_t)kPkgBytes, kPkgBytes);
                     if (g >= 2 && !mbar_wait_ab(&mma1[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
                     mbar_expect_tx(&fullPA[st], kPkgPartA);
-                    bulk_g2s(sm + kSPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
+                    bulk_g2s(sm + kChPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
                     last_ph[st] = (int)((g >> 1) & 1);
                 } else if (cpart == 1) {
                     if (g >= 2 && !mbar_wait_ab(&vt_ready[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
                     mbar_expect_tx(&fullU[st], kPkgUBytes + kPkgGBytes);
-                    bulk_g2s(sm + kSU + st * kPkgUBytes, src + kPkgU, kPkgUBytes, &fullU[st]);
-                    bulk_g2s(sm + kSG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
+                    bulk_g2s(sm + kChU + st * kPkgUBytes, src + kPkgU, kPkgUBytes, &fullU[st]);
+                    bulk_g2s(sm + kChG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
                     last_ph[st] = (int)((g >> 1) & 1);
                 } else if (cpart == 2) {
                     if (g >= 1 && !mbar_wait_ab(mma2, (g - 1) & 1, p.err, abort)) { ok = false; break; }
                     mbar_expect_tx(fullKC, kPkgKTBytes);
-                    bulk_g2s(sm + kSKC, src + kPkgKT, kPkgKTBytes, fullKC);
+                    bulk_g2s(sm + kChKC, src + kPkgKT, kPkgKTBytes, fullKC);
                     last_ph[0] = (int)(g & 1);
                 } else {
                     if (g >= 1 && !mbar_wait_ab(&mma3[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err, abort)) { ok = false; break; }
                     mbar_expect_tx(fullAT, kPkgAQKBytes);
-                    bulk_g2s(sm + kSAT, src + kPkgAQK, kPkgAQKBytes, fullAT);
+                    bulk_g2s(sm + kChAT, src + kPkgAQK, kPkgAQKBytes, fullAT);
                     last_ph[0] = (int)(g & 1);
                 }
             }
@@ -371,7 +371,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (rec) CH_MARK(8);
                 float uu[32];
                 if (okc) {
-                    const uint8_t* ub = sm + kSU + st * kPkgUBytes + q * kPkgUQ + (lane & 3) * 4;
+                    const uint8_t* ub = sm + kChU + st * kPkgUBytes + q * kPkgUQ + (lane & 3) * 4;
                     const uint32_t cpos = lane >> 2;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -415,7 +415,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (rec) CH_MARK(11);
                 if (okc) {
                     tc_fence_after();
-                    const float* gam = reinterpret_cast<const float*>(sm + kSG + (g & 3) * kPkgGBytes) + 64 * wg;
+                    const float* gam = reinterpret_cast<const float*>(sm + kChG + (g & 3) * kPkgGBytes) + 64 * wg;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {  // 32 key channels at a time
                         float d0[16], d1v[16];

@@ -86,6 +86,9 @@ struct IntraParams {
     int fused_C, nct, ring_slots;
     uint32_t* ready;     // [C][ring_slots]: t + 1 once the slot holds chunk t
     uint32_t* consumed;  // [C]: chunks of the chain whose slots the chain stage has released
+    // fused kernel: items are taken from this counter in order (a CTA whose item waits for a
+    // slot holds up no other chain's items); otherwise CTA b takes items b, b + ncta, ...
+    int* item_ctr;
 };
 
 // Shared-memory map of the intra kernel (offsets from a 1024-aligned base).  q and k are
@@ -125,6 +128,7 @@ constexpr uint32_t kTmemCols = 512, kTLo = 256, kTDiag = 160;
 __device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
 
 struct ItemInfo {
+    int item;  // item index (>= the item count: no further item)
     int h, n, L;
     int64_t t0;
     size_t pkg;  // package index (ring slot in the fused kernel)
@@ -162,6 +166,7 @@ __device__ __forceinline__ int4 fetch_item(const IntraParams& p, int item) {
 }
 __device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item, int4 e) {
     ItemInfo it;
+    it.item = item;
     it.n = e.z;
     it.t0 = (static_cast<int64_t>(e.y) << 32) | static_cast<uint32_t>(e.x);
     it.L = e.w;
@@ -179,6 +184,11 @@ __device__ __forceinline__ ItemInfo decode_item(const IntraParams& p, int item, 
         it.pkg = (size_t)it.h * p.maxchunks + chunk;
     }
     return it;
+}
+// The item a CTA takes after `cur` (the first one: cur = -1).
+__device__ __forceinline__ int take_item(const IntraParams& p, int cur, int cta, int ncta) {
+    if (p.item_ctr) return atomicAdd(p.item_ctr, 1);
+    return cur < 0 ? cta : cur + ncta;
 }
 
 // TMA: [64 rows][128] bf16 tiles of one or two tensors for this item (two 64-column
@@ -443,10 +453,18 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
     // The issuing thread walks the item table and publishes each item's description and
     // A_log in s_item / s_alog (two slots by item parity) one item before its use, so the
     // row warps start an item without global loads.
+    // The issuing thread also takes the items: it keeps the index of the item after the one
+    // it publishes (taken one item early, so that a counter's latency is never waited for).
     __shared__ ItemInfo s_item[2];
     __shared__ float s_alog[2];
-    if ((int)cta < n_items && tid == kIss) {
-        const ItemInfo first = decode_item(p, cta, fetch_item(p, cta));
+    int lead_next = n_items;
+    if (tid == kIss) {
+        const int first_item = take_item(p, -1, cta, ncta);
+        s_item[0].item = first_item;
+        if (first_item < n_items) lead_next = take_item(p, first_item, cta, ncta);
+    }
+    if (tid == kIss && s_item[0].item < n_items) {
+        const ItemInfo first = decode_item(p, s_item[0].item, fetch_item(p, s_item[0].item));
         load_tiles(&p.tq, sm + kOffQ, &p.tk, sm + kOffK, first, &qk_bar[0]);
         load_tiles(&p.tv, sm + kVBuf, nullptr, nullptr, first, v_bar);
         load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, first, z_bar);
@@ -457,19 +475,26 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         s_alog[0] = __ldg(p.A_log + first.h);
     }
     intra_sync();
-    if ((int)cta < n_items) load_beta(p, s_item[0], reinterpret_cast<float*>(sm + kBeta), tid);
+    if (s_item[0].item < n_items) load_beta(p, s_item[0], reinterpret_cast<float*>(sm + kBeta), tid);
 
     int iter = 0;
     KDA_PHASE_INIT();
-    for (int item = cta; item < n_items; item += ncta, ++iter) {
+    for (;; ++iter) {
         KDA_PHASE(7);
         const int b = iter & 1;
+        // published before the previous item's last barrier (or the first one's)
+        if (s_item[b].item >= n_items) break;
         uint8_t* qk = sm + b * kQKBuf;
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
         const int itL = s_item[b].L;  // rows of this item (< 64 for a sequence's last chunk)
         const float alog = s_alog[b];
-        const int next = item + ncta;
+        // the next item, known to the issuing thread (which took it one item ago) and
+        // needed by its warp only (that warp loads the next item's beta); the item after it
+        // is taken now
+        const int next = warp == (kIss >> 5) ? __shfl_sync(0xffffffffu, lead_next, kIss & 31) : n_items;
         const bool has_next = next < n_items;
+        int next2 = n_items;
+        if (tid == kIss && has_next) next2 = take_item(p, next, cta, ncta);
         unsigned short beta_nx[2] = {0, 0};  // issuing thread's warp: the next item's beta (bf16)
         float alog_nx = 0.f;                 // issuing thread: the next item's A_log
         // issuing thread: the next item's table entry, decoded once the scan is done
@@ -539,6 +564,7 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         // z is consumed: the issuing thread publishes the next item and fetches its z
         // (issued here, where a long phase follows, so that a slow issue never holds up a
         // barrier)
+        if (tid == kIss && !has_next) s_item[b ^ 1].item = n_items;  // no further item
         if (warp == (kIss >> 5) && has_next) {
             if (tid == kIss) {
                 const ItemInfo nx = decode_item(p, next, raw_next);
@@ -935,6 +961,7 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
                 pub_slot = (int)s_item[b].pkg;
                 pub_val = (uint32_t)s_item[b].ft + 1;
             }
+            lead_next = next2;
         }
     }
     KDA_PHASE_FLUSH();

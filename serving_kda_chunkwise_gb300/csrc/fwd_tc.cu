@@ -160,7 +160,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
 // at once.  Every CTA is resident (cooperative launch), and every wait is bounded.
 constexpr int kFusedThreads = 384;
 constexpr uint32_t kFusedSmem = kIntraSmem > kChainSmem ? kIntraSmem : kChainSmem;
-constexpr int kRingSlots = 8;
+// Ring slots per chain: enough to cover the intra stage's latency from taking a slot to
+// publishing it (about two item periods of a CTA, several chunks of a chain), capped so
+// that the ring stays well inside L2.
+constexpr int kRingSlotsMax = 12, kRingSlotsMin = 8;
+constexpr size_t kRingBytesMax = size_t(64) << 20;
 constexpr int kFusedMaxChains = 64;
 
 struct FusedParams {
@@ -262,18 +266,20 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     // then follows every chain in step), at most kFusedMaxChains chains, and SMs left over
     // for the intra stage.  KDA_FWD_FUSED=0 in the environment selects the two-launch form.
     // The ring and its flags live in the workspace's package region, which holds
-    // H * maxchunks >= C * nct packages: nct > kRingSlots leaves room for both.
+    // H * maxchunks >= C * nct packages: nct > ring_slots leaves room for both.
     const int C = a.N * a.H;
     const int64_t nct_all = a.N > 0 ? (a.T_total / a.N + kC - 1) / kC : 0;
+    int ring_slots = C > 0 ? (int)(kRingBytesMax / ((size_t)C * kPkgBytes)) : 0;
+    ring_slots = ring_slots > kRingSlotsMax ? kRingSlotsMax : ring_slots;
     const char* fenv = getenv("KDA_FWD_FUSED");
     const bool fused = a.cu_seqlens == nullptr && a.T_total > 0 && C <= kFusedMaxChains &&
-                       sms - C >= 16 && nct_all > kRingSlots &&
+                       sms - C >= 16 && ring_slots >= kRingSlotsMin && nct_all > ring_slots &&
                        !(fenv && strcmp(fenv, "0") == 0);
     // fused: the ring [C][kRingSlots] packages, then ready flags [C][kRingSlots] and consumed
     // counters [C], inside the package region of the workspace
     uint8_t* ring = pkg;
-    uint32_t* flags = reinterpret_cast<uint32_t*>(pkg + (size_t)C * kRingSlots * kPkgBytes);
-    const int n_flags = fused ? C * (kRingSlots + 1) : 0;
+    uint32_t* flags = reinterpret_cast<uint32_t*>(pkg + (size_t)C * ring_slots * kPkgBytes);
+    const int n_flags = fused ? C * (ring_slots + 1) + 1 : 0;  // + the item counter
 
     {
         ProfScope prof("plan_kernel", a.stream);
@@ -319,11 +325,12 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         const int64_t len = a.T_total / a.N;
         ip.fused_C = C;
         ip.nct = (int)((len + kC - 1) / kC);
-        ip.ring_slots = kRingSlots;
+        ip.ring_slots = ring_slots;
         ip.ready = flags;
-        ip.consumed = flags + (size_t)C * kRingSlots;
+        ip.consumed = flags + (size_t)C * ring_slots;
+        ip.item_ctr = reinterpret_cast<int*>(flags + (size_t)C * (ring_slots + 1));
         cp.fused = 1;
-        cp.ring_slots = kRingSlots;
+        cp.ring_slots = ring_slots;
         cp.ring = ring;
         cp.ready = ip.ready;
         cp.consumed = ip.consumed;

@@ -215,7 +215,7 @@ def test_fwd_fused_matches_two_launch(kda, monkeypatch):
     packages handed from the intra stage to the chain stage through a ring in L2).  It runs
     the same arithmetic as the two-launch form, so the results are bitwise equal, and both
     meet the parity rule against the oracle."""
-    inp = inputs.forward_inputs(seed=91, B=3, T=1000, H=5, dk=128, dv=128, dtype="bf16",
+    inp = inputs.forward_inputs(seed=91, B=3, T=2000, H=5, dk=128, dv=128, dtype="bf16",
                                 with_state=True, g_min=-6.0)
     kda.profile_begin()
     o_f, S_f = gpu_forward(inp, use_cu=False)
