@@ -121,18 +121,23 @@ kda_status_t kda_fwd_chunked(const void *q, const void *k, const void *v, const 
 
 /*
  * kda_fwd_chunked_softplus -- the same chunked forward with the gate the bound replaces
- * ([blog] "Chunkwise parallel form"): g = -e^{A_log[h]} Softplus(z), unbounded below, so
- * no decay factor can be split into a bounded row factor and column factor.  This runs the
- * explicit path (every pair's decay e^{G_r - G_i}, exponent <= 0, formed on CUDA cores in
- * fp32), a comparison variant: it measures what the bound buys.  Arguments as
- * kda_fwd_chunked without g_min and without a workspace (none is needed).  z must be finite
- * or -inf.
+ * ([blog] "Chunkwise parallel form"): g = -e^{A_log[h]} Softplus(z), unbounded below, so a
+ * sub-tile's decay can leave the exponent range and no decay factor of a diagonal sub-tile
+ * splits into a bounded row factor and column factor.  A comparison variant: it measures
+ * what the bound buys.  bf16 with dk = dv = 128 runs the mixed path the page describes: the
+ * off-diagonal 16-token sub-tile pairs on the tensor cores with sub-tile-start references
+ * (every factor <= 1), the diagonal 16 x 16 blocks per pair on CUDA cores (e^{G_r - G_i},
+ * exponent <= 0, in fp32).  Other shapes and fp32 run the explicit per-pair path (every
+ * pair on CUDA cores).  Arguments as kda_fwd_chunked without g_min; the workspace is sized
+ * by kda_fwd_workspace_size (0 bytes, and workspace may be NULL, on the explicit path).
+ * z must be finite or -inf.
  */
 kda_status_t kda_fwd_chunked_softplus(const void *q, const void *k, const void *v,
                                       const void *beta, const void *z, const float *A_log,
                                       const float *S0, float *S_out, const int32_t *cu_seqlens,
                                       int N, int64_t T_total, int H, int dk, int dv,
-                                      kda_dtype_t io_dt, void *o, kda_stream_t stream);
+                                      kda_dtype_t io_dt, void *o, void *workspace,
+                                      size_t ws_bytes, kda_stream_t stream);
 
 /*
  * kda_bwd -- gradients of kda_fwd_chunked's outputs ([blog] "Kimi Delta Attention": the

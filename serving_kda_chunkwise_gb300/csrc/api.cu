@@ -217,7 +217,8 @@ kda_status_t kda_fwd_chunked_softplus(const void* q, const void* k, const void* 
                                       const void* beta, const void* z, const float* A_log,
                                       const float* S0, float* S_out, const int32_t* cu_seqlens,
                                       int N, int64_t T_total, int H, int dk, int dv,
-                                      kda_dtype_t io_dt, void* o, kda_stream_t stream) {
+                                      kda_dtype_t io_dt, void* o, void* workspace,
+                                      size_t ws_bytes, kda_stream_t stream) {
     t_last_error.clear();
     KDA_REQUIRE(io_dt == KDA_F32 || io_dt == KDA_BF16, "io_dt=%d is not a kda_dtype_t", (int)io_dt);
     KDA_REQUIRE(N >= 0, "N=%d must be >= 0", N);
@@ -245,15 +246,25 @@ kda_status_t kda_fwd_chunked_softplus(const void* q, const void* k, const void* 
     KDA_OPTIONAL_PTR(S0, "S0");
     KDA_OPTIONAL_PTR(S_out, "S_out");
     KDA_OPTIONAL_PTR(cu_seqlens, "cu_seqlens");
+    const size_t need = kda_fwd_workspace_size(T_total, N, H, dk, dv, io_dt);
+    if (need > 0) {
+        KDA_REQUIRE_PTR(workspace, "workspace");
+        KDA_REQUIRE(ws_bytes >= need, "workspace of %zu bytes is smaller than the %zu needed",
+                    ws_bytes, need);
+    }
     kda::FwdArgs a{};
     a.q = q; a.k = k; a.v = v; a.beta = beta; a.z = z;
     a.A_log = A_log; a.g_min = -1.f; a.S0 = S0; a.S_out = S_out;
     a.cu_seqlens = cu_seqlens; a.N = N; a.T_total = T_total; a.H = H; a.dk = dk; a.dv = dv;
     a.io_bf16 = (io_dt == KDA_BF16); a.gate_kind = 1; a.o = o;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
     a.dev_err = device_error_ptr();
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     if (a.dev_err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
-    cudaError_t e = kda::launch_fwd_generic(a);
+    // bf16 with d = 128: the mixed path (tensor cores off the diagonal sub-tiles); otherwise
+    // the explicit per-pair path
+    cudaError_t e =
+        use_tc_path(dk, dv, io_dt) ? kda::launch_fwd_tc(a) : kda::launch_fwd_generic(a);
     if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_chunked_softplus launch");
     return KDA_OK;
 }

@@ -127,6 +127,32 @@ constexpr uint32_t kTmemCols = 512, kTLo = 256, kTDiag = 160;
 
 __device__ __constant__ int kStkOff[4] = {0, 16, 48, 96};  // B-stack row offset per version
 
+// Gate kinds.  kGateBounded: g = g_min Sigmoid(e^{A_h} z).  kGateSoftplus: the gate the bound
+// replaces, g = -e^{A_h} Softplus(z), on the mixed path of the same page and section: with
+// no bound, a sub-tile's decay can exceed the exponent range, so every factor must stay
+// <= 1.  The reference of sub-tile s is then G at its start (rho_s = G_{16 s - 1}, rho_0 = 0):
+// the row factor e^{G_r - rho_s} (r in sub-tile s) and the column operand
+// k_i e^{rho_s - G_i} (i < 16 s) are both <= 1, so the off-diagonal sub-tile pairs stay on
+// the tensor cores (three column versions, s = 1..3, 96 stack rows), while the diagonal
+// 16 x 16 blocks, where no such split exists, are formed per pair on CUDA cores as
+// sum_c q_rc k_ic e^{G_rc - G_ic} (exponent <= 0), during the Gram MMAs.
+constexpr int kGateBounded = 0, kGateSoftplus = 1;
+// B-stack block stride (two 64-channel blocks): 160 rows, or 96 on the mixed path
+template <int kGate>
+__device__ __forceinline__ constexpr uint32_t stk_blk() { return kGate == kGateBounded ? 20480u : 12288u; }
+// mixed path: the stack row offset of version s = 1..3 (0, 16, 48)
+__device__ __forceinline__ int stk_off_sp(int s) { return 8 * s * (s - 1); }
+// mixed path: G (fp32 [64 rows][128]) during the Gram MMAs, then the diagonal blocks
+// A_d, L_d (fp32 [4 sub-tiles][16][16] each); the 32 KB after the 96-row stack
+constexpr uint32_t kSpXch = kBStk + 24576;
+static_assert(kSpXch + 32768 <= kXch, "the mixed path's exchange must fit before rho");
+
+__device__ __forceinline__ float lg2f(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 struct ItemInfo {
     int item;  // item index (>= the item count: no further item)
     int h, n, L;
@@ -215,6 +241,21 @@ __device__ __forceinline__ float ex2f(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// The gate in log2 units (G2 = G log2 e, so that every decay factor is one ex2).
+//   bounded:  g_min Sigmoid(e^{A_h} z) log2 e = gmin2 / (1 + 2^{-scale2 z}),
+//             scale2 = e^{A_h} log2 e, gmin2 = g_min log2 e;
+//   softplus: -e^{A_h} Softplus(z) log2 e = -eA (max(z, 0) log2 e + log2(1 + 2^{-|z| log2 e})),
+//             eA = e^{A_h}; z = -inf gives -0 (alpha = 1), z must be finite otherwise.
+template <int kGate>
+__device__ __forceinline__ float gate2(float z, float scale2, float gmin2, float eA) {
+    if constexpr (kGate == kGateBounded) {
+        return __fdividef(gmin2, 1.f + ex2f(-scale2 * z));
+    } else {
+        constexpr float kLog2e = 1.4426950408889634f;
+        return -eA * fmaf(fmaxf(z, 0.f), kLog2e, lg2f(1.f + ex2f(-fabsf(z) * kLog2e)));
+    }
 }
 
 // 8 consecutive bf16 of a swizzled tile <-> fp32 registers
@@ -409,7 +450,131 @@ __device__ __forceinline__ void solve_tril64(const float* sL, float* sT, float* 
     intra_sync();
 }
 
+// Mixed path: the diagonal 16 x 16 blocks of both Grams, per pair on CUDA cores.  Thread
+// (sub-tile ds, row pair dp, channel slice dsl) takes rows ra = 16 ds + dp and
+// rb = 16 ds + 15 - dp (17 pairs together, the same for every thread) over the 16 channels
+// [16 dsl, 16 dsl + 16); the 8 slices of a row pair are adjacent lanes and are summed by a
+// reduce-scatter (each lane ends with 6 of the pair sums).  G comes from `xg` (fp32 [64][128],
+// written by every thread); the blocks go to the same region afterwards: A_d at xg, L_d at
+// xg + 1024 (fp32 [4][16][16], row-local index then column-local index; entries above the
+// diagonal are not written).  Rows and columns at or past L read as zero.
+__device__ __forceinline__ void diag_blocks(const uint8_t* qk, float* xg, const float* sBeta,
+                                            int itL, int tid) {
+    const int ds = tid >> 6, dp = (tid >> 3) & 7, dsl = tid & 7;
+    const int ra = 16 * ds + dp, rb = 16 * ds + 15 - dp;
+    float aA[8], aL[8], bA[16], bL[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        bA[j] = 0.f;
+        bL[j] = 0.f;
+        if (j < 8) {
+            aA[j] = 0.f;
+            aL[j] = 0.f;
+        }
+    }
+#pragma unroll 1
+    for (int hc = 0; hc < 2; ++hc) {
+        const int c0 = 16 * dsl + 8 * hc;  // 8 channels: one 16-byte chunk of a tile row
+        const uint32_t blk = (c0 >> 6) * 8192;
+        const int chk = (c0 & 63) >> 3;
+        float qa[8], ka[8], qb[8], kb[8], Ga[8], Gb[8];
+        ld8(qk + kOffQ + blk + sw128_chunk(ra, chk), qa);
+        ld8(qk + kOffK + blk + sw128_chunk(ra, chk), ka);
+        ld8(qk + kOffQ + blk + sw128_chunk(rb, chk), qb);
+        ld8(qk + kOffK + blk + sw128_chunk(rb, chk), kb);
+        {
+            const float4* pa = reinterpret_cast<const float4*>(xg + ra * 128 + c0);
+            const float4* pb = reinterpret_cast<const float4*>(xg + rb * 128 + c0);
+            const float4 a0 = pa[0], a1 = pa[1], b0 = pb[0], b1 = pb[1];
+            Ga[0] = a0.x; Ga[1] = a0.y; Ga[2] = a0.z; Ga[3] = a0.w;
+            Ga[4] = a1.x; Ga[5] = a1.y; Ga[6] = a1.z; Ga[7] = a1.w;
+            Gb[0] = b0.x; Gb[1] = b0.y; Gb[2] = b0.z; Gb[3] = b0.w;
+            Gb[4] = b1.x; Gb[5] = b1.y; Gb[6] = b1.z; Gb[7] = b1.w;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (ra >= itL) { qa[e] = 0.f; ka[e] = 0.f; }
+            if (rb >= itL) { qb[e] = 0.f; kb[e] = 0.f; }
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int i = 16 * ds + j;
+            float ki[8], Gi[8];
+            ld8(qk + kOffK + blk + sw128_chunk(i, chk), ki);
+            {
+                const float4* pi = reinterpret_cast<const float4*>(xg + i * 128 + c0);
+                const float4 i0 = pi[0], i1 = pi[1];
+                Gi[0] = i0.x; Gi[1] = i0.y; Gi[2] = i0.z; Gi[3] = i0.w;
+                Gi[4] = i1.x; Gi[5] = i1.y; Gi[6] = i1.z; Gi[7] = i1.w;
+            }
+            const bool live = i < itL;
+            if (j <= 15 - dp) {  // i <= rb
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float kf = live ? ki[e] * ex2f(Gb[e] - Gi[e]) : 0.f;
+                    bA[j] = fmaf(qb[e], kf, bA[j]);
+                    bL[j] = fmaf(kb[e], kf, bL[j]);
+                }
+            }
+            if (j < 8) {
+                if (j <= dp) {  // i <= ra
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float kf = live ? ki[e] * ex2f(Ga[e] - Gi[e]) : 0.f;
+                        aA[j] = fmaf(qa[e], kf, aA[j]);
+                        aL[j] = fmaf(ka[e], kf, aL[j]);
+                    }
+                }
+            }
+        }
+    }
+    // reduce-scatter over the 8 slices: values [bA 16 | bL 16 | aA 8 | aL 8]; after the
+    // rounds with lane masks 4, 2, 1 the lane with slice bits (b2 b1 b0) holds the sums of
+    // values 24 b2 + 12 b1 + 6 b0 + u, u < 6
+    float V[48];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        V[j] = bA[j];
+        V[16 + j] = bL[j];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        V[32 + j] = aA[j];
+        V[40 + j] = aL[j];
+    }
+    const bool b2 = (dsl >> 2) & 1, b1 = (dsl >> 1) & 1, b0 = dsl & 1;
+    float W1[24], W2[12], W3[6];
+#pragma unroll
+    for (int t = 0; t < 24; ++t)
+        W1[t] = (b2 ? V[24 + t] : V[t]) + __shfl_xor_sync(0xffffffffu, b2 ? V[t] : V[24 + t], 4);
+#pragma unroll
+    for (int t = 0; t < 12; ++t)
+        W2[t] = (b1 ? W1[12 + t] : W1[t]) + __shfl_xor_sync(0xffffffffu, b1 ? W1[t] : W1[12 + t], 2);
+#pragma unroll
+    for (int t = 0; t < 6; ++t)
+        W3[t] = (b0 ? W2[6 + t] : W2[t]) + __shfl_xor_sync(0xffffffffu, b0 ? W2[t] : W2[6 + t], 1);
+    intra_sync();  // every thread has read G: the region takes the blocks
+    float* dA = xg;
+    float* dL = xg + 1024;
+#pragma unroll
+    for (int u = 0; u < 6; ++u) {
+        const int idx = 24 * b2 + 12 * b1 + 6 * b0 + u;
+        const bool rowb = idx < 32;
+        const bool isL = rowb ? idx >= 16 : idx >= 40;
+        const int j = rowb ? (idx & 15) : (idx - 32) & 7;
+        const int rl = rowb ? 15 - dp : dp;
+        const int o = (16 * ds + rl) * 16 + j;
+        if (isL)
+            dL[o] = (j < rl) ? W3[u] * sBeta[16 * ds + rl] : 0.f;
+        else
+            dA[o] = W3[u];
+    }
+    intra_sync();  // the blocks are complete
+}
+
+template <int kGate>
 __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_raw, int cta, int ncta) {
+    constexpr uint32_t kStkBlk = stk_blk<kGate>();
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -517,7 +682,8 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         float G[4][8], gl[8], pre[8];
         float* xtot = xrho + 512;  // [128]: G2 of the chunk's last row
         {
-            const float scale2 = expf(alog) * 1.4426950408889634f;  // e^{A_log} log2 e
+            const float eA = expf(alog);
+            const float scale2 = eA * 1.4426950408889634f;  // e^{A_log} log2 e
             const float gmin2 = p.g_min * 1.4426950408889634f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -530,7 +696,7 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
                 for (int e = 0; e < 8; ++e) {
                     // evaluated for every row and masked after (a conditional evaluation
                     // serialises the special-function work)
-                    const float g = __fdividef(gmin2, 1.f + ex2f(-scale2 * zz[e]));
+                    const float g = gate2<kGate>(zz[e], scale2, gmin2, eA);
                     acc[e] += live ? g : 0.f;
                     G[i][e] = acc[e];
                 }
@@ -600,9 +766,18 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
             }
         }
         KDA_PHASE(10);
-        if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
+        if constexpr (kGate == kGateBounded) {
+            if ((rg & 3) == 1)  // rows 4 rg + 3 = 16 s + 7: the reference of sub-tile s
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
+                for (int e = 0; e < 8; ++e) xrho[sub * 128 + ch0 + e] = G[3][e];
+        } else {
+            if ((rg & 3) == 3 && sub < 3)  // row 16 (s + 1) - 1: the reference of sub-tile s + 1
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xrho[(sub + 1) * 128 + ch0 + e] = G[3][e];
+            if (rg == 0)  // sub-tile 0 starts at the chunk start
+#pragma unroll
+                for (int e = 0; e < 8; ++e) xrho[ch0 + e] = 0.f;
+        }
         if (mbar_wait(&qk_bar[b], (iter >> 1) & 1, p.err)) {
             if (tid == kIss) pend_q[b] = -1;
         } else {
@@ -644,20 +819,27 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
             if (lane == 0) s_alog[b ^ 1] = alog_nx;
         }
 
-        // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}; the
-        //      column operand of version s2 >= s is k_r e^{rho_s2 - G_r}.
+        // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}.
+        //      Bounded gate: the column operand of version s2 >= s is k_r e^{rho_s2 - G_r},
+        //      own version hi + lo.  Mixed path: versions s2 > s only, k_r e^{rho_s2 - G_r}
+        //      formed as e^{rho_{s+1} - G_r} e^{rho_s2 - rho_{s+1}} (both factors <= 1).
         {
-            // Ev[v][e] = e^{rho_{s2} - rho_s} for the later sub-tiles s2 = sub + 1 + v (<= 1;
-            // may underflow to 0, which drops Gram terms below e^-13 of their neighbours):
-            // the column operand of version s2 is then k e^{rho_s - G} Ev.
-            float rho[8], Ev[3][8];
+            // Ev[v][e] = e^{rho_{s2} - rho_b} for the later sub-tiles s2 = sub + 1 + v, with
+            // rho_b = rho_s (bounded) or rho_{s+1} (mixed); <= 1 and may underflow to 0,
+            // which drops Gram terms below e^-13 of their neighbours (bounded gate) or terms
+            // whose true factor underflows too (mixed path)
+            float rho[8], rhob[8], Ev[3][8];
+            const int sb = kGate == kGateBounded ? sub : min(sub + 1, 3);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) rho[e] = xrho[sub * 128 + ch0 + e];  // (log2 units, as G)
+            for (int e = 0; e < 8; ++e) {
+                rho[e] = xrho[sub * 128 + ch0 + e];  // (log2 units, as G)
+                rhob[e] = kGate == kGateBounded ? rho[e] : xrho[sb * 128 + ch0 + e];
+            }
 #pragma unroll
             for (int v = 0; v < 3; ++v) {
                 const int s2 = min(sub + 1 + v, 3);  // entries past sub-tile 3 are unused
 #pragma unroll
-                for (int e = 0; e < 8; ++e) Ev[v][e] = ex2f(xrho[s2 * 128 + ch0 + e] - rho[e]);
+                for (int e = 0; e < 8; ++e) Ev[v][e] = ex2f(xrho[s2 * 128 + ch0 + e] - rhob[e]);
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -673,7 +855,7 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
                 for (int e = 0; e < 8; ++e) {
                     if (!ok) { qv[e] = 0.f; kv[e] = 0.f; }
                     e1[e] = ex2f(G[i][e] - rho[e]);
-                    dc[e] = ex2f(rho[e] - G[i][e]);
+                    dc[e] = ex2f(rhob[e] - G[i][e]);
                 }
                 uint4 hi, lo;
 #pragma unroll
@@ -684,20 +866,23 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
 #pragma unroll
                 for (int e = 0; e < 8; ++e) t[e] = br * kv[e] * e1[e];
                 *reinterpret_cast<uint4*>(sm + kAStk + o128 + 64 * 128) = pk8(t);
+                if constexpr (kGate == kGateBounded) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e];
-                pk8_hilo(t, hi, lo);
-                *reinterpret_cast<uint4*>(
-                    sm + kBStk + (cg >> 3) * 20480 + sw128_chunk(kStkOff[sub] + r, cg & 7)) = hi;
-                *reinterpret_cast<uint4*>(sm + kBLo + o64) = lo;
+                    for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e];
+                    pk8_hilo(t, hi, lo);
+                    *reinterpret_cast<uint4*>(sm + kBStk + (cg >> 3) * kStkBlk +
+                                              sw128_chunk(kStkOff[sub] + r, cg & 7)) = hi;
+                    *reinterpret_cast<uint4*>(sm + kBLo + o64) = lo;
+                }
 #pragma unroll
                 for (int v = 0; v < 3; ++v) {
                     const int s2 = sub + 1 + v;
                     if (s2 < 4) {  // uniform within a warp
 #pragma unroll
                         for (int e = 0; e < 8; ++e) t[e] = kv[e] * dc[e] * Ev[v][e];
-                        *reinterpret_cast<uint4*>(sm + kBStk + (cg >> 3) * 20480 +
-                                                  sw128_chunk(kStkOff[s2] + r, cg & 7)) = pk8(t);
+                        const int srow = kGate == kGateBounded ? kStkOff[s2] : stk_off_sp(s2);
+                        *reinterpret_cast<uint4*>(sm + kBStk + (cg >> 3) * kStkBlk +
+                                                  sw128_chunk(srow + r, cg & 7)) = pk8(t);
                     }
                 }
             }
@@ -719,7 +904,8 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         //      D_lo = Q'_lo Bstack_hi^T (its k-side lanes are unused)
         if (tid == kIss) {
             tc_fence_after();
-            constexpr uint32_t id160 = idesc_bf16(128, 160, false, false);
+            // N = the stack's rows: 160 (four versions) or 96 (mixed path: three)
+            constexpr uint32_t idN = idesc_bf16(128, kGate == kGateBounded ? 160 : 96, false, false);
             constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
             // descriptors differ only in the start-address field (address / 16)
             const uint64_t dA = sdesc_sw128(sbase + kAStk, 0, 1024);
@@ -730,16 +916,18 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t kofs = (ks & 3) * 32;
                 const uint64_t ah = dA + (((ks >> 2) * 16384 + kofs) >> 4);
-                const uint64_t bh = dB + (((ks >> 2) * 20480 + kofs) >> 4);
-                mma_bf16(tmem, ah, bh, id160, ks > 0);
-                mma_bf16(tmem + kTLo, dAl + (((ks >> 2) * 8192 + kofs) >> 4), bh, id160, ks > 0);
+                const uint64_t bh = dB + (((ks >> 2) * kStkBlk + kofs) >> 4);
+                mma_bf16(tmem, ah, bh, idN, ks > 0);
+                mma_bf16(tmem + kTLo, dAl + (((ks >> 2) * 8192 + kofs) >> 4), bh, idN, ks > 0);
             }
-            // diagonal-column lo parts of all four versions at once: D' = A_hi Blo^T
+            if constexpr (kGate == kGateBounded) {
+                // diagonal-column lo parts of all four versions at once: D' = A_hi Blo^T
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t kofs = (ks & 3) * 32;
-                mma_bf16(tmem + kTDiag, dA + (((ks >> 2) * 16384 + kofs) >> 4),
-                         dBl + (((ks >> 2) * 8192 + kofs) >> 4), id64, ks > 0);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kofs = (ks & 3) * 32;
+                    mma_bf16(tmem + kTDiag, dA + (((ks >> 2) * 16384 + kofs) >> 4),
+                             dBl + (((ks >> 2) * 8192 + kofs) >> 4), id64, ks > 0);
+                }
             }
             mma_commit(mma_bar);
         }
@@ -780,6 +968,21 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         }
         }
 
+        // ---- mixed path, while the Gram MMAs run: the diagonal 16 x 16 blocks per pair,
+        //      A_d[r][i] = sum_c q_rc k_ic 2^{G_rc - G_ic} (i <= r) and
+        //      L_d[r][i] = beta_r sum_c k_rc k_ic 2^{G_rc - G_ic} (i < r), r, i in one sub-tile
+        if constexpr (kGate == kGateSoftplus) {
+            float* xg = reinterpret_cast<float*>(sm + kSpXch);  // G [64][128]
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float4* d = reinterpret_cast<float4*>(xg + (4 * rg + i) * 128 + ch0);
+                d[0] = make_float4(G[i][0], G[i][1], G[i][2], G[i][3]);
+                d[1] = make_float4(G[i][4], G[i][5], G[i][6], G[i][7]);
+            }
+            intra_sync();
+            diag_blocks(qk, xg, sBeta, itL, tid);
+        }
+
         if (!mbar_wait(mma_bar, mma_phase & 1, p.err)) s_abort = 1;
         ++mma_phase;
         tc_fence_after();
@@ -788,37 +991,85 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         // ---- Gram epilogue: q-side rows -> A tile (bf16 hi + lo), k-side rows -> L (fp32).
         //      TMEM lane m = 32 (warp % 4) + lane; the groups of 16 columns a lane quadrant
         //      needs are split between the two warpgroups.
-        {
+        if constexpr (kGate == kGateBounded) {
+            {
+                const int quad = warp & 3, wg = warp >> 2;
+                const int m = 32 * quad + lane;
+                const int side = m >> 6, r = m & 63, s = r >> 4;
+                float* sL = reinterpret_cast<float*>(sm + kSL);
+                uint8_t* aq = sm + kAqkTile;
+                // rows 0..31 of a side need groups 0..2 (versions 0, 1); rows 32..63 groups 3..9
+                const int g_lo = (quad & 1) ? (wg ? 7 : 3) : (wg ? 2 : 0);
+                const int g_hi = (quad & 1) ? (wg ? 10 : 7) : (wg ? 3 : 2);
+                for (int g = g_lo; g < g_hi; ++g) {
+                    float v[16], vl[16], vd[16];
+                    const int sg = (g == 0) ? 0 : (g < 3) ? 1 : (g < 6) ? 2 : 3;
+                    const int ib = 16 * g - kStkOff[sg];
+                    const bool diag = (ib == 16 * sg);  // this group holds version sg's own sub-tile
+                    tmem_ld16(tmem + lane_base + 16 * g, v);
+                    tmem_ld16(tmem + lane_base + kTLo + 16 * g, vl);
+                    if (diag) tmem_ld16(tmem + lane_base + kTDiag + 16 * sg, vd);
+                    tmem_ld_wait();
+                    if (diag)
+    #pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] += vd[e];
+                    if (sg == s) {
+                        if (side == 0) {
+    #pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                float a8[8];
+    #pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const int j0 = 8 * hf + e;
+                                    a8[e] = (ib + j0 <= r) ? v[j0] + vl[j0] : 0.f;
+                                }
+                                uint4 hi, lo;
+                                pk8_hilo(a8, hi, lo);
+                                *reinterpret_cast<uint4*>(aq + sw128_chunk(r, (ib >> 3) + hf)) = hi;
+                                *reinterpret_cast<uint4*>(sm + kAqkLoTile +
+                                                          sw128_chunk(r, (ib >> 3) + hf)) = lo;
+                            }
+                        } else {
+    #pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                sL[r * kLd + ib + e] = (ib + e < r) ? v[e] : 0.f;
+                        }
+                    }
+                }
+                if (side == 0 && wg == 0)  // columns past this sub-tile's version are zero
+                    for (int ch = 2 * (s + 1); ch < 8; ++ch) {
+                        *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(sm + kAqkLoTile + sw128_chunk(r, ch)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+            }
+        } else {
+            // mixed path: version s (of rows in sub-tile s = 1..3) holds columns i < 16 s in
+            // TMEM groups gbase(s) + i / 16 (gbase = 0, 1, 3); the diagonal block comes from
+            // the per-pair pass.  Groups by warp: lane quadrants 0 / 2 (rows 0..31 of a side)
+            // need group 0, quadrants 1 / 3 (rows 32..63) groups 1..5; warpgroup 0 takes
+            // groups 0..3, warpgroup 1 groups 4, 5 and the diagonal blocks.
             const int quad = warp & 3, wg = warp >> 2;
             const int m = 32 * quad + lane;
-            const int side = m >> 6, r = m & 63, s = r >> 4;
+            const int side = m >> 6, r = m & 63, s = r >> 4, rl = r & 15;
             float* sL = reinterpret_cast<float*>(sm + kSL);
             uint8_t* aq = sm + kAqkTile;
-            // rows 0..31 of a side need groups 0..2 (versions 0, 1); rows 32..63 groups 3..9
-            const int g_lo = (quad & 1) ? (wg ? 7 : 3) : (wg ? 2 : 0);
-            const int g_hi = (quad & 1) ? (wg ? 10 : 7) : (wg ? 3 : 2);
+            const int g_lo = (quad & 1) ? (wg ? 4 : 1) : 0;
+            const int g_hi = (quad & 1) ? (wg ? 6 : 4) : (wg ? 0 : 1);
             for (int g = g_lo; g < g_hi; ++g) {
-                float v[16], vl[16], vd[16];
-                const int sg = (g == 0) ? 0 : (g < 3) ? 1 : (g < 6) ? 2 : 3;
-                const int ib = 16 * g - kStkOff[sg];
-                const bool diag = (ib == 16 * sg);  // this group holds version sg's own sub-tile
+                float v[16], vl[16];
+                const int sg = (g == 0) ? 1 : (g < 3) ? 2 : 3;
+                const int ib = 16 * (g - stk_off_sp(sg) / 16);
                 tmem_ld16(tmem + lane_base + 16 * g, v);
                 tmem_ld16(tmem + lane_base + kTLo + 16 * g, vl);
-                if (diag) tmem_ld16(tmem + lane_base + kTDiag + 16 * sg, vd);
                 tmem_ld_wait();
-                if (diag)
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) v[e] += vd[e];
                 if (sg == s) {
                     if (side == 0) {
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
                             float a8[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j0 = 8 * hf + e;
-                                a8[e] = (ib + j0 <= r) ? v[j0] + vl[j0] : 0.f;
-                            }
+                            for (int e = 0; e < 8; ++e) a8[e] = v[8 * hf + e] + vl[8 * hf + e];
                             uint4 hi, lo;
                             pk8_hilo(a8, hi, lo);
                             *reinterpret_cast<uint4*>(aq + sw128_chunk(r, (ib >> 3) + hf)) = hi;
@@ -827,12 +1078,31 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
                         }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            sL[r * kLd + ib + e] = (ib + e < r) ? v[e] : 0.f;
+                        for (int e = 0; e < 16; ++e) sL[r * kLd + ib + e] = v[e];
                     }
                 }
             }
-            if (side == 0 && wg == 0)  // columns past this sub-tile's version are zero
+            if (wg == 1) {  // the diagonal block of this row (masked and beta-scaled already
+                            // for L; A masked here)
+                const float* dA = reinterpret_cast<const float*>(sm + kSpXch) + (16 * s + rl) * 16;
+                const float* dL = reinterpret_cast<const float*>(sm + kSpXch) + 1024 + (16 * s + rl) * 16;
+                if (side == 0) {
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        float a8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) a8[e] = (8 * hf + e <= rl) ? dA[8 * hf + e] : 0.f;
+                        uint4 hi, lo;
+                        pk8_hilo(a8, hi, lo);
+                        *reinterpret_cast<uint4*>(aq + sw128_chunk(r, 2 * s + hf)) = hi;
+                        *reinterpret_cast<uint4*>(sm + kAqkLoTile + sw128_chunk(r, 2 * s + hf)) = lo;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) sL[r * kLd + 16 * s + e] = (e < rl) ? dL[e] : 0.f;
+                }
+            }
+            if (side == 0 && wg == 0)  // columns past the diagonal block are zero
                 for (int ch = 2 * (s + 1); ch < 8; ++ch) {
                     *reinterpret_cast<uint4*>(aq + sw128_chunk(r, ch)) = make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4*>(sm + kAqkLoTile + sw128_chunk(r, ch)) =

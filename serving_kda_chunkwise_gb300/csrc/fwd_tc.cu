@@ -143,9 +143,10 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 
 // ============================================================== kernels ====
 
+template <int kGate>
 __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_constant__ IntraParams p) {
     extern __shared__ uint8_t smem_raw[];
-    intra_body(p, smem_raw, blockIdx.x, gridDim.x);
+    intra_body<kGate>(p, smem_raw, blockIdx.x, gridDim.x);
 }
 
 __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainParams p) {
@@ -173,12 +174,13 @@ struct FusedParams {
     int C;
 };
 
+template <int kGate>
 __global__ void __launch_bounds__(kFusedThreads, 1) fwd_fused_kernel(const __grid_constant__ FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     if ((int)blockIdx.x < p.C) {
         if (threadIdx.x < kChainThreads) chain_body(p.cp, smem_raw, blockIdx.x, p.C);
     } else if (threadIdx.x < kIntraThreads) {
-        intra_body(p.ip, smem_raw, blockIdx.x - p.C, gridDim.x - p.C);
+        intra_body<kGate>(p.ip, smem_raw, blockIdx.x - p.C, gridDim.x - p.C);
     }
 }
 
@@ -251,6 +253,7 @@ size_t fwd_tc_workspace_size(int64_t T_total, int N, int H) {
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
     using namespace fwdtc;
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    const bool mixed = a.gate_kind == 1;  // the softplus gate on the mixed path
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     const WsLayout L = ws_layout(a.T_total, a.N, a.H);
     const int maxchunks = (int)(a.T_total / kC + a.N);
@@ -338,23 +341,28 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         fp.ip = ip;
         fp.cp = cp;
         fp.C = C;
-        e = cudaFuncSetAttribute(fwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kFusedSmem);
+        const void* fn = mixed ? reinterpret_cast<const void*>(fwd_fused_kernel<kGateSoftplus>)
+                               : reinterpret_cast<const void*>(fwd_fused_kernel<kGateBounded>);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmem);
         if (e != cudaSuccess) return e;
         void* args[] = {&fp};
-        ProfScope prof("fwd_fused_kernel", a.stream);
-        e = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fwd_fused_kernel), dim3(sms),
-                                        dim3(kFusedThreads), args, kFusedSmem, a.stream);
+        ProfScope prof(mixed ? "fwd_fused_mixed_kernel" : "fwd_fused_kernel", a.stream);
+        e = cudaLaunchCooperativeKernel(fn, dim3(sms), dim3(kFusedThreads), args, kFusedSmem,
+                                        a.stream);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
 
     if (a.T_total > 0) {
-        e = cudaFuncSetAttribute(intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kIntraSmem);
+        const void* fn = mixed ? reinterpret_cast<const void*>(intra_kernel<kGateSoftplus>)
+                               : reinterpret_cast<const void*>(intra_kernel<kGateBounded>);
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kIntraSmem);
         if (e != cudaSuccess) return e;
-        ProfScope prof("intra_kernel", a.stream);
-        intra_kernel<<<sms, kIntraThreads, kIntraSmem, a.stream>>>(ip);
+        ProfScope prof(mixed ? "intra_mixed_kernel" : "intra_kernel", a.stream);
+        if (mixed)
+            intra_kernel<kGateSoftplus><<<sms, kIntraThreads, kIntraSmem, a.stream>>>(ip);
+        else
+            intra_kernel<kGateBounded><<<sms, kIntraThreads, kIntraSmem, a.stream>>>(ip);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -21,7 +21,7 @@ struct FwdArgs {
     int64_t T_total;
     int H, dk, dv;
     int io_bf16;  // 1: bf16 I/O, 0: fp32 I/O
-    int gate_kind;  // 0: g_min Sigmoid(e^A z); 1: -e^A Softplus(z) (explicit path only)
+    int gate_kind;  // 0: g_min Sigmoid(e^A z); 1: -e^A Softplus(z)
     void* o;
     void* workspace;
     size_t ws_bytes;

@@ -68,7 +68,7 @@ def _load():
     lib.kda_quantile_balance.argtypes = [vp, vp, i64, i32, i32, vp, vp, vp, vp, sz, vp]
     lib.kda_fwd_chunked_softplus.restype = ctypes.c_int
     lib.kda_fwd_chunked_softplus.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32,
-                                             i32, i32, i32, vp, vp]
+                                             i32, i32, i32, vp, vp, sz, vp]
     lib.kda_bwd_workspace_size.restype = sz
     lib.kda_bwd_workspace_size.argtypes = [i64, i32, i32, i32, i32]
     lib.kda_bwd.restype = ctypes.c_int
@@ -278,10 +278,11 @@ def fwd_chunked_host(q, k, v, beta, z, A_log, g_min: float, S0=None, cu_seqlens=
 
 
 def fwd_chunked_softplus(q, k, v, beta, z, A_log, S0=None, cu_seqlens=None, N=None, o=None,
-                         S_out=None, want_state=True, stream=None):
-    """The chunked forward with the unbounded gate -e^A softplus(z) (explicit path).
+                         S_out=None, want_state=True, workspace=None, stream=None):
+    """The chunked forward with the unbounded gate -e^A softplus(z): the mixed path (bf16,
+    d = 128) or the explicit per-pair path.
 
-    Same arguments as fwd_chunked without g_min and workspace.  Returns (o, S_out).
+    Same arguments as fwd_chunked without g_min.  Returns (o, S_out).
     """
     for t, nm in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (z, "z")):
         _need(t, nm, q.dtype)
@@ -299,10 +300,15 @@ def fwd_chunked_softplus(q, k, v, beta, z, A_log, S0=None, cu_seqlens=None, N=No
         S_out = torch.empty((N, H, dk, dv), dtype=torch.float32, device=q.device)
     if S0 is not None:
         _need(S0, "S0", torch.float32)
+    need = workspace_size(T, N, H, dk, dv, q.dtype)
+    if need > 0 and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib.kda_fwd_chunked_softplus(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(z),
                                          _ptr(A_log), _ptr(S0), _ptr(S_out), _ptr(cu_seqlens),
                                          int(N), int(T), int(H), int(dk), int(dv), _dt(q),
-                                         _ptr(o), _stream(stream)), "kda_fwd_chunked_softplus")
+                                         _ptr(o), _ptr(workspace), ws_bytes, _stream(stream)),
+           "kda_fwd_chunked_softplus")
     return o, S_out
 
 

@@ -168,16 +168,27 @@ def test_softplus_forward_validation(lib):
     i64 = ctypes.c_int64
     lib.kda_fwd_chunked_softplus.restype = ctypes.c_int
     lib.kda_last_error.restype = ctypes.c_char_p
-    # q, k, v, beta, z, A_log, S0, S_out, cu, N, T, H, dk, dv, io_dt, o, stream
+    sz = ctypes.c_size_t
+    # q, k, v, beta, z, A_log, S0, S_out, cu, N, T, H, dk, dv, io_dt, o, workspace, ws, stream
     rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 1, i64(64), 2, 96,
-                                      128, 1, a, None)
+                                      128, 1, a, None, sz(0), None)
     assert rc == 2
     rc = lib.kda_fwd_chunked_softplus(a, a, a, a, None, a, None, None, None, 1, i64(64), 2, 128,
-                                      128, 1, a, None)
+                                      128, 1, a, None, sz(0), None)
     assert rc == 1 and b"z is NULL" in lib.kda_last_error()
     rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 3, i64(64), 2, 128,
-                                      128, 1, a, None)
+                                      128, 1, a, None, sz(0), None)
     assert rc == 1 and b"multiple of N" in lib.kda_last_error()
+    # bf16, d = 128 (the mixed path) needs the forward's workspace
+    lib.kda_fwd_workspace_size.restype = ctypes.c_size_t
+    need = lib.kda_fwd_workspace_size(i64(64), 1, 2, 128, 128, 1)
+    assert need > 0
+    rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 1, i64(64), 2, 128,
+                                      128, 1, a, None, sz(0), None)
+    assert rc == 1 and b"workspace is NULL" in lib.kda_last_error()
+    rc = lib.kda_fwd_chunked_softplus(a, a, a, a, a, a, None, None, None, 1, i64(64), 2, 128,
+                                      128, 1, a, a, sz(need - 1), None)
+    assert rc == 1 and b"smaller than" in lib.kda_last_error()
 
 
 def test_bwd_validation(lib):

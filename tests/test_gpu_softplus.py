@@ -1,7 +1,8 @@
 """GPU parity of the comparison variant: the chunked forward with the gate the bound replaces,
-g = -e^{A_h} Softplus(z) ("Kimi k3 技术报告详解（1）", section "Chunkwise parallel form"), on the
-explicit per-pair path, against the fp64 token recurrence.  Same tolerances as the bounded
-forward (kda_testutil)."""
+g = -e^{A_h} Softplus(z) ("Kimi k3 技术报告详解（1）", section "Chunkwise parallel form"),
+against the fp64 token recurrence.  bf16 with d = 128 runs the mixed path (off-diagonal
+sub-tiles on the tensor cores, diagonal sub-tiles per pair), everything else the explicit
+per-pair path.  Same tolerances as the bounded forward (kda_testutil)."""
 import numpy as np
 import pytest
 
@@ -18,13 +19,16 @@ def kda():
     return _k
 
 
-def _gpu(kda, inp):
+def _gpu(kda, inp, use_cu=True):
     import torch
     dev = {k: getattr(inp, k).as_torch("cuda") for k in ("q", "k", "v", "beta", "z")}
+    if use_cu:
+        kw = dict(cu_seqlens=torch.from_numpy(inp.cu_seqlens.astype(np.int32)).cuda())
+    else:  # equal lengths without cu_seqlens
+        kw = dict(N=len(inp.cu_seqlens) - 1)
     o, S = kda.fwd_chunked_softplus(
         dev["q"], dev["k"], dev["v"], dev["beta"], dev["z"], torch.from_numpy(inp.A_log).cuda(),
-        S0=None if inp.S0 is None else torch.from_numpy(inp.S0).cuda(),
-        cu_seqlens=torch.from_numpy(inp.cu_seqlens.astype(np.int32)).cuda())
+        S0=None if inp.S0 is None else torch.from_numpy(inp.S0).cuda(), **kw)
     kda.device_status()
     return o.float().cpu().numpy(), S.cpu().numpy()
 
@@ -75,3 +79,46 @@ def test_full_size_sampled(kda):
     S = S.cpu().numpy()
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
     check_forward(sp, o, S, oracle_forward(sp, heads=[0, 17], gate="softplus"))
+
+
+def test_mixed_path_kernels_and_fused_form(kda, monkeypatch):
+    """bf16, d = 128 takes the mixed path; equal lengths without cu_seqlens take its fused
+    form (bitwise equal to the two-launch form), and both meet the parity rule."""
+    inp = inputs.forward_inputs(seed=64, B=2, T=1280, H=4, dk=128, dv=128, dtype="bf16",
+                                with_state=True)
+    kda.profile_begin()
+    o_f, S_f = _gpu(kda, inp, use_cu=False)
+    names = kda.profile_end()
+    assert "fwd_fused_mixed_kernel" in names and "fwd_generic_kernel" not in names
+    monkeypatch.setenv("KDA_FWD_FUSED", "0")
+    kda.profile_begin()
+    o_2, S_2 = _gpu(kda, inp, use_cu=False)
+    names = kda.profile_end()
+    assert "intra_mixed_kernel" in names and "chain_kernel" in names
+    assert np.array_equal(o_f, o_2) and np.array_equal(S_f, S_2)
+    check_forward(inp, o_f, S_f, oracle_forward(inp, gate="softplus"))
+
+
+@pytest.mark.parametrize("dz", [-2.0, 1.5, 6.0])
+def test_mixed_path_decay_range(kda, dz):
+    """From weak (z - 2) to very strong (z + 6: g ~ -6 e^A per token, a 16-token sub-tile's
+    decay past the fp32 range) decay, with ragged tails: every factor of the mixed path is
+    <= 1, so the result stays finite and meets the parity rule."""
+    inp = _shift_z(inputs.forward_inputs(seed=65, lengths=[64 * 5 + 17, 64 * 3 - 5, 7], H=3,
+                                         dk=128, dv=128, dtype="bf16", with_state=True), dz)
+    o, S = _gpu(kda, inp)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(S))
+    check_forward(inp, o, S, oracle_forward(inp, gate="softplus"))
+
+
+def test_mixed_path_matches_explicit_path(kda, monkeypatch):
+    """The mixed path and the explicit per-pair path on the same bf16 inputs both meet the
+    parity rule against the oracle."""
+    inp = inputs.forward_inputs(seed=66, lengths=[200, 333], H=2, dk=128, dv=128,
+                                dtype="bf16", with_state=True)
+    ref = oracle_forward(inp, gate="softplus")
+    o_m, S_m = _gpu(kda, inp)
+    monkeypatch.setenv("KDA_FWD_PATH", "generic")
+    o_e, S_e = _gpu(kda, inp)
+    check_forward(inp, o_m, S_m, ref)
+    check_forward(inp, o_e, S_e, ref)
