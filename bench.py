@@ -34,6 +34,10 @@ METRIC = ("KDA chunked-fwd tokens/s & TFLOP/s (T=64K,H=32,d=128) as % bf16 peak;
 BYTES_PER_TOKEN_HEAD = 4 * 2 * D + 2 + 2 * D        # q,k,v,z in; beta; o out = 1282 B
 STATE_BYTES = 4 * D * D                              # one fp32 state (S_out write)
 FLOP_CAUSAL = 6 * D * D + (C - 1) * D + 4 * (C + 1) * D + C * C // 3   # 141,013
+# ... of which the intra-chunk stage (the two causal Grams, the UT solve, W and U) and the
+# state chain (W S, (Gamma*Q) S, K~^T Vt and the causal A Vt)
+FLOP_INTRA = 4 * (C + 1) * D + C * C // 3
+FLOP_CHAIN = FLOP_CAUSAL - FLOP_INTRA
 FLOP_DENSE = 6 * D * D + 2 * C * (3 * D + 2 * D) + C * C // 3           # 181,589
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "source": "fallback"}
@@ -256,8 +260,16 @@ def run_ours(args, rank, world, local_rank, dist):
     kernels = {name: {"launches": n, "avg_ms": tot / max(n, 1), "share": 0.0}
                for name, (n, tot) in prof.items()}
     tot_all = sum(v["avg_ms"] * v["launches"] for v in kernels.values()) or 1.0
-    for v in kernels.values():
+    # causal-count FLOPs each kernel performs per launch, and its rate against the measured
+    # dense bf16 peak (burst: the kernels are timed in a short loop)
+    flop_k = {"intra_kernel": T * H * FLOP_INTRA, "chain_kernel": T * H * FLOP_CHAIN,
+              "fwd_fused_kernel": T * H * FLOP_CAUSAL}
+    for name, v in kernels.items():
         v["share"] = v["avg_ms"] * v["launches"] / tot_all
+        if name in flop_k:
+            v["flop_causal"] = flop_k[name]
+            v["tflops"] = flop_k[name] / (v["avg_ms"] / 1e3) / 1e12
+            v["frac_bf16_peak"] = v["tflops"] / peaks["bf16_tflops"]
     kname = max(kernels, key=lambda k: kernels[k]["avg_ms"] * kernels[k]["launches"])
     # algorithmic bytes each kernel must move (per launch) on this workload
     alg = {"intra_kernel": T * H * (4 * 2 * D + 2),              # q, k, v, z, beta in
@@ -267,15 +279,14 @@ def run_ours(args, rank, world, local_rank, dist):
            "plan_kernel": 8}
     bytes_k = alg.get(kname, T * H * BYTES_PER_TOKEN_HEAD)
     achieved = bytes_k / (kernels[kname]["avg_ms"] / 1e3) / 1e9
-    src = {"intra_kernel": "fwd_tc.cu", "chain_kernel": "fwd_tc.cu", "plan_kernel": "fwd_tc.cu",
-           "fwd_fused_kernel": "fwd_tc.cu",
-           "fwd_generic_kernel": "fwd_generic.cu"}.get(kname, "fwd_tc.cu")
+    tc_src = ("fwd_tc.cu", "fwd_intra.cuh", "fwd_chain.cuh", "fwd_tc_layout.cuh", "tc_util.cuh")
+    src = {"fwd_generic_kernel": ("fwd_generic.cu",)}.get(kname, tc_src)
     path_ms = sum(v["avg_ms"] for v in kernels.values())
     path_bytes = T * H * BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"],
                 "traffic": traffic_from_profile(kname, source_hash(
-                    "serving_kda_chunkwise_gb300/csrc/" + src)),
+                    *("serving_kda_chunkwise_gb300/csrc/" + f for f in src))),
                 "kernel": kname, "peak_source": peaks["source"] + " (burst copy)",
                 "algorithmic_bytes_per_launch": bytes_k,
                 "path": {"kernels": sorted(kernels), "algorithmic_bytes": path_bytes,
@@ -284,6 +295,16 @@ def run_ours(args, rank, world, local_rank, dist):
                          "frac": path_bytes / (path_ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
                 "per_kernel": kernels}
     launches_per_step = sum(v["launches"] for v in kernels.values()) / args.steps
+
+    if args.forward_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": tok_s, "unit": "tokens/s",
+                              "ms_per_step": ms_per_step, "steps": args.steps,
+                              "config": {"workload": WORKLOAD, "T": T, "H": H},
+                              "tflops_causal": tflops_causal, "roofline": roofline,
+                              "clocks": clk, "note": "forward only (profiler case)"}),
+                  flush=True)
+        return
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     host = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "beta", "z")}
@@ -328,6 +349,12 @@ def run_ours(args, rank, world, local_rank, dist):
     # quantile balancing of a routing batch (65536 tokens x 256 experts, k = 8)
     qbm = bench_quantile_balance(dev, stream, peaks)
 
+    # the other forward workloads at d = 128: two sequences of 4096 tokens x 16 heads, and
+    # 64 packed sequences of U[128, 16384] tokens x 32 heads
+    del ws
+    others = {name: bench_forward_workload(dev, stream, peaks, name)
+              for name in ("fwd_bf16_B2_T4096_H16_d128", "fwd_bf16_varlen64_H32_d128")}
+
     # decode step: 256 sequences x 32 heads, state updated in place
     dec = None
     if not args.no_decode:
@@ -356,8 +383,68 @@ def run_ours(args, rank, world, local_rank, dist):
                 "pct_bf16_peak_causal": 100 * tflops_causal / (world * peaks["bf16_tflops"]),
                 "roofline": roofline, "e2e": e2e,
                 "gpu_launches": int(round(launches_per_step * args.steps)),
-                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "gate_comparison": gcmp, "backward": bw, "decode": dec, "cpu_baseline": cpu}
+                "clocks": clk, "output_gate": og, "quantile_balance": qbm, "gate_comparison": gcmp, "backward": bw, "decode": dec, "cpu_baseline": cpu,
+                "other_workloads": others}
         print(json.dumps(line), flush=True)
+
+
+def bench_forward_workload(dev, stream, peaks, name, reps=5):
+    """The forward on another named workload (its own inputs, initial states and cu_seqlens
+    where it has them).  L2 is flushed (a 256 MB write, outside the timed region) before
+    every timed call, so a workload smaller than L2 is not served from it."""
+    import torch
+
+    from serving_kda_chunkwise_gb300 import inputs, kda
+
+    sp = inputs.workload_spec(name)
+    d = sp.to_device(dev)
+    T_, H_, N_ = sp.T, sp.H, sp.N
+    lens = [int(x) for x in (sp.cu_seqlens[1:] - sp.cu_seqlens[:-1])]
+    cu = None if len(set(lens)) == 1 else d["cu"]  # equal lengths need no cu_seqlens
+    S_out = torch.empty((N_, H_, D, D), dtype=torch.float32, device=dev)
+    o = torch.empty((T_, H_, D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(kda.workspace_size(T_, N_, H_, D, D, torch.bfloat16), 16),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        kda.fwd_chunked(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], sp.g_min,
+                        S0=d["S0"], cu_seqlens=cu, N=N_, o=o, S_out=S_out, workspace=ws,
+                        stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    kda.profile_begin()
+    for _ in range(reps):
+        flush.fill_(1)
+        ev0.record(stream)
+        call()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        total += ev0.elapsed_time(ev1)
+    prof = kda.profile_end()
+    kda.device_status(stream)
+    ms = total / reps
+    th = T_ * H_
+    alg_bytes = th * BYTES_PER_TOKEN_HEAD + N_ * H_ * STATE_BYTES * (2 if sp.with_state else 1)
+    flop = th * FLOP_CAUSAL
+    out = {"workload": name, "T_total": T_, "N": N_, "H": H_, "ms": ms,
+           "tokens_per_s": T_ / (ms / 1e3), "tflops_causal": flop / (ms / 1e3) / 1e12,
+           "frac_bf16_peak": flop / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+           "roofline": {"bound": "hbm", "algorithmic_bytes": alg_bytes,
+                        "achieved": alg_bytes / (ms / 1e3) / 1e9, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s",
+                        "frac": alg_bytes / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]},
+           "kernels": {k: {"launches": n, "avg_ms": t / max(n, 1)} for k, (n, t) in prof.items()},
+           "l2": "flushed before every call", "steps": reps,
+           "longest_sequence_tokens": max(lens)}
+    del d, ws, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def bench_output_gate(dev, stream, peaks, o, gate, reps=20):
@@ -591,6 +678,10 @@ def main():
     ap.add_argument("--heads", type=int, default=0,
                     help="run the forward workload with this many heads instead of 32 (a "
                          "smaller case for profiler captures; not a bench line)")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time the forward step only: no end-to-end, output-gate, gate "
+                         "comparison, backward, quantile-balancing, other-workload, decode or "
+                         "CPU blocks (for profiler captures; not a bench line)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the forward workload with this many tokens instead of 65536 "
                          "(a smaller case for profiler captures; not a bench line)")
