@@ -623,10 +623,12 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
     __shared__ ItemInfo s_item[2];
     __shared__ float s_alog[2];
     int lead_next = n_items;
+    int4 raw_lead;  // issuing thread: lead_next's chunk-table entry, fetched when it is taken
     if (tid == kIss) {
         const int first_item = take_item(p, -1, cta, ncta);
         s_item[0].item = first_item;
         if (first_item < n_items) lead_next = take_item(p, first_item, cta, ncta);
+        if (lead_next < n_items) raw_lead = fetch_item(p, lead_next);
     }
     if (tid == kIss && s_item[0].item < n_items) {
         const ItemInfo first = decode_item(p, s_item[0].item, fetch_item(p, s_item[0].item));
@@ -653,18 +655,39 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         float* sBeta = reinterpret_cast<float*>(sm + kBeta) + 64 * b;
         const int itL = s_item[b].L;  // rows of this item (< 64 for a sequence's last chunk)
         const float alog = s_alog[b];
-        // the next item, known to the issuing thread (which took it one item ago) and
-        // needed by its warp only (that warp loads the next item's beta); the item after it
-        // is taken now
+        // the next item, known to the issuing thread (which took it and fetched its table
+        // entry one item ago) and needed by its warp only: the issuing thread publishes it
+        // now (read after the next CTA barrier) and the warp loads its beta, a whole gate
+        // phase ahead of the store into its slot.  The item after it is taken and its
+        // entry fetched now.
         const int next = warp == (kIss >> 5) ? __shfl_sync(0xffffffffu, lead_next, kIss & 31) : n_items;
         const bool has_next = next < n_items;
         int next2 = n_items;
-        if (tid == kIss && has_next) next2 = take_item(p, next, cta, ncta);
         unsigned short beta_nx[2] = {0, 0};  // issuing thread's warp: the next item's beta (bf16)
         float alog_nx = 0.f;                 // issuing thread: the next item's A_log
-        // issuing thread: the next item's table entry, decoded once the scan is done
-        int4 raw_next;
-        if (tid == kIss && has_next) raw_next = fetch_item(p, next);
+        if (warp == (kIss >> 5)) {
+            if (tid == kIss) {
+                if (has_next) {
+                    const ItemInfo nx = decode_item(p, next, raw_lead);
+                    s_item[b ^ 1] = nx;
+                    alog_nx = ld_ahead(p.A_log + nx.h);
+                    next2 = take_item(p, next, cta, ncta);
+                    if (next2 < n_items) raw_lead = fetch_item(p, next2);
+                } else {
+                    s_item[b ^ 1].item = n_items;  // no further item
+                }
+            }
+            __syncwarp();
+            if (has_next) {
+                const ItemInfo& nxs = s_item[b ^ 1];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int r = lane + 32 * h2;
+                    if (r < nxs.L)
+                        beta_nx[h2] = ld_ahead(p.beta + (size_t)(nxs.t0 + r) * p.H + nxs.h);
+                }
+            }
+        }
         // this item's package (re-read where used: nothing held in registers across phases)
         auto item_pkg = [&]() { return p.pkg + s_item[b].pkg * kPkgBytes; };
 
@@ -727,28 +750,11 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
             xtot[tid] = a;
         }
         intra_sync();
-        // z is consumed: the issuing thread publishes the next item and fetches its z
-        // (issued here, where a long phase follows, so that a slow issue never holds up a
-        // barrier)
-        if (tid == kIss && !has_next) s_item[b ^ 1].item = n_items;  // no further item
-        if (warp == (kIss >> 5) && has_next) {
-            if (tid == kIss) {
-                const ItemInfo nx = decode_item(p, next, raw_next);
-                s_item[b ^ 1] = nx;  // read after the next CTA barrier
-                alog_nx = ld_ahead(p.A_log + nx.h);
-                load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, nx, z_bar);
-                pend_z = (iter + 1) & 1;
-            }
-            __syncwarp();
-            // the next item's beta (rows lane, lane + 32), stored into its slot during the
-            // operand pass, where this warp has no other work
-            const ItemInfo& nxs = s_item[b ^ 1];
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int r = lane + 32 * h2;
-                if (r < nxs.L)
-                    beta_nx[h2] = ld_ahead(p.beta + (size_t)(nxs.t0 + r) * p.H + nxs.h);
-            }
+        // z is consumed: the issuing thread fetches the next item's z (issued here, where a
+        // long phase follows, so that a slow issue never holds up a barrier)
+        if (tid == kIss && has_next) {
+            load_tiles(&p.tz, sm + kZBuf, nullptr, nullptr, s_item[b ^ 1], z_bar);
+            pend_z = (iter + 1) & 1;
         }
         {
             const float4 pa = *reinterpret_cast<const float4*>(tot + warp * 128 + ch0);
