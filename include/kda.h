@@ -89,7 +89,7 @@ kda_status_t kda_gate(const void *z, kda_dtype_t z_dt, const float *A_log, float
 
 /*
  * Bytes of device workspace kda_fwd_chunked needs for this problem shape (0 when the
- * selected kernels need none).  T_total is the packed token count, N the number of
+ * selected kernels need none: fp32 I/O).  T_total is the packed token count, N the number of
  * sequences.  Safe to call without a GPU.
  */
 size_t kda_fwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv,
@@ -124,11 +124,10 @@ kda_status_t kda_fwd_chunked(const void *q, const void *k, const void *v, const 
  * ([blog] "Chunkwise parallel form"): g = -e^{A_log[h]} Softplus(z), unbounded below, so a
  * sub-tile's decay can leave the exponent range and no decay factor of a diagonal sub-tile
  * splits into a bounded row factor and column factor.  A comparison variant: it measures
- * what the bound buys.  bf16 with dk = dv = 128 runs the mixed path the page describes: the
- * off-diagonal 16-token sub-tile pairs on the tensor cores with sub-tile-start references
- * (every factor <= 1), the diagonal 16 x 16 blocks per pair on CUDA cores (e^{G_r - G_i},
- * exponent <= 0, in fp32).  Other shapes and fp32 run the explicit per-pair path (every
- * pair on CUDA cores).  Arguments as kda_fwd_chunked without g_min; the workspace is sized
+ * what the bound buys.  bf16 runs the mixed path the page describes: the off-diagonal
+ * 16-token sub-tile pairs on the tensor cores with sub-tile-start references (every factor
+ * <= 1), the diagonal 16 x 16 blocks per pair on CUDA cores (e^{G_r - G_i}, exponent <= 0,
+ * in fp32).  fp32 runs the explicit per-pair path (every pair on CUDA cores).  Arguments as kda_fwd_chunked without g_min; the workspace is sized
  * by kda_fwd_workspace_size (0 bytes, and workspace may be NULL, on the explicit path).
  * z must be finite or -inf.
  */

@@ -125,11 +125,11 @@ kda_status_t kda_gate(const void* z, kda_dtype_t z_dt, const float* A_log, float
     return KDA_OK;
 }
 
-// Which forward kernels a problem takes: the tensor-core path for bf16 I/O with
-// dk = dv = 128, the fp32 CUDA-core path otherwise.  KDA_FWD_PATH=generic in the
-// environment forces the CUDA-core path (the tests use it to cross-check the two).
+// Which forward kernels a problem takes: bf16 I/O the tensor-core path at every head size
+// (a 64 runs zero-padded to 128), fp32 I/O the fp32 CUDA-core path.  KDA_FWD_PATH=generic
+// in the environment forces the CUDA-core path (the tests use it to cross-check the two).
 static bool use_tc_path(int dk, int dv, kda_dtype_t io_dt) {
-    if (io_dt != KDA_BF16 || dk != 128 || dv != 128) return false;
+    if (io_dt != KDA_BF16 || (dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return false;
     const char* env = getenv("KDA_FWD_PATH");
     return !(env && strcmp(env, "generic") == 0);
 }
@@ -261,8 +261,8 @@ kda_status_t kda_fwd_chunked_softplus(const void* q, const void* k, const void* 
     a.dev_err = device_error_ptr();
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     if (a.dev_err == nullptr) return fail(KDA_ERR_CUDA, "no CUDA device is usable");
-    // bf16 with d = 128: the mixed path (tensor cores off the diagonal sub-tiles); otherwise
-    // the explicit per-pair path
+    // bf16: the mixed path (tensor cores off the diagonal sub-tiles); fp32: the explicit
+    // per-pair path
     cudaError_t e =
         use_tc_path(dk, dv, io_dt) ? kda::launch_fwd_tc(a) : kda::launch_fwd_generic(a);
     if (e != cudaSuccess) return cuda_fail(e, "kda_fwd_chunked_softplus launch");

@@ -89,6 +89,9 @@ struct ChainParams {
     unsigned* err;
     int64_t T_total;
     int N, H, maxchunks;
+    // head sizes of q, k (dk) and v, o, S (dv), 64 or 128: a 64 is zero-padded to 128 inside
+    // (the tensor maps read zeros past it), so only the state and output addresses use them
+    int dk, dv;
     // fused kernel only (fused = 0 otherwise): CTA c serves chain c and reads chunk t from
     // ring slot c * ring_slots + t % ring_slots once ready[slot] >= t + 1; it raises
     // consumed[c] to t + 1 once every part of chunk t is in shared memory
@@ -325,8 +328,12 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             tmem_ld16(col + 16, o1);
             tmem_ld_wait();
             const int64_t r0 = t0 + 32 * wg;
-            __nv_bfloat16* orow = p.o + ((size_t)r0 * p.H + c.h) * kD + j;
-            const size_t rstride = (size_t)p.H * kD;
+            if (j >= p.dv) {  // a padding column: nothing to store
+                tc_fence_before();
+                return true;
+            }
+            __nv_bfloat16* orow = p.o + ((size_t)r0 * p.H + c.h) * p.dv + j;
+            const size_t rstride = (size_t)p.H * p.dv;
             if (r0 + 32 <= c.t_end) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e) orow[e * rstride] = __float2bfloat16_rn(o0[e]);
@@ -347,11 +354,13 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             const int ci = chain_of(k, cta, G);
             if (ci >= n_chains) break;
             const Chain c = decode_chain(p, ci);
-            // S[e] = S[i = 64 wg + e][j] (fp32, registers)
+            // S[e] = S[i = 64 wg + e][j] (fp32, registers); padding rows (i >= dk) and
+            // columns (j >= dv) hold zeros and are neither read nor written
             float S[64];
-            const size_t sbase_el = ((size_t)(c.n * p.H + c.h) * kD + 64 * wg) * kD + j;
+            const bool sv = j < p.dv && 64 * wg < p.dk;
+            const size_t sbase_el = ((size_t)(c.n * p.H + c.h) * p.dk + 64 * wg) * p.dv + j;
 #pragma unroll
-            for (int e = 0; e < 64; ++e) S[e] = p.S0 ? p.S0[sbase_el + (size_t)e * kD] : 0.f;
+            for (int e = 0; e < 64; ++e) S[e] = (p.S0 && sv) ? p.S0[sbase_el + (size_t)e * p.dv] : 0.f;
             if (c.nch > 0) {
                 uint32_t pk[32];
 #pragma unroll
@@ -455,9 +464,9 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (rec) CH_MARK(14);
             }
             if (!ok) break;
-            if (p.S_out) {
+            if (p.S_out && sv) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e) p.S_out[sbase_el + (size_t)e * kD] = S[e];
+                for (int e = 0; e < 64; ++e) p.S_out[sbase_el + (size_t)e * p.dv] = S[e];
             }
         }
     }

@@ -229,13 +229,15 @@ int debug_phase_cycles(unsigned long long* out, int n) {
 }
 #endif
 
-// [T_total, H, 128] bf16 tensor, boxes of `box_cols` columns x 1 head x 64 rows; 64-column
-// boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle, 128-column boxes none.
-bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int box_cols) {
+// [T_total, H, d] bf16 tensor (d = 64 or 128), boxes of `box_cols` columns x 1 head x 64
+// rows; 64-column boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle,
+// 128-column boxes none.  With d = 64 a box at column 64 lies wholly outside the tensor and
+// reads zeros: the kernels then see the head zero-padded to 128 channels.
+bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int d, int box_cols) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T_total};
-    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T_total};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
     const cuuint32_t box[3] = {(cuuint32_t)box_cols, 1, kC};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapSwizzle sw = box_cols == 64   ? CU_TENSOR_MAP_SWIZZLE_128B
@@ -306,8 +308,10 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     IntraParams ip{};
     ChainParams cp{};
     if (a.T_total > 0) {
-        if (!make_map(&ip.tq, a.q, a.T_total, a.H, 64) || !make_map(&ip.tk, a.k, a.T_total, a.H, 64) ||
-            !make_map(&ip.tv, a.v, a.T_total, a.H, 64) || !make_map(&ip.tz, a.z, a.T_total, a.H, 64))
+        if (!make_map(&ip.tq, a.q, a.T_total, a.H, a.dk, 64) ||
+            !make_map(&ip.tk, a.k, a.T_total, a.H, a.dk, 64) ||
+            !make_map(&ip.tv, a.v, a.T_total, a.H, a.dv, 64) ||
+            !make_map(&ip.tz, a.z, a.T_total, a.H, a.dk, 64))
             return cudaErrorInvalidValue;
     }
     ip.beta = static_cast<const __nv_bfloat16*>(a.beta);
@@ -333,6 +337,8 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     cp.T_total = a.T_total;
     cp.N = a.N;
     cp.H = a.H;
+    cp.dk = a.dk;
+    cp.dv = a.dv;
     cp.maxchunks = maxchunks;
 
     if (fused) {

@@ -71,10 +71,10 @@ inline WsLayout ws_layout(int64_t T_total, int N, int H) {
     return l;
 }
 
-// [T_total, H, 128] bf16 tensor map with boxes of `box_cols` columns x 1 head x 64 rows:
-// 64-column boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle, 128-column
-// boxes none (fwd_tc.cu).
-bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int box_cols);
+// [T_total, H, d] bf16 tensor map (d = 64 or 128) with boxes of `box_cols` columns x 1 head
+// x 64 rows: 64-column boxes use the 128-byte swizzle, 32-column boxes the 64-byte swizzle,
+// 128-column boxes none (fwd_tc.cu).  Columns past d read as zero.
+bool make_map(CUtensorMap* m, const void* base, int64_t T_total, int H, int d, int box_cols);
 
 }  // namespace fwdtc
 }  // namespace kda

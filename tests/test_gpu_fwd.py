@@ -228,3 +228,53 @@ def test_fwd_fused_matches_two_launch(kda, monkeypatch):
     assert "chain_kernel" in names and "fwd_fused_kernel" not in names
     assert np.array_equal(o_f, o_2) and np.array_equal(S_f, S_2)
     check_forward(inp, o_f, S_f, oracle_forward(inp))
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64)])
+def test_fwd_bf16_small_heads_on_tensor_cores(kda, monkeypatch, dk, dv):
+    """bf16 heads of 64 channels take the tensor-core path, zero-padded to 128 inside (the
+    tensor maps read zeros past the head, and zero channels add nothing to q.k, the state or
+    o).  The fused form and the two-launch form agree bitwise and meet the parity rule,
+    initial and final state included."""
+    inp = inputs.forward_inputs(seed=92, B=2, T=1280, H=3, dk=dk, dv=dv, dtype="bf16",
+                                with_state=True)
+    kda.profile_begin()
+    o_f, S_f = gpu_forward(inp, use_cu=False)
+    names = kda.profile_end()
+    assert "fwd_fused_kernel" in names and "fwd_generic_kernel" not in names
+    monkeypatch.setenv("KDA_FWD_FUSED", "0")
+    kda.profile_begin()
+    o_2, S_2 = gpu_forward(inp, use_cu=False)
+    names = kda.profile_end()
+    assert "intra_kernel" in names and "chain_kernel" in names
+    assert np.array_equal(o_f, o_2) and np.array_equal(S_f, S_2)
+    check_forward(inp, o_f, S_f, oracle_forward(inp))
+
+
+def test_fwd_bf16_d64_output_canaries(kda):
+    """The zero-padded tensor-core path writes only o and S_out of a 64-channel head
+    (guard regions around both stay intact), fused and two-launch forms."""
+    import torch
+    for B, lens in ((2, None), (None, [77, 190])):
+        if B:
+            inp = inputs.forward_inputs(seed=43, B=B, T=1024, H=2, dk=64, dv=64, dtype="bf16",
+                                        with_state=True)
+        else:
+            inp = inputs.forward_inputs(seed=42, lengths=lens, H=2, dk=64, dv=64, dtype="bf16",
+                                        with_state=True)
+        from kda_testutil import device_inputs
+        d = device_inputs(inp)
+        N = len(inp.cu_seqlens) - 1
+        T, H, dv = int(inp.cu_seqlens[-1]), 2, 64
+        pad = 4096
+        o_buf = torch.full((pad + T * H * dv + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+        S_buf = torch.full((pad + N * H * 64 * dv + pad,), 9.0, dtype=torch.float32, device="cuda")
+        o = o_buf[pad:pad + T * H * dv].view(T, H, dv)
+        S = S_buf[pad:pad + N * H * 64 * dv].view(N, H, 64, dv)
+        kw = dict(N=N) if B else dict(cu_seqlens=d["cu"])
+        kda.fwd_chunked(d["q"], d["k"], d["v"], d["beta"], d["z"], d["A_log"], inp.g_min,
+                        S0=d["S0"], o=o, S_out=S, **kw)
+        torch.cuda.synchronize()
+        assert torch.all(o_buf[:pad] == 7.0) and torch.all(o_buf[-pad:] == 7.0)
+        assert torch.all(S_buf[:pad] == 9.0) and torch.all(S_buf[-pad:] == 9.0)
+        check_forward(inp, o.float().cpu().numpy(), S.cpu().numpy(), oracle_forward(inp))
