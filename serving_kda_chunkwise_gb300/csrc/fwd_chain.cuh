@@ -66,11 +66,11 @@ constexpr int kCopyT = 288;  // lane 0 of warp 9
 
 // shared memory (1024-aligned offsets)
 constexpr uint32_t kChPA = 0;          // part A, two stages of 32 KB
-constexpr uint32_t kChKC = 65536;      // K~ hi + lo (32 KB)
-constexpr uint32_t kChAT = 98304;      // A hi + lo (16 KB)
-constexpr uint32_t kChU = 114688;      // U, two stages of 32 KB
-constexpr uint32_t kChG = 180224;      // gamma^C, four stages of 512 B
-constexpr uint32_t kChBars = 182272;
+constexpr uint32_t kChKC = 65536;      // K~ hi + lo, two stages of 32 KB
+constexpr uint32_t kChAT = 131072;     // A hi + lo (16 KB)
+constexpr uint32_t kChU = 147456;      // U, two stages of 32 KB
+constexpr uint32_t kChG = 212992;      // gamma^C, four stages of 512 B
+constexpr uint32_t kChBars = 215040;
 constexpr uint32_t kChainSmem = kChBars + 256 + 1024;
 static_assert(kChainSmem <= 232448, "chain kernel exceeds the shared-memory limit");
 
@@ -132,15 +132,15 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     const uint32_t sbase = smem_u32(sm);
     uint64_t* fullPA = reinterpret_cast<uint64_t*>(sm + kChBars);  // [2] part A
     uint64_t* fullU = fullPA + 2;                                  // [2] U + gamma^C
-    uint64_t* fullKC = fullPA + 4;
-    uint64_t* fullAT = fullPA + 5;
-    uint64_t* mma1 = fullPA + 6;                                   // [2]
-    uint64_t* mma2 = fullPA + 8;
-    uint64_t* mma3 = fullPA + 9;                                   // [2]
-    uint64_t* vt_ready = fullPA + 11;                              // [2], 8 arrivals
-    uint64_t* s_ready = fullPA + 13;                               // 8 arrivals
-    uint64_t* drain = fullPA + 14;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullPA + 15);
+    uint64_t* fullKC = fullPA + 4;                                 // [2]
+    uint64_t* fullAT = fullPA + 6;
+    uint64_t* mma1 = fullPA + 7;                                   // [2]
+    uint64_t* mma2 = fullPA + 9;                                   // [2]
+    uint64_t* mma3 = fullPA + 11;                                  // [2]
+    uint64_t* vt_ready = fullPA + 13;                              // [2], 8 arrivals
+    uint64_t* s_ready = fullPA + 15;                               // 8 arrivals
+    uint64_t* drain = fullPA + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fullPA + 17);
     __shared__ int s_abort;
     __shared__ uint32_t s_landed_v;  // fused: chunks (counted over the CTA's chains) in smem
     volatile uint32_t* s_landed = &s_landed_v;
@@ -148,7 +148,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &s_abort;
     if (tid == 0) {
-        for (int i = 0; i < 15; ++i) mbar_init(&fullPA[i], 1);
+        for (int i = 0; i < 17; ++i) mbar_init(&fullPA[i], 1);
         mbar_init(&vt_ready[0], 8);
         mbar_init(&vt_ready[1], 8);
         mbar_init(s_ready, 8);
@@ -194,7 +194,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                                 id1, ks > 0);
                 mma_commit(&mma1[st]);
                 CH_MARK(2);
-                if (!mbar_wait_ab(fullKC, g & 1, p.err, abort)) { ok = false; break; }
+                if (!mbar_wait_ab(&fullKC[st], ph, p.err, abort)) { ok = false; break; }
                 CH_MARK(3);
                 if (!mbar_wait_ab(&vt_ready[st], ph, p.err, abort)) { ok = false; break; }
                 CH_MARK(4);
@@ -203,9 +203,10 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 for (int ks = 0; ks < 12; ++ks) {
                     const int seg = ks >> 2, kk = ks & 3;
                     mma_bf16_ts(tmem + kTDS, tmem + (seg == 1 ? kTVlo : kTV) + 8 * kk,
-                                dKC + (((seg == 2 ? 16384u : 0u) + kk * 2048) >> 4), id2, ks > 0);
+                                dKC + ((st * kPkgKTBytes + (seg == 2 ? 16384u : 0u) + kk * 2048) >> 4),
+                                id2, ks > 0);
                 }
-                mma_commit(mma2);
+                mma_commit(&mma2[st]);
                 CH_MARK(5);
                 if (!mbar_wait_ab(fullAT, g & 1, p.err, abort)) { ok = false; break; }
                 CH_MARK(6);
@@ -227,7 +228,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     //   lane 0: part A ([W; Gamma*Q]), two stages, free once MMA1 of chunk g - 2 completed;
     //   lane 1: U and gamma^C, two stages of U (free once E1 of chunk g - 2 is done) and four
     //           of gamma (E2 of chunk g - 4 precedes E1 of chunk g - 2 on the same warps);
-    //   lane 2: K~ hi + lo, one stage, free once MMA2 of chunk g - 1 completed;
+    //   lane 2: K~ hi + lo, two stages, free once MMA2 of chunk g - 2 completed;
     //   lane 3: A hi + lo, one stage, free once MMA3 of chunk g - 1 completed.
     int last_ph[2] = {-1, -1};  // the phase parity a drain must let land, per stage
     const int cpart = (warp == kCopyT / 32 && lane < 4) ? lane : -1;
@@ -262,10 +263,10 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                     bulk_g2s(sm + kChG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
                     last_ph[st] = (int)((g >> 1) & 1);
                 } else if (cpart == 2) {
-                    if (g >= 1 && !mbar_wait_ab(mma2, (g - 1) & 1, p.err, abort)) { ok = false; break; }
-                    mbar_expect_tx(fullKC, kPkgKTBytes);
-                    bulk_g2s(sm + kChKC, src + kPkgKT, kPkgKTBytes, fullKC);
-                    last_ph[0] = (int)(g & 1);
+                    if (g >= 2 && !mbar_wait_ab(&mma2[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
+                    mbar_expect_tx(&fullKC[st], kPkgKTBytes);
+                    bulk_g2s(sm + kChKC + st * kPkgKTBytes, src + kPkgKT, kPkgKTBytes, &fullKC[st]);
+                    last_ph[st] = (int)((g >> 1) & 1);
                 } else {
                     if (g >= 1 && !mbar_wait_ab(&mma3[(g - 1) & 1], ((g - 1) >> 1) & 1, p.err, abort)) { ok = false; break; }
                     mbar_expect_tx(fullAT, kPkgAQKBytes);
@@ -420,7 +421,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (t > 0 && !store_out(g - 1, t0 - kC, c)) { ok = false; break; }
                 if (rec) CH_MARK(13);
                 // ---- E2: S^T <- S^T Diag(gamma^C) + dS^T; bf16 copy for the next MMA1
-                okc = okc && mbar_wait_ab(mma2, g & 1, p.err, abort);
+                okc = okc && mbar_wait_ab(&mma2[st], ph, p.err, abort);
                 if (rec) CH_MARK(11);
                 if (okc) {
                     tc_fence_after();

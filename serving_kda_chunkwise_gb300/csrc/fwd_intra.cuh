@@ -818,13 +818,6 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
 #pragma unroll
             for (int e = 0; e < 8; ++e) reinterpret_cast<float*>(item_pkg() + kPkgG)[ch0 + e] = ex2f(gl[e]);
 
-        if (warp == (kIss >> 5)) {
-            float* dst = reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1);
-            dst[lane] = __bfloat162float(__ushort_as_bfloat16(beta_nx[0]));
-            dst[lane + 32] = __bfloat162float(__ushort_as_bfloat16(beta_nx[1]));
-            if (lane == 0) s_alog[b ^ 1] = alog_nx;
-        }
-
         // ---- decay-scaled operands.  Row r of sub-tile s uses e1 = e^{G_r - rho_s}.
         //      Bounded gate: the column operand of version s2 >= s is k_r e^{rho_s2 - G_r},
         //      own version hi + lo.  Mixed path: versions s2 > s only, k_r e^{rho_s2 - G_r}
@@ -972,6 +965,15 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
             for (int e = 0; e < 8; ++e) t[e] = kv[e] * eg[e];
             *reinterpret_cast<uint4*>(sm + kKbar + o64) = pk8(t);         // Gam*K
         }
+        }
+
+        // the next item's beta and A_log into their slots (loaded at the top of the loop;
+        // stored here, where a late load holds up no barrier)
+        if (warp == (kIss >> 5)) {
+            float* dst = reinterpret_cast<float*>(sm + kBeta) + 64 * (b ^ 1);
+            dst[lane] = __bfloat162float(__ushort_as_bfloat16(beta_nx[0]));
+            dst[lane + 32] = __bfloat162float(__ushort_as_bfloat16(beta_nx[1]));
+            if (lane == 0) s_alog[b ^ 1] = alog_nx;
         }
 
         // ---- mixed path, while the Gram MMAs run: the diagonal 16 x 16 blocks per pair,
