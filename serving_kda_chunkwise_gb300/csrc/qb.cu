@@ -12,9 +12,10 @@
 //
 // Kernels, all on the caller's stream:
 //   qb_alpha_kernel   one warp per token: the row's n values in registers (n <= 1024,
-//                     ceil(n/32) per lane), the (k+1)-th largest by k+1 rounds of warp
-//                     maximum and removal of one occurrence (or the (n-k)-th smallest, by
-//                     rounds of minimum, when that takes fewer rounds).
+//                     ceil(n/32) per lane, sorted within the lane), the (k+1)-th largest by
+//                     k+1 rounds of warp maximum over the lanes' first values and removal of
+//                     that value from the lowest lane holding it (or the (n-k)-th smallest,
+//                     by rounds of minimum, when that takes fewer rounds).
 //   qb_hist_kernel    radix select over the margins of every expert at once, 8 bits per pass
 //                     (4 passes, most significant digit first) on an order-preserving
 //                     uint32 key, inverted so that ascending keys are descending margins:
@@ -23,11 +24,11 @@
 //                     digits of the keys that still match the expert's prefix in shared
 //                     memory and adds its counts to a global [n][256] histogram.  The
 //                     scores (m n 4 bytes) are re-read every pass; at 64 MB they stay in L2.
-//   qb_select_kernel  one warp per expert: the digit holding rank q (prefix scan over the
-//                     256 counts), appended to the expert's prefix; the histogram is cleared
-//                     for the next pass.  After the last pass the key is the (q+1)-th
-//                     largest margin itself.
-//   qb_mean_kernel    one CTA: bhat and bhat - mean(bhat).
+//                     The last CTA of each column of experts to finish a pass selects
+//                     their digits (the digit holding rank q, by a prefix scan over the 256
+//                     counts, appended to the expert's prefix) and clears their counts; after
+//                     the last pass the key is the (q+1)-th largest margin itself, and the last
+//                     column to finish forms bhat - mean(bhat).
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -47,9 +48,23 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float(u);
 }
 
-// kP values per lane (n <= 32 kP).  The (k+1)-th largest is found by k+1 rounds of "take the
-// warp maximum, remove one occurrence", or, when that is shorter, as the (n-k)-th smallest by
-// rounds of minimum.
+// Sort kP values descending (odd-even transposition network, unrolled).
+template <int kP>
+__device__ __forceinline__ void sort_desc(float (&v)[kP]) {
+#pragma unroll
+    for (int rnd = 0; rnd < kP; ++rnd)
+#pragma unroll
+        for (int e = rnd & 1; e + 1 < kP; e += 2) {
+            const float a = v[e], b2 = v[e + 1];
+            v[e] = fmaxf(a, b2);
+            v[e + 1] = fminf(a, b2);
+        }
+}
+
+// kP values per lane (n <= 32 kP), kept sorted (largest first), so a lane's candidate is
+// its first value.  The (k+1)-th largest is found by k+1 rounds of "take the warp maximum of
+// the lanes' first values, and the lowest lane holding it drops that value", or, when that
+// is shorter, as the (n-k)-th smallest by rounds of minimum (on negated values).
 template <int kP>
 __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__ s,
                                                        const float* __restrict__ b, int64_t m,
@@ -72,31 +87,24 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__
         for (int e = 0; e < kP; ++e) {
             const int j = lane + 32 * e;
             // s + b in fp32; the top-down search works on -v, so both are "largest first"
-            const float x = (j < n) ? s[i * n + j] + bj[e] : pad;
+            const float x = (j < n) ? __ldg(s + i * n + j) + bj[e] : pad;
             v[e] = from_top ? x : -x;
         }
+        sort_desc(v);
         float a = 0.f;
         for (int r = 0; r < rounds; ++r) {
-            float mx = v[0];
-#pragma unroll
-            for (int e = 1; e < kP; ++e) mx = fmaxf(mx, v[e]);
-            float wm = mx;
+            float wm = v[0];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
                 wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
             a = wm;
             if (r + 1 == rounds) break;
-            // remove one occurrence of the maximum: in the lowest lane holding it, its first
-            const unsigned holders = __ballot_sync(0xffffffffu, mx == wm);
-            if (lane == __ffs(holders) - 1) {
-                bool done = false;
+            // the lowest lane holding the maximum drops it (its list moves up by one)
+            const unsigned holders = __ballot_sync(0xffffffffu, v[0] == wm);
+            const bool pop = lane == __ffs(holders) - 1;
 #pragma unroll
-                for (int e = 0; e < kP; ++e)
-                    if (!done && v[e] == wm) {
-                        v[e] = -INFINITY;
-                        done = true;
-                    }
-            }
+            for (int e = 0; e + 1 < kP; ++e) v[e] = pop ? v[e + 1] : v[e];
+            v[kP - 1] = pop ? -INFINITY : v[kP - 1];
         }
         if (lane == 0) alpha[i] = from_top ? a : -a;
     }
@@ -107,62 +115,19 @@ struct QbColumn {
     uint32_t rank;    // rank of the wanted key among the keys with that prefix (0-based)
 };
 
-__global__ void __launch_bounds__(256) qb_hist_kernel(const float* __restrict__ s,
-                                                      const float* __restrict__ alpha, int64_t m,
-                                                      int n, int rows_per_cta, int shift,
-                                                      const QbColumn* __restrict__ col_state,
-                                                      unsigned* __restrict__ hist) {
-    __shared__ unsigned sh[32][257];  // padded: lane + bin spreads over the banks
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < 32 * 257; i += blockDim.x) (&sh[0][0])[i] = 0u;
-    __syncthreads();
-    const int col = blockIdx.y * 32 + lane;
-    const bool live = col < n;
-    uint32_t prefix = 0u;
-    if (live && shift < 24) prefix = col_state[col].prefix >> (shift + 8);
-    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
-    const int64_t r1 = min(m, r0 + rows_per_cta);
-    if (live) {
-        auto count = [&](float x, float al) {
-            const uint32_t key = desc_key(x - al);
-            if (shift == 24 || (key >> (shift + 8)) == prefix)
-                atomicAdd(&sh[lane][(key >> shift) & 255u], 1u);
-        };
-        int64_t i = r0 + warp;
-        for (; i + 24 < r1; i += 32) {  // four rows per step, loads first
-            float x[4], al[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                x[u] = s[(i + 8 * u) * n + col];
-                al[u] = __ldg(alpha + i + 8 * u);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) count(x[u], al[u]);
-        }
-        for (; i < r1; i += 8) count(s[i * n + col], __ldg(alpha + i));
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < 32 * 256; idx += blockDim.x) {
-        const int c = idx >> 8, bin = idx & 255;
-        const unsigned cnt = sh[c][bin];
-        if (cnt && blockIdx.y * 32 + c < n) atomicAdd(&hist[(size_t)(blockIdx.y * 32 + c) * 256 + bin], cnt);
-    }
-}
-
-__global__ void __launch_bounds__(256) qb_select_kernel(int n, int shift, uint32_t q,
-                                                        QbColumn* __restrict__ col_state,
-                                                        unsigned* __restrict__ hist,
-                                                        float* __restrict__ bhat) {
+// The digit of expert `col` holding its rank (prefix scan over the 256 counts of `h`, one
+// warp), appended to the expert's prefix; the counts are cleared for the next pass.  After
+// the last pass (shift 0) the key is the (q+1)-th largest margin and bhat = -(its value).
+__device__ __forceinline__ void select_digit(int col, int shift, uint32_t q,
+                                             QbColumn* __restrict__ col_state,
+                                             unsigned* __restrict__ h, float* __restrict__ bhat) {
     const int lane = threadIdx.x & 31;
-    const int col = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (col >= n) return;
     QbColumn st = (shift == 24) ? QbColumn{0u, q} : col_state[col];
-    unsigned* h = hist + (size_t)col * 256;
     unsigned c[8];
     unsigned tot = 0u;
 #pragma unroll
     for (int e = 0; e < 8; ++e) {  // lane holds bins 8 lane .. 8 lane + 7
-        c[e] = h[8 * lane + e];
+        c[e] = __ldcg(h + 8 * lane + e);
         tot += c[e];
     }
     unsigned incl = tot;  // inclusive prefix over the lanes
@@ -195,50 +160,129 @@ __global__ void __launch_bounds__(256) qb_select_kernel(int n, int shift, uint32
     for (int e = 0; e < 8; ++e) h[8 * lane + e] = 0u;  // ready for the next pass
 }
 
-__global__ void __launch_bounds__(1024) qb_mean_kernel(const float* __restrict__ bhat, int n,
-                                                       float* __restrict__ b_new) {
-    __shared__ double part[32];
-    double acc = 0.0;
-    for (int j = threadIdx.x; j < n; j += blockDim.x) acc += (double)bhat[j];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+// One radix pass: a CTA counts the digits of 32 experts' margins over its token range and
+// adds them to the global histogram; the last CTA of a column of experts to finish then
+// selects those experts' digits, and after the last pass the last column to finish forms
+// bias_new = bhat - mean(bhat) (one launch per pass in all).
+template <int kU>
+__global__ void __launch_bounds__(256) qb_hist_kernel(const float* __restrict__ s,
+                                                      const float* __restrict__ alpha, int64_t m,
+                                                      int n, int rows_per_cta, int shift,
+                                                      uint32_t q, QbColumn* __restrict__ col_state,
+                                                      unsigned* __restrict__ hist,
+                                                      unsigned* __restrict__ done,
+                                                      float* __restrict__ bhat,
+                                                      float* __restrict__ b_new) {
+    __shared__ unsigned sh[32][257];  // padded: lane + bin spreads over the banks
+    __shared__ double part[8];
+    __shared__ int last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 32 * 257; i += blockDim.x) (&sh[0][0])[i] = 0u;
     __syncthreads();
-    if (threadIdx.x < 32) {
-        double t = (threadIdx.x < blockDim.x / 32) ? part[threadIdx.x] : 0.0;
+    const int col = blockIdx.y * 32 + lane;
+    const bool live = col < n;
+    uint32_t prefix = 0u;
+    if (live && shift < 24) prefix = __ldcg(&col_state[col].prefix) >> (shift + 8);
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = min(m, r0 + rows_per_cta);
+    if (live) {
+        auto count = [&](float x, float al) {
+            const uint32_t key = desc_key(x - al);
+            if (shift == 24 || (key >> (shift + 8)) == prefix)
+                atomicAdd(&sh[lane][(key >> shift) & 255u], 1u);
+        };
+        int64_t i = r0 + warp;
+        for (; i + 8 * (kU - 1) < r1; i += 8 * kU) {  // kU rows per step, loads first
+            float x[kU], al[kU];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-        if (threadIdx.x == 0) part[0] = t;
+            for (int u = 0; u < kU; ++u) {
+                x[u] = __ldg(s + (i + 8 * u) * n + col);
+                al[u] = __ldg(alpha + i + 8 * u);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) count(x[u], al[u]);
+        }
+        for (; i < r1; i += 8) count(__ldg(s + i * n + col), __ldg(alpha + i));
     }
     __syncthreads();
-    const double mean = part[0] / n;
-    for (int j = threadIdx.x; j < n; j += blockDim.x) b_new[j] = (float)((double)bhat[j] - mean);
+    for (int idx = threadIdx.x; idx < 32 * 256; idx += blockDim.x) {
+        const int c = idx >> 8, bin = idx & 255;
+        const unsigned cnt = sh[c][bin];
+        if (cnt && blockIdx.y * 32 + c < n) atomicAdd(&hist[(size_t)(blockIdx.y * 32 + c) * 256 + bin], cnt);
+    }
+    // the last CTA of this column of experts selects their digits
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&done[blockIdx.y], 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int c = warp; c < 32; c += blockDim.x / 32) {
+        const int cc = blockIdx.y * 32 + c;
+        if (cc < n) select_digit(cc, shift, q, col_state, hist + (size_t)cc * 256, bhat);
+    }
+    if (threadIdx.x == 0) done[blockIdx.y] = 0u;  // ready for the next pass
+    if (shift != 0) return;
+    // after the last pass: the last column to finish forms bias_new
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&done[gridDim.y], 1u) == gridDim.y - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double acc = 0.0;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) acc += (double)__ldcg(bhat + j);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) part[warp] = acc;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += part[w];
+    const double mean = tot / n;
+    for (int j = threadIdx.x; j < n; j += blockDim.x)
+        b_new[j] = (float)((double)__ldcg(bhat + j) - mean);
+    if (threadIdx.x == 0) done[gridDim.y] = 0u;
 }
 
 }  // namespace
 
-size_t qb_workspace_size(int64_t m, int n) {
+// workspace: alpha [m], hist [n][256], pass counters [column blocks + 1], column states [n],
+// bhat [n]
+struct QbWs {
+    size_t alpha, hist, done, cols, bhat, total;
+};
+static QbWs qb_ws(int64_t m, int n) {
     auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
-    return al((size_t)m * 4) + al((size_t)n * 256 * 4) + al((size_t)n * sizeof(QbColumn)) +
-           al((size_t)n * 4);
+    QbWs w;
+    w.alpha = 0;
+    w.hist = al((size_t)m * 4);
+    w.done = w.hist + al((size_t)n * 256 * 4);
+    w.cols = w.done + al((size_t)((n + 31) / 32 + 1) * 4);
+    w.bhat = w.cols + al((size_t)n * sizeof(QbColumn));
+    w.total = w.bhat + al((size_t)n * 4);
+    return w;
 }
+
+size_t qb_workspace_size(int64_t m, int n) { return qb_ws(m, n).total; }
 
 cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, int n, int k,
                                     float* b_new, float* bhat_out, float* alpha_out,
                                     void* workspace, cudaStream_t stream) {
-    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const QbWs L = qb_ws(m, n);
     uint8_t* w = static_cast<uint8_t*>(workspace);
-    float* alpha = reinterpret_cast<float*>(w);
-    unsigned* hist = reinterpret_cast<unsigned*>(w + al((size_t)m * 4));
-    QbColumn* cols = reinterpret_cast<QbColumn*>(w + al((size_t)m * 4) + al((size_t)n * 1024));
-    float* bhat = reinterpret_cast<float*>(w + al((size_t)m * 4) + al((size_t)n * 1024) +
-                                           al((size_t)n * sizeof(QbColumn)));
+    float* alpha = reinterpret_cast<float*>(w + L.alpha);
+    unsigned* hist = reinterpret_cast<unsigned*>(w + L.hist);
+    unsigned* done = reinterpret_cast<unsigned*>(w + L.done);
+    QbColumn* cols = reinterpret_cast<QbColumn*>(w + L.cols);
+    float* bhat = reinterpret_cast<float*>(w + L.bhat);
     if (alpha_out) alpha = alpha_out;
     if (bhat_out) bhat = bhat_out;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)n * 1024, stream);
+    // histogram and pass counters cleared (contiguous); every pass leaves them cleared
+    cudaError_t e = cudaMemsetAsync(w + L.hist, 0, L.cols - L.hist, stream);
     if (e != cudaSuccess) return e;
     {
         const int64_t want = (m + 7) / 8;
@@ -260,24 +304,17 @@ cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, i
     }
     const uint32_t q = (uint32_t)((m * k) / n);
     const int col_blocks = (n + 31) / 32;
-    // about four CTAs per SM in total, at least 256 tokens each
-    int64_t row_blocks = ((int64_t)sms * 4 + col_blocks - 1) / col_blocks;
+    // about two CTAs per SM in total (each with 16 rows of loads in flight per warp), at
+    // least 256 tokens each
+    int64_t row_blocks = ((int64_t)sms * 2 + col_blocks - 1) / col_blocks;
     if (row_blocks > (m + 255) / 256) row_blocks = (m + 255) / 256;
     if (row_blocks < 1) row_blocks = 1;
     const int rows_per_cta = (int)((m + row_blocks - 1) / row_blocks);
     row_blocks = (m + rows_per_cta - 1) / rows_per_cta;
     for (int shift = 24; shift >= 0; shift -= 8) {
-        {
-            ProfScope prof("qb_hist_kernel", stream);
-            qb_hist_kernel<<<dim3((unsigned)row_blocks, (unsigned)col_blocks), 256, 0, stream>>>(
-                s, alpha, m, n, rows_per_cta, shift, cols, hist);
-        }
-        ProfScope prof("qb_select_kernel", stream);
-        qb_select_kernel<<<(n + 7) / 8, 256, 0, stream>>>(n, shift, q, cols, hist, bhat);
-    }
-    {
-        ProfScope prof("qb_mean_kernel", stream);
-        qb_mean_kernel<<<1, 1024, 0, stream>>>(bhat, n, b_new);
+        ProfScope prof("qb_hist_kernel", stream);
+        qb_hist_kernel<16><<<dim3((unsigned)row_blocks, (unsigned)col_blocks), 256, 0, stream>>>(
+            s, alpha, m, n, rows_per_cta, shift, q, cols, hist, done, bhat, b_new);
     }
     return cudaGetLastError();
 }
