@@ -932,7 +932,7 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
         }
 
         // ---- while the Gram MMAs run: the globally scaled operands of the later products,
-        //      Gam*Q and K*gamma^C/Gam (package, for the state kernel) and Gam*K (W = M Gam K)
+        //      Gam*Q and K*gamma^C/Gam (package, for the chain stage) and Gam*K (W = M Gam K)
         {
         uint8_t* pkg = item_pkg();
 #pragma unroll

@@ -1,5 +1,6 @@
 // fwd_tc.cu -- chunked KDA forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA),
-// bf16 I/O, dk = dv = 128, chunk C = 64 with 16-token sub-tiles, fp32 state.
+// bf16 I/O, heads of 64 or 128 channels (a 64 runs zero-padded to 128), chunk C = 64 with
+// 16-token sub-tiles, fp32 state.
 //
 // Method ("Kimi k3 技术报告详解（1）——架构再升华", section "Chunkwise parallel form"):
 // per chunk, with G[r] = sum_{s<=r} g_s (per key channel) and gamma = e^G,
@@ -8,20 +9,21 @@
 //   Vt = U - W S,  O = (Gamma*Q) S + A Vt,  S <- Diag(gamma^C) S + (K*gamma^C/Gamma)^T Vt
 // The last line (chunk-to-chunk update) is the recurrence unrolled over one chunk.
 //
-// Three launches on the caller's stream:
-//   plan_kernel   chunk offsets of every sequence (exclusive scan of ceil(len/64)) and a
-//                 table entry per chunk (first row, sequence, rows).
-//   intra_kernel  every (chunk, head) in parallel (persistent, one CTA per SM: 8 warps, one
-//                 thread of which also issues; inputs by TMA, next item prefetched): gate +
-//                 in-chunk cumsum, the two sub-tiled Gram matrices in ONE tcgen05 MMA, the
-//                 UT solve (fp32 forward substitution on the diagonal blocks, tf32
-//                 mma.sync for the rest), W and U by tcgen05; writes one "package" per
-//                 (head, chunk) whose bytes are the shared-memory image of the state
-//                 kernel's MMA operands.
-//   state_kernel  four CTAs per (sequence, head), each owning 32 of the 128 value columns
-//                 (the columns of S evolve independently), serial over chunks: state S in
-//                 fp32 registers, packages streamed in by bulk copies (double buffered),
-//                 [W; Gamma Q] S, K~^T Vt and A Vt on tcgen05.
+// Two stages (fwd_intra.cuh, fwd_chain.cuh) joined by a per-(head, chunk) "package" of
+// S-independent operands (fwd_tc_layout.cuh):
+//   intra stage   every (chunk, head) in parallel: gate + in-chunk cumsum, both sub-tiled
+//                 Gram matrices in one tcgen05 MMA, the UT solve, W and U by tcgen05; writes
+//                 the chunk's package, whose bytes are the chain stage's shared-memory tiles.
+//   chain stage   per (sequence, head), serial over chunks, the state transposed in TMEM:
+//                 [W; Gamma Q] S, K~^T Vt and A Vt on tcgen05, fp32 state in registers.
+// Launch forms, on the caller's stream, after plan_kernel (chunk offsets of every sequence,
+// a table entry per chunk, the sequences longest first):
+//   fwd_fused_kernel  one cooperative launch: CTAs [0, C) run the C chains, the others the
+//                     intra stage, the packages handed over through a ring of slots that
+//                     stays in L2 (equal-length sequences without cu_seqlens, C <= 64);
+//   intra_kernel, then chain_kernel  the packages through the workspace in HBM (otherwise).
+// The intra stage also has the mixed-path instantiation for the softplus gate (see
+// fwd_intra.cuh).
 //
 // Sub-tiling ("16-token tiles" of the same section; the bounded gate g > g_min is what
 // keeps these factors finite): the Gram entry for rows r >= i needs e^{G_r - G_i} per

@@ -39,7 +39,7 @@ def _shift_z(inp, dz):
     return inp
 
 
-@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f32", 128)])
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f32", 128), ("bf16", 64)])
 def test_matches_recurrence(kda, dtype, d):
     inp = inputs.forward_inputs(seed=61, lengths=[100, 64, 1, 300, 0, 129], H=2, dk=d, dv=d,
                                 dtype=dtype, with_state=True)
