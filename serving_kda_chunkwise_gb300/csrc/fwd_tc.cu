@@ -176,9 +176,11 @@ struct FusedParams {
     int C;
 };
 
-// Registers: the launch gives every thread 168 (384 x 168 = 64,512).  In an intra CTA the
-// third warpgroup has no work: it returns its registers (24 each) and the two working
-// warpgroups take 240 each, 2 x 128 x 240 + 128 x 24 = 64,512, the launch's total.
+// Registers: the launch gives every thread 168 (384 x 168 = 64,512).  In an intra CTA of the
+// bounded gate the third warpgroup has no work: it returns its registers (24 each) and the
+// two working warpgroups take 240 each, 2 x 128 x 240 + 128 x 24 = 64,512, the launch's
+// total.  (The softplus instantiation measured faster at 168: 4.77 against 5.0 ms at
+// T = 65536, H = 32, so it keeps the launch's registers.)
 constexpr int kFusedRegs = 168, kIntraRegs = 240, kIdleRegs = 24;
 static_assert(kFusedThreads == kIntraThreads + 128, "one idle warpgroup in an intra CTA");
 static_assert(kIntraThreads * kIntraRegs + 128 * kIdleRegs <= kFusedThreads * kFusedRegs,
@@ -190,9 +192,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fwd_fused_kernel(const __gri
     if ((int)blockIdx.x < p.C) {
         if (threadIdx.x < kChainThreads) chain_body(p.cp, smem_raw, blockIdx.x, p.C);
     } else if (threadIdx.x >= kIntraThreads) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIdleRegs));
+        if constexpr (kGate == kGateBounded) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIdleRegs));
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kIntraRegs));
+        if constexpr (kGate == kGateBounded) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kIntraRegs));
         intra_body<kGate>(p.ip, smem_raw, blockIdx.x - p.C, gridDim.x - p.C);
     }
 }
