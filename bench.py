@@ -331,7 +331,8 @@ def run_ours(args, rank, world, local_rank, dist):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     e2e = {"value": job_rate(world, T, e2e_steps, e2e_ms), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "link": host_link_bandwidth(dev, stream)}
     del host
 
     # the gated output step after the forward ("Gated MLA"), on the forward's output, with the
@@ -386,6 +387,33 @@ def run_ours(args, rank, world, local_rank, dist):
                 "clocks": clk, "output_gate": og, "quantile_balance": qbm, "gate_comparison": gcmp, "backward": bw, "decode": dec, "cpu_baseline": cpu,
                 "other_workloads": others}
         print(json.dumps(line), flush=True)
+
+
+def host_link_bandwidth(dev, stream, nbytes=1 << 30, reps=3):
+    """What bounds the end-to-end figure: one 1 GiB copy each way between pinned host memory
+    (page-locked, allocated by this process on its own NUMA node) and the device, on the
+    launch stream, timed with CUDA events (best of reps)."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        best = None
+        for _ in range(reps):
+            ev0 = torch.cuda.Event(enable_timing=True)
+            ev1 = torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            with torch.cuda.stream(stream):
+                fn()
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = ev0.elapsed_time(ev1)
+            best = ms if best is None else min(best, ms)
+        out[name + "_GBs"] = nbytes / (best / 1e3) / 1e9
+    out["how"] = "1 GiB pinned host <-> device copy each way, CUDA events, best of 3"
+    del h, d
+    return out
 
 
 def bench_forward_workload(dev, stream, peaks, name, reps=5):

@@ -295,8 +295,8 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     const bool fused = a.cu_seqlens == nullptr && a.T_total > 0 && C <= kFusedMaxChains &&
                        sms - C >= 16 && ring_slots >= kRingSlotsMin && nct_all > ring_slots &&
                        !(fenv && strcmp(fenv, "0") == 0);
-    // fused: the ring [C][kRingSlots] packages, then ready flags [C][kRingSlots] and consumed
-    // counters [C], inside the package region of the workspace
+    // fused: the ring [C][ring_slots] packages, then ready flags [C][ring_slots], consumed
+    // counters [C] and the item counter, inside the package region of the workspace
     uint8_t* ring = pkg;
     uint32_t* flags = reinterpret_cast<uint32_t*>(pkg + (size_t)C * ring_slots * kPkgBytes);
     const int n_flags = fused ? C * (ring_slots + 1) + 1 : 0;  // + the item counter
