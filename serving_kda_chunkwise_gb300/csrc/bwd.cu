@@ -11,7 +11,9 @@
 //   dz = dx e^{A_h};   dA_h += sum dx x.
 // The pages print no backward; these are the derivatives of the forward they define.
 //
-// On CUDA cores in fp32, parallel over chunks.  The state and its gradient are the only
+// Parallel over chunks.  For bf16 problems the states at the chunk starts come from the
+// tensor-core forward (its chain stage writes them, no output); otherwise, and for the rest,
+// on CUDA cores in fp32.  The state and its gradient are the only
 // serial quantities, and over one 64-token chunk both are affine.  Forward, S_t =
 // (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T, so S_(chunk end) =
 // A S_(chunk start) + B.  Backward, going back through token t maps dS_t to
@@ -22,6 +24,8 @@
 // state-shaped matrix and lane l its columns l, l + 32, ..; matrices live in registers, and
 // each chunk's token inputs are staged in shared memory once):
 //   bwd_plan_kernel   chunk offsets of every sequence and a table entry per chunk
+//   (bf16)            the tensor-core forward (fwd_tc.cu) with its chain stage writing the
+//                     state at every chunk start, the checkpoints, in place of the next two
 //   bwd_fwdtrans_kernel  per (chunk, head), all in parallel: the chunk's forward map on the
 //                     state, S_end = A S_start + B
 //   bwd_chain_kernel<fwd>  per (sequence, head, 32-column slice): S at every chunk start
@@ -756,8 +760,11 @@ __global__ void bwd_dA_kernel(const float* __restrict__ part, const int32_t* __r
     dA_log[h] = s;
 }
 
+// ckpt_ready: the states at the chunk starts are already in p.ckpt (written by the
+// tensor-core forward), so the forward maps and their chain are skipped.
 template <typename IO, int DK, int DV>
-cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream_t stream) {
+cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, bool ckpt_ready,
+                     cudaStream_t stream) {
     constexpr int chain_smem = (DK * kChainCols + DK * DK) * 4;
     cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
@@ -777,11 +784,11 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream
         e = cudaFuncSetAttribute(bwd_item_kernel<IO, DK, DV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_item);
     if (e != cudaSuccess) return e;
-    {
-        ProfScope prof("bwd_fwdtrans_kernel", stream);
-        bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_fwdtrans, stream>>>(p);
-    }
-    {
+    if (!ckpt_ready) {
+        {
+            ProfScope prof("bwd_fwdtrans_kernel", stream);
+            bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_fwdtrans, stream>>>(p);
+        }
         ProfScope prof("bwd_fchain_kernel", stream);
         bwd_chain_kernel<DK, DV, true><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
     }
@@ -812,9 +819,10 @@ int sm_count() {
 // Workspace, for at most C = T/64 + N chunks: chunk offsets [N + 1] and table [C]; the state
 // at each chunk start, Psi and the state's gradient at each chunk end [C][H][dk][dv] fp32;
 // Phi [C][H][dk][dk] fp32; kNB + kSB = 16 states of scratch per CTA of the per-chunk kernel;
-// [C][H] dA_log partials.
+// [C][H] dA_log partials; then the workspace of the tensor-core forward, which writes the
+// chunk-start states of bf16 problems.
 struct BwdLayoutWs {
-    size_t off, tab, ckpt, phi, psi, dsend, snap, dA, total;
+    size_t off, tab, ckpt, phi, psi, dsend, snap, dA, fwd, total;
 };
 
 BwdLayoutWs bwd_ws_layout(int64_t T_total, int N, int H, int dk, int dv, int grid_items) {
@@ -830,6 +838,8 @@ BwdLayoutWs bwd_ws_layout(int64_t T_total, int N, int H, int dk, int dv, int gri
     w.dsend = o; o += al(C * H * dk * dv * 4);
     w.snap = o;  o += al((size_t)grid_items * (kNB + kSB) * dk * dv * 4);
     w.dA = o;    o += al(C * H * 4);
+    o = (o + 1023) & ~size_t(1023);  // the forward's tiles want 1 KB alignment
+    w.fwd = o;   o += al(fwd_tc_workspace_size(T_total, N, H));
     w.total = o;
     return w;
 }
@@ -872,16 +882,33 @@ cudaError_t launch_bwd(const BwdArgs& a) {
                                                   p.chunk_tab, a.dev_err);
     }
     cudaError_t e;
+    // bf16: the chunk-start states come from the tensor-core forward (its chain stage
+    // writes them, and no output), in place of the forward maps and their chain
+    const bool tc = a.io_bf16 != 0;
+    if (tc) {
+        FwdArgs f{};
+        f.q = a.q; f.k = a.k; f.v = a.v; f.beta = a.beta; f.z = a.z;
+        f.A_log = a.A_log; f.g_min = a.g_min; f.S0 = a.S0; f.S_out = nullptr;
+        f.cu_seqlens = a.cu_seqlens; f.N = a.N; f.T_total = a.T_total; f.H = a.H;
+        f.dk = a.dk; f.dv = a.dv; f.io_bf16 = 1; f.gate_kind = 0; f.o = nullptr;
+        f.workspace = ws + w.fwd;
+        f.ws_bytes = fwd_tc_workspace_size(a.T_total, a.N, a.H);
+        f.dev_err = a.dev_err;
+        f.stream = a.stream;
+        f.ckpt = p.ckpt;
+        e = launch_fwd_tc(f);
+        if (e != cudaSuccess) return e;
+    }
     if (a.io_bf16) {
-        if (a.dk == 128 && a.dv == 128) e = launch_t<__nv_bfloat16, 128, 128>(p, grid_nh, grid_items, a.stream);
-        else if (a.dk == 128 && a.dv == 64) e = launch_t<__nv_bfloat16, 128, 64>(p, grid_nh, grid_items, a.stream);
-        else if (a.dk == 64 && a.dv == 128) e = launch_t<__nv_bfloat16, 64, 128>(p, grid_nh, grid_items, a.stream);
-        else e = launch_t<__nv_bfloat16, 64, 64>(p, grid_nh, grid_items, a.stream);
+        if (a.dk == 128 && a.dv == 128) e = launch_t<__nv_bfloat16, 128, 128>(p, grid_nh, grid_items, tc, a.stream);
+        else if (a.dk == 128 && a.dv == 64) e = launch_t<__nv_bfloat16, 128, 64>(p, grid_nh, grid_items, tc, a.stream);
+        else if (a.dk == 64 && a.dv == 128) e = launch_t<__nv_bfloat16, 64, 128>(p, grid_nh, grid_items, tc, a.stream);
+        else e = launch_t<__nv_bfloat16, 64, 64>(p, grid_nh, grid_items, tc, a.stream);
     } else {
-        if (a.dk == 128 && a.dv == 128) e = launch_t<float, 128, 128>(p, grid_nh, grid_items, a.stream);
-        else if (a.dk == 128 && a.dv == 64) e = launch_t<float, 128, 64>(p, grid_nh, grid_items, a.stream);
-        else if (a.dk == 64 && a.dv == 128) e = launch_t<float, 64, 128>(p, grid_nh, grid_items, a.stream);
-        else e = launch_t<float, 64, 64>(p, grid_nh, grid_items, a.stream);
+        if (a.dk == 128 && a.dv == 128) e = launch_t<float, 128, 128>(p, grid_nh, grid_items, false, a.stream);
+        else if (a.dk == 128 && a.dv == 64) e = launch_t<float, 128, 64>(p, grid_nh, grid_items, false, a.stream);
+        else if (a.dk == 64 && a.dv == 128) e = launch_t<float, 64, 128>(p, grid_nh, grid_items, false, a.stream);
+        else e = launch_t<float, 64, 64>(p, grid_nh, grid_items, false, a.stream);
     }
     if (e != cudaSuccess) return e;
     ProfScope prof("bwd_dA_kernel", a.stream);

@@ -92,6 +92,10 @@ struct ChainParams {
     // head sizes of q, k (dk) and v, o, S (dv), 64 or 128: a 64 is zero-padded to 128 inside
     // (the tensor maps read zeros past it), so only the state and output addresses use them
     int dk, dv;
+    // optional (nullptr otherwise): the state at every chunk start, fp32
+    // [chunks][H][dk][dv] with chunk = chunk_off[n] + t, for a backward pass; with o ==
+    // nullptr the output is not stored
+    float* ckpt;
     // fused kernel only (fused = 0 otherwise): CTA c serves chain c and reads chunk t from
     // ring slot c * ring_slots + t % ring_slots once ready[slot] >= t + 1; it raises
     // consumed[c] to t + 1 once every part of chunk t is in shared memory
@@ -329,7 +333,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             tmem_ld16(col + 16, o1);
             tmem_ld_wait();
             const int64_t r0 = t0 + 32 * wg;
-            if (j >= p.dv) {  // a padding column: nothing to store
+            if (j >= p.dv || p.o == nullptr) {  // a padding column, or no output wanted
                 tc_fence_before();
                 return true;
             }
@@ -362,7 +366,17 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             const size_t sbase_el = ((size_t)(c.n * p.H + c.h) * p.dk + 64 * wg) * p.dv + j;
 #pragma unroll
             for (int e = 0; e < 64; ++e) S[e] = (p.S0 && sv) ? p.S0[sbase_el + (size_t)e * p.dv] : 0.f;
+            // the state at the start of chunk t, for a backward pass (coalesced: for each row
+            // the 32 lanes of a warp write 128 contiguous bytes)
+            auto store_ckpt = [&](int t) {
+                if (!p.ckpt || !sv) return;
+                const int chunk = __ldg(p.chunk_off + c.n) + t;
+                float* dst = p.ckpt + (((size_t)chunk * p.H + c.h) * p.dk + 64 * wg) * p.dv + j;
+#pragma unroll
+                for (int e = 0; e < 64; ++e) dst[(size_t)e * p.dv] = S[e];
+            };
             if (c.nch > 0) {
+                store_ckpt(0);
                 uint32_t pk[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e) pk[e] = pack2(S[2 * e], S[2 * e + 1]);
@@ -459,6 +473,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0 && t + 1 < c.nch) mbar_arrive(s_ready);
+                if (t + 1 < c.nch) store_ckpt(t + 1);
                 if (rec) CH_MARK(12);
                 if (t + 1 == c.nch && !store_out(g, t0, c)) { ok = false; break; }
                 tc_fence_before();

@@ -343,6 +343,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     cp.H = a.H;
     cp.dk = a.dk;
     cp.dv = a.dv;
+    cp.ckpt = a.ckpt;
     cp.maxchunks = maxchunks;
 
     if (fused) {

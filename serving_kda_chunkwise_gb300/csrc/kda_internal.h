@@ -22,11 +22,14 @@ struct FwdArgs {
     int H, dk, dv;
     int io_bf16;  // 1: bf16 I/O, 0: fp32 I/O
     int gate_kind;  // 0: g_min Sigmoid(e^A z); 1: -e^A Softplus(z)
-    void* o;
+    void* o;              // may be nullptr on the tensor-core path (no output stored)
     void* workspace;
     size_t ws_bytes;
     unsigned* dev_err;
     cudaStream_t stream;
+    // tensor-core path only, optional: the fp32 state at every chunk start,
+    // [chunks][H][dk][dv] in the order of the chunk offsets (for a backward pass)
+    float* ckpt;
 };
 
 struct BwdArgs {
