@@ -24,8 +24,11 @@
 // state-shaped matrix and lane l its columns l, l + 32, ..; matrices live in registers, and
 // each chunk's token inputs are staged in shared memory once):
 //   bwd_plan_kernel   chunk offsets of every sequence and a table entry per chunk
-//   (bf16)            the tensor-core forward (fwd_tc.cu) with its chain stage writing the
-//                     state at every chunk start, the checkpoints, in place of the next two
+//   (bf16)            the tensor-core forward (fwd_tc.cu, two-launch form) with its chain
+//                     stage writing the state at every chunk start, the checkpoints, then
+//                     the gradient chain on the tensor cores (bwd_chain_tc.cu) reading its
+//                     chunk packages: dS at every chunk end and dS0.  They replace the next
+//                     four kernels.
 //   bwd_fwdtrans_kernel  per (chunk, head), all in parallel: the chunk's forward map on the
 //                     state, S_end = A S_start + B
 //   bwd_chain_kernel<fwd>  per (sequence, head, 32-column slice): S at every chunk start
@@ -760,10 +763,11 @@ __global__ void bwd_dA_kernel(const float* __restrict__ part, const int32_t* __r
     dA_log[h] = s;
 }
 
-// ckpt_ready: the states at the chunk starts are already in p.ckpt (written by the
-// tensor-core forward), so the forward maps and their chain are skipped.
+// tc_chains: the states at the chunk starts (p.ckpt) and the state's gradient at the chunk
+// ends (p.dsend, and dS0) were written by the tensor-core chains, so the per-chunk maps and
+// their CUDA-core chains are skipped.
 template <typename IO, int DK, int DV>
-cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, bool ckpt_ready,
+cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, bool tc_chains,
                      cudaStream_t stream) {
     constexpr int chain_smem = (DK * kChainCols + DK * DK) * 4;
     cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, true>,
@@ -784,19 +788,19 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, bool ckpt_
         e = cudaFuncSetAttribute(bwd_item_kernel<IO, DK, DV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_item);
     if (e != cudaSuccess) return e;
-    if (!ckpt_ready) {
+    if (!tc_chains) {
         {
             ProfScope prof("bwd_fwdtrans_kernel", stream);
             bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_fwdtrans, stream>>>(p);
         }
-        ProfScope prof("bwd_fchain_kernel", stream);
-        bwd_chain_kernel<DK, DV, true><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
-    }
-    {
-        ProfScope prof("bwd_phi_kernel", stream);
-        bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_phi, stream>>>(p);
-    }
-    {
+        {
+            ProfScope prof("bwd_fchain_kernel", stream);
+            bwd_chain_kernel<DK, DV, true><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
+        }
+        {
+            ProfScope prof("bwd_phi_kernel", stream);
+            bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_phi, stream>>>(p);
+        }
         ProfScope prof("bwd_chain_kernel", stream);
         bwd_chain_kernel<DK, DV, false><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
     }
@@ -883,7 +887,10 @@ cudaError_t launch_bwd(const BwdArgs& a) {
     }
     cudaError_t e;
     // bf16: the chunk-start states come from the tensor-core forward (its chain stage
-    // writes them, and no output), in place of the forward maps and their chain
+    // writes them, and no output) in its two-launch form, which leaves the chunk packages in
+    // its workspace; the gradient chain on the tensor cores reads those packages and writes
+    // the state's gradient at every chunk end.  They replace the per-chunk maps and the
+    // CUDA-core chains.
     const bool tc = a.io_bf16 != 0;
     if (tc) {
         FwdArgs f{};
@@ -896,7 +903,10 @@ cudaError_t launch_bwd(const BwdArgs& a) {
         f.dev_err = a.dev_err;
         f.stream = a.stream;
         f.ckpt = p.ckpt;
+        f.keep_packages = 1;
         e = launch_fwd_tc(f);
+        if (e != cudaSuccess) return e;
+        e = launch_bwd_chain_tc(a, ws + w.fwd, p.dsend, a.stream);
         if (e != cudaSuccess) return e;
     }
     if (a.io_bf16) {

@@ -284,7 +284,8 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // The fused form needs equal sequence lengths (no cu_seqlens: the chunk-major item order
     // then follows every chain in step), at most kFusedMaxChains chains, and SMs left over
-    // for the intra stage.  KDA_FWD_FUSED=0 in the environment selects the two-launch form.
+    // for the intra stage, and keep_packages unset.  KDA_FWD_FUSED=0 in the environment
+    // selects the two-launch form.
     // The ring and its flags live in the workspace's package region, which holds
     // H * maxchunks >= C * nct packages: nct > ring_slots leaves room for both.
     const int C = a.N * a.H;
@@ -292,8 +293,8 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     int ring_slots = C > 0 ? (int)(kRingBytesMax / ((size_t)C * kPkgBytes)) : 0;
     ring_slots = ring_slots > kRingSlotsMax ? kRingSlotsMax : ring_slots;
     const char* fenv = getenv("KDA_FWD_FUSED");
-    const bool fused = a.cu_seqlens == nullptr && a.T_total > 0 && C <= kFusedMaxChains &&
-                       sms - C >= 16 && ring_slots >= kRingSlotsMin && nct_all > ring_slots &&
+    const bool fused = !a.keep_packages && a.cu_seqlens == nullptr && a.T_total > 0 &&
+                       C <= kFusedMaxChains && sms - C >= 16 && ring_slots >= kRingSlotsMin && nct_all > ring_slots &&
                        !(fenv && strcmp(fenv, "0") == 0);
     // fused: the ring [C][ring_slots] packages, then ready flags [C][ring_slots], consumed
     // counters [C] and the item counter, inside the package region of the workspace

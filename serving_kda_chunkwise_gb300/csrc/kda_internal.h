@@ -30,6 +30,9 @@ struct FwdArgs {
     // tensor-core path only, optional: the fp32 state at every chunk start,
     // [chunks][H][dk][dv] in the order of the chunk offsets (for a backward pass)
     float* ckpt;
+    // tensor-core path only: nonzero selects the two-launch form, which leaves every
+    // (chunk, head) package in the workspace (the backward's gradient chain reads them)
+    int keep_packages;
 };
 
 struct BwdArgs {
@@ -91,6 +94,11 @@ cudaError_t launch_fwd_generic(const FwdArgs& a);
 // fwd_tc_workspace_size() bytes.
 size_t fwd_tc_workspace_size(int64_t T_total, int N, int H);
 cudaError_t launch_fwd_tc(const FwdArgs& a);
+
+// The backward's gradient chain on tcgen05 tensor cores (bwd_chain_tc.cu), bf16 problems:
+// from the packages that launch_fwd_tc with keep_packages left in `fwd_ws`, the state's
+// gradient at every chunk end into dsend ([chunks][H][dk][dv] fp32) and a.dS0.
+cudaError_t launch_bwd_chain_tc(const BwdArgs& a, void* fwd_ws, float* dsend, cudaStream_t stream);
 
 // The argument checks of kda_fwd_chunked except those of the workspace (api.cu): KDA_OK, or
 // the failing status with the calling thread's last error set.
