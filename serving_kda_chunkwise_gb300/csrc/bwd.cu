@@ -41,6 +41,7 @@
 //                     the chunk's checkpoint by 8-token sub-blocks (per-CTA scratch)
 //   bwd_dA_kernel     dA_log[h] = the per-(chunk, head) partial sums in chunk order
 //                     (deterministic)
+#include "bwd_tc_layout.cuh"
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -763,12 +764,8 @@ __global__ void bwd_dA_kernel(const float* __restrict__ part, const int32_t* __r
     dA_log[h] = s;
 }
 
-// tc_chains: the states at the chunk starts (p.ckpt) and the state's gradient at the chunk
-// ends (p.dsend, and dS0) were written by the tensor-core chains, so the per-chunk maps and
-// their CUDA-core chains are skipped.
 template <typename IO, int DK, int DV>
-cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, bool tc_chains,
-                     cudaStream_t stream) {
+cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream_t stream) {
     constexpr int chain_smem = (DK * kChainCols + DK * DK) * 4;
     cudaError_t e = cudaFuncSetAttribute(bwd_chain_kernel<DK, DV, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem);
@@ -788,19 +785,19 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, bool tc_ch
         e = cudaFuncSetAttribute(bwd_item_kernel<IO, DK, DV>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem_item);
     if (e != cudaSuccess) return e;
-    if (!tc_chains) {
-        {
-            ProfScope prof("bwd_fwdtrans_kernel", stream);
-            bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_fwdtrans, stream>>>(p);
-        }
-        {
-            ProfScope prof("bwd_fchain_kernel", stream);
-            bwd_chain_kernel<DK, DV, true><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
-        }
-        {
-            ProfScope prof("bwd_phi_kernel", stream);
-            bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_phi, stream>>>(p);
-        }
+    {
+        ProfScope prof("bwd_fwdtrans_kernel", stream);
+        bwd_fwdtrans_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_fwdtrans, stream>>>(p);
+    }
+    {
+        ProfScope prof("bwd_fchain_kernel", stream);
+        bwd_chain_kernel<DK, DV, true><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
+    }
+    {
+        ProfScope prof("bwd_phi_kernel", stream);
+        bwd_phi_kernel<IO, DK, DV><<<grid_items, kBwdThreads, smem_phi, stream>>>(p);
+    }
+    {
         ProfScope prof("bwd_chain_kernel", stream);
         bwd_chain_kernel<DK, DV, false><<<grid_nh, kBwdThreads, chain_smem, stream>>>(p);
     }
@@ -820,30 +817,37 @@ int sm_count() {
 
 }  // namespace
 
-// Workspace, for at most C = T/64 + N chunks: chunk offsets [N + 1] and table [C]; the state
-// at each chunk start, Psi and the state's gradient at each chunk end [C][H][dk][dv] fp32;
-// Phi [C][H][dk][dk] fp32; kNB + kSB = 16 states of scratch per CTA of the per-chunk kernel;
-// [C][H] dA_log partials; then the workspace of the tensor-core forward, which writes the
-// chunk-start states of bf16 problems.
+// Workspace, for at most C = T/64 + N chunks.  fp32 problems: chunk offsets [N + 1] and table
+// [C]; the state at each chunk start, Psi and the state's gradient at each chunk end
+// [C][H][dk][dv] fp32; Phi [C][H][dk][dk] fp32; kNB + kSB = 16 states of scratch per CTA of
+// the per-chunk kernel; [C][H] dA_log partials.  bf16 problems: the chunk offsets and table,
+// the dA_log partials, the workspace of the tensor-core forward (plan and chunk packages),
+// then the image and mid blocks of the tensor-core per-chunk kernels, [C][H] each
+// (bwd_tc_layout.cuh).  The public size is the larger of the two.
 struct BwdLayoutWs {
-    size_t off, tab, ckpt, phi, psi, dsend, snap, dA, fwd, total;
+    size_t off, tab, ckpt, phi, psi, dsend, snap, dA, fwd, bimg, mid, total;
 };
 
-BwdLayoutWs bwd_ws_layout(int64_t T_total, int N, int H, int dk, int dv, int grid_items) {
-    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+BwdLayoutWs bwd_ws_layout(int64_t T_total, int N, int H, int dk, int dv, int grid_items,
+                          bool bf16) {
+    auto al = [](size_t x) { return (x + 1023) & ~size_t(1023); };
     const size_t C = (size_t)(T_total / kBwdC + N);
     BwdLayoutWs w{};
     size_t o = 0;
     w.off = o;   o += al((size_t)(N + 1) * 4);
     w.tab = o;   o += al(C * 16);
-    w.ckpt = o;  o += al(C * H * dk * dv * 4);
-    w.phi = o;   o += al(C * H * dk * dk * 4);
-    w.psi = o;   o += al(C * H * dk * dv * 4);
-    w.dsend = o; o += al(C * H * dk * dv * 4);
-    w.snap = o;  o += al((size_t)grid_items * (kNB + kSB) * dk * dv * 4);
     w.dA = o;    o += al(C * H * 4);
-    o = (o + 1023) & ~size_t(1023);  // the forward's tiles want 1 KB alignment
-    w.fwd = o;   o += al(fwd_tc_workspace_size(T_total, N, H));
+    if (bf16) {
+        w.fwd = o;   o += al(fwd_tc_workspace_size(T_total, N, H));
+        w.bimg = o;  o += al(C * H * (size_t)bwdtc::kBiBytes);
+        w.mid = o;   o += al(C * H * (size_t)bwdtc::kMdBytes);
+    } else {
+        w.ckpt = o;  o += al(C * H * dk * dv * 4);
+        w.phi = o;   o += al(C * H * dk * dk * 4);
+        w.psi = o;   o += al(C * H * dk * dv * 4);
+        w.dsend = o; o += al(C * H * dk * dv * 4);
+        w.snap = o;  o += al((size_t)grid_items * (kNB + kSB) * dk * dv * 4);
+    }
     w.total = o;
     return w;
 }
@@ -855,7 +859,10 @@ int bwd_grid_items(int64_t T_total, int N, int H) {
 }
 
 size_t bwd_workspace_size_public(int64_t T_total, int N, int H, int dk, int dv) {
-    return bwd_ws_layout(T_total, N, H, dk, dv, bwd_grid_items(T_total, N, H)).total;
+    const int gi = bwd_grid_items(T_total, N, H);
+    const size_t a = bwd_ws_layout(T_total, N, H, dk, dv, gi, false).total;
+    const size_t b = bwd_ws_layout(T_total, N, H, dk, dv, gi, true).total;
+    return a > b ? a : b;
 }
 
 cudaError_t launch_bwd(const BwdArgs& a) {
@@ -864,7 +871,7 @@ cudaError_t launch_bwd(const BwdArgs& a) {
     const int64_t nh = (int64_t)a.N * a.H * (a.dv / kChainCols);  // chain CTAs: column slices
     const int cap_nh = sm_count() * 2;
     const int grid_nh = (int)(nh < cap_nh ? nh : cap_nh);
-    const BwdLayoutWs w = bwd_ws_layout(a.T_total, a.N, a.H, a.dk, a.dv, grid_items);
+    const BwdLayoutWs w = bwd_ws_layout(a.T_total, a.N, a.H, a.dk, a.dv, grid_items, a.io_bf16 != 0);
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     BwdParams p{};
     p.q = a.q; p.k = a.k; p.v = a.v; p.beta = a.beta; p.z = a.z; p.dout = a.dout;
@@ -886,13 +893,10 @@ cudaError_t launch_bwd(const BwdArgs& a) {
                                                   p.chunk_tab, a.dev_err);
     }
     cudaError_t e;
-    // bf16: the chunk-start states come from the tensor-core forward (its chain stage
-    // writes them, and no output) in its two-launch form, which leaves the chunk packages in
-    // its workspace; the gradient chain on the tensor cores reads those packages and writes
-    // the state's gradient at every chunk end.  They replace the per-chunk maps and the
-    // CUDA-core chains.
-    const bool tc = a.io_bf16 != 0;
-    if (tc) {
+    if (a.io_bf16) {
+        // bf16: the tensor-core forward in its two-launch form (its packages stay in the
+        // workspace; its intra stage writes N and its chain S_0 and Vt into the image
+        // blocks), the gradient chain (dS_C, dVt and dS0), then the per-chunk kernels
         FwdArgs f{};
         f.q = a.q; f.k = a.k; f.v = a.v; f.beta = a.beta; f.z = a.z;
         f.A_log = a.A_log; f.g_min = a.g_min; f.S0 = a.S0; f.S_out = nullptr;
@@ -902,23 +906,16 @@ cudaError_t launch_bwd(const BwdArgs& a) {
         f.ws_bytes = fwd_tc_workspace_size(a.T_total, a.N, a.H);
         f.dev_err = a.dev_err;
         f.stream = a.stream;
-        f.ckpt = p.ckpt;
-        f.keep_packages = 1;
+        f.bimg = ws + w.bimg;
         e = launch_fwd_tc(f);
-        if (e != cudaSuccess) return e;
-        e = launch_bwd_chain_tc(a, ws + w.fwd, p.dsend, a.stream);
-        if (e != cudaSuccess) return e;
-    }
-    if (a.io_bf16) {
-        if (a.dk == 128 && a.dv == 128) e = launch_t<__nv_bfloat16, 128, 128>(p, grid_nh, grid_items, tc, a.stream);
-        else if (a.dk == 128 && a.dv == 64) e = launch_t<__nv_bfloat16, 128, 64>(p, grid_nh, grid_items, tc, a.stream);
-        else if (a.dk == 64 && a.dv == 128) e = launch_t<__nv_bfloat16, 64, 128>(p, grid_nh, grid_items, tc, a.stream);
-        else e = launch_t<__nv_bfloat16, 64, 64>(p, grid_nh, grid_items, tc, a.stream);
+        if (e == cudaSuccess) e = launch_bwd_chain_tc(a, ws + w.fwd, ws + w.bimg, a.stream);
+        if (e == cudaSuccess)
+            e = launch_bwd_items_tc(a, ws + w.fwd, ws + w.bimg, ws + w.mid, p.dA_item, a.stream);
     } else {
-        if (a.dk == 128 && a.dv == 128) e = launch_t<float, 128, 128>(p, grid_nh, grid_items, false, a.stream);
-        else if (a.dk == 128 && a.dv == 64) e = launch_t<float, 128, 64>(p, grid_nh, grid_items, false, a.stream);
-        else if (a.dk == 64 && a.dv == 128) e = launch_t<float, 64, 128>(p, grid_nh, grid_items, false, a.stream);
-        else e = launch_t<float, 64, 64>(p, grid_nh, grid_items, false, a.stream);
+        if (a.dk == 128 && a.dv == 128) e = launch_t<float, 128, 128>(p, grid_nh, grid_items, a.stream);
+        else if (a.dk == 128 && a.dv == 64) e = launch_t<float, 128, 64>(p, grid_nh, grid_items, a.stream);
+        else if (a.dk == 64 && a.dv == 128) e = launch_t<float, 64, 128>(p, grid_nh, grid_items, a.stream);
+        else e = launch_t<float, 64, 64>(p, grid_nh, grid_items, a.stream);
     }
     if (e != cudaSuccess) return e;
     ProfScope prof("bwd_dA_kernel", a.stream);

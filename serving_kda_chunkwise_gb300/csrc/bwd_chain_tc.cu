@@ -12,14 +12,17 @@
 //
 // One CTA per (sequence, head) at a time, the gradient transposed in TMEM (lane j holds
 // column j of dS, i.e. row j of dS^T), as in the forward's chain stage (fwd_chain.cuh):
-//   MMA1  Z^T  = dS'^T [K~_hi; K~_lo]^T + dO^T [A_hi; A_lo]      (M = 128 value columns, N = 64)
+//   MMA1  Z^T  = dS'^T_hi [K~_hi; K~_lo]^T + dS'^T_lo K~_hi^T + dO^T [A_hi; A_lo]
+//                                                            (M = 128 value columns, N = 64)
 //   E1    -Z^T -> bf16 hi + lo into TMEM
 //   MMA2  D2   = dO^T (Gamma*Q) + (-Z)^T_hi W + (-Z)^T_lo W       (N = 128 key channels)
-//   E2    dS^T <- dS'^T Diag(gamma^C) + D2 in fp32 registers; bf16 copy into TMEM
-// Before each chunk the gradient at its end is written out (the per-chunk reverse kernel
-// starts from it), and after a sequence's first chunk the gradient of the initial state.
+//   E2    dS^T <- dS'^T Diag(gamma^C) + D2 in fp32 registers; bf16 hi + lo copy into TMEM
+// For the per-chunk kernels, each chunk's image block (bwd_tc_layout.cuh) receives dS_C^T (the
+// gradient at the chunk's end) and dVt^T as bf16 operand images; after a sequence's first
+// chunk the gradient of the initial state is written out in fp32.
 #include <cuda.h>
 
+#include "bwd_tc_layout.cuh"
 #include "fwd_tc_layout.cuh"
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -47,9 +50,9 @@ constexpr uint32_t kBars = 198656;
 constexpr uint32_t kSmem = kBars + 256 + 1024;
 static_assert(kSmem <= 232448, "gradient chain exceeds the shared-memory limit");
 
-// TMEM columns: dS^T bf16 [0, 64); -Z^T bf16 hi [64, 96), lo [96, 128); D1 (Z^T) [128, 192);
-// D2 [256, 384)
-constexpr uint32_t kTS = 0, kTZ = 64, kTZlo = 96, kTD1 = 128, kTD2 = 256, kTCols = 512;
+// TMEM columns: dS^T bf16 hi [0, 64); -Z^T bf16 hi [64, 96), lo [96, 128); D1 (Z^T) [128, 192);
+// dS^T bf16 lo [192, 256); D2 [256, 384)
+constexpr uint32_t kTS = 0, kTZ = 64, kTZlo = 96, kTD1 = 128, kTSlo = 192, kTD2 = 256, kTCols = 512;
 
 struct Params {
     CUtensorMap tdo;  // dO [T_total, H, dv] bf16, boxes of 64 columns x 1 head x 64 rows
@@ -58,7 +61,7 @@ struct Params {
     const int32_t* chunk_off;
     const int32_t* order;     // sequences, longest first
     const float* dS_out;      // [N][H][dk][dv] or nullptr
-    float* dsend;             // [chunks][H][dk][dv]: the gradient at each chunk end
+    uint8_t* bimg;            // image blocks [chunks][H]
     float* dS0;               // [N][H][dk][dv] or nullptr
     unsigned* err;
     int64_t T_total;
@@ -148,10 +151,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 //     + dO^T [A_hi; A_lo]      (K = 64 query tokens, A rows as MN-major B)
                 const uint64_t dKC = sdesc_sw128(sbase + kKC + st * 32768, 0, 1024);
 #pragma unroll
-                for (int ks = 0; ks < 16; ++ks) {
-                    const int part = ks >> 3, kk = ks & 7;  // part 0: K~ hi, 1: K~ lo
-                    mma_bf16_ts(d1, tmem + kTS + 8 * kk,
-                                dKC + ((part * 16384 + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+                for (int ks = 0; ks < 24; ++ks) {
+                    // part 0: dS hi x K~ hi, 1: dS hi x K~ lo, 2: dS lo x K~ hi
+                    const int part = ks >> 3, kk = ks & 7;
+                    mma_bf16_ts(d1, tmem + (part == 2 ? kTSlo : kTS) + 8 * kk,
+                                dKC + (((part == 1 ? 16384 : 0) + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
                                 id1s, ks > 0);
                 }
                 const uint64_t dDO = sdesc_sw128(sbase + kDO + st * 16384, 8192, 1024);
@@ -247,10 +251,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
 #pragma unroll
             for (int e = 0; e < 64; ++e) dS[e] = (p.dS_out && sv) ? p.dS_out[sbase_el + (size_t)e * p.dv] : 0.f;
             if (c.nch > 0) {
-                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) pk[e] = pack_bf16x2(dS[2 * e], dS[2 * e + 1]);
-                tmem_st32(tmem + lb + kTS + 32 * wg, pk);
+                for (int x = 0; x < 4; ++x) {
+                    uint32_t ph8[8], pl8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float a0 = dS[16 * x + 2 * e], a1 = dS[16 * x + 2 * e + 1];
+                        ph8[e] = pack_bf16x2(a0, a1);
+                        pl8[e] = pack_bf16x2(a0 - __uint_as_float(ph8[e] << 16),
+                                             a1 - __uint_as_float(ph8[e] & 0xffff0000u));
+                    }
+                    tmem_st8(tmem + lb + kTS + 32 * wg + 8 * x, ph8);
+                    tmem_st8(tmem + lb + kTSlo + 32 * wg + 8 * x, pl8);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -258,11 +271,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
             }
             for (int t = c.nch - 1; t >= 0; --t, ++g) {
                 const uint32_t st = g & 1, ph = (g >> 1) & 1;
-                // the gradient at this chunk's end, for the per-chunk reverse
-                if (sv) {
-                    float* dst = p.dsend + (((size_t)(c.c0 + t) * p.H + c.h) * p.dk + 64 * wg) * p.dv + j;
+                // the gradient at this chunk's end: row j of key-channel block wg of the dS_C^T
+                // image (bf16 hi + lo), the 64 channels in eight 16-byte chunks
+                uint8_t* blk = p.bimg + ((size_t)(c.c0 + t) * p.H + c.h) * kBiBytes;
+                {
+                    uint8_t* dst = blk + kBiDS + wg * 16384 + j * 128;
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) dst[(size_t)e * p.dv] = dS[e];
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float v8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v8[e] = dS[8 * c8 + e];
+                        uint4 hi, lo;
+                        pk8_hilo(v8, hi, lo);
+                        const uint32_t off = (uint32_t)((c8 ^ (j & 7)) << 4);
+                        *reinterpret_cast<uint4*>(dst + off) = hi;
+                        *reinterpret_cast<uint4*>(dst + 32768 + off) = lo;
+                    }
                 }
                 // ---- E1: -Z^T as bf16 hi + lo for tokens r = 32 wg + e
                 bool okc = mbar_wait_ab(&mma1[st], ph, p.err, abort);
@@ -272,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                     tmem_ld16(tmem + lb + kTD1 + 32 * wg, z0);
                     tmem_ld16(tmem + lb + kTD1 + 32 * wg + 16, z1);
                     tmem_ld_wait();
+                    uint8_t* zimg = blk + kBiDV + j * 128;  // dVt^T row j
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         uint32_t hi[8], lo[8];
@@ -285,6 +310,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                         }
                         tmem_st8(tmem + lb + kTZ + 16 * wg + 8 * hf, hi);
                         tmem_st8(tmem + lb + kTZlo + 16 * wg + 8 * hf, lo);
+                        // tokens 32 wg + 16 hf + 8 x (x = 0, 1) are chunk 4 wg + 2 hf + x of the
+                        // row; the image holds +Z, so hi and lo are the negated words
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const uint32_t off = (uint32_t)(((4 * wg + 2 * hf + x) ^ (j & 7)) << 4);
+                            constexpr uint32_t kSign = 0x80008000u;
+                            *reinterpret_cast<uint4*>(zimg + off) =
+                                make_uint4(hi[4 * x] ^ kSign, hi[4 * x + 1] ^ kSign, hi[4 * x + 2] ^ kSign,
+                                           hi[4 * x + 3] ^ kSign);
+                            *reinterpret_cast<uint4*>(zimg + 16384 + off) =
+                                make_uint4(lo[4 * x] ^ kSign, lo[4 * x + 1] ^ kSign, lo[4 * x + 2] ^ kSign,
+                                           lo[4 * x + 3] ^ kSign);
+                        }
                     }
                     tmem_st_wait();
                 }
@@ -308,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                         tmem_ld_wait();
 #pragma unroll
                         for (int qt = 0; qt < 2; ++qt) {
-                            uint32_t pk[8];
+                            uint32_t pk[8], pl[8];
 #pragma unroll
                             for (int e4 = 0; e4 < 4; ++e4) {
                                 const float4 g4 = gv[4 * qt + e4];
@@ -318,10 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                                 dS[e + 1] = fmaf(g4.y, dS[e + 1], dd[4 * e4 + 1]);
                                 dS[e + 2] = fmaf(g4.z, dS[e + 2], dd[4 * e4 + 2]);
                                 dS[e + 3] = fmaf(g4.w, dS[e + 3], dd[4 * e4 + 3]);
-                                pk[2 * e4] = pack_bf16x2(dS[e], dS[e + 1]);
-                                pk[2 * e4 + 1] = pack_bf16x2(dS[e + 2], dS[e + 3]);
+#pragma unroll
+                                for (int y = 0; y < 2; ++y) {
+                                    const float a0 = dS[e + 2 * y], a1 = dS[e + 2 * y + 1];
+                                    const uint32_t h = pack_bf16x2(a0, a1);
+                                    pk[2 * e4 + y] = h;
+                                    pl[2 * e4 + y] = pack_bf16x2(a0 - __uint_as_float(h << 16),
+                                                                 a1 - __uint_as_float(h & 0xffff0000u));
+                                }
                             }
                             tmem_st8(tmem + lb + kTS + 32 * wg + 16 * hf + 8 * qt, pk);
+                            tmem_st8(tmem + lb + kTSlo + 32 * wg + 16 * hf + 8 * qt, pl);
                         }
                     }
                     tmem_st_wait();
@@ -363,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
 }  // namespace bwdtc
 
 // The gradient chain on the tensor cores: reads the packages the forward's two-launch form
-// left in its workspace (fwd_ws) and writes dsend and dS0 in the backward's layout.
-cudaError_t launch_bwd_chain_tc(const BwdArgs& a, void* fwd_ws, float* dsend, cudaStream_t stream) {
+// left in its workspace (fwd_ws), writes dS_C and dVt into the image blocks and dS0.
+cudaError_t launch_bwd_chain_tc(const BwdArgs& a, void* fwd_ws, void* bimg, cudaStream_t stream) {
     using namespace bwdtc;
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
     const fwdtc::WsLayout L = fwdtc::ws_layout(a.T_total, a.N, a.H);
@@ -377,7 +422,7 @@ cudaError_t launch_bwd_chain_tc(const BwdArgs& a, void* fwd_ws, float* dsend, cu
     p.chunk_off = reinterpret_cast<const int32_t*>(ws + L.off_chunk_off);
     p.order = reinterpret_cast<const int32_t*>(ws + L.off_order);
     p.dS_out = a.dS_out;
-    p.dsend = dsend;
+    p.bimg = static_cast<uint8_t*>(bimg);
     p.dS0 = a.dS0;
     p.err = a.dev_err;
     p.T_total = a.T_total;

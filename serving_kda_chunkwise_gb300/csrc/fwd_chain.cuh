@@ -27,6 +27,7 @@
 
 #include <cuda.h>
 
+#include "bwd_tc_layout.cuh"
 #include "fwd_tc_layout.cuh"
 #include "kda_common.cuh"
 #include "tc_util.cuh"
@@ -92,10 +93,11 @@ struct ChainParams {
     // head sizes of q, k (dk) and v, o, S (dv), 64 or 128: a 64 is zero-padded to 128 inside
     // (the tensor maps read zeros past it), so only the state and output addresses use them
     int dk, dv;
-    // optional (nullptr otherwise): the state at every chunk start, fp32
-    // [chunks][H][dk][dv] with chunk = chunk_off[n] + t, for a backward pass; with o ==
-    // nullptr the output is not stored
-    float* ckpt;
+    // optional (nullptr otherwise), for a backward pass: the image blocks [chunks][H]
+    // (bwd_tc_layout.cuh), chunk = chunk_off[n] + t, receive S_0^T (the state at the chunk
+    // start) and Vt^T as bf16 hi + lo operand images; with o == nullptr the output is not
+    // stored
+    uint8_t* bimg;
     // fused kernel only (fused = 0 otherwise): CTA c serves chain c and reads chunk t from
     // ring slot c * ring_slots + t % ring_slots once ready[slot] >= t + 1; it raises
     // consumed[c] to t + 1 once every part of chunk t is in shared memory
@@ -366,14 +368,26 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             const size_t sbase_el = ((size_t)(c.n * p.H + c.h) * p.dk + 64 * wg) * p.dv + j;
 #pragma unroll
             for (int e = 0; e < 64; ++e) S[e] = (p.S0 && sv) ? p.S0[sbase_el + (size_t)e * p.dv] : 0.f;
-            // the state at the start of chunk t, for a backward pass (coalesced: for each row
-            // the 32 lanes of a warp write 128 contiguous bytes)
+            // the image block of chunk t (backward pass only)
+            auto bimg_of = [&](int t) -> uint8_t* {
+                return p.bimg + ((size_t)(__ldg(p.chunk_off + c.n) + t) * p.H + c.h) * bwdtc::kBiBytes;
+            };
+            // S_0^T of chunk t as bf16 hi + lo: row j of key-channel block wg, the 64 channels
+            // in eight 16-byte chunks (padding rows and columns are zeros)
             auto store_ckpt = [&](int t) {
-                if (!p.ckpt || !sv) return;
-                const int chunk = __ldg(p.chunk_off + c.n) + t;
-                float* dst = p.ckpt + (((size_t)chunk * p.H + c.h) * p.dk + 64 * wg) * p.dv + j;
+                if (!p.bimg) return;
+                uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + j * 128;
 #pragma unroll
-                for (int e = 0; e < 64; ++e) dst[(size_t)e * p.dv] = S[e];
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float v8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v8[e] = S[8 * c8 + e];
+                    uint4 hi, lo;
+                    pk8_hilo(v8, hi, lo);
+                    const uint32_t off = (uint32_t)((c8 ^ (j & 7)) << 4);
+                    *reinterpret_cast<uint4*>(dst + off) = hi;
+                    *reinterpret_cast<uint4*>(dst + 32768 + off) = lo;
+                }
             };
             if (c.nch > 0) {
                 store_ckpt(0);
@@ -411,6 +425,8 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                     tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg, x0);
                     tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg + 16, x1);
                     tmem_ld_wait();
+                    // backward pass: Vt^T row j, tokens 32 wg + 16 hf + 8 x in chunk 4 wg + 2 hf + x
+                    uint8_t* vimg = p.bimg ? bimg_of(t) + bwdtc::kBiV + j * 128 : nullptr;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         uint32_t hi[8], lo[8];
@@ -424,6 +440,16 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                         }
                         tmem_st8(tmem + lb + kTV + 16 * wg + 8 * hf, hi);
                         tmem_st8(tmem + lb + kTVlo + 16 * wg + 8 * hf, lo);
+                        if (vimg) {
+#pragma unroll
+                            for (int x = 0; x < 2; ++x) {
+                                const uint32_t off = (uint32_t)(((4 * wg + 2 * hf + x) ^ (j & 7)) << 4);
+                                *reinterpret_cast<uint4*>(vimg + off) =
+                                    make_uint4(hi[4 * x], hi[4 * x + 1], hi[4 * x + 2], hi[4 * x + 3]);
+                                *reinterpret_cast<uint4*>(vimg + 16384 + off) =
+                                    make_uint4(lo[4 * x], lo[4 * x + 1], lo[4 * x + 2], lo[4 * x + 3]);
+                            }
+                        }
                     }
                     tmem_st_wait();
                 }

@@ -16,6 +16,7 @@
 // every sub-tile pair.
 #pragma once
 
+#include "bwd_tc_layout.cuh"
 #include "fwd_tc_layout.cuh"
 #include "kda_common.cuh"
 #include "tc_util.cuh"
@@ -89,6 +90,9 @@ struct IntraParams {
     // fused kernel: items are taken from this counter in order (a CTA whose item waits for a
     // slot holds up no other chain's items); otherwise CTA b takes items b, b + ncta, ...
     int* item_ctr;
+    // two-launch form, optional (nullptr otherwise): the backward's image blocks
+    // [chunks][H] (bwd_tc_layout.cuh); item = chunk * H + h writes N = (I + L)^{-1} there
+    uint8_t* bimg;
 };
 
 // Shared-memory map of the intra kernel (offsets from a 1024-aligned base).  q and k are
@@ -146,12 +150,6 @@ __device__ __forceinline__ int stk_off_sp(int s) { return 8 * s * (s - 1); }
 // A_d, L_d (fp32 [4 sub-tiles][16][16] each); the 32 KB after the 96-row stack
 constexpr uint32_t kSpXch = kBStk + 24576;
 static_assert(kSpXch + 32768 <= kXch, "the mixed path's exchange must fit before rho");
-
-__device__ __forceinline__ float lg2f(float x) {
-    float y;
-    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 struct ItemInfo {
     int item;  // item index (>= the item count: no further item)
@@ -236,13 +234,6 @@ __device__ __forceinline__ void load_beta(const IntraParams& p, const ItemInfo& 
         dst[tid] = (tid < it.L) ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
 }
 
-// 2^x (the hardware approximation; results below 2^-126 flush to zero)
-__device__ __forceinline__ float ex2f(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // The gate in log2 units (G2 = G log2 e, so that every decay factor is one ex2).
 //   bounded:  g_min Sigmoid(e^{A_h} z) log2 e = gmin2 / (1 + 2^{-scale2 z}),
 //             scale2 = e^{A_h} log2 e, gmin2 = g_min log2 e;
@@ -256,34 +247,6 @@ __device__ __forceinline__ float gate2(float z, float scale2, float gmin2, float
         constexpr float kLog2e = 1.4426950408889634f;
         return -eA * fmaf(fmaxf(z, 0.f), kLog2e, lg2f(1.f + ex2f(-fabsf(z) * kLog2e)));
     }
-}
-
-// 8 consecutive bf16 of a swizzled tile <-> fp32 registers
-__device__ __forceinline__ void ld8(const uint8_t* p, float (&v)[8]) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-        v[2 * e] = f.x;
-        v[2 * e + 1] = f.y;
-    }
-}
-__device__ __forceinline__ uint4 pk8(const float (&v)[8]) {
-    return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                      pack_bf16x2(v[6], v[7]));
-}
-// hi = bf16(v), lo = bf16(v - hi)  (the fp32 value of a packed bf16 is its bits shifted up)
-__device__ __forceinline__ void pk8_hilo(const float (&v)[8], uint4& hi, uint4& lo) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        h[e] = pack_bf16x2(v[2 * e], v[2 * e + 1]);
-        l[e] = pack_bf16x2(v[2 * e] - __uint_as_float(h[e] << 16),
-                           v[2 * e + 1] - __uint_as_float(h[e] & 0xffff0000u));
-    }
-    hi = make_uint4(h[0], h[1], h[2], h[3]);
-    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // ---- 16x16 fp32 tiles on the legacy warp-level tensor-core path (mma.sync, tf32 inputs,
@@ -1134,6 +1097,17 @@ __device__ __forceinline__ void intra_body(const IntraParams& p, uint8_t* smem_r
             // 128-row operand [M; M] of the W / U MMA
             {
                 const int r = tid >> 2, cq = tid & 3;
+                if (p.bimg) {  // N = T (lower triangle) in fp32 for the backward
+                    float4* nd = reinterpret_cast<float4*>(
+                        p.bimg + (size_t)s_item[b].item * bwdtc::kBiBytes + bwdtc::kBiN + r * 256 + 64 * cq);
+#pragma unroll
+                    for (int e4 = 0; e4 < 4; ++e4) {
+                        const int c0 = 16 * cq + 4 * e4;
+                        const float* tr = sT + r * kLd + c0;
+                        nd[e4] = make_float4(c0 <= r ? tr[0] : 0.f, c0 + 1 <= r ? tr[1] : 0.f,
+                                             c0 + 2 <= r ? tr[2] : 0.f, c0 + 3 <= r ? tr[3] : 0.f);
+                    }
+                }
                 uint8_t* mt = sm + kMTile;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {

@@ -284,7 +284,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // The fused form needs equal sequence lengths (no cu_seqlens: the chunk-major item order
     // then follows every chain in step), at most kFusedMaxChains chains, and SMs left over
-    // for the intra stage, and keep_packages unset.  KDA_FWD_FUSED=0 in the environment
+    // for the intra stage, and no backward image blocks wanted.  KDA_FWD_FUSED=0 in the environment
     // selects the two-launch form.
     // The ring and its flags live in the workspace's package region, which holds
     // H * maxchunks >= C * nct packages: nct > ring_slots leaves room for both.
@@ -293,7 +293,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     int ring_slots = C > 0 ? (int)(kRingBytesMax / ((size_t)C * kPkgBytes)) : 0;
     ring_slots = ring_slots > kRingSlotsMax ? kRingSlotsMax : ring_slots;
     const char* fenv = getenv("KDA_FWD_FUSED");
-    const bool fused = !a.keep_packages && a.cu_seqlens == nullptr && a.T_total > 0 &&
+    const bool fused = !a.bimg && a.cu_seqlens == nullptr && a.T_total > 0 &&
                        C <= kFusedMaxChains && sms - C >= 16 && ring_slots >= kRingSlotsMin && nct_all > ring_slots &&
                        !(fenv && strcmp(fenv, "0") == 0);
     // fused: the ring [C][ring_slots] packages, then ready flags [C][ring_slots], consumed
@@ -331,6 +331,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     ip.N = a.N;
     ip.H = a.H;
     ip.maxchunks = maxchunks;
+    ip.bimg = static_cast<uint8_t*>(a.bimg);
     cp.pkg = pkg;
     cp.cu = a.cu_seqlens;
     cp.chunk_off = chunk_off;
@@ -344,7 +345,7 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
     cp.H = a.H;
     cp.dk = a.dk;
     cp.dv = a.dv;
-    cp.ckpt = a.ckpt;
+    cp.bimg = static_cast<uint8_t*>(a.bimg);
     cp.maxchunks = maxchunks;
 
     if (fused) {

@@ -27,12 +27,11 @@ struct FwdArgs {
     size_t ws_bytes;
     unsigned* dev_err;
     cudaStream_t stream;
-    // tensor-core path only, optional: the fp32 state at every chunk start,
-    // [chunks][H][dk][dv] in the order of the chunk offsets (for a backward pass)
-    float* ckpt;
-    // tensor-core path only: nonzero selects the two-launch form, which leaves every
-    // (chunk, head) package in the workspace (the backward's gradient chain reads them)
-    int keep_packages;
+    // tensor-core path only, for a backward pass (nullptr otherwise): the backward's image
+    // blocks [chunks][H] in the order of the chunk offsets (bwd_tc_layout.cuh), which
+    // receive S_0, Vt and N of every chunk; selects the two-launch form, which also leaves
+    // every (chunk, head) package in the workspace
+    void* bimg;
 };
 
 struct BwdArgs {
@@ -96,9 +95,15 @@ size_t fwd_tc_workspace_size(int64_t T_total, int N, int H);
 cudaError_t launch_fwd_tc(const FwdArgs& a);
 
 // The backward's gradient chain on tcgen05 tensor cores (bwd_chain_tc.cu), bf16 problems:
-// from the packages that launch_fwd_tc with keep_packages left in `fwd_ws`, the state's
-// gradient at every chunk end into dsend ([chunks][H][dk][dv] fp32) and a.dS0.
-cudaError_t launch_bwd_chain_tc(const BwdArgs& a, void* fwd_ws, float* dsend, cudaStream_t stream);
+// from the packages that launch_fwd_tc with bimg set left in `fwd_ws`, the state's gradient
+// at every chunk end and dVt into the image blocks `bimg`, and a.dS0.
+cudaError_t launch_bwd_chain_tc(const BwdArgs& a, void* fwd_ws, void* bimg, cudaStream_t stream);
+
+// The backward's per-chunk kernels on tcgen05 tensor cores (bwd_item_tc.cu), bf16 problems:
+// from the image blocks, every gradient but dS0, plus the [chunks][H] dA_log partials; `mid`
+// holds the mid blocks between its two kernels.
+cudaError_t launch_bwd_items_tc(const BwdArgs& a, void* fwd_ws, const void* bimg, void* mid,
+                                float* dA_item, cudaStream_t stream);
 
 // The argument checks of kda_fwd_chunked except those of the workspace (api.cu): KDA_OK, or
 // the failing status with the calling thread's last error set.
