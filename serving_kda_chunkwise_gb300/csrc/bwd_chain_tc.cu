@@ -277,15 +277,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 {
                     uint8_t* dst = blk + kBiDS + wg * 16384 + j * 128;
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        float v8[8];
+                    for (int c8 = 0; c8 < 8; c8 += 2) {
+                        float v0[8], v1[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v8[e] = dS[8 * c8 + e];
-                        uint4 hi, lo;
-                        pk8_hilo(v8, hi, lo);
-                        const uint32_t off = (uint32_t)((c8 ^ (j & 7)) << 4);
-                        *reinterpret_cast<uint4*>(dst + off) = hi;
-                        *reinterpret_cast<uint4*>(dst + 32768 + off) = lo;
+                        for (int e = 0; e < 8; ++e) {
+                            v0[e] = dS[8 * c8 + e];
+                            v1[e] = dS[8 * c8 + 8 + e];
+                        }
+                        uint4 h0, l0, h1, l1;
+                        pk8_hilo(v0, h0, l0);
+                        pk8_hilo(v1, h1, l1);
+                        st_swz_pair(dst, c8, j, h0, h1);
+                        st_swz_pair(dst + 32768, c8, j, l0, l1);
                     }
                 }
                 // ---- E1: -Z^T as bf16 hi + lo for tokens r = 32 wg + e
@@ -312,17 +315,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                         tmem_st8(tmem + lb + kTZlo + 16 * wg + 8 * hf, lo);
                         // tokens 32 wg + 16 hf + 8 x (x = 0, 1) are chunk 4 wg + 2 hf + x of the
                         // row; the image holds +Z, so hi and lo are the negated words
-#pragma unroll
-                        for (int x = 0; x < 2; ++x) {
-                            const uint32_t off = (uint32_t)(((4 * wg + 2 * hf + x) ^ (j & 7)) << 4);
-                            constexpr uint32_t kSign = 0x80008000u;
-                            *reinterpret_cast<uint4*>(zimg + off) =
-                                make_uint4(hi[4 * x] ^ kSign, hi[4 * x + 1] ^ kSign, hi[4 * x + 2] ^ kSign,
-                                           hi[4 * x + 3] ^ kSign);
-                            *reinterpret_cast<uint4*>(zimg + 16384 + off) =
-                                make_uint4(lo[4 * x] ^ kSign, lo[4 * x + 1] ^ kSign, lo[4 * x + 2] ^ kSign,
-                                           lo[4 * x + 3] ^ kSign);
-                        }
+                        constexpr uint32_t kSign = 0x80008000u;
+                        st_swz_pair(zimg, 4 * wg + 2 * hf, j,
+                                    make_uint4(hi[0] ^ kSign, hi[1] ^ kSign, hi[2] ^ kSign, hi[3] ^ kSign),
+                                    make_uint4(hi[4] ^ kSign, hi[5] ^ kSign, hi[6] ^ kSign, hi[7] ^ kSign));
+                        st_swz_pair(zimg + 16384, 4 * wg + 2 * hf, j,
+                                    make_uint4(lo[0] ^ kSign, lo[1] ^ kSign, lo[2] ^ kSign, lo[3] ^ kSign),
+                                    make_uint4(lo[4] ^ kSign, lo[5] ^ kSign, lo[6] ^ kSign, lo[7] ^ kSign));
                     }
                     tmem_st_wait();
                 }

@@ -33,8 +33,28 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 288;  // 8 compute warps, then the issuing thread (warp 8, lane 0)
-constexpr int kIss = 256;
+// Optional per-phase cycle counters (debug builds with -DKDA_PHASE_TIMING only): thread 0 and
+// the issuing thread of CTA 0 accumulate clock64() deltas between marked points.
+#ifdef KDA_PHASE_TIMING
+__device__ unsigned long long g_bwd_phase[32];
+#define BP_T0() long long bp_t = clock64()
+#define BP_MARK(i)                                                                          \
+    do {                                                                                    \
+        const long long bp_n = clock64();                                                   \
+        if (blockIdx.x == 0 && tid == 0)                                                    \
+            atomicAdd(&g_bwd_phase[(i)], (unsigned long long)(bp_n - bp_t));                 \
+        bp_t = bp_n;                                                                        \
+    } while (0)
+#else
+#define BP_T0() \
+    do {        \
+    } while (0)
+#define BP_MARK(i) \
+    do {           \
+    } while (0)
+#endif
+
+constexpr int kThreads = 256;  // 8 warps; thread 0 also issues every copy and MMA
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct ItemParams {
@@ -141,8 +161,9 @@ constexpr uint32_t kVI = 98304;      // Vt^T hi, lo (bulk)
 constexpr uint32_t kYI = 131072;     // z tile, then Y^T hi (rows j); batch 3: dS_C^T lo
 constexpr uint32_t kDVO = 147456;    // k tile, then Y^T lo (rows j); batch 3: dS_C^T lo
 constexpr uint32_t kDOt = 163840;    // dO tile; after batch 2: dM fp32 [64][64]
-constexpr uint32_t kRX = 180224;     // K+ (K-major rows s) + M (rows r); after batch 2: X0^T, N^T
-constexpr uint32_t kDVN = 212992;    // dV^T (one bf16, rows j)
+constexpr uint32_t kRX = 180224;     // K+ (K-major rows s) + M (rows r); after batch 1: dV^T
+                                     // (one bf16, rows j); after batch 2: X0^T, N^T fp32
+constexpr uint32_t kVt = 212992;     // v tile
 constexpr uint32_t kMisc = 229376;   // beta [64], tot [128], glast [128]
 constexpr uint32_t kSBars = kMisc + 1280;
 constexpr uint32_t kStateSmem = kSBars + 128 + 1024;
@@ -152,13 +173,15 @@ static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limi
 // batch 3 dS_C S_0^T [0, 128) (only its diagonal is read)
 constexpr uint32_t kTCols = 512;
 
+// The state kernel: one CTA of 256 threads per SM walks items (chunk, head); thread 0 also
+// issues every copy and MMA, each right after the barrier that makes its operands ready.
 __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_constant__ ItemParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const uint32_t sb = smem_u32(sm);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kSBars);
-    uint64_t* fullZK = bars + 0;
+    uint64_t* fullIn = bars + 0;  // z, k, v tiles
     uint64_t* fullS = bars + 1;
     uint64_t* fullV = bars + 2;
     uint64_t* fullDO = bars + 3;
@@ -166,11 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     uint64_t* mma1 = bars + 5;
     uint64_t* mma2 = bars + 6;
     uint64_t* mma3 = bars + 7;
-    uint64_t* ready1 = bars + 8;  // 8 arrivals: K+ and M built
-    uint64_t* ready2 = bars + 9;  // 8 arrivals: dV^T, Y^T images written, TMEM [0, 128) read
-    uint64_t* done = bars + 10;   // 8 arrivals: the item's shared memory is no longer read
-    uint64_t* drain = bars + 11;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+    uint64_t* drain = bars + 8;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
     float* sBeta = reinterpret_cast<float*>(sm + kMisc);
     float* sTot = sBeta + 64;
     float* sGlast = sTot + 128;
@@ -178,12 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     volatile int* abort = &s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool iss = tid == 0;
     if (tid == 0) {
-        for (int i = 0; i < 8; ++i) mbar_init(&bars[i], 1);
-        mbar_init(ready1, 8);
-        mbar_init(ready2, 8);
-        mbar_init(done, 8);
-        mbar_init(drain, 1);
+        for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -194,25 +211,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const int n_items = __ldg(p.chunk_off + p.N) * p.H;
 
-    uint32_t inflight = 0, inflight_ph = 0;  // issuing thread: copies of the current item
-    if (tid == kIss) {
-        // ------------------------------------------------------ issuing thread
-        constexpr uint32_t idV = idesc_bf16(128, 64, false, true);    // dVt^T x M
-        constexpr uint32_t idY = idesc_bf16(128, 64, false, false);   // S_0^T x K+^T
-        constexpr uint32_t idMN = idesc_bf16(128, 64, true, false);   // S_0 x dO^T, [Vt; Y] x dO^T
-        constexpr uint32_t idMM = idesc_bf16(128, 64, true, true);    // MN-major A and B, N = 64
-        constexpr uint32_t idD = idesc_bf16(128, 128, true, true);    // dS_C x S_0^T
-        uint32_t iter = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
-            const Item it = decode(p, item);
-            const uint32_t ph = iter & 1;
-            if (iter > 0 && !mbar_wait_ab(done, ph ^ 1, p.err, abort)) break;
-            const uint8_t* blk = p.bimg + (size_t)item * kBiBytes;
-            inflight = 0xfu;  // fullZK, fullS, fullV, fullDO
+    constexpr uint32_t idV = idesc_bf16(128, 64, false, true);    // dVt^T x M
+    constexpr uint32_t idY = idesc_bf16(128, 64, false, false);   // S_0^T x K+^T
+    constexpr uint32_t idMN = idesc_bf16(128, 64, true, false);   // S_0 x dO^T, [Vt; Y] x dO^T
+    constexpr uint32_t idMM = idesc_bf16(128, 64, true, true);    // MN-major A and B, N = 64
+    constexpr uint32_t idD = idesc_bf16(128, 128, true, true);    // dS_C x S_0^T
+
+    const int wq = warp & 3, wh = warp >> 2;
+    const int ch = 32 * wq + lane;  // TMEM lane: a key or value channel (or a token s)
+    const uint32_t lb = static_cast<uint32_t>(32 * wq) << 16;
+    uint32_t inflight = 0, inflight_ph = 0;  // thread 0: copies of the current item
+    bool ok = true;
+    uint32_t iter = 0;
+    BP_T0();
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
+        const Item it = decode(p, item);
+        const uint32_t ph = iter & 1;
+        const uint8_t* blk = p.bimg + (size_t)item * kBiBytes;
+        if (iss) {
+            inflight = 0xfu;  // fullIn, fullS, fullV, fullDO
             inflight_ph = ph;
-            mbar_expect_tx(fullZK, 32768);
-            load_tile(&p.tz, sm + kYI, it, fullZK);
-            load_tile(&p.tk, sm + kDVO, it, fullZK);
+            mbar_expect_tx(fullIn, 49152);
+            load_tile(&p.tz, sm + kYI, it, fullIn);
+            load_tile(&p.tk, sm + kDVO, it, fullIn);
+            load_tile(&p.tv, sm + kVt, it, fullIn);
             mbar_expect_tx(fullS, 65536);
             bulk_g2s(sm + kSI, blk + kBiS, 65536, fullS);
             mbar_expect_tx(fullV, 65536);
@@ -220,55 +242,151 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
             bulk_g2s(sm + kVI, blk + kBiV, 32768, fullV);
             mbar_expect_tx(fullDO, 16384);
             load_tile(&p.tdo, sm + kDOt, it, fullDO);
-            if (!mbar_wait_ab(ready1, ph, p.err, abort) || !mbar_wait_ab(fullS, ph, p.err, abort) ||
-                !mbar_wait_ab(fullV, ph, p.err, abort) || !mbar_wait_ab(fullDO, ph, p.err, abort))
-                break;
-            tc_fence_after();
-            // batch 1 ---------------------------------------------------------------
-            // dV^T = dVt^T M: A = dVt^T rows j hi, lo (K = 64 tokens, K-major), B = M rows r
-            // (MN-major)
-            {
-                const uint64_t dM = sdesc_sw128(sb + kRX + 16384, 8192, 1024);
+            const int nx = item + gridDim.x;  // the next item's inputs into L2
+            if (nx < n_items) {
+                const Item in = decode(p, nx);
+                l2_prefetch(p.bimg + (size_t)nx * kBiBytes, kBiBytes);
+                for (int b = 0; b < 2; ++b) {
+                    tma_prefetch_3d(&p.tz, 64 * b, in.h, (int)in.t0);
+                    tma_prefetch_3d(&p.tk, 64 * b, in.h, (int)in.t0);
+                    tma_prefetch_3d(&p.tv, 64 * b, in.h, (int)in.t0);
+                    tma_prefetch_3d(&p.tdo, 64 * b, in.h, (int)in.t0);
+                }
+            }
+        }
+        const float eA = expf(__ldg(p.A_log + it.h));
+        const float scale2 = eA * kLog2e, gmin2 = p.g_min * kLog2e;
+        uint8_t* mid = p.mid + (size_t)item * kMdBytes;
+        const float* Ng = reinterpret_cast<const float*>(blk + kBiN);
+        if (tid < 64)
+            sBeta[tid] = tid < it.L ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
+        ok = ok && mbar_wait_ab(fullIn, ph, p.err, abort);
+        BP_MARK(0);
+        float G2[32];
+        if (ok) {
+            gate_scan(sm + kYI, ch, wh, it.L, scale2, gmin2, sTot, G2);
+            if (wh == 1) sGlast[ch] = G2[31];
+            // K+ = Gamma*K, rows s of this half (K-major [2 blocks][64 rows][128 B])
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                const int s = 32 * wh + e;
+                const float kv = s < it.L ? ldbf(sm + kDVO + swz2(s, ch, 64)) : 0.f;
+                *reinterpret_cast<uint16_t*>(sm + kRX + swz2(s, ch, 64)) = bfbits(ex2f(G2[e]) * kv);
+            }
+            // M = N Diag(beta): row r, 16 columns per thread (MN-major rows r); N from global
+            const int r = tid >> 2, cq = tid & 3;
+            const float4* nr = reinterpret_cast<const float4*>(Ng + r * 64 + 16 * cq);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float4 n0 = __ldg(nr + 2 * hf), n1 = __ldg(nr + 2 * hf + 1);
+                const float* b = sBeta + 16 * cq + 8 * hf;
+                const float v8[8] = {n0.x * b[0], n0.y * b[1], n0.z * b[2], n0.w * b[3],
+                                     n1.x * b[4], n1.y * b[5], n1.z * b[6], n1.w * b[7]};
+                *reinterpret_cast<uint4*>(sm + kRX + 16384 + r * 128 + (((2 * cq + hf) ^ (r & 7)) << 4)) = pk8(v8);
+            }
+        } else {
+            csync();  // the gate scan's barrier
+        }
+        fence_async_smem();
+        ok = csync_and(ok);
+        BP_MARK(1);
+        if (iss && ok) {
+            ok = mbar_wait_ab(fullS, ph, p.err, abort) && mbar_wait_ab(fullV, ph, p.err, abort) &&
+                 mbar_wait_ab(fullDO, ph, p.err, abort);
+            if (ok) {
+                tc_fence_after();
+                // batch 1 -----------------------------------------------------------
+                // dV^T = dVt^T M: A = dVt^T rows j hi, lo (K = 64 tokens, K-major), B = M rows r
+                // (MN-major)
+                const uint64_t dMd = sdesc_sw128(sb + kRX + 16384, 8192, 1024);
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     const uint64_t dA = sdesc_sw128(sb + kDVI + 16384 * x, 0, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + 0, dA + ((kk * 32) >> 4), dM + ((kk * 2048) >> 4), idV,
+                        mma_bf16(tmem + 0, dA + ((kk * 32) >> 4), dMd + ((kk * 2048) >> 4), idV,
                                  (x | kk) != 0);
                 }
-            }
-            // (K+ S_0)^T = S_0^T K+^T: A = S_0^T hi rows j (K = 128 key channels, K-major),
-            // B = K+ rows s (K-major)
-            {
-                const uint64_t dA = sdesc_sw128(sb + kSI, 0, 1024);
-                const uint64_t dB = sdesc_sw128(sb + kRX, 0, 1024);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + 64, dA + ((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
-                             dB + ((((kk >> 2) * 8192) + (kk & 3) * 32) >> 4), idY, kk > 0);
-            }
-            // S_0 dO^T: A = S_0 hi, lo (M = key channels, MN-major rows j), B = dO rows r
-            // (K-major; K = 128 value channels)
-            {
-                const uint64_t dB = sdesc_sw128(sb + kDOt, 0, 1024);
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const uint64_t dA = sdesc_sw128(sb + kSI + 32768 * x, 16384, 1024);
+                // (K+ S_0)^T = S_0^T K+^T: A = S_0^T hi rows j (K = 128 key channels, K-major),
+                // B = K+ rows s (K-major)
+                {
+                    const uint64_t dA = sdesc_sw128(sb + kSI, 0, 1024);
+                    const uint64_t dB = sdesc_sw128(sb + kRX, 0, 1024);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16(tmem + 128, dA + ((kk * 2048) >> 4),
-                                 dB + ((((kk >> 2) * 8192) + (kk & 3) * 32) >> 4), idMN,
-                                 (x | kk) != 0);
+                        mma_bf16(tmem + 64, dA + ((((kk >> 2) * 16384) + (kk & 3) * 32) >> 4),
+                                 dB + ((((kk >> 2) * 8192) + (kk & 3) * 32) >> 4), idY, kk > 0);
                 }
+                // S_0 dO^T: A = S_0 hi, lo (M = key channels, MN-major rows j), B = dO rows r
+                // (K-major; K = 128 value channels)
+                {
+                    const uint64_t dB = sdesc_sw128(sb + kDOt, 0, 1024);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const uint64_t dA = sdesc_sw128(sb + kSI + 32768 * x, 16384, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16(tmem + 128, dA + ((kk * 2048) >> 4),
+                                     dB + ((((kk >> 2) * 8192) + (kk & 3) * 32) >> 4), idMN,
+                                     (x | kk) != 0);
+                    }
+                }
+                mma_commit(mma1);
             }
-            mma_commit(mma1);
-            if (!mbar_wait_ab(ready2, ph, p.err, abort)) break;
+        }
+        // ---- epilogue 1
+        ok = ok && mbar_wait_ab(mma1, ph, p.err, abort);
+        BP_MARK(2);
+        if (ok) {
+            tc_fence_after();
+            // dV^T and Y^T: lane = value channel j, columns s of this half
+            const int j = ch;
+            float a0[16], a1[16], y0[16], y1[16];
+            tmem_ld16(tmem + lb + 0 + 32 * wh, a0);
+            tmem_ld16(tmem + lb + 16 + 32 * wh, a1);
+            tmem_ld16(tmem + lb + 64 + 32 * wh, y0);
+            tmem_ld16(tmem + lb + 80 + 32 * wh, y1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                float dv8[8], y8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int u = 8 * x + e;  // token s = 32 wh + u
+                    const int s = 32 * wh + u;
+                    const float vv = s < it.L ? ldbf(sm + kVt + swz2(s, j, 64)) : 0.f;
+                    dv8[e] = u < 16 ? a0[u] : a1[u - 16];
+                    y8[e] = vv - (u < 16 ? y0[u] : y1[u - 16]);
+                    if (s < it.L && j < p.dv)
+                        p.dvg[((size_t)(it.t0 + s) * p.H + it.h) * p.dv + j] = __float2bfloat16_rn(dv8[e]);
+                }
+                const uint32_t off = (uint32_t)(j * 128 + (((4 * wh + x) ^ (j & 7)) << 4));
+                *reinterpret_cast<uint4*>(sm + kRX + off) = pk8(dv8);
+                uint4 yh, yl;
+                pk8_hilo(y8, yh, yl);
+                *reinterpret_cast<uint4*>(sm + kYI + off) = yh;
+                *reinterpret_cast<uint4*>(sm + kDVO + off) = yl;
+            }
+            // pQ = Gamma*(S_0 dO^T): lane = key channel i, columns r of this half
+            float q0[16], q1[16];
+            tmem_ld16(tmem + lb + 128 + 32 * wh, q0);
+            tmem_ld16(tmem + lb + 144 + 32 * wh, q1);
+            tmem_ld_wait();
+            float* pq = reinterpret_cast<float*>(mid + kMdQ) + ch;
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                pq[(32 * wh + u) * 128] = ex2f(G2[u]) * (u < 16 ? q0[u] : q1[u - 16]);
+        }
+        tc_fence_before();
+        fence_async_smem();
+        ok = csync_and(ok);
+        BP_MARK(3);
+        if (iss && ok) {
             tc_fence_after();
             // batch 2 ---------------------------------------------------------------
             // S_0 dV^T: A = S_0 hi, lo (MN-major), B = dV^T rows j (MN-major, N = 64 tokens)
             {
-                const uint64_t dB = sdesc_sw128(sb + kDVN, 8192, 1024);
+                const uint64_t dB = sdesc_sw128(sb + kRX, 8192, 1024);
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
                     const uint64_t dA = sdesc_sw128(sb + kSI + 32768 * x, 16384, 1024);
@@ -304,292 +422,225 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                              (x | kk) != 0);
             }
             mma_commit(mma2);
-            // dVt and Y are consumed once batch 2 completes: dS_C^T hi, lo into their place
-            if (!mbar_wait_ab(mma2, ph, p.err, abort)) break;
+        }
+        // ---- epilogue 2
+        ok = ok && mbar_wait_ab(mma2, ph, p.err, abort);
+        BP_MARK(4);
+        if (iss && ok) {
+            // dVt and Y are consumed: dS_C^T hi, lo into their place
             inflight |= 0x10u;
             mbar_expect_tx(fullDS, 65536);
             bulk_g2s(sm + kDVI, blk + kBiDS, 32768, fullDS);
             bulk_g2s(sm + kYI, blk + kBiDS + 32768, 32768, fullDS);
-            if (!mbar_wait_ab(fullDS, ph, p.err, abort)) break;
-            // batch 3 ---------------------------------------------------------------
-            // dS_C Vt^T: A = dS_C (MN-major rows j), B = Vt^T rows j (MN-major); hi x hi,
-            // hi x lo, lo x hi
-#pragma unroll
-            for (int x = 0; x < 3; ++x) {
-                const uint64_t dA = sdesc_sw128(sb + (x == 2 ? kYI : kDVI), 16384, 1024);
-                const uint64_t dB = sdesc_sw128(sb + kVI + (x == 1 ? 16384 : 0), 8192, 1024);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + 384, dA + ((kk * 2048) >> 4), dB + ((kk * 2048) >> 4), idMM,
-                             (x | kk) != 0);
-            }
-            // dS_C S_0^T (N = 128 key channels; the diagonal is rs): B = S_0^T rows j, MN-major
-#pragma unroll
-            for (int x = 0; x < 3; ++x) {
-                const uint64_t dA = sdesc_sw128(sb + (x == 2 ? kYI : kDVI), 16384, 1024);
-                const uint64_t dB = sdesc_sw128(sb + kSI + (x == 1 ? 32768 : 0), 16384, 1024);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + 0, dA + ((kk * 2048) >> 4), dB + ((kk * 2048) >> 4), idD,
-                             (x | kk) != 0);
-            }
-            mma_commit(mma3);
         }
-    }
-
-    if (warp < 8) {
-        // ------------------------------------------------------- compute warps
-        const int wq = warp & 3, wh = warp >> 2;
-        const int ch = 32 * wq + lane;  // TMEM lane: a key or value channel (or a token s)
-        const uint32_t lb = static_cast<uint32_t>(32 * wq) << 16;
-        uint32_t iter = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
-            const Item it = decode(p, item);
-            const uint32_t ph = iter & 1;
-            const float eA = expf(__ldg(p.A_log + it.h));
-            const float scale2 = eA * kLog2e, gmin2 = p.g_min * kLog2e;
-            uint8_t* mid = p.mid + (size_t)item * kMdBytes;
-            const float* Ng = reinterpret_cast<const float*>(p.bimg + (size_t)item * kBiBytes + kBiN);
-            if (tid < 64)
-                sBeta[tid] = tid < it.L ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
-            bool ok = mbar_wait_ab(fullZK, ph, p.err, abort);
-            float G2[32];
-            if (ok) {
-                gate_scan(sm + kYI, ch, wh, it.L, scale2, gmin2, sTot, G2);
-                if (wh == 1) sGlast[ch] = G2[31];
-                // K+ = Gamma*K, rows s of this half (K-major [2 blocks][64 rows][128 B])
+        if (ok) {
+            tc_fence_after();
+            // pP = -Gamma*(S_0 dV^T): lane = key channel
+            float* pp = reinterpret_cast<float*>(mid + kMdP) + ch;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int s = 32 * wh + e;
-                    const float kv = s < it.L ? ldbf(sm + kDVO + swz2(s, ch, 64)) : 0.f;
-                    *reinterpret_cast<uint16_t*>(sm + kRX + swz2(s, ch, 64)) = bfbits(ex2f(G2[e]) * kv);
-                }
-                // M = N Diag(beta): row r, 16 columns per thread (MN-major rows r); N from global
-                const int r = tid >> 2, cq = tid & 3;
-                const float4* nr = reinterpret_cast<const float4*>(Ng + r * 64 + 16 * cq);
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const float4 n0 = __ldg(nr + 2 * hf), n1 = __ldg(nr + 2 * hf + 1);
-                    const float* b = sBeta + 16 * cq + 8 * hf;
-                    const float v8[8] = {n0.x * b[0], n0.y * b[1], n0.z * b[2], n0.w * b[3],
-                                         n1.x * b[4], n1.y * b[5], n1.z * b[6], n1.w * b[7]};
-                    *reinterpret_cast<uint4*>(sm + kRX + 16384 + r * 128 + (((2 * cq + hf) ^ (r & 7)) << 4)) = pk8(v8);
-                }
-            } else {
-                csync();  // the gate scan's barrier
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ready1);
-            // ---- epilogue 1
-            ok = ok && mbar_wait_ab(mma1, ph, p.err, abort);
-            if (ok) {
-                tc_fence_after();
-                // dV^T and Y^T: lane = value channel j, columns s of this half
-                const int j = ch;
-                float a0[16], a1[16], y0[16], y1[16];
-                tmem_ld16(tmem + lb + 0 + 32 * wh, a0);
-                tmem_ld16(tmem + lb + 16 + 32 * wh, a1);
-                tmem_ld16(tmem + lb + 64 + 32 * wh, y0);
-                tmem_ld16(tmem + lb + 80 + 32 * wh, y1);
+            for (int hf = 0; hf < 2; ++hf) {
+                float b16[16];
+                tmem_ld16(tmem + lb + 192 + 32 * wh + 16 * hf, b16);
                 tmem_ld_wait();
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    float dv8[8], y8[8];
+                for (int e = 0; e < 16; ++e) {
+                    const int u = 16 * hf + e;
+                    pp[(32 * wh + u) * 128] = -ex2f(G2[u]) * b16[e];
+                }
+            }
+            if (wq < 2) {
+                // dA^T (lane s): row s of the dA image, columns c = 63 - r (hi, lo)
+                const int s = ch;
+                float d0[16], d1[16];
+                tmem_ld16(tmem + lb + 256 + 32 * wh, d0);
+                tmem_ld16(tmem + lb + 272 + 32 * wh, d1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float v8[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int u = 8 * x + e;  // token s = 32 wh + u
-                        const int s = 32 * wh + u;
-                        dv8[e] = u < 16 ? a0[u] : a1[u - 16];
-                        const float vv = (s < it.L && j < p.dv)
-                                             ? __bfloat162float(p.v[((size_t)(it.t0 + s) * p.H + it.h) * p.dv + j])
-                                             : 0.f;
-                        y8[e] = vv - (u < 16 ? y0[u] : y1[u - 16]);
-                        if (s < it.L && j < p.dv)
-                            p.dvg[((size_t)(it.t0 + s) * p.H + it.h) * p.dv + j] = __float2bfloat16_rn(dv8[e]);
+                        const int u = 31 - 8 * k - e;  // r = 32 wh + u
+                        const int r = 32 * wh + u;
+                        const float d = u < 16 ? d0[u] : d1[u - 16];
+                        v8[e] = (r >= s && r < it.L) ? d : 0.f;
                     }
-                    const uint32_t off = (uint32_t)(j * 128 + (((4 * wh + x) ^ (j & 7)) << 4));
-                    *reinterpret_cast<uint4*>(sm + kDVN + off) = pk8(dv8);
-                    uint4 yh, yl;
-                    pk8_hilo(y8, yh, yl);
-                    *reinterpret_cast<uint4*>(sm + kYI + off) = yh;
-                    *reinterpret_cast<uint4*>(sm + kDVO + off) = yl;
-                }
-                // pQ = Gamma*(S_0 dO^T): lane = key channel i, columns r of this half
-                float q0[16], q1[16];
-                tmem_ld16(tmem + lb + 128 + 32 * wh, q0);
-                tmem_ld16(tmem + lb + 144 + 32 * wh, q1);
-                tmem_ld_wait();
-                float* pq = reinterpret_cast<float*>(mid + kMdQ) + ch;
-#pragma unroll
-                for (int u = 0; u < 32; ++u)
-                    pq[(32 * wh + u) * 128] = ex2f(G2[u]) * (u < 16 ? q0[u] : q1[u - 16]);
-            }
-            tc_fence_before();
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ready2);
-            // ---- epilogue 2
-            ok = ok && mbar_wait_ab(mma2, ph, p.err, abort);
-            if (ok) {
-                tc_fence_after();
-                // pP = -Gamma*(S_0 dV^T): lane = key channel
-                float* pp = reinterpret_cast<float*>(mid + kMdP) + ch;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float b16[16];
-                    tmem_ld16(tmem + lb + 192 + 32 * wh + 16 * hf, b16);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int u = 16 * hf + e;
-                        pp[(32 * wh + u) * 128] = -ex2f(G2[u]) * b16[e];
-                    }
-                }
-                if (wq < 2) {
-                    // dA^T (lane s): row s of the dA image, columns c = 63 - r (hi, lo)
-                    const int s = ch;
-                    float d0[16], d1[16];
-                    tmem_ld16(tmem + lb + 256 + 32 * wh, d0);
-                    tmem_ld16(tmem + lb + 272 + 32 * wh, d1);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float v8[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int u = 31 - 8 * k - e;  // r = 32 wh + u
-                            const int r = 32 * wh + u;
-                            const float d = u < 16 ? d0[u] : d1[u - 16];
-                            v8[e] = (r >= s && r < it.L) ? d : 0.f;
-                        }
-                        uint4 hi, lo;
-                        pk8_hilo(v8, hi, lo);
-                        const uint32_t off = (uint32_t)(s * 128 + (((4 - 4 * wh + k) ^ (s & 7)) << 4));
-                        *reinterpret_cast<uint4*>(mid + kMdA + off) = hi;
-                        *reinterpret_cast<uint4*>(mid + kMdA + 8192 + off) = lo;
-                    }
-                } else {
-                    // dM^T (lane 64 + s): dM[r][s] into the fp32 scratch (rows r)
-                    const int s = ch - 64;
-                    float d0[16], d1[16];
-                    tmem_ld16(tmem + lb + 320 + 32 * wh, d0);
-                    tmem_ld16(tmem + lb + 336 + 32 * wh, d1);
-                    tmem_ld_wait();
-                    float* dm = reinterpret_cast<float*>(sm + kDOt);
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) dm[(32 * wh + u) * 64 + s] = u < 16 ? d0[u] : d1[u - 16];
-                }
-            }
-            tc_fence_before();
-            ok = csync_and(ok);
-            // ---- the solve's reverse, fp32 on CUDA cores (while batch 3 runs): X0 = N^T dM,
-            //      dbeta1 = diag X0, dL = -StrictTril(X0 M^T), M = N Diag(beta)
-            if (ok) {
-                float* NT = reinterpret_cast<float*>(sm + kRX + 16384);
-                for (int x = tid; x < 4096; x += 256) NT[(x & 63) * 64 + (x >> 6)] = __ldg(Ng + x);
-                const float* dm = reinterpret_cast<const float*>(sm + kDOt);
-                float* X0T = reinterpret_cast<float*>(sm + kRX);
-                const int a0 = 4 * (tid >> 4), s0 = 4 * (tid & 15);
-                float acc[4][4] = {};
-                for (int r = a0; r < 64; ++r) {  // N[r][a] = 0 for r < a
-                    const float4 n4 = __ldg(reinterpret_cast<const float4*>(Ng + r * 64 + a0));
-                    const float4 m4 = *reinterpret_cast<const float4*>(dm + r * 64 + s0);
-                    const float nv[4] = {n4.x, n4.y, n4.z, n4.w}, mv[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-#pragma unroll
-                        for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(nv[x], mv[y], acc[x][y]);
-                }
-#pragma unroll
-                for (int y = 0; y < 4; ++y)
-                    *reinterpret_cast<float4*>(X0T + (s0 + y) * 64 + a0) =
-                        make_float4(acc[0][y], acc[1][y], acc[2][y], acc[3][y]);
-                if (a0 == s0) {
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) reinterpret_cast<float*>(mid + kMdB)[a0 + x] = acc[x][x];
-                }
-                csync();
-                // dL[r][i] for r in [r0, r0 + 4), i in [i0, i0 + 4): -sum_{s <= i} X0[r][s] N[i][s] beta_s
-                const int r0 = 4 * (tid >> 4), i0 = 4 * (tid & 15);
-                float dl[4][4] = {};
-                for (int s = 0; s <= i0 + 3; ++s) {
-                    const float4 x4 = *reinterpret_cast<const float4*>(X0T + s * 64 + r0);
-                    const float4 n4 = *reinterpret_cast<const float4*>(NT + s * 64 + i0);
-                    const float bs = sBeta[s];
-                    const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
-                    const float nv[4] = {n4.x * bs, n4.y * bs, n4.z * bs, n4.w * bs};
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-#pragma unroll
-                        for (int y = 0; y < 4; ++y) dl[x][y] = fmaf(xv[x], nv[y], dl[x][y]);
-                }
-                // dL image: row i, columns c = 63 - r (the four columns 60 - r0 .. 63 - r0 hold
-                // rows r0 + 3 .. r0), hi and lo
-#pragma unroll
-                for (int y = 0; y < 4; ++y) {
-                    const int i = i0 + y;
-                    float v4[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int r = r0 + 3 - x;
-                        v4[x] = (i < r && r < it.L) ? -dl[3 - x][y] : 0.f;
-                    }
-                    uint32_t h2[2], l2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        h2[e] = pack_bf16x2(v4[2 * e], v4[2 * e + 1]);
-                        l2[e] = pack_bf16x2(v4[2 * e] - __uint_as_float(h2[e] << 16),
-                                            v4[2 * e + 1] - __uint_as_float(h2[e] & 0xffff0000u));
-                    }
-                    const uint32_t off = swz(i, 60 - r0);
-                    *reinterpret_cast<uint2*>(mid + kMdL + off) = make_uint2(h2[0], h2[1]);
-                    *reinterpret_cast<uint2*>(mid + kMdL + 8192 + off) = make_uint2(l2[0], l2[1]);
+                    uint4 hi, lo;
+                    pk8_hilo(v8, hi, lo);
+                    const uint32_t off = (uint32_t)(s * 128 + (((4 - 4 * wh + k) ^ (s & 7)) << 4));
+                    *reinterpret_cast<uint4*>(mid + kMdA + off) = hi;
+                    *reinterpret_cast<uint4*>(mid + kMdA + 8192 + off) = lo;
                 }
             } else {
-                csync();
+                // dM^T (lane 64 + s): dM[r][s] into the fp32 scratch (rows r)
+                const int s = ch - 64;
+                float d0[16], d1[16];
+                tmem_ld16(tmem + lb + 320 + 32 * wh, d0);
+                tmem_ld16(tmem + lb + 336 + 32 * wh, d1);
+                tmem_ld_wait();
+                float* dm = reinterpret_cast<float*>(sm + kDOt);
+#pragma unroll
+                for (int u = 0; u < 32; ++u) dm[(32 * wh + u) * 64 + s] = u < 16 ? d0[u] : d1[u - 16];
             }
-            // ---- epilogue 3: pE = (gamma^C/Gamma)*(dS_C Vt^T) and rs = diag(dS_C S_0^T)
-            ok = ok && mbar_wait_ab(mma3, ph, p.err, abort);
+        }
+        tc_fence_before();
+        ok = csync_and(ok);
+        BP_MARK(5);
+        if (iss && ok) {
+            ok = mbar_wait_ab(fullDS, ph, p.err, abort);
             if (ok) {
                 tc_fence_after();
-                const float gl = sGlast[ch];
-                float* pe = reinterpret_cast<float*>(mid + kMdE) + ch;
+                // batch 3 -----------------------------------------------------------
+                // dS_C Vt^T: A = dS_C (MN-major rows j), B = Vt^T rows j (MN-major); hi x hi,
+                // hi x lo, lo x hi
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    float c16[16];
-                    tmem_ld16(tmem + lb + 384 + 32 * wh + 16 * hf, c16);
-                    tmem_ld_wait();
+                for (int x = 0; x < 3; ++x) {
+                    const uint64_t dA = sdesc_sw128(sb + (x == 2 ? kYI : kDVI), 16384, 1024);
+                    const uint64_t dB = sdesc_sw128(sb + kVI + (x == 1 ? 16384 : 0), 8192, 1024);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int u = 16 * hf + e;
-                        pe[(32 * wh + u) * 128] = ex2f(gl - G2[u]) * c16[e];
-                    }
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tmem + 384, dA + ((kk * 2048) >> 4), dB + ((kk * 2048) >> 4), idMM,
+                                 (x | kk) != 0);
                 }
-                if (wh == 0) {  // lane i reads column i of its warp's 32 columns
-                    float d0[16], d1[16];
-                    tmem_ld16(tmem + lb + 32 * wq, d0);
-                    tmem_ld16(tmem + lb + 32 * wq + 16, d1);
-                    tmem_ld_wait();
-                    float rs = 0.f;
+                // dS_C S_0^T (N = 128 key channels; its diagonal is rs): B = S_0^T rows j, MN-major
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        rs = (lane == e) ? d0[e] : rs;
-                        rs = (lane == 16 + e) ? d1[e] : rs;
-                    }
-                    reinterpret_cast<float*>(mid + kMdRs)[ch] = rs;
+                for (int x = 0; x < 3; ++x) {
+                    const uint64_t dA = sdesc_sw128(sb + (x == 2 ? kYI : kDVI), 16384, 1024);
+                    const uint64_t dB = sdesc_sw128(sb + kSI + (x == 1 ? 32768 : 0), 16384, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16(tmem + 0, dA + ((kk * 2048) >> 4), dB + ((kk * 2048) >> 4), idD,
+                                 (x | kk) != 0);
+                }
+                mma_commit(mma3);
+            }
+        }
+        // ---- the solve's reverse, fp32 on CUDA cores (while batch 3 runs): X0 = N^T dM,
+        //      dbeta1 = diag X0, dL = -StrictTril(X0 M^T), M = N Diag(beta)
+        float* NT = reinterpret_cast<float*>(sm + kRX + 16384);  // N^T (dV^T is consumed)
+        float* X0T = reinterpret_cast<float*>(sm + kRX);
+        if (ok) {  // N^T: thread (row r, 16 columns), conflict-free stores down the columns
+            const int r = tid & 63, cb = tid >> 6;
+            const float4* nr = reinterpret_cast<const float4*>(Ng + r * 64 + 16 * cb);
+            float4 n4[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) n4[x] = __ldg(nr + x);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int c = 16 * cb + 4 * x;
+                NT[c * 64 + r] = n4[x].x;
+                NT[(c + 1) * 64 + r] = n4[x].y;
+                NT[(c + 2) * 64 + r] = n4[x].z;
+                NT[(c + 3) * 64 + r] = n4[x].w;
+            }
+        }
+        csync();
+        const int a0 = 4 * (tid >> 4), s0 = 4 * (tid & 15);
+        if (ok) {
+            const float* dm = reinterpret_cast<const float*>(sm + kDOt);
+            float acc[4][4] = {};
+#pragma unroll 4
+            for (int r = a0; r < 64; ++r) {  // N[r][a] = 0 for r < a
+                const float4 m4 = *reinterpret_cast<const float4*>(dm + r * 64 + s0);
+                const float nv[4] = {NT[a0 * 64 + r], NT[(a0 + 1) * 64 + r], NT[(a0 + 2) * 64 + r],
+                                     NT[(a0 + 3) * 64 + r]};
+                const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(nv[x], mv[y], acc[x][y]);
+            }
+#pragma unroll
+            for (int y = 0; y < 4; ++y)
+                *reinterpret_cast<float4*>(X0T + (s0 + y) * 64 + a0) =
+                    make_float4(acc[0][y], acc[1][y], acc[2][y], acc[3][y]);
+            if (a0 == s0) {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) reinterpret_cast<float*>(mid + kMdB)[a0 + x] = acc[x][x];
+            }
+        }
+        csync();
+        if (ok) {
+            // dL[r][i] for r in [r0, r0 + 4), i in [i0, i0 + 4): -sum_{s <= i} X0[r][s] N[i][s] beta_s
+            const int r0 = a0, i0 = s0;
+            float dl[4][4] = {};
+#pragma unroll 4
+            for (int s = 0; s <= i0 + 3; ++s) {
+                const float4 x4 = *reinterpret_cast<const float4*>(X0T + s * 64 + r0);
+                const float4 n4 = *reinterpret_cast<const float4*>(NT + s * 64 + i0);
+                const float bs = sBeta[s];
+                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
+                const float nv[4] = {n4.x * bs, n4.y * bs, n4.z * bs, n4.w * bs};
+#pragma unroll
+                for (int x = 0; x < 4; ++x)
+#pragma unroll
+                    for (int y = 0; y < 4; ++y) dl[x][y] = fmaf(xv[x], nv[y], dl[x][y]);
+            }
+            // dL image: row i, columns c = 63 - r (the four columns 60 - r0 .. 63 - r0 hold rows
+            // r0 + 3 .. r0), hi and lo
+#pragma unroll
+            for (int y = 0; y < 4; ++y) {
+                const int i = i0 + y;
+                float v4[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int r = r0 + 3 - x;
+                    v4[x] = (i < r && r < it.L) ? -dl[3 - x][y] : 0.f;
+                }
+                uint32_t h2[2], l2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    h2[e] = pack_bf16x2(v4[2 * e], v4[2 * e + 1]);
+                    l2[e] = pack_bf16x2(v4[2 * e] - __uint_as_float(h2[e] << 16),
+                                        v4[2 * e + 1] - __uint_as_float(h2[e] & 0xffff0000u));
+                }
+                const uint32_t off = swz(i, 60 - r0);
+                *reinterpret_cast<uint2*>(mid + kMdL + off) = make_uint2(h2[0], h2[1]);
+                *reinterpret_cast<uint2*>(mid + kMdL + 8192 + off) = make_uint2(l2[0], l2[1]);
+            }
+        }
+        BP_MARK(6);
+        // ---- epilogue 3: pE = (gamma^C/Gamma)*(dS_C Vt^T) and rs = diag(dS_C S_0^T)
+        ok = ok && mbar_wait_ab(mma3, ph, p.err, abort);
+        BP_MARK(7);
+        if (ok) {
+            tc_fence_after();
+            const float gl = sGlast[ch];
+            float* pe = reinterpret_cast<float*>(mid + kMdE) + ch;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float c16[16];
+                tmem_ld16(tmem + lb + 384 + 32 * wh + 16 * hf, c16);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int u = 16 * hf + e;
+                    pe[(32 * wh + u) * 128] = ex2f(gl - G2[u]) * c16[e];
                 }
             }
-            tc_fence_before();
-            fence_async_smem();  // the next item's copies overwrite what was written here
-            csync();
-            if (lane == 0) mbar_arrive(done);
-            if (!ok) break;
+            if (wh == 0) {  // lane i reads column i of its warp's 32 columns
+                float d0[16], d1[16];
+                tmem_ld16(tmem + lb + 32 * wq, d0);
+                tmem_ld16(tmem + lb + 32 * wq + 16, d1);
+                tmem_ld_wait();
+                float rs = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    rs = (lane == e) ? d0[e] : rs;
+                    rs = (lane == 16 + e) ? d1[e] : rs;
+                }
+                reinterpret_cast<float*>(mid + kMdRs)[ch] = rs;
+            }
         }
+        tc_fence_before();
+        fence_async_smem();  // the next item's copies overwrite what was written here
+        ok = csync_and(ok);
+        BP_MARK(8);
+        if (!ok) break;
     }
 
     __syncthreads();
-    if (s_abort && tid == kIss) {
+    if (s_abort && iss) {
         // let the copies and MMAs still in flight land before the CTA leaves
         for (int b = 0; b < 5; ++b)
             if (inflight & (1u << b)) mbar_wait(&bars[b], inflight_ph, nullptr);
@@ -631,10 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
     uint64_t* fullIn = bars + 0;
     uint64_t* fullX = bars + 1;
     uint64_t* mma1 = bars + 2;
-    uint64_t* ready1 = bars + 3;  // 8 arrivals
-    uint64_t* done = bars + 4;    // 8 arrivals
-    uint64_t* drain = bars + 5;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+    uint64_t* drain = bars + 3;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
     float* sBeta = reinterpret_cast<float*>(sm + kDMisc);
     float* sTot = sBeta + 64;
     float* sGlast = sTot + 128;
@@ -646,11 +695,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
     volatile int* abort = &s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool iss = tid == 0;
     if (tid == 0) {
-        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
-        mbar_init(ready1, 8);
-        mbar_init(done, 8);
-        mbar_init(drain, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -661,14 +708,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const int n_items = __ldg(p.chunk_off + p.N) * p.H;
 
+    const int wq = warp & 3, wh = warp >> 2;
+    const int ch = 32 * wq + lane;  // key channel i = TMEM lane
+    const uint32_t lb = static_cast<uint32_t>(32 * wq) << 16;
     uint32_t inflight = 0, inflight_ph = 0;
-    if (tid == kIss) {
-        uint32_t iter = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
-            const Item it = decode(p, item);
-            const uint32_t ph = iter & 1;
-            if (iter > 0 && !mbar_wait_ab(done, ph ^ 1, p.err, abort)) break;
-            const uint8_t* mid = p.mid + (size_t)item * kMdBytes;
+    bool ok = true;
+    uint32_t iter = 0;
+    BP_T0();
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
+        const Item it = decode(p, item);
+        const uint32_t ph = iter & 1;
+        const uint8_t* mid = p.mid + (size_t)item * kMdBytes;
+        if (iss) {
             inflight = 0x3u;
             inflight_ph = ph;
             mbar_expect_tx(fullIn, 49152);
@@ -677,220 +728,233 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
             load_tile(&p.tz, sm + kZt, it, fullIn);
             mbar_expect_tx(fullX, 32768);
             bulk_g2s(sm + kDAi, mid + kMdA, 32768, fullX);  // dA then dL images (adjacent)
-            if (!mbar_wait_ab(ready1, ph, p.err, abort) || !mbar_wait_ab(fullX, ph, p.err, abort)) break;
-            tc_fence_after();
-            // D(X, K) per block S: A = K~^T rows s in S (MN-major, M = 128 key channels),
-            // B = X^T rows s in S with columns c = 63 - r < 64 - 16 S (MN-major, N = 64 - 16 S);
-            // hi x hi + hi x lo + lo x hi
-#pragma unroll
-            for (int S = 0; S < 4; ++S) {
-                const uint32_t idS = idesc_bf16(128, 64 - 16 * S, true, true);
-                const uint64_t kh = sdesc_sw128(sb + kKT + 2048 * S, 8192, 1024);
-                const uint64_t kl = sdesc_sw128(sb + kKT + 16384 + 2048 * S, 8192, 1024);
-#pragma unroll
-                for (int xs = 0; xs < 2; ++xs) {  // 0: dA, 1: dL
-                    const uint32_t xb = sb + (xs ? kDLi : kDAi) + 2048 * S;
-                    const uint64_t xh = sdesc_sw128(xb, 8192, 1024);
-                    const uint64_t xl = sdesc_sw128(xb + 8192, 8192, 1024);
-                    const uint32_t d = tmem + 160 * xs + kOffS[S];
-                    mma_bf16(d, kh, xh, idS, 0);
-                    mma_bf16(d, kh, xl, idS, 1);
-                    mma_bf16(d, kl, xh, idS, 1);
+            const int nx = item + gridDim.x;  // the next item's inputs into L2
+            if (nx < n_items) {
+                const Item in = decode(p, nx);
+                l2_prefetch(p.mid + (size_t)nx * kMdBytes, kMdBytes);
+                for (int b = 0; b < 2; ++b) {
+                    tma_prefetch_3d(&p.tq, 64 * b, in.h, (int)in.t0);
+                    tma_prefetch_3d(&p.tk, 64 * b, in.h, (int)in.t0);
+                    tma_prefetch_3d(&p.tz, 64 * b, in.h, (int)in.t0);
                 }
             }
-            // D^T per row block R: A = Q^^T (then K^b^T) rows 63 - r for r in R (MN-major),
-            // B = dA (then dL) rows s < 16 (R + 1), K = the columns 63 - r of block R (K-major)
-#pragma unroll
-            for (int R = 0; R < 4; ++R) {
-                const uint32_t idR = idesc_bf16(128, 16 * (R + 1), true, false);
-                const uint32_t arow = (48 - 16 * R) * 128, bcol = (48 - 16 * R) * 2;
-                const uint32_t d = tmem + 320 + kOffR[R];
-#pragma unroll
-                for (int xs = 0; xs < 2; ++xs) {
-                    const uint32_t ab = sb + (xs ? kKB : kQH) + arow;
-                    const uint64_t ah = sdesc_sw128(ab, 8192, 1024);
-                    const uint64_t al = sdesc_sw128(ab + 16384, 8192, 1024);
-                    const uint32_t xb = sb + (xs ? kDLi : kDAi) + bcol;
-                    const uint64_t xh = sdesc_sw128(xb, 0, 1024);
-                    const uint64_t xl = sdesc_sw128(xb + 8192, 0, 1024);
-                    mma_bf16(d, ah, xh, idR, xs);
-                    mma_bf16(d, ah, xl, idR, 1);
-                    mma_bf16(d, al, xh, idR, 1);
-                }
-            }
-            mma_commit(mma1);
         }
-    }
-
-    if (warp < 8) {
-        const int wq = warp & 3, wh = warp >> 2;
-        const int ch = 32 * wq + lane;  // key channel i = TMEM lane
-        const uint32_t lb = static_cast<uint32_t>(32 * wq) << 16;
-        uint32_t iter = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++iter) {
-            const Item it = decode(p, item);
-            const uint32_t ph = iter & 1;
-            const float eA = expf(__ldg(p.A_log + it.h));
-            const float scale2 = eA * kLog2e, gmin2 = p.g_min * kLog2e;
-            const uint8_t* mid = p.mid + (size_t)item * kMdBytes;
-            if (tid < 64)
-                sBeta[tid] = tid < it.L ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
-            bool ok = mbar_wait_ab(fullIn, ph, p.err, abort);
-            float G2[32];
-            if (ok) {
-                gate_scan(sm + kZt, ch, wh, it.L, scale2, gmin2, sTot, G2);
-                if (wh == 1) sGlast[ch] = G2[31];
-                sRho[(2 * wh) * 128 + ch] = G2[8];
-                sRho[(2 * wh + 1) * 128 + ch] = G2[24];
-            } else {
-                csync();
-            }
+        const float eA = expf(__ldg(p.A_log + it.h));
+        const float scale2 = eA * kLog2e, gmin2 = p.g_min * kLog2e;
+        if (tid < 64)
+            sBeta[tid] = tid < it.L ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
+        ok = ok && mbar_wait_ab(fullIn, ph, p.err, abort);
+        BP_MARK(10);
+        float G2[32];
+        if (ok) {
+            gate_scan(sm + kZt, ch, wh, it.L, scale2, gmin2, sTot, G2);
+            if (wh == 1) sGlast[ch] = G2[31];
+            sRho[(2 * wh) * 128 + ch] = G2[8];
+            sRho[(2 * wh + 1) * 128 + ch] = G2[24];
+        } else {
             csync();
-            if (ok) {
-                // K~ (rows s), Q^ and K^b (rows 63 - r), this thread's channel and half
-                const float rhoA = sRho[(2 * wh) * 128 + ch], rhoB = sRho[(2 * wh + 1) * 128 + ch];
+        }
+        csync();
+        BP_MARK(11);
+        if (ok) {
+            // K~ (rows s), Q^ and K^b (rows 63 - r), this thread's channel and half
+            const float rhoA = sRho[(2 * wh) * 128 + ch], rhoB = sRho[(2 * wh + 1) * 128 + ch];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int r = 32 * wh + e;
-                    const float rho = e < 16 ? rhoA : rhoB;
+            for (int e = 0; e < 32; ++e) {
+                const int r = 32 * wh + e;
+                const float rho = e < 16 ? rhoA : rhoB;
+                const bool live = r < it.L;
+                const float kv = live ? ldbf(sm + kKt + swz2(r, ch, 64)) : 0.f;
+                const float qv = live ? ldbf(sm + kQt + swz2(r, ch, 64)) : 0.f;
+                const float up = ex2f(G2[e] - rho), dn = ex2f(rho - G2[e]);
+                const uint32_t o = swz2(r, ch, 64), orv = swz2(63 - r, ch, 64);
+                st_hilo(sm + kKT + o, sm + kKT + 16384 + o, kv * dn);
+                st_hilo(sm + kQH + orv, sm + kQH + 16384 + orv, qv * up);
+                st_hilo(sm + kKB + orv, sm + kKB + 16384 + orv, sBeta[r] * kv * up);
+            }
+        }
+        fence_async_smem();
+        ok = csync_and(ok);
+        BP_MARK(12);
+        if (iss && ok) {
+            ok = mbar_wait_ab(fullX, ph, p.err, abort);
+            if (ok) {
+                tc_fence_after();
+                // D(X, K) per block S: A = K~^T rows s in S (MN-major, M = 128 key channels),
+                // B = X^T rows s in S with columns c = 63 - r < 64 - 16 S (MN-major,
+                // N = 64 - 16 S); hi x hi + hi x lo + lo x hi
+#pragma unroll
+                for (int S = 0; S < 4; ++S) {
+                    const uint32_t idS = idesc_bf16(128, 64 - 16 * S, true, true);
+                    const uint64_t kh = sdesc_sw128(sb + kKT + 2048 * S, 8192, 1024);
+                    const uint64_t kl = sdesc_sw128(sb + kKT + 16384 + 2048 * S, 8192, 1024);
+#pragma unroll
+                    for (int xs = 0; xs < 2; ++xs) {  // 0: dA, 1: dL
+                        const uint32_t xb = sb + (xs ? kDLi : kDAi) + 2048 * S;
+                        const uint64_t xh = sdesc_sw128(xb, 8192, 1024);
+                        const uint64_t xl = sdesc_sw128(xb + 8192, 8192, 1024);
+                        const uint32_t d = tmem + 160 * xs + kOffS[S];
+                        mma_bf16(d, kh, xh, idS, 0);
+                        mma_bf16(d, kh, xl, idS, 1);
+                        mma_bf16(d, kl, xh, idS, 1);
+                    }
+                }
+                // D^T per row block R: A = Q^^T (then K^b^T) rows 63 - r for r in R (MN-major),
+                // B = dA (then dL) rows s < 16 (R + 1), K = the columns 63 - r of block R
+                // (K-major)
+#pragma unroll
+                for (int R = 0; R < 4; ++R) {
+                    const uint32_t idR = idesc_bf16(128, 16 * (R + 1), true, false);
+                    const uint32_t arow = (48 - 16 * R) * 128, bcol = (48 - 16 * R) * 2;
+                    const uint32_t d = tmem + 320 + kOffR[R];
+#pragma unroll
+                    for (int xs = 0; xs < 2; ++xs) {
+                        const uint32_t ab = sb + (xs ? kKB : kQH) + arow;
+                        const uint64_t ah = sdesc_sw128(ab, 8192, 1024);
+                        const uint64_t al = sdesc_sw128(ab + 16384, 8192, 1024);
+                        const uint32_t xb = sb + (xs ? kDLi : kDAi) + bcol;
+                        const uint64_t xh = sdesc_sw128(xb, 0, 1024);
+                        const uint64_t xl = sdesc_sw128(xb + 8192, 0, 1024);
+                        mma_bf16(d, ah, xh, idR, xs);
+                        mma_bf16(d, ah, xl, idR, 1);
+                        mma_bf16(d, al, xh, idR, 1);
+                    }
+                }
+                mma_commit(mma1);
+            }
+        }
+        ok = ok && mbar_wait_ab(mma1, ph, p.err, abort);
+        BP_MARK(13);
+        float dG[32];
+        float lastp = 0.f;
+        if (ok) {
+            tc_fence_after();
+            const float* pQ = reinterpret_cast<const float*>(mid + kMdQ) + ch;
+            const float* pP = reinterpret_cast<const float*>(mid + kMdP) + ch;
+            const float* pE = reinterpret_cast<const float*>(mid + kMdE) + ch;
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                const int r0 = 32 * wh + 16 * g, R0 = 2 * wh + g;
+                float pq16[16], pp16[16], pe16[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) pq16[u] = __ldg(pQ + (r0 + u) * 128);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) pp16[u] = __ldg(pP + (r0 + u) * 128);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) pe16[u] = __ldg(pE + (r0 + u) * 128);
+                float dqd[16], ee[16], ff[16], t16[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) { dqd[u] = 0.f; ee[u] = 0.f; ff[u] = 0.f; }
+                // D(., K): element e of columns 48 - r0 .. is token r0 + 15 - e
+                for (int S = 0; S <= R0; ++S) {
+                    const float rho = sRho[S * 128 + ch];
+                    float a16[16];
+                    tmem_ld16(tmem + lb + kOffS[S] + 48 - r0, a16);
+                    tmem_ld16(tmem + lb + 160 + kOffS[S] + 48 - r0, t16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int u = 15 - e;
+                        const float f = ex2f(G2[16 * g + u] - rho);
+                        dqd[u] = fmaf(f, a16[e], dqd[u]);
+                        ee[u] = fmaf(f, t16[e], ee[u]);
+                    }
+                }
+                // D^T: element e of columns r0 .. of block R is token r0 + e
+                for (int R = R0; R < 4; ++R) {
+                    const float rho = sRho[R * 128 + ch];
+                    tmem_ld16(tmem + lb + 320 + kOffR[R] + r0, t16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ff[e] = fmaf(ex2f(rho - G2[16 * g + e]), t16[e], ff[e]);
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int r = r0 + u;
                     const bool live = r < it.L;
                     const float kv = live ? ldbf(sm + kKt + swz2(r, ch, 64)) : 0.f;
                     const float qv = live ? ldbf(sm + kQt + swz2(r, ch, 64)) : 0.f;
-                    const float up = ex2f(G2[e] - rho), dn = ex2f(rho - G2[e]);
-                    const uint32_t o = swz2(r, ch, 64), orv = swz2(63 - r, ch, 64);
-                    st_hilo(sm + kKT + o, sm + kKT + 16384 + o, kv * dn);
-                    st_hilo(sm + kQH + orv, sm + kQH + 16384 + orv, qv * up);
-                    st_hilo(sm + kKB + orv, sm + kKB + 16384 + orv, sBeta[r] * kv * up);
-                }
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ready1);
-            ok = ok && mbar_wait_ab(mma1, ph, p.err, abort);
-            float dG[32];
-            float lastp = 0.f;
-            if (ok) {
-                tc_fence_after();
-                const float* pQ = reinterpret_cast<const float*>(mid + kMdQ) + ch;
-                const float* pP = reinterpret_cast<const float*>(mid + kMdP) + ch;
-                const float* pE = reinterpret_cast<const float*>(mid + kMdE) + ch;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    const int r0 = 32 * wh + 16 * g, R0 = 2 * wh + g;
-                    float dqd[16], ee[16], ff[16], t16[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) { dqd[u] = 0.f; ee[u] = 0.f; ff[u] = 0.f; }
-                    // D(., K): element e of columns 48 - r0 .. is token r0 + 15 - e
-                    for (int S = 0; S <= R0; ++S) {
-                        const float rho = sRho[S * 128 + ch];
-                        float a16[16];
-                        tmem_ld16(tmem + lb + kOffS[S] + 48 - r0, a16);
-                        tmem_ld16(tmem + lb + 160 + kOffS[S] + 48 - r0, t16);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int u = 15 - e;
-                            const float f = ex2f(G2[16 * g + u] - rho);
-                            dqd[u] = fmaf(f, a16[e], dqd[u]);
-                            ee[u] = fmaf(f, t16[e], ee[u]);
-                        }
-                    }
-                    // D^T: element e of columns r0 .. of block R is token r0 + e
-                    for (int R = R0; R < 4; ++R) {
-                        const float rho = sRho[R * 128 + ch];
-                        tmem_ld16(tmem + lb + 320 + kOffR[R] + r0, t16);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) ff[e] = fmaf(ex2f(rho - G2[16 * g + e]), t16[e], ff[e]);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const int r = r0 + u;
-                        const bool live = r < it.L;
-                        const float kv = live ? ldbf(sm + kKt + swz2(r, ch, 64)) : 0.f;
-                        const float qv = live ? ldbf(sm + kQt + swz2(r, ch, 64)) : 0.f;
-                        const float b = sBeta[r];
-                        const float pq = pQ[r * 128], pp = pP[r * 128], pe = pE[r * 128];
-                        const float dq = pq + dqd[u];
-                        const float dkv = pp + b * ee[u] + ff[u] + pe;
-                        dG[16 * g + u] = live ? kv * (pp + b * ee[u] - ff[u] - pe) + qv * dq : 0.f;
-                        lastp = fmaf(kv, pe, lastp);
-                        t16[u] = kv * ee[u];  // dbeta's E term, summed over channels below
-                        if (live && ch < p.dk) {
-                            const size_t o = ((size_t)(it.t0 + r) * p.H + it.h) * p.dk + ch;
-                            p.dq[o] = __float2bfloat16_rn(dq);
-                            p.dkg[o] = __float2bfloat16_rn(dkv);
-                        }
-                    }
-                    // sum over the 32 channels of this warp, then over the four warps
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        float v = t16[u];
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                        if (lane == 0) sDb[wq * 64 + r0 + u] = v;
+                    const float b = sBeta[r];
+                    const float pq = pq16[u], pp = pp16[u], pe = pe16[u];
+                    const float dq = pq + dqd[u];
+                    const float dkv = pp + b * ee[u] + ff[u] + pe;
+                    dG[16 * g + u] = live ? kv * (pp + b * ee[u] - ff[u] - pe) + qv * dq : 0.f;
+                    lastp = fmaf(kv, pe, lastp);
+                    t16[u] = kv * ee[u];  // dbeta's E term, summed over channels below
+                    if (live && ch < p.dk) {
+                        const size_t o = ((size_t)(it.t0 + r) * p.H + it.h) * p.dk + ch;
+                        p.dq[o] = __float2bfloat16_rn(dq);
+                        p.dkg[o] = __float2bfloat16_rn(dkv);
                     }
                 }
-                sLast[wh * 128 + ch] = lastp;
-            }
-            csync();
-            float dAp = 0.f;
-            if (ok) {
-                // dG of the chunk's last row L - 1 also takes sum_r K pE + gamma^C rs
-                const float last = sLast[ch] + sLast[128 + ch] +
-                                   ex2f(sGlast[ch]) * reinterpret_cast<const float*>(mid + kMdRs)[ch];
-                const int ul = it.L - 1 - 32 * wh;
-                // reverse cumulative sum over this half, then the second half's total
-                float acc = 0.f;
+                // sum over the 32 channels of this warp, then over the four warps
 #pragma unroll
-                for (int u = 31; u >= 0; --u) {
-                    if (u == ul) dG[u] += last;
-                    acc += dG[u];
-                    dG[u] = acc;
-                }
-                if (wh == 1) sTot[ch] = acc;
-            }
-            csync();
-            if (ok) {
-                const float add = wh == 0 ? sTot[ch] : 0.f;
+                for (int u = 0; u < 16; ++u) {
+                    float v = t16[u];
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int r = 32 * wh + u;
-                    if (r < it.L) {
-                        const float x = eA * ldbf(sm + kZt + swz2(r, ch, 64));
-                        const float sg = 1.f / (1.f + __expf(-x));
-                        const float dx = (dG[u] + add) * p.g_min * sg * (1.f - sg);
-                        dAp = fmaf(dx, x, dAp);
-                        if (ch < p.dk)
-                            p.dz[((size_t)(it.t0 + r) * p.H + it.h) * p.dk + ch] = __float2bfloat16_rn(dx * eA);
-                    }
-                }
-                if (tid < 64 && tid < it.L) {
-                    const float db = reinterpret_cast<const float*>(mid + kMdB)[tid] + sDb[tid] +
-                                     sDb[64 + tid] + sDb[128 + tid] + sDb[192 + tid];
-                    p.dbeta[(size_t)(it.t0 + tid) * p.H + it.h] = __float2bfloat16_rn(db);
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) sDb[wq * 64 + r0 + u] = v;
                 }
             }
-            // dA_log partial of the item: channels past dk have zero z and contribute x = 0
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
-            if (lane == 0) sRed[warp] = dAp;
-            csync();
-            if (tid == 0 && ok) {
-                float s = 0.f;
-                for (int w = 0; w < 8; ++w) s += sRed[w];
-                p.dA_item[item] = s;
-            }
-            tc_fence_before();
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(done);
-            if (!ok) break;
+            sLast[wh * 128 + ch] = lastp;
         }
+        BP_MARK(14);
+        csync();
+        float dAp = 0.f;
+        if (ok) {
+            // dG of the chunk's last row L - 1 also takes sum_r K pE + gamma^C rs
+            const float last = sLast[ch] + sLast[128 + ch] +
+                               ex2f(sGlast[ch]) * __ldg(reinterpret_cast<const float*>(mid + kMdRs) + ch);
+            const int ul = it.L - 1 - 32 * wh;
+            // reverse cumulative sum over this half, then the second half's total
+            float acc = 0.f;
+#pragma unroll
+            for (int u = 31; u >= 0; --u) {
+                if (u == ul) dG[u] += last;
+                acc += dG[u];
+                dG[u] = acc;
+            }
+            if (wh == 1) sTot[ch] = acc;
+        }
+        csync();
+        if (ok) {
+            const float add = wh == 0 ? sTot[ch] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int r = 32 * wh + u;
+                if (r < it.L) {
+                    const float x = eA * ldbf(sm + kZt + swz2(r, ch, 64));
+                    const float sg = __fdividef(1.f, 1.f + __expf(-x));
+                    const float dx = (dG[u] + add) * p.g_min * sg * (1.f - sg);
+                    dAp = fmaf(dx, x, dAp);
+                    if (ch < p.dk)
+                        p.dz[((size_t)(it.t0 + r) * p.H + it.h) * p.dk + ch] = __float2bfloat16_rn(dx * eA);
+                }
+            }
+            if (tid < 64 && tid < it.L) {
+                const float db = __ldg(reinterpret_cast<const float*>(mid + kMdB) + tid) + sDb[tid] +
+                                 sDb[64 + tid] + sDb[128 + tid] + sDb[192 + tid];
+                p.dbeta[(size_t)(it.t0 + tid) * p.H + it.h] = __float2bfloat16_rn(db);
+            }
+        }
+        // dA_log partial of the item: channels past dk have zero z and contribute x = 0
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
+        if (lane == 0) sRed[warp] = dAp;
+        tc_fence_before();
+        fence_async_smem();
+        ok = csync_and(ok);
+        if (tid == 0 && ok) {
+            float s = 0.f;
+            for (int w = 0; w < 8; ++w) s += sRed[w];
+            p.dA_item[item] = s;
+        }
+        BP_MARK(15);
+        if (!ok) break;
     }
 
     __syncthreads();
-    if (s_abort && tid == kIss) {
+    if (s_abort && iss) {
         for (int b = 0; b < 2; ++b)
             if (inflight & (1u << b)) mbar_wait(&bars[b], inflight_ph, nullptr);
         mma_commit(drain);
@@ -909,6 +973,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
 
 // The per-chunk backward on the tensor cores (see the top of this file): fwd_ws holds the
 // forward's plan (chunk offsets and table), bimg the image blocks, mid the mid blocks.
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_bwd_cycles(unsigned long long* out, int n) {
+    if (n > 32) n = 32;
+    if (cudaMemcpyFromSymbol(out, bwdtc::g_bwd_phase, n * sizeof(unsigned long long)) != cudaSuccess)
+        return -1;
+    static const unsigned long long zeros[32] = {};
+    return cudaMemcpyToSymbol(bwdtc::g_bwd_phase, zeros, sizeof zeros) == cudaSuccess ? n : -1;
+}
+#endif
+
 cudaError_t launch_bwd_items_tc(const BwdArgs& a, void* fwd_ws, const void* bimg, void* mid,
                                 float* dA_item, cudaStream_t stream) {
     using namespace bwdtc;

@@ -378,15 +378,18 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (!p.bimg) return;
                 uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + j * 128;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float v8[8];
+                for (int c8 = 0; c8 < 8; c8 += 2) {
+                    float v0[8], v1[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) v8[e] = S[8 * c8 + e];
-                    uint4 hi, lo;
-                    pk8_hilo(v8, hi, lo);
-                    const uint32_t off = (uint32_t)((c8 ^ (j & 7)) << 4);
-                    *reinterpret_cast<uint4*>(dst + off) = hi;
-                    *reinterpret_cast<uint4*>(dst + 32768 + off) = lo;
+                    for (int e = 0; e < 8; ++e) {
+                        v0[e] = S[8 * c8 + e];
+                        v1[e] = S[8 * c8 + 8 + e];
+                    }
+                    uint4 h0, l0, h1, l1;
+                    pk8_hilo(v0, h0, l0);
+                    pk8_hilo(v1, h1, l1);
+                    st_swz_pair(dst, c8, j, h0, h1);
+                    st_swz_pair(dst + 32768, c8, j, l0, l1);
                 }
             };
             if (c.nch > 0) {
@@ -441,14 +444,10 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                         tmem_st8(tmem + lb + kTV + 16 * wg + 8 * hf, hi);
                         tmem_st8(tmem + lb + kTVlo + 16 * wg + 8 * hf, lo);
                         if (vimg) {
-#pragma unroll
-                            for (int x = 0; x < 2; ++x) {
-                                const uint32_t off = (uint32_t)(((4 * wg + 2 * hf + x) ^ (j & 7)) << 4);
-                                *reinterpret_cast<uint4*>(vimg + off) =
-                                    make_uint4(hi[4 * x], hi[4 * x + 1], hi[4 * x + 2], hi[4 * x + 3]);
-                                *reinterpret_cast<uint4*>(vimg + 16384 + off) =
-                                    make_uint4(lo[4 * x], lo[4 * x + 1], lo[4 * x + 2], lo[4 * x + 3]);
-                            }
+                            st_swz_pair(vimg, 4 * wg + 2 * hf, j, make_uint4(hi[0], hi[1], hi[2], hi[3]),
+                                        make_uint4(hi[4], hi[5], hi[6], hi[7]));
+                            st_swz_pair(vimg + 16384, 4 * wg + 2 * hf, j, make_uint4(lo[0], lo[1], lo[2], lo[3]),
+                                        make_uint4(lo[4], lo[5], lo[6], lo[7]));
                         }
                     }
                     tmem_st_wait();

@@ -145,6 +145,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// TMA prefetch of a tile into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // TMA store of a tile from shared memory (this thread's bulk group).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0,
                                              int c1, int c2) {
@@ -382,6 +390,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+
+// 32-byte global store of two 16-byte chunks (32-byte aligned address)
+__device__ __forceinline__ void st_global_32(void* p, const uint4& a, const uint4& b) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x),
+                 "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+// Chunks c, c + 1 (c even) of row x of a 128-byte-swizzled tile sit at positions c ^ (x & 7)
+// and that ^ 1: one aligned 32-byte block at position c ^ (x & 6), in swapped order for odd x.
+__device__ __forceinline__ void st_swz_pair(uint8_t* row, int c, int x, const uint4& a, const uint4& b) {
+    uint8_t* dst = row + ((c ^ (x & 6)) << 4);
+    if (x & 1) st_global_32(dst, b, a);
+    else st_global_32(dst, a, b);
+}
 
 // ------------------------------------------------------ fp32 <-> bf16 helpers --
 
