@@ -59,6 +59,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct ItemParams {
     CUtensorMap tq, tk, tv, tz, tdo;  // [T_total, H, d] bf16, boxes of 64 columns x 1 x 64 rows
+    CUtensorMap tdq, tdk, tdz, tdv;   // the outputs, same boxes (TMA stores of full chunks)
     const __nv_bfloat16* beta;
     const __nv_bfloat16* v;           // raw v (the state kernel's Y = V - K+ S_0)
     const float* A_log;
@@ -97,6 +98,35 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 __device__ __forceinline__ uint32_t swz2(int row, int ch, int rows) {
     return static_cast<uint32_t>((ch >> 6) * rows * 128) + swz(row, ch & 63);
 }
+// Global loads issued where they are written (a plain load may be sunk to its first use,
+// which would expose its latency there).
+__device__ __forceinline__ float ld_early(const float* q) {
+    float r;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(r) : "l"(q));
+    return r;
+}
+__device__ __forceinline__ float4 ld_early4(const float* q) {
+    float4 r;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(q));
+    return r;
+}
+// Sum of v[u] over the 32 lanes of the warp for 16 values at once (transposing halving
+// exchange: 16 shuffles); lanes 2u and 2u + 1 end with the sum of value u, returned.
+__device__ __forceinline__ float warp_sum16(float (&v)[16], int lane) {
+#pragma unroll
+    for (int w = 8, o = 16; w >= 1; w >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const float keep = up ? v[k + w] : v[k], send = up ? v[k] : v[k + w];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 __device__ __forceinline__ float ldbf(const uint8_t* p) {
     return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
 }
@@ -128,6 +158,29 @@ __device__ __forceinline__ void load_tile(const CUtensorMap* m, uint8_t* dst, co
                                           uint64_t* bar) {
     tma_load_3d(dst, m, 0, it.h, (int)it.t0, bar);
     tma_load_3d(dst + 8192, m, 64, it.h, (int)it.t0, bar);
+}
+
+// Rows [0, L) of a staged [2 blocks][64 rows][128 B] bf16 tile into out [T_total, H, d]: a full
+// chunk by two TMA stores from thread 0 (which must later wait for their reads before the tile
+// is rewritten), a short one by 16-byte copies of the valid rows (rows past L belong to the
+// next sequence).  The tile's writers have fenced and synchronised before.
+__device__ __forceinline__ void store_tile(const CUtensorMap* m, const uint8_t* tile,
+                                           __nv_bfloat16* out, const Item& it, int H, int d,
+                                           int tid) {
+    if (it.L == 64) {
+        if (tid == 0) {
+            tma_store_3d(m, tile, 0, it.h, (int)it.t0);
+            tma_store_3d(m, tile + 8192, 64, it.h, (int)it.t0);
+            bulk_commit();
+        }
+        return;
+    }
+    for (int q = tid; q < it.L * 16; q += 256) {
+        const int r = q >> 4, blk = (q >> 3) & 1, c = q & 7;
+        if (64 * blk + 8 * c >= d) continue;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + blk * 8192 + r * 128 + ((c ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(out + ((size_t)(it.t0 + r) * H + it.h) * d + 64 * blk + 8 * c) = v;
+    }
 }
 
 // The cumulative gate of channel i over rows [32 wh, 32 wh + 32) in log2 units (rows past L
@@ -164,13 +217,14 @@ constexpr uint32_t kDOt = 163840;    // dO tile; after batch 2: dM fp32 [64][64]
 constexpr uint32_t kRX = 180224;     // K+ (K-major rows s) + M (rows r); after batch 1: dV^T
                                      // (one bf16, rows j); after batch 2: X0^T, N^T fp32
 constexpr uint32_t kVt = 212992;     // v tile
-constexpr uint32_t kMisc = 229376;   // beta [64], tot [128], glast [128]
-constexpr uint32_t kSBars = kMisc + 1280;
+constexpr uint32_t kMisc = 229376;   // beta [64], tot [128], glast [128], dbeta1 halves [2][64]
+constexpr uint32_t kSBars = kMisc + 1792;
 constexpr uint32_t kStateSmem = kSBars + 128 + 1024;
 static_assert(kStateSmem <= 232448, "state kernel exceeds the shared-memory limit");
 // TMEM columns: dV^T [0, 64), (K+ S_0)^T [64, 128), S_0 dO^T [128, 192), S_0 dV^T [192, 256),
-// dA^T (lanes 0..63) [256, 320), dM^T (lanes 64..127) [320, 384), dS_C Vt^T [384, 448), and in
-// batch 3 dS_C S_0^T [0, 128) (only its diagonal is read)
+// dA^T (lanes 0..63) [256, 320), dM^T (lanes 64..127) [320, 384), dS_C Vt^T [384, 448), in
+// batch 3 dS_C S_0^T [0, 128) (only its diagonal is read), then the solve's reverse:
+// Z1^T [128, 192), Z1^T bf16 hi [192, 224), lo [224, 256), dL^T [256, 320)
 constexpr uint32_t kTCols = 512;
 
 // The state kernel: one CTA of 256 threads per SM walks items (chunk, head); thread 0 also
@@ -189,18 +243,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     uint64_t* mma1 = bars + 5;
     uint64_t* mma2 = bars + 6;
     uint64_t* mma3 = bars + 7;
-    uint64_t* drain = bars + 8;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 9);
+    uint64_t* mma4 = bars + 8;  // Z1^T = M dM^T
+    uint64_t* mma5 = bars + 9;  // dL^T = (N^T Z1)^T
+    uint64_t* drain = bars + 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
     float* sBeta = reinterpret_cast<float*>(sm + kMisc);
     float* sTot = sBeta + 64;
     float* sGlast = sTot + 128;
+    float* sDb1 = sGlast + 128;  // [2][64]: dbeta1 halves
     __shared__ int s_abort;
     volatile int* abort = &s_abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool iss = tid == 0;
     if (tid == 0) {
-        for (int i = 0; i < 9; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 11; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         s_abort = 0;
     }
@@ -211,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const int n_items = __ldg(p.chunk_off + p.N) * p.H;
 
+    constexpr uint32_t idZ = idesc_bf16(128, 64, false, true);    // M x dM^T, Z1^T x N
     constexpr uint32_t idV = idesc_bf16(128, 64, false, true);    // dVt^T x M
     constexpr uint32_t idY = idesc_bf16(128, 64, false, false);   // S_0^T x K+^T
     constexpr uint32_t idMN = idesc_bf16(128, 64, true, false);   // S_0 x dO^T, [Vt; Y] x dO^T
@@ -229,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         const uint32_t ph = iter & 1;
         const uint8_t* blk = p.bimg + (size_t)item * kBiBytes;
         if (iss) {
+            bulk_wait_read0();  // the previous item's dv store has read the v tile's place
             inflight = 0xfu;  // fullIn, fullS, fullV, fullDO
             inflight_ph = ph;
             mbar_expect_tx(fullIn, 49152);
@@ -260,6 +319,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         const float* Ng = reinterpret_cast<const float*>(blk + kBiN);
         if (tid < 64)
             sBeta[tid] = tid < it.L ? __bfloat162float(p.beta[(size_t)(it.t0 + tid) * p.H + it.h]) : 0.f;
+        // this thread's 16 entries of N (row tid / 4) for the M image, in flight during the gate
+        float4 nrow[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) nrow[x] = ld_early4(Ng + (tid >> 2) * 64 + 16 * (tid & 3) + 4 * x);
         ok = ok && mbar_wait_ab(fullIn, ph, p.err, abort);
         BP_MARK(0);
         float G2[32];
@@ -273,12 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                 const float kv = s < it.L ? ldbf(sm + kDVO + swz2(s, ch, 64)) : 0.f;
                 *reinterpret_cast<uint16_t*>(sm + kRX + swz2(s, ch, 64)) = bfbits(ex2f(G2[e]) * kv);
             }
-            // M = N Diag(beta): row r, 16 columns per thread (MN-major rows r); N from global
+            // M = N Diag(beta): row r, 16 columns per thread (MN-major rows r)
             const int r = tid >> 2, cq = tid & 3;
-            const float4* nr = reinterpret_cast<const float4*>(Ng + r * 64 + 16 * cq);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const float4 n0 = __ldg(nr + 2 * hf), n1 = __ldg(nr + 2 * hf + 1);
+                const float4 n0 = nrow[2 * hf], n1 = nrow[2 * hf + 1];
                 const float* b = sBeta + 16 * cq + 8 * hf;
                 const float v8[8] = {n0.x * b[0], n0.y * b[1], n0.z * b[2], n0.w * b[3],
                                      n1.x * b[4], n1.y * b[5], n1.z * b[6], n1.w * b[7]};
@@ -354,11 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                 for (int e = 0; e < 8; ++e) {
                     const int u = 8 * x + e;  // token s = 32 wh + u
                     const int s = 32 * wh + u;
-                    const float vv = s < it.L ? ldbf(sm + kVt + swz2(s, j, 64)) : 0.f;
+                    uint8_t* vs = sm + kVt + swz2(s, j, 64);
+                    const float vv = s < it.L ? ldbf(vs) : 0.f;
                     dv8[e] = u < 16 ? a0[u] : a1[u - 16];
                     y8[e] = vv - (u < 16 ? y0[u] : y1[u - 16]);
-                    if (s < it.L && j < p.dv)
-                        p.dvg[((size_t)(it.t0 + s) * p.H + it.h) * p.dv + j] = __float2bfloat16_rn(dv8[e]);
+                    *reinterpret_cast<uint16_t*>(vs) = bfbits(dv8[e]);  // dv replaces v (staged)
                 }
                 const uint32_t off = (uint32_t)(j * 128 + (((4 * wh + x) ^ (j & 7)) << 4));
                 *reinterpret_cast<uint4*>(sm + kRX + off) = pk8(dv8);
@@ -422,8 +484,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                              (x | kk) != 0);
             }
             mma_commit(mma2);
+            if (it.L == 64) store_tile(&p.tdv, sm + kVt, p.dvg, it, p.H, p.dv, tid);
         }
         // ---- epilogue 2
+        float nc[32];  // lanes 64 + s: N[r][s] for r of this half (dbeta1 = sum_r N[r][s] dM[r][s])
+        if (wq >= 2) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) nc[u] = ld_early(Ng + (32 * wh + u) * 64 + (ch - 64));
+        }
         ok = ok && mbar_wait_ab(mma2, ph, p.err, abort);
         BP_MARK(4);
         if (iss && ok) {
@@ -472,15 +540,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                     *reinterpret_cast<uint4*>(mid + kMdA + 8192 + off) = lo;
                 }
             } else {
-                // dM^T (lane 64 + s): dM[r][s] into the fp32 scratch (rows r)
+                // dM^T (lane 64 + s): row s of the dM^T image (r contiguous, hi and lo) and this
+                // half's part of dbeta1_s = sum_r N[r][s] dM[r][s]
                 const int s = ch - 64;
                 float d0[16], d1[16];
                 tmem_ld16(tmem + lb + 320 + 32 * wh, d0);
                 tmem_ld16(tmem + lb + 336 + 32 * wh, d1);
                 tmem_ld_wait();
-                float* dm = reinterpret_cast<float*>(sm + kDOt);
+                float db = 0.f;
 #pragma unroll
-                for (int u = 0; u < 32; ++u) dm[(32 * wh + u) * 64 + s] = u < 16 ? d0[u] : d1[u - 16];
+                for (int x = 0; x < 4; ++x) {
+                    float v8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int u = 8 * x + e;
+                        v8[e] = u < 16 ? d0[u] : d1[u - 16];
+                        db = fmaf(nc[u], v8[e], db);
+                    }
+                    uint4 hi, lo;
+                    pk8_hilo(v8, hi, lo);
+                    const uint32_t off = (uint32_t)(s * 128 + (((4 * wh + x) ^ (s & 7)) << 4));
+                    *reinterpret_cast<uint4*>(sm + kDOt + off) = hi;
+                    *reinterpret_cast<uint4*>(sm + kDOt + 8192 + off) = lo;
+                }
+                sDb1[64 * wh + s] = db;
             }
         }
         tc_fence_before();
@@ -515,90 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                 mma_commit(mma3);
             }
         }
-        // ---- the solve's reverse, fp32 on CUDA cores (while batch 3 runs): X0 = N^T dM,
-        //      dbeta1 = diag X0, dL = -StrictTril(X0 M^T), M = N Diag(beta)
-        float* NT = reinterpret_cast<float*>(sm + kRX + 16384);  // N^T (dV^T is consumed)
-        float* X0T = reinterpret_cast<float*>(sm + kRX);
-        if (ok) {  // N^T: thread (row r, 16 columns), conflict-free stores down the columns
-            const int r = tid & 63, cb = tid >> 6;
-            const float4* nr = reinterpret_cast<const float4*>(Ng + r * 64 + 16 * cb);
-            float4 n4[4];
+        if (tid < 64 && ok) reinterpret_cast<float*>(mid + kMdB)[tid] = sDb1[tid] + sDb1[64 + tid];
+        // this thread's 16 entries of N (row tid / 4) for the solve's operand images
 #pragma unroll
-            for (int x = 0; x < 4; ++x) n4[x] = __ldg(nr + x);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int c = 16 * cb + 4 * x;
-                NT[c * 64 + r] = n4[x].x;
-                NT[(c + 1) * 64 + r] = n4[x].y;
-                NT[(c + 2) * 64 + r] = n4[x].z;
-                NT[(c + 3) * 64 + r] = n4[x].w;
-            }
-        }
-        csync();
-        const int a0 = 4 * (tid >> 4), s0 = 4 * (tid & 15);
-        if (ok) {
-            const float* dm = reinterpret_cast<const float*>(sm + kDOt);
-            float acc[4][4] = {};
-#pragma unroll 4
-            for (int r = a0; r < 64; ++r) {  // N[r][a] = 0 for r < a
-                const float4 m4 = *reinterpret_cast<const float4*>(dm + r * 64 + s0);
-                const float nv[4] = {NT[a0 * 64 + r], NT[(a0 + 1) * 64 + r], NT[(a0 + 2) * 64 + r],
-                                     NT[(a0 + 3) * 64 + r]};
-                const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-                for (int x = 0; x < 4; ++x)
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(nv[x], mv[y], acc[x][y]);
-            }
-#pragma unroll
-            for (int y = 0; y < 4; ++y)
-                *reinterpret_cast<float4*>(X0T + (s0 + y) * 64 + a0) =
-                    make_float4(acc[0][y], acc[1][y], acc[2][y], acc[3][y]);
-            if (a0 == s0) {
-#pragma unroll
-                for (int x = 0; x < 4; ++x) reinterpret_cast<float*>(mid + kMdB)[a0 + x] = acc[x][x];
-            }
-        }
-        csync();
-        if (ok) {
-            // dL[r][i] for r in [r0, r0 + 4), i in [i0, i0 + 4): -sum_{s <= i} X0[r][s] N[i][s] beta_s
-            const int r0 = a0, i0 = s0;
-            float dl[4][4] = {};
-#pragma unroll 4
-            for (int s = 0; s <= i0 + 3; ++s) {
-                const float4 x4 = *reinterpret_cast<const float4*>(X0T + s * 64 + r0);
-                const float4 n4 = *reinterpret_cast<const float4*>(NT + s * 64 + i0);
-                const float bs = sBeta[s];
-                const float xv[4] = {x4.x, x4.y, x4.z, x4.w};
-                const float nv[4] = {n4.x * bs, n4.y * bs, n4.z * bs, n4.w * bs};
-#pragma unroll
-                for (int x = 0; x < 4; ++x)
-#pragma unroll
-                    for (int y = 0; y < 4; ++y) dl[x][y] = fmaf(xv[x], nv[y], dl[x][y]);
-            }
-            // dL image: row i, columns c = 63 - r (the four columns 60 - r0 .. 63 - r0 hold rows
-            // r0 + 3 .. r0), hi and lo
-#pragma unroll
-            for (int y = 0; y < 4; ++y) {
-                const int i = i0 + y;
-                float v4[4];
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int r = r0 + 3 - x;
-                    v4[x] = (i < r && r < it.L) ? -dl[3 - x][y] : 0.f;
-                }
-                uint32_t h2[2], l2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    h2[e] = pack_bf16x2(v4[2 * e], v4[2 * e + 1]);
-                    l2[e] = pack_bf16x2(v4[2 * e] - __uint_as_float(h2[e] << 16),
-                                        v4[2 * e + 1] - __uint_as_float(h2[e] & 0xffff0000u));
-                }
-                const uint32_t off = swz(i, 60 - r0);
-                *reinterpret_cast<uint2*>(mid + kMdL + off) = make_uint2(h2[0], h2[1]);
-                *reinterpret_cast<uint2*>(mid + kMdL + 8192 + off) = make_uint2(l2[0], l2[1]);
-            }
-        }
+        for (int x = 0; x < 4; ++x) nrow[x] = ld_early4(Ng + (tid >> 2) * 64 + 16 * (tid & 3) + 4 * x);
         BP_MARK(6);
         // ---- epilogue 3: pE = (gamma^C/Gamma)*(dS_C Vt^T) and rs = diag(dS_C S_0^T)
         ok = ok && mbar_wait_ab(mma3, ph, p.err, abort);
@@ -632,6 +635,110 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                 reinterpret_cast<float*>(mid + kMdRs)[ch] = rs;
             }
         }
+        // ---- the solve's reverse on the tensor cores: Z1 = dM M^T, dL = -StrictTril(N^T Z1)
+        //      (= -StrictTril(X0 M^T) with X0 = N^T dM), both hi x hi + hi x lo + lo x hi.
+        //      Operand images in the S_0 region (batch 3 has read it): M rows i hi, lo
+        //      [0, 16 KB), N rows r hi, lo [16, 32 KB), both with the 64 columns contiguous
+        if (ok) {
+            const int r = tid >> 2, cq = tid & 3;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const float4 n0 = nrow[2 * hf], n1 = nrow[2 * hf + 1];
+                const float* b = sBeta + 16 * cq + 8 * hf;
+                const float nv[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+                float mv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mv[e] = nv[e] * b[e];
+                uint4 nh, nl, mh, ml;
+                pk8_hilo(nv, nh, nl);
+                pk8_hilo(mv, mh, ml);
+                const uint32_t off = (uint32_t)(r * 128 + (((2 * cq + hf) ^ (r & 7)) << 4));
+                *reinterpret_cast<uint4*>(sm + kSI + off) = mh;
+                *reinterpret_cast<uint4*>(sm + kSI + 8192 + off) = ml;
+                *reinterpret_cast<uint4*>(sm + kSI + 16384 + off) = nh;
+                *reinterpret_cast<uint4*>(sm + kSI + 24576 + off) = nl;
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        ok = csync_and(ok);
+        if (iss && ok) {
+            tc_fence_after();
+            // Z1^T = M dM^T: A = M rows i (K-major; rows 64..127 are not read back),
+            // B = dM^T rows s (MN-major, N = 64 tokens r)
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+                const uint64_t dA = sdesc_sw128(sb + kSI + (x == 2 ? 8192 : 0), 0, 1024);
+                const uint64_t dB = sdesc_sw128(sb + kDOt + (x == 1 ? 8192 : 0), 8192, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + 128, dA + ((kk * 32) >> 4), dB + ((kk * 2048) >> 4), idZ,
+                             (x | kk) != 0);
+            }
+            mma_commit(mma4);
+        }
+        ok = ok && mbar_wait_ab(mma4, ph, p.err, abort);
+        if (ok && wq < 2) {  // lanes i < 64: Z1^T -> bf16 hi + lo into TMEM (tokens in pairs)
+            tc_fence_after();
+            float z0[16], z1[16];
+            tmem_ld16(tmem + lb + 128 + 32 * wh, z0);
+            tmem_ld16(tmem + lb + 144 + 32 * wh, z1);
+            tmem_ld_wait();
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const float a0 = e < 8 ? z0[2 * e] : z1[2 * e - 16];
+                const float a1 = e < 8 ? z0[2 * e + 1] : z1[2 * e - 15];
+                hi[e] = pack_bf16x2(a0, a1);
+                lo[e] = pack_bf16x2(a0 - __uint_as_float(hi[e] << 16), a1 - __uint_as_float(hi[e] & 0xffff0000u));
+            }
+            tmem_st16(tmem + lb + 192 + 16 * wh, hi);
+            tmem_st16(tmem + lb + 224 + 16 * wh, lo);
+            tmem_st_wait();
+        }
+        tc_fence_before();
+        ok = csync_and(ok);
+        if (iss && ok) {
+            tc_fence_after();
+            // dL^T = Z1^T N: A = Z1^T from TMEM (K = 64 tokens r), B = N rows r (MN-major)
+#pragma unroll
+            for (int x = 0; x < 3; ++x) {
+                const uint64_t dB = sdesc_sw128(sb + kSI + 16384 + (x == 1 ? 8192 : 0), 8192, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ts(tmem + 256, tmem + (x == 2 ? 224 : 192) + 8 * kk, dB + ((kk * 2048) >> 4),
+                                idZ, (x | kk) != 0);
+            }
+            mma_commit(mma5);
+        }
+        ok = ok && mbar_wait_ab(mma5, ph, p.err, abort);
+        if (ok && wq < 2) {
+            // lane i: row i of the dL image, columns c = 63 - r' (hi, lo): dL[r'][i] = -D[i][r']
+            // for i < r' < L
+            tc_fence_after();
+            const int i = ch;
+            float d0[16], d1[16];
+            tmem_ld16(tmem + lb + 256 + 32 * wh, d0);
+            tmem_ld16(tmem + lb + 272 + 32 * wh, d1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float v8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int u = 31 - 8 * k - e;  // r' = 32 wh + u
+                    const int rr = 32 * wh + u;
+                    const float d = u < 16 ? d0[u] : d1[u - 16];
+                    v8[e] = (i < rr && rr < it.L) ? -d : 0.f;
+                }
+                uint4 hi, lo;
+                pk8_hilo(v8, hi, lo);
+                const uint32_t off = (uint32_t)(i * 128 + (((4 - 4 * wh + k) ^ (i & 7)) << 4));
+                *reinterpret_cast<uint4*>(mid + kMdL + off) = hi;
+                *reinterpret_cast<uint4*>(mid + kMdL + 8192 + off) = lo;
+            }
+        }
+        if (ok && it.L < 64) store_tile(&p.tdv, sm + kVt, p.dvg, it, p.H, p.dv, tid);
         tc_fence_before();
         fence_async_smem();  // the next item's copies overwrite what was written here
         ok = csync_and(ok);
@@ -720,6 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
         const uint32_t ph = iter & 1;
         const uint8_t* mid = p.mid + (size_t)item * kMdBytes;
         if (iss) {
+            bulk_wait_read0();  // the previous item's output stores have read the stack region
             inflight = 0x3u;
             inflight_ph = ph;
             mbar_expect_tx(fullIn, 49152);
@@ -827,6 +935,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
         BP_MARK(13);
         float dG[32];
         float lastp = 0.f;
+        const float rs_i = ld_early(reinterpret_cast<const float*>(mid + kMdRs) + ch);
+        const float db1 = ld_early(reinterpret_cast<const float*>(mid + kMdB) + (tid & 63));
         if (ok) {
             tc_fence_after();
             const float* pQ = reinterpret_cast<const float*>(mid + kMdQ) + ch;
@@ -837,11 +947,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
                 const int r0 = 32 * wh + 16 * g, R0 = 2 * wh + g;
                 float pq16[16], pp16[16], pe16[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) pq16[u] = __ldg(pQ + (r0 + u) * 128);
+                for (int u = 0; u < 16; ++u) pq16[u] = ld_early(pQ + (r0 + u) * 128);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) pp16[u] = __ldg(pP + (r0 + u) * 128);
+                for (int u = 0; u < 16; ++u) pp16[u] = ld_early(pP + (r0 + u) * 128);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) pe16[u] = __ldg(pE + (r0 + u) * 128);
+                for (int u = 0; u < 16; ++u) pe16[u] = ld_early(pE + (r0 + u) * 128);
+                BP_MARK(16);
                 float dqd[16], ee[16], ff[16], t16[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) { dqd[u] = 0.f; ee[u] = 0.f; ff[u] = 0.f; }
@@ -860,6 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
                         ee[u] = fmaf(f, t16[e], ee[u]);
                     }
                 }
+                BP_MARK(17);
                 // D^T: element e of columns r0 .. of block R is token r0 + e
                 for (int R = R0; R < 4; ++R) {
                     const float rho = sRho[R * 128 + ch];
@@ -868,6 +980,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
 #pragma unroll
                     for (int e = 0; e < 16; ++e) ff[e] = fmaf(ex2f(rho - G2[16 * g + e]), t16[e], ff[e]);
                 }
+                BP_MARK(18);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int r = r0 + u;
@@ -881,30 +994,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
                     dG[16 * g + u] = live ? kv * (pp + b * ee[u] - ff[u] - pe) + qv * dq : 0.f;
                     lastp = fmaf(kv, pe, lastp);
                     t16[u] = kv * ee[u];  // dbeta's E term, summed over channels below
-                    if (live && ch < p.dk) {
-                        const size_t o = ((size_t)(it.t0 + r) * p.H + it.h) * p.dk + ch;
-                        p.dq[o] = __float2bfloat16_rn(dq);
-                        p.dkg[o] = __float2bfloat16_rn(dkv);
-                    }
+                    const uint32_t o = swz2(r, ch, 64);  // dq, dk staged (the stacks are consumed)
+                    *reinterpret_cast<uint16_t*>(sm + kKT + o) = bfbits(dq);
+                    *reinterpret_cast<uint16_t*>(sm + kKT + 16384 + o) = bfbits(dkv);
                 }
+                BP_MARK(19);
                 // sum over the 32 channels of this warp, then over the four warps
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float v = t16[u];
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) sDb[wq * 64 + r0 + u] = v;
+                {
+                    const float v = warp_sum16(t16, lane);
+                    if ((lane & 1) == 0) sDb[wq * 64 + r0 + (lane >> 1)] = v;
                 }
+                BP_MARK(20);
             }
             sLast[wh * 128 + ch] = lastp;
         }
         BP_MARK(14);
         csync();
+        BP_MARK(21);
         float dAp = 0.f;
         if (ok) {
             // dG of the chunk's last row L - 1 also takes sum_r K pE + gamma^C rs
-            const float last = sLast[ch] + sLast[128 + ch] +
-                               ex2f(sGlast[ch]) * __ldg(reinterpret_cast<const float*>(mid + kMdRs) + ch);
+            const float last = sLast[ch] + sLast[128 + ch] + ex2f(sGlast[ch]) * rs_i;
             const int ul = it.L - 1 - 32 * wh;
             // reverse cumulative sum over this half, then the second half's total
             float acc = 0.f;
@@ -917,6 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
             if (wh == 1) sTot[ch] = acc;
         }
         csync();
+        BP_MARK(22);
         if (ok) {
             const float add = wh == 0 ? sTot[ch] : 0.f;
 #pragma unroll
@@ -927,13 +1038,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
                     const float sg = __fdividef(1.f, 1.f + __expf(-x));
                     const float dx = (dG[u] + add) * p.g_min * sg * (1.f - sg);
                     dAp = fmaf(dx, x, dAp);
-                    if (ch < p.dk)
-                        p.dz[((size_t)(it.t0 + r) * p.H + it.h) * p.dk + ch] = __float2bfloat16_rn(dx * eA);
+                    *reinterpret_cast<uint16_t*>(sm + kQH + swz2(r, ch, 64)) = bfbits(dx * eA);
                 }
             }
             if (tid < 64 && tid < it.L) {
-                const float db = __ldg(reinterpret_cast<const float*>(mid + kMdB) + tid) + sDb[tid] +
-                                 sDb[64 + tid] + sDb[128 + tid] + sDb[192 + tid];
+                const float db = db1 + sDb[tid] + sDb[64 + tid] + sDb[128 + tid] + sDb[192 + tid];
                 p.dbeta[(size_t)(it.t0 + tid) * p.H + it.h] = __float2bfloat16_rn(db);
             }
         }
@@ -941,6 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) dAp += __shfl_xor_sync(0xffffffffu, dAp, o);
         if (lane == 0) sRed[warp] = dAp;
+        BP_MARK(23);
         tc_fence_before();
         fence_async_smem();
         ok = csync_and(ok);
@@ -949,6 +1059,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
             for (int w = 0; w < 8; ++w) s += sRed[w];
             p.dA_item[item] = s;
         }
+        if (ok) {
+            store_tile(&p.tdq, sm + kKT, p.dq, it, p.H, p.dk, tid);
+            store_tile(&p.tdk, sm + kKT + 16384, p.dkg, it, p.H, p.dk, tid);
+            store_tile(&p.tdz, sm + kQH, p.dz, it, p.H, p.dk, tid);
+        }
+        csync();  // a short chunk's copies have read the staged tiles
         BP_MARK(15);
         if (!ok) break;
     }
@@ -994,7 +1110,11 @@ cudaError_t launch_bwd_items_tc(const BwdArgs& a, void* fwd_ws, const void* bimg
         !fwdtc::make_map(&p.tk, a.k, a.T_total, a.H, a.dk, 64) ||
         !fwdtc::make_map(&p.tv, a.v, a.T_total, a.H, a.dv, 64) ||
         !fwdtc::make_map(&p.tz, a.z, a.T_total, a.H, a.dk, 64) ||
-        !fwdtc::make_map(&p.tdo, a.dout, a.T_total, a.H, a.dv, 64))
+        !fwdtc::make_map(&p.tdo, a.dout, a.T_total, a.H, a.dv, 64) ||
+        !fwdtc::make_map(&p.tdq, a.dq, a.T_total, a.H, a.dk, 64) ||
+        !fwdtc::make_map(&p.tdk, a.dk_, a.T_total, a.H, a.dk, 64) ||
+        !fwdtc::make_map(&p.tdz, a.dz, a.T_total, a.H, a.dk, 64) ||
+        !fwdtc::make_map(&p.tdv, a.dv_, a.T_total, a.H, a.dv, 64))
         return cudaErrorInvalidValue;
     p.beta = static_cast<const __nv_bfloat16*>(a.beta);
     p.v = static_cast<const __nv_bfloat16*>(a.v);
