@@ -146,14 +146,16 @@ kda_status_t kda_fwd_chunked_softplus(const void *q, const void *k, const void *
  *   dq, dk, dz : [T_total, H, dk] io_dt     dv : [T_total, H, dv] io_dt
  *   dbeta      : [T_total, H] io_dt         dA_log : [H] fp32 (summed over sequences)
  *   dS0        : [N, H, dk, dv] fp32, or NULL when not wanted
- * Other arguments as kda_fwd_chunked (same inputs, S0 may be NULL).  The workspace
- * (kda_bwd_workspace_size bytes) holds, per 64-token chunk and head, the state at the chunk
- * start, the state's gradient at the chunk end and the chunk's transfer matrices, plus
- * per-CTA scratch.  On CUDA cores in fp32, parallel over chunks: every chunk's forward and
- * backward maps on the state are formed at once, two short chains over each sequence's
- * chunks give the state and its gradient at every chunk boundary, and every (chunk, head)
- * then applies the reverse rules token by token (not the tensor-core chunk form).  Correct
- * for every shape kda_fwd_chunked takes.  Deterministic.
+ * Other arguments as kda_fwd_chunked (same inputs, S0 may be NULL).
+ * bf16 problems (dk, dv in {64, 128}) take the chunk form on the tcgen05 tensor cores: the
+ * tensor-core forward (its chunk packages kept) and a reversed chain give the state and its
+ * gradient at every chunk boundary as bf16 operand images, then two per-chunk kernels form
+ * every gradient.  fp32 problems run on CUDA cores in fp32, parallel over chunks: every
+ * chunk's forward and backward maps on the state are formed at once, two short chains give
+ * the state and its gradient at every chunk boundary, and every (chunk, head) applies the
+ * reverse rules token by token.  The workspace (kda_bwd_workspace_size bytes, the larger of
+ * the two layouts) holds those per-(chunk, head) blocks.  Correct for every shape
+ * kda_fwd_chunked takes.  Deterministic.
  */
 size_t kda_bwd_workspace_size(int64_t T_total, int N, int H, int dk, int dv);
 kda_status_t kda_bwd(const void *q, const void *k, const void *v, const void *beta,
