@@ -214,6 +214,15 @@ def run_ours(args, rank, world, local_rank, dist):
     H, T = sp.H, sp.T
     d = sp.to_device(dev)
     stream = torch.cuda.current_stream(dev)
+    if args.backward_only:
+        bw = bench_backward(dev, stream, d, sp, peaks, reps=args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": "kda_bwd_tokens_per_s", "value": bw["tokens_per_s"],
+                              "unit": "tokens/s", "ms_per_call": bw["ms_per_call"],
+                              "config": {"workload": WORKLOAD, "T": T, "H": H},
+                              "kernel_ms": bw["kernel_ms"], "note": "backward only (profiler case)"}),
+                  flush=True)
+        return
     S_out = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
     o = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
     ws_bytes = kda.workspace_size(T, 1, H, D, D, torch.bfloat16)
@@ -709,6 +718,9 @@ def main():
                     help="time the forward step only: no end-to-end, output-gate, gate "
                          "comparison, backward, quantile-balancing, other-workload, decode or "
                          "CPU blocks (for profiler captures; not a bench line)")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time the backward only, --steps calls after one untimed call (for "
+                         "profiler captures; not a bench line)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="run the forward workload with this many tokens instead of 65536 "
                          "(a smaller case for profiler captures; not a bench line)")
