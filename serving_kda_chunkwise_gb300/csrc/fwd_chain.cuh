@@ -14,6 +14,7 @@
 //   E2    S^T <- S^T Diag(gamma^C) + dS^T in fp32 registers; bf16 copy of S^T into TMEM
 //   MMA3  O^T += [Vt_hi | Vt_lo | Vt_hi]^T [A_hi; A_hi; A_lo]^T  (into D1's columns 64..127)
 //   E3    O^T -> bf16 -> o (for each token, the 32 lanes of a warp store 64 contiguous bytes)
+// With no output wanted (the forward of a backward pass), neither the A tile, MMA3 nor E3 runs.
 // The state update takes three bf16 products (hi x hi, lo x hi, hi x lo) so that the fp32
 // state is not limited by bf16 rounding of K~ or Vt; the output takes the same three.
 // No intermediate of the chain goes through shared memory, so a chain step is
@@ -169,6 +170,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     const uint32_t tmem = *tmem_slot;
     const int n_chains = p.N * p.H;
     const int G = ncta;
+    const bool want_o = p.o != nullptr;
 
     if (tid == kMmaT) {
         // ------------------------------------------------------------ MMA thread
@@ -214,6 +216,10 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 }
                 mma_commit(&mma2[st]);
                 CH_MARK(5);
+                if (!want_o) {  // no output: neither the A tile nor MMA3
+                    if (p.fused) *s_landed = g + 1;
+                    continue;
+                }
                 if (!mbar_wait_ab(fullAT, g & 1, p.err, abort)) { ok = false; break; }
                 CH_MARK(6);
                 if (p.fused) *s_landed = g + 1;  // every part of chunk g is in shared memory
@@ -237,7 +243,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     //   lane 2: K~ hi + lo, two stages, free once MMA2 of chunk g - 2 completed;
     //   lane 3: A hi + lo, one stage, free once MMA3 of chunk g - 1 completed.
     int last_ph[2] = {-1, -1};  // the phase parity a drain must let land, per stage
-    const int cpart = (warp == kCopyT / 32 && lane < 4) ? lane : -1;
+    const int cpart = (warp == kCopyT / 32 && lane < (want_o ? 4 : 3)) ? lane : -1;
     if (cpart >= 0) {
         uint32_t g = 0;
         bool ok = true;
@@ -327,6 +333,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
         // token the 32 lanes of a warp write 64 contiguous bytes); rows past the sequence end
         // belong to the next sequence and are skipped
         auto store_out = [&](uint32_t gg, int64_t t0, const Chain& c) -> bool {
+            if (!want_o) return true;
             if (!mbar_wait_ab(&mma3[gg & 1], (gg >> 1) & 1, p.err, abort)) return false;
             tc_fence_after();
             float o0[16], o1[16];
