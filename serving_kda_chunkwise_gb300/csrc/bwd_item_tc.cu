@@ -772,7 +772,8 @@ constexpr uint32_t kDAi = 147456; // dA image hi, lo (+8192)
 constexpr uint32_t kDLi = 163840; // dL image hi, lo (+8192)
 constexpr uint32_t kDMisc = 180224;  // beta [64], tot [128], glast [128], rho [4][128],
                                      // last [2][128], dbeta [4][64], red [8]
-constexpr uint32_t kDBars = kDMisc + 6144;
+constexpr uint32_t kDG = kDMisc + 6144;  // G (log2 units) fp32 [64 rows][128 channels]
+constexpr uint32_t kDBars = kDG + 32768;
 constexpr uint32_t kDecaySmem = kDBars + 128 + 1024;
 static_assert(kDecaySmem <= 232448, "decay kernel exceeds the shared-memory limit");
 // TMEM: D(dA, K) per block S at [kOffS[S], + 64 - 16 S), D(dL, K) at 160 + the same, and
@@ -859,26 +860,59 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
             if (wh == 1) sGlast[ch] = G2[31];
             sRho[(2 * wh) * 128 + ch] = G2[8];
             sRho[(2 * wh + 1) * 128 + ch] = G2[24];
+            float* gs = reinterpret_cast<float*>(sm + kDG) + 32 * wh * 128 + ch;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) gs[e * 128] = G2[e];
         } else {
             csync();
         }
         csync();
         BP_MARK(11);
         if (ok) {
-            // K~ (rows s), Q^ and K^b (rows 63 - r), this thread's channel and half
-            const float rhoA = sRho[(2 * wh) * 128 + ch], rhoB = sRho[(2 * wh + 1) * 128 + ch];
+            // K~ (rows s), Q^ and K^b (rows 63 - r): thread = (row, 8 channels), four of them,
+            // 16-byte chunks in and out
+            const float* gs = reinterpret_cast<const float*>(sm + kDG);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int r = 32 * wh + e;
-                const float rho = e < 16 ? rhoA : rhoB;
-                const bool live = r < it.L;
-                const float kv = live ? ldbf(sm + kKt + swz2(r, ch, 64)) : 0.f;
-                const float qv = live ? ldbf(sm + kQt + swz2(r, ch, 64)) : 0.f;
-                const float up = ex2f(G2[e] - rho), dn = ex2f(rho - G2[e]);
-                const uint32_t o = swz2(r, ch, 64), orv = swz2(63 - r, ch, 64);
-                st_hilo(sm + kKT + o, sm + kKT + 16384 + o, kv * dn);
-                st_hilo(sm + kQH + orv, sm + kQH + 16384 + orv, qv * up);
-                st_hilo(sm + kKB + orv, sm + kKB + 16384 + orv, sBeta[r] * kv * up);
+            for (int x = 0; x < 4; ++x) {
+                const int u = tid + 256 * x, r = u >> 4, c = u & 15, blk = c >> 3, cc = c & 7;
+                const int c0 = 8 * c;
+                const uint32_t oin = blk * 8192 + r * 128 + ((cc ^ (r & 7)) << 4);
+                const int rv = 63 - r;
+                const uint32_t orv = blk * 8192 + rv * 128 + ((cc ^ (rv & 7)) << 4);
+                float kv[8], qv[8];
+                if (r < it.L) {
+                    ld8(sm + kKt + oin, kv);
+                    ld8(sm + kQt + oin, qv);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { kv[e] = 0.f; qv[e] = 0.f; }
+                }
+                const float4 g0 = *reinterpret_cast<const float4*>(gs + r * 128 + c0);
+                const float4 g1 = *reinterpret_cast<const float4*>(gs + r * 128 + c0 + 4);
+                const float* rh = sRho + (r >> 4) * 128 + c0;
+                const float4 h0 = *reinterpret_cast<const float4*>(rh);
+                const float4 h1 = *reinterpret_cast<const float4*>(rh + 4);
+                const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                const float b = sBeta[r];
+                float kt[8], qh[8], kb[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float up = ex2f(gv[e] - hv[e]), dn = ex2f(hv[e] - gv[e]);
+                    kt[e] = kv[e] * dn;
+                    qh[e] = qv[e] * up;
+                    kb[e] = b * kv[e] * up;
+                }
+                uint4 hi, lo;
+                pk8_hilo(kt, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kKT + oin) = hi;
+                *reinterpret_cast<uint4*>(sm + kKT + 16384 + oin) = lo;
+                pk8_hilo(qh, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kQH + orv) = hi;
+                *reinterpret_cast<uint4*>(sm + kQH + 16384 + orv) = lo;
+                pk8_hilo(kb, hi, lo);
+                *reinterpret_cast<uint4*>(sm + kKB + orv) = hi;
+                *reinterpret_cast<uint4*>(sm + kKB + 16384 + orv) = lo;
             }
         }
         fence_async_smem();
