@@ -299,7 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                     tmem_ld16(tmem + lb + kTD1 + 32 * wg, z0);
                     tmem_ld16(tmem + lb + kTD1 + 32 * wg + 16, z1);
                     tmem_ld_wait();
-                    uint8_t* zimg = blk + kBiDV + j * 128;  // dVt^T row j
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         uint32_t hi[8], lo[8];
@@ -313,21 +312,38 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                         }
                         tmem_st8(tmem + lb + kTZ + 16 * wg + 8 * hf, hi);
                         tmem_st8(tmem + lb + kTZlo + 16 * wg + 8 * hf, lo);
-                        // tokens 32 wg + 16 hf + 8 x (x = 0, 1) are chunk 4 wg + 2 hf + x of the
-                        // row; the image holds +Z, so hi and lo are the negated words
-                        constexpr uint32_t kSign = 0x80008000u;
-                        st_swz_pair(zimg, 4 * wg + 2 * hf, j,
-                                    make_uint4(hi[0] ^ kSign, hi[1] ^ kSign, hi[2] ^ kSign, hi[3] ^ kSign),
-                                    make_uint4(hi[4] ^ kSign, hi[5] ^ kSign, hi[6] ^ kSign, hi[7] ^ kSign));
-                        st_swz_pair(zimg + 16384, 4 * wg + 2 * hf, j,
-                                    make_uint4(lo[0] ^ kSign, lo[1] ^ kSign, lo[2] ^ kSign, lo[3] ^ kSign),
-                                    make_uint4(lo[4] ^ kSign, lo[5] ^ kSign, lo[6] ^ kSign, lo[7] ^ kSign));
                     }
                     tmem_st_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&z_ready[st]);
+                // dVt^T row j into the image block, read back from TMEM while MMA2 runs: tokens
+                // 32 wg + 8 x are chunk 4 wg + x of the row; TMEM holds -Z, so the words are
+                // negated
+                if (okc) {
+                    float fh[16], fl[16];
+                    tmem_ld16(tmem + lb + kTZ + 16 * wg, fh);
+                    tmem_ld16(tmem + lb + kTZlo + 16 * wg, fl);
+                    tmem_ld_wait();
+                    constexpr uint32_t kSign = 0x80008000u;
+                    uint32_t wh[16], wl[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        wh[e] = __float_as_uint(fh[e]) ^ kSign;
+                        wl[e] = __float_as_uint(fl[e]) ^ kSign;
+                    }
+                    uint8_t* zimg = blk + kBiDV + j * 128;
+#pragma unroll
+                    for (int pr = 0; pr < 2; ++pr) {
+                        st_swz_pair(zimg, 4 * wg + 2 * pr, j,
+                                    make_uint4(wh[8 * pr], wh[8 * pr + 1], wh[8 * pr + 2], wh[8 * pr + 3]),
+                                    make_uint4(wh[8 * pr + 4], wh[8 * pr + 5], wh[8 * pr + 6], wh[8 * pr + 7]));
+                        st_swz_pair(zimg + 16384, 4 * wg + 2 * pr, j,
+                                    make_uint4(wl[8 * pr], wl[8 * pr + 1], wl[8 * pr + 2], wl[8 * pr + 3]),
+                                    make_uint4(wl[8 * pr + 4], wl[8 * pr + 5], wl[8 * pr + 6], wl[8 * pr + 7]));
+                    }
+                }
                 // ---- E2: dS^T <- dS'^T Diag(gamma^C) + D2; bf16 copy for the next MMA1
                 okc = okc && mbar_wait_ab(&mma2[st], ph, p.err, abort);
                 if (okc) {

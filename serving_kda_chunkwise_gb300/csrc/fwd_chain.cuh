@@ -435,8 +435,6 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                     tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg, x0);
                     tmem_ld16(tmem + lb + kTD1 + 128 * st + 32 * wg + 16, x1);
                     tmem_ld_wait();
-                    // backward pass: Vt^T row j, tokens 32 wg + 16 hf + 8 x in chunk 4 wg + 2 hf + x
-                    uint8_t* vimg = p.bimg ? bimg_of(t) + bwdtc::kBiV + j * 128 : nullptr;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         uint32_t hi[8], lo[8];
@@ -450,18 +448,36 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                         }
                         tmem_st8(tmem + lb + kTV + 16 * wg + 8 * hf, hi);
                         tmem_st8(tmem + lb + kTVlo + 16 * wg + 8 * hf, lo);
-                        if (vimg) {
-                            st_swz_pair(vimg, 4 * wg + 2 * hf, j, make_uint4(hi[0], hi[1], hi[2], hi[3]),
-                                        make_uint4(hi[4], hi[5], hi[6], hi[7]));
-                            st_swz_pair(vimg + 16384, 4 * wg + 2 * hf, j, make_uint4(lo[0], lo[1], lo[2], lo[3]),
-                                        make_uint4(lo[4], lo[5], lo[6], lo[7]));
-                        }
                     }
                     tmem_st_wait();
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&vt_ready[st]);
+                // backward pass: Vt^T row j into the image block, read back from TMEM while MMA2
+                // runs (tokens 32 wg + 8 x form chunk 4 wg + x of the row)
+                if (p.bimg && okc) {
+                    float fh16[16], fl16[16];
+                    tmem_ld16(tmem + lb + kTV + 16 * wg, fh16);
+                    tmem_ld16(tmem + lb + kTVlo + 16 * wg, fl16);
+                    tmem_ld_wait();
+                    uint32_t wh16[16], wl16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        wh16[e] = __float_as_uint(fh16[e]);
+                        wl16[e] = __float_as_uint(fl16[e]);
+                    }
+                    uint8_t* vimg = bimg_of(t) + bwdtc::kBiV + j * 128;
+#pragma unroll
+                    for (int pr = 0; pr < 2; ++pr) {
+                        st_swz_pair(vimg, 4 * wg + 2 * pr, j,
+                                    make_uint4(wh16[8 * pr], wh16[8 * pr + 1], wh16[8 * pr + 2], wh16[8 * pr + 3]),
+                                    make_uint4(wh16[8 * pr + 4], wh16[8 * pr + 5], wh16[8 * pr + 6], wh16[8 * pr + 7]));
+                        st_swz_pair(vimg + 16384, 4 * wg + 2 * pr, j,
+                                    make_uint4(wl16[8 * pr], wl16[8 * pr + 1], wl16[8 * pr + 2], wl16[8 * pr + 3]),
+                                    make_uint4(wl16[8 * pr + 4], wl16[8 * pr + 5], wl16[8 * pr + 6], wl16[8 * pr + 7]));
+                    }
+                }
                 if (rec) CH_MARK(10);
                 // ---- E3 of the previous chunk, while MMA2 of this one runs
                 if (t > 0 && !store_out(g - 1, t0 - kC, c)) { ok = false; break; }
