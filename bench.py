@@ -551,8 +551,10 @@ def bench_backward(dev, stream, d, sp, peaks, reps=1):
     gbs = nbytes / (ms / 1e3) / 1e9
     return {"ms_per_call": ms, "tokens_per_s": T_ / (ms / 1e3), "T": T_, "H": H_, "d": dk,
             "algorithmic_GB": nbytes / 1e9, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
-            "form": "parallel over 64-token chunks on CUDA cores: per-chunk forward maps and "
-                    "gradient transfer matrices, two short chains over chunks, per-chunk reverse",
+            "form": "the chunk form on the tcgen05 tensor cores: the forward (two-launch, "
+                    "packages kept) and a reversed chain write each chunk's start state, end "
+                    "gradient, Vt and dVt as bf16 operand images; a state kernel and a decay "
+                    "kernel form every gradient per (chunk, head)",
             "kernel_ms": split}
 
 
