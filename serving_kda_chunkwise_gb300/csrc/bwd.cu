@@ -41,6 +41,9 @@
 //                     the chunk's checkpoint by 8-token sub-blocks (per-CTA scratch)
 //   bwd_dA_kernel     dA_log[h] = the per-(chunk, head) partial sums in chunk order
 //                     (deterministic)
+#include <map>
+#include <mutex>
+
 #include "bwd_tc_layout.cuh"
 #include "kda_common.cuh"
 #include "kda_internal.h"
@@ -808,6 +811,29 @@ cudaError_t launch_t(const BwdParams& p, int grid_nh, int grid_items, cudaStream
     return cudaGetLastError();
 }
 
+// A second stream (and its fork and join events) per device, created on first use.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaError_t ok = cudaErrorNotReady;
+    std::mutex mu;
+};
+SideStream& side_stream() {
+    static std::mutex mu;
+    static std::map<int, SideStream*> streams;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    SideStream*& ss = streams[dev];
+    if (!ss) {
+        ss = new SideStream;
+        ss->ok = cudaStreamCreateWithFlags(&ss->s, cudaStreamNonBlocking);
+        if (ss->ok == cudaSuccess) ss->ok = cudaEventCreateWithFlags(&ss->fork, cudaEventDisableTiming);
+        if (ss->ok == cudaSuccess) ss->ok = cudaEventCreateWithFlags(&ss->join, cudaEventDisableTiming);
+    }
+    return *ss;
+}
+
 int sm_count() {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -907,8 +933,22 @@ cudaError_t launch_bwd(const BwdArgs& a) {
         f.dev_err = a.dev_err;
         f.stream = a.stream;
         f.bimg = ws + w.bimg;
-        e = launch_fwd_tc(f);
-        if (e == cudaSuccess) e = launch_bwd_chain_tc(a, ws + w.fwd, ws + w.bimg, a.stream);
+        // The gradient chain needs the packages and dout but nothing of the forward's chain,
+        // so it runs on a second stream next to it (each holds one CTA per chain; together
+        // 2 C of the SMs), forked once the intra stage is enqueued and joined before the
+        // per-chunk kernels.  The enqueue is serialised, so concurrent calls do not mix up
+        // the fork and join events.
+        SideStream& ss = side_stream();
+        std::lock_guard<std::mutex> lock(ss.mu);
+        e = ss.ok;
+        if (e == cudaSuccess) {
+            f.after_intra = ss.fork;
+            e = launch_fwd_tc(f);
+        }
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ss.s, ss.fork, 0);
+        if (e == cudaSuccess) e = launch_bwd_chain_tc(a, ws + w.fwd, ws + w.bimg, ss.s);
+        if (e == cudaSuccess) e = cudaEventRecord(ss.join, ss.s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(a.stream, ss.join, 0);
         if (e == cudaSuccess)
             e = launch_bwd_items_tc(a, ws + w.fwd, ws + w.bimg, ws + w.mid, p.dA_item, a.stream);
     } else {

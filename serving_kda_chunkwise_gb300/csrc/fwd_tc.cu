@@ -390,6 +390,10 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    if (a.after_intra) {
+        e = cudaEventRecord(a.after_intra, a.stream);
+        if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kChainSmem);
     if (e != cudaSuccess) return e;

@@ -32,6 +32,9 @@ struct FwdArgs {
     // receive S_0, Vt and N of every chunk; selects the two-launch form, which also leaves
     // every (chunk, head) package in the workspace
     void* bimg;
+    // two-launch form, optional: recorded on `stream` once the intra stage is enqueued (the
+    // backward starts its gradient chain on a second stream from there)
+    cudaEvent_t after_intra;
 };
 
 struct BwdArgs {
