@@ -383,20 +383,55 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             // in eight 16-byte chunks (padding rows and columns are zeros)
             auto store_ckpt = [&](int t) {
                 if (!p.bimg) return;
-                uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + j * 128;
+                if (want_o) {  // direct 32-byte stores of swizzle-adjacent chunk pairs
+                    uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + j * 128;
 #pragma unroll
-                for (int c8 = 0; c8 < 8; c8 += 2) {
-                    float v0[8], v1[8];
+                    for (int c8 = 0; c8 < 8; c8 += 2) {
+                        float v0[8], v1[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        v0[e] = S[8 * c8 + e];
-                        v1[e] = S[8 * c8 + 8 + e];
+                        for (int e = 0; e < 8; ++e) {
+                            v0[e] = S[8 * c8 + e];
+                            v1[e] = S[8 * c8 + 8 + e];
+                        }
+                        uint4 h0, l0, h1, l1;
+                        pk8_hilo(v0, h0, l0);
+                        pk8_hilo(v1, h1, l1);
+                        st_swz_pair(dst, c8, j, h0, h1);
+                        st_swz_pair(dst + 32768, c8, j, l0, l1);
                     }
-                    uint4 h0, l0, h1, l1;
-                    pk8_hilo(v0, h0, l0);
-                    pk8_hilo(v1, h1, l1);
-                    st_swz_pair(dst, c8, j, h0, h1);
-                    st_swz_pair(dst + 32768, c8, j, l0, l1);
+                    return;
+                }
+                // No output wanted: the A-tile buffer is free, 2 KB per epilogue warp.  The
+                // warp's 32 rows (row j = this lane, 32 (w mod 4) + lane of key block wg) are
+                // 4 KB contiguous in the image: 16 rows at a time are written into the buffer
+                // in the image's own swizzled order, then copied out as 512-byte contiguous
+                // stores (four 128-byte lines per warp store instead of 32)
+                uint8_t* stage = sm + kChAT + warp * 2048;
+                uint8_t* rows = bimg_of(t) + bwdtc::kBiS + wg * 16384 + (32 * q) * 128;
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {      // hi, lo
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {  // rows 16 half .. + 15 of the warp
+                        if ((lane >> 4) == half) {
+#pragma unroll
+                            for (int c8 = 0; c8 < 8; ++c8) {
+                                float v8[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) v8[e] = S[8 * c8 + e];
+                                uint4 hi, lo;
+                                pk8_hilo(v8, hi, lo);
+                                *reinterpret_cast<uint4*>(stage + (lane & 15) * 128 + ((c8 ^ (lane & 7)) << 4)) =
+                                    part ? lo : hi;
+                            }
+                        }
+                        __syncwarp();
+                        uint8_t* dst = rows + part * 32768 + half * 2048;
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+                            *reinterpret_cast<uint4*>(dst + (x * 32 + lane) * 16) =
+                                *reinterpret_cast<const uint4*>(stage + (x * 32 + lane) * 16);
+                        __syncwarp();
+                    }
                 }
             };
             if (c.nch > 0) {
