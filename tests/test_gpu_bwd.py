@@ -34,11 +34,12 @@ def _close(d, ref, dtype, what):
         assert bf16_rms_err(d, ref) <= BF16_RMS_TOL, what
 
 
-def _run(kda, lengths, H, d, dtype, seed, with_dS=True, dv=None):
+def _run(kda, lengths, H, d, dtype, seed, with_dS=True, dv=None, g_min=None):
     import torch
     dv = d if dv is None else dv
+    kw = {} if g_min is None else {"g_min": g_min}
     inp = inputs.forward_inputs(seed=seed, lengths=lengths, H=H, dk=d, dv=dv, dtype=dtype,
-                                with_state=True)
+                                with_state=True, **kw)
     rng = np.random.default_rng(seed + 1)
     T, N = int(inp.cu_seqlens[-1]), len(lengths)
     do = inputs.store(rng.standard_normal((T, H, dv)).astype(np.float32), dtype)
@@ -78,11 +79,21 @@ def test_matches_oracle(kda, dtype, d):
     _run(kda, [70, 0, 129, 1], H=2, d=d, dtype=dtype, seed=71)
 
 
-@pytest.mark.parametrize("dtype,dk,dv", [("f32", 64, 128), ("f32", 128, 64), ("bf16", 64, 64)])
+@pytest.mark.parametrize("dtype,dk,dv", [("f32", 64, 128), ("f32", 128, 64), ("bf16", 64, 64),
+                                         ("bf16", 128, 64), ("bf16", 64, 128)])
 def test_other_head_sizes(kda, dtype, dk, dv):
-    """d_k != d_v (the state's rows and columns split differently over the threads) and bf16
-    at d = 64."""
+    """d_k != d_v (the state's rows and columns split differently over the threads; on the
+    tensor-core path the padded key or value channels of the operand images are zeros) and
+    bf16 at d = 64."""
     _run(kda, [90, 17], H=2, d=dk, dv=dv, dtype=dtype, seed=75)
+
+
+@pytest.mark.parametrize("g_min", [-3.0, -6.0])
+def test_gate_bound_range(kda, g_min):
+    """bf16 at the ends of the gate bounds used by the benchmark's sweep: at g_min = -6 a
+    16-token block spans decay factors up to e^{48} on either side of its reference, the range
+    the decayed products' references are built for."""
+    _run(kda, [130, 64], H=2, d=128, dtype="bf16", seed=77, g_min=g_min)
 
 
 def test_without_final_state_gradient(kda):
