@@ -1015,13 +1015,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
                     for (int e = 0; e < 16; ++e) ff[e] = fmaf(ex2f(rho - G2[16 * g + e]), t16[e], ff[e]);
                 }
                 BP_MARK(18);
+                // this group's k, q and beta first (loads after the staging stores below may
+                // not be hoisted above them)
+                float k16[16], q16[16], b16[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int r = r0 + u;
                     const bool live = r < it.L;
-                    const float kv = live ? ldbf(sm + kKt + swz2(r, ch, 64)) : 0.f;
-                    const float qv = live ? ldbf(sm + kQt + swz2(r, ch, 64)) : 0.f;
-                    const float b = sBeta[r];
+                    k16[u] = live ? ldbf(sm + kKt + swz2(r, ch, 64)) : 0.f;
+                    q16[u] = live ? ldbf(sm + kQt + swz2(r, ch, 64)) : 0.f;
+                    b16[u] = sBeta[r];
+                }
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int r = r0 + u;
+                    const bool live = r < it.L;
+                    const float kv = k16[u], qv = q16[u], b = b16[u];
                     const float pq = pq16[u], pp = pp16[u], pe = pe16[u];
                     const float dq = pq + dqd[u];
                     const float dkv = pp + b * ee[u] + ff[u] + pe;
@@ -1064,21 +1073,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_decay_kernel(const __grid_con
         BP_MARK(22);
         if (ok) {
             const float add = wh == 0 ? sTot[ch] : 0.f;
+            // every z first: a load after a shared-memory store may not be hoisted above it
+            float zz[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) zz[u] = ldbf(sm + kZt + swz2(32 * wh + u, ch, 64));
+            const float gm = p.g_min;
 #pragma unroll
             for (int u = 0; u < 32; ++u) {
                 const int r = 32 * wh + u;
-                if (r < it.L) {
-                    const float x = eA * ldbf(sm + kZt + swz2(r, ch, 64));
-                    const float sg = __fdividef(1.f, 1.f + __expf(-x));
-                    const float dx = (dG[u] + add) * p.g_min * sg * (1.f - sg);
-                    dAp = fmaf(dx, x, dAp);
-                    *reinterpret_cast<uint16_t*>(sm + kQH + swz2(r, ch, 64)) = bfbits(dx * eA);
-                }
+                const float x = eA * zz[u];
+                const float sg = __fdividef(1.f, 1.f + __expf(-x));
+                const float dx = r < it.L ? (dG[u] + add) * gm * sg * (1.f - sg) : 0.f;
+                dAp = fmaf(dx, x, dAp);
+                *reinterpret_cast<uint16_t*>(sm + kQH + swz2(r, ch, 64)) = bfbits(dx * eA);
             }
+            BP_MARK(24);
             if (tid < 64 && tid < it.L) {
                 const float db = db1 + sDb[tid] + sDb[64 + tid] + sDb[128 + tid] + sDb[192 + tid];
                 p.dbeta[(size_t)(it.t0 + tid) * p.H + it.h] = __float2bfloat16_rn(db);
             }
+            BP_MARK(25);
         }
         // dA_log partial of the item: channels past dk have zero z and contribute x = 0
 #pragma unroll
