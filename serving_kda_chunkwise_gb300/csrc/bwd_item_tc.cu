@@ -329,13 +329,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         if (ok) {
             gate_scan(sm + kYI, ch, wh, it.L, scale2, gmin2, sTot, G2);
             if (wh == 1) sGlast[ch] = G2[31];
-            // K+ = Gamma*K, rows s of this half (K-major [2 blocks][64 rows][128 B])
+            // K+ = Gamma*K, rows s of this half (K-major [2 blocks][64 rows][128 B]); every k
+            // is read before the first store
+            float kk[32];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int s = 32 * wh + e;
-                const float kv = s < it.L ? ldbf(sm + kDVO + swz2(s, ch, 64)) : 0.f;
-                *reinterpret_cast<uint16_t*>(sm + kRX + swz2(s, ch, 64)) = bfbits(ex2f(G2[e]) * kv);
-            }
+            for (int e = 0; e < 32; ++e)
+                kk[e] = 32 * wh + e < it.L ? ldbf(sm + kDVO + swz2(32 * wh + e, ch, 64)) : 0.f;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                *reinterpret_cast<uint16_t*>(sm + kRX + swz2(32 * wh + e, ch, 64)) = bfbits(ex2f(G2[e]) * kk[e]);
             // M = N Diag(beta): row r, 16 columns per thread (MN-major rows r)
             const int r = tid >> 2, cq = tid & 3;
 #pragma unroll
@@ -408,6 +410,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
             tmem_ld16(tmem + lb + 16 + 32 * wh, a1);
             tmem_ld16(tmem + lb + 64 + 32 * wh, y0);
             tmem_ld16(tmem + lb + 80 + 32 * wh, y1);
+            // v of this lane's value channel for the tokens of this half, all before the stores
+            // below (a load after a shared-memory store may not be hoisted above it)
+            float vv[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u)
+                vv[u] = 32 * wh + u < it.L ? ldbf(sm + kVt + swz2(32 * wh + u, j, 64)) : 0.f;
             tmem_ld_wait();
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
@@ -416,11 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
                 for (int e = 0; e < 8; ++e) {
                     const int u = 8 * x + e;  // token s = 32 wh + u
                     const int s = 32 * wh + u;
-                    uint8_t* vs = sm + kVt + swz2(s, j, 64);
-                    const float vv = s < it.L ? ldbf(vs) : 0.f;
                     dv8[e] = u < 16 ? a0[u] : a1[u - 16];
-                    y8[e] = vv - (u < 16 ? y0[u] : y1[u - 16]);
-                    *reinterpret_cast<uint16_t*>(vs) = bfbits(dv8[e]);  // dv replaces v (staged)
+                    y8[e] = vv[u] - (u < 16 ? y0[u] : y1[u - 16]);
+                    // dv replaces v (staged for the output store)
+                    *reinterpret_cast<uint16_t*>(sm + kVt + swz2(s, j, 64)) = bfbits(dv8[e]);
                 }
                 const uint32_t off = (uint32_t)(j * 128 + (((4 * wh + x) ^ (j & 7)) << 4));
                 *reinterpret_cast<uint4*>(sm + kRX + off) = pk8(dv8);
