@@ -68,6 +68,9 @@ constexpr int kCopyT = 288;  // lane 0 of warp 9
 
 // shared memory (1024-aligned offsets)
 constexpr uint32_t kChPA = 0;          // part A, two stages of 32 KB
+// no output wanted (a backward pass): part A holds W alone (two stages of 16 KB), and the
+// stages of the image stores take the rest of its place, 4 KB per epilogue warp
+constexpr uint32_t kChWOnly = 16384, kChStage = 32768;
 constexpr uint32_t kChKC = 65536;      // K~ hi + lo, two stages of 32 KB
 constexpr uint32_t kChAT = 131072;     // A hi + lo (16 KB)
 constexpr uint32_t kChU = 147456;      // U, two stages of 32 KB
@@ -94,10 +97,9 @@ struct ChainParams {
     // head sizes of q, k (dk) and v, o, S (dv), 64 or 128: a 64 is zero-padded to 128 inside
     // (the tensor maps read zeros past it), so only the state and output addresses use them
     int dk, dv;
-    // optional (nullptr otherwise), for a backward pass: the image blocks [chunks][H]
-    // (bwd_tc_layout.cuh), chunk = chunk_off[n] + t, receive S_0^T (the state at the chunk
-    // start) and Vt^T as bf16 hi + lo operand images; with o == nullptr the output is not
-    // stored
+    // optional (nullptr otherwise), for a backward pass, which wants no output (o == nullptr):
+    // the image blocks [chunks][H] (bwd_tc_layout.cuh), chunk = chunk_off[n] + t, receive
+    // S_0^T (the state at the chunk start) and Vt^T as bf16 hi + lo operand images
     uint8_t* bimg;
     // fused kernel only (fused = 0 otherwise): CTA c serves chain c and reads chunk t from
     // ring slot c * ring_slots + t % ring_slots once ready[slot] >= t + 1; it raises
@@ -175,6 +177,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     if (tid == kMmaT) {
         // ------------------------------------------------------------ MMA thread
         constexpr uint32_t id1 = idesc_bf16(128, 128, false, false);
+        constexpr uint32_t id1w = idesc_bf16(128, 64, false, false);  // no output: W rows alone
         constexpr uint32_t id2 = idesc_bf16(128, 128, false, true);
         constexpr uint32_t id3 = idesc_bf16(128, 64, false, false);
         const uint64_t dPA = sdesc_sw128(sbase + kChPA, 0, 1024);
@@ -195,11 +198,19 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 CH_MARK(1);
                 tc_fence_after();
                 const uint32_t d1 = tmem + kTD1 + 128 * st;
+                if (want_o) {
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    mma_bf16_ts(d1, tmem + kTS + 8 * ks,
-                                dPA + ((st * kPkgPartA + (ks >> 2) * kPkgStkBlk + (ks & 3) * 32) >> 4),
-                                id1, ks > 0);
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(d1, tmem + kTS + 8 * ks,
+                                    dPA + ((st * kPkgPartA + (ks >> 2) * kPkgStkBlk + (ks & 3) * 32) >> 4),
+                                    id1, ks > 0);
+                } else {  // X^T = S^T W^T only (N = 64): the W rows of each key block, 8 KB apart
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        mma_bf16_ts(d1, tmem + kTS + 8 * ks,
+                                    dPA + ((st * kChWOnly + (ks >> 2) * 8192 + (ks & 3) * 32) >> 4),
+                                    id1w, ks > 0);
+                }
                 mma_commit(&mma1[st]);
                 CH_MARK(2);
                 if (!mbar_wait_ab(&fullKC[st], ph, p.err, abort)) { ok = false; break; }
@@ -265,8 +276,14 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (cpart == 0) {
                     if (!p.fused && t + 3 < c.nch) l2_prefetch(src + 3 * (size_t)kPkgBytes, kPkgBytes);
                     if (g >= 2 && !mbar_wait_ab(&mma1[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
-                    mbar_expect_tx(&fullPA[st], kPkgPartA);
-                    bulk_g2s(sm + kChPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
+                    if (want_o) {
+                        mbar_expect_tx(&fullPA[st], kPkgPartA);
+                        bulk_g2s(sm + kChPA + st * kPkgPartA, src + kPkgStk, kPkgPartA, &fullPA[st]);
+                    } else {  // the W rows (the first 8 KB) of the two key blocks
+                        mbar_expect_tx(&fullPA[st], kChWOnly);
+                        bulk_g2s(sm + kChPA + st * kChWOnly, src + kPkgStk, 8192, &fullPA[st]);
+                        bulk_g2s(sm + kChPA + st * kChWOnly + 8192, src + kPkgStk + kPkgStkBlk, 8192, &fullPA[st]);
+                    }
                     last_ph[st] = (int)((g >> 1) & 1);
                 } else if (cpart == 1) {
                     if (g >= 2 && !mbar_wait_ab(&vt_ready[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
@@ -379,59 +396,25 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             auto bimg_of = [&](int t) -> uint8_t* {
                 return p.bimg + ((size_t)(__ldg(p.chunk_off + c.n) + t) * p.H + c.h) * bwdtc::kBiBytes;
             };
-            // S_0^T of chunk t as bf16 hi + lo: row j of key-channel block wg, the 64 channels
-            // in eight 16-byte chunks (padding rows and columns are zeros)
+            // S_0^T of chunk t as bf16 hi + lo (no output wanted): row j of key-channel block wg,
+            // the 64 channels in eight 16-byte chunks (padding rows and columns are zeros),
+            // staged by the warp's 32 rows and stored as whole lines
+            uint8_t* stage = sm + kChStage + warp * 4096;
             auto store_ckpt = [&](int t) {
                 if (!p.bimg) return;
-                if (want_o) {  // direct 32-byte stores of swizzle-adjacent chunk pairs
-                    uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + j * 128;
+                uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + (32 * q) * 128;
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; c8 += 2) {
-                        float v0[8], v1[8];
+                for (int part = 0; part < 2; ++part) {  // hi, lo
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            v0[e] = S[8 * c8 + e];
-                            v1[e] = S[8 * c8 + 8 + e];
-                        }
-                        uint4 h0, l0, h1, l1;
-                        pk8_hilo(v0, h0, l0);
-                        pk8_hilo(v1, h1, l1);
-                        st_swz_pair(dst, c8, j, h0, h1);
-                        st_swz_pair(dst + 32768, c8, j, l0, l1);
+                    for (int c8 = 0; c8 < 8; ++c8) {
+                        float v8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v8[e] = S[8 * c8 + e];
+                        uint4 hi, lo;
+                        pk8_hilo(v8, hi, lo);
+                        stage_chunk(stage, lane, c8, part ? lo : hi);
                     }
-                    return;
-                }
-                // No output wanted: the A-tile buffer is free, 2 KB per epilogue warp.  The
-                // warp's 32 rows (row j = this lane, 32 (w mod 4) + lane of key block wg) are
-                // 4 KB contiguous in the image: 16 rows at a time are written into the buffer
-                // in the image's own swizzled order, then copied out as 512-byte contiguous
-                // stores (four 128-byte lines per warp store instead of 32)
-                uint8_t* stage = sm + kChAT + warp * 2048;
-                uint8_t* rows = bimg_of(t) + bwdtc::kBiS + wg * 16384 + (32 * q) * 128;
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {      // hi, lo
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {  // rows 16 half .. + 15 of the warp
-                        if ((lane >> 4) == half) {
-#pragma unroll
-                            for (int c8 = 0; c8 < 8; ++c8) {
-                                float v8[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) v8[e] = S[8 * c8 + e];
-                                uint4 hi, lo;
-                                pk8_hilo(v8, hi, lo);
-                                *reinterpret_cast<uint4*>(stage + (lane & 15) * 128 + ((c8 ^ (lane & 7)) << 4)) =
-                                    part ? lo : hi;
-                            }
-                        }
-                        __syncwarp();
-                        uint8_t* dst = rows + part * 32768 + half * 2048;
-#pragma unroll
-                        for (int x = 0; x < 4; ++x)
-                            *reinterpret_cast<uint4*>(dst + (x * 32 + lane) * 16) =
-                                *reinterpret_cast<const uint4*>(stage + (x * 32 + lane) * 16);
-                        __syncwarp();
-                    }
+                    flush_rows(dst + part * 32768, stage, lane);
                 }
             };
             if (c.nch > 0) {
@@ -490,27 +473,25 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&vt_ready[st]);
                 // backward pass: Vt^T row j into the image block, read back from TMEM while MMA2
-                // runs (tokens 32 wg + 8 x form chunk 4 wg + x of the row)
-                if (p.bimg && okc) {
-                    float fh16[16], fl16[16];
-                    tmem_ld16(tmem + lb + kTV + 16 * wg, fh16);
-                    tmem_ld16(tmem + lb + kTVlo + 16 * wg, fl16);
-                    tmem_ld_wait();
-                    uint32_t wh16[16], wl16[16];
+                // runs, once every warp's half of the row is there: warps of the first group
+                // store the hi rows, the second group the lo rows (64 tokens each, chunk x =
+                // tokens 8x .. 8x + 7)
+                if (p.bimg) {
+                    okc = okc && mbar_wait_ab(&vt_ready[st], ph, p.err, abort);
+                    if (okc) {
+                        tc_fence_after();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        wh16[e] = __float_as_uint(fh16[e]);
-                        wl16[e] = __float_as_uint(fl16[e]);
-                    }
-                    uint8_t* vimg = bimg_of(t) + bwdtc::kBiV + j * 128;
+                        for (int hf = 0; hf < 2; ++hf) {
+                            float f16[16];
+                            tmem_ld16(tmem + lb + (wg ? kTVlo : kTV) + 16 * hf, f16);
+                            tmem_ld_wait();
 #pragma unroll
-                    for (int pr = 0; pr < 2; ++pr) {
-                        st_swz_pair(vimg, 4 * wg + 2 * pr, j,
-                                    make_uint4(wh16[8 * pr], wh16[8 * pr + 1], wh16[8 * pr + 2], wh16[8 * pr + 3]),
-                                    make_uint4(wh16[8 * pr + 4], wh16[8 * pr + 5], wh16[8 * pr + 6], wh16[8 * pr + 7]));
-                        st_swz_pair(vimg + 16384, 4 * wg + 2 * pr, j,
-                                    make_uint4(wl16[8 * pr], wl16[8 * pr + 1], wl16[8 * pr + 2], wl16[8 * pr + 3]),
-                                    make_uint4(wl16[8 * pr + 4], wl16[8 * pr + 5], wl16[8 * pr + 6], wl16[8 * pr + 7]));
+                            for (int x = 0; x < 4; ++x)
+                                stage_chunk(stage, lane, 4 * hf + x,
+                                            make_uint4(__float_as_uint(f16[4 * x]), __float_as_uint(f16[4 * x + 1]),
+                                                       __float_as_uint(f16[4 * x + 2]), __float_as_uint(f16[4 * x + 3])));
+                        }
+                        flush_rows(bimg_of(t) + bwdtc::kBiV + wg * 16384 + (32 * q) * 128, stage, lane);
                     }
                 }
                 if (rec) CH_MARK(10);

@@ -270,6 +270,7 @@ size_t fwd_tc_workspace_size(int64_t T_total, int N, int H) {
 cudaError_t launch_fwd_tc(const FwdArgs& a) {
     using namespace fwdtc;
     if ((int64_t)a.N * a.H == 0) return cudaSuccess;
+    if (a.bimg && a.o) return cudaErrorInvalidValue;  // the image stores take the output's place
     const bool mixed = a.gate_kind == 1;  // the softplus gate on the mixed path
     uint8_t* ws = static_cast<uint8_t*>(a.workspace);
     const WsLayout L = ws_layout(a.T_total, a.N, a.H);

@@ -27,10 +27,10 @@ struct FwdArgs {
     size_t ws_bytes;
     unsigned* dev_err;
     cudaStream_t stream;
-    // tensor-core path only, for a backward pass (nullptr otherwise): the backward's image
-    // blocks [chunks][H] in the order of the chunk offsets (bwd_tc_layout.cuh), which
-    // receive S_0, Vt and N of every chunk; selects the two-launch form, which also leaves
-    // every (chunk, head) package in the workspace
+    // tensor-core path only, for a backward pass (nullptr otherwise; o must then be nullptr):
+    // the backward's image blocks [chunks][H] in the order of the chunk offsets
+    // (bwd_tc_layout.cuh), which receive S_0, Vt and N of every chunk; selects the two-launch
+    // form, which also leaves every (chunk, head) package in the workspace
     void* bimg;
     // two-launch form, optional: recorded on `stream` once the intra stage is enqueued (the
     // backward starts its gradient chain on a second stream from there)
