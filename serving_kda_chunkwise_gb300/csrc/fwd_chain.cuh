@@ -68,15 +68,17 @@ constexpr int kCopyT = 288;  // lane 0 of warp 9
 
 // shared memory (1024-aligned offsets)
 constexpr uint32_t kChPA = 0;          // part A, two stages of 32 KB
-// no output wanted (a backward pass): part A holds W alone (two stages of 16 KB), and the
-// stages of the image stores take the rest of its place, 4 KB per epilogue warp
+// no output wanted (a backward pass): part A holds W alone (two stages of 16 KB) and the
+// image stores have two 4 KB stages per epilogue warp: the first set in the rest of part A's
+// place, the second in the A tile's place (warps 0..3) and at kChStageB (warps 4..7)
 constexpr uint32_t kChWOnly = 16384, kChStage = 32768;
 constexpr uint32_t kChKC = 65536;      // K~ hi + lo, two stages of 32 KB
 constexpr uint32_t kChAT = 131072;     // A hi + lo (16 KB)
 constexpr uint32_t kChU = 147456;      // U, two stages of 32 KB
-constexpr uint32_t kChG = 212992;      // gamma^C, four stages of 512 B
-constexpr uint32_t kChBars = 215040;
-constexpr uint32_t kChainSmem = kChBars + 256 + 1024;
+constexpr uint32_t kChG = 212992;      // gamma^C, three stages of 512 B
+constexpr uint32_t kChBars = 214528;
+constexpr uint32_t kChStageB = 214784;
+constexpr uint32_t kChainSmem = kChStageB + 16384 + 1024;
 static_assert(kChainSmem <= 232448, "chain kernel exceeds the shared-memory limit");
 
 // TMEM columns: S^T bf16 [0, 64); Vt^T bf16 hi [64, 96), lo [96, 128); D1 for chunk g in
@@ -135,6 +137,8 @@ __device__ __forceinline__ Chain decode_chain(const ChainParams& p, int ci) {
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
+// kImg: the backward's instantiation, which writes the operand images (p.bimg) and no output.
+template <bool kImg>
 __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_raw, int cta, int ncta) {
     uint8_t* sm = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -172,7 +176,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     const uint32_t tmem = *tmem_slot;
     const int n_chains = p.N * p.H;
     const int G = ncta;
-    const bool want_o = p.o != nullptr;
+    const bool want_o = !kImg && p.o != nullptr;
 
     if (tid == kMmaT) {
         // ------------------------------------------------------------ MMA thread
@@ -289,7 +293,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                     if (g >= 2 && !mbar_wait_ab(&vt_ready[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
                     mbar_expect_tx(&fullU[st], kPkgUBytes + kPkgGBytes);
                     bulk_g2s(sm + kChU + st * kPkgUBytes, src + kPkgU, kPkgUBytes, &fullU[st]);
-                    bulk_g2s(sm + kChG + (g & 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
+                    bulk_g2s(sm + kChG + (g % 3) * kPkgGBytes, src + kPkgG, kPkgGBytes, &fullU[st]);
                     last_ph[st] = (int)((g >> 1) & 1);
                 } else if (cpart == 2) {
                     if (g >= 2 && !mbar_wait_ab(&mma2[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
@@ -396,15 +400,38 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
             auto bimg_of = [&](int t) -> uint8_t* {
                 return p.bimg + ((size_t)(__ldg(p.chunk_off + c.n) + t) * p.H + c.h) * bwdtc::kBiBytes;
             };
-            // S_0^T of chunk t as bf16 hi + lo (no output wanted): row j of key-channel block wg,
-            // the 64 channels in eight 16-byte chunks (padding rows and columns are zeros),
-            // staged by the warp's 32 rows and stored as whole lines
-            uint8_t* stage = sm + kChStage + warp * 4096;
+            // Image stores (no output wanted): the warp's 32 rows of an image part go into one
+            // of its two 4 KB stages in the image's own order, and lane 0 hands the 4 KB to a
+            // bulk copy, so that no epilogue warp waits for its stores to leave the SM.  Per
+            // chunk the parts are S_0 hi (first stage), S_0 lo (second) and Vt (first); a stage
+            // is rewritten once lane 0's bulk copies have read it (all but the newest for the
+            // second stage and for Vt, all for S_0 hi).
+            uint8_t* stg0 = sm + kChStage + warp * 4096;
+            uint8_t* stg1 = warp < 4 ? sm + kChAT + warp * 4096 : sm + kChStageB + (warp - 4) * 4096;
+            auto stage_free = [&](bool all) {
+                if (lane == 0) {
+                    if (all) bulk_wait_read0();
+                    else bulk_wait_read1();
+                }
+                __syncwarp();
+            };
+            auto stage_out = [&](uint8_t* dst, const uint8_t* stg) {
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    bulk_s2g(dst, stg, 4096);
+                    bulk_commit();
+                }
+            };
+            // S_0^T of chunk t as bf16 hi + lo: row j of key-channel block wg, the 64 channels
+            // in eight 16-byte chunks (padding rows and columns are zeros)
             auto store_ckpt = [&](int t) {
-                if (!p.bimg) return;
+                if constexpr (!kImg) return;
                 uint8_t* dst = bimg_of(t) + bwdtc::kBiS + wg * 16384 + (32 * q) * 128;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {  // hi, lo
+                    uint8_t* stg = part ? stg1 : stg0;
+                    stage_free(part == 0);
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8) {
                         float v8[8];
@@ -412,9 +439,9 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                         for (int e = 0; e < 8; ++e) v8[e] = S[8 * c8 + e];
                         uint4 hi, lo;
                         pk8_hilo(v8, hi, lo);
-                        stage_chunk(stage, lane, c8, part ? lo : hi);
+                        stage_chunk(stg, lane, c8, part ? lo : hi);
                     }
-                    flush_rows(dst + part * 32768, stage, lane);
+                    stage_out(dst + part * 32768, stg);
                 }
             };
             if (c.nch > 0) {
@@ -476,10 +503,11 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 // runs, once every warp's half of the row is there: warps of the first group
                 // store the hi rows, the second group the lo rows (64 tokens each, chunk x =
                 // tokens 8x .. 8x + 7)
-                if (p.bimg) {
-                    okc = okc && mbar_wait_ab(&vt_ready[st], ph, p.err, abort);
+                if constexpr (kImg) {
+                    okc = __all_sync(0xffffffffu, okc && mbar_wait_ab(&vt_ready[st], ph, p.err, abort));
                     if (okc) {
                         tc_fence_after();
+                        stage_free(false);
 #pragma unroll
                         for (int hf = 0; hf < 2; ++hf) {
                             float f16[16];
@@ -487,11 +515,11 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                             tmem_ld_wait();
 #pragma unroll
                             for (int x = 0; x < 4; ++x)
-                                stage_chunk(stage, lane, 4 * hf + x,
+                                stage_chunk(stg0, lane, 4 * hf + x,
                                             make_uint4(__float_as_uint(f16[4 * x]), __float_as_uint(f16[4 * x + 1]),
                                                        __float_as_uint(f16[4 * x + 2]), __float_as_uint(f16[4 * x + 3])));
                         }
-                        flush_rows(bimg_of(t) + bwdtc::kBiV + wg * 16384 + (32 * q) * 128, stage, lane);
+                        stage_out(bimg_of(t) + bwdtc::kBiV + wg * 16384 + (32 * q) * 128, stg0);
                     }
                 }
                 if (rec) CH_MARK(10);
@@ -503,7 +531,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 if (rec) CH_MARK(11);
                 if (okc) {
                     tc_fence_after();
-                    const float* gam = reinterpret_cast<const float*>(sm + kChG + (g & 3) * kPkgGBytes) + 64 * wg;
+                    const float* gam = reinterpret_cast<const float*>(sm + kChG + (g % 3) * kPkgGBytes) + 64 * wg;
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {  // 32 key channels at a time
                         float d0[16], d1v[16];
@@ -549,6 +577,7 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                 for (int e = 0; e < 64; ++e) p.S_out[sbase_el + (size_t)e * p.dv] = S[e];
             }
         }
+        if (kImg && lane == 0) bulk_wait0();  // the stages are read and the images written
     }
 
     chain_sync();

@@ -151,9 +151,10 @@ __global__ void __launch_bounds__(kIntraThreads, 1) intra_kernel(const __grid_co
     intra_body<kGate>(p, smem_raw, blockIdx.x, gridDim.x);
 }
 
+template <bool kImg>
 __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainParams p) {
     extern __shared__ uint8_t smem_raw[];
-    chain_body(p, smem_raw, blockIdx.x, gridDim.x);
+    chain_body<kImg>(p, smem_raw, blockIdx.x, gridDim.x);
 }
 
 // The two stages in one cooperative launch: CTAs [0, C) run the chain of (sequence, head)
@@ -190,7 +191,7 @@ template <int kGate>
 __global__ void __launch_bounds__(kFusedThreads, 1) fwd_fused_kernel(const __grid_constant__ FusedParams p) {
     extern __shared__ uint8_t smem_raw[];
     if ((int)blockIdx.x < p.C) {
-        if (threadIdx.x < kChainThreads) chain_body(p.cp, smem_raw, blockIdx.x, p.C);
+        if (threadIdx.x < kChainThreads) chain_body<false>(p.cp, smem_raw, blockIdx.x, p.C);
     } else if (threadIdx.x >= kIntraThreads) {
         if constexpr (kGate == kGateBounded) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIdleRegs));
     } else {
@@ -395,12 +396,16 @@ cudaError_t launch_fwd_tc(const FwdArgs& a) {
         e = cudaEventRecord(a.after_intra, a.stream);
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kChainSmem);
+    const void* cfn = a.bimg ? reinterpret_cast<const void*>(chain_kernel<true>)
+                             : reinterpret_cast<const void*>(chain_kernel<false>);
+    e = cudaFuncSetAttribute(cfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kChainSmem);
     if (e != cudaSuccess) return e;
     const int grid = (int)(C < sms ? C : sms);
     ProfScope prof("chain_kernel", a.stream);
-    chain_kernel<<<grid, kChainThreads, kChainSmem, a.stream>>>(cp);
+    if (a.bimg)
+        chain_kernel<true><<<grid, kChainThreads, kChainSmem, a.stream>>>(cp);
+    else
+        chain_kernel<false><<<grid, kChainThreads, kChainSmem, a.stream>>>(cp);
     return cudaGetLastError();
 }
 
