@@ -36,6 +36,26 @@ using namespace tc;
 using fwdtc::kC;
 using fwdtc::kD;
 
+// Optional per-phase cycle counters (debug builds with -DKDA_PHASE_TIMING only): the MMA
+// thread and thread 0 of CTA 0 accumulate clock64() deltas.
+#ifdef KDA_PHASE_TIMING
+__device__ unsigned long long g_gchain_phase[16];
+#define GC_T0() long long gc_t = clock64()
+#define GC_MARK(i)                                                                         \
+    do {                                                                                   \
+        const long long gc_n = clock64();                                                  \
+        if (cta == 0) atomicAdd(&g_gchain_phase[(i)], (unsigned long long)(gc_n - gc_t)); \
+        gc_t = gc_n;                                                                       \
+    } while (0)
+#else
+#define GC_T0() \
+    do {        \
+    } while (0)
+#define GC_MARK(i) \
+    do {           \
+    } while (0)
+#endif
+
 constexpr int kThreads = 320;  // 8 epilogue warps, an MMA thread (warp 8), copy lanes (warp 9)
 constexpr int kMmaT = 256;
 constexpr int kCopyW = 9;
@@ -132,23 +152,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
         constexpr uint32_t id2z = idesc_bf16(128, 128, false, true);  // (-Z)^T x W
         uint32_t g = 0;
         bool ok = true;
+        GC_T0();
         for (int k = 0; ok; ++k) {
             const int ci = chain_of(k, cta, G);
             if (ci >= n_chains) break;
             const Chain c = decode_chain(p, ci);
             for (int t = c.nch - 1; t >= 0; --t, ++g) {
                 const uint32_t st = g & 1, ph = (g >> 1) & 1;
-                if (!mbar_wait_ab(&fullKC[st], ph, p.err, abort) ||
-                    !mbar_wait_ab(&fullAT[st], ph, p.err, abort) ||
-                    !mbar_wait_ab(&fullDO[st], ph, p.err, abort) ||
-                    !mbar_wait_ab(s_ready, g & 1, p.err, abort)) {
-                    ok = false;
-                    break;
-                }
+                // Z^T = dO^T [A_hi; A_lo]      (K = 64 query tokens, A rows as MN-major B)
+                //     + dS'^T [K~_hi; K~_lo]^T (K = 128 key channels, K~ rows as K-major B).
+                // The dO part needs no dS': it is issued first, while E2 of the previous chunk
+                // still runs (D1 is free: E1 of the previous chunk, its reader, preceded the
+                // previous MMA2).
+                if (!mbar_wait_ab(&fullAT[st], ph, p.err, abort)) { ok = false; break; }
+                GC_MARK(1);
+                if (!mbar_wait_ab(&fullDO[st], ph, p.err, abort)) { ok = false; break; }
+                GC_MARK(2);
                 tc_fence_after();
                 const uint32_t d1 = tmem + kTD1;
-                // Z^T = dS'^T [K~_hi; K~_lo]^T (K = 128 key channels, K~ rows as K-major B)
-                //     + dO^T [A_hi; A_lo]      (K = 64 query tokens, A rows as MN-major B)
+                const uint64_t dDO = sdesc_sw128(sbase + kDO + st * 16384, 8192, 1024);
+                const uint64_t dAT = sdesc_sw128(sbase + kAT + st * 16384, 8192, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int part = ks >> 2, kk = ks & 3;  // part 0: A hi, 1: A lo
+                    mma_bf16(d1, dDO + ((kk * 2048) >> 4), dAT + ((part * 8192 + kk * 2048) >> 4),
+                             id1d, ks > 0);
+                }
+                if (!mbar_wait_ab(&fullKC[st], ph, p.err, abort)) { ok = false; break; }
+                GC_MARK(0);
+                if (!mbar_wait_ab(s_ready, g & 1, p.err, abort)) { ok = false; break; }
+                GC_MARK(3);
+                tc_fence_after();
                 const uint64_t dKC = sdesc_sw128(sbase + kKC + st * 32768, 0, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 24; ++ks) {
@@ -156,22 +190,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                     const int part = ks >> 3, kk = ks & 7;
                     mma_bf16_ts(d1, tmem + (part == 2 ? kTSlo : kTS) + 8 * kk,
                                 dKC + (((part == 1 ? 16384 : 0) + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
-                                id1s, ks > 0);
-                }
-                const uint64_t dDO = sdesc_sw128(sbase + kDO + st * 16384, 8192, 1024);
-                const uint64_t dAT = sdesc_sw128(sbase + kAT + st * 16384, 8192, 1024);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int part = ks >> 2, kk = ks & 3;  // part 0: A hi, 1: A lo
-                    mma_bf16(d1, dDO + ((kk * 2048) >> 4), dAT + ((part * 8192 + kk * 2048) >> 4),
-                             id1d, 1);
+                                id1s, 1);
                 }
                 mma_commit(&mma1[st]);
-                if (!mbar_wait_ab(&fullPA[st], ph, p.err, abort) ||
-                    !mbar_wait_ab(&z_ready[st], ph, p.err, abort)) {
-                    ok = false;
-                    break;
-                }
+                GC_MARK(4);
+                if (!mbar_wait_ab(&fullPA[st], ph, p.err, abort)) { ok = false; break; }
+                GC_MARK(5);
+                if (!mbar_wait_ab(&z_ready[st], ph, p.err, abort)) { ok = false; break; }
+                GC_MARK(6);
                 tc_fence_after();
                 // D2 = dO^T (Gamma*Q) + (-Z)^T_hi W + (-Z)^T_lo W  (K = 64 tokens)
                 const uint64_t dQ = sdesc_sw128(sbase + kPA + st * 32768 + fwdtc::kPkgStkQ,
@@ -188,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                                 dW + ((kk * 2048) >> 4), id2z, 1);
                 }
                 mma_commit(&mma2[st]);
+                GC_MARK(7);
             }
         }
     }
@@ -240,6 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
         const uint32_t lb = static_cast<uint32_t>(32 * q) << 16;
         uint32_t g = 0;
         bool ok = true;
+        const bool rec = (tid == 0);
+        GC_T0();
         for (int k = 0; ok; ++k) {
             const int ci = chain_of(k, cta, G);
             if (ci >= n_chains) break;
@@ -291,8 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                         st_swz_pair(dst + 32768, c8, j, l0, l1);
                     }
                 }
+                if (rec) GC_MARK(8);
                 // ---- E1: -Z^T as bf16 hi + lo for tokens r = 32 wg + e
                 bool okc = mbar_wait_ab(&mma1[st], ph, p.err, abort);
+                if (rec) GC_MARK(9);
                 if (okc) {
                     tc_fence_after();
                     float z0[16], z1[16];
@@ -318,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&z_ready[st]);
+                if (rec) GC_MARK(10);
                 // dVt^T row j into the image block, read back from TMEM while MMA2 runs: tokens
                 // 32 wg + 8 x are chunk 4 wg + x of the row; TMEM holds -Z, so the words are
                 // negated
@@ -344,8 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                                     make_uint4(wl[8 * pr + 4], wl[8 * pr + 5], wl[8 * pr + 6], wl[8 * pr + 7]));
                     }
                 }
+                if (rec) GC_MARK(11);
                 // ---- E2: dS^T <- dS'^T Diag(gamma^C) + D2; bf16 copy for the next MMA1
                 okc = okc && mbar_wait_ab(&mma2[st], ph, p.err, abort);
+                if (rec) GC_MARK(12);
                 if (okc) {
                     tc_fence_after();
                     const float* gam = reinterpret_cast<const float*>(sm + kGm + (g & 3) * fwdtc::kPkgGBytes) + 64 * wg;
@@ -390,6 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 __syncwarp();
                 if (!okc) { ok = false; break; }
                 if (lane == 0 && t > 0) mbar_arrive(s_ready);
+                if (rec) GC_MARK(13);
             }
             if (!ok) break;
             if (p.dS0 && sv) {
@@ -421,6 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
 
 }  // namespace
 }  // namespace bwdtc
+
+#ifdef KDA_PHASE_TIMING
+extern "C" int kda_debug_gchain_cycles(unsigned long long* out, int n) {
+    if (n > 16) n = 16;
+    if (cudaMemcpyFromSymbol(out, bwdtc::g_gchain_phase, n * sizeof(unsigned long long)) != cudaSuccess)
+        return -1;
+    static const unsigned long long zeros[16] = {};
+    return cudaMemcpyToSymbol(bwdtc::g_gchain_phase, zeros, sizeof zeros) == cudaSuccess ? n : -1;
+}
+#endif
 
 // The gradient chain on the tensor cores: reads the packages the forward's two-launch form
 // left in its workspace (fwd_ws), writes dS_C and dVt into the image blocks and dS0.
