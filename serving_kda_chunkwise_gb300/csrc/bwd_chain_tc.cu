@@ -70,9 +70,9 @@ constexpr uint32_t kBars = 198656;
 constexpr uint32_t kSmem = kBars + 256 + 1024;
 static_assert(kSmem <= 232448, "gradient chain exceeds the shared-memory limit");
 
-// TMEM columns: dS^T bf16 hi [0, 64); -Z^T bf16 hi [64, 96), lo [96, 128); D1 (Z^T) [128, 192);
-// dS^T bf16 lo [192, 256); D2 [256, 384)
-constexpr uint32_t kTS = 0, kTZ = 64, kTZlo = 96, kTD1 = 128, kTSlo = 192, kTD2 = 256, kTCols = 512;
+// TMEM columns: dS^T bf16 hi [0, 64); -Z^T bf16 hi [64, 96), lo [96, 128); D1 and D1b (Z^T in
+// two parts, added in E1) [128, 192) and [384, 448); dS^T bf16 lo [192, 256); D2 [256, 384)
+constexpr uint32_t kTS = 0, kTZ = 64, kTZlo = 96, kTD1 = 128, kTSlo = 192, kTD2 = 256, kTD1b = 384, kTCols = 512;
 
 struct Params {
     CUtensorMap tdo;  // dO [T_total, H, dv] bf16, boxes of 64 columns x 1 head x 64 rows
@@ -184,13 +184,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 GC_MARK(3);
                 tc_fence_after();
                 const uint64_t dKC = sdesc_sw128(sbase + kKC + st * 32768, 0, 1024);
+                // two independent accumulators, issued alternately: D1 takes dS hi x K~ hi and
+                // dS lo x K~ hi over key steps 0..3, D1b dS hi x K~ lo and dS lo x K~ hi over
+                // steps 4..7 (E1 adds them)
 #pragma unroll
-                for (int ks = 0; ks < 24; ++ks) {
-                    // part 0: dS hi x K~ hi, 1: dS hi x K~ lo, 2: dS lo x K~ hi
-                    const int part = ks >> 3, kk = ks & 7;
-                    mma_bf16_ts(d1, tmem + (part == 2 ? kTSlo : kTS) + 8 * kk,
-                                dKC + (((part == 1 ? 16384 : 0) + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
-                                id1s, 1);
+                for (int i = 0; i < 12; ++i) {
+                    const int kka = i < 8 ? i : i - 8;           // D1: hi x hi (8), lo x hi (kk 0..3)
+                    const bool loa = i >= 8;
+                    mma_bf16_ts(d1, tmem + (loa ? kTSlo : kTS) + 8 * kka,
+                                dKC + (((kka >> 2) * 8192 + (kka & 3) * 32) >> 4), id1s, 1);
+                    const int kkb = i < 8 ? i : i - 4;           // D1b: hi x lo (8), lo x hi (kk 4..7)
+                    const bool lob = i >= 8;
+                    mma_bf16_ts(tmem + kTD1b, tmem + (lob ? kTSlo : kTS) + 8 * kkb,
+                                dKC + (((lob ? 0 : 16384) + (kkb >> 2) * 8192 + (kkb & 3) * 32) >> 4), id1s,
+                                i > 0);
                 }
                 mma_commit(&mma1[st]);
                 GC_MARK(4);
@@ -326,10 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 if (rec) GC_MARK(9);
                 if (okc) {
                     tc_fence_after();
-                    float z0[16], z1[16];
+                    float z0[16], z1[16], y0[16], y1[16];
                     tmem_ld16(tmem + lb + kTD1 + 32 * wg, z0);
                     tmem_ld16(tmem + lb + kTD1 + 32 * wg + 16, z1);
+                    tmem_ld16(tmem + lb + kTD1b + 32 * wg, y0);
+                    tmem_ld16(tmem + lb + kTD1b + 32 * wg + 16, y1);
                     tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        z0[e] += y0[e];
+                        z1[e] += y1[e];
+                    }
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         uint32_t hi[8], lo[8];
