@@ -203,10 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 GC_MARK(4);
                 if (!mbar_wait_ab(&fullPA[st], ph, p.err, abort)) { ok = false; break; }
                 GC_MARK(5);
-                if (!mbar_wait_ab(&z_ready[st], ph, p.err, abort)) { ok = false; break; }
-                GC_MARK(6);
-                tc_fence_after();
-                // D2 = dO^T (Gamma*Q) + (-Z)^T_hi W + (-Z)^T_lo W  (K = 64 tokens)
+                // D2 = dO^T (Gamma*Q) + (-Z)^T_hi W + (-Z)^T_lo W  (K = 64 tokens).  The dO part
+                // needs no Z: it goes in before E1 ends (D2 is free: E2 of the previous chunk,
+                // its reader, preceded this chunk's dS' products).
                 const uint64_t dQ = sdesc_sw128(sbase + kPA + st * 32768 + fwdtc::kPkgStkQ,
                                                 fwdtc::kPkgStkBlk, 1024);
                 const uint64_t dW = sdesc_sw128(sbase + kPA + st * 32768, fwdtc::kPkgStkBlk, 1024);
@@ -214,6 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_chain_tc_kernel(const __grid_
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + kTD2, dDO + ((kk * 2048) >> 4), dQ + ((kk * 2048) >> 4), id2d,
                              kk > 0);
+                if (!mbar_wait_ab(&z_ready[st], ph, p.err, abort)) { ok = false; break; }
+                GC_MARK(6);
+                tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const int part = ks >> 2, kk = ks & 3;  // part 0: -Z hi, 1: -Z lo
