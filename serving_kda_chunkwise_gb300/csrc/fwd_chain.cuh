@@ -14,7 +14,10 @@
 //   E2    S^T <- S^T Diag(gamma^C) + dS^T in fp32 registers; bf16 copy of S^T into TMEM
 //   MMA3  O^T += [Vt_hi | Vt_lo | Vt_hi]^T [A_hi; A_hi; A_lo]^T  (into D1's columns 64..127)
 //   E3    O^T -> bf16 -> o (for each token, the 32 lanes of a warp store 64 contiguous bytes)
-// With no output wanted (the forward of a backward pass), neither the A tile, MMA3 nor E3 runs.
+// With no output wanted (the forward of a backward pass), neither the A tile, MMA3 nor E3 runs,
+// and MMA1 takes the W rows alone (N = 64).  The backward's instantiation (kImg) also writes
+// S_0^T and Vt^T of every chunk as operand images, each warp's 4 KB parts through shared-memory
+// stages and bulk copies.
 // The state update takes three bf16 products (hi x hi, lo x hi, hi x lo) so that the fp32
 // state is not limited by bf16 rounding of K~ or Vt; the output takes the same three.
 // No intermediate of the chain goes through shared memory, so a chain step is
@@ -253,8 +256,8 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
     // Copy lanes: lanes 0..3 of warp 9 each stream one part of the packages, so that a part
     // is fetched as soon as its buffer is free, independently of the others.
     //   lane 0: part A ([W; Gamma*Q]), two stages, free once MMA1 of chunk g - 2 completed;
-    //   lane 1: U and gamma^C, two stages of U (free once E1 of chunk g - 2 is done) and four
-    //           of gamma (E2 of chunk g - 4 precedes E1 of chunk g - 2 on the same warps);
+    //   lane 1: U and gamma^C, two stages of U (free once E1 of chunk g - 2 is done) and three
+    //           of gamma (E2 of chunk g - 3 precedes E1 of chunk g - 2 on the same warps);
     //   lane 2: K~ hi + lo, two stages, free once MMA2 of chunk g - 2 completed;
     //   lane 3: A hi + lo, one stage, free once MMA3 of chunk g - 1 completed.
     int last_ph[2] = {-1, -1};  // the phase parity a drain must let land, per stage
