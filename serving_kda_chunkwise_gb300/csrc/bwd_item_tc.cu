@@ -278,7 +278,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     const int wq = warp & 3, wh = warp >> 2;
     const int ch = 32 * wq + lane;  // TMEM lane: a key or value channel (or a token s)
     const uint32_t lb = static_cast<uint32_t>(32 * wq) << 16;
-    uint32_t inflight = 0, inflight_ph = 0;  // thread 0: copies of the current item
+    // thread 0: the phase each copy barrier (fullIn, fullS, fullV, fullDO, fullDS) has in
+    // flight, or -1
+    int pend[5] = {-1, -1, -1, -1, -1};
+    // z, k, dVt and Vt of an item: issued while the previous item finishes (its batch 3 has
+    // read their places), or at the item's start for a CTA's first item
+    auto issue_early = [&](const Item& e, const uint8_t* eblk, uint32_t eph) {
+        pend[0] = (int)eph;
+        mbar_expect_tx(fullIn, 32768);
+        load_tile(&p.tz, sm + kYI, e, fullIn);
+        load_tile(&p.tk, sm + kDVO, e, fullIn);
+        pend[2] = (int)eph;
+        mbar_expect_tx(fullV, 65536);
+        bulk_g2s(sm + kDVI, eblk + kBiDV, 32768, fullV);
+        bulk_g2s(sm + kVI, eblk + kBiV, 32768, fullV);
+    };
+    bool early_done = false;  // thread 0: this item's early copies are issued
     bool ok = true;
     uint32_t iter = 0;
     BP_T0();
@@ -287,18 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         const uint32_t ph = iter & 1;
         const uint8_t* blk = p.bimg + (size_t)item * kBiBytes;
         if (iss) {
+            if (!early_done) issue_early(it, blk, ph);
+            early_done = false;
             bulk_wait_read0();  // the previous item's dv store has read the v tile's place
-            inflight = 0xfu;  // fullIn, fullS, fullV, fullDO
-            inflight_ph = ph;
-            mbar_expect_tx(fullIn, 49152);
-            load_tile(&p.tz, sm + kYI, it, fullIn);
-            load_tile(&p.tk, sm + kDVO, it, fullIn);
-            load_tile(&p.tv, sm + kVt, it, fullIn);
-            mbar_expect_tx(fullS, 65536);
+            pend[1] = (int)ph;  // S_0 (read by batch 1) and v (epilogue 1)
+            mbar_expect_tx(fullS, 65536 + 16384);
             bulk_g2s(sm + kSI, blk + kBiS, 65536, fullS);
-            mbar_expect_tx(fullV, 65536);
-            bulk_g2s(sm + kDVI, blk + kBiDV, 32768, fullV);
-            bulk_g2s(sm + kVI, blk + kBiV, 32768, fullV);
+            load_tile(&p.tv, sm + kVt, it, fullS);
+            pend[3] = (int)ph;
             mbar_expect_tx(fullDO, 16384);
             load_tile(&p.tdo, sm + kDOt, it, fullDO);
             const int nx = item + gridDim.x;  // the next item's inputs into L2
@@ -324,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
 #pragma unroll
         for (int x = 0; x < 4; ++x) nrow[x] = ld_early4(Ng + (tid >> 2) * 64 + 16 * (tid & 3) + 4 * x);
         ok = ok && mbar_wait_ab(fullIn, ph, p.err, abort);
+        if (iss && ok) pend[0] = -1;
         BP_MARK(0);
         float G2[32];
         if (ok) {
@@ -358,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
             ok = mbar_wait_ab(fullS, ph, p.err, abort) && mbar_wait_ab(fullV, ph, p.err, abort) &&
                  mbar_wait_ab(fullDO, ph, p.err, abort);
             if (ok) {
+                pend[1] = pend[2] = pend[3] = -1;
                 tc_fence_after();
                 // batch 1 -----------------------------------------------------------
                 // dV^T = dVt^T M: A = dVt^T rows j hi, lo (K = 64 tokens, K-major), B = M rows r
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         BP_MARK(4);
         if (iss && ok) {
             // dVt and Y are consumed: dS_C^T hi, lo into their place
-            inflight |= 0x10u;
+            pend[4] = (int)ph;
             mbar_expect_tx(fullDS, 65536);
             bulk_g2s(sm + kDVI, blk + kBiDS, 32768, fullDS);
             bulk_g2s(sm + kYI, blk + kBiDS + 32768, 32768, fullDS);
@@ -579,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         if (iss && ok) {
             ok = mbar_wait_ab(fullDS, ph, p.err, abort);
             if (ok) {
+                pend[4] = -1;
                 tc_fence_after();
                 // batch 3 -----------------------------------------------------------
                 // dS_C Vt^T: A = dS_C (MN-major rows j), B = Vt^T rows j (MN-major); hi x hi,
@@ -613,6 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
         // ---- epilogue 3: pE = (gamma^C/Gamma)*(dS_C Vt^T) and rs = diag(dS_C S_0^T)
         ok = ok && mbar_wait_ab(mma3, ph, p.err, abort);
         BP_MARK(7);
+        // batch 3 has read the dS_C, Vt and Y places: the next item's z, k, dVt and Vt go in
+        // now, so that they land during this item's last phases
+        if (iss && ok) {
+            const int nx = item + (int)gridDim.x;
+            if (nx < n_items) {
+                issue_early(decode(p, nx), p.bimg + (size_t)nx * kBiBytes, ph ^ 1u);
+                early_done = true;
+            }
+        }
         if (ok) {
             tc_fence_after();
             const float gl = sGlast[ch];
@@ -757,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_state_kernel(const __grid_con
     if (s_abort && iss) {
         // let the copies and MMAs still in flight land before the CTA leaves
         for (int b = 0; b < 5; ++b)
-            if (inflight & (1u << b)) mbar_wait(&bars[b], inflight_ph, nullptr);
+            if (pend[b] >= 0) mbar_wait(&bars[b], (uint32_t)pend[b], nullptr);
         mma_commit(drain);
         mbar_wait(drain, 0, nullptr);
     }
