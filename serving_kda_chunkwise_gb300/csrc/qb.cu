@@ -80,16 +80,27 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__
         bj[e] = (j < n) ? __ldg(b + j) : 0.f;
     }
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t i = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); i < m;
-         i += warps) {
+    // the scores of the warp's next token are loaded while it selects in the current one
+    auto load_row = [&](int64_t i, float (&x)[kP]) {
+#pragma unroll
+        for (int e = 0; e < kP; ++e) {
+            const int j = lane + 32 * e;
+            x[e] = (i < m && j < n) ? __ldg(s + i * n + j) : 0.f;
+        }
+    };
+    int64_t i = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    float xn[kP];
+    load_row(i, xn);
+    for (; i < m; i += warps) {
         float v[kP];
 #pragma unroll
         for (int e = 0; e < kP; ++e) {
             const int j = lane + 32 * e;
             // s + b in fp32; the top-down search works on -v, so both are "largest first"
-            const float x = (j < n) ? __ldg(s + i * n + j) + bj[e] : pad;
+            const float x = (j < n) ? xn[e] + bj[e] : pad;
             v[e] = from_top ? x : -x;
         }
+        load_row(i + warps, xn);
         sort_desc(v);
         float a = 0.f;
         for (int r = 0; r < rounds; ++r) {
@@ -160,10 +171,61 @@ __device__ __forceinline__ void select_digit(int col, int shift, uint32_t q,
     for (int e = 0; e < 8; ++e) h[8 * lane + e] = 0u;  // ready for the next pass
 }
 
+// The end of a radix pass, after a CTA has counted its keys into `sh`: its counts go into the
+// global histogram; the last CTA of its column of experts to finish selects their digits, and
+// after the last pass the last column to finish forms bias_new = bhat - mean(bhat).
+__device__ __forceinline__ void finish_pass(unsigned (&sh)[32][257], double (&part)[8], int& last,
+                                            int n, int shift, uint32_t q,
+                                            QbColumn* __restrict__ col_state,
+                                            unsigned* __restrict__ hist,
+                                            unsigned* __restrict__ done,
+                                            float* __restrict__ bhat,
+                                            float* __restrict__ b_new) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < 32 * 256; idx += blockDim.x) {
+        const int c = idx >> 8, bin = idx & 255;
+        const unsigned cnt = sh[c][bin];
+        if (cnt && blockIdx.y * 32 + c < n) atomicAdd(&hist[(size_t)(blockIdx.y * 32 + c) * 256 + bin], cnt);
+    }
+    // the last CTA of this column of experts selects their digits
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&done[blockIdx.y], 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    for (int c = warp; c < 32; c += blockDim.x / 32) {
+        const int cc = blockIdx.y * 32 + c;
+        if (cc < n) select_digit(cc, shift, q, col_state, hist + (size_t)cc * 256, bhat);
+    }
+    if (threadIdx.x == 0) done[blockIdx.y] = 0u;  // ready for the next pass
+    if (shift != 0) return;
+    // after the last pass: the last column to finish forms bias_new
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(&done[gridDim.y], 1u) == gridDim.y - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double acc = 0.0;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) acc += (double)__ldcg(bhat + j);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) part[warp] = acc;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += part[w];
+    const double mean = tot / n;
+    for (int j = threadIdx.x; j < n; j += blockDim.x)
+        b_new[j] = (float)((double)__ldcg(bhat + j) - mean);
+    if (threadIdx.x == 0) done[gridDim.y] = 0u;
+}
+
 // One radix pass: a CTA counts the digits of 32 experts' margins over its token range and
-// adds them to the global histogram; the last CTA of a column of experts to finish then
-// selects those experts' digits, and after the last pass the last column to finish forms
-// bias_new = bhat - mean(bhat) (one launch per pass in all).
+// adds them to the global histogram (then finish_pass).  A lane takes one expert, so a warp
+// load reads 128 contiguous bytes of a score row.
 template <int kU>
 __global__ void __launch_bounds__(256) qb_hist_kernel(const float* __restrict__ s,
                                                       const float* __restrict__ alpha, int64_t m,
@@ -204,45 +266,77 @@ __global__ void __launch_bounds__(256) qb_hist_kernel(const float* __restrict__ 
         }
         for (; i < r1; i += 8) count(__ldg(s + i * n + col), __ldg(alpha + i));
     }
+    finish_pass(sh, part, last, n, shift, q, col_state, hist, done, bhat, b_new);
+}
+
+// The same pass for n a multiple of 4 (and 16-byte aligned scores): a lane takes four
+// consecutive experts of one row (lane = 8 x row of 4 + quad), so that a warp load reads 4
+// rows x 128 bytes, four times the bytes per load instruction and in flight.
+template <int kU>
+__global__ void __launch_bounds__(256) qb_hist4_kernel(const float* __restrict__ s,
+                                                       const float* __restrict__ alpha, int64_t m,
+                                                       int n, int rows_per_cta, int shift,
+                                                       uint32_t q, QbColumn* __restrict__ col_state,
+                                                       unsigned* __restrict__ hist,
+                                                       unsigned* __restrict__ done,
+                                                       float* __restrict__ bhat,
+                                                       float* __restrict__ b_new) {
+    __shared__ unsigned sh[32][257];
+    __shared__ double part[8];
+    __shared__ int last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 32 * 257; i += blockDim.x) (&sh[0][0])[i] = 0u;
     __syncthreads();
-    for (int idx = threadIdx.x; idx < 32 * 256; idx += blockDim.x) {
-        const int c = idx >> 8, bin = idx & 255;
-        const unsigned cnt = sh[c][bin];
-        if (cnt && blockIdx.y * 32 + c < n) atomicAdd(&hist[(size_t)(blockIdx.y * 32 + c) * 256 + bin], cnt);
-    }
-    // the last CTA of this column of experts selects their digits
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(&done[blockIdx.y], 1u) == gridDim.x - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    for (int c = warp; c < 32; c += blockDim.x / 32) {
-        const int cc = blockIdx.y * 32 + c;
-        if (cc < n) select_digit(cc, shift, q, col_state, hist + (size_t)cc * 256, bhat);
-    }
-    if (threadIdx.x == 0) done[blockIdx.y] = 0u;  // ready for the next pass
-    if (shift != 0) return;
-    // after the last pass: the last column to finish forms bias_new
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(&done[gridDim.y], 1u) == gridDim.y - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    double acc = 0.0;
-    for (int j = threadIdx.x; j < n; j += blockDim.x) acc += (double)__ldcg(bhat + j);
+    const int r4 = lane >> 3, eq = lane & 7;
+    const int c0 = blockIdx.y * 32 + 4 * eq;  // this lane's experts c0 .. c0 + 3 (all live or none)
+    const bool live = c0 < n;
+    uint32_t prefix[4] = {0u, 0u, 0u, 0u};
+    if (live && shift < 24) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) part[warp] = acc;
-    __syncthreads();
-    double tot = 0.0;
+        for (int e = 0; e < 4; ++e) prefix[e] = __ldcg(&col_state[c0 + e].prefix) >> (shift + 8);
+    }
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = min(m, r0 + rows_per_cta);
+    if (live) {
+        // a step: rows b + 32 u + r4 for u < kU, b = r0 + 4 warp + 32 kU (step); the next
+        // step's loads are issued before this step's keys are counted
+        auto load_step = [&](int64_t b, float4 (&x)[kU], float (&al)[kU]) {
 #pragma unroll
-    for (int w = 0; w < 8; ++w) tot += part[w];
-    const double mean = tot / n;
-    for (int j = threadIdx.x; j < n; j += blockDim.x)
-        b_new[j] = (float)((double)__ldcg(bhat + j) - mean);
-    if (threadIdx.x == 0) done[gridDim.y] = 0u;
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = b + 32 * u + r4;
+                if (i < r1) {
+                    x[u] = __ldg(reinterpret_cast<const float4*>(s + i * n + c0));
+                    al[u] = __ldg(alpha + i);
+                }
+            }
+        };
+        float4 xn[kU];
+        float aln[kU];
+        load_step(r0 + 4 * warp, xn, aln);
+        for (int64_t b = r0 + 4 * warp; b < r1; b += 32 * kU) {
+            float4 x[kU];
+            float al[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                x[u] = xn[u];
+                al[u] = aln[u];
+            }
+            load_step(b + 32 * kU, xn, aln);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (b + 32 * u + r4 < r1) {
+                    const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t key = desc_key(xv[e] - al[u]);
+                        if (shift == 24 || (key >> (shift + 8)) == prefix[e])
+                            atomicAdd(&sh[4 * eq + e][(key >> shift) & 255u], 1u);
+                    }
+                }
+            }
+        }
+    }
+    finish_pass(sh, part, last, n, shift, q, col_state, hist, done, bhat, b_new);
 }
 
 }  // namespace
@@ -304,17 +398,24 @@ cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, i
     }
     const uint32_t q = (uint32_t)((m * k) / n);
     const int col_blocks = (n + 31) / 32;
-    // about two CTAs per SM in total (each with 16 rows of loads in flight per warp), at
-    // least 256 tokens each
+    // about two CTAs per SM in total (each warp with a step of loads in flight while it
+    // counts the previous one), at least 256 tokens each
     int64_t row_blocks = ((int64_t)sms * 2 + col_blocks - 1) / col_blocks;
     if (row_blocks > (m + 255) / 256) row_blocks = (m + 255) / 256;
     if (row_blocks < 1) row_blocks = 1;
     const int rows_per_cta = (int)((m + row_blocks - 1) / row_blocks);
     row_blocks = (m + rows_per_cta - 1) / rows_per_cta;
+    // four experts a lane when the rows allow 16-byte loads
+    const bool quad = n % 4 == 0 && (reinterpret_cast<uintptr_t>(s) & 15) == 0;
     for (int shift = 24; shift >= 0; shift -= 8) {
         ProfScope prof("qb_hist_kernel", stream);
-        qb_hist_kernel<16><<<dim3((unsigned)row_blocks, (unsigned)col_blocks), 256, 0, stream>>>(
-            s, alpha, m, n, rows_per_cta, shift, q, cols, hist, done, bhat, b_new);
+        const dim3 grid((unsigned)row_blocks, (unsigned)col_blocks);
+        if (quad)
+            qb_hist4_kernel<8><<<grid, 256, 0, stream>>>(s, alpha, m, n, rows_per_cta, shift, q, cols,
+                                                         hist, done, bhat, b_new);
+        else
+            qb_hist_kernel<16><<<grid, 256, 0, stream>>>(s, alpha, m, n, rows_per_cta, shift, q, cols,
+                                                         hist, done, bhat, b_new);
     }
     return cudaGetLastError();
 }
