@@ -108,6 +108,15 @@ def test_deterministic(kda):
         assert torch.equal(g1[nm], g2[nm]), nm
 
 
+def test_more_chains_than_sms(kda):
+    """64 packed sequences of 1..130 tokens at H = 3: 192 (sequence, head) chains, more than the
+    GPU has SMs, so each chain CTA of both chains runs several chains in turn (their operand
+    images through the same shared-memory stages and bulk copies)."""
+    rng = np.random.default_rng(82)
+    lengths = [int(x) for x in rng.integers(1, 131, size=64)]
+    _run(kda, lengths, H=3, d=64, dtype="bf16", seed=83)
+
+
 def test_long_sequences(kda):
     """Sequences of 2100 and 1000 tokens (33 and 16 chunks, ragged tails): the checkpoints and
     the per-chunk recompute over many chunks."""
