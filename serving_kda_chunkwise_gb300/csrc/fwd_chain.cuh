@@ -281,7 +281,6 @@ __device__ __forceinline__ void chain_body(const ChainParams& p, uint8_t* smem_r
                     src = c.pkg0 + (size_t)t * kPkgBytes;
                 }
                 if (cpart == 0) {
-                    if (!p.fused && t + 3 < c.nch) l2_prefetch(src + 3 * (size_t)kPkgBytes, kPkgBytes);
                     if (g >= 2 && !mbar_wait_ab(&mma1[st], ((g - 2) >> 1) & 1, p.err, abort)) { ok = false; break; }
                     if (want_o) {
                         mbar_expect_tx(&fullPA[st], kPkgPartA);
