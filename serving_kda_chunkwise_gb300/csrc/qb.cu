@@ -48,23 +48,33 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float(u);
 }
 
-// Sort kP values descending (odd-even transposition network, unrolled).
+// order-preserving map of fp32 to uint32 (ascending floats -> ascending keys) and back
+__device__ __forceinline__ uint32_t asc_key(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float asc_value(uint32_t asc) {
+    return __uint_as_float((asc & 0x80000000u) ? (asc & 0x7fffffffu) : ~asc);
+}
+
+// Sort kP keys descending (odd-even transposition network, unrolled).
 template <int kP>
-__device__ __forceinline__ void sort_desc(float (&v)[kP]) {
+__device__ __forceinline__ void sort_desc(uint32_t (&v)[kP]) {
 #pragma unroll
     for (int rnd = 0; rnd < kP; ++rnd)
 #pragma unroll
         for (int e = rnd & 1; e + 1 < kP; e += 2) {
-            const float a = v[e], b2 = v[e + 1];
-            v[e] = fmaxf(a, b2);
-            v[e + 1] = fminf(a, b2);
+            const uint32_t a = v[e], b2 = v[e + 1];
+            v[e] = max(a, b2);
+            v[e + 1] = min(a, b2);
         }
 }
 
-// kP values per lane (n <= 32 kP), kept sorted (largest first), so a lane's candidate is
-// its first value.  The (k+1)-th largest is found by k+1 rounds of "take the warp maximum of
-// the lanes' first values, and the lowest lane holding it drops that value", or, when that
-// is shorter, as the (n-k)-th smallest by rounds of minimum (on negated values).
+// kP values per lane (n <= 32 kP) as order-preserving keys, kept sorted (largest first), so a
+// lane's candidate is its first key.  The (k+1)-th largest is found by k+1 rounds of "take
+// the warp maximum of the lanes' first keys (one warp reduction), and the lowest lane holding
+// it drops that key", or, when that is shorter, as the (n-k)-th smallest by the same rounds
+// on negated values.  Zeros are made +0 first, so that the two zeros are one key.
 template <int kP>
 __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__ s,
                                                        const float* __restrict__ b, int64_t m,
@@ -73,6 +83,7 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__
     const bool from_top = k + 1 <= n - k;
     const int rounds = from_top ? k + 1 : n - k;
     const float pad = from_top ? -INFINITY : INFINITY;  // never selected
+    constexpr uint32_t kGone = 0u;                       // below every value's key
     float bj[kP];
 #pragma unroll
     for (int e = 0; e < kP; ++e) {
@@ -92,22 +103,19 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__
     float xn[kP];
     load_row(i, xn);
     for (; i < m; i += warps) {
-        float v[kP];
+        uint32_t v[kP];
 #pragma unroll
         for (int e = 0; e < kP; ++e) {
             const int j = lane + 32 * e;
             // s + b in fp32; the top-down search works on -v, so both are "largest first"
             const float x = (j < n) ? xn[e] + bj[e] : pad;
-            v[e] = from_top ? x : -x;
+            v[e] = asc_key((from_top ? x : -x) + 0.f);
         }
         load_row(i + warps, xn);
         sort_desc(v);
-        float a = 0.f;
+        uint32_t a = 0u;
         for (int r = 0; r < rounds; ++r) {
-            float wm = v[0];
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
+            const uint32_t wm = __reduce_max_sync(0xffffffffu, v[0]);
             a = wm;
             if (r + 1 == rounds) break;
             // the lowest lane holding the maximum drops it (its list moves up by one)
@@ -115,9 +123,12 @@ __global__ void __launch_bounds__(256) qb_alpha_kernel(const float* __restrict__
             const bool pop = lane == __ffs(holders) - 1;
 #pragma unroll
             for (int e = 0; e + 1 < kP; ++e) v[e] = pop ? v[e + 1] : v[e];
-            v[kP - 1] = pop ? -INFINITY : v[kP - 1];
+            v[kP - 1] = pop ? kGone : v[kP - 1];
         }
-        if (lane == 0) alpha[i] = from_top ? a : -a;
+        if (lane == 0) {
+            const float av = asc_value(a);
+            alpha[i] = from_top ? av : -av;
+        }
     }
 }
 
