@@ -635,7 +635,8 @@ def bench_quantile_balance(dev, stream, peaks, reps=20):
     gbs = nbytes / (us / 1e6) / 1e9
     return {"us_per_call": us, "m": w["m"], "n": w["n"], "k": w["k"],
             "scores_GB": nbytes / 1e9, "GB_s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
-            "l2": "flushed before every call", "kernels": ["qb_alpha_kernel", "qb_hist_kernel"]}
+            "l2": "flushed before every call",
+            "kernels": ["qb_alpha_kernel", "qb_bracket_kernel", "qb_count_kernel", "qb_select_kernel"]}
 
 
 def bench_decode(args, dev, stream, peaks):

@@ -16,6 +16,20 @@
 //                     k+1 rounds of warp maximum over the lanes' first values and removal of
 //                     that value from the lowest lane holding it (or the (n-k)-th smallest,
 //                     by rounds of minimum, when that takes fewer rounds).
+// Then, for n a multiple of 4 and 8192 <= m <= 2^18 (the sampled-bracket path):
+//   qb_bracket_kernel a CTA per expert gathers the margins of every 2^sshift-th token (2048
+//                     to 4095 of them) and takes, to 16 bits of the key, the sample margins a
+//                     few binomial standard deviations either side of the wanted quantile as
+//                     the expert's bracket [lo, hi].
+//   qb_count_kernel   one pass over all margins: per expert the number above hi, and the
+//                     margins in [lo, hi] (a few thousand) copied to the expert's candidate
+//                     list.
+//   qb_select_kernel  a CTA per expert: when the bracket holds the wanted margin (at most q
+//                     margins above hi, at least q + 1 at or above lo) and the list did not
+//                     overflow, radix select among the candidates; otherwise among all m
+//                     margins of the expert.  The selection is exact either way; the sample
+//                     only decides how much work it takes.  The last CTA forms bhat - mean.
+// Otherwise (the radix path):
 //   qb_hist_kernel    radix select over the margins of every expert at once, 8 bits per pass
 //                     (4 passes, most significant digit first) on an order-preserving
 //                     uint32 key, inverted so that ascending keys are descending margins:
@@ -29,6 +43,9 @@
 //                     counts, appended to the expert's prefix) and clears their counts; after
 //                     the last pass the key is the (q+1)-th largest margin itself, and the last
 //                     column to finish forms bhat - mean(bhat).
+// Scores are taken to be finite (a NaN margin has no place in the order).
+#include <cmath>
+
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -182,6 +199,33 @@ __device__ __forceinline__ void select_digit(int col, int shift, uint32_t q,
     for (int e = 0; e < 8; ++e) h[8 * lane + e] = 0u;  // ready for the next pass
 }
 
+// bias_new = bhat - mean(bhat), by the last of `total` CTAs to arrive on the counter *ctr
+// (which it clears again); the mean in fp64.  At most 8 warps a CTA.
+__device__ __forceinline__ void form_bias(int n, const float* __restrict__ bhat,
+                                          float* __restrict__ b_new, unsigned* __restrict__ ctr,
+                                          unsigned total, double (&part)[8], int& last) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(ctr, 1u) == total - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    double acc = 0.0;
+    for (int j = threadIdx.x; j < n; j += blockDim.x) acc += (double)__ldcg(bhat + j);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) part[warp] = acc;
+    __syncthreads();
+    double tot = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += part[w];
+    const double mean = tot / n;
+    for (int j = threadIdx.x; j < n; j += blockDim.x)
+        b_new[j] = (float)((double)__ldcg(bhat + j) - mean);
+    if (threadIdx.x == 0) *ctr = 0u;
+}
+
 // The end of a radix pass, after a CTA has counted its keys into `sh`: its counts go into the
 // global histogram; the last CTA of its column of experts to finish selects their digits, and
 // after the last pass the last column to finish forms bias_new = bhat - mean(bhat).
@@ -192,7 +236,7 @@ __device__ __forceinline__ void finish_pass(unsigned (&sh)[32][257], double (&pa
                                             unsigned* __restrict__ done,
                                             float* __restrict__ bhat,
                                             float* __restrict__ b_new) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int warp = threadIdx.x >> 5;
     __syncthreads();
     for (int idx = threadIdx.x; idx < 32 * 256; idx += blockDim.x) {
         const int c = idx >> 8, bin = idx & 255;
@@ -213,25 +257,7 @@ __device__ __forceinline__ void finish_pass(unsigned (&sh)[32][257], double (&pa
     if (threadIdx.x == 0) done[blockIdx.y] = 0u;  // ready for the next pass
     if (shift != 0) return;
     // after the last pass: the last column to finish forms bias_new
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(&done[gridDim.y], 1u) == gridDim.y - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    double acc = 0.0;
-    for (int j = threadIdx.x; j < n; j += blockDim.x) acc += (double)__ldcg(bhat + j);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) part[warp] = acc;
-    __syncthreads();
-    double tot = 0.0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += part[w];
-    const double mean = tot / n;
-    for (int j = threadIdx.x; j < n; j += blockDim.x)
-        b_new[j] = (float)((double)__ldcg(bhat + j) - mean);
-    if (threadIdx.x == 0) done[gridDim.y] = 0u;
+    form_bias(n, bhat, b_new, done + gridDim.y, gridDim.y, part, last);
 }
 
 // One radix pass: a CTA counts the digits of 32 experts' margins over its token range and
@@ -350,32 +376,478 @@ __global__ void __launch_bounds__(256) qb_hist4_kernel(const float* __restrict__
     finish_pass(sh, part, last, n, shift, q, col_state, hist, done, bhat, b_new);
 }
 
+
+// ---- the sampled-bracket path ----
+
+// The three kernels after the thresholds are launched as programmatic dependents of the one
+// before (their launch and setup overlap its tail); each waits here for that grid to complete
+// and its writes to be visible before it reads them.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Radix select among the cnt keys key_at(0 .. cnt - 1): the key at 0-based position `rank`
+// (rank < cnt) in ascending order, 8-bit digits from bit shift0 + 8 down.  The bits above
+// were fixed by the caller in `prefix` (every key shares them); with npass < the remaining
+// digits it stops early and returns the prefix of the bin holding the rank (low bits zero).
+// kMatch: the keys of a warp step that share a digit add to the count with one
+// shared-memory atomic (match_any) -- for key sets whose leading digits are concentrated --
+// else one atomic per key.  Every thread of the CTA calls it; hist is shared [256], st shared
+// [2].  (hist and st are written by other threads between the barriers, so they must not be
+// declared __restrict__: with it the compiler kept the counts and the selected digit of an
+// earlier read.)
+template <bool kMatch, class KeyAt>
+__device__ uint32_t block_select(KeyAt key_at, int64_t cnt, uint32_t rank, uint32_t prefix,
+                                 int shift0, int npass, unsigned* hist, uint32_t* st) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int shift = shift0, pass = 0; shift >= 0 && pass < npass; shift -= 8, ++pass) {
+        for (int d = threadIdx.x; d < 256; d += blockDim.x) hist[d] = 0u;
+        __syncthreads();
+        const uint32_t fixed = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
+        for (int64_t base = (int64_t)warp * 32; base < cnt; base += (int64_t)nw * 32) {
+            const int64_t idx = base + lane;
+            unsigned digit = 256u;  // none
+            if (idx < cnt) {
+                const uint32_t key = key_at(idx);
+                if (((key ^ prefix) & fixed) == 0u) digit = (key >> shift) & 255u;
+            }
+            if (kMatch) {
+                const unsigned peers = __match_any_sync(0xffffffffu, digit);
+                if (digit < 256u && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (unsigned)__popc(peers));
+            } else if (digit < 256u) {
+                atomicAdd(&hist[digit], 1u);
+            }
+        }
+        __syncthreads();
+        if (warp == 0) {  // the digit holding the rank: prefix scan over the 256 counts
+            unsigned c[8];
+            unsigned tot = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                c[e] = hist[8 * lane + e];
+                tot += c[e];
+            }
+            unsigned incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned t = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += t;
+            }
+            const unsigned excl = incl - tot;
+            const unsigned mine = __ballot_sync(0xffffffffu, excl <= rank && rank < incl);
+            if (lane == __ffs(mine) - 1) {
+                unsigned before = excl;
+                int digit = 8 * lane;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (rank < before + c[e]) {
+                        digit = 8 * lane + e;
+                        break;
+                    }
+                    before += c[e];
+                }
+                st[0] = prefix | ((uint32_t)digit << shift);
+                st[1] = rank - before;
+            }
+        }
+        __syncthreads();
+        prefix = st[0];
+        rank = st[1];
+    }
+    return prefix;
+}
+
+// The bracket of every expert from a sample of the tokens: a CTA per expert gathers the
+// margins of every 2^sshift-th token (S of them) and finds, to 16 bits of the key, the bins
+// holding the sample margins at descending positions r_hi and r_lo; hi = the largest value of
+// the first bin (+inf when r_hi < 0), lo = the smallest of the second (-inf when r_lo >= S).
+// At most r_hi sample margins lie above hi and at least r_lo + 1 at or above lo.  The bracket
+// only steers the counting pass; the selection checks afterwards that the wanted margin
+// lies inside it, so its precision matters for speed alone.
+__global__ void __launch_bounds__(256) qb_bracket_kernel(const float* __restrict__ s,
+                                                         const float* __restrict__ alpha, int n,
+                                                         int sshift, int S, int r_hi, int r_lo,
+                                                         float2* __restrict__ brk) {
+    extern __shared__ uint32_t keys[];  // [S]
+    __shared__ unsigned hist[256];
+    __shared__ uint32_t st[2];
+    const int j = blockIdx.x;
+    grid_dependency_wait();
+    constexpr int kG = 8;  // gathers in flight per thread
+    for (int t0 = threadIdx.x; t0 < S; t0 += kG * blockDim.x) {
+        float x[kG], a[kG];
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const int t = t0 + g * blockDim.x;
+            const int64_t i = (int64_t)min(t, S - 1) << sshift;
+            x[g] = __ldg(s + i * n + j);
+            a[g] = __ldg(alpha + i);
+        }
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const int t = t0 + g * blockDim.x;
+            if (t < S) keys[t] = desc_key((x[g] - a[g]) + 0.f);
+        }
+    }
+    __syncthreads();
+    auto at = [&](int64_t idx) { return keys[idx]; };
+    float hi = INFINITY, lo = -INFINITY;
+    if (r_hi >= 0) hi = key_value(block_select<true>(at, S, (uint32_t)r_hi, 0u, 24, 2, hist, st));
+    if (r_lo < S) lo = key_value(block_select<true>(at, S, (uint32_t)r_lo, 0u, 24, 2, hist, st) | 0xffffu);
+    // +0 for a zero bound, as for the margins, so that the candidates' keys lie between the
+    // bounds' keys
+    if (threadIdx.x == 0) brk[j] = make_float2(lo + 0.f, hi + 0.f);
+}
+
+constexpr int kCountSlots = 8;          // candidates a thread stages per expert
+constexpr int kCountStride = 4 * kCountSlots + 1;  // words per thread (padded against conflicts)
+constexpr int kSelKeys = 8192;          // candidates the selection stages in shared memory
+
+// The counting pass over all margins (n a multiple of 4, 16-byte aligned scores): per expert,
+// the number of margins above hi, and the margins in [lo, hi] appended (as descending keys)
+// to the expert's candidate list of `cap` entries (the count keeps growing past cap, which
+// tells the selection that the list overflowed).  A CTA takes 256 experts (64 quads of four
+// consecutive experts, a lane per quad, so that a warp load reads 512 contiguous bytes of a
+// row) and four interleaved token streams over its range; the next step's loads are issued
+// before the current step is compared.  A thread keeps its experts' counts in registers and
+// its candidates in its own shared-memory slots (kCountSlots per expert, past which it appends
+// to the global list directly); at the end the CTA reserves each expert's place in the list
+// with one global atomic and copies the staged candidates there.
+template <int kU>
+__global__ void __launch_bounds__(256, 3) qb_count_kernel(const float* __restrict__ s,
+                                                          const float* __restrict__ alpha,
+                                                          int64_t m, int n, int rows_per_cta,
+                                                          const float2* __restrict__ brk,
+                                                          unsigned* __restrict__ cnt_hi,
+                                                          unsigned* __restrict__ cand_cnt,
+                                                          uint32_t* __restrict__ cand, int cap) {
+    __shared__ unsigned sh[256];     // margins above hi, per expert
+    __shared__ unsigned scnt[256];   // staged candidates, per expert; then the CTA's base
+    __shared__ uint32_t sbuf[256 * kCountStride];
+    const int qd = threadIdx.x & 63, rl = threadIdx.x >> 6;
+    const int c0 = blockIdx.y * 256 + 4 * qd;
+    const bool live = c0 < n;
+    grid_dependency_wait();
+    sh[threadIdx.x] = 0u;
+    scnt[threadIdx.x] = 0u;
+    __syncthreads();
+    uint32_t* mine = sbuf + threadIdx.x * kCountStride;
+    unsigned nc[4] = {0u, 0u, 0u, 0u};
+    const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
+    const int64_t r1 = min(m, r0 + rows_per_cta);
+    if (live) {
+        float lo[4], hi[4];
+        unsigned ch[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 b2 = __ldcg(brk + c0 + e);
+            lo[e] = b2.x;
+            hi[e] = b2.y;
+        }
+        // a step: rows b + 4 u for u < kU; b = r0 + rl + 4 kU (step)
+        auto load_step = [&](int64_t b, float4 (&x)[kU], float (&al)[kU]) {
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int64_t i = b + 4 * u;
+                if (i < r1) {
+                    x[u] = __ldg(reinterpret_cast<const float4*>(s + i * n + c0));
+                    al[u] = __ldg(alpha + i);
+                }
+            }
+        };
+        float4 xn[kU];
+        float aln[kU];
+        load_step(r0 + rl, xn, aln);
+        for (int64_t b = r0 + rl; b < r1; b += 4 * kU) {
+            float4 x[kU];
+            float al[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                x[u] = xn[u];
+                al[u] = aln[u];
+            }
+            load_step(b + 4 * kU, xn, aln);
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (b + 4 * u < r1) {
+                    const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float mg = xv[e] - al[u];
+                        if (mg > hi[e]) {
+                            ++ch[e];
+                        } else if (mg >= lo[e]) {
+                            const uint32_t key = desc_key(mg + 0.f);
+                            if (nc[e] < (unsigned)kCountSlots) {
+                                mine[e * kCountSlots + nc[e]] = key;
+                            } else {  // this thread's slots are full: straight to the list
+                                const unsigned g = atomicAdd(cand_cnt + c0 + e, 1u);
+                                if (g < (unsigned)cap) cand[(int64_t)(c0 + e) * cap + g] = key;
+                            }
+                            ++nc[e];
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (ch[e]) atomicAdd(&sh[4 * qd + e], ch[e]);
+    }
+    // each thread's place among the CTA's staged candidates of its experts
+    unsigned off[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        nc[e] = min(nc[e], (unsigned)kCountSlots);
+        off[e] = nc[e] ? atomicAdd(&scnt[4 * qd + e], nc[e]) : 0u;
+    }
+    __syncthreads();
+    // one global atomic per expert for the count above, one to reserve the CTA's candidates
+    const int col = blockIdx.y * 256 + threadIdx.x;
+    if (col < n) {
+        if (sh[threadIdx.x]) atomicAdd(cnt_hi + col, sh[threadIdx.x]);
+        const unsigned c = scnt[threadIdx.x];
+        sh[threadIdx.x] = c ? atomicAdd(cand_cnt + col, c) : 0u;  // the CTA's base in the list
+    }
+    __syncthreads();
+    if (live) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const unsigned base = sh[4 * qd + e] + off[e];
+            for (unsigned t = 0; t < nc[e]; ++t)
+                if (base + t < (unsigned)cap)
+                    cand[(int64_t)(c0 + e) * cap + base + t] = mine[e * kCountSlots + t];
+        }
+    }
+}
+
+// The selection, a CTA per expert: when the wanted margin (descending position q) lies in
+// the bracket -- at most q margins above hi, at least q + 1 at or above lo -- and the list
+// did not overflow, it is the candidate at descending position q - (count above hi), selected
+// in shared memory when the list fits kSelKeys;
+// otherwise the CTA selects position q among all m margins of the expert, recomputed from
+// the scores and thresholds.  bhat = -(that margin); the last CTA forms bias_new.
+__global__ void __launch_bounds__(256) qb_select_kernel(const float* __restrict__ s,
+                                                        const float* __restrict__ alpha, int64_t m,
+                                                        int n, uint32_t q,
+                                                        const float2* __restrict__ brk,
+                                                        const unsigned* __restrict__ cnt_hi,
+                                                        const unsigned* __restrict__ cand_cnt,
+                                                        const uint32_t* __restrict__ cand, int cap,
+                                                        float* __restrict__ bhat,
+                                                        float* __restrict__ b_new,
+                                                        unsigned* __restrict__ done) {
+    extern __shared__ uint32_t skeys[];  // [kSelKeys]
+    __shared__ unsigned hist[256];
+    __shared__ uint32_t st[2];
+    __shared__ double part[8];
+    __shared__ int last;
+    const int j = blockIdx.x;
+    grid_dependency_wait();
+    const unsigned above = __ldcg(cnt_hi + j), mid = __ldcg(cand_cnt + j);
+    uint32_t key;
+    if (above <= q && (uint64_t)above + mid >= (uint64_t)q + 1u && mid <= (unsigned)cap) {
+        // every candidate lies in [lo, hi], so its key shares the leading bits of the keys of
+        // hi and lo: the whole bytes of those are fixed, the digits start below them
+        const float2 b2 = __ldcg(brk + j);
+        const uint32_t k0 = desc_key(b2.y), k1 = desc_key(b2.x);
+        const int same = (k0 == k1) ? 32 : __clz(k0 ^ k1);
+        const int bytes = same >= 32 ? 3 : same / 8;  // whole leading bytes fixed (at most 3)
+        const uint32_t prefix = bytes == 0 ? 0u : (k0 & (0xffffffffu << (32 - 8 * bytes)));
+        const int shift0 = 24 - 8 * bytes;
+        const uint32_t* cj = cand + (int64_t)j * cap;
+        if (mid <= (unsigned)kSelKeys) {  // the list staged in shared memory (one read)
+            for (unsigned t0 = threadIdx.x; t0 < mid; t0 += 8 * blockDim.x) {
+                uint32_t v[8];
+#pragma unroll
+                for (int g = 0; g < 8; ++g) v[g] = __ldcg(cj + min(t0 + g * blockDim.x, mid - 1));
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    if (t0 + g * blockDim.x < mid) skeys[t0 + g * blockDim.x] = v[g];
+            }
+            __syncthreads();
+            key = block_select<false>([&](int64_t idx) { return skeys[idx]; }, (int64_t)mid,
+                                      q - above, prefix, shift0, 4, hist, st);
+        } else {
+            key = block_select<false>([&](int64_t idx) { return __ldcg(cj + idx); }, (int64_t)mid,
+                                      q - above, prefix, shift0, 4, hist, st);
+        }
+    } else {
+        key = block_select<true>([&](int64_t i) { return desc_key((__ldg(s + i * n + j) - __ldcg(alpha + i)) + 0.f); },
+                                 m, q, 0u, 24, 4, hist, st);
+    }
+    if (threadIdx.x == 0) bhat[j] = -key_value(key);
+    form_bias(n, bhat, b_new, done, gridDim.x, part, last);
+}
+
 }  // namespace
 
-// workspace: alpha [m], hist [n][256], pass counters [column blocks + 1], column states [n],
-// bhat [n]
+// workspace of the radix path: alpha [m], hist [n][256], pass counters [column blocks + 1],
+// column states [n], bhat [n]
 struct QbWs {
     size_t alpha, hist, done, cols, bhat, total;
 };
+static size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 static QbWs qb_ws(int64_t m, int n) {
-    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
     QbWs w;
     w.alpha = 0;
-    w.hist = al((size_t)m * 4);
-    w.done = w.hist + al((size_t)n * 256 * 4);
-    w.cols = w.done + al((size_t)((n + 31) / 32 + 1) * 4);
-    w.bhat = w.cols + al((size_t)n * sizeof(QbColumn));
-    w.total = w.bhat + al((size_t)n * 4);
+    w.hist = al256((size_t)m * 4);
+    w.done = w.hist + al256((size_t)n * 256 * 4);
+    w.cols = w.done + al256((size_t)((n + 31) / 32 + 1) * 4);
+    w.bhat = w.cols + al256((size_t)n * sizeof(QbColumn));
+    w.total = w.bhat + al256((size_t)n * 4);
     return w;
 }
 
-size_t qb_workspace_size(int64_t m, int n) { return qb_ws(m, n).total; }
+// The sampled-bracket path: for n a multiple of 4 and 8192 <= m <= 2^18, every 2^sshift-th
+// token (S = ceil(m / 2^sshift) in [2048, 4096) of them) is sampled, and every expert's
+// candidate list holds `cap` margins: three times the number a bracket of
+// 6 sqrt(S p (1 - p)) + 4 sample positions either side of the wanted one takes in
+// expectation, at p (1 - p) <= 1/4, so the size does not depend on k.  Workspace: alpha [m],
+// brackets [n], counts above [n], candidate counts [n], the done counter, bhat [n],
+// candidates [n][cap]; at most 64 MiB of candidates, else the radix path.
+struct QbFast {
+    bool ok;
+    int sshift, S, cap;
+    size_t alpha, brk, cnt_hi, cand_cnt, done, bhat, cand, total;
+};
+static QbFast qb_fast(int64_t m, int n) {
+    QbFast f{};
+    f.ok = false;
+    if (n % 4 != 0 || m < 8192 || m > (int64_t(1) << 18)) return f;
+    f.sshift = 0;
+    while ((m >> (f.sshift + 1)) >= 2048) ++f.sshift;
+    f.S = (int)((m + (int64_t(1) << f.sshift) - 1) >> f.sshift);
+    const double dmax = 3.0 * std::sqrt((double)f.S) + 4.0;
+    const double expect = 2.0 * dmax * (double)(int64_t(1) << f.sshift) + 64.0;
+    int64_t cap = 1024;
+    while ((double)cap < 3.0 * expect) cap *= 2;
+    if ((double)n * (double)cap * 4.0 > 64.0 * 1024 * 1024) return f;
+    f.cap = (int)cap;
+    f.alpha = 0;
+    f.brk = al256((size_t)m * 4);
+    f.cnt_hi = f.brk + al256((size_t)n * 8);
+    f.cand_cnt = f.cnt_hi + al256((size_t)n * 4);
+    f.done = f.cand_cnt + al256((size_t)n * 4);
+    f.bhat = f.done + 256;
+    f.cand = f.bhat + al256((size_t)n * 4);
+    f.total = f.cand + al256((size_t)n * cap * 4);
+    f.ok = true;
+    return f;
+}
+
+size_t qb_workspace_size(int64_t m, int n) {
+    const QbFast f = qb_fast(m, n);
+    return f.ok ? f.total : qb_ws(m, n).total;
+}
+
+static cudaError_t launch_alpha(const float* s, const float* b, int64_t m, int n, int k,
+                                float* alpha, int sms, cudaStream_t stream) {
+    const int64_t want = (m + 7) / 8;
+    const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    ProfScope prof("qb_alpha_kernel", stream);
+    const int per_lane = (n + 31) / 32;
+    if (per_lane <= 1)
+        qb_alpha_kernel<1><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+    else if (per_lane <= 2)
+        qb_alpha_kernel<2><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+    else if (per_lane <= 4)
+        qb_alpha_kernel<4><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+    else if (per_lane <= 8)
+        qb_alpha_kernel<8><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+    else if (per_lane <= 16)
+        qb_alpha_kernel<16><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+    else
+        qb_alpha_kernel<32><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
+    return cudaGetLastError();
+}
+
+// a launch that may begin while the previous kernel on the stream finishes (the kernel waits
+// for it with griddepcontrol.wait)
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+static cudaError_t launch_fast(const QbFast& f, const float* s, const float* b, int64_t m,
+                               int n, int k, float* b_new, float* bhat_out, float* alpha_out,
+                               uint8_t* w, int sms, cudaStream_t stream) {
+    float* alpha = alpha_out ? alpha_out : reinterpret_cast<float*>(w + f.alpha);
+    float2* brk = reinterpret_cast<float2*>(w + f.brk);
+    unsigned* cnt_hi = reinterpret_cast<unsigned*>(w + f.cnt_hi);
+    unsigned* cand_cnt = reinterpret_cast<unsigned*>(w + f.cand_cnt);
+    unsigned* done = reinterpret_cast<unsigned*>(w + f.done);
+    float* bhat = bhat_out ? bhat_out : reinterpret_cast<float*>(w + f.bhat);
+    uint32_t* cand = reinterpret_cast<uint32_t*>(w + f.cand);
+    const uint32_t q = (uint32_t)((m * k) / n);
+    // the sample positions of the bracket: the wanted margin is the (q+1)-th largest, so
+    // about q S / m sample margins lie above it; delta = 6 binomial standard deviations + 4
+    const double p = (double)(q + 1) / (double)m;
+    const double delta = 6.0 * std::sqrt((double)f.S * p * (1.0 - p)) + 4.0;
+    const double r_hi_d = std::floor((double)q * f.S / (double)m - delta);
+    const double r_lo_d = std::ceil((double)(q + 1) * f.S / (double)m + delta);
+    const int r_hi = r_hi_d < 0.0 ? -1 : (int)r_hi_d;
+    const int r_lo = r_lo_d >= (double)f.S ? f.S : (int)r_lo_d;
+    // counts and the done counter cleared (contiguous)
+    cudaError_t e = cudaMemsetAsync(w + f.cnt_hi, 0, f.bhat - f.cnt_hi, stream);
+    if (e == cudaSuccess) e = launch_alpha(s, b, m, n, k, alpha, sms, stream);
+    if (e != cudaSuccess) return e;
+    {
+        const int smem = f.S * 4;
+        e = cudaFuncSetAttribute(qb_bracket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        ProfScope prof("qb_bracket_kernel", stream);
+        e = launch_dependent(qb_bracket_kernel, dim3(n), dim3(256), smem, stream, s,
+                             (const float*)alpha, n, f.sshift, f.S, r_hi, r_lo, brk);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const int col_blocks = (n + 255) / 256;
+        int64_t row_blocks = ((int64_t)sms * 3 + col_blocks - 1) / col_blocks;
+        const int rows_per_cta = (int)((m + row_blocks - 1) / row_blocks);
+        row_blocks = (m + rows_per_cta - 1) / rows_per_cta;
+        ProfScope prof("qb_count_kernel", stream);
+        e = launch_dependent(qb_count_kernel<4>, dim3((unsigned)row_blocks, (unsigned)col_blocks),
+                             dim3(256), 0, stream, s, (const float*)alpha, m, n, rows_per_cta,
+                             (const float2*)brk, cnt_hi, cand_cnt, cand, f.cap);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const int smem = kSelKeys * 4;
+        e = cudaFuncSetAttribute(qb_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        ProfScope prof("qb_select_kernel", stream);
+        e = launch_dependent(qb_select_kernel, dim3(n), dim3(256), smem, stream, s,
+                             (const float*)alpha, m, n, q, (const float2*)brk,
+                             (const unsigned*)cnt_hi, (const unsigned*)cand_cnt,
+                             (const uint32_t*)cand, f.cap, bhat, b_new, done);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, int n, int k,
                                     float* b_new, float* bhat_out, float* alpha_out,
                                     void* workspace, cudaStream_t stream) {
-    const QbWs L = qb_ws(m, n);
     uint8_t* w = static_cast<uint8_t*>(workspace);
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const QbFast f = qb_fast(m, n);
+    if (f.ok && (reinterpret_cast<uintptr_t>(s) & 15) == 0)
+        return launch_fast(f, s, b, m, n, k, b_new, bhat_out, alpha_out, w, sms, stream);
+    const QbWs L = qb_ws(m, n);
     float* alpha = reinterpret_cast<float*>(w + L.alpha);
     unsigned* hist = reinterpret_cast<unsigned*>(w + L.hist);
     unsigned* done = reinterpret_cast<unsigned*>(w + L.done);
@@ -383,30 +855,10 @@ cudaError_t launch_quantile_balance(const float* s, const float* b, int64_t m, i
     float* bhat = reinterpret_cast<float*>(w + L.bhat);
     if (alpha_out) alpha = alpha_out;
     if (bhat_out) bhat = bhat_out;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     // histogram and pass counters cleared (contiguous); every pass leaves them cleared
     cudaError_t e = cudaMemsetAsync(w + L.hist, 0, L.cols - L.hist, stream);
+    if (e == cudaSuccess) e = launch_alpha(s, b, m, n, k, alpha, sms, stream);
     if (e != cudaSuccess) return e;
-    {
-        const int64_t want = (m + 7) / 8;
-        const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
-        ProfScope prof("qb_alpha_kernel", stream);
-        const int per_lane = (n + 31) / 32;
-        if (per_lane <= 1)
-            qb_alpha_kernel<1><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
-        else if (per_lane <= 2)
-            qb_alpha_kernel<2><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
-        else if (per_lane <= 4)
-            qb_alpha_kernel<4><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
-        else if (per_lane <= 8)
-            qb_alpha_kernel<8><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
-        else if (per_lane <= 16)
-            qb_alpha_kernel<16><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
-        else
-            qb_alpha_kernel<32><<<grid, 256, 0, stream>>>(s, b, m, n, k, alpha);
-    }
     const uint32_t q = (uint32_t)((m * k) / n);
     const int col_blocks = (n + 31) / 32;
     // about two CTAs per SM in total (each warp with a step of loads in flight while it

@@ -48,6 +48,38 @@ def test_ties(kda, m, n, k):
     _check(kda, s, b, k)
 
 
+@pytest.mark.parametrize("m,n,k", [(8192, 256, 8), (12000, 64, 5), (200000, 16, 3),
+                                   (262144, 4, 1), (300000, 8, 2)])
+def test_sampled_bracket_sizes(kda, m, n, k):
+    """Sizes at and around the sampled-bracket path's limits (8192 <= m <= 2^18, n a
+    multiple of 4): every token sampled at m = 8192, a non-power-of-two sample count, a
+    sample of one token in 16, the largest m, and one past it (the radix path)."""
+    s, b = inputs.qb_inputs(seed=m + 3 * n + k, m=m, n=n)
+    _check(kda, s, b, k)
+
+
+@pytest.mark.parametrize("m,n,k,grid", [(16384, 64, 6, 0.25), (65536, 64, 4, 1.0)])
+def test_sampled_bracket_ties(kda, m, n, k, grid):
+    """Coarse grids: the wanted margin is tied with thousands of others (on the grid of 1,
+    more candidates than an expert's list holds, so the selection falls back to the whole
+    column)."""
+    s, b = inputs.qb_inputs(seed=11 + m + n, m=m, n=n, grid=grid)
+    _check(kda, s, b, k)
+
+
+def test_sampled_bracket_misses(kda):
+    """A sample that misrepresents some experts: with m = 16384 every second token is
+    sampled; expert 0 scores far higher on the sampled tokens, expert 1 far lower, and
+    expert 2 far higher on the others, so their brackets miss the wanted margin and the
+    selection recomputes them from the whole column."""
+    m, n, k = 16384, 32, 2
+    s, b = inputs.qb_inputs(seed=41, m=m, n=n)
+    s[0::2, 0] += 20.0
+    s[0::2, 1] -= 20.0
+    s[1::2, 2] += 20.0
+    _check(kda, s, b, k)
+
+
 def test_full_size(kda):
     """The benchmark's batch: 65536 tokens, 256 experts, 8 per token."""
     w = inputs.QB_WORKLOAD
