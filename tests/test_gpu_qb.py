@@ -80,6 +80,17 @@ def test_sampled_bracket_misses(kda):
     _check(kda, s, b, k)
 
 
+@pytest.mark.parametrize("stride", [32, 16])
+def test_thresholds_concentrated(kda, stride):
+    """Scores raised by 5 on every 32nd (16th) expert: the row's largest values sit in one
+    (two) of the 32 lanes of the threshold kernel's warp, so one lane gives up value after
+    value in its rounds."""
+    m, n, k = 3000, 256, 8
+    s, b = inputs.qb_inputs(seed=70 + stride, m=m, n=n)
+    s[:, ::stride] += 5.0
+    _check(kda, s, b, k)
+
+
 def test_full_size(kda):
     """The benchmark's batch: 65536 tokens, 256 experts, 8 per token."""
     w = inputs.QB_WORKLOAD
