@@ -200,10 +200,11 @@ __device__ __forceinline__ void select_digit(int col, int shift, uint32_t q,
 }
 
 // bias_new = bhat - mean(bhat), by the last of `total` CTAs to arrive on the counter *ctr
-// (which it clears again); the mean in fp64.  At most 8 warps a CTA.
+// (which it clears again); the mean in fp64.  part holds a partial sum per warp.
+template <int kW>
 __device__ __forceinline__ void form_bias(int n, const float* __restrict__ bhat,
                                           float* __restrict__ b_new, unsigned* __restrict__ ctr,
-                                          unsigned total, double (&part)[8], int& last) {
+                                          unsigned total, double (&part)[kW], int& last) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __threadfence();
     __syncthreads();
@@ -218,8 +219,7 @@ __device__ __forceinline__ void form_bias(int n, const float* __restrict__ bhat,
     if (lane == 0) part[warp] = acc;
     __syncthreads();
     double tot = 0.0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) tot += part[w];
+    for (int w = 0; w < (int)(blockDim.x / 32); ++w) tot += part[w];
     const double mean = tot / n;
     for (int j = threadIdx.x; j < n; j += blockDim.x)
         b_new[j] = (float)((double)__ldcg(bhat + j) - mean);
@@ -386,6 +386,41 @@ __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// One warp: the digit whose bin of the 256 counts h holds position `rank` (a prefix scan over
+// the counts, eight bins a lane), and the count of the bins before it.  True on the one lane
+// that found it.
+__device__ __forceinline__ bool pick_digit(const unsigned* h, uint32_t rank, uint32_t& digit,
+                                           uint32_t& before) {
+    const int lane = threadIdx.x & 31;
+    unsigned c[8];
+    unsigned tot = 0u;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        c[e] = h[8 * lane + e];
+        tot += c[e];
+    }
+    unsigned incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+    }
+    const unsigned excl = incl - tot;
+    const unsigned mine = __ballot_sync(0xffffffffu, excl <= rank && rank < incl);
+    if (lane != __ffs(mine) - 1) return false;
+    before = excl;
+    digit = 8 * lane;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (rank < before + c[e]) {
+            digit = 8 * lane + e;
+            break;
+        }
+        before += c[e];
+    }
+    return true;
+}
+
 // Radix select among the cnt keys key_at(0 .. cnt - 1): the key at 0-based position `rank`
 // (rank < cnt) in ascending order, 8-bit digits from bit shift0 + 8 down.  The bits above
 // were fixed by the caller in `prefix` (every key shares them); with npass < the remaining
@@ -419,34 +454,10 @@ __device__ uint32_t block_select(KeyAt key_at, int64_t cnt, uint32_t rank, uint3
             }
         }
         __syncthreads();
-        if (warp == 0) {  // the digit holding the rank: prefix scan over the 256 counts
-            unsigned c[8];
-            unsigned tot = 0u;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                c[e] = hist[8 * lane + e];
-                tot += c[e];
-            }
-            unsigned incl = tot;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned t = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += t;
-            }
-            const unsigned excl = incl - tot;
-            const unsigned mine = __ballot_sync(0xffffffffu, excl <= rank && rank < incl);
-            if (lane == __ffs(mine) - 1) {
-                unsigned before = excl;
-                int digit = 8 * lane;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    if (rank < before + c[e]) {
-                        digit = 8 * lane + e;
-                        break;
-                    }
-                    before += c[e];
-                }
-                st[0] = prefix | ((uint32_t)digit << shift);
+        if (warp == 0) {  // the digit holding the rank
+            uint32_t digit, before;
+            if (pick_digit(hist, rank, digit, before)) {
+                st[0] = prefix | (digit << shift);
                 st[1] = rank - before;
             }
         }
@@ -458,8 +469,9 @@ __device__ uint32_t block_select(KeyAt key_at, int64_t cnt, uint32_t rank, uint3
 }
 
 // The bracket of every expert from a sample of the tokens: a CTA per expert gathers the
-// margins of every 2^sshift-th token (S of them) and finds, to 16 bits of the key, the bins
-// holding the sample margins at descending positions r_hi and r_lo; hi = the largest value of
+// margins of every 2^sshift-th token (S of them) and finds, to 16 bits of the key (two
+// histogram passes shared by both), the bins holding the sample margins at descending
+// positions r_hi and r_lo; hi = the largest value of
 // the first bin (+inf when r_hi < 0), lo = the smallest of the second (-inf when r_lo >= S).
 // At most r_hi sample margins lie above hi and at least r_lo + 1 at or above lo.  The bracket
 // only steers the counting pass; the selection checks afterwards that the wanted margin
@@ -469,8 +481,8 @@ __global__ void __launch_bounds__(256) qb_bracket_kernel(const float* __restrict
                                                          int sshift, int S, int r_hi, int r_lo,
                                                          float2* __restrict__ brk) {
     extern __shared__ uint32_t keys[];  // [S]
-    __shared__ unsigned hist[256];
-    __shared__ uint32_t st[2];
+    __shared__ unsigned hist[512];
+    __shared__ uint32_t st[4];
     const int j = blockIdx.x;
     grid_dependency_wait();
     constexpr int kG = 8;  // gathers in flight per thread
@@ -490,10 +502,40 @@ __global__ void __launch_bounds__(256) qb_bracket_kernel(const float* __restrict
         }
     }
     __syncthreads();
-    auto at = [&](int64_t idx) { return keys[idx]; };
+    // both positions at once: one histogram of the top byte, then one of the second byte
+    // for each of the two bins found (warp 0 picks for hi, warp 1 for lo)
+    const int warp = threadIdx.x >> 5;
+    const uint32_t rank[2] = {(uint32_t)max(r_hi, 0), (uint32_t)min(r_lo, S - 1)};
+    for (int d = threadIdx.x; d < 512; d += blockDim.x) hist[d] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < S; t += blockDim.x) atomicAdd(&hist[keys[t] >> 24], 1u);
+    __syncthreads();
+    if (warp < 2) {
+        uint32_t digit, before;
+        if (pick_digit(hist, rank[warp], digit, before)) {
+            st[2 * warp] = digit;
+            st[2 * warp + 1] = rank[warp] - before;
+        }
+    }
+    __syncthreads();
+    const uint32_t top0 = st[0], top1 = st[2], rest0 = st[1], rest1 = st[3];
+    for (int d = threadIdx.x; d < 512; d += blockDim.x) hist[d] = 0u;
+    __syncthreads();
+    for (int t = threadIdx.x; t < S; t += blockDim.x) {
+        const uint32_t key = keys[t], d2 = (key >> 16) & 255u;
+        if ((key >> 24) == top0) atomicAdd(&hist[d2], 1u);
+        if ((key >> 24) == top1) atomicAdd(&hist[256 + d2], 1u);
+    }
+    __syncthreads();
+    if (warp < 2) {
+        uint32_t digit, before;
+        if (pick_digit(hist + 256 * warp, warp ? rest1 : rest0, digit, before))
+            st[2 * warp] = ((warp ? top1 : top0) << 24) | (digit << 16);
+    }
+    __syncthreads();
     float hi = INFINITY, lo = -INFINITY;
-    if (r_hi >= 0) hi = key_value(block_select<true>(at, S, (uint32_t)r_hi, 0u, 24, 2, hist, st));
-    if (r_lo < S) lo = key_value(block_select<true>(at, S, (uint32_t)r_lo, 0u, 24, 2, hist, st) | 0xffffu);
+    if (r_hi >= 0) hi = key_value(st[0]);
+    if (r_lo < S) lo = key_value(st[2] | 0xffffu);
     // +0 for a zero bound, as for the margins, so that the candidates' keys lie between the
     // bounds' keys
     if (threadIdx.x == 0) brk[j] = make_float2(lo + 0.f, hi + 0.f);
@@ -504,8 +546,8 @@ constexpr int kCountStride = 4 * kCountSlots + 1;  // words per thread (padded a
 constexpr int kSelKeys = 8192;          // candidates the selection stages in shared memory
 
 // The counting pass over all margins (n a multiple of 4, 16-byte aligned scores): per expert,
-// the number of margins above hi, and the margins in [lo, hi] appended (as descending keys)
-// to the expert's candidate list of `cap` entries (the count keeps growing past cap, which
+// the number of margins above hi, and the margins in [lo, hi] appended to the expert's
+// candidate list of `cap` entries (the count keeps growing past cap, which
 // tells the selection that the list overflowed).  A CTA takes 256 experts (64 quads of four
 // consecutive experts, a lane per quad, so that a warp load reads 512 contiguous bytes of a
 // row) and four interleaved token streams over its range; the next step's loads are issued
@@ -520,10 +562,10 @@ __global__ void __launch_bounds__(256, 3) qb_count_kernel(const float* __restric
                                                           const float2* __restrict__ brk,
                                                           unsigned* __restrict__ cnt_hi,
                                                           unsigned* __restrict__ cand_cnt,
-                                                          uint32_t* __restrict__ cand, int cap) {
+                                                          float* __restrict__ cand, int cap) {
     __shared__ unsigned sh[256];     // margins above hi, per expert
     __shared__ unsigned scnt[256];   // staged candidates, per expert; then the CTA's base
-    __shared__ uint32_t sbuf[256 * kCountStride];
+    __shared__ float sbuf[256 * kCountStride];
     const int qd = threadIdx.x & 63, rl = threadIdx.x >> 6;
     const int c0 = blockIdx.y * 256 + 4 * qd;
     const bool live = c0 < n;
@@ -531,7 +573,7 @@ __global__ void __launch_bounds__(256, 3) qb_count_kernel(const float* __restric
     sh[threadIdx.x] = 0u;
     scnt[threadIdx.x] = 0u;
     __syncthreads();
-    uint32_t* mine = sbuf + threadIdx.x * kCountStride;
+    float* mine = sbuf + threadIdx.x * kCountStride;
     unsigned nc[4] = {0u, 0u, 0u, 0u};
     const int64_t r0 = (int64_t)blockIdx.x * rows_per_cta;
     const int64_t r1 = min(m, r0 + rows_per_cta);
@@ -577,12 +619,11 @@ __global__ void __launch_bounds__(256, 3) qb_count_kernel(const float* __restric
                         if (mg > hi[e]) {
                             ++ch[e];
                         } else if (mg >= lo[e]) {
-                            const uint32_t key = desc_key(mg + 0.f);
                             if (nc[e] < (unsigned)kCountSlots) {
-                                mine[e * kCountSlots + nc[e]] = key;
+                                mine[e * kCountSlots + nc[e]] = mg;
                             } else {  // this thread's slots are full: straight to the list
                                 const unsigned g = atomicAdd(cand_cnt + c0 + e, 1u);
-                                if (g < (unsigned)cap) cand[(int64_t)(c0 + e) * cap + g] = key;
+                                if (g < (unsigned)cap) cand[(int64_t)(c0 + e) * cap + g] = mg;
                             }
                             ++nc[e];
                         }
@@ -627,50 +668,50 @@ __global__ void __launch_bounds__(256, 3) qb_count_kernel(const float* __restric
 // in shared memory when the list fits kSelKeys;
 // otherwise the CTA selects position q among all m margins of the expert, recomputed from
 // the scores and thresholds.  bhat = -(that margin); the last CTA forms bias_new.
-__global__ void __launch_bounds__(256) qb_select_kernel(const float* __restrict__ s,
+__global__ void __launch_bounds__(512) qb_select_kernel(const float* __restrict__ s,
                                                         const float* __restrict__ alpha, int64_t m,
                                                         int n, uint32_t q,
                                                         const float2* __restrict__ brk,
                                                         const unsigned* __restrict__ cnt_hi,
                                                         const unsigned* __restrict__ cand_cnt,
-                                                        const uint32_t* __restrict__ cand, int cap,
+                                                        const float* __restrict__ cand, int cap,
                                                         float* __restrict__ bhat,
                                                         float* __restrict__ b_new,
                                                         unsigned* __restrict__ done) {
     extern __shared__ uint32_t skeys[];  // [kSelKeys]
     __shared__ unsigned hist[256];
     __shared__ uint32_t st[2];
-    __shared__ double part[8];
+    __shared__ double part[16];
     __shared__ int last;
     const int j = blockIdx.x;
     grid_dependency_wait();
     const unsigned above = __ldcg(cnt_hi + j), mid = __ldcg(cand_cnt + j);
+    const float2 b2 = __ldcg(brk + j);
     uint32_t key;
     if (above <= q && (uint64_t)above + mid >= (uint64_t)q + 1u && mid <= (unsigned)cap) {
         // every candidate lies in [lo, hi], so its key shares the leading bits of the keys of
         // hi and lo: the whole bytes of those are fixed, the digits start below them
-        const float2 b2 = __ldcg(brk + j);
         const uint32_t k0 = desc_key(b2.y), k1 = desc_key(b2.x);
         const int same = (k0 == k1) ? 32 : __clz(k0 ^ k1);
         const int bytes = same >= 32 ? 3 : same / 8;  // whole leading bytes fixed (at most 3)
         const uint32_t prefix = bytes == 0 ? 0u : (k0 & (0xffffffffu << (32 - 8 * bytes)));
         const int shift0 = 24 - 8 * bytes;
-        const uint32_t* cj = cand + (int64_t)j * cap;
-        if (mid <= (unsigned)kSelKeys) {  // the list staged in shared memory (one read)
+        const float* cj = cand + (int64_t)j * cap;
+        if (mid <= (unsigned)kSelKeys) {  // the list staged in shared memory (one read) as keys
             for (unsigned t0 = threadIdx.x; t0 < mid; t0 += 8 * blockDim.x) {
-                uint32_t v[8];
+                float v[8];
 #pragma unroll
                 for (int g = 0; g < 8; ++g) v[g] = __ldcg(cj + min(t0 + g * blockDim.x, mid - 1));
 #pragma unroll
                 for (int g = 0; g < 8; ++g)
-                    if (t0 + g * blockDim.x < mid) skeys[t0 + g * blockDim.x] = v[g];
+                    if (t0 + g * blockDim.x < mid) skeys[t0 + g * blockDim.x] = desc_key(v[g] + 0.f);
             }
             __syncthreads();
             key = block_select<false>([&](int64_t idx) { return skeys[idx]; }, (int64_t)mid,
                                       q - above, prefix, shift0, 4, hist, st);
         } else {
-            key = block_select<false>([&](int64_t idx) { return __ldcg(cj + idx); }, (int64_t)mid,
-                                      q - above, prefix, shift0, 4, hist, st);
+            key = block_select<false>([&](int64_t idx) { return desc_key(__ldcg(cj + idx) + 0.f); },
+                                      (int64_t)mid, q - above, prefix, shift0, 4, hist, st);
         }
     } else {
         key = block_select<true>([&](int64_t i) { return desc_key((__ldg(s + i * n + j) - __ldcg(alpha + i)) + 0.f); },
@@ -789,7 +830,7 @@ static cudaError_t launch_fast(const QbFast& f, const float* s, const float* b, 
     unsigned* cand_cnt = reinterpret_cast<unsigned*>(w + f.cand_cnt);
     unsigned* done = reinterpret_cast<unsigned*>(w + f.done);
     float* bhat = bhat_out ? bhat_out : reinterpret_cast<float*>(w + f.bhat);
-    uint32_t* cand = reinterpret_cast<uint32_t*>(w + f.cand);
+    float* cand = reinterpret_cast<float*>(w + f.cand);
     const uint32_t q = (uint32_t)((m * k) / n);
     // the sample positions of the bracket: the wanted margin is the (q+1)-th largest, so
     // about q S / m sample margins lie above it; delta = 6 binomial standard deviations + 4
@@ -828,10 +869,10 @@ static cudaError_t launch_fast(const QbFast& f, const float* s, const float* b, 
         e = cudaFuncSetAttribute(qb_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         ProfScope prof("qb_select_kernel", stream);
-        e = launch_dependent(qb_select_kernel, dim3(n), dim3(256), smem, stream, s,
+        e = launch_dependent(qb_select_kernel, dim3(n), dim3(512), smem, stream, s,
                              (const float*)alpha, m, n, q, (const float2*)brk,
                              (const unsigned*)cnt_hi, (const unsigned*)cand_cnt,
-                             (const uint32_t*)cand, f.cap, bhat, b_new, done);
+                             (const float*)cand, f.cap, bhat, b_new, done);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
