@@ -80,6 +80,15 @@ def test_sampled_bracket_misses(kda):
     _check(kda, s, b, k)
 
 
+def test_sampled_bracket_wide(kda):
+    """Half the experts per token (p = 1/2): the bracket holds about 36 k margins of each
+    expert, more than the selection stages in shared memory (it reads them from the list) and
+    more than a thread's candidate slots (the counting pass appends straight to the list)."""
+    m, n, k = 262144, 4, 2
+    s, b = inputs.qb_inputs(seed=91, m=m, n=n)
+    _check(kda, s, b, k)
+
+
 @pytest.mark.parametrize("stride", [32, 16])
 def test_thresholds_concentrated(kda, stride):
     """Scores raised by 5 on every 32nd (16th) expert: the row's largest values sit in one
