@@ -74,17 +74,29 @@ __device__ __forceinline__ float asc_value(uint32_t asc) {
     return __uint_as_float((asc & 0x80000000u) ? (asc & 0x7fffffffu) : ~asc);
 }
 
-// Sort kP keys descending (odd-even transposition network, unrolled).
+__device__ __forceinline__ void cx_desc(uint32_t& a, uint32_t& b) {
+    const uint32_t hi = max(a, b), lo = min(a, b);
+    a = hi;
+    b = lo;
+}
+
+// Sort kP keys descending: eight by Batcher's odd-even merge network (19 comparators), other
+// counts by odd-even transposition (unrolled).
 template <int kP>
 __device__ __forceinline__ void sort_desc(uint32_t (&v)[kP]) {
+    if constexpr (kP == 8) {
+        cx_desc(v[0], v[1]); cx_desc(v[2], v[3]); cx_desc(v[4], v[5]); cx_desc(v[6], v[7]);
+        cx_desc(v[0], v[2]); cx_desc(v[1], v[3]); cx_desc(v[4], v[6]); cx_desc(v[5], v[7]);
+        cx_desc(v[1], v[2]); cx_desc(v[5], v[6]);
+        cx_desc(v[0], v[4]); cx_desc(v[1], v[5]); cx_desc(v[2], v[6]); cx_desc(v[3], v[7]);
+        cx_desc(v[2], v[4]); cx_desc(v[3], v[5]);
+        cx_desc(v[1], v[2]); cx_desc(v[3], v[4]); cx_desc(v[5], v[6]);
+    } else {
 #pragma unroll
-    for (int rnd = 0; rnd < kP; ++rnd)
+        for (int rnd = 0; rnd < kP; ++rnd)
 #pragma unroll
-        for (int e = rnd & 1; e + 1 < kP; e += 2) {
-            const uint32_t a = v[e], b2 = v[e + 1];
-            v[e] = max(a, b2);
-            v[e + 1] = min(a, b2);
-        }
+            for (int e = rnd & 1; e + 1 < kP; e += 2) cx_desc(v[e], v[e + 1]);
+    }
 }
 
 // kP values per lane (n <= 32 kP) as order-preserving keys, kept sorted (largest first), so a
