@@ -49,11 +49,13 @@ def test_ties(kda, m, n, k):
 
 
 @pytest.mark.parametrize("m,n,k", [(8192, 256, 8), (12000, 64, 5), (200000, 16, 3),
-                                   (262144, 4, 1), (300000, 8, 2)])
+                                   (262144, 4, 1), (300000, 8, 2), (8192, 1024, 31),
+                                   (16384, 32, 0)])
 def test_sampled_bracket_sizes(kda, m, n, k):
     """Sizes at and around the sampled-bracket path's limits (8192 <= m <= 2^18, n a
-    multiple of 4): every token sampled at m = 8192, a non-power-of-two sample count, a
-    sample of one token in 16, the largest m, and one past it (the radix path)."""
+    multiple of 4): the smallest m, a non-power-of-two sample count, sparser samples, the
+    largest m and one past it (the radix path), the most experts, and k = 0 (q = 0: the
+    largest margin, no upper bound to the bracket)."""
     s, b = inputs.qb_inputs(seed=m + 3 * n + k, m=m, n=n)
     _check(kda, s, b, k)
 
