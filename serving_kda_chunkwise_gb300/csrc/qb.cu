@@ -625,19 +625,28 @@ __global__ void __launch_bounds__(256, 3) qb_count_kernel(const float* __restric
             for (int u = 0; u < kU; ++u) {
                 if (b + 4 * u < r1) {
                     const float xv[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                    // the row's four comparisons first, then one branch into the candidates
+                    float mg[4];
+                    unsigned cm = 0u;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float mg = xv[e] - al[u];
-                        if (mg > hi[e]) {
-                            ++ch[e];
-                        } else if (mg >= lo[e]) {
-                            if (nc[e] < (unsigned)kCountSlots) {
-                                mine[e * kCountSlots + nc[e]] = mg;
-                            } else {  // this thread's slots are full: straight to the list
-                                const unsigned g = atomicAdd(cand_cnt + c0 + e, 1u);
-                                if (g < (unsigned)cap) cand[(int64_t)(c0 + e) * cap + g] = mg;
+                        mg[e] = xv[e] - al[u];
+                        const bool above = mg[e] > hi[e];
+                        ch[e] += above ? 1u : 0u;
+                        cm |= (!above && mg[e] >= lo[e]) ? (1u << e) : 0u;
+                    }
+                    if (cm) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if ((cm >> e) & 1u) {
+                                if (nc[e] < (unsigned)kCountSlots) {
+                                    mine[e * kCountSlots + nc[e]] = mg[e];
+                                } else {  // this thread's slots are full: straight to the list
+                                    const unsigned g = atomicAdd(cand_cnt + c0 + e, 1u);
+                                    if (g < (unsigned)cap) cand[(int64_t)(c0 + e) * cap + g] = mg[e];
+                                }
+                                ++nc[e];
                             }
-                            ++nc[e];
                         }
                     }
                 }
